@@ -1,0 +1,149 @@
+"""CPU oracle for the strided batched product C <- alpha*A*B (+C0).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline leg are the only callers.  The CUDA library never imports or calls
+anything here, and nothing here imports the CUDA library.
+
+The arithmetic lives in ``sbgemm_ref.c`` (plain C, fp64 accumulation); this
+module builds it with gcc and marshals numpy arrays to it.  Operands are passed
+as objects with ``storage`` (1-D float32 numpy array), ``offset``, ``rs``,
+``cs`` and ``bs`` attributes: element (b, i, j) is
+``storage[offset + b*bs + i*rs + j*cs]``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sbgemm_ref.c")
+_LIB_PATH = os.path.join(_HERE, "libsbgemm_ref.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_fp = ctypes.c_void_p
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with gcc.  Contraction of a*b+c into fused
+    multiply-adds is switched off so the fp64 arithmetic is the same on every
+    host architecture."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                        "-ffp-contract=off", "-fno-fast-math", "-o", tmp, src, "-lm"],
+                       check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    lib.sbgemm_ref.restype = ctypes.c_int
+    lib.sbgemm_ref.argtypes = [
+        _fp, _i64, _i64, _i64, _fp, _i64, _i64, _i64, _fp, _i64, _i64, _i64,
+        _i64, _i64, _i64, _i64, ctypes.c_float, ctypes.c_int,
+        _fp, _fp, ctypes.c_int, ctypes.c_int]
+    lib.sbgemm_ref_points.restype = ctypes.c_int
+    lib.sbgemm_ref_points.argtypes = [
+        _fp, _i64, _i64, _i64, _fp, _i64, _i64, _i64, _fp, _i64, _i64, _i64,
+        _i64, _i64, _i64, _i64, ctypes.c_float, ctypes.c_int,
+        _fp, _i64, _fp, _fp]
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library.  ``path`` selects
+    another build of the same source, e.g. a mutated copy in a test."""
+    global _lib
+    if path is not None:
+        return _bind(path)
+    with _lock:
+        if _lib is None:
+            _lib = _bind(build())
+        return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _span_ok(op, batch, rows, cols) -> bool:
+    """Every element the strides can reach lies inside the storage."""
+    if batch == 0 or rows == 0 or cols == 0:
+        return True
+    lo = hi = op.offset
+    for stride, extent in ((op.bs, batch), (op.rs, rows), (op.cs, cols)):
+        d = stride * (extent - 1)
+        lo, hi = (lo + d, hi) if d < 0 else (lo, hi + d)
+    return lo >= 0 and hi < op.storage.size
+
+
+def _ptr(op):
+    st = op.storage
+    assert st.dtype == np.float32 and st.flags.c_contiguous and st.ndim == 1
+    return st.ctypes.data + 4 * int(op.offset)
+
+
+def _check(A, B, C, M, N, K, batch, accumulate):
+    if not _span_ok(A, batch, M, K):
+        raise ValueError("oracle: A strides reach outside its storage")
+    if not _span_ok(B, batch, K, N):
+        raise ValueError("oracle: B strides reach outside its storage")
+    if accumulate and not _span_ok(C, batch, M, N):
+        raise ValueError("oracle: C strides reach outside its storage")
+
+
+def product(A, B, C, M, N, K, batch, alpha, accumulate, nthreads=None,
+            reverse=False, lib=None):
+    """Full product.  Returns (ref, bound), float64 arrays of shape [batch, M, N]."""
+    _check(A, B, C, M, N, K, batch, accumulate)
+    lib = lib or load()
+    ref = np.zeros((batch, M, N), dtype=np.float64)
+    bound = np.zeros((batch, M, N), dtype=np.float64)
+    rc = lib.sbgemm_ref(_ptr(A), A.rs, A.cs, A.bs, _ptr(B), B.rs, B.cs, B.bs,
+                        _ptr(C), C.rs, C.cs, C.bs, M, N, K, batch,
+                        float(alpha), int(accumulate),
+                        ref.ctypes.data, bound.ctypes.data,
+                        int(nthreads or default_threads()), int(bool(reverse)))
+    if rc != 0:
+        raise RuntimeError(f"oracle sbgemm_ref failed with {rc}")
+    return ref, bound
+
+
+def product_points(A, B, C, M, N, K, batch, alpha, accumulate, idx, lib=None):
+    """The product at selected outputs.  ``idx`` is an int64 array [P, 3] of
+    (b, m, n).  Returns (ref, bound), float64 arrays of length P."""
+    _check(A, B, C, M, N, K, batch, accumulate)
+    lib = lib or load()
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 3)
+    P = idx.shape[0]
+    ref = np.zeros(P, dtype=np.float64)
+    bound = np.zeros(P, dtype=np.float64)
+    rc = lib.sbgemm_ref_points(_ptr(A), A.rs, A.cs, A.bs, _ptr(B), B.rs, B.cs, B.bs,
+                               _ptr(C), C.rs, C.cs, C.bs, M, N, K, batch,
+                               float(alpha), int(accumulate),
+                               idx.ctypes.data, P, ref.ctypes.data, bound.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"oracle sbgemm_ref_points failed with {rc}")
+    return ref, bound
+
+
+def case_product(case, **kw):
+    """Full product of a workloads.Case."""
+    return product(case.A, case.B, case.C, case.M, case.N, case.K, case.batch,
+                   case.alpha, case.accumulate, **kw)
+
+
+def case_points(case, idx, **kw):
+    return product_points(case.A, case.B, case.C, case.M, case.N, case.K,
+                          case.batch, case.alpha, case.accumulate, idx, **kw)

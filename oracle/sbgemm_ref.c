@@ -1,0 +1,165 @@
+/*
+ * Oracle for the strided batched product  C <- alpha * A * B  (optionally + C).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct CPU
+ * statement of what the CUDA library computes.  Only the tests, the smoke check
+ * and the benchmark's CPU-baseline leg may load it.  It shares no code, header or
+ * constant with the CUDA library, and the library never calls it.
+ *
+ * Definition followed (StaleyNET "GPU Implementation", section "The matrix
+ * product"): for a batch of matrix pairs, C <- alpha * A * B, optionally adding
+ * the previous C.  Each input is described by the memory distance between
+ * neighbouring rows and neighbouring columns, so a transposed read is the same
+ * memory with the two distances exchanged; a third distance steps between the
+ * matrices of the batch.  Element (b, i, j) of an operand X is X[b*bs + i*rs + j*cs]
+ * with distances counted in fp32 elements.
+ *
+ * Readings where the page is silent:
+ *  - "optionally + C" adds the previous C unscaled: ref = alpha*(A*B) + C0.
+ *  - Without accumulation the previous C is not read at all.
+ *  - Strides are in elements and may be zero or negative for A and B.
+ *
+ * For every output element the oracle forms, in fp64,
+ *     s     = sum_{k=0..K-1} A[b,m,k] * B[b,k,n]       (k increasing)
+ *     t     = sum_{k=0..K-1} |A[b,m,k] * B[b,k,n]|
+ *     ref   = alpha * s + (accumulate ? C0[b,m,n] : 0)
+ *     bound = |alpha| * t + (accumulate ? |C0[b,m,n]| : 0)
+ * Products of two fp32 values are exact in fp64.  `bound` is the scale the
+ * tolerance of a GPU result is measured against.
+ *
+ * Parity pins for this file live in tests/test_oracle.py.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    const float* A; int64_t rsA, csA, bsA;
+    const float* B; int64_t rsB, csB, bsB;
+    const float* C0; int64_t rsC, csC, bsC;
+    int64_t M, N, K, batch;
+    double alpha;
+    int accumulate;
+    double* ref;      /* dense [batch][M][N] */
+    double* bound;    /* dense [batch][M][N], may be NULL */
+    int nthreads;
+    int thread;
+    int reverse;      /* walk this thread's rows last-to-first */
+} oracle_job;
+
+/* One output row (b, m): every n of that row, each sum in increasing k. */
+static void oracle_row(const oracle_job* j, int64_t b, int64_t m,
+                       double* acc, double* mag) {
+    const int64_t N = j->N, K = j->K;
+    for (int64_t n = 0; n < N; ++n) { acc[n] = 0.0; mag[n] = 0.0; }
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = (double)j->A[b * j->bsA + m * j->rsA + k * j->csA];
+        const float* brow = j->B + b * j->bsB + k * j->rsB;
+        for (int64_t n = 0; n < N; ++n) {
+            const double p = a * (double)brow[n * j->csB];
+            acc[n] += p;
+            mag[n] += fabs(p);
+        }
+    }
+    double* out = j->ref + (b * j->M + m) * N;
+    double* bnd = j->bound ? j->bound + (b * j->M + m) * N : NULL;
+    for (int64_t n = 0; n < N; ++n) {
+        double r = j->alpha * acc[n];
+        double t = fabs(j->alpha) * mag[n];
+        if (j->accumulate) {
+            const double c0 = (double)j->C0[b * j->bsC + m * j->rsC + n * j->csC];
+            r += c0;
+            t += fabs(c0);
+        }
+        out[n] = r;
+        if (bnd) bnd[n] = t;
+    }
+}
+
+static void* oracle_worker(void* arg) {
+    const oracle_job* j = (const oracle_job*)arg;
+    const int64_t rows = j->batch * j->M;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)(j->N > 0 ? j->N : 1));
+    double* mag = (double*)malloc(sizeof(double) * (size_t)(j->N > 0 ? j->N : 1));
+    if (!acc || !mag) { free(acc); free(mag); return (void*)1; }
+    /* Rows are independent; thread t takes rows t, t+T, t+2T, ... */
+    int64_t count = rows > j->thread ? (rows - 1 - j->thread) / j->nthreads + 1 : 0;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t step = j->reverse ? count - 1 - i : i;
+        int64_t r = j->thread + step * j->nthreads;
+        oracle_row(j, r / j->M, r % j->M, acc, mag);
+    }
+    free(acc);
+    free(mag);
+    return NULL;
+}
+
+/* Full product.  Returns 0 on success, -1 on a bad argument, -2 on a thread or
+ * allocation failure. */
+int sbgemm_ref(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+               const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+               const float* C0, int64_t rsC, int64_t csC, int64_t bsC,
+               int64_t M, int64_t N, int64_t K, int64_t batch,
+               float alpha, int accumulate,
+               double* ref, double* bound, int nthreads, int reverse) {
+    if (M < 0 || N < 0 || K < 0 || batch < 0) return -1;
+    if (M == 0 || N == 0 || batch == 0) return 0;
+    if (!ref || (K > 0 && (!A || !B)) || (accumulate && !C0)) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    oracle_job base = {A, rsA, csA, bsA, B, rsB, csB, bsB, C0, rsC, csC, bsC,
+                       M, N, K, batch, (double)alpha, accumulate, ref, bound,
+                       nthreads, 0, reverse};
+    oracle_job jobs[256];
+    pthread_t tid[256];
+    int started = 0, failed = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = base;
+        jobs[t].thread = t;
+        if (t == nthreads - 1) break;     /* the calling thread runs the last */
+        if (pthread_create(&tid[t], NULL, oracle_worker, &jobs[t]) != 0) { failed = 1; break; }
+        ++started;
+    }
+    if (!failed && oracle_worker(&jobs[nthreads - 1]) != NULL) failed = 1;
+    for (int t = 0; t < started; ++t) {
+        void* rv = NULL;
+        pthread_join(tid[t], &rv);
+        if (rv != NULL) failed = 1;
+    }
+    return failed ? -2 : 0;
+}
+
+/* The same definition at selected outputs only: idx holds n_points triples
+ * (b, m, n).  Used where the full product is too large for the CPU. */
+int sbgemm_ref_points(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+                      const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+                      const float* C0, int64_t rsC, int64_t csC, int64_t bsC,
+                      int64_t M, int64_t N, int64_t K, int64_t batch,
+                      float alpha, int accumulate,
+                      const int64_t* idx, int64_t n_points,
+                      double* ref, double* bound) {
+    if (M < 0 || N < 0 || K < 0 || batch < 0 || n_points < 0) return -1;
+    for (int64_t p = 0; p < n_points; ++p) {
+        const int64_t b = idx[3 * p], m = idx[3 * p + 1], n = idx[3 * p + 2];
+        if (b < 0 || b >= batch || m < 0 || m >= M || n < 0 || n >= N) return -1;
+        double s = 0.0, t = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double prod = (double)A[b * bsA + m * rsA + k * csA] *
+                                (double)B[b * bsB + k * rsB + n * csB];
+            s += prod;
+            t += fabs(prod);
+        }
+        double r = (double)alpha * s;
+        double u = fabs((double)alpha) * t;
+        if (accumulate) {
+            const double c0 = (double)C0[b * bsC + m * rsC + n * csC];
+            r += c0;
+            u += fabs(c0);
+        }
+        ref[p] = r;
+        if (bound) bound[p] = u;
+    }
+    return 0;
+}

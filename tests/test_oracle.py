@@ -1,0 +1,272 @@
+"""Pins for the CPU oracle, run without a GPU.
+
+Each test checks the oracle against something other than itself: values the
+pages print (tests/golden), closed forms, special cases that reduce to a numpy
+library routine on explicitly materialised matrices, exact integer brute force,
+and invariants of the product's definition (StaleyNET "GPU Implementation",
+section "The matrix product").
+"""
+
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+# Awkward sizes: StaleyNET "Testing the kernels" (17 x 33 x 9, 5 x 129 x 31) and
+# the kael "How it is tested" matmul shapes (rows, inner, columns).
+AWKWARD_MNK = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (4, 4, 4), (5, 9, 3),
+               (8, 7, 16), (33, 65, 20), (64, 64, 1), (1, 1, 64)]
+LAYOUTS = ["row", "col", "neg_row", "gap", "bcast_row"]
+
+
+def _int_expected(case):
+    """alpha*A@B + C0 for integer-valued operands, computed exactly with numpy's
+    int64 matmul on the materialised strided views."""
+    A = case.A.view(case.batch, case.M, case.K).astype(np.int64)
+    B = case.B.view(case.batch, case.K, case.N).astype(np.int64)
+    s = np.matmul(A, B)
+    t = np.matmul(np.abs(A), np.abs(B))
+    ref = case.alpha * s.astype(np.float64)
+    bound = abs(case.alpha) * t.astype(np.float64)
+    if case.accumulate:
+        c0 = case.C.view(case.batch, case.M, case.N).astype(np.float64)
+        ref = ref + c0
+        bound = bound + np.abs(c0)
+    return ref, bound
+
+
+def _cases(seed=0):
+    rng = np.random.default_rng(seed)
+    out = []
+    j = 0
+    for i, (M, K, N) in enumerate(AWKWARD_MNK):
+        for la in LAYOUTS:
+            lb = LAYOUTS[(i + LAYOUTS.index(la)) % len(LAYOUTS)]
+            bsm = [("dense", "dense"), ("zero", "dense"), ("dense", "neg"),
+                   ("neg", "zero")][(i + len(la)) % 4]
+            batch = [1, 3, 2][i % 3]
+            # alpha and accumulate cycle independently so every pairing occurs.
+            alpha = [1.0, 0.125, -2.0][j % 3]
+            acc = (j // 3) % 2
+            j += 1
+            out.append(wl.random_strided(rng, M, N, K, batch, la, lb,
+                                         c_layout="col" if i % 2 else "row",
+                                         bs_mode=bsm, values="int",
+                                         accumulate=acc, alpha=alpha))
+    return out
+
+
+def run_int_pins(lib=None):
+    """Exact brute-force comparison over every layout; returns the number of
+    mismatching cases (0 for a correct oracle).  Also used on mutated builds."""
+    bad = 0
+    for case in _cases():
+        ref, bound = oracle.case_product(case, lib=lib, nthreads=3)
+        eref, ebound = _int_expected(case)
+        if not (np.array_equal(ref, eref) and np.array_equal(bound, ebound)):
+            bad += 1
+    return bad
+
+
+def test_brute_force_integers_all_layouts(oracle_lib):
+    assert run_int_pins() == 0
+
+
+def test_real_values_match_numpy_float64():
+    rng = np.random.default_rng(1)
+    for la, lb in [("row", "col"), ("col", "row"), ("neg_row", "gap"), ("gap", "bcast_row")]:
+        case = wl.random_strided(rng, 37, 29, 131, 2, la, lb, values="real",
+                                 accumulate=1, alpha=0.7)
+        ref, bound = oracle.case_product(case)
+        A = case.A.view(case.batch, case.M, case.K).astype(np.float64)
+        B = case.B.view(case.batch, case.K, case.N).astype(np.float64)
+        C0 = case.C.view(case.batch, case.M, case.N).astype(np.float64)
+        want = np.float64(np.float32(0.7)) * np.einsum("bmk,bkn->bmn", A, B) + C0
+        assert np.all(np.abs(ref - want) <= 1e-12 * bound + 1e-300)
+
+
+def test_golden_transposed_view():
+    """kael trace: x [2,3] = 0..5 read with strides (1,3) is [[0,3],[1,4],[2,5]].
+    I(3) * x^T through the oracle must reproduce the printed read-out."""
+    g = {}
+    for line in open(os.path.join(GOLDEN, "kael_transpose_view.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        key, *vals = line.split()
+        g[key] = [int(v) for v in vals]
+    storage = np.array(g["storage"], dtype=np.float32)
+    rs, cs = g["xT_strides"]
+    K, N = g["xT_shape"]           # x^T is [3, 2]: it plays B with K=3, N=2
+    eye = np.eye(K, dtype=np.float32).reshape(-1)
+    A = wl.Operand(eye, 0, K, 1, 0)
+    B = wl.Operand(storage, 0, rs, cs, 0)
+    C = wl.Operand(np.zeros(K * N, np.float32), 0, N, 1, 0)
+    ref, _ = oracle.product(A, B, C, K, N, K, 1, 1.0, 0)
+    assert ref.reshape(-1).tolist() == [float(v) for v in g["xT_rowmajor"]]
+
+
+def test_identity_exact_real_values():
+    rng = np.random.default_rng(2)
+    M, K, N = 19, 19, 23
+    a = rng.standard_normal(M * K).astype(np.float32)
+    b = rng.standard_normal(K * N).astype(np.float32)
+    eye = np.eye(19, dtype=np.float32).reshape(-1)
+    C = wl.Operand(np.zeros(M * N, np.float32), 0, N, 1, 0)
+    # A = I  =>  C = B bitwise (one non-zero term per sum).
+    ref, _ = oracle.product(wl.Operand(eye, 0, K, 1, 0), wl.Operand(b, 0, N, 1, 0),
+                            C, M, N, K, 1, 1.0, 0)
+    assert np.array_equal(ref[0], b.reshape(K, N).astype(np.float64))
+    # B = I read with swapped strides (still I)  =>  C = A.
+    C2 = wl.Operand(np.zeros(M * K, np.float32), 0, K, 1, 0)
+    ref, _ = oracle.product(wl.Operand(a, 0, K, 1, 0), wl.Operand(eye, 0, 1, 19, 0),
+                            C2, M, K, K, 1, 1.0, 0)
+    assert np.array_equal(ref[0], a.reshape(M, K).astype(np.float64))
+
+
+def test_zero_operand_and_overwrite_does_not_read_c():
+    M, K, N = 7, 5, 6
+    zeros = np.zeros(M * K, np.float32)
+    b = np.arange(K * N, dtype=np.float32)
+    c0 = np.random.default_rng(3).standard_normal(M * N).astype(np.float32)
+    nan_c = np.full(M * N, np.nan, np.float32)
+    A, B = wl.Operand(zeros, 0, K, 1, 0), wl.Operand(b, 0, N, 1, 0)
+    ref, _ = oracle.product(A, B, wl.Operand(nan_c, 0, N, 1, 0), M, N, K, 1, 1.0, 0)
+    assert np.all(ref == 0.0)
+    ref, bound = oracle.product(A, B, wl.Operand(c0, 0, N, 1, 0), M, N, K, 1, 3.0, 1)
+    assert np.array_equal(ref[0], c0.reshape(M, N).astype(np.float64))
+    assert np.array_equal(bound[0], np.abs(c0.reshape(M, N)).astype(np.float64))
+
+
+def test_swapped_strides_equal_explicit_transpose_copy():
+    rng = np.random.default_rng(4)
+    M, K, N = 13, 21, 17
+    a_km = rng.standard_normal((K, M)).astype(np.float32)   # stores A^T
+    b_nk = rng.standard_normal((N, K)).astype(np.float32)   # stores B^T
+    C = wl.Operand(np.zeros(M * N, np.float32), 0, N, 1, 0)
+    swapped, _ = oracle.product(wl.Operand(a_km.reshape(-1), 0, 1, M, 0),
+                                wl.Operand(b_nk.reshape(-1), 0, 1, K, 0),
+                                C, M, N, K, 1, 1.0, 0)
+    a_copy = np.ascontiguousarray(a_km.T).reshape(-1)
+    b_copy = np.ascontiguousarray(b_nk.T).reshape(-1)
+    copied, _ = oracle.product(wl.Operand(a_copy, 0, K, 1, 0),
+                               wl.Operand(b_copy, 0, N, 1, 0),
+                               C, M, N, K, 1, 1.0, 0)
+    assert np.array_equal(swapped, copied)
+
+
+def test_alpha_power_of_two_scaling_exact():
+    case = wl.make("c1", "real")
+    base, _ = oracle.case_product(case)
+    for j in (-3, 1, 5):
+        case.alpha = 2.0 ** j
+        scaled, _ = oracle.case_product(case)
+        assert np.array_equal(scaled, base * 2.0 ** j)
+
+
+def test_accumulate_minus_c0_equals_overwrite_integers():
+    rng = np.random.default_rng(5)
+    case = wl.random_strided(rng, 23, 11, 40, 2, "row", "col", values="int",
+                             accumulate=1, alpha=0.125)
+    acc, _ = oracle.case_product(case)
+    case.accumulate = 0
+    over, _ = oracle.case_product(case)
+    c0 = case.C.view(case.batch, case.M, case.N).astype(np.float64)
+    assert np.array_equal(acc - c0, over)
+
+
+def test_batch_permutation_and_zero_batch_stride():
+    rng = np.random.default_rng(6)
+    M, K, N, batch = 9, 12, 10, 4
+    a = rng.standard_normal(batch * M * K).astype(np.float32)
+    b = rng.standard_normal(batch * K * N).astype(np.float32)
+    C = wl.Operand(np.zeros(batch * M * N, np.float32), 0, N, 1, M * N)
+    ref, _ = oracle.product(wl.Operand(a, 0, K, 1, M * K), wl.Operand(b, 0, N, 1, K * N),
+                            C, M, N, K, batch, 1.0, 0)
+    perm = [2, 0, 3, 1]
+    ap = a.reshape(batch, -1)[perm].reshape(-1).copy()
+    bp = b.reshape(batch, -1)[perm].reshape(-1).copy()
+    refp, _ = oracle.product(wl.Operand(ap, 0, K, 1, M * K), wl.Operand(bp, 0, N, 1, K * N),
+                             C, M, N, K, batch, 1.0, 0)
+    assert np.array_equal(refp, ref[perm])
+    # Batch stride 0 on A and B: every batch entry is the same product.
+    ref0, _ = oracle.product(wl.Operand(a, 0, K, 1, 0), wl.Operand(b, 0, N, 1, 0),
+                             C, M, N, K, batch, 1.0, 0)
+    for i in range(1, batch):
+        assert np.array_equal(ref0[i], ref0[0])
+    assert np.array_equal(ref0[0], ref[0])
+
+
+def test_all_ones_closed_form_and_softmax_rows():
+    M, K, N = 8, 300, 5
+    ones_a = np.ones(M * K, np.float32)
+    ones_b = np.ones(K * N, np.float32)
+    C = wl.Operand(np.zeros(M * N, np.float32), 0, N, 1, 0)
+    ref, bound = oracle.product(wl.Operand(ones_a, 0, K, 1, 0),
+                                wl.Operand(ones_b, 0, N, 1, 0), C, M, N, K, 1, 1.0, 0)
+    assert np.all(ref == K) and np.all(bound == K)
+    # Softmax rows of the attention-output workload times a ones column sum to 1.
+    case = wl.make("c4", "real", batch=2, M=16, K=512, N=1)
+    ones = wl.Operand(np.ones(512, np.float32), 0, 1, 0, 0)
+    ref, _ = oracle.product(case.A, ones, wl.Operand(np.zeros(32, np.float32), 0, 1, 1, 16),
+                            16, 1, 512, 2, 1.0, 0)
+    assert np.all(np.abs(ref - 1.0) <= 1e-6)
+
+
+def test_thread_count_and_reverse_order_do_not_change_results():
+    case = wl.make("c2b", "real")
+    r1, b1 = oracle.case_product(case, nthreads=1)
+    r7, b7 = oracle.case_product(case, nthreads=7, reverse=True)
+    assert np.array_equal(r1, r7) and np.array_equal(b1, b7)
+
+
+def test_points_match_full_product():
+    rng = np.random.default_rng(7)
+    case = wl.random_strided(rng, 31, 27, 45, 3, "neg_row", "col", values="real",
+                             accumulate=1, alpha=-0.5, bs_mode=("neg", "dense"))
+    ref, bound = oracle.case_product(case)
+    idx = np.stack([rng.integers(0, 3, 50), rng.integers(0, 31, 50),
+                    rng.integers(0, 27, 50)], axis=1)
+    pr, pb = oracle.case_points(case, idx)
+    assert np.array_equal(pr, ref[idx[:, 0], idx[:, 1], idx[:, 2]])
+    assert np.array_equal(pb, bound[idx[:, 0], idx[:, 1], idx[:, 2]])
+
+
+def test_degenerate_sizes():
+    a = np.arange(12, dtype=np.float32)
+    c0 = np.arange(12, dtype=np.float32) - 5
+    A = wl.Operand(a, 0, 3, 1, 0)
+    # K = 0: overwrite gives zeros, accumulate gives C0 unchanged.
+    ref, _ = oracle.product(A, A, wl.Operand(c0, 0, 4, 1, 0), 3, 4, 0, 1, 2.0, 0)
+    assert np.all(ref == 0)
+    ref, _ = oracle.product(A, A, wl.Operand(c0, 0, 4, 1, 0), 3, 4, 0, 1, 2.0, 1)
+    assert np.array_equal(ref[0], c0.reshape(3, 4).astype(np.float64))
+    # Empty M, N or batch: nothing to compute.
+    for M, N, batch in ((0, 4, 1), (3, 0, 1), (3, 4, 0)):
+        ref, _ = oracle.product(A, A, wl.Operand(c0, 0, 4, 1, 0), M, N, 2, batch, 1.0, 0)
+        assert ref.size == 0
+
+
+def test_golden_flop_convention():
+    """The rate the pages print is 2*d0*d1*d2 / CPU time (printed rounded)."""
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "pytorch_demystified_gflops.txt"))
+            if l.strip() and not l.startswith("#")]
+    assert len(rows) == 21
+    for d0, d1, d2, _wall, t, g in rows:
+        decimals = len(t.split(".")[1]) if "." in t else 0
+        half = 0.5 * 10.0 ** (-decimals)
+        t_us = float(t)
+        lo = wl.gflops_per_s(int(d0), int(d1), int(d2), 1, (t_us + half) * 1e-6)
+        hi = wl.gflops_per_s(int(d0), int(d1), int(d2), 1, (t_us - half) * 1e-6)
+        assert lo <= float(g) <= hi, (d0, d1, d2, t, g)
+
+
+def test_spans_outside_storage_are_refused():
+    a = np.zeros(6, np.float32)
+    with pytest.raises(ValueError):
+        oracle.product(wl.Operand(a, 0, 3, 1, 0), wl.Operand(a, 0, 3, 1, 0),
+                       wl.Operand(a, 0, 3, 1, 0), 3, 3, 3, 1, 1.0, 0)

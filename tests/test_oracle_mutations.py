@@ -1,0 +1,50 @@
+"""The oracle's pins are sensitive: each plausible slip planted in a copy of the
+oracle's C source (on the CPU, in a temporary directory) makes at least one pin
+fail.  The oracle in the repository is never modified."""
+
+import os
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.test_oracle import run_int_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "sbgemm_ref.c")
+
+# (name, text in the source, replacement)
+MUTATIONS = [
+    ("drop_last_k_term", "for (int64_t k = 0; k < K; ++k) {\n        const double a",
+     "for (int64_t k = 0; k < K - 1; ++k) {\n        const double a"),
+    ("wrong_sign", "acc[n] += p;", "acc[n] -= p;"),
+    ("transposed_A", "m * j->rsA + k * j->csA", "m * j->csA + k * j->rsA"),
+    ("transposed_B_index", "brow[n * j->csB]", "brow[n * j->rsB]"),
+    ("alpha_scales_c0", "r += c0;\n            t += fabs(c0);",
+     "r += j->alpha * c0;\n            t += fabs(c0);"),
+    ("ignore_B_batch_stride", "j->B + b * j->bsB + k * j->rsB", "j->B + k * j->rsB"),
+    ("c0_row_col_swapped", "m * j->rsC + n * j->csC", "m * j->csC + n * j->rsC"),
+    ("bound_without_abs", "mag[n] += fabs(p);", "mag[n] += p;"),
+    ("output_rows_batch_major_swapped", "double* out = j->ref + (b * j->M + m) * N;",
+     "double* out = j->ref + (m * j->batch + b) * N;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = tmp_path / "mut.c"
+    mutated.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmut.so")
+    oracle.build(force=True, src=str(mutated), out=so)
+    lib = oracle.load(so)
+    assert run_int_pins(lib=lib) > 0, f"planted mistake {name} went unnoticed"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    shutil.copy(SRC, tmp_path / "same.c")
+    so = str(tmp_path / "libsame.so")
+    oracle.build(force=True, src=str(tmp_path / "same.c"), out=so)
+    assert run_int_pins(lib=oracle.load(so)) == 0

@@ -1,0 +1,342 @@
+"""Seeded synthetic inputs for the strided batched product C <- alpha*A*B (+C).
+
+This module is shared by the tests, the benchmark and the smoke check. It only
+draws random storage and describes how each operand is laid over that storage
+(pointer offset plus row / column / batch strides, in fp32 elements). It holds
+none of the product's arithmetic: the oracle and the CUDA library each compute
+the product on their own from these inputs.
+
+The workloads restate the five cases of the strided-batched problem statement
+(StaleyNET "GPU Implementation", section "The matrix product"; the linear-layer
+and attention shapes of "rvllm CUDA path", section "Matmuls go to cuBLAS"):
+
+  c1      one 64x48x32 product, row-major, overwrite
+  c2a     MLP layer y = x W^T, x [256,784], W [512,784] read transposed via strides
+  c2b     follow-on layer [256,512] . W2^T, W2 stored [10,512] (out, in)
+  c3      128 attention score products Q[512,64] K^T, alpha = 1/8
+  c3gqa   grouped-query variant: 4 Q heads stacked as 2048 rows against one K
+  c4      128 products P[512,512] V[512,64] + C0 (accumulate)
+  c5a     8192 x 960 -> 2560, W [2560,960] read transposed
+  c5b     8192 x 2560 -> 960, W [960,2560] read transposed
+  c5c     4096^3, row-major, accumulate
+  c5d     4096^3, A and B both read transposed by swapped strides, accumulate
+
+Every workload also has an integer pass (values uniform in {-8..8}) in which
+every partial sum is an exact fp32 integer.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional, Tuple
+
+import numpy as np
+
+__all__ = ["Operand", "Case", "WORKLOADS", "make", "flops", "gflops_per_s",
+           "alg_bytes", "SEEDS"]
+
+
+@dataclasses.dataclass
+class Operand:
+    """One operand laid over a flat fp32 storage array.
+
+    Element (b, i, j) of the logical [batch, rows, cols] operand lives at
+    ``storage[offset + b*bs + i*rs + j*cs]``.
+    """
+    storage: np.ndarray          # 1-D float32, C-contiguous
+    offset: int                  # element offset of (0, 0, 0)
+    rs: int
+    cs: int
+    bs: int
+
+    def view(self, batch: int, rows: int, cols: int) -> np.ndarray:
+        """Strided numpy view of the logical [batch, rows, cols] operand (no copy).
+
+        Used only by tests to materialise operands for library cross-checks.
+        """
+        base = self.storage[self.offset:]
+        item = self.storage.itemsize
+        return np.lib.stride_tricks.as_strided(
+            base, shape=(batch, rows, cols),
+            strides=(self.bs * item, self.rs * item, self.cs * item),
+            writeable=False)
+
+
+@dataclasses.dataclass
+class Case:
+    name: str
+    A: Operand
+    B: Operand
+    C: Operand                   # C0 lives in C.storage when accumulate
+    M: int
+    N: int
+    K: int
+    batch: int
+    alpha: float
+    accumulate: int
+    values: str                  # "real" or "int"
+    note: str = ""
+
+    @property
+    def flops(self) -> int:
+        return flops(self.M, self.N, self.K, self.batch)
+
+
+def flops(M: int, N: int, K: int, batch: int = 1) -> int:
+    """Multiply-adds counted as two operations, one pair per (b, m, n, k).
+
+    This is the counting the pages' own GFLOP/s tables use (checked against the
+    printed google-benchmark rows in the golden test)."""
+    return 2 * int(M) * int(N) * int(K) * int(batch)
+
+
+def gflops_per_s(M: int, N: int, K: int, batch: int, seconds: float) -> float:
+    return flops(M, N, K, batch) / seconds / 1e9
+
+
+def alg_bytes(case: "Case") -> int:
+    """Algorithmic HBM bytes of one product: A and B read once, C written once,
+    C0 read once when accumulating (fp32 elements; broadcast operands once)."""
+    a_batches = 1 if case.A.bs == 0 else case.batch
+    b_batches = 1 if case.B.bs == 0 else case.batch
+    n = (a_batches * case.M * case.K + b_batches * case.K * case.N
+         + case.batch * case.M * case.N * (2 if case.accumulate else 1))
+    return 4 * n
+
+
+# Seeds follow the order of the workload list: c1 = 0 (as the problem states),
+# c2 = 1, c3 = 2, c4 = 3, c5 = 4.
+SEEDS = {"c1": 0, "c2a": 1, "c2b": 1, "c3": 2, "c3gqa": 2, "c4": 3,
+         "c5a": 4, "c5b": 4, "c5c": 4, "c5d": 4}
+# Sub-stream per workload sharing a seed, so c2a and c2b draw different values.
+_STREAM = {"c1": 0, "c2a": 0, "c2b": 1, "c3": 0, "c3gqa": 1, "c4": 0,
+           "c5a": 0, "c5b": 1, "c5c": 2, "c5d": 2}
+
+# Full-size shapes.  Keys that a caller may override to shrink a case for the
+# oracle: batch, M, N, K (and heads/seqs for the attention cases).
+FULL: Dict[str, Dict[str, int]] = {
+    "c1": dict(batch=1, M=64, N=48, K=32),
+    "c2a": dict(batch=1, M=256, N=512, K=784),
+    "c2b": dict(batch=1, M=256, N=10, K=512),
+    "c3": dict(batch=128, M=512, N=512, K=64),          # 8 sequences x 16 heads
+    "c3gqa": dict(batch=32, M=2048, N=512, K=64),       # 8 seqs x 4 KV heads, 4 Q heads each
+    "c4": dict(batch=128, M=512, N=64, K=512),
+    "c5a": dict(batch=1, M=8192, N=2560, K=960),
+    "c5b": dict(batch=1, M=8192, N=960, K=2560),
+    "c5c": dict(batch=1, M=4096, N=4096, K=4096),
+    "c5d": dict(batch=1, M=4096, N=4096, K=4096),
+}
+WORKLOADS = tuple(FULL)
+
+
+def _rng(name: str, values: str) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(
+        [SEEDS[name], _STREAM[name], 0 if values == "real" else 1]))
+
+
+def _flat(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+
+
+def _ints(rng: np.random.Generator, shape) -> np.ndarray:
+    return rng.integers(-8, 9, size=shape).astype(np.float32)
+
+
+def _uniform(rng, lo, hi, shape):
+    return rng.uniform(lo, hi, size=shape).astype(np.float32)
+
+
+def _normal(rng, std, shape):
+    return (rng.standard_normal(size=shape, dtype=np.float32) * np.float32(std))
+
+
+def _softmax_rows(logits: np.ndarray) -> np.ndarray:
+    """Row-wise softmax, used only to shape the config-4 probability inputs."""
+    z = logits.astype(np.float64)
+    z = z - z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+def make(name: str, values: str = "real", **shape) -> Case:
+    """Build workload ``name`` with ``values`` in {"real", "int"}.
+
+    ``shape`` may override batch / M / N / K to obtain a smaller case of the
+    same layout (for the oracle); strides follow the (possibly shrunk) sizes.
+    """
+    if name not in FULL:
+        raise KeyError(name)
+    if values not in ("real", "int"):
+        raise ValueError(values)
+    dims = dict(FULL[name])
+    dims.update({k: int(v) for k, v in shape.items()})
+    batch, M, N, K = dims["batch"], dims["M"], dims["N"], dims["K"]
+    rng = _rng(name, values)
+    is_int = values == "int"
+
+    def draw(kind: str, shp, *args):
+        if is_int:
+            return _ints(rng, shp)
+        if kind == "u":
+            return _uniform(rng, args[0], args[1], shp)
+        if kind == "n":
+            return _normal(rng, args[0], shp)
+        if kind == "softmax":
+            return _softmax_rows(_normal(rng, args[0], shp))
+        raise ValueError(kind)
+
+    empty_c = lambda: np.zeros(batch * M * N, dtype=np.float32)
+
+    if name == "c1":
+        a = draw("u", (M, K), -1.0, 1.0)
+        b = draw("u", (K, N), -1.0, 1.0)
+        return Case(name, Operand(_flat(a), 0, K, 1, M * K),
+                    Operand(_flat(b), 0, N, 1, K * N),
+                    Operand(empty_c(), 0, N, 1, M * N),
+                    M, N, K, batch, 1.0, 0, values,
+                    "row-major A and B, overwrite")
+
+    if name in ("c2a", "c2b"):
+        x = draw("u", (M, K), 0.0, 1.0)
+        w = draw("n", (N, K), 0.05)
+        # y = x W^T: B[k][n] = W[n][k] -> rsB = 1, csB = K (W's row length).
+        return Case(name, Operand(_flat(x), 0, K, 1, M * K),
+                    Operand(_flat(w), 0, 1, K, N * K),
+                    Operand(empty_c(), 0, N, 1, M * N),
+                    M, N, K, batch, 1.0, 0, values,
+                    "weights [out,in] read transposed by swapped strides")
+
+    if name == "c3":
+        # Q and K head-major, contiguous per (sequence, head): [batch, T, D].
+        q = draw("n", (batch, M, K), 1.0)
+        k = draw("n", (batch, N, K), 1.0)
+        return Case(name, Operand(_flat(q), 0, K, 1, M * K),
+                    Operand(_flat(k), 0, 1, K, N * K),
+                    Operand(empty_c(), 0, N, 1, M * N),
+                    M, N, K, batch, 0.125, 0, values,
+                    "S = Q K^T / sqrt(64), K read transposed")
+
+    if name == "c3gqa":
+        # Q stored [seqs, kv_heads, 4 q heads, T, D]; the 4 Q heads of a group
+        # are consecutive, so they read as M = 4*T rows with rsA = D.
+        q = draw("n", (batch, M, K), 1.0)
+        k = draw("n", (batch, N, K), 1.0)
+        return Case(name, Operand(_flat(q), 0, K, 1, M * K),
+                    Operand(_flat(k), 0, 1, K, N * K),
+                    Operand(empty_c(), 0, N, 1, M * N),
+                    M, N, K, batch, 0.125, 0, values,
+                    "grouped-query: 4 Q heads stacked as rows against one K")
+
+    if name == "c4":
+        p = draw("softmax", (batch, M, K), 2.0)
+        v = draw("n", (batch, K, N), 1.0)
+        c0 = draw("n", (batch, M, N), 1.0)
+        return Case(name, Operand(_flat(p), 0, K, 1, M * K),
+                    Operand(_flat(v), 0, N, 1, K * N),
+                    Operand(_flat(c0), 0, N, 1, M * N),
+                    M, N, K, batch, 1.0, 1, values,
+                    "O = P V + C0, P rows softmax of normal(0,2) logits")
+
+    if name in ("c5a", "c5b"):
+        act = draw("n", (M, K), 1.0)
+        w = draw("n", (N, K), 0.02)
+        return Case(name, Operand(_flat(act), 0, K, 1, M * K),
+                    Operand(_flat(w), 0, 1, K, N * K),
+                    Operand(empty_c(), 0, N, 1, M * N),
+                    M, N, K, batch, 1.0, 0, values,
+                    "projection, W [out,in] read transposed")
+
+    if name in ("c5c", "c5d"):
+        # The square workloads may be shrunk to a non-square box; storage
+        # stays row-major in each operand's own stored shape.
+        a = draw("n", (M, K), 1.0) if name == "c5c" else draw("n", (K, M), 1.0)
+        b = draw("n", (K, N), 0.02) if name == "c5c" else draw("n", (N, K), 0.02)
+        c0 = draw("n", (M, N), 1.0)
+        if name == "c5c":
+            A = Operand(_flat(a), 0, K, 1, M * K)
+            B = Operand(_flat(b), 0, N, 1, K * N)
+            note = "square, row-major, accumulate"
+        else:
+            # A stored row-major [K, M] and read transposed: rsA = 1, csA = M.
+            A = Operand(_flat(a), 0, 1, M, M * K)
+            B = Operand(_flat(b), 0, 1, K, K * N)
+            note = "square, A and B read transposed by swapped strides, accumulate"
+        return Case(name, A, B, Operand(_flat(c0), 0, N, 1, M * N),
+                    M, N, K, batch, 1.0, 1, values, note)
+
+    raise AssertionError(name)
+
+
+def small_shape(name: str) -> Dict[str, int]:
+    """A reduced size of each workload that the CPU oracle computes in about a
+    second while still spanning several 128x128 tiles and a ragged tail."""
+    return {
+        "c1": dict(FULL["c1"]),
+        "c2a": dict(FULL["c2a"]),
+        "c2b": dict(FULL["c2b"]),
+        "c3": dict(batch=3, M=512, N=512, K=64),
+        "c3gqa": dict(batch=2, M=2048, N=512, K=64),
+        "c4": dict(batch=3, M=512, N=64, K=512),
+        "c5a": dict(batch=1, M=300, N=2560, K=960),
+        "c5b": dict(batch=1, M=300, N=960, K=2560),
+        "c5c": dict(batch=1, M=260, N=1030, K=1024),
+        "c5d": dict(batch=1, M=260, N=1030, K=1024),
+    }[name]
+
+
+def random_strided(rng: np.random.Generator, M: int, N: int, K: int, batch: int,
+                   a_layout: str, b_layout: str, c_layout: str = "row",
+                   bs_mode: Tuple[str, str] = ("dense", "dense"),
+                   values: str = "int", accumulate: int = 0, alpha: float = 1.0,
+                   pad: int = 0) -> Case:
+    """Small case with a chosen layout per operand.
+
+    Layouts: "row" (unit column stride), "col" (unit row stride), "neg_row"
+    (row-major but rows walked backwards: negative row stride), "gap" (row-major
+    with a padded row pitch), "bcast_row" (row stride 0: every row is the same
+    memory). ``bs_mode`` per A/B: "dense", "zero" (batch stride 0, one shared
+    matrix), "neg" (batches walked backwards).
+    """
+    def lay(rows, cols, layout, bsm):
+        if layout in ("row", "neg_row", "gap"):
+            rs, cs = (cols + (3 if layout == "gap" else 0) + pad), 1
+            span = rows * rs
+        elif layout == "col":
+            rs, cs = 1, rows + pad
+            span = cols * cs
+        elif layout == "bcast_row":
+            rs, cs = 0, 1
+            span = cols
+        else:
+            raise ValueError(layout)
+        nb = 1 if bsm == "zero" else batch
+        bs = 0 if bsm == "zero" else span
+        total = max(1, nb * span)
+        if values == "int":
+            st = rng.integers(-8, 9, size=total).astype(np.float32)
+        else:
+            st = rng.uniform(-1, 1, size=total).astype(np.float32)
+        off = 0
+        if layout == "neg_row":
+            off += (rows - 1) * rs
+            rs = -rs
+        if bsm == "neg":
+            off += (nb - 1) * bs
+            bs = -bs
+        return Operand(st, off, rs, cs, bs)
+
+    A = lay(M, K, a_layout, bs_mode[0])
+    B = lay(K, N, b_layout, bs_mode[1])
+    if c_layout == "row":
+        C = Operand(np.zeros(max(1, batch * M * N), np.float32), 0, N, 1, M * N)
+    elif c_layout == "col":
+        C = Operand(np.zeros(max(1, batch * M * N), np.float32), 0, 1, M, M * N)
+    else:
+        raise ValueError(c_layout)
+    if accumulate:
+        if values == "int":
+            C.storage[:] = rng.integers(-8, 9, size=C.storage.size)
+        else:
+            C.storage[:] = rng.uniform(-1, 1, size=C.storage.size)
+    return Case(f"rand_{a_layout}_{b_layout}_{c_layout}", A, B, C, M, N, K, batch,
+                alpha, accumulate, values)
