@@ -1,0 +1,482 @@
+#!/usr/bin/env python3
+"""Benchmark of the strided batched fp32 product on GB300.
+
+One step = the large projection sweep, four products through the C-ABI on one
+stream, each over resident synthetic inputs:
+    c5a  8192 x 960  -> 2560, W[2560,960] read transposed by strides
+    c5b  8192 x 2560 -> 960,  W[960,2560] read transposed by strides
+    c5c  4096^3, row-major, accumulate into C
+    c5d  4096^3, A and B read transposed by swapped strides, accumulate
+(`--workload` selects another workload of the same set instead).
+
+Prints ONE JSON line: GFLOP/s of the timed steps (2*M*N*K*batch per product),
+the dominant kernel's roofline fraction, the CPU oracle timed on a bounded
+sample, an end-to-end figure with host buffers, and the SM clocks sampled
+while the timed steps ran.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--math fp32|tf32]
+                    [--workload c5|c1|...] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "GFLOP/s of strided batched fp32 GEMM; % of FP32 (or TF32 TC) peak, 1×GB300"
+L2_BYTES = 129 * 1024 * 1024
+FP32_FLOP_PER_CLK_PER_SM = 256      # 128 FP32 lanes x 2 flop per FMA
+TF32_OVER_BF16_NOMINAL = 1.1 / 2.25  # dense nominal tf32 / bf16 tensor rates
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}
+
+SWEEPS = {"c5": ["c5a", "c5b", "c5c", "c5d"], "c3all": ["c3", "c3gqa"]}
+DESCR = {
+    "c5": "large projection sweep: 8192x960->2560 (W^T), 8192x2560->960 (W^T), "
+          "4096^3 row-major +C, 4096^3 A^T B^T +C",
+}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- peaks, clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None, period_ms: int = 100):
+        self.rows = []
+        self.proc = None
+        self.marks = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               "-lms", str(period_ms)]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc is not None and not self.rows and time.time() - t0 < timeout:
+            time.sleep(0.05)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1]
+        if not rows:
+            rows = [r for (_, r) in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_uuid(torch):
+    try:
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- workloads
+
+def workload_cases(name):
+    names = SWEEPS.get(name, [name])
+    return names, [wl.make(n, "real") for n in names]
+
+
+def case_args(case, dA, dB, dC):
+    return (dA.data_ptr() + 4 * case.A.offset, case.A.rs, case.A.cs, case.A.bs,
+            dB.data_ptr() + 4 * case.B.offset, case.B.rs, case.B.cs, case.B.bs,
+            dC.data_ptr() + 4 * case.C.offset, case.C.rs, case.C.cs, case.C.bs,
+            case.M, case.N, case.K, case.batch, case.alpha, case.accumulate)
+
+
+def kernel_source_digest(path_name):
+    files = {"gather_ffma": ["ffma_gather.cu"], "tma_ffma": ["ffma_tma.cu"],
+             "tma_tf32": ["tf32_tc.cu"]}.get(path_name, [])
+    h = hashlib.sha256()
+    for f in files:
+        p = os.path.join(ROOT, "strided_gemm_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(path_name, case_name):
+    """DRAM bytes per launch from a committed ncu summary, if its kernel source
+    digest still matches the source being timed."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{path_name}_{case_name}.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_digest") != kernel_source_digest(path_name):
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(cases, seconds_target, threads, rows_override=None):
+    """Times the oracle on the first rows of each product.  Returns
+    (gflop_per_s, seconds, flops, rows)."""
+    import oracle
+    oracle.load()
+
+    def run(rows):
+        fl = 0
+        t0 = time.perf_counter()
+        for c in cases:
+            r = min(rows, c.M)
+            oracle.product(c.A, c.B, c.C, r, c.N, c.K, min(c.batch, 1), c.alpha, c.accumulate,
+                           nthreads=threads)
+            fl += wl.flops(r, c.N, c.K, min(c.batch, 1))
+        return time.perf_counter() - t0, fl
+
+    if rows_override is None:
+        dt, fl = run(threads)                         # calibration pass
+        rate = fl / max(dt, 1e-6)
+        per_row = sum(wl.flops(1, c.N, c.K, 1) for c in cases)
+        rows = int(max(threads, min(max(c.M for c in cases),
+                                    seconds_target * rate / per_row)))
+    else:
+        rows = rows_override
+    dt, fl = run(rows)
+    return fl / dt / 1e9, dt, fl, rows
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args, world, rank, local, dist):
+    import torch
+    import strided_gemm_gb300 as sg
+    from strided_gemm_gb300 import build as sgbuild
+
+    torch.cuda.set_device(local)
+    sgbuild.build()
+    sg.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    s_handle = stream.cuda_stream
+    math = sg.MATH_TF32 if args.math == "tf32" else sg.MATH_FP32
+
+    names, cases = workload_cases(args.workload)
+    dev_bufs = []
+    for c in cases:
+        dA = torch.from_numpy(c.A.storage).to(dev)
+        dB = torch.from_numpy(c.B.storage).to(dev)
+        dC = torch.from_numpy(c.C.storage).to(dev)
+        dev_bufs.append((dA, dB, dC))
+    calls = [case_args(c, *b) for c, b in zip(cases, dev_bufs)]
+    plans = [sg.sbgemm_plan(*a[:16], c.accumulate, math=math) for c, a in zip(cases, calls)]
+    flops_step = sum(c.flops for c in cases)
+    bytes_step = sum(wl.alg_bytes(c) for c in cases)
+    ws_bytes = sum(c.A.storage.nbytes + c.B.storage.nbytes + c.C.storage.nbytes for c in cases)
+
+    def launch(i):
+        sg.sbgemm_ex(*calls[i], s_handle, math=math)
+
+    def step():
+        for i in range(len(calls)):
+            launch(i)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_uuid(torch))
+    sampler.wait_first()
+    # Per-launch events for the kernel-level roofline; whole-step events below.
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for k in range(args.steps):
+        for i in range(len(calls)):
+            ev[k][i][0].record(stream)
+            launch(i)
+            ev[k][i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(dist)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    elapsed_ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(dist, elapsed_ms)
+    ms_per_step = ms_max / args.steps
+    value = flops_step * world * args.steps / (ms_max * 1e-3) / 1e9
+
+    per = {}
+    for i, (n, c) in enumerate(zip(names, cases)):
+        ms = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
+        avg = sum(ms) / len(ms)
+        per[n] = {"ms": round(avg, 4), "gflops": round(c.flops / (avg * 1e-3) / 1e9, 1),
+                  "path": plans[i]["path_name"], "tile": [plans[i]["tile_m"], plans[i]["tile_n"]],
+                  "total_ms": sum(ms)}
+
+    # Dominant kernel: the launch (product) with the largest total time.
+    dom = max(per, key=lambda n: per[n]["total_ms"])
+    dcase = cases[names.index(dom)]
+    peaks, peaks_src = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = float(peaks.get("sm_max_mhz") or FALLBACK["sm_max_mhz"])
+    dom_path = per[dom]["path"]
+    avg_s = per[dom]["ms"] * 1e-3
+    if dom_path == "tma_tf32":
+        peak = float(peaks.get("bf16_tflops", FALLBACK["bf16_tflops"])) * TF32_OVER_BF16_NOMINAL
+        roof = {"bound": "tensor", "achieved": round(dcase.flops / avg_s / 1e12, 2),
+                "peak": round(peak, 1), "unit": "TFLOP/s",
+                "peak_source": f"{peaks_src} bf16 dense burst x nominal tf32/bf16 ratio "
+                               f"{TF32_OVER_BF16_NOMINAL:.3f}"}
+    else:
+        peak = sms * FP32_FLOP_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": round(dcase.flops / avg_s / 1e12, 2),
+                "peak": round(peak, 2), "unit": "TFLOP/s",
+                "peak_source": f"{sms} SMs x 256 fp32 flop/clk x {sm_max:.0f} MHz ({peaks_src} max clock)"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    if clocks.get("sm_mhz"):
+        roof["frac_at_sampled_clock"] = round(roof["frac"] * sm_max / clocks["sm_mhz"], 4)
+    roof["traffic"] = profiled_traffic(dom_path, dom)
+    roof["kernel"] = f"{dom_path} ({dom})"
+    roof["alg_bytes_per_launch"] = wl.alg_bytes(dcase)
+    roof["hbm_frac"] = round(wl.alg_bytes(dcase) / avg_s / 1e9 /
+                             float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])), 4)
+
+    # End to end through the public API with host buffers: every step copies its
+    # inputs from pinned host memory, runs the products and reads C back.
+    e2e = None
+    if not args.no_e2e:
+        host_in = [(torch.from_numpy(c.A.storage).pin_memory(),
+                    torch.from_numpy(c.B.storage).pin_memory(),
+                    torch.from_numpy(c.C.storage).pin_memory()) for c in cases]
+        host_out = [torch.empty_like(h[2]).pin_memory() for h in host_in]
+        h2d = sum(h[0].numel() * 4 + h[1].numel() * 4 + (h[2].numel() * 4 if c.accumulate else 0)
+                  for h, c in zip(host_in, cases))
+        d2h = sum(h.numel() * 4 for h in host_out)
+        n_e2e = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            for i, c in enumerate(cases):
+                dA, dB, dC = dev_bufs[i]
+                dA.copy_(host_in[i][0], non_blocking=True)
+                dB.copy_(host_in[i][1], non_blocking=True)
+                if c.accumulate:
+                    dC.copy_(host_in[i][2], non_blocking=True)
+                launch(i)
+                host_out[i].copy_(dC, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
+        e2e = {"value": round(flops_step * world * n_e2e / (e_ms * 1e-3) / 1e9, 1),
+               "unit": "GFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": n_e2e, "ms_per_step": round(e_ms / n_e2e, 3)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.default_threads()
+        g, dt, fl, rows = oracle_sample(cases, args.cpu_seconds, threads)
+        cpu = {"value": round(g, 3), "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} rows of each product of the step "
+                         f"({fl / 1e9:.2f} GFLOP, {dt:.1f} s), fp64 accumulation"}
+
+    if rank != 0:
+        return None
+    wsmb = ws_bytes / 2**20
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if math == sg.MATH_FP32 else "tf32",
+        "data": "synthetic (seeded numpy generators, shapes and value distributions of the workload)",
+        "config": {"workload": DESCR.get(args.workload, args.workload),
+                   "products_per_step": len(cases), "math": args.math,
+                   "gflop_per_step": round(flops_step / 1e9, 3),
+                   "alg_mb_per_step": round(bytes_step / 2**20, 1),
+                   "l2": f"inputs larger than L2: {wsmb:.0f} MiB resident per step vs "
+                         f"{L2_BYTES / 2**20:.0f} MiB L2, no flush",
+                   "parallelism": f"replicas x{world} (each GPU runs the whole step)"},
+        "pct_of_peak": round(100 * value / world / 1e3 / roof["peak"], 2)
+        if roof["unit"] == "TFLOP/s" else None,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": len(calls) * args.steps,
+        "clocks": clocks,
+        "per_product": {n: {k: v for k, v in d.items() if k != "total_ms"} for n, d in per.items()},
+    }
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands on the host cores, one bounded sample of the
+    workload per step."""
+    if rank != 0:
+        return None
+    import oracle
+    threads = oracle.default_threads()
+    names, cases = workload_cases(args.workload)
+    _, dt, fl, rows = oracle_sample(cases, args.ref_step_seconds, threads)
+    for _ in range(args.warmup):
+        oracle_sample(cases, 0, threads, rows_override=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(cases, 0, threads, rows_override=rows)
+    el = time.perf_counter() - t0
+    value = fl * args.steps / el / 1e9
+    sample = f"first {rows} rows of each product per step ({fl / 1e9:.3f} GFLOP)"
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCR.get(args.workload, args.workload), "math": "fp64 oracle"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "kind": "oracle",
+                         "cores": threads, "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--math", choices=["fp32", "tf32"], default="fp32")
+    ap.add_argument("--workload", default="c5",
+                    choices=sorted(set(wl.WORKLOADS) | set(SWEEPS)))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=0.5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+    else:
+        dist = init_dist(world)
+        out = run_ours(args, world, rank, local, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

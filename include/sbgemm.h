@@ -1,0 +1,174 @@
+/*
+ * sbgemm: strided batched fp32 matrix product on one GB300 (sm_103a).
+ *
+ *     C[b] <- alpha * A[b] * B[b]            (accumulate == 0)
+ *     C[b] <- alpha * A[b] * B[b] + C[b]     (accumulate != 0)
+ *
+ * for b = 0 .. batch-1, where A[b] is M x K, B[b] is K x N and C[b] is M x N.
+ *
+ * Source of the operation: StaleyNET, "GPU Implementation", section "The matrix
+ * product" -- one kernel computes, for a batch of matrix pairs, alpha times A
+ * times B with the previous C optionally added; every input is described by the
+ * memory distance between neighbouring rows and between neighbouring columns,
+ * so a transposed input is the same memory with the two distances exchanged,
+ * and the batch covers all heads and sequences of attention in one launch.  The
+ * argument list generalises the row-major cuBLAS call of "rvllm CUDA path"
+ * (section "Matmuls go to cuBLAS": lda/ldb/ldc and a strided batch) and the
+ * {batches, rows, inner, columns} sizes of the kael.cpp "CUDA backend" page.
+ *
+ * Layout.  Every operand is a base pointer plus three strides counted in fp32
+ * ELEMENTS (not bytes), signed 64-bit:
+ *     A[b][m][k] = A[b*bsA + m*rsA + k*csA]
+ *     B[b][k][n] = B[b*bsB + k*rsB + n*csB]
+ *     C[b][m][n] = C[b*bsC + m*rsC + n*csC]
+ * A transposed read is the stored matrix with rs and cs exchanged (a row-major
+ * W[N][K] read as B = W^T has rsB = 1, csB = K).  Strides of A and B may be
+ * zero (broadcast: one matrix shared by every batch entry, or one row shared
+ * by every row) or negative.  C's strides must map distinct (b, m, n) to
+ * distinct elements.
+ *
+ * Numerics.  sbgemm and sbgemm_ex with math = SBGEMM_MATH_FP32 compute every
+ * product and sum in fp32 with fused multiply-adds, each output's terms added
+ * in increasing k, and the result formed as fmaf(alpha, sum, C_old).  Integer
+ * inputs whose partial sums stay below 2^24 give exact results.
+ * SBGEMM_MATH_TF32 (opt-in, sbgemm_ex only) rounds A and B to tf32 on the
+ * tensor cores and accumulates in fp32.
+ *
+ * Ownership and synchronisation.  All pointers are device memory owned by the
+ * caller (cudaMalloc, cudaMallocAsync, managed memory, or any allocator that
+ * hands out such memory).  The library allocates nothing per call; it keeps
+ * only immutable per-device properties, initialised once.  Calls are enqueued
+ * on `stream` (a cudaStream_t; NULL = the legacy default stream) and return
+ * without synchronising; errors raised inside a kernel surface at the
+ * caller's next synchronisation.  The functions are thread-safe.
+ *
+ * Edge cases.  M, N or batch equal to 0: nothing is done (SBGEMM_OK, pointers
+ * may be NULL).  K == 0: C <- alpha*0 (overwrite) or C is left as it was
+ * (accumulate).  Without accumulation C is never read, so stale NaNs in C do
+ * not leak into the result.
+ *
+ * Errors are returned as sbgemm_status codes; nothing is launched on error.
+ */
+#ifndef SBGEMM_H
+#define SBGEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SBGEMM_API __attribute__((visibility("default")))
+#else
+#define SBGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SBGEMM_OK = 0,
+    SBGEMM_ERR_INVALID_VALUE = 1,   /* negative size, misaligned pointer, stride
+                                       span overflowing int64, bad option value */
+    SBGEMM_ERR_NULL_POINTER = 2,    /* a needed operand pointer is NULL */
+    SBGEMM_ERR_OUTPUT_OVERLAP = 3,  /* C's strides map two outputs to one element,
+                                       or C's address span meets A's or B's */
+    SBGEMM_ERR_UNSUPPORTED = 4,     /* a forced path cannot serve this layout */
+    SBGEMM_ERR_CUDA = 5,            /* CUDA runtime/driver error (launch, attribute,
+                                       tensor-map encoding, no device) */
+    SBGEMM_ERR_DEVICE_TIMEOUT = 6,  /* a bounded in-kernel wait expired; see
+                                       sbgemm_device_status */
+    SBGEMM_ERR_NOT_DEVICE_MEMORY = 7 /* an operand is not device-accessible memory,
+                                       or its span leaves its allocation */
+} sbgemm_status;
+
+/* Arithmetic of sbgemm_options.math. */
+enum {
+    SBGEMM_MATH_FP32 = 0,  /* fp32 FFMA on the CUDA cores (default, strict) */
+    SBGEMM_MATH_TF32 = 1   /* tf32 inputs, fp32 accumulation, on the tensor cores */
+};
+
+/* Kernel paths; sbgemm_options.force_path and sbgemm_plan_info.path. */
+enum {
+    SBGEMM_PATH_NONE = -1,        /* nothing to launch (empty problem, or
+                                     K == 0 with accumulate) */
+    SBGEMM_PATH_AUTO = 0,         /* let the planner choose */
+    SBGEMM_PATH_GATHER_FFMA = 1,  /* any strides: coalesced strided gather into
+                                     shared memory, FFMA register micro-tiles */
+    SBGEMM_PATH_TMA_FFMA = 2,     /* unit-stride operands: TMA + mbarrier ring,
+                                     FFMA register micro-tiles */
+    SBGEMM_PATH_TMA_TF32 = 3      /* unit-stride operands: TMA + tcgen05.mma
+                                     kind::tf32 with the accumulator in TMEM */
+};
+
+/* Operand layout classes reported by sbgemm_plan. */
+enum {
+    SBGEMM_LAYOUT_K_MAJOR = 0,   /* unit stride along K (A: csA == 1, B: rsB == 1);
+                                    for C: unit stride along N (csC == 1) */
+    SBGEMM_LAYOUT_MN_MAJOR = 1,  /* unit stride along M (A) or N (B);
+                                    for C: unit stride along M (rsC == 1) */
+    SBGEMM_LAYOUT_GENERAL = 2    /* no unit stride */
+};
+
+typedef struct {
+    int math;          /* SBGEMM_MATH_* */
+    int force_path;    /* SBGEMM_PATH_AUTO or a specific path */
+    int reserved[6];   /* must be zero */
+} sbgemm_options;
+
+typedef struct {
+    int path;                 /* SBGEMM_PATH_* chosen (NONE: no launch) */
+    int a_layout, b_layout, c_layout;   /* SBGEMM_LAYOUT_* */
+    int a_broadcast, b_broadcast;       /* batch stride 0 with batch > 1 */
+    int a_tma, b_tma;         /* operand can be fetched by a TMA tensor map */
+    int tile_m, tile_n, tile_k;
+    int ctas_per_sm;          /* resident CTAs per SM the plan assumes */
+    int64_t ctas;             /* CTAs launched (0 when path == NONE) */
+    int64_t tiles;            /* output tiles over all batch entries */
+    int reserved[8];
+} sbgemm_plan_info;
+
+/* Strict fp32 product on the CUDA cores; the planner picks the kernel.
+ * Arguments as described above; stream is a cudaStream_t (NULL = default). */
+SBGEMM_API int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+           const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+           float* C, int64_t rsC, int64_t csC, int64_t bsC,
+           int64_t M, int64_t N, int64_t K, int64_t batch,
+           float alpha, int accumulate, void* stream);
+
+/* As sbgemm, with the arithmetic and the kernel path chosen by `opt` (NULL =
+ * defaults).  math = SBGEMM_MATH_TF32 opts in to the tensor cores; when the
+ * operands cannot be fetched by TMA the planner falls back to strict fp32
+ * unless the TF32 path was forced (then SBGEMM_ERR_UNSUPPORTED). */
+SBGEMM_API int sbgemm_ex(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+              const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+              float* C, int64_t rsC, int64_t csC, int64_t bsC,
+              int64_t M, int64_t N, int64_t K, int64_t batch,
+              float alpha, int accumulate, void* stream,
+              const sbgemm_options* opt);
+
+/* Validate and plan without launching or touching device memory: reports the
+ * layout classes and the kernel path, tile and CTA count that sbgemm_ex would
+ * use.  Pointers are only checked for NULL and alignment (no device query). */
+SBGEMM_API int sbgemm_plan(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+                const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+                const float* C, int64_t rsC, int64_t csC, int64_t bsC,
+                int64_t M, int64_t N, int64_t K, int64_t batch,
+                int accumulate, const sbgemm_options* opt,
+                sbgemm_plan_info* info);
+
+/* Reads and clears the device-side status word that bounded in-kernel waits
+ * set when they give up (after synchronising `stream`).  Returns SBGEMM_OK or
+ * SBGEMM_ERR_DEVICE_TIMEOUT; *where_out (may be NULL) receives a code naming
+ * the wait that expired (0 if none). */
+SBGEMM_API int sbgemm_device_status(void* stream, int* where_out);
+
+/* Static, human-readable name of a status code. */
+SBGEMM_API const char* sbgemm_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+SBGEMM_API int sbgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SBGEMM_H */

@@ -1,0 +1,202 @@
+"""Python binding of libsbgemm, the strided batched fp32 product for GB300.
+
+The functions below carry the C names and arguments of include/sbgemm.h and do
+argument marshalling only: every step of the product runs in the library's
+CUDA kernels.  Pointers are plain integers (device addresses); strides are in
+fp32 elements.  A non-zero status raises SbgemmError.
+
+``matmul`` is a convenience over torch CUDA tensors viewed as [batch, rows,
+cols] (any strides, including expand()-ed zero strides).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "SbgemmError", "load", "sbgemm", "sbgemm_ex", "sbgemm_plan",
+    "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version", "matmul",
+    "SBGEMM_OK", "SBGEMM_ERR_INVALID_VALUE", "SBGEMM_ERR_NULL_POINTER",
+    "SBGEMM_ERR_OUTPUT_OVERLAP", "SBGEMM_ERR_UNSUPPORTED", "SBGEMM_ERR_CUDA",
+    "SBGEMM_ERR_DEVICE_TIMEOUT", "SBGEMM_ERR_NOT_DEVICE_MEMORY",
+    "MATH_FP32", "MATH_TF32", "PATH_NONE", "PATH_AUTO", "PATH_GATHER_FFMA",
+    "PATH_TMA_FFMA", "PATH_TMA_TF32", "LAYOUT_K_MAJOR", "LAYOUT_MN_MAJOR",
+    "LAYOUT_GENERAL", "EXPORTED_SYMBOLS", "LIB_PATH",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsbgemm.so")
+
+SBGEMM_OK = 0
+SBGEMM_ERR_INVALID_VALUE = 1
+SBGEMM_ERR_NULL_POINTER = 2
+SBGEMM_ERR_OUTPUT_OVERLAP = 3
+SBGEMM_ERR_UNSUPPORTED = 4
+SBGEMM_ERR_CUDA = 5
+SBGEMM_ERR_DEVICE_TIMEOUT = 6
+SBGEMM_ERR_NOT_DEVICE_MEMORY = 7
+
+MATH_FP32, MATH_TF32 = 0, 1
+PATH_NONE, PATH_AUTO, PATH_GATHER_FFMA, PATH_TMA_FFMA, PATH_TMA_TF32 = -1, 0, 1, 2, 3
+LAYOUT_K_MAJOR, LAYOUT_MN_MAJOR, LAYOUT_GENERAL = 0, 1, 2
+PATH_NAMES = {PATH_NONE: "none", PATH_GATHER_FFMA: "gather_ffma",
+              PATH_TMA_FFMA: "tma_ffma", PATH_TMA_TF32: "tma_tf32"}
+
+# Every function include/sbgemm.h declares.
+EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_device_status",
+                    "sbgemm_status_string", "sbgemm_version")
+
+
+class SbgemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {sbgemm_status_string(status)} ({status})")
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("math", ctypes.c_int), ("force_path", ctypes.c_int),
+                ("reserved", ctypes.c_int * 6)]
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("a_layout", ctypes.c_int),
+                ("b_layout", ctypes.c_int), ("c_layout", ctypes.c_int),
+                ("a_broadcast", ctypes.c_int), ("b_broadcast", ctypes.c_int),
+                ("a_tma", ctypes.c_int), ("b_tma", ctypes.c_int),
+                ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("tile_k", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
+                ("reserved", ctypes.c_int * 8)]
+
+
+_lock = threading.Lock()
+_lib = None
+_i64, _vp = ctypes.c_int64, ctypes.c_void_p
+_ARGS = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _i64,
+         _i64, _i64, _i64, _i64]
+
+
+def load(path: str = LIB_PATH):
+    """Load libsbgemm.so.  Raises if the library has not been built: there is
+    no fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libsbgemm.so is missing at {path}; build it with "
+                "`python -m strided_gemm_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(path)
+        lib.sbgemm.restype = ctypes.c_int
+        lib.sbgemm.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp]
+        lib.sbgemm_ex.restype = ctypes.c_int
+        lib.sbgemm_ex.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp,
+                                          ctypes.POINTER(_Options)]
+        lib.sbgemm_plan.restype = ctypes.c_int
+        lib.sbgemm_plan.argtypes = _ARGS + [ctypes.c_int, ctypes.POINTER(_Options),
+                                            ctypes.POINTER(_PlanInfo)]
+        lib.sbgemm_device_status.restype = ctypes.c_int
+        lib.sbgemm_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
+        lib.sbgemm_status_string.restype = ctypes.c_char_p
+        lib.sbgemm_status_string.argtypes = [ctypes.c_int]
+        lib.sbgemm_version.restype = ctypes.c_int
+        lib.sbgemm_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _opts(math: int, force_path: int):
+    o = _Options()
+    o.math = int(math)
+    o.force_path = int(force_path)
+    return o
+
+
+def sbgemm_status_string(status: int) -> str:
+    return load().sbgemm_status_string(int(status)).decode()
+
+
+def sbgemm_version() -> int:
+    return load().sbgemm_version()
+
+
+def sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+           M, N, K, batch, alpha, accumulate, stream=0) -> None:
+    st = load().sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                       M, N, K, batch, float(alpha), int(bool(accumulate)), stream or None)
+    if st:
+        raise SbgemmError(st, "sbgemm")
+
+
+def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+              M, N, K, batch, alpha, accumulate, stream=0,
+              math: int = MATH_FP32, force_path: int = PATH_AUTO) -> None:
+    o = _opts(math, force_path)
+    st = load().sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                          M, N, K, batch, float(alpha), int(bool(accumulate)),
+                          stream or None, ctypes.byref(o))
+    if st:
+        raise SbgemmError(st, "sbgemm_ex")
+
+
+def sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                M, N, K, batch, accumulate=0, math: int = MATH_FP32,
+                force_path: int = PATH_AUTO) -> dict:
+    """Validate and plan without launching; returns the plan as a dict."""
+    o = _opts(math, force_path)
+    info = _PlanInfo()
+    st = load().sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                            M, N, K, batch, int(bool(accumulate)), ctypes.byref(o),
+                            ctypes.byref(info))
+    if st:
+        raise SbgemmError(st, "sbgemm_plan")
+    d = {name: getattr(info, name) for name, _ in _PlanInfo._fields_ if name != "reserved"}
+    d["path_name"] = PATH_NAMES.get(d["path"], "?")
+    return d
+
+
+def sbgemm_device_status(stream=0):
+    """Synchronise `stream`, then read and clear the in-kernel wait status.
+    Returns (status, where)."""
+    where = ctypes.c_int(0)
+    st = load().sbgemm_device_status(stream or None, ctypes.byref(where))
+    return st, where.value
+
+
+def _as3(t, name):
+    if t.dim() == 2:
+        t = t.unsqueeze(0)
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be 2-D or 3-D, got {tuple(t.shape)}")
+    return t
+
+
+def matmul(A, B, C, alpha: float = 1.0, accumulate: bool = False,
+           math: int = MATH_FP32, force_path: int = PATH_AUTO, stream=None):
+    """C <- alpha*A@B (+C) on torch CUDA float32 tensors viewed as [batch, M, K],
+    [batch, K, N] and [batch, M, N] (2-D means batch 1).  Strides are taken from
+    the tensors, so transposed or expanded views need no copy.  Returns C."""
+    import torch
+    A3, B3, C3 = _as3(A, "A"), _as3(B, "B"), _as3(C, "C")
+    for t, n in ((A3, "A"), (B3, "B"), (C3, "C")):
+        if t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{n} must be a float32 CUDA tensor")
+    batch, M, K = C3.shape[0], C3.shape[1], A3.shape[2]
+    N = C3.shape[2]
+    if A3.shape[1] != M or B3.shape[1] != K or B3.shape[2] != N:
+        raise ValueError(f"shape mismatch: A{tuple(A3.shape)} B{tuple(B3.shape)} C{tuple(C3.shape)}")
+    for t, n in ((A3, "A"), (B3, "B")):
+        if t.shape[0] not in (1, batch):
+            raise ValueError(f"{n} batch {t.shape[0]} does not match {batch}")
+    bsA = A3.stride(0) if A3.shape[0] == batch else 0
+    bsB = B3.stride(0) if B3.shape[0] == batch else 0
+    if stream is None:
+        stream = torch.cuda.current_stream(C3.device).cuda_stream
+    sbgemm_ex(A3.data_ptr(), A3.stride(1), A3.stride(2), bsA,
+              B3.data_ptr(), B3.stride(1), B3.stride(2), bsB,
+              C3.data_ptr(), C3.stride(1), C3.stride(2), C3.stride(0),
+              M, N, K, batch, alpha, accumulate, stream, math, force_path)
+    return C

@@ -1,0 +1,63 @@
+// Internal declarations shared by the host API and the kernel translation units.
+// Nothing here is exported from the shared library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sbgemm.h"
+
+namespace sbg {
+
+// One call of the product, strides in fp32 elements (see include/sbgemm.h).
+struct Problem {
+    const float* A; int64_t rsA, csA, bsA;
+    const float* B; int64_t rsB, csB, bsB;
+    float* C;       int64_t rsC, csC, bsC;
+    int64_t M, N, K, batch;
+    float alpha;
+    int accumulate;
+};
+
+// Per-device properties, read once per device and immutable afterwards.
+struct DeviceProps {
+    int device;
+    int sm_count;
+    int max_smem_per_block_optin;   // bytes
+    int max_smem_per_sm;            // bytes
+    int cc_major, cc_minor;
+};
+
+// Returns NULL if the device cannot be queried.
+const DeviceProps* device_props(int device);
+
+// Kernel variant chosen by the planner.
+struct Plan {
+    int path = SBGEMM_PATH_NONE;
+    int a_layout = SBGEMM_LAYOUT_GENERAL, b_layout = SBGEMM_LAYOUT_GENERAL,
+        c_layout = SBGEMM_LAYOUT_GENERAL;
+    bool a_broadcast = false, b_broadcast = false;
+    bool a_tma = false, b_tma = false;
+    int tile_m = 0, tile_n = 0, tile_k = 0;
+    int ctas_per_sm = 0;
+    int variant = 0;                // kernel-specific configuration index
+    int64_t tiles_m = 0, tiles_n = 0;
+    int64_t tiles = 0;              // tiles_m * tiles_n * batch
+    int64_t ctas = 0;
+};
+
+// ---- strided-gather FFMA path (ffma_gather.cu) --------------------------------
+// Tile configurations of the gather kernel.
+struct GatherConfig { int bm, bn, bk, threads, ctas_per_sm; };
+int gather_config_count();
+GatherConfig gather_config(int variant);
+// Picks a variant for the problem size on a device with `sm_count` SMs.
+int gather_pick_variant(const Problem& p, int sm_count);
+cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t stream);
+
+// ---- driver entry points (driver.cpp) ---------------------------------------
+// [base, base+size) of the allocation that contains `ptr`; false if `ptr` is not
+// in a device-accessible allocation known to the driver.
+bool device_allocation_range(const void* ptr, uintptr_t* base, size_t* size);
+
+}  // namespace sbg

@@ -1,0 +1,362 @@
+// C-ABI boundary: argument validation, operand layout classification, kernel
+// planning and dispatch for the strided batched product.
+//
+// The checks follow the StaleyNET "GPU Implementation" page, section "Safety":
+// every size the kernel depends on is checked before the launch, so a launch
+// never reads or writes memory outside what the caller described.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <array>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "sbgemm.h"
+
+namespace sbg {
+
+// ---- device properties ------------------------------------------------------
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::array<std::once_flag, kMaxDevices> g_props_once;
+std::array<DeviceProps, kMaxDevices> g_props;
+std::array<bool, kMaxDevices> g_props_ok{};
+}  // namespace
+
+const DeviceProps* device_props(int device) {
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    std::call_once(g_props_once[device], [device] {
+        DeviceProps d{};
+        d.device = device;
+        bool ok = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.max_smem_per_block_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.max_smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, device) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, device) == cudaSuccess;
+        g_props[device] = d;
+        g_props_ok[device] = ok;
+    });
+    return g_props_ok[device] ? &g_props[device] : nullptr;
+}
+
+namespace {
+
+inline int64_t mag(int64_t x) { return x < 0 ? -x : x; }
+
+// Element-offset span [lo, hi] of an operand over its [batch][rows][cols] box.
+// Returns false if the span does not fit comfortably in int64 byte offsets.
+struct Span { int64_t lo, hi; };
+
+bool operand_span(int64_t batch, int64_t rows, int64_t cols,
+                  int64_t bs, int64_t rs, int64_t cs, Span* out) {
+    __int128 lo = 0, hi = 0;
+    const int64_t st[3] = {bs, rs, cs};
+    const int64_t ex[3] = {batch, rows, cols};
+    for (int i = 0; i < 3; ++i) {
+        __int128 d = (__int128)st[i] * (ex[i] - 1);
+        if (d < 0) lo += d; else hi += d;
+    }
+    const __int128 limit = (__int128)1 << 60;   // elements; 4x that in bytes
+    if (lo < -limit || hi > limit) return false;
+    out->lo = (int64_t)lo;
+    out->hi = (int64_t)hi;
+    return true;
+}
+
+// Distinct (b, m, n) map to distinct elements: sorted by stride magnitude,
+// each stride must exceed the largest offset reachable by the smaller ones.
+// This sufficient test rejects a few exotic injective layouts as overlapping.
+bool output_injective(int64_t batch, int64_t M, int64_t N,
+                      int64_t bs, int64_t rs, int64_t cs) {
+    std::array<std::pair<int64_t, int64_t>, 3> d = {{{mag(bs), batch}, {mag(rs), M}, {mag(cs), N}}};
+    std::sort(d.begin(), d.end());
+    __int128 reach = 0;
+    for (auto& [s, e] : d) {
+        if (e <= 1) continue;
+        if ((__int128)s <= reach) return false;
+        reach += (__int128)s * (e - 1);
+    }
+    return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int classify_a(const Problem& p) {
+    if (p.K == 1 || p.csA == 1) return SBGEMM_LAYOUT_K_MAJOR;
+    if (p.M == 1 || p.rsA == 1) return SBGEMM_LAYOUT_MN_MAJOR;
+    return SBGEMM_LAYOUT_GENERAL;
+}
+int classify_b(const Problem& p) {
+    if (p.K == 1 || p.rsB == 1) return SBGEMM_LAYOUT_K_MAJOR;
+    if (p.N == 1 || p.csB == 1) return SBGEMM_LAYOUT_MN_MAJOR;
+    return SBGEMM_LAYOUT_GENERAL;
+}
+int classify_c(const Problem& p) {
+    if (p.N == 1 || p.csC == 1) return SBGEMM_LAYOUT_K_MAJOR;
+    if (p.M == 1 || p.rsC == 1) return SBGEMM_LAYOUT_MN_MAJOR;
+    return SBGEMM_LAYOUT_GENERAL;
+}
+
+// A TMA tensor map can describe the operand: a unit stride on its inner index,
+// a 16-byte aligned base, and outer / batch strides that are positive
+// multiples of 16 bytes below 2^40 (a stride over an extent of 1 is unused).
+bool tma_eligible(const void* base, int layout, int64_t outer_stride, int64_t outer_extent,
+                  int64_t bs, int64_t batch, int64_t inner_extent) {
+    if (layout == SBGEMM_LAYOUT_GENERAL) return false;
+    if (!aligned(base, 16)) return false;
+    auto ok_stride = [](int64_t s, int64_t extent) {
+        if (extent <= 1) return true;
+        return s > 0 && (s * 4) % 16 == 0 && (s * 4) < ((int64_t)1 << 40);
+    };
+    if (!ok_stride(outer_stride, outer_extent)) return false;
+    if (batch > 1 && bs != 0 && !ok_stride(bs, batch)) return false;
+    if (inner_extent >= ((int64_t)1 << 32) || outer_extent >= ((int64_t)1 << 32) ||
+        batch >= ((int64_t)1 << 32)) return false;
+    return true;
+}
+
+int check_options(const sbgemm_options* opt, sbgemm_options* out) {
+    sbgemm_options o{};
+    if (opt) o = *opt;
+    if (o.math != SBGEMM_MATH_FP32 && o.math != SBGEMM_MATH_TF32) return SBGEMM_ERR_INVALID_VALUE;
+    if (o.force_path < SBGEMM_PATH_AUTO || o.force_path > SBGEMM_PATH_TMA_TF32) return SBGEMM_ERR_INVALID_VALUE;
+    for (int r : o.reserved) if (r != 0) return SBGEMM_ERR_INVALID_VALUE;
+    *out = o;
+    return SBGEMM_OK;
+}
+
+// Host-side checks that need no device.  Fills the spans of A, B and C.
+int validate(const Problem& p, Span* sa, Span* sb, Span* sc, bool* empty) {
+    if (p.M < 0 || p.N < 0 || p.K < 0 || p.batch < 0) return SBGEMM_ERR_INVALID_VALUE;
+    *empty = (p.M == 0 || p.N == 0 || p.batch == 0);
+    if (*empty) return SBGEMM_OK;
+    if (!p.C) return SBGEMM_ERR_NULL_POINTER;
+    if (p.K > 0 && (!p.A || !p.B)) return SBGEMM_ERR_NULL_POINTER;
+    if (!aligned(p.C, 4) || (p.K > 0 && (!aligned(p.A, 4) || !aligned(p.B, 4))))
+        return SBGEMM_ERR_INVALID_VALUE;
+    if (!operand_span(p.batch, p.M, p.N, p.bsC, p.rsC, p.csC, sc)) return SBGEMM_ERR_INVALID_VALUE;
+    if (p.K > 0) {
+        if (!operand_span(p.batch, p.M, p.K, p.bsA, p.rsA, p.csA, sa)) return SBGEMM_ERR_INVALID_VALUE;
+        if (!operand_span(p.batch, p.K, p.N, p.bsB, p.rsB, p.csB, sb)) return SBGEMM_ERR_INVALID_VALUE;
+    }
+    if (!output_injective(p.batch, p.M, p.N, p.bsC, p.rsC, p.csC)) return SBGEMM_ERR_OUTPUT_OVERLAP;
+    if (p.K > 0) {
+        auto bytes = [](const void* base, const Span& s, __int128* lo, __int128* hi) {
+            *lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.lo * 4;
+            *hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.hi * 4 + 4;
+        };
+        __int128 clo, chi, lo, hi;
+        bytes(p.C, *sc, &clo, &chi);
+        bytes(p.A, *sa, &lo, &hi);
+        if (lo < chi && clo < hi) return SBGEMM_ERR_OUTPUT_OVERLAP;
+        bytes(p.B, *sb, &lo, &hi);
+        if (lo < chi && clo < hi) return SBGEMM_ERR_OUTPUT_OVERLAP;
+    }
+    return SBGEMM_OK;
+}
+
+// The operand's whole span lies inside one device-accessible allocation.
+bool span_in_allocation(const void* base, const Span& s) {
+    uintptr_t abase = 0;
+    size_t asize = 0;
+    if (!device_allocation_range(base, &abase, &asize)) return false;
+    const __int128 lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.lo * 4;
+    const __int128 hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.hi * 4 + 4;
+    return lo >= (__int128)abase && hi <= (__int128)abase + (__int128)asize;
+}
+
+int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empty, Plan* plan) {
+    *plan = Plan{};
+    if (empty || (p.K == 0 && p.accumulate)) {
+        plan->path = SBGEMM_PATH_NONE;
+        return SBGEMM_OK;
+    }
+    plan->a_layout = classify_a(p);
+    plan->b_layout = classify_b(p);
+    plan->c_layout = classify_c(p);
+    plan->a_broadcast = p.batch > 1 && p.bsA == 0;
+    plan->b_broadcast = p.batch > 1 && p.bsB == 0;
+    if (p.K > 0) {
+        // A: inner index K (K-major) or M; B: inner index K (K-major) or N.
+        const bool ak = plan->a_layout == SBGEMM_LAYOUT_K_MAJOR;
+        const bool bk = plan->b_layout == SBGEMM_LAYOUT_K_MAJOR;
+        plan->a_tma = tma_eligible(p.A, plan->a_layout, ak ? p.rsA : p.csA, ak ? p.M : p.K,
+                                   p.bsA, p.batch, ak ? p.K : p.M);
+        plan->b_tma = tma_eligible(p.B, plan->b_layout, bk ? p.csB : p.rsB, bk ? p.N : p.K,
+                                   p.bsB, p.batch, bk ? p.K : p.N);
+    }
+
+    int path = o.force_path;
+    if (path == SBGEMM_PATH_TMA_FFMA || path == SBGEMM_PATH_TMA_TF32) {
+        return SBGEMM_ERR_UNSUPPORTED;   // kernels not built into this library yet
+    }
+    if (path == SBGEMM_PATH_AUTO) path = SBGEMM_PATH_GATHER_FFMA;
+
+    plan->path = path;
+    const int v = gather_pick_variant(p, sm_count);
+    const GatherConfig g = gather_config(v);
+    plan->variant = v;
+    plan->tile_m = g.bm;
+    plan->tile_n = g.bn;
+    plan->tile_k = g.bk;
+    plan->ctas_per_sm = g.ctas_per_sm;
+    plan->tiles_m = (p.M + g.bm - 1) / g.bm;
+    plan->tiles_n = (p.N + g.bn - 1) / g.bn;
+    if (plan->tiles_m * plan->tiles_n >= ((int64_t)1 << 31)) return SBGEMM_ERR_UNSUPPORTED;
+    plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
+    plan->ctas = plan->tiles_m * plan->tiles_n * std::min<int64_t>(p.batch, 65535);
+    return SBGEMM_OK;
+}
+
+Problem make_problem(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+                     const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+                     const float* C, int64_t rsC, int64_t csC, int64_t bsC,
+                     int64_t M, int64_t N, int64_t K, int64_t batch,
+                     float alpha, int accumulate) {
+    Problem p;
+    p.A = A; p.rsA = rsA; p.csA = csA; p.bsA = bsA;
+    p.B = B; p.rsB = rsB; p.csB = csB; p.bsB = bsB;
+    p.C = const_cast<float*>(C); p.rsC = rsC; p.csC = csC; p.bsC = bsC;
+    p.M = M; p.N = N; p.K = K; p.batch = batch;
+    p.alpha = alpha;
+    p.accumulate = accumulate ? 1 : 0;
+    return p;
+}
+
+void fill_info(const Plan& plan, sbgemm_plan_info* info) {
+    std::memset(info, 0, sizeof(*info));
+    info->path = plan.path;
+    info->a_layout = plan.a_layout;
+    info->b_layout = plan.b_layout;
+    info->c_layout = plan.c_layout;
+    info->a_broadcast = plan.a_broadcast;
+    info->b_broadcast = plan.b_broadcast;
+    info->a_tma = plan.a_tma;
+    info->b_tma = plan.b_tma;
+    info->tile_m = plan.tile_m;
+    info->tile_n = plan.tile_n;
+    info->tile_k = plan.tile_k;
+    info->ctas_per_sm = plan.ctas_per_sm;
+    info->ctas = plan.ctas;
+    info->tiles = plan.tiles;
+}
+
+// SM count for planning: the current device's when one is present, otherwise
+// the GB300 figure, so sbgemm_plan works on machines without a GPU.
+int planning_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+        if (const DeviceProps* d = device_props(dev)) return d->sm_count;
+    }
+    cudaGetLastError();
+    return 152;
+}
+
+}  // namespace
+}  // namespace sbg
+
+using namespace sbg;
+
+extern "C" {
+
+int sbgemm_version(void) { return 100; }
+
+const char* sbgemm_status_string(int status) {
+    switch (status) {
+        case SBGEMM_OK: return "SBGEMM_OK";
+        case SBGEMM_ERR_INVALID_VALUE: return "SBGEMM_ERR_INVALID_VALUE";
+        case SBGEMM_ERR_NULL_POINTER: return "SBGEMM_ERR_NULL_POINTER";
+        case SBGEMM_ERR_OUTPUT_OVERLAP: return "SBGEMM_ERR_OUTPUT_OVERLAP";
+        case SBGEMM_ERR_UNSUPPORTED: return "SBGEMM_ERR_UNSUPPORTED";
+        case SBGEMM_ERR_CUDA: return "SBGEMM_ERR_CUDA";
+        case SBGEMM_ERR_DEVICE_TIMEOUT: return "SBGEMM_ERR_DEVICE_TIMEOUT";
+        case SBGEMM_ERR_NOT_DEVICE_MEMORY: return "SBGEMM_ERR_NOT_DEVICE_MEMORY";
+        default: return "SBGEMM_ERR_UNKNOWN";
+    }
+}
+
+int sbgemm_plan(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+                const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+                const float* C, int64_t rsC, int64_t csC, int64_t bsC,
+                int64_t M, int64_t N, int64_t K, int64_t batch,
+                int accumulate, const sbgemm_options* opt,
+                sbgemm_plan_info* info) {
+    if (!info) return SBGEMM_ERR_NULL_POINTER;
+    sbgemm_options o;
+    int st = check_options(opt, &o);
+    if (st) return st;
+    Problem p = make_problem(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                             M, N, K, batch, 1.0f, accumulate);
+    Span sa{}, sb{}, sc{};
+    bool empty = false;
+    st = validate(p, &sa, &sb, &sc, &empty);
+    if (st) return st;
+    Plan plan;
+    st = make_plan(p, o, planning_sm_count(), empty, &plan);
+    if (st) return st;
+    fill_info(plan, info);
+    return SBGEMM_OK;
+}
+
+int sbgemm_ex(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+              const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+              float* C, int64_t rsC, int64_t csC, int64_t bsC,
+              int64_t M, int64_t N, int64_t K, int64_t batch,
+              float alpha, int accumulate, void* stream,
+              const sbgemm_options* opt) {
+    sbgemm_options o;
+    int st = check_options(opt, &o);
+    if (st) return st;
+    Problem p = make_problem(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                             M, N, K, batch, alpha, accumulate);
+    Span sa{}, sb{}, sc{};
+    bool empty = false;
+    st = validate(p, &sa, &sb, &sc, &empty);
+    if (st) return st;
+    if (empty || (p.K == 0 && p.accumulate)) return SBGEMM_OK;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
+    const DeviceProps* props = device_props(dev);
+    if (!props) return SBGEMM_ERR_CUDA;
+
+    if (!span_in_allocation(p.C, sc)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    if (p.K > 0 && (!span_in_allocation(p.A, sa) || !span_in_allocation(p.B, sb)))
+        return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+
+    Plan plan;
+    st = make_plan(p, o, props->sm_count, false, &plan);
+    if (st) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaSuccess;
+    switch (plan.path) {
+        case SBGEMM_PATH_GATHER_FFMA: err = launch_gather_ffma(p, plan, s); break;
+        default: return SBGEMM_ERR_UNSUPPORTED;
+    }
+    if (err != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
+    return SBGEMM_OK;
+}
+
+int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+           const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+           float* C, int64_t rsC, int64_t csC, int64_t bsC,
+           int64_t M, int64_t N, int64_t K, int64_t batch,
+           float alpha, int accumulate, void* stream) {
+    return sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                     M, N, K, batch, alpha, accumulate, stream, nullptr);
+}
+
+int sbgemm_device_status(void* stream, int* where_out) {
+    if (where_out) *where_out = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SBGEMM_ERR_CUDA;
+    }
+    return SBGEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, and validates / classifies / plans without a device.  No
+compute call is made here."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import strided_gemm_gb300 as sg
+from strided_gemm_gb300 import build as sgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sbgemm.h")
+
+BASE = 0x7F0000000000   # fake, 256-byte aligned addresses: sbgemm_plan never dereferences
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    sgbuild.build()
+    sg.load()
+
+
+def header_functions():
+    txt = open(HEADER).read()
+    return re.findall(r"SBGEMM_API\s+[\w\s\*]+?\b(sbgemm\w*)\s*\(", txt)
+
+
+def test_header_and_binding_agree():
+    assert sorted(header_functions()) == sorted(sg.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(sg.LIB_PATH)
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", sg.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert exported == set(header_functions()), exported
+
+
+def test_status_strings_and_version():
+    assert sg.sbgemm_status_string(0) == "SBGEMM_OK"
+    assert sg.sbgemm_status_string(3) == "SBGEMM_ERR_OUTPUT_OVERLAP"
+    assert sg.sbgemm_status_string(99) == "SBGEMM_ERR_UNKNOWN"
+    assert sg.sbgemm_version() >= 100
+
+
+def call_plan(A, B, C, M, N, K, batch, accumulate=0, **kw):
+    return sg.sbgemm_plan(*A, *B, *C, M, N, K, batch, accumulate, **kw)
+
+
+def rowmajor(base, rows, cols, batch):
+    return (base, cols, 1, rows * cols)
+
+
+def test_classifier_layouts():
+    M, N, K = 256, 512, 784
+    # y = x W^T: A row-major (K-major), B = W^T with rsB = 1 (K-major), C row-major.
+    p = call_plan(rowmajor(BASE, M, K, 1), (BASE + (1 << 32), 1, K, N * K),
+                  rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1)
+    assert (p["a_layout"], p["b_layout"], p["c_layout"]) == (sg.LAYOUT_K_MAJOR,) * 3
+    assert p["a_tma"] and p["b_tma"]
+    # P V: B row-major -> unit stride along N.
+    p = call_plan(rowmajor(BASE, 512, 512, 1), rowmajor(BASE + (1 << 32), 512, 64, 1),
+                  rowmajor(BASE + (2 << 32), 512, 64, 1), 512, 64, 512, 1)
+    assert p["b_layout"] == sg.LAYOUT_MN_MAJOR
+    # Both operands read transposed via swapped strides.
+    p = call_plan((BASE, 1, 4096, 0), (BASE + (1 << 32), 1, 4096, 0),
+                  rowmajor(BASE + (2 << 32), 4096, 4096, 1), 4096, 4096, 4096, 1)
+    assert (p["a_layout"], p["b_layout"]) == (sg.LAYOUT_MN_MAJOR, sg.LAYOUT_K_MAJOR)
+    # General strides (no unit stride) are not TMA-eligible.
+    p = call_plan((BASE, 3, 7, 0), (BASE + (1 << 32), 5, 2, 0),
+                  rowmajor(BASE + (2 << 32), 10, 10, 1), 10, 10, 10, 1)
+    assert p["a_layout"] == sg.LAYOUT_GENERAL and not p["a_tma"]
+    assert p["path"] == sg.PATH_GATHER_FFMA
+
+
+def test_tma_eligibility_rules():
+    M, N, K = 64, 48, 32
+    good = call_plan(rowmajor(BASE, M, K, 1), rowmajor(BASE + (1 << 32), K, N, 1),
+                     rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1)
+    assert good["a_tma"] and good["b_tma"]
+    # Base not 16-byte aligned.
+    p = call_plan((BASE + 4, K, 1, 0), rowmajor(BASE + (1 << 32), K, N, 1),
+                  rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1)
+    assert not p["a_tma"]
+    # Row pitch not a multiple of 16 bytes (33 floats).
+    p = call_plan((BASE, 33, 1, 0), rowmajor(BASE + (1 << 32), K, N, 1),
+                  rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1)
+    assert not p["a_tma"]
+    # Negative row stride.
+    p = call_plan((BASE + 4096 * 64, -K, 1, 0), rowmajor(BASE + (1 << 32), K, N, 1),
+                  rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1)
+    assert not p["a_tma"] and p["path"] == sg.PATH_GATHER_FFMA
+    # Zero batch stride (shared operand) keeps TMA eligibility and is flagged.
+    p = call_plan((BASE, K, 1, 0), rowmajor(BASE + (1 << 32), K, N, 1),
+                  (BASE + (2 << 32), N, 1, M * N), M, N, K, 4)
+    assert p["a_tma"] and p["a_broadcast"] and not p["b_broadcast"]
+
+
+def test_validation_errors():
+    A = rowmajor(BASE, 8, 8, 1)
+    B = rowmajor(BASE + (1 << 32), 8, 8, 1)
+    C = rowmajor(BASE + (2 << 32), 8, 8, 1)
+
+    def code(*args, **kw):
+        with pytest.raises(sg.SbgemmError) as e:
+            call_plan(*args, **kw)
+        return e.value.status
+
+    assert code(A, B, C, -1, 8, 8, 1) == sg.SBGEMM_ERR_INVALID_VALUE
+    assert code(A, B, C, 8, 8, 8, -2) == sg.SBGEMM_ERR_INVALID_VALUE
+    assert code(A, B, (0, 8, 1, 64), 8, 8, 8, 1) == sg.SBGEMM_ERR_NULL_POINTER
+    assert code((0, 8, 1, 64), B, C, 8, 8, 8, 1) == sg.SBGEMM_ERR_NULL_POINTER
+    assert code((BASE + 2, 8, 1, 64), B, C, 8, 8, 8, 1) == sg.SBGEMM_ERR_INVALID_VALUE
+    # C not injective: zero batch stride with batch > 1, zero row stride, or
+    # a row pitch shorter than the row.
+    assert code(A, B, (C[0], 8, 1, 0), 8, 8, 8, 2) == sg.SBGEMM_ERR_OUTPUT_OVERLAP
+    assert code(A, B, (C[0], 0, 1, 64), 8, 8, 8, 1) == sg.SBGEMM_ERR_OUTPUT_OVERLAP
+    assert code(A, B, (C[0], 4, 1, 64), 8, 8, 8, 1) == sg.SBGEMM_ERR_OUTPUT_OVERLAP
+    # C overlapping A's span.
+    assert code(A, B, (BASE + 4 * 32, 8, 1, 64), 8, 8, 8, 1) == sg.SBGEMM_ERR_OUTPUT_OVERLAP
+    # Spans that overflow.
+    assert code((BASE, 1 << 62, 1, 0), B, C, 8, 8, 8, 1) == sg.SBGEMM_ERR_INVALID_VALUE
+    # Bad options.
+    assert code(A, B, C, 8, 8, 8, 1, math=7) == sg.SBGEMM_ERR_INVALID_VALUE
+    assert code(A, B, C, 8, 8, 8, 1, force_path=9) == sg.SBGEMM_ERR_INVALID_VALUE
+
+
+def test_injective_layouts_accepted():
+    A = rowmajor(BASE, 8, 8, 1)
+    B = rowmajor(BASE + (1 << 32), 8, 8, 1)
+    # Column-major C, padded pitch, negative strides, batch-innermost layout.
+    for C in [(BASE + (2 << 32), 1, 8, 64), (BASE + (2 << 32), 11, 1, 100),
+              (BASE + (2 << 32) + 4 * 1000, -8, -1, 64), (BASE + (2 << 32), 24, 3, 1)]:
+        p = call_plan(A, B, C, 8, 8, 8, 3)
+        assert p["path"] != sg.PATH_NONE
+
+
+def test_empty_and_degenerate_plans():
+    A = rowmajor(BASE, 8, 8, 1)
+    B = rowmajor(BASE + (1 << 32), 8, 8, 1)
+    C = rowmajor(BASE + (2 << 32), 8, 8, 1)
+    for M, N, batch in ((0, 8, 1), (8, 0, 1), (8, 8, 0)):
+        assert call_plan(A, B, C, M, N, 8, batch)["path"] == sg.PATH_NONE
+    # Null pointers are fine when there is nothing to do.
+    assert call_plan((0, 0, 0, 0), (0, 0, 0, 0), (0, 0, 0, 0), 0, 0, 0, 0)["path"] == sg.PATH_NONE
+    # K == 0: overwrite still writes zeros (a launch); accumulate leaves C alone.
+    assert call_plan((0, 0, 0, 0), (0, 0, 0, 0), C, 8, 8, 0, 1)["path"] != sg.PATH_NONE
+    assert call_plan((0, 0, 0, 0), (0, 0, 0, 0), C, 8, 8, 0, 1, accumulate=1)["path"] == sg.PATH_NONE
+
+
+def test_plan_tiles_and_ctas():
+    M, N, K = 8192, 2560, 960
+    p = call_plan(rowmajor(BASE, M, K, 1), (BASE + (1 << 32), 1, K, 0),
+                  rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1)
+    assert p["tiles"] == -(-M // p["tile_m"]) * -(-N // p["tile_n"])
+    assert p["ctas"] >= 1
+    # Batch over the 65535 grid limit still plans (the kernel loops over batch).
+    p = call_plan((BASE, 1, 1, 1), (BASE + (1 << 32), 1, 1, 1), (BASE + (2 << 32), 1, 1, 1),
+                  1, 1, 1, 70000)
+    assert p["tiles"] == 70000

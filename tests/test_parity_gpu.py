@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path against the CPU oracle, element by element.
+
+Tolerances follow the strided-batched problem statement: every element within
+1e-5 * (|alpha| sum_k |a||b| + |C0|) on the fp32 path and 2e-3 times that bound
+on the tf32 path; integer-valued inputs must match bit for bit.
+"""
+
+import numpy as np
+import pytest
+
+import strided_gemm_gb300 as sg
+import workloads as wl
+from strided_gemm_gb300 import build as sgbuild
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+FFMA_PATHS = [sg.PATH_AUTO, sg.PATH_GATHER_FFMA]
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    assert t.cuda.is_available(), "GPU tests need a CUDA device"
+    sgbuild.build()
+    sg.load()
+    return t
+
+
+def _supported(case, math, path):
+    try:
+        sg.sbgemm_plan(0x10000, case.A.rs, case.A.cs, case.A.bs,
+                       0x20000, case.B.rs, case.B.cs, case.B.bs,
+                       0x1000000000, case.C.rs, case.C.cs, case.C.bs,
+                       case.M, case.N, case.K, case.batch, case.accumulate,
+                       math=math, force_path=path)
+        return True
+    except sg.SbgemmError as e:
+        assert e.status == sg.SBGEMM_ERR_UNSUPPORTED
+        return False
+
+
+@pytest.mark.parametrize("name", wl.WORKLOADS)
+@pytest.mark.parametrize("values", ["real", "int"])
+@pytest.mark.parametrize("path", FFMA_PATHS)
+def test_workloads_small(torch, name, values, path):
+    case = wl.make(name, values, **wl.small_shape(name))
+    got = gu.run_case(case, torch, force_path=path)
+    gu.check_full(case, got, exact=(values == "int"))
+
+
+AWKWARD = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (4, 4, 4), (5, 9, 3), (8, 7, 16),
+           (33, 65, 20), (64, 64, 1), (1, 1, 64), (130, 70, 257), (257, 129, 131)]
+LAYOUT_PAIRS = [("row", "row"), ("row", "col"), ("col", "row"), ("col", "col"),
+                ("neg_row", "gap"), ("gap", "bcast_row"), ("bcast_row", "neg_row")]
+
+
+@pytest.mark.parametrize("mkn", AWKWARD, ids=[f"{m}x{k}x{n}" for m, k, n in AWKWARD])
+@pytest.mark.parametrize("layouts", LAYOUT_PAIRS, ids=["-".join(l) for l in LAYOUT_PAIRS])
+def test_awkward_shapes_all_layouts(torch, mkn, layouts):
+    M, K, N = mkn
+    rng = np.random.default_rng(M * 1000 + K * 10 + N)
+    for i, (bsm, c_layout, acc, alpha) in enumerate([
+            (("dense", "dense"), "row", 0, 1.0),
+            (("zero", "neg"), "col", 1, -0.5),
+            (("neg", "zero"), "row", 1, 0.125)]):
+        batch = [1, 3, 2][i]
+        for values in ("int", "real"):
+            case = wl.random_strided(rng, M, N, K, batch, layouts[0], layouts[1],
+                                     c_layout=c_layout, bs_mode=bsm, values=values,
+                                     accumulate=acc, alpha=alpha)
+            for path in FFMA_PATHS:
+                if not _supported(case, sg.MATH_FP32, path):
+                    continue
+                got = gu.run_case(case, torch, force_path=path)
+                gu.check_full(case, got, exact=(values == "int"))
+
+
+@pytest.mark.parametrize("name", wl.WORKLOADS)
+def test_workloads_full_size_sampled(torch, name):
+    """Full-size inputs through the default entry point (the call the benchmark
+    times), checked at sampled outputs including every corner."""
+    case = wl.make(name, "real")
+    got = gu.run_case(case, torch, entry="sbgemm")
+    gu.check_points(case, got)
+    case_i = wl.make(name, "int")
+    got = gu.run_case(case_i, torch, entry="sbgemm")
+    gu.check_points(case_i, got, exact=True)
+
+
+def test_overwrite_never_reads_c(torch):
+    case = wl.make("c2a", "real")
+    nan_c = np.full_like(case.C.storage, np.nan)
+    got = gu.run_case(case, torch, c_init=nan_c)
+    assert not np.isnan(gu.logical_c(case, got)).any()
+    gu.check_full(case, got)
+
+
+def test_k_zero(torch):
+    rng = np.random.default_rng(11)
+    case = wl.random_strided(rng, 37, 21, 0, 2, "row", "row", values="real", accumulate=0,
+                             alpha=3.0)
+    case.C.storage[:] = 7.0
+    got = gu.run_case(case, torch)
+    assert np.all(gu.logical_c(case, got) == 0.0)
+    case.accumulate = 1
+    got = gu.run_case(case, torch)
+    assert np.all(gu.logical_c(case, got) == 7.0)
+
+
+def test_batch_beyond_grid_limit(torch):
+    rng = np.random.default_rng(12)
+    case = wl.random_strided(rng, 2, 3, 4, 70000, "row", "col", values="int",
+                             accumulate=1, alpha=1.0)
+    got = gu.run_case(case, torch)
+    gu.check_full(case, got, exact=True)
+
+
+def test_swapped_strides_bitwise_equal_to_transposed_copy(torch):
+    rng = np.random.default_rng(13)
+    M, K, N = 300, 517, 260
+    a_km = rng.standard_normal((K, M)).astype(np.float32)
+    b_nk = rng.standard_normal((N, K)).astype(np.float32)
+    c = np.zeros(M * N, np.float32)
+    swapped = wl.Case("swapped", wl.Operand(a_km.reshape(-1), 0, 1, M, 0),
+                      wl.Operand(b_nk.reshape(-1), 0, 1, K, 0),
+                      wl.Operand(c.copy(), 0, N, 1, 0), M, N, K, 1, 1.0, 0, "real")
+    copied = wl.Case("copied", wl.Operand(np.ascontiguousarray(a_km.T).reshape(-1), 0, K, 1, 0),
+                     wl.Operand(np.ascontiguousarray(b_nk.T).reshape(-1), 0, N, 1, 0),
+                     wl.Operand(c.copy(), 0, N, 1, 0), M, N, K, 1, 1.0, 0, "real")
+    for path in FFMA_PATHS:
+        g1 = gu.run_case(swapped, torch, force_path=path)
+        g2 = gu.run_case(copied, torch, force_path=path)
+        assert np.array_equal(g1, g2)
+    gu.check_full(swapped, g1)
+
+
+def test_alpha_power_of_two_and_batch_permutation_bitwise(torch):
+    case = wl.make("c3", "real", batch=4, M=200, N=130, K=64)
+    base = gu.logical_c(case, gu.run_case(case, torch))
+    case.alpha = 0.5
+    half = gu.logical_c(case, gu.run_case(case, torch))
+    assert np.array_equal(half, base * 4)     # alpha 1/8 -> 1/2 is a factor 4
+    perm = [3, 1, 0, 2]
+    a = case.A.storage.reshape(4, -1)[perm].reshape(-1).copy()
+    b = case.B.storage.reshape(4, -1)[perm].reshape(-1).copy()
+    case.A.storage, case.B.storage = a, b
+    case.alpha = 0.125
+    permuted = gu.logical_c(case, gu.run_case(case, torch))
+    assert np.array_equal(permuted, base[perm])
+
+
+def test_identity_reproduces_operand_bitwise(torch):
+    rng = np.random.default_rng(14)
+    M = K = 150
+    N = 333
+    eye = np.eye(M, dtype=np.float32).reshape(-1)
+    b = rng.standard_normal(K * N).astype(np.float32)
+    case = wl.Case("eye", wl.Operand(eye, 0, K, 1, 0), wl.Operand(b, 0, N, 1, 0),
+                   wl.Operand(np.zeros(M * N, np.float32), 0, N, 1, 0), M, N, K, 1, 1.0, 0, "real")
+    got = gu.logical_c(case, gu.run_case(case, torch))
+    assert np.array_equal(got[0], b.reshape(K, N))
+
+
+def test_errors_surface_as_status(torch):
+    x = torch.zeros(64, device="cuda")
+    # C overlapping A.
+    with pytest.raises(sg.SbgemmError) as e:
+        sg.sbgemm(x.data_ptr(), 4, 1, 0, x.data_ptr(), 4, 1, 0, x.data_ptr() + 4 * 8, 4, 1, 0,
+                  4, 4, 4, 1, 1.0, 0)
+    assert e.value.status == sg.SBGEMM_ERR_OUTPUT_OVERLAP
+    # Span leaving the allocation: a 16-float tensor sits in a small-block
+    # segment of a few MB; rows 64 M floats apart leave any such segment.
+    # The rows walk away from C so that the spans do not meet (which would be
+    # reported as an overlap first).
+    y = torch.zeros(16, device="cuda")
+    z = torch.zeros(16, device="cuda")
+    rs = -(1 << 26) if z.data_ptr() > y.data_ptr() else (1 << 26)
+    with pytest.raises(sg.SbgemmError) as e:
+        sg.sbgemm(y.data_ptr(), rs, 1, 0, y.data_ptr(), 4, 1, 0, z.data_ptr(), 4, 1, 0,
+                  4, 4, 4, 1, 1.0, 0)
+    assert e.value.status == sg.SBGEMM_ERR_NOT_DEVICE_MEMORY
+    # Host memory is not accepted.
+    h = np.zeros(16, np.float32)
+    with pytest.raises(sg.SbgemmError) as e:
+        sg.sbgemm(h.ctypes.data, 4, 1, 0, y.data_ptr(), 4, 1, 0, z.data_ptr(), 4, 1, 0,
+                  4, 4, 4, 1, 1.0, 0)
+    assert e.value.status == sg.SBGEMM_ERR_NOT_DEVICE_MEMORY
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK and where == 0
+
+
+def test_torch_tensor_helper(torch):
+    g = torch.Generator(device="cpu").manual_seed(5)
+    A = torch.randn(3, 70, 90, generator=g).cuda()
+    W = torch.randn(50, 90, generator=g).cuda()
+    C = torch.empty(3, 70, 50, device="cuda")
+    sg.matmul(A, W.t().unsqueeze(0).expand(3, 90, 50), C)
+    torch.cuda.synchronize()
+    want = (A.double() @ W.t().double()).float()
+    assert torch.allclose(C, want, atol=1e-4, rtol=1e-5)
