@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "sbgemm.h"
@@ -55,9 +56,25 @@ GatherConfig gather_config(int variant);
 int gather_pick_variant(const Problem& p, int sm_count);
 cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t stream);
 
+// ---- TMA-fed FFMA path (ffma_tma.cu) -----------------------------------------
+struct TmaFfmaConfig { int bm, bn, bk, stages, threads; };
+int tma_ffma_config_count();
+TmaFfmaConfig tma_ffma_config(int variant);
+int tma_ffma_pick_variant(const Problem& p, int sm_count);
+cudaError_t launch_tma_ffma(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
+
+// Reads and clears the status words of the kernels that use bounded waits.
+// Returns the first non-zero code found (0 if none).
+unsigned int read_and_clear_wait_status_tma_ffma(cudaStream_t stream);
+
 // ---- driver entry points (driver.cpp) ---------------------------------------
 // [base, base+size) of the allocation that contains `ptr`; false if `ptr` is not
 // in a device-accessible allocation known to the driver.
 bool device_allocation_range(const void* ptr, uintptr_t* base, size_t* size);
+
+// Rank-3 fp32 tiled tensor map: dims innermost first, byte strides of dims 1
+// and 2, box extents, optional 128-byte swizzle.  Zero fill out of bounds.
+bool encode_tmap_f32_3d(CUtensorMap* map, const void* base, const uint64_t dims[3],
+                        const uint64_t strides_bytes[2], const uint32_t box[3], bool swizzle128);
 
 }  // namespace sbg

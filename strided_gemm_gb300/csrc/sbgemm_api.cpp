@@ -101,20 +101,23 @@ int classify_c(const Problem& p) {
 }
 
 // A TMA tensor map can describe the operand: a unit stride on its inner index,
-// a 16-byte aligned base, and outer / batch strides that are positive
-// multiples of 16 bytes below 2^40 (a stride over an extent of 1 is unused).
+// a 16-byte aligned base, outer / batch strides that are positive multiples of
+// 16 bytes below 2^40 laid out without overlap (outer stride >= inner extent,
+// batch stride >= one matrix), and extents that fit 32-bit tile coordinates.
+// A stride over an extent of 1 is never used and is not checked.
 bool tma_eligible(const void* base, int layout, int64_t outer_stride, int64_t outer_extent,
                   int64_t bs, int64_t batch, int64_t inner_extent) {
     if (layout == SBGEMM_LAYOUT_GENERAL) return false;
     if (!aligned(base, 16)) return false;
-    auto ok_stride = [](int64_t s, int64_t extent) {
-        if (extent <= 1) return true;
-        return s > 0 && (s * 4) % 16 == 0 && (s * 4) < ((int64_t)1 << 40);
-    };
-    if (!ok_stride(outer_stride, outer_extent)) return false;
-    if (batch > 1 && bs != 0 && !ok_stride(bs, batch)) return false;
-    if (inner_extent >= ((int64_t)1 << 32) || outer_extent >= ((int64_t)1 << 32) ||
-        batch >= ((int64_t)1 << 32)) return false;
+    const int64_t lim = (int64_t)1 << 31;
+    if (inner_extent >= lim || outer_extent >= lim || batch >= lim) return false;
+    auto ok_stride = [](int64_t s) { return s > 0 && (s * 4) % 16 == 0 && (s * 4) < ((int64_t)1 << 40); };
+    if (outer_extent > 1 && (!ok_stride(outer_stride) || outer_stride < inner_extent)) return false;
+    if (batch > 1 && bs != 0) {
+        if (!ok_stride(bs)) return false;
+        const int64_t one = outer_extent > 1 ? outer_stride * outer_extent : inner_extent;
+        if (bs < one) return false;
+    }
     return true;
 }
 
@@ -189,13 +192,28 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
                                    p.bsB, p.batch, bk ? p.K : p.N);
     }
 
+    const bool tma_ok = p.K > 0 && plan->a_tma && plan->b_tma;
     int path = o.force_path;
-    if (path == SBGEMM_PATH_TMA_FFMA || path == SBGEMM_PATH_TMA_TF32) {
-        return SBGEMM_ERR_UNSUPPORTED;   // kernels not built into this library yet
-    }
-    if (path == SBGEMM_PATH_AUTO) path = SBGEMM_PATH_GATHER_FFMA;
-
+    if (path == SBGEMM_PATH_TMA_TF32) return SBGEMM_ERR_UNSUPPORTED;   // not built yet
+    if (path == SBGEMM_PATH_TMA_FFMA && !tma_ok) return SBGEMM_ERR_UNSUPPORTED;
+    if (path == SBGEMM_PATH_AUTO) path = tma_ok ? SBGEMM_PATH_TMA_FFMA : SBGEMM_PATH_GATHER_FFMA;
     plan->path = path;
+
+    if (path == SBGEMM_PATH_TMA_FFMA) {
+        const int v = tma_ffma_pick_variant(p, sm_count);
+        const TmaFfmaConfig c = tma_ffma_config(v);
+        plan->variant = v;
+        plan->tile_m = c.bm;
+        plan->tile_n = c.bn;
+        plan->tile_k = c.bk;
+        plan->ctas_per_sm = 1;
+        plan->tiles_m = (p.M + c.bm - 1) / c.bm;
+        plan->tiles_n = (p.N + c.bn - 1) / c.bn;
+        plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
+        plan->ctas = std::min<int64_t>(plan->tiles, sm_count);
+        return SBGEMM_OK;
+    }
+
     const int v = gather_pick_variant(p, sm_count);
     const GatherConfig g = gather_config(v);
     plan->variant = v;
@@ -335,6 +353,7 @@ int sbgemm_ex(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     cudaError_t err = cudaSuccess;
     switch (plan.path) {
         case SBGEMM_PATH_GATHER_FFMA: err = launch_gather_ffma(p, plan, s); break;
+        case SBGEMM_PATH_TMA_FFMA: err = launch_tma_ffma(p, plan, props->sm_count, s); break;
         default: return SBGEMM_ERR_UNSUPPORTED;
     }
     if (err != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
@@ -352,9 +371,15 @@ int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
 
 int sbgemm_device_status(void* stream, int* where_out) {
     if (where_out) *where_out = 0;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return SBGEMM_ERR_CUDA;
+    }
+    const unsigned int code = read_and_clear_wait_status_tma_ffma(s);
+    if (code != 0) {
+        if (where_out) *where_out = (int)code;
+        return SBGEMM_ERR_DEVICE_TIMEOUT;
     }
     return SBGEMM_OK;
 }

@@ -15,7 +15,7 @@ from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
-FFMA_PATHS = [sg.PATH_AUTO, sg.PATH_GATHER_FFMA]
+FFMA_PATHS = [sg.PATH_AUTO, sg.PATH_GATHER_FFMA, sg.PATH_TMA_FFMA]
 
 
 @pytest.fixture(scope="module")
@@ -28,10 +28,12 @@ def torch():
 
 
 def _supported(case, math, path):
+    """Whether a forced path can serve the case (device allocations are at
+    least 256-byte aligned, so only the element offsets matter)."""
     try:
-        sg.sbgemm_plan(0x10000, case.A.rs, case.A.cs, case.A.bs,
-                       0x20000, case.B.rs, case.B.cs, case.B.bs,
-                       0x1000000000, case.C.rs, case.C.cs, case.C.bs,
+        sg.sbgemm_plan(0x10000000 + 4 * case.A.offset, case.A.rs, case.A.cs, case.A.bs,
+                       0x20000000 + 4 * case.B.offset, case.B.rs, case.B.cs, case.B.bs,
+                       0x1000000000 + 4 * case.C.offset, case.C.rs, case.C.cs, case.C.bs,
                        case.M, case.N, case.K, case.batch, case.accumulate,
                        math=math, force_path=path)
         return True
@@ -45,6 +47,7 @@ def _supported(case, math, path):
 @pytest.mark.parametrize("path", FFMA_PATHS)
 def test_workloads_small(torch, name, values, path):
     case = wl.make(name, values, **wl.small_shape(name))
+    assert _supported(case, sg.MATH_FP32, path), "every workload is TMA-eligible"
     got = gu.run_case(case, torch, force_path=path)
     gu.check_full(case, got, exact=(values == "int"))
 
@@ -52,7 +55,8 @@ def test_workloads_small(torch, name, values, path):
 AWKWARD = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (4, 4, 4), (5, 9, 3), (8, 7, 16),
            (33, 65, 20), (64, 64, 1), (1, 1, 64), (130, 70, 257), (257, 129, 131)]
 LAYOUT_PAIRS = [("row", "row"), ("row", "col"), ("col", "row"), ("col", "col"),
-                ("neg_row", "gap"), ("gap", "bcast_row"), ("bcast_row", "neg_row")]
+                ("neg_row", "gap"), ("gap", "bcast_row"), ("bcast_row", "neg_row"),
+                ("row16", "row16"), ("row16", "col16"), ("col16", "row16"), ("col16", "col16")]
 
 
 @pytest.mark.parametrize("mkn", AWKWARD, ids=[f"{m}x{k}x{n}" for m, k, n in AWKWARD])
@@ -118,7 +122,7 @@ def test_batch_beyond_grid_limit(torch):
 
 def test_swapped_strides_bitwise_equal_to_transposed_copy(torch):
     rng = np.random.default_rng(13)
-    M, K, N = 300, 517, 260
+    M, K, N = 300, 516, 260     # pitches that are 16-byte multiples: every path applies
     a_km = rng.standard_normal((K, M)).astype(np.float32)
     b_nk = rng.standard_normal((N, K)).astype(np.float32)
     c = np.zeros(M * N, np.float32)
@@ -129,6 +133,7 @@ def test_swapped_strides_bitwise_equal_to_transposed_copy(torch):
                      wl.Operand(np.ascontiguousarray(b_nk.T).reshape(-1), 0, N, 1, 0),
                      wl.Operand(c.copy(), 0, N, 1, 0), M, N, K, 1, 1.0, 0, "real")
     for path in FFMA_PATHS:
+        assert _supported(swapped, sg.MATH_FP32, path) and _supported(copied, sg.MATH_FP32, path)
         g1 = gu.run_case(swapped, torch, force_path=path)
         g2 = gu.run_case(copied, torch, force_path=path)
         assert np.array_equal(g1, g2)

@@ -279,8 +279,8 @@ def small_shape(name: str) -> Dict[str, int]:
         "c4": dict(batch=3, M=512, N=64, K=512),
         "c5a": dict(batch=1, M=300, N=2560, K=960),
         "c5b": dict(batch=1, M=300, N=960, K=2560),
-        "c5c": dict(batch=1, M=260, N=1030, K=1024),
-        "c5d": dict(batch=1, M=260, N=1030, K=1024),
+        "c5c": dict(batch=1, M=260, N=1028, K=1024),
+        "c5d": dict(batch=1, M=260, N=1028, K=1024),
     }[name]
 
 
@@ -294,15 +294,25 @@ def random_strided(rng: np.random.Generator, M: int, N: int, K: int, batch: int,
     Layouts: "row" (unit column stride), "col" (unit row stride), "neg_row"
     (row-major but rows walked backwards: negative row stride), "gap" (row-major
     with a padded row pitch), "bcast_row" (row stride 0: every row is the same
-    memory). ``bs_mode`` per A/B: "dense", "zero" (batch stride 0, one shared
-    matrix), "neg" (batches walked backwards).
+    memory), "row16" / "col16" (row- / column-major with the pitch rounded up
+    to a multiple of 4 elements, i.e. 16 bytes). ``bs_mode`` per A/B: "dense",
+    "zero" (batch stride 0, one shared matrix), "neg" (batches walked
+    backwards).
     """
+    def up4(x):
+        return (x + 3) // 4 * 4
+
     def lay(rows, cols, layout, bsm):
-        if layout in ("row", "neg_row", "gap"):
-            rs, cs = (cols + (3 if layout == "gap" else 0) + pad), 1
+        if layout in ("row", "neg_row", "gap", "row16"):
+            rs = cols + (3 if layout == "gap" else 0) + pad
+            if layout == "row16":
+                rs = up4(rs)
+            cs = 1
             span = rows * rs
-        elif layout == "col":
+        elif layout in ("col", "col16"):
             rs, cs = 1, rows + pad
+            if layout == "col16":
+                cs = up4(cs)
             span = cols * cs
         elif layout == "bcast_row":
             rs, cs = 0, 1
