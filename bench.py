@@ -265,13 +265,20 @@ def run_ours(args, world, rank, local, dist):
         dC = torch.from_numpy(c.C.storage).to(dev)
         dev_bufs.append((dA, dB, dC))
     calls = [case_args(c, *b) for c, b in zip(cases, dev_bufs)]
-    plans = [sg.sbgemm_plan(*a[:16], c.accumulate, math=math) for c, a in zip(cases, calls)]
+    # Caller-owned scratch that lets the planner split the last waves along K.
+    ws = None
+    ws_kw = {}
+    if not args.no_workspace:
+        ws = torch.empty(sg.sbgemm_workspace_bytes(local), dtype=torch.uint8, device=dev)
+        ws_kw = dict(workspace=ws.data_ptr(), workspace_bytes=ws.numel())
+    plans = [sg.sbgemm_plan(*a[:16], c.accumulate, math=math, **ws_kw)
+             for c, a in zip(cases, calls)]
     flops_step = sum(c.flops for c in cases)
     bytes_step = sum(wl.alg_bytes(c) for c in cases)
     ws_bytes = sum(c.A.storage.nbytes + c.B.storage.nbytes + c.C.storage.nbytes for c in cases)
 
     def launch(i):
-        sg.sbgemm_ex(*calls[i], s_handle, math=math)
+        sg.sbgemm_ex(*calls[i], s_handle, math=math, **ws_kw)
 
     def step():
         for i in range(len(calls)):
@@ -314,7 +321,7 @@ def run_ours(args, world, rank, local, dist):
         avg = sum(ms) / len(ms)
         per[n] = {"ms": round(avg, 4), "gflops": round(c.flops / (avg * 1e-3) / 1e9, 1),
                   "path": plans[i]["path_name"], "tile": [plans[i]["tile_m"], plans[i]["tile_n"]],
-                  "total_ms": sum(ms)}
+                  "stream_k": bool(plans[i]["stream_k"]), "total_ms": sum(ms)}
 
     # Dominant kernel: the launch (product) with the largest total time.
     dom = max(per, key=lambda n: per[n]["total_ms"])
@@ -407,7 +414,8 @@ def run_ours(args, world, rank, local, dist):
                    "alg_mb_per_step": round(bytes_step / 2**20, 1),
                    "l2": f"inputs larger than L2: {wsmb:.0f} MiB resident per step vs "
                          f"{L2_BYTES / 2**20:.0f} MiB L2, no flush",
-                   "parallelism": f"replicas x{world} (each GPU runs the whole step)"},
+                   "parallelism": f"replicas x{world} (each GPU runs the whole step)",
+                   "workspace_mib": round(ws.numel() / 2**20, 1) if ws is not None else 0},
         "pct_of_peak": round(100 * value / world / 1e3 / roof["peak"], 2)
         if roof["unit"] == "TFLOP/s" else None,
         "roofline": roof,
@@ -464,6 +472,8 @@ def main(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=0.5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="call without scratch (data-parallel schedule only)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
     world, rank, local = dist_env()

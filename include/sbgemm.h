@@ -52,6 +52,7 @@
 #ifndef SBGEMM_H
 #define SBGEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -111,7 +112,14 @@ enum {
 typedef struct {
     int math;          /* SBGEMM_MATH_* */
     int force_path;    /* SBGEMM_PATH_AUTO or a specific path */
-    int reserved[6];   /* must be zero */
+    void* workspace;   /* optional device scratch owned by the caller, 256-byte
+                          aligned, at least sbgemm_workspace_bytes() long; NULL
+                          = none.  With it the planner may split the last waves
+                          of tiles along K across all SMs (stream-K).  The
+                          library writes it on `stream` during the call; calls
+                          that may run concurrently need separate workspaces. */
+    size_t workspace_bytes;
+    int reserved[2];   /* must be zero */
 } sbgemm_options;
 
 typedef struct {
@@ -123,7 +131,12 @@ typedef struct {
     int ctas_per_sm;          /* resident CTAs per SM the plan assumes */
     int64_t ctas;             /* CTAs launched (0 when path == NONE) */
     int64_t tiles;            /* output tiles over all batch entries */
-    int reserved[8];
+    int stream_k;             /* 1: the last waves are split along K (needs a
+                                 workspace); each split tile continues one
+                                 k-ordered FMA chain, so results do not change */
+    int k_slices;             /* K slices (tile_k deep) per tile */
+    int64_t dp_tiles;         /* tiles computed whole, data-parallel */
+    int reserved[4];
 } sbgemm_plan_info;
 
 /* Strict fp32 product on the CUDA cores; the planner picks the kernel.
@@ -154,6 +167,12 @@ SBGEMM_API int sbgemm_plan(const float* A, int64_t rsA, int64_t csA, int64_t bsA
                 int64_t M, int64_t N, int64_t K, int64_t batch,
                 int accumulate, const sbgemm_options* opt,
                 sbgemm_plan_info* info);
+
+/* Workspace size that lets sbgemm_ex use the stream-K schedule on `device`
+ * (one fp32 tile of partial sums per SM plus one flag word per SM).  Returns
+ * SBGEMM_OK and writes *bytes, or SBGEMM_ERR_CUDA if the device cannot be
+ * queried. */
+SBGEMM_API int sbgemm_workspace_bytes(int device, size_t* bytes);
 
 /* Reads and clears the device-side status word that bounded in-kernel waits
  * set when they give up (after synchronising `stream`).  Returns SBGEMM_OK or

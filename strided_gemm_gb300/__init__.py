@@ -16,7 +16,7 @@ import os
 import threading
 
 __all__ = [
-    "SbgemmError", "load", "sbgemm", "sbgemm_ex", "sbgemm_plan",
+    "SbgemmError", "load", "sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_workspace_bytes",
     "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version", "matmul",
     "SBGEMM_OK", "SBGEMM_ERR_INVALID_VALUE", "SBGEMM_ERR_NULL_POINTER",
     "SBGEMM_ERR_OUTPUT_OVERLAP", "SBGEMM_ERR_UNSUPPORTED", "SBGEMM_ERR_CUDA",
@@ -45,8 +45,8 @@ PATH_NAMES = {PATH_NONE: "none", PATH_GATHER_FFMA: "gather_ffma",
               PATH_TMA_FFMA: "tma_ffma", PATH_TMA_TF32: "tma_tf32"}
 
 # Every function include/sbgemm.h declares.
-EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_device_status",
-                    "sbgemm_status_string", "sbgemm_version")
+EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_workspace_bytes",
+                    "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version")
 
 
 class SbgemmError(RuntimeError):
@@ -57,7 +57,8 @@ class SbgemmError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("math", ctypes.c_int), ("force_path", ctypes.c_int),
-                ("reserved", ctypes.c_int * 6)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("reserved", ctypes.c_int * 2)]
 
 
 class _PlanInfo(ctypes.Structure):
@@ -68,7 +69,8 @@ class _PlanInfo(ctypes.Structure):
                 ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("tile_k", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
-                ("reserved", ctypes.c_int * 8)]
+                ("stream_k", ctypes.c_int), ("k_slices", ctypes.c_int),
+                ("dp_tiles", ctypes.c_int64), ("reserved", ctypes.c_int * 4)]
 
 
 _lock = threading.Lock()
@@ -98,6 +100,8 @@ def load(path: str = LIB_PATH):
         lib.sbgemm_plan.restype = ctypes.c_int
         lib.sbgemm_plan.argtypes = _ARGS + [ctypes.c_int, ctypes.POINTER(_Options),
                                             ctypes.POINTER(_PlanInfo)]
+        lib.sbgemm_workspace_bytes.restype = ctypes.c_int
+        lib.sbgemm_workspace_bytes.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
         lib.sbgemm_device_status.restype = ctypes.c_int
         lib.sbgemm_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
         lib.sbgemm_status_string.restype = ctypes.c_char_p
@@ -108,11 +112,22 @@ def load(path: str = LIB_PATH):
         return lib
 
 
-def _opts(math: int, force_path: int):
+def _opts(math: int, force_path: int, workspace=0, workspace_bytes=0):
     o = _Options()
     o.math = int(math)
     o.force_path = int(force_path)
+    o.workspace = int(workspace) or None
+    o.workspace_bytes = int(workspace_bytes)
     return o
+
+
+def sbgemm_workspace_bytes(device: int = 0) -> int:
+    """Bytes of caller-owned workspace that enable the stream-K schedule."""
+    n = ctypes.c_size_t(0)
+    st = load().sbgemm_workspace_bytes(int(device), ctypes.byref(n))
+    if st:
+        raise SbgemmError(st, "sbgemm_workspace_bytes")
+    return n.value
 
 
 def sbgemm_status_string(status: int) -> str:
@@ -133,8 +148,9 @@ def sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
 
 def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
               M, N, K, batch, alpha, accumulate, stream=0,
-              math: int = MATH_FP32, force_path: int = PATH_AUTO) -> None:
-    o = _opts(math, force_path)
+              math: int = MATH_FP32, force_path: int = PATH_AUTO,
+              workspace: int = 0, workspace_bytes: int = 0) -> None:
+    o = _opts(math, force_path, workspace, workspace_bytes)
     st = load().sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                           M, N, K, batch, float(alpha), int(bool(accumulate)),
                           stream or None, ctypes.byref(o))
@@ -144,9 +160,10 @@ def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
 
 def sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                 M, N, K, batch, accumulate=0, math: int = MATH_FP32,
-                force_path: int = PATH_AUTO) -> dict:
+                force_path: int = PATH_AUTO, workspace: int = 0,
+                workspace_bytes: int = 0) -> dict:
     """Validate and plan without launching; returns the plan as a dict."""
-    o = _opts(math, force_path)
+    o = _opts(math, force_path, workspace, workspace_bytes)
     info = _PlanInfo()
     st = load().sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                             M, N, K, batch, int(bool(accumulate)), ctypes.byref(o),
@@ -175,7 +192,8 @@ def _as3(t, name):
 
 
 def matmul(A, B, C, alpha: float = 1.0, accumulate: bool = False,
-           math: int = MATH_FP32, force_path: int = PATH_AUTO, stream=None):
+           math: int = MATH_FP32, force_path: int = PATH_AUTO, stream=None,
+           workspace=None):
     """C <- alpha*A@B (+C) on torch CUDA float32 tensors viewed as [batch, M, K],
     [batch, K, N] and [batch, M, N] (2-D means batch 1).  Strides are taken from
     the tensors, so transposed or expanded views need no copy.  Returns C."""
@@ -195,8 +213,11 @@ def matmul(A, B, C, alpha: float = 1.0, accumulate: bool = False,
     bsB = B3.stride(0) if B3.shape[0] == batch else 0
     if stream is None:
         stream = torch.cuda.current_stream(C3.device).cuda_stream
+    ws, ws_bytes = 0, 0
+    if workspace is not None:
+        ws, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     sbgemm_ex(A3.data_ptr(), A3.stride(1), A3.stride(2), bsA,
               B3.data_ptr(), B3.stride(1), B3.stride(2), bsB,
               C3.data_ptr(), C3.stride(1), C3.stride(2), C3.stride(0),
-              M, N, K, batch, alpha, accumulate, stream, math, force_path)
+              M, N, K, batch, alpha, accumulate, stream, math, force_path, ws, ws_bytes)
     return C

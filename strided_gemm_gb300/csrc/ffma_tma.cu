@@ -67,6 +67,81 @@ struct Params {
     int accumulate;
     int a_bcast, b_bcast;   // batch stride 0: always batch coordinate 0
     int c_vec4;             // csC == 1 and 16-byte aligned rows: float4 epilogue
+    // Schedule: tiles [0, dp_tiles) are computed whole, tile t by CTA t % grid.
+    // The K slices of tiles [dp_tiles, tiles_total) are split evenly across
+    // the grid (stream-K) when sk_units > 0.
+    int64_t dp_tiles;
+    int64_t sk_units;       // (tiles_total - dp_tiles) * nk
+    float2* ws_partial;     // [grid][kThreads * 64] partial accumulators
+    unsigned int* ws_flag;  // [grid] partial-ready flags, zeroed before launch
+};
+
+// One unit of a CTA's work: slices [kb, ke) of one tile.  A HEAD item leaves
+// its partial sums in the workspace for the next CTA; a TAIL item starts from
+// the previous CTA's partial sums and finishes the tile.
+enum : int { kFull = 0, kHead = 1, kTail = 2 };
+struct Item { int64_t tile; int kb, ke, mode; };
+
+// The CTA's ordered work list: its data-parallel tiles, then (stream-K) the
+// head of the tile its K range ends in, the whole tiles inside the range, and
+// last the tail of the tile its range starts in.  The head is produced first
+// and the tail consumed last, so a tail's partial is normally long ready.
+struct Schedule {
+    int64_t n_dp, n_items;
+    int64_t full_first, n_full;   // stream-K whole tiles
+    int64_t head_tile, tail_tile;
+    int head_end, tail_begin;     // head: slices [0, head_end); tail: [tail_begin, nk)
+    int has_head, has_tail;
+
+    __device__ __forceinline__ void init(const Params& p) {
+        const int64_t c = blockIdx.x, G = gridDim.x;
+        n_dp = p.dp_tiles > c ? (p.dp_tiles - 1 - c) / G + 1 : 0;
+        has_head = has_tail = 0;
+        n_full = 0;
+        full_first = head_tile = tail_tile = 0;
+        head_end = tail_begin = 0;
+        if (p.sk_units > 0) {
+            const int64_t u0 = c * p.sk_units / G, u1 = (c + 1) * p.sk_units / G;
+            const int64_t t0 = u0 / p.nk, t1 = (u1 - 1) / p.nk;
+            const int s0 = (int)(u0 % p.nk), e1 = (int)((u1 - 1) % p.nk);
+            has_tail = s0 > 0;
+            has_head = e1 < p.nk - 1;
+            tail_tile = p.dp_tiles + t0;
+            tail_begin = s0;
+            head_tile = p.dp_tiles + t1;
+            head_end = e1 + 1;
+            full_first = t0 + has_tail;
+            const int64_t last = t1 - has_head;
+            n_full = last >= full_first ? last - full_first + 1 : 0;
+            full_first += p.dp_tiles;
+        }
+        n_items = n_dp + has_head + n_full + has_tail;
+    }
+
+    __device__ __forceinline__ Item item(const Params& p, int64_t w) const {
+        if (w < n_dp) return {blockIdx.x + w * (int64_t)gridDim.x, 0, p.nk, kFull};
+        w -= n_dp;
+        if (has_head) {
+            if (w == 0) return {head_tile, 0, head_end, kHead};
+            --w;
+        }
+        if (w < n_full) return {full_first + w, 0, p.nk, kFull};
+        return {tail_tile, tail_begin, p.nk, kTail};
+    }
+
+    __device__ __forceinline__ int64_t slices(const Params& p) const {
+        return (n_dp + n_full) * p.nk + (has_head ? head_end : 0) + (has_tail ? p.nk - tail_begin : 0);
+    }
+};
+
+// Copy issuer state (thread 0 only, kept in shared memory so that it costs
+// no registers in the consumers' hot loop): the next (item, slice) to load.
+struct Issuer {
+    int64_t w;          // item of the next slice to load
+    int kt;             // slice within that item's tile
+    int pad;
+    uint64_t issued;    // slices issued so far (global iteration count)
+    int64_t total;      // slices this CTA loads in all
 };
 
 template <int BM, int BN>
@@ -81,6 +156,10 @@ struct Cfg {
         float b[kStages][BN * BK];
         uint64_t full[kStages];
         uint64_t empty[kStages];
+        uint64_t stored;    // every thread has written its partial (stream-K head)
+        uint64_t ready;     // the predecessor's partial is visible (stream-K tail)
+        Schedule sched;     // the CTA's work list, computed once by thread 0
+        Issuer iss;         // copy issuer state (thread 0)
     };
     static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + alignment slack
 };
@@ -139,8 +218,12 @@ __device__ __forceinline__ void load_frag2(const float* tile, int k0, int wbase,
         for (int i = 0; i < R; ++i) {
             const char* q = ((i & 1) ? b1 : b0) + i * LANES * 128;
             if (PAIRED) {
-                f[i][0] = *reinterpret_cast<const float*>(q);
-                f[i][1] = *reinterpret_cast<const float*>(q + 4);
+                // Two 4-byte loads kept apart (the compiler would otherwise merge
+                // them into one wide load whose registers cannot form pairs
+                // across rows without moves).
+                const uint32_t a = smem_u32(q);
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f[i][0]) : "r"(a));
+                asm volatile("ld.shared.f32 %0, [%1+4];" : "=f"(f[i][1]) : "r"(a));
             } else {
                 const float2 v = *reinterpret_cast<const float2*>(q);
                 f[i][0] = v.x;
@@ -199,18 +282,14 @@ __device__ __forceinline__ void fma_step(float2 (&acc)[64], const float (&a)[TM]
 #endif
 }
 
-// Copy issuer state (thread 0 only): the next (tile, slice) to load.
-struct Issuer {
-    int64_t t;          // tile index of the next slice to load
-    int kt;             // slice within that tile
-    uint64_t issued;    // slices issued so far (global iteration count)
-};
-
 template <int BM, int BN, bool A_K, bool B_K>
 __device__ __forceinline__ void issue_next(typename Cfg<BM, BN>::Smem& sh, const CUtensorMap* ta,
-                                           const CUtensorMap* tb, const Params& p, Issuer& is) {
+                                           const CUtensorMap* tb, const Params& p,
+                                           const Schedule& sc, Issuer& is) {
     using C = Cfg<BM, BN>;
-    const TileCoord tc = tile_coord<BM, BN>(p, is.t);
+    Item itm = sc.item(p, is.w);
+    if (is.kt < itm.kb) is.kt = itm.kb;
+    const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
     const int s = (int)(is.issued % C::kStages);
     const int ba = p.a_bcast ? 0 : (int)tc.b;
     const int bb = p.b_bcast ? 0 : (int)tc.b;
@@ -221,7 +300,7 @@ __device__ __forceinline__ void issue_next(typename Cfg<BM, BN>::Smem& sh, const
     if (B_K) tma_load_3d(sh.b[s], tb, &sh.full[s], k0, (int)tc.n0, bb);
     else     tma_load_3d(sh.b[s], tb, &sh.full[s], (int)tc.n0, k0, bb);
     ++is.issued;
-    if (++is.kt == p.nk) { is.kt = 0; is.t += gridDim.x; }
+    if (++is.kt == itm.ke) { is.kt = 0; ++is.w; }
 }
 
 // On a failed wait the issuer may still have copies landing in shared memory;
@@ -235,6 +314,33 @@ __device__ __forceinline__ void drain(uint64_t* full, uint64_t consumed, uint64_
         }
 }
 
+// Slices the issuer has loaded that the consumers have not yet taken, given the
+// consumers' 32-bit running count (the issuer is never more than a few stages
+// ahead, so the low 32 bits of the difference are exact).
+__device__ __forceinline__ uint64_t in_flight(uint64_t issued, uint32_t consumed) {
+    return (uint64_t)(uint32_t)((uint32_t)issued - consumed);
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait for the predecessor CTA's partial-ready flag.
+__device__ __forceinline__ bool wait_flag(const unsigned int* f) {
+    if (ld_acquire_gpu(f) != 0u) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(f) == 0u) {
+        __nanosleep(64);
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+    return true;
+}
+
 template <int BM, int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(kThreads, 1)
 tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
@@ -245,22 +351,28 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     auto& sh = *reinterpret_cast<typename C::Smem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const bool issuer = threadIdx.x == 0;
-    Issuer is{blockIdx.x, 0, 0};
+    const Schedule& sc = sh.sched;
+    Issuer& is = sh.iss;
     if (issuer) {
+        sh.sched.init(p);
+        is.w = 0;
+        is.kt = 0;
+        is.issued = 0;
+        is.total = sh.sched.slices(p);
         for (int s = 0; s < S; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], kWarps);
         }
+        mbar_init(&sh.stored, kThreads);
+        mbar_init(&sh.ready, 1);
         fence_mbar_init();
         prefetch_tensormap(&ta);
         prefetch_tensormap(&tb);
     }
     __syncthreads();
-    const int64_t my_slices = (p.tiles_total > (int64_t)blockIdx.x)
-        ? ((p.tiles_total - 1 - blockIdx.x) / gridDim.x + 1) * p.nk : 0;
     if (issuer) {
-        for (int q = 0; q < S - 1 && (int64_t)is.issued < my_slices; ++q)
-            issue_next<BM, BN, A_K, B_K>(sh, &ta, &tb, p, is);
+        for (int q = 0; q < S - 1 && (int64_t)is.issued < is.total; ++q)
+            issue_next<BM, BN, A_K, B_K>(sh, &ta, &tb, p, sc, is);
     }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -269,30 +381,57 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     // Pair along the dimension whose operand arrives with adjacent values:
     // rows when A is MN-major, otherwise columns.
     constexpr bool PI = !A_K;
-    uint64_t it = 0;
-    for (int64_t t = blockIdx.x; t < p.tiles_total; t += gridDim.x) {
-        const TileCoord tc = tile_coord<BM, BN>(p, t);
+    uint32_t it = 0;        // slices consumed so far (low 32 bits)
+    int stage = 0;          // it % S, kept incrementally
+    uint32_t phase = 0;     // (it / S) & 1
+    const int64_t n_items = sc.n_items;
+    for (int64_t w = 0; w < n_items; ++w) {
         float2 acc[64];
+        if (sc.item(p, w).mode == kTail) {
+            // Continue the predecessor's FMA chains from its partial sums.
+            const float2* src = p.ws_partial + (int64_t)(blockIdx.x - 1) * (kThreads * 64);
+            if (issuer) {
+                if (!wait_flag(p.ws_flag + (blockIdx.x - 1))) {
+                    record_status(&g_wait_status, kWaitPartial);
+                    drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
+                    return;
+                }
+                mbar_arrive(&sh.ready);
+            }
+            if (!mbar_wait(&sh.ready, 0)) {
+                record_status(&g_wait_status, kWaitPartial);
+                return;
+            }
 #pragma unroll
-        for (int q = 0; q < 64; ++q) acc[q] = make_float2(0.0f, 0.0f);
+            for (int q = 0; q < 64; ++q) acc[q] = __ldcg(src + q * kThreads + threadIdx.x);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 64; ++q) acc[q] = make_float2(0.0f, 0.0f);
+        }
 
-        for (int kt = 0; kt < p.nk; ++kt, ++it) {
-            if (issuer && (int64_t)is.issued < my_slices) {
+        int kt_end;
+        {
+            const Item itm = sc.item(p, w);
+            kt_end = itm.ke - itm.kb;
+        }
+        for (int kt = 0; kt < kt_end; ++kt, ++it) {
+            if (issuer && (int64_t)is.issued < is.total) {
                 // Refill the stage every warp released at slice it-1.
                 if (is.issued >= (uint64_t)S &&
                     !mbar_wait(&sh.empty[is.issued % S], (uint32_t)(((is.issued / S) - 1) & 1))) {
                     record_status(&g_wait_status, kWaitEmpty);
-                    drain<S>(sh.full, it, is.issued);
+                    drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
                     return;
                 }
-                issue_next<BM, BN, A_K, B_K>(sh, &ta, &tb, p, is);
+                issue_next<BM, BN, A_K, B_K>(sh, &ta, &tb, p, sc, is);
             }
-            const int s = (int)(it % S);
-            if (!mbar_wait(&sh.full[s], (uint32_t)((it / S) & 1))) {
+            const int s = stage;
+            if (!mbar_wait(&sh.full[s], phase)) {
                 record_status(&g_wait_status, kWaitFull);
-                if (issuer) drain<S>(sh.full, it, is.issued);
+                if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
                 return;
             }
+            if (++stage == S) { stage = 0; phase ^= 1u; }
             const float* As = sh.a[s];
             const float* Bs = sh.b[s];
             // Unrolling deeper lets ptxas hoist fragment loads until the 128
@@ -318,7 +457,28 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             if (lane == 0) mbar_arrive(&sh.empty[s]);
         }
 
+        const Item itm = sc.item(p, w);
+        if (itm.mode == kHead) {
+            // Leave the partial sums for the next CTA, then raise its flag once
+            // every thread's stores are visible device-wide.
+            float2* dst = p.ws_partial + (int64_t)blockIdx.x * (kThreads * 64);
+#pragma unroll
+            for (int q = 0; q < 64; ++q) __stcg(dst + q * kThreads + threadIdx.x, acc[q]);
+            __threadfence();
+            mbar_arrive(&sh.stored);
+            if (issuer) {
+                if (!mbar_wait(&sh.stored, 0)) {
+                    record_status(&g_wait_status, kWaitPartial);
+                    drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
+                    return;
+                }
+                st_release_gpu(p.ws_flag + blockIdx.x, 1u);
+            }
+            continue;
+        }
+
         // Epilogue straight from registers.
+        const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
         float* Cb = p.C + tc.b * p.bsC;
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
@@ -423,7 +583,33 @@ cudaError_t launch_impl(const Problem& pr, const Plan& plan, int sm_count, cudaS
     p.b_bcast = b_bc;
     p.c_vec4 = pr.csC == 1 && (reinterpret_cast<uintptr_t>(pr.C) % 16 == 0) &&
                (pr.M == 1 || pr.rsC % 4 == 0) && (pr.batch == 1 || pr.bsC % 4 == 0);
-    const int64_t grid = plan.tiles < (int64_t)sm_count ? plan.tiles : (int64_t)sm_count;
+    const int64_t grid = plan.ctas;
+    p.dp_tiles = plan.stream_k ? plan.dp_tiles : plan.tiles;
+    p.sk_units = plan.stream_k ? (plan.tiles - plan.dp_tiles) * p.nk : 0;
+    p.ws_partial = nullptr;
+    p.ws_flag = nullptr;
+    if (plan.stream_k) {
+        // Partials first, then one flag word per CTA (see workspace_bytes).
+        p.ws_partial = static_cast<float2*>(plan.workspace);
+        p.ws_flag = reinterpret_cast<unsigned int*>(
+            static_cast<char*>(plan.workspace) + (size_t)grid * kThreads * 64 * sizeof(float2));
+        cudaError_t e = cudaMemsetAsync(p.ws_flag, 0, (size_t)grid * sizeof(unsigned int), stream);
+        if (e != cudaSuccess) return e;
+        // CTAs wait on one another's partial sums: make them co-resident.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tma_ffma_kernel<BM, BN, A_K, B_K>, ta, tb, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     tma_ffma_kernel<BM, BN, A_K, B_K><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(ta, tb, p);
     return cudaGetLastError();
 }
@@ -463,6 +649,41 @@ int tma_ffma_pick_variant(const Problem& p, int sm_count) {
         if (v == 0 || cost < best_cost) { best = v; best_cost = cost; }
     }
     return best;
+}
+
+size_t tma_ffma_workspace_bytes(int sm_count) {
+    // One partial tile per CTA (every thread's 64 accumulator pairs) and one
+    // flag word per CTA; the same for every tile shape (256 threads x 128).
+    return (size_t)sm_count * kThreads * 64 * sizeof(float2) + (size_t)sm_count * sizeof(unsigned int);
+}
+
+// Data-parallel for all but the last one or two waves, whose K slices are
+// split evenly over the grid.  Chosen only when it removes at least 3% of the
+// estimated time, every CTA's share spans at least one whole tile (so a tile
+// is split at most once), and a tile has enough slices to amortise the
+// exchange of its partial sums.
+void tma_ffma_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_bytes,
+                       const void* ws) {
+    const TmaFfmaConfig c = kConfigs[plan.variant];
+    const int64_t nk = (pr.K + c.bk - 1) / c.bk;
+    const int64_t G = sm_count;
+    plan.k_slices = (int)nk;
+    plan.stream_k = false;
+    plan.dp_tiles = plan.tiles;
+    plan.ctas = plan.tiles < G ? plan.tiles : G;
+    if (!ws || ws_bytes < tma_ffma_workspace_bytes(sm_count)) return;
+    if ((reinterpret_cast<uintptr_t>(ws) % 256) != 0) return;
+    if (plan.tiles < G || nk < 8) return;
+    const int64_t full_waves = plan.tiles / G - 1;
+    const int64_t dp = full_waves * G;
+    const int64_t rem_units = (plan.tiles - dp) * nk;
+    const double t_dp = (double)((plan.tiles + G - 1) / G) * nk;
+    const double t_sk = (double)full_waves * nk + (double)((rem_units + G - 1) / G) + 1.0;
+    if (t_sk > 0.97 * t_dp) return;
+    plan.stream_k = true;
+    plan.dp_tiles = dp;
+    plan.ctas = G;
+    plan.workspace = const_cast<void*>(ws);
 }
 
 cudaError_t launch_tma_ffma(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream) {

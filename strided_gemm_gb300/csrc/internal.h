@@ -45,6 +45,10 @@ struct Plan {
     int64_t tiles_m = 0, tiles_n = 0;
     int64_t tiles = 0;              // tiles_m * tiles_n * batch
     int64_t ctas = 0;
+    int k_slices = 0;               // K slices per tile
+    bool stream_k = false;          // last waves split along K (needs workspace)
+    int64_t dp_tiles = 0;           // tiles computed whole
+    void* workspace = nullptr;      // caller's scratch when stream_k
 };
 
 // ---- strided-gather FFMA path (ffma_gather.cu) --------------------------------
@@ -61,6 +65,10 @@ struct TmaFfmaConfig { int bm, bn, bk, stages, threads; };
 int tma_ffma_config_count();
 TmaFfmaConfig tma_ffma_config(int variant);
 int tma_ffma_pick_variant(const Problem& p, int sm_count);
+// Bytes of workspace the stream-K schedule needs on a device with sm_count SMs.
+size_t tma_ffma_workspace_bytes(int sm_count);
+// Fills plan.ctas / stream_k / dp_tiles / k_slices for the chosen variant.
+void tma_ffma_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws);
 cudaError_t launch_tma_ffma(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
 
 // Reads and clears the status words of the kernels that use bounded waits.

@@ -18,6 +18,7 @@ enum : unsigned int {
     kWaitDrain = 3,      // producer draining its last copies on the way out
     kWaitMma = 4,        // epilogue waiting for the accumulator
     kWaitAccFree = 5,    // MMA issuer waiting for the epilogue to free TMEM
+    kWaitPartial = 6,    // stream-K: exchanging partial sums between CTAs
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -127,6 +127,8 @@ int check_options(const sbgemm_options* opt, sbgemm_options* out) {
     if (o.math != SBGEMM_MATH_FP32 && o.math != SBGEMM_MATH_TF32) return SBGEMM_ERR_INVALID_VALUE;
     if (o.force_path < SBGEMM_PATH_AUTO || o.force_path > SBGEMM_PATH_TMA_TF32) return SBGEMM_ERR_INVALID_VALUE;
     for (int r : o.reserved) if (r != 0) return SBGEMM_ERR_INVALID_VALUE;
+    if (o.workspace && (reinterpret_cast<uintptr_t>(o.workspace) % 256) != 0)
+        return SBGEMM_ERR_INVALID_VALUE;
     *out = o;
     return SBGEMM_OK;
 }
@@ -210,7 +212,7 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
         plan->tiles_m = (p.M + c.bm - 1) / c.bm;
         plan->tiles_n = (p.N + c.bn - 1) / c.bn;
         plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
-        plan->ctas = std::min<int64_t>(plan->tiles, sm_count);
+        tma_ffma_schedule(p, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace);
         return SBGEMM_OK;
     }
 
@@ -260,6 +262,9 @@ void fill_info(const Plan& plan, sbgemm_plan_info* info) {
     info->ctas_per_sm = plan.ctas_per_sm;
     info->ctas = plan.ctas;
     info->tiles = plan.tiles;
+    info->stream_k = plan.stream_k;
+    info->k_slices = plan.k_slices;
+    info->dp_tiles = plan.dp_tiles;
 }
 
 // SM count for planning: the current device's when one is present, otherwise
@@ -349,6 +354,21 @@ int sbgemm_ex(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     st = make_plan(p, o, props->sm_count, false, &plan);
     if (st) return st;
 
+    if (plan.stream_k) {
+        // The workspace is written by the kernel: it must be device memory and
+        // must not meet any operand.
+        const Span sw{0, (int64_t)(o.workspace_bytes / 4) - 1};
+        if (!span_in_allocation(o.workspace, sw)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+        auto meets = [&](const void* base, const Span& sp) {
+            const __int128 lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)sp.lo * 4;
+            const __int128 hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)sp.hi * 4 + 4;
+            const __int128 wlo = (__int128)reinterpret_cast<uintptr_t>(o.workspace);
+            const __int128 whi = wlo + (__int128)o.workspace_bytes;
+            return lo < whi && wlo < hi;
+        };
+        if (meets(p.C, sc) || meets(p.A, sa) || meets(p.B, sb)) return SBGEMM_ERR_OUTPUT_OVERLAP;
+    }
+
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = cudaSuccess;
     switch (plan.path) {
@@ -367,6 +387,14 @@ int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
            float alpha, int accumulate, void* stream) {
     return sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                      M, N, K, batch, alpha, accumulate, stream, nullptr);
+}
+
+int sbgemm_workspace_bytes(int device, size_t* bytes) {
+    if (!bytes) return SBGEMM_ERR_NULL_POINTER;
+    const DeviceProps* d = device_props(device);
+    if (!d) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
+    *bytes = tma_ffma_workspace_bytes(d->sm_count);
+    return SBGEMM_OK;
 }
 
 int sbgemm_device_status(void* stream, int* where_out) {

@@ -165,3 +165,36 @@ def test_plan_tiles_and_ctas():
     p = call_plan((BASE, 1, 1, 1), (BASE + (1 << 32), 1, 1, 1), (BASE + (2 << 32), 1, 1, 1),
                   1, 1, 1, 70000)
     assert p["tiles"] == 70000
+
+
+def test_stream_k_planning():
+    """With a workspace the last waves of tiles are split along K; without
+    one, or for problems that fill whole waves or have few K slices, the
+    schedule stays data-parallel."""
+    ws = BASE + (8 << 32)
+    big = 1 << 30
+    M = N = K = 4096
+    A = rowmajor(BASE, M, K, 1)
+    B = rowmajor(BASE + (1 << 32), K, N, 1)
+    C = rowmajor(BASE + (2 << 32), M, N, 1)
+    p0 = call_plan(A, B, C, M, N, K, 1)
+    assert p0["path"] == sg.PATH_TMA_FFMA and not p0["stream_k"]
+    assert p0["dp_tiles"] == p0["tiles"] and p0["ctas"] == min(p0["tiles"], 152)
+    p1 = call_plan(A, B, C, M, N, K, 1, workspace=ws, workspace_bytes=big)
+    assert p1["stream_k"] and p1["ctas"] == 152
+    assert p1["dp_tiles"] % 152 == 0 and p1["tiles"] - p1["dp_tiles"] >= 152
+    assert p1["k_slices"] == 4096 // p1["tile_k"]
+    # Too small a workspace, or a misaligned one.
+    assert not call_plan(A, B, C, M, N, K, 1, workspace=ws, workspace_bytes=1024)["stream_k"]
+    with pytest.raises(sg.SbgemmError) as e:
+        call_plan(A, B, C, M, N, K, 1, workspace=ws + 16, workspace_bytes=big)
+    assert e.value.status == sg.SBGEMM_ERR_INVALID_VALUE
+    # Fewer tiles than SMs, or few K slices: nothing to gain.
+    small = call_plan(rowmajor(BASE, 512, 512, 1), rowmajor(BASE + (1 << 32), 512, 512, 1),
+                      rowmajor(BASE + (2 << 32), 512, 512, 1), 512, 512, 512, 1,
+                      workspace=ws, workspace_bytes=big)
+    assert not small["stream_k"]
+    shortk = call_plan(rowmajor(BASE, 4096, 64, 1), (BASE + (1 << 32), 1, 64, 0),
+                       rowmajor(BASE + (2 << 32), 4096, 4096, 1), 4096, 4096, 64, 1,
+                       workspace=ws, workspace_bytes=big)
+    assert not shortk["stream_k"]

@@ -204,3 +204,63 @@ def test_torch_tensor_helper(torch):
     torch.cuda.synchronize()
     want = (A.double() @ W.t().double()).float()
     assert torch.allclose(C, want, atol=1e-4, rtol=1e-5)
+
+
+STREAM_K_SHAPES = [
+    # (name, M, N, K, batch, a_layout, b_layout, accumulate)
+    ("160_tiles_all_split", 2048, 2560, 1024, 1, "row16", "col16", 0),
+    ("ragged_k", 2048, 2600, 1000, 1, "row16", "row16", 1),
+    ("batched", 1024, 1024, 768, 5, "col16", "row16", 1),
+    ("mn_major_both", 4100, 1200, 640, 1, "col16", "row16", 0),
+]
+
+
+@pytest.fixture(scope="module")
+def workspace(torch):
+    nbytes = sg.sbgemm_workspace_bytes(torch.cuda.current_device())
+    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+
+def _run_ws(case, torch, ws, entry_kw=None):
+    kw = dict(workspace=ws.data_ptr(), workspace_bytes=ws.numel()) if ws is not None else {}
+    dA, dB = gu.to_device(case.A, torch), gu.to_device(case.B, torch)
+    dC = torch.from_numpy(case.C.storage.copy()).to("cuda")
+    args = (dA.data_ptr() + 4 * case.A.offset, case.A.rs, case.A.cs, case.A.bs,
+            dB.data_ptr() + 4 * case.B.offset, case.B.rs, case.B.cs, case.B.bs,
+            dC.data_ptr() + 4 * case.C.offset, case.C.rs, case.C.cs, case.C.bs,
+            case.M, case.N, case.K, case.batch, case.alpha, case.accumulate,
+            torch.cuda.current_stream().cuda_stream)
+    plan = sg.sbgemm_plan(*args[:16], case.accumulate, **kw)
+    sg.sbgemm_ex(*args, **kw)
+    torch.cuda.synchronize()
+    return dC.cpu().numpy(), plan
+
+
+@pytest.mark.parametrize("shape", STREAM_K_SHAPES, ids=[s[0] for s in STREAM_K_SHAPES])
+def test_stream_k_bitwise_equals_data_parallel(torch, workspace, shape):
+    """Split tiles continue one k-ordered FMA chain through the workspace, so
+    the stream-K schedule reproduces the data-parallel result bit for bit."""
+    _, M, N, K, batch, la, lb, acc = shape
+    rng = np.random.default_rng(M + N + K)
+    case = wl.random_strided(rng, M, N, K, batch, la, lb, values="real", accumulate=acc,
+                             alpha=0.75)
+    dp, plan_dp = _run_ws(case, torch, None)
+    sk, plan_sk = _run_ws(case, torch, workspace)
+    assert not plan_dp["stream_k"] and plan_sk["stream_k"], (plan_dp, plan_sk)
+    assert np.array_equal(dp, sk)
+    gu.check_points(case, sk, n=4000)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
+def test_stream_k_repeated_calls_reuse_workspace(torch, workspace):
+    """The flags are cleared on the stream before every launch, so back-to-back
+    calls through one workspace stay exact (integer inputs)."""
+    rng = np.random.default_rng(3)
+    case = wl.random_strided(rng, 2048, 2560, 1024, 1, "row16", "row16", values="int")
+    first, plan = _run_ws(case, torch, workspace)
+    assert plan["stream_k"]
+    for _ in range(3):
+        again, _ = _run_ws(case, torch, workspace)
+        assert np.array_equal(again, first)
+    gu.check_full(case, first, exact=True)
