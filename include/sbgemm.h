@@ -174,6 +174,32 @@ SBGEMM_API int sbgemm_plan(const float* A, int64_t rsA, int64_t csA, int64_t bsA
  * queried. */
 SBGEMM_API int sbgemm_workspace_bytes(int device, size_t* bytes);
 
+/* The strict fp32 product for callers that cannot allocate device memory.
+ * The paper has no counterpart: it exists because the stream-K schedule needs
+ * scratch that sbgemm_ex takes from its caller, and some callers cannot make
+ * any (code running under CUDA graph capture, plugins given only their input
+ * and output buffers, loops that must not pay cudaMalloc's synchronisation,
+ * runtimes whose allocator owns all device memory).
+ *
+ * Arguments, layout and errors are those of sbgemm.  The scratch is a
+ * file-scope device array of 20 MiB + 4 KiB inside the library (room for the
+ * schedule on devices of up to 160 SMs), created when the library's module is
+ * loaded and held on every GPU that loads the library until the process
+ * exits.  Nothing is allocated per call: no cudaMalloc, cudaFree or
+ * allocating library routine runs.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call shares the one
+ * array and the schedule clears its flags on `stream` before each launch, so
+ * calls that overlap on the GPU (different streams, or different host
+ * threads) race on the scratch and must be serialised by the caller.
+ * Returns SBGEMM_ERR_UNSUPPORTED if the current device would need more
+ * scratch than the array holds (more than 160 SMs). */
+SBGEMM_API int sbgemm_noalloc(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+                              const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+                              float* C, int64_t rsC, int64_t csC, int64_t bsC,
+                              int64_t M, int64_t N, int64_t K, int64_t batch,
+                              float alpha, int accumulate, void* stream);
+
 /* Reads and clears the device-side status word that bounded in-kernel waits
  * set when they give up (after synchronising `stream`).  Returns SBGEMM_OK or
  * SBGEMM_ERR_DEVICE_TIMEOUT; *where_out (may be NULL) receives a code naming

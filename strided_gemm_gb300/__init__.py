@@ -17,6 +17,7 @@ import threading
 
 __all__ = [
     "SbgemmError", "load", "sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_workspace_bytes",
+    "sbgemm_noalloc",
     "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version", "matmul",
     "SBGEMM_OK", "SBGEMM_ERR_INVALID_VALUE", "SBGEMM_ERR_NULL_POINTER",
     "SBGEMM_ERR_OUTPUT_OVERLAP", "SBGEMM_ERR_UNSUPPORTED", "SBGEMM_ERR_CUDA",
@@ -46,7 +47,8 @@ PATH_NAMES = {PATH_NONE: "none", PATH_GATHER_FFMA: "gather_ffma",
 
 # Every function include/sbgemm.h declares.
 EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_workspace_bytes",
-                    "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version")
+                    "sbgemm_noalloc", "sbgemm_device_status", "sbgemm_status_string",
+                    "sbgemm_version")
 
 
 class SbgemmError(RuntimeError):
@@ -100,6 +102,8 @@ def load(path: str = LIB_PATH):
         lib.sbgemm_plan.restype = ctypes.c_int
         lib.sbgemm_plan.argtypes = _ARGS + [ctypes.c_int, ctypes.POINTER(_Options),
                                             ctypes.POINTER(_PlanInfo)]
+        lib.sbgemm_noalloc.restype = ctypes.c_int
+        lib.sbgemm_noalloc.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp]
         lib.sbgemm_workspace_bytes.restype = ctypes.c_int
         lib.sbgemm_workspace_bytes.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
         lib.sbgemm_device_status.restype = ctypes.c_int
@@ -144,6 +148,18 @@ def sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                        M, N, K, batch, float(alpha), int(bool(accumulate)), stream or None)
     if st:
         raise SbgemmError(st, "sbgemm")
+
+
+def sbgemm_noalloc(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                   M, N, K, batch, alpha, accumulate, stream=0) -> None:
+    """As sbgemm, for callers that cannot allocate device memory: the scratch
+    of the stream-K schedule is the library's own static device array (shared
+    by all calls, so calls that overlap on the GPU must be serialised)."""
+    st = load().sbgemm_noalloc(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                               M, N, K, batch, float(alpha), int(bool(accumulate)),
+                               stream or None)
+    if st:
+        raise SbgemmError(st, "sbgemm_noalloc")
 
 
 def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
