@@ -75,6 +75,11 @@ cudaError_t launch_tma_ffma(const Problem& p, const Plan& plan, int sm_count, cu
 // Returns the first non-zero code found (0 if none).
 unsigned int read_and_clear_wait_status_tma_ffma(cudaStream_t stream);
 
+// ---- TF32 tensor-core path (tf32_tc.cu) ----------------------------------------
+TmaFfmaConfig tf32_tc_config();
+cudaError_t launch_tf32_tc(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
+unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream);
+
 // ---- driver entry points (driver.cpp) ---------------------------------------
 // [base, base+size) of the allocation that contains `ptr`; false if `ptr` is not
 // in a device-accessible allocation known to the driver.

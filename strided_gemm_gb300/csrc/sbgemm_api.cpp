@@ -195,11 +195,32 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
     }
 
     const bool tma_ok = p.K > 0 && plan->a_tma && plan->b_tma;
+    // The tensor-core path reads both operands K-major (unit stride along K).
+    const bool tf32_ok = tma_ok && plan->a_layout == SBGEMM_LAYOUT_K_MAJOR &&
+                         plan->b_layout == SBGEMM_LAYOUT_K_MAJOR;
     int path = o.force_path;
-    if (path == SBGEMM_PATH_TMA_TF32) return SBGEMM_ERR_UNSUPPORTED;   // not built yet
+    if (path == SBGEMM_PATH_TMA_TF32 && !tf32_ok) return SBGEMM_ERR_UNSUPPORTED;
     if (path == SBGEMM_PATH_TMA_FFMA && !tma_ok) return SBGEMM_ERR_UNSUPPORTED;
-    if (path == SBGEMM_PATH_AUTO) path = tma_ok ? SBGEMM_PATH_TMA_FFMA : SBGEMM_PATH_GATHER_FFMA;
+    if (path == SBGEMM_PATH_AUTO) {
+        if (o.math == SBGEMM_MATH_TF32 && tf32_ok) path = SBGEMM_PATH_TMA_TF32;
+        else path = tma_ok ? SBGEMM_PATH_TMA_FFMA : SBGEMM_PATH_GATHER_FFMA;
+    }
     plan->path = path;
+
+    if (path == SBGEMM_PATH_TMA_TF32) {
+        const TmaFfmaConfig c = tf32_tc_config();
+        plan->tile_m = c.bm;
+        plan->tile_n = c.bn;
+        plan->tile_k = c.bk;
+        plan->ctas_per_sm = 1;
+        plan->tiles_m = (p.M + c.bm - 1) / c.bm;
+        plan->tiles_n = (p.N + c.bn - 1) / c.bn;
+        plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
+        plan->k_slices = (int)((p.K + c.bk - 1) / c.bk);
+        plan->dp_tiles = plan->tiles;
+        plan->ctas = std::min<int64_t>(plan->tiles, sm_count);
+        return SBGEMM_OK;
+    }
 
     if (path == SBGEMM_PATH_TMA_FFMA) {
         const int v = tma_ffma_pick_variant(p, sm_count);
@@ -374,6 +395,7 @@ int sbgemm_ex(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     switch (plan.path) {
         case SBGEMM_PATH_GATHER_FFMA: err = launch_gather_ffma(p, plan, s); break;
         case SBGEMM_PATH_TMA_FFMA: err = launch_tma_ffma(p, plan, props->sm_count, s); break;
+        case SBGEMM_PATH_TMA_TF32: err = launch_tf32_tc(p, plan, props->sm_count, s); break;
         default: return SBGEMM_ERR_UNSUPPORTED;
     }
     if (err != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
@@ -404,7 +426,9 @@ int sbgemm_device_status(void* stream, int* where_out) {
         cudaGetLastError();
         return SBGEMM_ERR_CUDA;
     }
-    const unsigned int code = read_and_clear_wait_status_tma_ffma(s);
+    unsigned int code = read_and_clear_wait_status_tma_ffma(s);
+    const unsigned int code_tc = read_and_clear_wait_status_tf32(s);
+    if (code == 0) code = code_tc;
     if (code != 0) {
         if (where_out) *where_out = (int)code;
         return SBGEMM_ERR_DEVICE_TIMEOUT;

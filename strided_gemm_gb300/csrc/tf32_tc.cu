@@ -1,0 +1,325 @@
+// TF32 tensor-core path (opt-in through sbgemm_options.math): tcgen05.mma
+// kind::tf32 with fp32 accumulators in tensor memory, for operands whose unit
+// stride runs along K (A row-major, B = a row-major matrix read transposed).
+//
+// Persistent, warp-specialised CTAs, one per SM, 192 threads:
+//  * warp 0, one lane: TMA producer.  Walks the CTA's tiles and their 32-deep
+//    K slices and loads a 128 x 32 box of A and a 256 x 32 box of B (128-byte
+//    swizzle) into a 4-stage shared-memory ring ("full" / "empty" mbarriers).
+//  * warp 1, one lane: MMA issuer.  Allocates 512 TMEM columns (two 128 x 256
+//    fp32 accumulators), and per slice issues four 128x256x8 MMAs whose smem
+//    descriptors advance 32 bytes along the swizzled rows; tcgen05.commit frees
+//    the stage when its MMAs are done, and marks the accumulator full after the
+//    tile's last slice.
+//  * warps 2..5: epilogue.  Each warp reads its 32 TMEM lanes (rows) in 32-
+//    column pieces (tcgen05.ld 32x32b.x32), forms alpha*acc (+ C_old) and
+//    stores with masks on ragged M / N, then releases the accumulator, so the
+//    next tile's MMAs overlap this tile's stores.
+// Every mbarrier wait is bounded; a role that gives up records a status code
+// and leaves its loop, the producer then waits (bounded) for the copies it
+// issued, the MMA issuer for its MMAs, and the allocating warp frees TMEM
+// before the CTA exits.
+//
+// TF32 reads the top 19 bits of each fp32 operand; products accumulate in fp32.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sbg {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 32;   // CTA tile; UMMA 128 x 256 x 8
+constexpr int kMmaK = 8;                     // tf32 elements per MMA
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 4;         // 16 KB
+constexpr int kBBytes = BN * BK * 4;         // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kAccCols = BN;            // fp32 accumulator: one column per n
+constexpr uint32_t kTmemCols = 2 * kAccCols; // double-buffered accumulator
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+
+__device__ unsigned int g_wait_status = 0;
+
+struct Params {
+    float* C;
+    int64_t rsC, csC, bsC;
+    int64_t M, N, K;
+    int64_t tiles_m, tiles_n, tiles_total;
+    int nk;
+    float alpha;
+    int accumulate;
+    int a_bcast, b_bcast;
+    int c_vec4;
+};
+
+struct Smem {
+    float a[kStages][BM * BK];
+    float b[kStages][BN * BK];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+// Instruction descriptor, kind::tf32: D fp32, A and B tf32, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+struct TileCoord { int64_t b, m0, n0; };
+
+__device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t) {
+    const int64_t per_batch = p.tiles_m * p.tiles_n;
+    const int64_t b = t / per_batch;
+    const int64_t r = t - b * per_batch;
+    constexpr int64_t G = 8;
+    const int64_t group = r / (G * p.tiles_n);
+    const int64_t first_m = group * G;
+    const int64_t gm = (p.tiles_m - first_m < G) ? (p.tiles_m - first_m) : G;
+    const int64_t w = r - group * G * p.tiles_n;
+    return {b, (first_m + w % gm) * BM, (w / gm) * BN};
+}
+
+__device__ __forceinline__ void producer(Smem& sh, const CUtensorMap* ta, const CUtensorMap* tb,
+                                         const Params& p) {
+    uint32_t stage = 0, phase = 0;
+    uint64_t issued = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < p.tiles_total && ok; t += gridDim.x) {
+        const TileCoord tc = tile_coord(p, t);
+        const int ba = p.a_bcast ? 0 : (int)tc.b;
+        const int bb = p.b_bcast ? 0 : (int)tc.b;
+        for (int kt = 0; kt < p.nk; ++kt) {
+            if (issued >= (uint64_t)kStages && !mbar_wait(&sh.empty[stage], phase ^ 1u)) {
+                record_status(&g_wait_status, kWaitEmpty);
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&sh.full[stage], kStageBytes);
+            tma_load_3d(sh.a[stage], ta, &sh.full[stage], kt * BK, (int)tc.m0, ba);
+            tma_load_3d(sh.b[stage], tb, &sh.full[stage], kt * BK, (int)tc.n0, bb);
+            ++issued;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+    }
+    // Wait for the copies still landing (the last kStages issued).
+    const uint64_t first = issued > (uint64_t)kStages ? issued - kStages : 0;
+    for (uint64_t q = first; q < issued; ++q)
+        if (!mbar_wait(&sh.full[q % kStages], (uint32_t)((q / kStages) & 1))) {
+            record_status(&g_wait_status, kWaitDrain);
+            return;
+        }
+}
+
+__device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params& p) {
+    uint32_t stage = 0, phase = 0;
+    uint64_t local = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < p.tiles_total && ok; t += gridDim.x, ++local) {
+        const uint32_t buf = (uint32_t)(local & 1);
+        const uint64_t use = local >> 1;
+        if (use > 0 && !mbar_wait(&sh.acc_empty[buf], (uint32_t)((use - 1) & 1))) {
+            record_status(&g_wait_status, kWaitAccFree);
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kAccCols;
+        for (int kt = 0; kt < p.nk; ++kt) {
+            if (!mbar_wait(&sh.full[stage], phase)) {
+                record_status(&g_wait_status, kWaitFull);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sh.a[stage]);
+            const uint32_t b0 = smem_u32(sh.b[stage]);
+#pragma unroll
+            for (int kk = 0; kk < BK / kMmaK; ++kk) {
+                const uint64_t ad = umma_desc_kmajor_sw128(a0 + kk * kMmaK * 4);
+                const uint64_t bd = umma_desc_kmajor_sw128(b0 + kk * kMmaK * 4);
+                mma_tf32(d, ad, bd, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&sh.empty[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&sh.acc_full[buf]);
+    }
+    // Nothing may still be writing TMEM when it is freed.
+    mma_commit(&sh.mma_done);
+    if (!mbar_wait(&sh.mma_done, 0)) record_status(&g_wait_status, kWaitMma);
+}
+
+__device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const Params& p, int warp,
+                                         int lane) {
+    const int quarter = warp & 3;               // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;
+    uint64_t local = 0;
+    for (int64_t t = blockIdx.x; t < p.tiles_total; t += gridDim.x, ++local) {
+        const uint32_t buf = (uint32_t)(local & 1);
+        if (!mbar_wait(&sh.acc_full[buf], (uint32_t)((local >> 1) & 1))) {
+            record_status(&g_wait_status, kWaitMma);
+            return;
+        }
+        tc_fence_after();
+        const TileCoord tc = tile_coord(p, t);
+        const int64_t m = tc.m0 + row;
+        const bool row_ok = m < p.M;
+        float* crow = p.C + tc.b * p.bsC + (row_ok ? m : 0) * p.rsC;
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * kAccCols;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            __syncwarp();
+            tmem_ld32(taddr + c * 32, v);      // whole warp, converged, every row
+            const int64_t n0 = tc.n0 + c * 32;
+            if (!row_ok || n0 >= p.N) {
+                // nothing of this piece is in C
+            } else if (p.c_vec4 && n0 + 32 <= p.N) {
+                float4* cp = reinterpret_cast<float4*>(crow + n0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (p.accumulate) o = cp[q];
+                    float4 r;
+                    r.x = p.accumulate ? fmaf(p.alpha, v[4 * q + 0], o.x) : p.alpha * v[4 * q + 0];
+                    r.y = p.accumulate ? fmaf(p.alpha, v[4 * q + 1], o.y) : p.alpha * v[4 * q + 1];
+                    r.z = p.accumulate ? fmaf(p.alpha, v[4 * q + 2], o.z) : p.alpha * v[4 * q + 2];
+                    r.w = p.accumulate ? fmaf(p.alpha, v[4 * q + 3], o.w) : p.alpha * v[4 * q + 3];
+                    cp[q] = r;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int64_t n = n0 + e;
+                    if (n < p.N) {
+                        float* cptr = crow + n * p.csC;
+                        *cptr = p.accumulate ? fmaf(p.alpha, v[e], *cptr) : p.alpha * v[e];
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.acc_empty[buf]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+               const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& sh = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                         ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.acc_full[b], 1);
+            mbar_init(&sh.acc_empty[b], kEpiWarps);
+        }
+        mbar_init(&sh.mma_done, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&ta);
+        prefetch_tensormap(&tb);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) producer(sh, &ta, &tb, p);
+    } else if (warp == 1) {
+        if (lane == 0) mma_issuer(sh, tmem, p);
+    } else {
+        epilogue(sh, tmem, p, warp, lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+bool make_kmajor_map(CUtensorMap* map, const float* base, int64_t K, int64_t rows, int64_t so,
+                     int64_t sb, int64_t batch, bool broadcast, int box_rows) {
+    const int64_t nb = broadcast ? 1 : batch;
+    const int64_t so_b = rows > 1 ? so * 4 : ((K * 4 + 15) / 16) * 16;
+    const int64_t sb_b = nb > 1 ? sb * 4 : so_b * (rows > 1 ? rows : 1);
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)nb};
+    const uint64_t strides[2] = {(uint64_t)so_b, (uint64_t)sb_b};
+    const uint32_t box[3] = {(uint32_t)BK, (uint32_t)box_rows, 1};
+    return encode_tmap_f32_3d(map, base, dims, strides, box, true);
+}
+
+}  // namespace
+
+TmaFfmaConfig tf32_tc_config() { return {BM, BN, BK, kStages, kThreads}; }
+
+cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cudaStream_t stream) {
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(tf32_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit);
+    }
+    CUtensorMap ta, tb;
+    const bool a_bc = pr.batch == 1 || pr.bsA == 0;
+    const bool b_bc = pr.batch == 1 || pr.bsB == 0;
+    if (!make_kmajor_map(&ta, pr.A, pr.K, pr.M, pr.rsA, pr.bsA, pr.batch, a_bc, BM))
+        return cudaErrorInvalidValue;
+    if (!make_kmajor_map(&tb, pr.B, pr.K, pr.N, pr.csB, pr.bsB, pr.batch, b_bc, BN))
+        return cudaErrorInvalidValue;
+    Params p;
+    p.C = pr.C; p.rsC = pr.rsC; p.csC = pr.csC; p.bsC = pr.bsC;
+    p.M = pr.M; p.N = pr.N; p.K = pr.K;
+    p.tiles_m = plan.tiles_m; p.tiles_n = plan.tiles_n; p.tiles_total = plan.tiles;
+    p.nk = (int)((pr.K + BK - 1) / BK);
+    p.alpha = pr.alpha;
+    p.accumulate = pr.accumulate;
+    p.a_bcast = a_bc;
+    p.b_bcast = b_bc;
+    p.c_vec4 = pr.csC == 1 && (reinterpret_cast<uintptr_t>(pr.C) % 16 == 0) &&
+               (pr.M == 1 || pr.rsC % 4 == 0) && (pr.batch == 1 || pr.bsC % 4 == 0);
+    const int64_t grid = plan.tiles < (int64_t)sm_count ? plan.tiles : (int64_t)sm_count;
+    tf32_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream) {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_wait_status, sizeof(v), 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_wait_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return v;
+}
+
+}  // namespace sbg

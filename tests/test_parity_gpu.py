@@ -264,3 +264,64 @@ def test_stream_k_repeated_calls_reuse_workspace(torch, workspace):
         again, _ = _run_ws(case, torch, workspace)
         assert np.array_equal(again, first)
     gu.check_full(case, first, exact=True)
+
+
+# ---- TF32 tensor-core path (opt-in) -------------------------------------------
+
+TF32_WORKLOADS = ["c2a", "c2b", "c3", "c3gqa", "c5a", "c5b"]   # both operands K-major
+
+
+@pytest.mark.parametrize("name", TF32_WORKLOADS)
+@pytest.mark.parametrize("values", ["real", "int"])
+def test_tf32_workloads_small(torch, name, values):
+    case = wl.make(name, values, **wl.small_shape(name))
+    assert _supported(case, sg.MATH_TF32, sg.PATH_TMA_TF32)
+    got = gu.run_case(case, torch, math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
+    gu.check_full(case, got, tol=gu.TOL_TF32, exact=(values == "int"))
+
+
+TF32_SHAPES = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (130, 70, 257), (257, 129, 300),
+               (128, 32, 256), (300, 1000, 520)]
+
+
+@pytest.mark.parametrize("mkn", TF32_SHAPES, ids=[f"{m}x{k}x{n}" for m, k, n in TF32_SHAPES])
+def test_tf32_awkward_shapes(torch, mkn):
+    M, K, N = mkn
+    rng = np.random.default_rng(M * 31 + K * 7 + N)
+    for i, (bsm, c_layout, acc, alpha) in enumerate([
+            (("dense", "dense"), "row", 0, 1.0),
+            (("zero", "dense"), "col", 1, -0.5),
+            (("dense", "zero"), "row", 1, 0.125)]):
+        batch = [1, 3, 2][i]
+        for values in ("int", "real"):
+            case = wl.random_strided(rng, M, N, K, batch, "row16", "col16", c_layout=c_layout,
+                                     bs_mode=bsm, values=values, accumulate=acc, alpha=alpha)
+            assert _supported(case, sg.MATH_TF32, sg.PATH_TMA_TF32)
+            got = gu.run_case(case, torch, math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
+            gu.check_full(case, got, tol=gu.TOL_TF32, exact=(values == "int"))
+
+
+def test_tf32_opt_in_falls_back_to_fp32_for_mn_major(torch):
+    """math=TF32 without a forced path serves MN-major operands with strict fp32."""
+    case = wl.make("c4", "real", **wl.small_shape("c4"))
+    plan = sg.sbgemm_plan(0x10000000, case.A.rs, case.A.cs, case.A.bs,
+                          0x20000000, case.B.rs, case.B.cs, case.B.bs,
+                          0x1000000000, case.C.rs, case.C.cs, case.C.bs,
+                          case.M, case.N, case.K, case.batch, case.accumulate,
+                          math=sg.MATH_TF32)
+    assert plan["path"] == sg.PATH_TMA_FFMA
+    assert not _supported(case, sg.MATH_TF32, sg.PATH_TMA_TF32)
+    got = gu.run_case(case, torch, math=sg.MATH_TF32)
+    gu.check_full(case, got)
+
+
+@pytest.mark.parametrize("name", ["c3", "c3gqa", "c5a", "c5b"])
+def test_tf32_full_size_sampled(torch, name):
+    case = wl.make(name, "real")
+    got = gu.run_case(case, torch, math=sg.MATH_TF32)
+    gu.check_points(case, got, tol=gu.TOL_TF32)
+    case_i = wl.make(name, "int")
+    got = gu.run_case(case_i, torch, math=sg.MATH_TF32)
+    gu.check_points(case_i, got, exact=True)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
