@@ -256,6 +256,8 @@ def run_ours(args, world, rank, local, dist):
     stream = torch.cuda.current_stream(dev)
     s_handle = stream.cuda_stream
     math = sg.MATH_TF32 if args.math == "tf32" else sg.MATH_FP32
+    force = {"auto": sg.PATH_AUTO, "gather": sg.PATH_GATHER_FFMA, "tma": sg.PATH_TMA_FFMA,
+             "tf32": sg.PATH_TMA_TF32}[args.path]
 
     names, cases = workload_cases(args.workload)
     dev_bufs = []
@@ -271,14 +273,15 @@ def run_ours(args, world, rank, local, dist):
     if not args.no_workspace:
         ws = torch.empty(sg.sbgemm_workspace_bytes(local), dtype=torch.uint8, device=dev)
         ws_kw = dict(workspace=ws.data_ptr(), workspace_bytes=ws.numel())
-    plans = [sg.sbgemm_plan(*a[:16], c.accumulate, math=math, **ws_kw)
+    plans = [sg.sbgemm_plan(*a[:16], c.accumulate, math=math, force_path=force, **ws_kw)
              for c, a in zip(cases, calls)]
     flops_step = sum(c.flops for c in cases)
     bytes_step = sum(wl.alg_bytes(c) for c in cases)
     ws_bytes = sum(c.A.storage.nbytes + c.B.storage.nbytes + c.C.storage.nbytes for c in cases)
 
-    def launch(i):
-        sg.sbgemm_ex(*calls[i], s_handle, math=math, **ws_kw)
+    def launch(i, m=None):
+        sg.sbgemm_ex(*calls[i], s_handle, math=math if m is None else m,
+                     force_path=force if m is None else sg.PATH_AUTO, **ws_kw)
 
     def step():
         for i in range(len(calls)):
@@ -390,6 +393,40 @@ def run_ours(args, world, rank, local, dist):
                "unit": "GFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": n_e2e, "ms_per_step": round(e_ms / n_e2e, 3)}
 
+    # The opt-in tensor-core path on the same products (operands that are not
+    # K-major fall back to strict fp32 and are reported as such).
+    tf32 = None
+    if not args.no_tf32 and math == sg.MATH_FP32:
+        tf32 = {"per_product": {}}
+        reps = max(3, min(args.steps, 20))
+        best = None
+        for i, (n, c) in enumerate(zip(names, cases)):
+            pl = sg.sbgemm_plan(*calls[i][:16], c.accumulate, math=sg.MATH_TF32, **ws_kw)
+            for _ in range(3):
+                launch(i, sg.MATH_TF32)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                launch(i, sg.MATH_TF32)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            tf32["per_product"][n] = {"ms": round(ms, 4), "gflops": round(c.flops / ms / 1e6, 1),
+                                      "path": pl["path_name"]}
+            if pl["path_name"] == "tma_tf32" and (best is None or ms > best[1]):
+                best = (n, ms, c)
+        if best is not None:
+            n, ms, c = best
+            peak = float(peaks.get("bf16_tflops", FALLBACK["bf16_tflops"])) * TF32_OVER_BF16_NOMINAL
+            ach = c.flops / (ms * 1e-3) / 1e12
+            tf32["roofline"] = {"bound": "tensor", "kernel": f"tma_tf32 ({n})",
+                                "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                                "frac": round(ach / peak, 4),
+                                "peak_source": f"{peaks_src} bf16 dense burst x nominal tf32/bf16 "
+                                               f"ratio {TF32_OVER_BF16_NOMINAL:.3f}",
+                                "traffic": profiled_traffic("tma_tf32", n)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -409,7 +446,7 @@ def run_ours(args, world, rank, local, dist):
         "dtype": "f32" if math == sg.MATH_FP32 else "tf32",
         "data": "synthetic (seeded numpy generators, shapes and value distributions of the workload)",
         "config": {"workload": DESCR.get(args.workload, args.workload),
-                   "products_per_step": len(cases), "math": args.math,
+                   "products_per_step": len(cases), "math": args.math, "path": args.path,
                    "gflop_per_step": round(flops_step / 1e9, 3),
                    "alg_mb_per_step": round(bytes_step / 2**20, 1),
                    "l2": f"inputs larger than L2: {wsmb:.0f} MiB resident per step vs "
@@ -421,6 +458,7 @@ def run_ours(args, world, rank, local, dist):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "tf32": tf32,
         "gpu_launches": len(calls) * args.steps,
         "clocks": clocks,
         "per_product": {n: {k: v for k, v in d.items() if k != "total_ms"} for n, d in per.items()},
@@ -474,6 +512,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workspace", action="store_true",
                     help="call without scratch (data-parallel schedule only)")
+    ap.add_argument("--path", choices=["auto", "gather", "tma", "tf32"], default="auto",
+                    help="force one kernel path for the timed products")
+    ap.add_argument("--no-tf32", action="store_true",
+                    help="skip the opt-in tensor-core measurement")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
     world, rank, local = dist_env()
