@@ -144,25 +144,58 @@ struct Issuer {
     int64_t total;      // slices this CTA loads in all
 };
 
-template <int BM, int BN>
+// TB: both operands K-major.  The B tile is then transposed in shared memory
+// into an MN-major buffer (two of them, alternating by slice), so the packed
+// FMAs find their column pairs in one 16-byte load instead of assembling them
+// from separate registers.
+template <int BM, int BN, bool TB = false>
 struct Cfg {
     static constexpr int kWarpsM = BM / WTM, kWarpsN = BN / WTN;
     static_assert(kWarpsM * kWarpsN == kWarps, "8 warps of 64 x 64");
     static constexpr int kABytes = BM * BK * 4, kBBytes = BN * BK * 4;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = 4;
+    static constexpr int kStages = (TB && BN > 128) ? 3 : 4;
+    static constexpr int kBtFloats = TB ? 2 * BK * BN : 4;
     struct Smem {
         float a[kStages][BM * BK];
         float b[kStages][BN * BK];
+        float bt[kBtFloats];          // TB: [2][BK][BN] transposed B slices
         uint64_t full[kStages];
         uint64_t empty[kStages];
+        uint64_t bt_done[2];          // TB: every thread wrote its part of bt[b]
+        uint64_t bt_used[2];          // TB: every thread finished reading bt[b]
         uint64_t stored;    // every thread has written its partial (stream-K head)
         uint64_t ready;     // the predecessor's partial is visible (stream-K tail)
         Schedule sched;     // the CTA's work list, computed once by thread 0
         Issuer iss;         // copy issuer state (thread 0)
     };
     static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
+
+// Transposes one K-major B slice ([BN_ rows][32 k], 128-byte swizzle) into
+// [32 k][BN_].  Each task moves a 4-row x 4-k block: four 16-byte loads, four
+// 16-byte stores.
+template <int BN_>
+__device__ __forceinline__ void transpose_b(const float* raw, float* bt) {
+    constexpr int kQuads = BN_ / 4;
+#pragma unroll
+    for (int task = threadIdx.x; task < kQuads * (BK / 4); task += kThreads) {
+        const int nq = task % kQuads, c = task / kQuads;
+        float4 v[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = 4 * nq + r;
+            v[r] = *reinterpret_cast<const float4*>(reinterpret_cast<const char*>(raw) + row * 128 +
+                                                    (((c ^ (row & 7)) & 7) << 4));
+        }
+        float* dst = bt + (4 * c) * BN_ + 4 * nq;
+        *reinterpret_cast<float4*>(dst) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
+        *reinterpret_cast<float4*>(dst + BN_) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
+        *reinterpret_cast<float4*>(dst + 2 * BN_) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
+        *reinterpret_cast<float4*>(dst + 3 * BN_) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+    }
+}
 
 struct TileCoord { int64_t b, m0, n0; };
 
@@ -283,10 +316,10 @@ __device__ __forceinline__ void fma_step(float2 (&acc)[64], const float (&a)[TM]
 }
 
 template <int BM, int BN, bool A_K, bool B_K>
-__device__ __forceinline__ void issue_next(typename Cfg<BM, BN>::Smem& sh, const CUtensorMap* ta,
+__device__ __forceinline__ void issue_next(typename Cfg<BM, BN, A_K && B_K>::Smem& sh, const CUtensorMap* ta,
                                            const CUtensorMap* tb, const Params& p,
                                            const Schedule& sc, Issuer& is) {
-    using C = Cfg<BM, BN>;
+    using C = Cfg<BM, BN, A_K && B_K>;
     Item itm = sc.item(p, is.w);
     if (is.kt < itm.kb) is.kt = itm.kb;
     const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
@@ -345,7 +378,9 @@ template <int BM, int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(kThreads, 1)
 tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                 const Params p) {
-    using C = Cfg<BM, BN>;
+    constexpr bool TB = A_K && B_K;
+    constexpr bool BKE = B_K && !TB;   // B layout as the mainloop sees it
+    using C = Cfg<BM, BN, TB>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     auto& sh = *reinterpret_cast<typename C::Smem*>(
@@ -362,6 +397,10 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
         for (int s = 0; s < S; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], kWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.bt_done[b], kThreads);
+            mbar_init(&sh.bt_used[b], kThreads);
         }
         mbar_init(&sh.stored, kThreads);
         mbar_init(&sh.ready, 1);
@@ -385,6 +424,19 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     int stage = 0;          // it % S, kept incrementally
     uint32_t phase = 0;     // (it / S) & 1
     const int64_t n_items = sc.n_items;
+    if constexpr (TB) {
+        // The first slice's B is transposed before the loop; every later one
+        // while the previous slice's stage is being released.
+        if (is.total > 0) {
+            if (!mbar_wait(&sh.full[0], 0)) {
+                record_status(&g_wait_status, kWaitFull);
+                if (issuer) drain<S>(sh.full, 0, is.issued);
+                return;
+            }
+            transpose_b<BN>(sh.b[0], sh.bt);
+            mbar_arrive(&sh.bt_done[0]);
+        }
+    }
     for (int64_t w = 0; w < n_items; ++w) {
         float2 acc[64];
         if (sc.item(p, w).mode == kTail) {
@@ -434,6 +486,14 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             if (++stage == S) { stage = 0; phase ^= 1u; }
             const float* As = sh.a[s];
             const float* Bs = sh.b[s];
+            if constexpr (TB) {
+                if (!mbar_wait(&sh.bt_done[it & 1], (it >> 1) & 1)) {
+                    record_status(&g_wait_status, kWaitFull);
+                    if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
+                    return;
+                }
+                Bs = sh.bt + (it & 1) * (BK * BN);
+            }
             // Unrolling deeper lets ptxas hoist fragment loads until the 128
             // accumulators spill; the warp's second neighbour on the scheduler
             // covers the shared-memory latency instead.
@@ -442,7 +502,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 float fa[TM][2], fb[TN][2];
                 // The pair operand is B unless A is MN-major (PI).
                 load_frag2<A_K, false, TM, 4, BM>(As, k, wm, lm, fa);
-                load_frag2<B_K, !PI, TN, 8, BN>(Bs, k, wn, ln, fb);
+                load_frag2<BKE, !PI, TN, 8, BN>(Bs, k, wn, ln, fb);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     float a[TM], b[TN];
@@ -455,6 +515,24 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.empty[s]);
+            if constexpr (TB) {
+                mbar_arrive(&sh.bt_used[it & 1]);
+                const uint32_t nx = it + 1;
+                if ((int64_t)nx < is.total) {
+                    const int nb = (int)(nx & 1);
+                    // Buffer nb last held slice nx-2: every thread must be done with it,
+                    // and slice nx's raw B (stage `stage`, phase `phase`) must have landed.
+                    const bool ok = (nx < 2 || mbar_wait(&sh.bt_used[nb], ((nx >> 1) - 1) & 1)) &&
+                                    mbar_wait(&sh.full[stage], phase);
+                    if (!ok) {
+                        record_status(&g_wait_status, kWaitFull);
+                        if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, nx), is.issued);
+                        return;
+                    }
+                    transpose_b<BN>(sh.b[stage], sh.bt + nb * (BK * BN));
+                    mbar_arrive(&sh.bt_done[nb]);
+                }
+            }
         }
 
         const Item itm = sc.item(p, w);
@@ -485,7 +563,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             const int64_t m = tc.m0 + row_of<A_K>(wm, lm, i);
             if (m >= p.M) continue;
             float* crow = Cb + m * p.rsC;
-            if (!B_K && p.c_vec4) {
+            if (!BKE && p.c_vec4) {
 #pragma unroll
                 for (int h = 0; h < TN / 4; ++h) {
                     const int64_t n = tc.n0 + col_of<false>(wn, ln, 4 * h);
@@ -519,7 +597,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             } else {
 #pragma unroll
                 for (int j = 0; j < TN; ++j) {
-                    const int64_t n = tc.n0 + col_of<B_K>(wn, ln, j);
+                    const int64_t n = tc.n0 + col_of<BKE>(wn, ln, j);
                     if (n >= p.N) continue;
                     float* c = crow + n * p.csC;
                     *c = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, j), *c)
@@ -549,7 +627,7 @@ bool make_map(CUtensorMap* map, const float* base, int64_t inner, int64_t outer,
 
 template <int BM, int BN, bool A_K, bool B_K>
 cudaError_t launch_impl(const Problem& pr, const Plan& plan, int sm_count, cudaStream_t stream) {
-    using C = Cfg<BM, BN>;
+    using C = Cfg<BM, BN, A_K && B_K>;
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaGetDevice(&dev);
