@@ -202,8 +202,17 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
     if (path == SBGEMM_PATH_TMA_TF32 && !tf32_ok) return SBGEMM_ERR_UNSUPPORTED;
     if (path == SBGEMM_PATH_TMA_FFMA && !tma_ok) return SBGEMM_ERR_UNSUPPORTED;
     if (path == SBGEMM_PATH_AUTO) {
-        if (o.math == SBGEMM_MATH_TF32 && tf32_ok) path = SBGEMM_PATH_TMA_TF32;
-        else path = tma_ok ? SBGEMM_PATH_TMA_FFMA : SBGEMM_PATH_GATHER_FFMA;
+        if (o.math == SBGEMM_MATH_TF32 && tf32_ok) {
+            path = SBGEMM_PATH_TMA_TF32;
+        } else if (tma_ok) {
+            // The persistent TMA kernel's 256x128 tiles leave most SMs idle on
+            // small products; the gather kernel's 64x64 tiles spread them wider.
+            const TmaFfmaConfig c = tma_ffma_config(tma_ffma_pick_variant(p, sm_count));
+            const int64_t tma_tiles = ((p.M + c.bm - 1) / c.bm) * ((p.N + c.bn - 1) / c.bn) * p.batch;
+            path = tma_tiles >= sm_count / 4 ? SBGEMM_PATH_TMA_FFMA : SBGEMM_PATH_GATHER_FFMA;
+        } else {
+            path = SBGEMM_PATH_GATHER_FFMA;
+        }
     }
     plan->path = path;
 

@@ -284,8 +284,13 @@ TF32_SHAPES = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (130, 70, 257), (257, 129, 
                (128, 32, 256), (300, 1000, 520)]
 
 
+TF32_LAYOUTS = [("row16", "col16")]   # A row-major, B column-major: both K-major
+
+
 @pytest.mark.parametrize("mkn", TF32_SHAPES, ids=[f"{m}x{k}x{n}" for m, k, n in TF32_SHAPES])
-def test_tf32_awkward_shapes(torch, mkn):
+@pytest.mark.parametrize("layouts", TF32_LAYOUTS, ids=["-".join(l) for l in TF32_LAYOUTS])
+def test_tf32_awkward_shapes(torch, mkn, layouts):
+    """Both operands K-major; zero batch strides, column-major C, ragged edges."""
     M, K, N = mkn
     rng = np.random.default_rng(M * 31 + K * 7 + N)
     for i, (bsm, c_layout, acc, alpha) in enumerate([
@@ -294,25 +299,30 @@ def test_tf32_awkward_shapes(torch, mkn):
             (("dense", "zero"), "row", 1, 0.125)]):
         batch = [1, 3, 2][i]
         for values in ("int", "real"):
-            case = wl.random_strided(rng, M, N, K, batch, "row16", "col16", c_layout=c_layout,
+            case = wl.random_strided(rng, M, N, K, batch, layouts[0], layouts[1], c_layout=c_layout,
                                      bs_mode=bsm, values=values, accumulate=acc, alpha=alpha)
             assert _supported(case, sg.MATH_TF32, sg.PATH_TMA_TF32)
             got = gu.run_case(case, torch, math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
             gu.check_full(case, got, tol=gu.TOL_TF32, exact=(values == "int"))
 
 
-def test_tf32_opt_in_falls_back_to_fp32_for_mn_major(torch):
-    """math=TF32 without a forced path serves MN-major operands with strict fp32."""
-    case = wl.make("c4", "real", **wl.small_shape("c4"))
-    plan = sg.sbgemm_plan(0x10000000, case.A.rs, case.A.cs, case.A.bs,
-                          0x20000000, case.B.rs, case.B.cs, case.B.bs,
-                          0x1000000000, case.C.rs, case.C.cs, case.C.bs,
-                          case.M, case.N, case.K, case.batch, case.accumulate,
-                          math=sg.MATH_TF32)
-    assert plan["path"] == sg.PATH_TMA_FFMA
-    assert not _supported(case, sg.MATH_TF32, sg.PATH_TMA_TF32)
-    got = gu.run_case(case, torch, math=sg.MATH_TF32)
-    gu.check_full(case, got)
+def test_tf32_opt_in_falls_back_to_fp32(torch):
+    """math=TF32 without a forced path serves operands the tensor-core path
+    does not take (MN-major tiles; strides TMA cannot fetch) with strict fp32."""
+    case = wl.make("c4", "real", **wl.small_shape("c4"))          # V is N-major
+    rng = np.random.default_rng(21)
+    general = wl.random_strided(rng, 70, 90, 50, 2, "gap", "neg_row", values="real",
+                                accumulate=1, alpha=0.5)
+    for c, want_path in ((case, (sg.PATH_TMA_FFMA, sg.PATH_GATHER_FFMA)),
+                         (general, (sg.PATH_GATHER_FFMA,))):
+        plan = sg.sbgemm_plan(0x10000000 + 4 * c.A.offset, c.A.rs, c.A.cs, c.A.bs,
+                              0x20000000 + 4 * c.B.offset, c.B.rs, c.B.cs, c.B.bs,
+                              0x1000000000, c.C.rs, c.C.cs, c.C.bs,
+                              c.M, c.N, c.K, c.batch, c.accumulate, math=sg.MATH_TF32)
+        assert plan["path"] in want_path
+        assert not _supported(c, sg.MATH_TF32, sg.PATH_TMA_TF32)
+        got = gu.run_case(c, torch, math=sg.MATH_TF32)
+        gu.check_full(c, got)
 
 
 @pytest.mark.parametrize("name", ["c3", "c3gqa", "c5a", "c5b"])
