@@ -83,6 +83,12 @@ def max_over_ranks(dist, x: float) -> float:
     return float(t.item())
 
 
+def job_rate(flops_per_step: int, world: int, steps: int, ms_slowest: float) -> float:
+    """Whole-job GFLOP/s: every rank runs the full step (replicas), so the job
+    does world x steps steps in the slowest rank's time."""
+    return flops_per_step * world * steps / (ms_slowest * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- peaks, clocks
 
 def measured_peaks():
@@ -316,7 +322,7 @@ def run_ours(args, world, rank, local, dist):
     elapsed_ms = start.elapsed_time(end)
     ms_max = max_over_ranks(dist, elapsed_ms)
     ms_per_step = ms_max / args.steps
-    value = flops_step * world * args.steps / (ms_max * 1e-3) / 1e9
+    value = job_rate(flops_step, world, args.steps, ms_max)
 
     per = {}
     for i, (n, c) in enumerate(zip(names, cases)):
@@ -389,7 +395,7 @@ def run_ours(args, world, rank, local, dist):
         torch.cuda.synchronize()
         barrier(dist)
         e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
-        e2e = {"value": round(flops_step * world * n_e2e / (e_ms * 1e-3) / 1e9, 1),
+        e2e = {"value": round(job_rate(flops_step, world, n_e2e, e_ms), 1),
                "unit": "GFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": n_e2e, "ms_per_step": round(e_ms / n_e2e, 3)}
 

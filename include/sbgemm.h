@@ -200,11 +200,25 @@ SBGEMM_API int sbgemm_noalloc(const float* A, int64_t rsA, int64_t csA, int64_t 
                               int64_t M, int64_t N, int64_t K, int64_t batch,
                               float alpha, int accumulate, void* stream);
 
-/* Reads and clears the device-side status word that bounded in-kernel waits
+/* Reads and clears the device-side status words that bounded in-kernel waits
  * set when they give up (after synchronising `stream`).  Returns SBGEMM_OK or
  * SBGEMM_ERR_DEVICE_TIMEOUT; *where_out (may be NULL) receives a code naming
- * the wait that expired (0 if none). */
+ * the wait that expired (0 if none): 1 a loaded stage, 2 a released stage, 3
+ * copies in flight at exit, 4 the MMAs of a tile, 5 a free accumulator, 6 a
+ * stream-K partial sum, 7 / 8 the self-test's mbarrier / flag. */
 SBGEMM_API int sbgemm_device_status(void* stream, int* where_out);
+
+/* Failure-detection self-test (a diagnostic of the library, not part of the
+ * product).  Launches one CTA on `stream` that waits, with the bounded-wait
+ * helpers every kernel uses and a limit of `limit_us` microseconds (1 ..
+ * 2,000,000), on a condition nothing satisfies: an mbarrier phase that never
+ * completes (SBGEMM_SELFTEST_MBARRIER) or a global flag no code sets
+ * (SBGEMM_SELFTEST_FLAG).  The wait gives up, records its code, and the kernel
+ * returns; the context stays usable and the next sbgemm_device_status call
+ * returns SBGEMM_ERR_DEVICE_TIMEOUT with that code.  Returns SBGEMM_OK once
+ * launched, SBGEMM_ERR_INVALID_VALUE for an unknown test or limit. */
+enum { SBGEMM_SELFTEST_MBARRIER = 1, SBGEMM_SELFTEST_FLAG = 2 };
+SBGEMM_API int sbgemm_selftest(int what, int64_t limit_us, void* stream);
 
 /* Static, human-readable name of a status code. */
 SBGEMM_API const char* sbgemm_status_string(int status);

@@ -17,7 +17,7 @@ import threading
 
 __all__ = [
     "SbgemmError", "load", "sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_workspace_bytes",
-    "sbgemm_noalloc",
+    "sbgemm_noalloc", "sbgemm_selftest", "SELFTEST_MBARRIER", "SELFTEST_FLAG",
     "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version", "matmul",
     "SBGEMM_OK", "SBGEMM_ERR_INVALID_VALUE", "SBGEMM_ERR_NULL_POINTER",
     "SBGEMM_ERR_OUTPUT_OVERLAP", "SBGEMM_ERR_UNSUPPORTED", "SBGEMM_ERR_CUDA",
@@ -47,8 +47,9 @@ PATH_NAMES = {PATH_NONE: "none", PATH_GATHER_FFMA: "gather_ffma",
 
 # Every function include/sbgemm.h declares.
 EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_workspace_bytes",
-                    "sbgemm_noalloc", "sbgemm_device_status", "sbgemm_status_string",
-                    "sbgemm_version")
+                    "sbgemm_noalloc", "sbgemm_selftest", "sbgemm_device_status",
+                    "sbgemm_status_string", "sbgemm_version")
+SELFTEST_MBARRIER, SELFTEST_FLAG = 1, 2
 
 
 class SbgemmError(RuntimeError):
@@ -106,6 +107,8 @@ def load(path: str = LIB_PATH):
         lib.sbgemm_noalloc.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp]
         lib.sbgemm_workspace_bytes.restype = ctypes.c_int
         lib.sbgemm_workspace_bytes.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+        lib.sbgemm_selftest.restype = ctypes.c_int
+        lib.sbgemm_selftest.argtypes = [ctypes.c_int, _i64, _vp]
         lib.sbgemm_device_status.restype = ctypes.c_int
         lib.sbgemm_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
         lib.sbgemm_status_string.restype = ctypes.c_char_p
@@ -189,6 +192,13 @@ def sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
     d = {name: getattr(info, name) for name, _ in _PlanInfo._fields_ if name != "reserved"}
     d["path_name"] = PATH_NAMES.get(d["path"], "?")
     return d
+
+
+def sbgemm_selftest(what: int, limit_us: int, stream=0) -> None:
+    """Launch the failure-detection self-test (a wait that must run out)."""
+    st = load().sbgemm_selftest(int(what), int(limit_us), stream or None)
+    if st:
+        raise SbgemmError(st, "sbgemm_selftest")
 
 
 def sbgemm_device_status(stream=0):

@@ -357,22 +357,6 @@ __device__ __forceinline__ uint64_t in_flight(uint64_t issued, uint32_t consumed
 __device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Bounded wait for the predecessor CTA's partial-ready flag.
-__device__ __forceinline__ bool wait_flag(const unsigned int* f) {
-    if (ld_acquire_gpu(f) != 0u) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (ld_acquire_gpu(f) == 0u) {
-        __nanosleep(64);
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
-    }
-    return true;
-}
 
 template <int BM, int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -80,6 +80,9 @@ TmaFfmaConfig tf32_tc_config();
 cudaError_t launch_tf32_tc(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream);
 
+// ---- failure-detection self-test (selftest.cu) ----------------------------------
+unsigned int read_and_clear_wait_status_selftest(cudaStream_t stream);
+
 // ---- driver entry points (driver.cpp) ---------------------------------------
 // [base, base+size) of the allocation that contains `ptr`; false if `ptr` is not
 // in a device-accessible allocation known to the driver.

@@ -19,6 +19,8 @@ enum : unsigned int {
     kWaitMma = 4,        // epilogue waiting for the accumulator
     kWaitAccFree = 5,    // MMA issuer waiting for the epilogue to free TMEM
     kWaitPartial = 6,    // stream-K: exchanging partial sums between CTAs
+    kWaitSelftestMbar = 7,   // self-test: an mbarrier phase nothing completes
+    kWaitSelftestFlag = 8,   // self-test: a global flag nothing sets
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -61,16 +63,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
-// false if it has not completed within kWaitTimeoutNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// false if it has not completed within `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until another CTA sets a global flag to a non-zero value.  Returns
+// false if it is still zero after `limit_ns`.
+__device__ __forceinline__ bool wait_flag(const unsigned int* f, uint64_t limit_ns = kWaitTimeoutNs) {
+    if (ld_acquire_gpu(f) != 0u) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(f) == 0u) {
+        __nanosleep(64);
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
 }
 
 // Records the first failure code in a status word.

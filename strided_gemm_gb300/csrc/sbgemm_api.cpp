@@ -437,7 +437,9 @@ int sbgemm_device_status(void* stream, int* where_out) {
     }
     unsigned int code = read_and_clear_wait_status_tma_ffma(s);
     const unsigned int code_tc = read_and_clear_wait_status_tf32(s);
+    const unsigned int code_st = read_and_clear_wait_status_selftest(s);
     if (code == 0) code = code_tc;
+    if (code == 0) code = code_st;
     if (code != 0) {
         if (where_out) *where_out = (int)code;
         return SBGEMM_ERR_DEVICE_TIMEOUT;
