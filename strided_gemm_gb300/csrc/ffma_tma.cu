@@ -144,26 +144,39 @@ struct Issuer {
     int64_t total;      // slices this CTA loads in all
 };
 
-// TB: both operands K-major.  The B tile is then transposed in shared memory
-// into an MN-major buffer (two of them, alternating by slice), so the packed
-// FMAs find their column pairs in one 16-byte load instead of assembling them
-// from separate registers.
-template <int BM, int BN, bool TB = false>
+// Shared-memory plan of one tile shape.  TA / TB: the A / B operand is
+// K-major and each of its slices is transposed in shared memory into an
+// MN-major buffer (two buffers, alternating by slice), so the mainloop always
+// reads both operands MN-major: 16-byte loads of 4 adjacent rows of A and 4
+// adjacent columns of B per k.  When both are transposed the raw TMA stage is
+// free as soon as its slice is transposed, so two raw stages keep two slices
+// in flight.
+constexpr size_t kSmemBudget = 232448 - 1024 - 512;   // opt-in limit - alignment - barriers
+
+template <int BM, int BN, bool TA = false, bool TB = false>
 struct Cfg {
     static constexpr int kWarpsM = BM / WTM, kWarpsN = BN / WTN;
     static_assert(kWarpsM * kWarpsN == kWarps, "8 warps of 64 x 64");
     static constexpr int kABytes = BM * BK * 4, kBBytes = BN * BK * 4;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = (TB && BN > 128) ? 3 : 4;
+    static constexpr bool kRawEarly = TA && TB;
+    static constexpr int kAtFloats = TA ? 2 * BK * BM : 4;
     static constexpr int kBtFloats = TB ? 2 * BK * BN : 4;
+    static constexpr size_t kTBytes = (size_t)(kAtFloats + kBtFloats) * 4;
+    static constexpr int kFit = (int)((kSmemBudget - kTBytes) / kStageBytes);
+    static constexpr int kStages = kFit > 4 ? 4 : kFit;
+    static_assert(kStages >= 2, "at least two raw stages");
+    // Slices issued ahead of the one being computed.
+    static constexpr int kLookahead = kRawEarly ? kStages : kStages - 1;
     struct Smem {
         float a[kStages][BM * BK];
         float b[kStages][BN * BK];
-        float bt[kBtFloats];          // TB: [2][BK][BN] transposed B slices
+        float at[kAtFloats];          // TA: [2][BK][BM]
+        float bt[kBtFloats];          // TB: [2][BK][BN]
         uint64_t full[kStages];
         uint64_t empty[kStages];
-        uint64_t bt_done[2];          // TB: every thread wrote its part of bt[b]
-        uint64_t bt_used[2];          // TB: every thread finished reading bt[b]
+        uint64_t t_done[2];           // every thread wrote its part of buffer b
+        uint64_t t_used[2];           // every thread finished reading buffer b
         uint64_t stored;    // every thread has written its partial (stream-K head)
         uint64_t ready;     // the predecessor's partial is visible (stream-K tail)
         Schedule sched;     // the CTA's work list, computed once by thread 0
@@ -173,11 +186,11 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-// Transposes one K-major B slice ([BN_ rows][32 k], 128-byte swizzle) into
-// [32 k][BN_].  Each task moves a 4-row x 4-k block: four 16-byte loads, four
-// 16-byte stores.
+// Transposes one K-major operand slice ([BN_ rows][32 k], 128-byte swizzle)
+// into [32 k][BN_].  Each task moves a 4-row x 4-k block: four 16-byte loads,
+// four 16-byte stores.
 template <int BN_>
-__device__ __forceinline__ void transpose_b(const float* raw, float* bt) {
+__device__ __forceinline__ void transpose_tile(const float* raw, float* bt) {
     constexpr int kQuads = BN_ / 4;
 #pragma unroll
     for (int task = threadIdx.x; task < kQuads * (BK / 4); task += kThreads) {
@@ -316,10 +329,10 @@ __device__ __forceinline__ void fma_step(float2 (&acc)[64], const float (&a)[TM]
 }
 
 template <int BM, int BN, bool A_K, bool B_K>
-__device__ __forceinline__ void issue_next(typename Cfg<BM, BN, A_K && B_K>::Smem& sh, const CUtensorMap* ta,
+__device__ __forceinline__ void issue_next(typename Cfg<BM, BN, A_K, B_K>::Smem& sh, const CUtensorMap* ta,
                                            const CUtensorMap* tb, const Params& p,
                                            const Schedule& sc, Issuer& is) {
-    using C = Cfg<BM, BN, A_K && B_K>;
+    using C = Cfg<BM, BN, A_K, B_K>;
     Item itm = sc.item(p, is.w);
     if (is.kt < itm.kb) is.kt = itm.kb;
     const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
@@ -362,10 +375,11 @@ template <int BM, int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(kThreads, 1)
 tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                 const Params p) {
-    constexpr bool TB = A_K && B_K;
-    constexpr bool BKE = B_K && !TB;   // B layout as the mainloop sees it
-    using C = Cfg<BM, BN, TB>;
+    constexpr bool TA = A_K, TB = B_K;   // K-major operands are transposed in smem
+    constexpr bool TT = TA || TB;
+    using C = Cfg<BM, BN, TA, TB>;
     constexpr int S = C::kStages;
+    constexpr bool RAW_EARLY = C::kRawEarly;
     extern __shared__ uint8_t smem_raw[];
     auto& sh = *reinterpret_cast<typename C::Smem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -383,8 +397,8 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             mbar_init(&sh.empty[s], kWarps);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&sh.bt_done[b], kThreads);
-            mbar_init(&sh.bt_used[b], kThreads);
+            mbar_init(&sh.t_done[b], kThreads);
+            mbar_init(&sh.t_used[b], kThreads);
         }
         mbar_init(&sh.stored, kThreads);
         mbar_init(&sh.ready, 1);
@@ -394,31 +408,36 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     }
     __syncthreads();
     if (issuer) {
-        for (int q = 0; q < S - 1 && (int64_t)is.issued < is.total; ++q)
+        for (int q = 0; q < C::kLookahead && (int64_t)is.issued < is.total; ++q)
             issue_next<BM, BN, A_K, B_K>(sh, &ta, &tb, p, sc, is);
     }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wm = (warp % C::kWarpsM) * WTM, wn = (warp / C::kWarpsM) * WTN;
     const int lm = lane >> 3, ln = lane & 7;
-    // Pair along the dimension whose operand arrives with adjacent values:
-    // rows when A is MN-major, otherwise columns.
-    constexpr bool PI = !A_K;
+    // Both operands reach the mainloop MN-major: pair rows of A (adjacent in
+    // one 16-byte load), broadcast B.
+    constexpr bool PI = true;
     uint32_t it = 0;        // slices consumed so far (low 32 bits)
     int stage = 0;          // it % S, kept incrementally
     uint32_t phase = 0;     // (it / S) & 1
     const int64_t n_items = sc.n_items;
-    if constexpr (TB) {
-        // The first slice's B is transposed before the loop; every later one
-        // while the previous slice's stage is being released.
+    if constexpr (TT) {
+        // The first slice is transposed before the loop, every later one at
+        // the end of the previous slice's iteration.
         if (is.total > 0) {
             if (!mbar_wait(&sh.full[0], 0)) {
                 record_status(&g_wait_status, kWaitFull);
                 if (issuer) drain<S>(sh.full, 0, is.issued);
                 return;
             }
-            transpose_b<BN>(sh.b[0], sh.bt);
-            mbar_arrive(&sh.bt_done[0]);
+            if constexpr (TA) transpose_tile<BM>(sh.a[0], sh.at);
+            if constexpr (TB) transpose_tile<BN>(sh.b[0], sh.bt);
+            if constexpr (RAW_EARLY) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.empty[0]);
+            }
+            mbar_arrive(&sh.t_done[0]);
         }
     }
     for (int64_t w = 0; w < n_items; ++w) {
@@ -462,21 +481,20 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 issue_next<BM, BN, A_K, B_K>(sh, &ta, &tb, p, sc, is);
             }
             const int s = stage;
-            if (!mbar_wait(&sh.full[s], phase)) {
+            if (!RAW_EARLY && !mbar_wait(&sh.full[s], phase)) {
                 record_status(&g_wait_status, kWaitFull);
                 if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
                 return;
             }
             if (++stage == S) { stage = 0; phase ^= 1u; }
-            const float* As = sh.a[s];
-            const float* Bs = sh.b[s];
-            if constexpr (TB) {
-                if (!mbar_wait(&sh.bt_done[it & 1], (it >> 1) & 1)) {
+            const float* As = TA ? sh.at + (it & 1) * (BK * BM) : sh.a[s];
+            const float* Bs = TB ? sh.bt + (it & 1) * (BK * BN) : sh.b[s];
+            if constexpr (TT) {
+                if (!mbar_wait(&sh.t_done[it & 1], (it >> 1) & 1)) {
                     record_status(&g_wait_status, kWaitFull);
                     if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
                     return;
                 }
-                Bs = sh.bt + (it & 1) * (BK * BN);
             }
             // Unrolling deeper lets ptxas hoist fragment loads until the 128
             // accumulators spill; the warp's second neighbour on the scheduler
@@ -485,8 +503,8 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             for (int k = 0; k < BK; k += 2) {
                 float fa[TM][2], fb[TN][2];
                 // The pair operand is B unless A is MN-major (PI).
-                load_frag2<A_K, false, TM, 4, BM>(As, k, wm, lm, fa);
-                load_frag2<BKE, !PI, TN, 8, BN>(Bs, k, wn, ln, fb);
+                load_frag2<false, false, TM, 4, BM>(As, k, wm, lm, fa);
+                load_frag2<false, false, TN, 8, BN>(Bs, k, wn, ln, fb);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     float a[TM], b[TN];
@@ -497,24 +515,31 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                     fma_step<PI>(acc, a, b);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-            if constexpr (TB) {
-                mbar_arrive(&sh.bt_used[it & 1]);
+            if constexpr (!RAW_EARLY) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.empty[s]);
+            }
+            if constexpr (TT) {
+                mbar_arrive(&sh.t_used[it & 1]);
                 const uint32_t nx = it + 1;
                 if ((int64_t)nx < is.total) {
                     const int nb = (int)(nx & 1);
                     // Buffer nb last held slice nx-2: every thread must be done with it,
-                    // and slice nx's raw B (stage `stage`, phase `phase`) must have landed.
-                    const bool ok = (nx < 2 || mbar_wait(&sh.bt_used[nb], ((nx >> 1) - 1) & 1)) &&
+                    // and slice nx's raw tiles (stage `stage`, phase `phase`) must have landed.
+                    const bool ok = (nx < 2 || mbar_wait(&sh.t_used[nb], ((nx >> 1) - 1) & 1)) &&
                                     mbar_wait(&sh.full[stage], phase);
                     if (!ok) {
                         record_status(&g_wait_status, kWaitFull);
                         if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, nx), is.issued);
                         return;
                     }
-                    transpose_b<BN>(sh.b[stage], sh.bt + nb * (BK * BN));
-                    mbar_arrive(&sh.bt_done[nb]);
+                    if constexpr (TA) transpose_tile<BM>(sh.a[stage], sh.at + nb * (BK * BM));
+                    if constexpr (TB) transpose_tile<BN>(sh.b[stage], sh.bt + nb * (BK * BN));
+                    if constexpr (RAW_EARLY) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sh.empty[stage]);
+                    }
+                    mbar_arrive(&sh.t_done[nb]);
                 }
             }
         }
@@ -544,10 +569,10 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
         float* Cb = p.C + tc.b * p.bsC;
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
-            const int64_t m = tc.m0 + row_of<A_K>(wm, lm, i);
+            const int64_t m = tc.m0 + row_of<false>(wm, lm, i);
             if (m >= p.M) continue;
             float* crow = Cb + m * p.rsC;
-            if (!BKE && p.c_vec4) {
+            if (p.c_vec4) {
 #pragma unroll
                 for (int h = 0; h < TN / 4; ++h) {
                     const int64_t n = tc.n0 + col_of<false>(wn, ln, 4 * h);
@@ -581,7 +606,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             } else {
 #pragma unroll
                 for (int j = 0; j < TN; ++j) {
-                    const int64_t n = tc.n0 + col_of<BKE>(wn, ln, j);
+                    const int64_t n = tc.n0 + col_of<false>(wn, ln, j);
                     if (n >= p.N) continue;
                     float* c = crow + n * p.csC;
                     *c = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, j), *c)
@@ -611,7 +636,7 @@ bool make_map(CUtensorMap* map, const float* base, int64_t inner, int64_t outer,
 
 template <int BM, int BN, bool A_K, bool B_K>
 cudaError_t launch_impl(const Problem& pr, const Plan& plan, int sm_count, cudaStream_t stream) {
-    using C = Cfg<BM, BN, A_K && B_K>;
+    using C = Cfg<BM, BN, A_K, B_K>;
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaGetDevice(&dev);
