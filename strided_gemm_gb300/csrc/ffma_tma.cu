@@ -186,12 +186,33 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-// Transposes one K-major operand slice ([BN_ rows][32 k], 128-byte swizzle)
-// into [32 k][BN_].  Each task moves a 4-row x 4-k block: four 16-byte loads,
-// four 16-byte stores.
-template <int BN_>
-__device__ __forceinline__ void transpose_tile(const float* raw, float* bt) {
-    constexpr int kQuads = BN_ / 4;
+// Transposes one K-major operand slice ([R rows][32 k], 128-byte swizzle) into
+// [32 k][R].  Two task shapes, measured per operand:
+//  - rows (A, 256 rows): task = one row's 16-byte chunk of 4 k values; a warp
+//    takes 32 consecutive rows of one chunk, so its 16-byte loads hit 8
+//    distinct swizzled chunks per quarter-warp and its 4-byte stores 32
+//    consecutive columns: no bank conflicts, more instructions;
+//  - quads (B, 128 rows): task = a 4-row x 4-k block, four 16-byte loads and
+//    four 16-byte stores: fewer instructions, some load conflicts.
+template <int R>
+__device__ __forceinline__ void transpose_rows(const float* raw, float* dst) {
+    static_assert(R % 32 == 0, "a warp covers 32 rows of one chunk");
+#pragma unroll 2
+    for (int task = threadIdx.x; task < R * (BK / 4); task += kThreads) {
+        const int row = task % R, c = task / R;
+        const float4 v = *reinterpret_cast<const float4*>(
+            reinterpret_cast<const char*>(raw) + row * 128 + (((c ^ (row & 7)) & 7) << 4));
+        float* d = dst + (4 * c) * R + row;
+        d[0] = v.x;
+        d[R] = v.y;
+        d[2 * R] = v.z;
+        d[3 * R] = v.w;
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void transpose_quads(const float* raw, float* dst) {
+    constexpr int kQuads = R / 4;
 #pragma unroll
     for (int task = threadIdx.x; task < kQuads * (BK / 4); task += kThreads) {
         const int nq = task % kQuads, c = task / kQuads;
@@ -202,11 +223,11 @@ __device__ __forceinline__ void transpose_tile(const float* raw, float* bt) {
             v[r] = *reinterpret_cast<const float4*>(reinterpret_cast<const char*>(raw) + row * 128 +
                                                     (((c ^ (row & 7)) & 7) << 4));
         }
-        float* dst = bt + (4 * c) * BN_ + 4 * nq;
-        *reinterpret_cast<float4*>(dst) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
-        *reinterpret_cast<float4*>(dst + BN_) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
-        *reinterpret_cast<float4*>(dst + 2 * BN_) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
-        *reinterpret_cast<float4*>(dst + 3 * BN_) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+        float* d = dst + (4 * c) * R + 4 * nq;
+        *reinterpret_cast<float4*>(d) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
+        *reinterpret_cast<float4*>(d + R) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
+        *reinterpret_cast<float4*>(d + 2 * R) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
+        *reinterpret_cast<float4*>(d + 3 * R) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
     }
 }
 
@@ -431,8 +452,8 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 if (issuer) drain<S>(sh.full, 0, is.issued);
                 return;
             }
-            if constexpr (TA) transpose_tile<BM>(sh.a[0], sh.at);
-            if constexpr (TB) transpose_tile<BN>(sh.b[0], sh.bt);
+            if constexpr (TA) transpose_rows<BM>(sh.a[0], sh.at);
+            if constexpr (TB) transpose_quads<BN>(sh.b[0], sh.bt);
             if constexpr (RAW_EARLY) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.empty[0]);
@@ -533,8 +554,8 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                         if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, nx), is.issued);
                         return;
                     }
-                    if constexpr (TA) transpose_tile<BM>(sh.a[stage], sh.at + nb * (BK * BM));
-                    if constexpr (TB) transpose_tile<BN>(sh.b[stage], sh.bt + nb * (BK * BN));
+                    if constexpr (TA) transpose_rows<BM>(sh.a[stage], sh.at + nb * (BK * BM));
+                    if constexpr (TB) transpose_quads<BN>(sh.b[stage], sh.bt + nb * (BK * BN));
                     if constexpr (RAW_EARLY) {
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sh.empty[stage]);
