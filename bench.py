@@ -360,8 +360,11 @@ def run_ours(args, world, rank, local, dist):
     roof["hbm_frac"] = round(wl.alg_bytes(dcase) / avg_s / 1e9 /
                              float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])), 4)
 
-    # End to end through the public API with host buffers: every step copies its
-    # inputs from pinned host memory, runs the products and reads C back.
+    # End to end through the public API with host buffers: every step copies all
+    # of its inputs from pinned host memory, runs the products and reads every
+    # C back.  Copies run on two copy streams so that product i+1's inputs move
+    # while product i computes and product i's result returns while i+1 runs;
+    # steps do not overlap one another.
     e2e = None
     if not args.no_e2e:
         host_in = [(torch.from_numpy(c.A.storage).pin_memory(),
@@ -372,16 +375,35 @@ def run_ours(args, world, rank, local, dist):
                   for h, c in zip(host_in, cases))
         d2h = sum(h.numel() * 4 for h in host_out)
         n_e2e = max(1, min(args.steps, args.e2e_steps))
+        up = torch.cuda.Stream(dev)
+        down = torch.cuda.Stream(dev)
 
         def e2e_step():
+            start = torch.cuda.Event()
+            start.record(stream)
+            up.wait_event(start)
+            inputs_ready = []
+            with torch.cuda.stream(up):
+                for i, c in enumerate(cases):
+                    dA, dB, dC = dev_bufs[i]
+                    dA.copy_(host_in[i][0], non_blocking=True)
+                    dB.copy_(host_in[i][1], non_blocking=True)
+                    if c.accumulate:
+                        dC.copy_(host_in[i][2], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(up)
+                    inputs_ready.append(ev)
             for i, c in enumerate(cases):
-                dA, dB, dC = dev_bufs[i]
-                dA.copy_(host_in[i][0], non_blocking=True)
-                dB.copy_(host_in[i][1], non_blocking=True)
-                if c.accumulate:
-                    dC.copy_(host_in[i][2], non_blocking=True)
+                stream.wait_event(inputs_ready[i])
                 launch(i)
-                host_out[i].copy_(dC, non_blocking=True)
+                done = torch.cuda.Event()
+                done.record(stream)
+                down.wait_event(done)
+                with torch.cuda.stream(down):
+                    host_out[i].copy_(dev_bufs[i][2], non_blocking=True)
+            back = torch.cuda.Event()
+            back.record(down)
+            stream.wait_event(back)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -397,7 +419,8 @@ def run_ours(args, world, rank, local, dist):
         e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
         e2e = {"value": round(job_rate(flops_step, world, n_e2e, e_ms), 1),
                "unit": "GFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": n_e2e, "ms_per_step": round(e_ms / n_e2e, 3)}
+               "steps": n_e2e, "ms_per_step": round(e_ms / n_e2e, 3),
+               "copies": "pinned host buffers, two copy streams overlapping the products"}
 
     # The opt-in tensor-core path on the same products (operands that are not
     # K-major fall back to strict fp32 and are reported as such).
