@@ -1,34 +1,34 @@
 // TMA-fed FFMA path for operands with a unit stride (K-major or MN-major) whose
 // other strides are 16-byte multiples.
 //
-// Persistent CTAs (one per SM) of eight warps walk their output tiles.  Each
-// tile's K range is cut into BK-deep slices that TMA copies (one box of A, one
-// of B) into a ring of shared-memory stages; "full" mbarriers signal a landed
-// stage and "empty" mbarriers (one arrival per warp) its release.  Thread 0
-// doubles as the copy issuer: at every slice it refills the stage that all
-// warps released one slice earlier, so copies run kStages-1 slices ahead,
-// across tile boundaries too (the next tile streams in during an epilogue).
+// Persistent CTAs (one per SM) of eight warps walk their work list: whole
+// output tiles, and with a workspace the K ranges of the last waves split
+// across CTAs (stream-K).  Each tile's K range is cut into 32-deep slices that
+// TMA copies (one box of A, one of B) into a ring of shared-memory stages;
+// "full" mbarriers signal a landed stage, "empty" mbarriers (one arrival per
+// warp) its release.  Thread 0 doubles as the copy issuer, refilling the stage
+// released one slice earlier, across tile boundaries too.
+//
+// The mainloop always reads both operands MN-major: a K-major slice (stored by
+// TMA as 128-byte swizzled rows along K) is first transposed in shared memory
+// into an MN-major buffer (two buffers, alternating by slice, synchronised by
+// bounded mbarriers).  When both operands are transposed the raw stage is free
+// as soon as its slice is, so two raw stages keep two slices in flight.
 //
 // Each warp computes a 64 x 64 warp tile as 16 x 8 register micro-tiles per
 // thread (the register blocking of the StaleyNET "GPU Implementation" page,
-// section "The matrix product", grown from 4 x 4).  The micro-tile size is set
-// by shared-memory bandwidth: an SM reads 32 fp32 words per clock from shared
-// memory but retires 128 FMA lanes, so a thread must do at least 4 FMAs per
-// word it loads; 16 x 8 does 128 per 24 (8 x 8 would sit exactly at the limit).
-// The FMAs are packed two lanes per instruction (FFMA2, fma.rn.f32x2): pairs
-// run along whichever operand arrives with adjacent values (an MN-major tile),
-// the other operand is broadcast.  Each output still has one fused
-// multiply-add chain in increasing k, so results are bit-identical to a
-// scalar fmaf loop and across layouts.  The epilogue writes alpha*acc
-// (+ C_old) straight from registers with masks on ragged M / N.
-//
-// Shared-memory layouts follow the operand's unit stride: a K-major tile is
-// stored [row][32 k] with the TMA 128-byte swizzle (conflict-free 8-byte
-// fragment reads along k), an MN-major tile [32 k][rows] unswizzled (16-byte
-// fragment reads along m or n).  Out-of-range rows, columns and k are
-// zero-filled by TMA.  Every mbarrier wait is bounded: on expiry the thread
-// records a status code and returns (the copy issuer first waits, again
-// bounded, for the copies it has in flight).
+// section "The matrix product", grown from 4 x 4).  The size follows from
+// shared-memory bandwidth: an SM reads 32 fp32 words per clock from shared
+// memory but retires 128 FMA lanes, so a thread needs at least 4 FMAs per word
+// it loads; 16 x 8 does 128 per 24.  The FMAs are packed two lanes per
+// instruction (FFMA2, fma.rn.f32x2) over pairs of adjacent A rows, with B
+// broadcast; the next k's fragments load while this k's FMAs run.  Each output
+// keeps one fused multiply-add chain in increasing k, so results are
+// bit-identical to a scalar fmaf loop, to the gather path and across layouts.
+// The epilogue writes alpha*acc (+ C_old) straight from registers with masks
+// on ragged M / N.  Every wait is bounded: on expiry the thread records a
+// status code and returns (the copy issuer first waits, again bounded, for the
+// copies it has in flight).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -41,15 +41,11 @@
 #ifndef SBGEMM_FFMA2
 #define SBGEMM_FFMA2 1
 #endif
-#ifndef SBGEMM_KUNROLL
-#define SBGEMM_KUNROLL 2
-#endif
 
 namespace sbg {
 namespace {
 
 constexpr int BK = 32;
-constexpr int kUnrollK = SBGEMM_KUNROLL;   // k-pair groups unrolled per slice
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int TM = 16, TN = 8;         // micro-tile per thread (rows of A x columns of B)
@@ -249,66 +245,13 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t) {
 }
 
 // Thread -> tile row of its i-th A row (16) / tile column of its j-th B column
-// (8).  K-major operands step by the lane count (distinct swizzle rows per
-// load); MN-major operands take runs of 4 adjacent values (one 16-byte load).
-template <bool K_MAJOR>
+// (8): runs of 4 adjacent values (one 16-byte load), the runs of a thread 16
+// rows / 32 columns apart so the lanes of a warp cover 64 x 64.
 __device__ __forceinline__ int row_of(int wbase, int lm, int i) {
-    return K_MAJOR ? wbase + lm + 4 * i : wbase + (i >> 2) * 16 + lm * 4 + (i & 3);
+    return wbase + (i >> 2) * 16 + lm * 4 + (i & 3);
 }
-template <bool K_MAJOR>
 __device__ __forceinline__ int col_of(int wbase, int ln, int j) {
-    return K_MAJOR ? wbase + ln + 8 * j : wbase + (j >> 2) * 32 + ln * 4 + (j & 3);
-}
-
-// Fragments of one operand for k = k0, k0+1 (k0 even): R values per thread
-// per k.  LANES distinct lane indices run along the dimension (4 for A rows, 8
-// for B columns).  `lidx` is the lane index, `wbase` the warp's first row.
-//
-// K-major tiles are [row][32 k] with the 128-byte swizzle: the 16-byte chunk c
-// of row r sits at chunk c ^ (r & 7).  A thread's rows wbase + lidx + LANES*i
-// fall into at most two swizzle classes (r & 7 = lidx + LANES*(i&1) mod 8), so
-// each k-chunk needs one XOR per class and every load is base + immediate.
-// PAIRED (K-major pair operand): 4-byte loads of k0 and k0+1 separately, so
-// values of neighbouring rows land in one register pair without moves.
-// Otherwise K-major uses one 8-byte load per row (k0, k0+1).
-// MN-major tiles are [k][TILE_ROWS]: 16-byte loads of 4 adjacent rows.
-template <bool K_MAJOR, bool PAIRED, int R, int LANES, int TILE_ROWS>
-__device__ __forceinline__ void load_frag2(const float* tile, int k0, int wbase, int lidx,
-                                           float (&f)[R][2]) {
-    if (K_MAJOR) {
-        const char* base = reinterpret_cast<const char*>(tile) + (wbase + lidx) * 128;
-        const int c = k0 >> 2;
-        const int x0 = lidx & 7, x1 = (lidx + LANES) & 7;
-        const char* b0 = base + (((c ^ x0) & 7) << 4) + ((k0 & 3) << 2);
-        const char* b1 = base + (((c ^ x1) & 7) << 4) + ((k0 & 3) << 2);
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-            const char* q = ((i & 1) ? b1 : b0) + i * LANES * 128;
-            if (PAIRED) {
-                // Two 4-byte loads kept apart (the compiler would otherwise merge
-                // them into one wide load whose registers cannot form pairs
-                // across rows without moves).
-                const uint32_t a = smem_u32(q);
-                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f[i][0]) : "r"(a));
-                asm volatile("ld.shared.f32 %0, [%1+4];" : "=f"(f[i][1]) : "r"(a));
-            } else {
-                const float2 v = *reinterpret_cast<const float2*>(q);
-                f[i][0] = v.x;
-                f[i][1] = v.y;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const float* row = tile + (k0 + kk) * TILE_ROWS + wbase + lidx * 4;
-#pragma unroll
-            for (int q = 0; q < R / 4; ++q) {
-                const float4 v = *reinterpret_cast<const float4*>(row + q * 4 * LANES);
-                f[4 * q + 0][kk] = v.x; f[4 * q + 1][kk] = v.y;
-                f[4 * q + 2][kk] = v.z; f[4 * q + 3][kk] = v.w;
-            }
-        }
-    }
+    return wbase + (j >> 2) * 32 + ln * 4 + (j & 3);
 }
 
 // Accumulators of the 16 x 8 micro-tile as 64 float pairs.  PAIR_I pairs rows
@@ -517,23 +460,41 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                     return;
                 }
             }
-            // Unrolling deeper lets ptxas hoist fragment loads until the 128
-            // accumulators spill; the warp's second neighbour on the scheduler
-            // covers the shared-memory latency instead.
-#pragma unroll kUnrollK
-            for (int k = 0; k < BK; k += 2) {
-                float fa[TM][2], fb[TN][2];
-                // The pair operand is B unless A is MN-major (PI).
-                load_frag2<false, false, TM, 4, BM>(As, k, wm, lm, fa);
-                load_frag2<false, false, TN, 8, BN>(Bs, k, wn, ln, fb);
+            {
+                // One k ahead: the next k's fragments (24 registers, 16-byte
+                // loads of 4 adjacent rows of A and columns of B) load while
+                // this k's 64 packed FMAs run.  Deeper unrolling spills.
+                float fa[2][TM], fb[2][TN];
+                const float* arow = As + wm + lm * 4;
+                const float* brow = Bs + wn + ln * 4;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    float a[TM], b[TN];
+                for (int q = 0; q < TM / 4; ++q) {
+                    const float4 v = *reinterpret_cast<const float4*>(arow + q * 16);
+                    fa[0][4 * q] = v.x; fa[0][4 * q + 1] = v.y; fa[0][4 * q + 2] = v.z; fa[0][4 * q + 3] = v.w;
+                }
 #pragma unroll
-                    for (int q = 0; q < TM; ++q) a[q] = fa[q][kk];
+                for (int q = 0; q < TN / 4; ++q) {
+                    const float4 v = *reinterpret_cast<const float4*>(brow + q * 32);
+                    fb[0][4 * q] = v.x; fb[0][4 * q + 1] = v.y; fb[0][4 * q + 2] = v.z; fb[0][4 * q + 3] = v.w;
+                }
+#pragma unroll 4
+                for (int k = 0; k < BK; ++k) {
+                    const int cur = k & 1;
+                    if (k + 1 < BK) {
 #pragma unroll
-                    for (int q = 0; q < TN; ++q) b[q] = fb[q][kk];
-                    fma_step<PI>(acc, a, b);
+                        for (int q = 0; q < TM / 4; ++q) {
+                            const float4 v = *reinterpret_cast<const float4*>(arow + (k + 1) * BM + q * 16);
+                            fa[cur ^ 1][4 * q] = v.x; fa[cur ^ 1][4 * q + 1] = v.y;
+                            fa[cur ^ 1][4 * q + 2] = v.z; fa[cur ^ 1][4 * q + 3] = v.w;
+                        }
+#pragma unroll
+                        for (int q = 0; q < TN / 4; ++q) {
+                            const float4 v = *reinterpret_cast<const float4*>(brow + (k + 1) * BN + q * 32);
+                            fb[cur ^ 1][4 * q] = v.x; fb[cur ^ 1][4 * q + 1] = v.y;
+                            fb[cur ^ 1][4 * q + 2] = v.z; fb[cur ^ 1][4 * q + 3] = v.w;
+                        }
+                    }
+                    fma_step<PI>(acc, fa[cur], fb[cur]);
                 }
             }
             if constexpr (!RAW_EARLY) {
@@ -590,13 +551,13 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
         float* Cb = p.C + tc.b * p.bsC;
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
-            const int64_t m = tc.m0 + row_of<false>(wm, lm, i);
+            const int64_t m = tc.m0 + row_of(wm, lm, i);
             if (m >= p.M) continue;
             float* crow = Cb + m * p.rsC;
             if (p.c_vec4) {
 #pragma unroll
                 for (int h = 0; h < TN / 4; ++h) {
-                    const int64_t n = tc.n0 + col_of<false>(wn, ln, 4 * h);
+                    const int64_t n = tc.n0 + col_of(wn, ln, 4 * h);
                     if (n + 3 < p.N) {
                         float4* cp = reinterpret_cast<float4*>(crow + n);
                         float4 v;
@@ -627,7 +588,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             } else {
 #pragma unroll
                 for (int j = 0; j < TN; ++j) {
-                    const int64_t n = tc.n0 + col_of<false>(wn, ln, j);
+                    const int64_t n = tc.n0 + col_of(wn, ln, j);
                     if (n >= p.N) continue;
                     float* c = crow + n * p.csC;
                     *c = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, j), *c)
