@@ -37,6 +37,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 #ifndef SBGEMM_FFMA2
 #define SBGEMM_FFMA2 1
@@ -70,64 +71,6 @@ struct Params {
     int64_t sk_units;       // (tiles_total - dp_tiles) * nk
     float2* ws_partial;     // [grid][kThreads * 64] partial accumulators
     unsigned int* ws_flag;  // [grid] partial-ready flags, zeroed before launch
-};
-
-// One unit of a CTA's work: slices [kb, ke) of one tile.  A HEAD item leaves
-// its partial sums in the workspace for the next CTA; a TAIL item starts from
-// the previous CTA's partial sums and finishes the tile.
-enum : int { kFull = 0, kHead = 1, kTail = 2 };
-struct Item { int64_t tile; int kb, ke, mode; };
-
-// The CTA's ordered work list: its data-parallel tiles, then (stream-K) the
-// head of the tile its K range ends in, the whole tiles inside the range, and
-// last the tail of the tile its range starts in.  The head is produced first
-// and the tail consumed last, so a tail's partial is normally long ready.
-struct Schedule {
-    int64_t n_dp, n_items;
-    int64_t full_first, n_full;   // stream-K whole tiles
-    int64_t head_tile, tail_tile;
-    int head_end, tail_begin;     // head: slices [0, head_end); tail: [tail_begin, nk)
-    int has_head, has_tail;
-
-    __device__ __forceinline__ void init(const Params& p) {
-        const int64_t c = blockIdx.x, G = gridDim.x;
-        n_dp = p.dp_tiles > c ? (p.dp_tiles - 1 - c) / G + 1 : 0;
-        has_head = has_tail = 0;
-        n_full = 0;
-        full_first = head_tile = tail_tile = 0;
-        head_end = tail_begin = 0;
-        if (p.sk_units > 0) {
-            const int64_t u0 = c * p.sk_units / G, u1 = (c + 1) * p.sk_units / G;
-            const int64_t t0 = u0 / p.nk, t1 = (u1 - 1) / p.nk;
-            const int s0 = (int)(u0 % p.nk), e1 = (int)((u1 - 1) % p.nk);
-            has_tail = s0 > 0;
-            has_head = e1 < p.nk - 1;
-            tail_tile = p.dp_tiles + t0;
-            tail_begin = s0;
-            head_tile = p.dp_tiles + t1;
-            head_end = e1 + 1;
-            full_first = t0 + has_tail;
-            const int64_t last = t1 - has_head;
-            n_full = last >= full_first ? last - full_first + 1 : 0;
-            full_first += p.dp_tiles;
-        }
-        n_items = n_dp + has_head + n_full + has_tail;
-    }
-
-    __device__ __forceinline__ Item item(const Params& p, int64_t w) const {
-        if (w < n_dp) return {blockIdx.x + w * (int64_t)gridDim.x, 0, p.nk, kFull};
-        w -= n_dp;
-        if (has_head) {
-            if (w == 0) return {head_tile, 0, head_end, kHead};
-            --w;
-        }
-        if (w < n_full) return {full_first + w, 0, p.nk, kFull};
-        return {tail_tile, tail_begin, p.nk, kTail};
-    }
-
-    __device__ __forceinline__ int64_t slices(const Params& p) const {
-        return (n_dp + n_full) * p.nk + (has_head ? head_end : 0) + (has_tail ? p.nk - tail_begin : 0);
-    }
 };
 
 // Copy issuer state (thread 0 only, kept in shared memory so that it costs
@@ -297,7 +240,7 @@ __device__ __forceinline__ void issue_next(typename Cfg<BM, BN, A_K, B_K>::Smem&
                                            const CUtensorMap* tb, const Params& p,
                                            const Schedule& sc, Issuer& is) {
     using C = Cfg<BM, BN, A_K, B_K>;
-    Item itm = sc.item(p, is.w);
+    Item itm = sc.item(is.w, p.nk);
     if (is.kt < itm.kb) is.kt = itm.kb;
     const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
     const int s = (int)(is.issued % C::kStages);
@@ -331,9 +274,6 @@ __device__ __forceinline__ uint64_t in_flight(uint64_t issued, uint32_t consumed
     return (uint64_t)(uint32_t)((uint32_t)issued - consumed);
 }
 
-__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 template <int BM, int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -351,11 +291,11 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     const Schedule& sc = sh.sched;
     Issuer& is = sh.iss;
     if (issuer) {
-        sh.sched.init(p);
+        sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
         is.w = 0;
         is.kt = 0;
         is.issued = 0;
-        is.total = sh.sched.slices(p);
+        is.total = sh.sched.slices(p.nk);
         for (int s = 0; s < S; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], kWarps);
@@ -406,7 +346,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     }
     for (int64_t w = 0; w < n_items; ++w) {
         float2 acc[64];
-        if (sc.item(p, w).mode == kTail) {
+        if (sc.item(w, p.nk).mode == kTail) {
             // Continue the predecessor's FMA chains from its partial sums.
             const float2* src = p.ws_partial + (int64_t)(blockIdx.x - 1) * (kThreads * 64);
             if (issuer) {
@@ -430,7 +370,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
 
         int kt_end;
         {
-            const Item itm = sc.item(p, w);
+            const Item itm = sc.item(w, p.nk);
             kt_end = itm.ke - itm.kb;
         }
         for (int kt = 0; kt < kt_end; ++kt, ++it) {
@@ -526,7 +466,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             }
         }
 
-        const Item itm = sc.item(p, w);
+        const Item itm = sc.item(w, p.nk);
         if (itm.mode == kHead) {
             // Leave the partial sums for the next CTA, then raise its flag once
             // every thread's stores are visible device-wide.
@@ -742,13 +682,9 @@ void tma_ffma_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_by
     plan.ctas = plan.tiles < G ? plan.tiles : G;
     if (!ws || ws_bytes < tma_ffma_workspace_bytes(sm_count)) return;
     if ((reinterpret_cast<uintptr_t>(ws) % 256) != 0) return;
-    if (plan.tiles < G || nk < 8) return;
-    const int64_t full_waves = plan.tiles / G - 1;
-    const int64_t dp = full_waves * G;
-    const int64_t rem_units = (plan.tiles - dp) * nk;
-    const double t_dp = (double)((plan.tiles + G - 1) / G) * nk;
-    const double t_sk = (double)full_waves * nk + (double)((rem_units + G - 1) / G) + 1.0;
-    if (t_sk > 0.97 * t_dp) return;
+    // About 20 us of exchange and reset cost: some 4 slices of a 256 x 128 tile.
+    const int64_t dp = stream_k_dp_tiles(plan.tiles, nk, G, 4);
+    if (dp < 0) return;
     plan.stream_k = true;
     plan.dp_tiles = dp;
     plan.ctas = G;

@@ -78,6 +78,8 @@ unsigned int read_and_clear_wait_status_tma_ffma(cudaStream_t stream);
 // ---- TF32 tensor-core path (tf32_tc.cu) ----------------------------------------
 TmaFfmaConfig tf32_tc_config();
 cudaError_t launch_tf32_tc(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
+// Fills plan.ctas / stream_k / dp_tiles / k_slices for the TF32 kernel.
+void tf32_tc_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws);
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream);
 
 // ---- failure-detection self-test (selftest.cu) ----------------------------------

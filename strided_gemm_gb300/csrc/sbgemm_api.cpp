@@ -225,9 +225,7 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
         plan->tiles_m = (p.M + c.bm - 1) / c.bm;
         plan->tiles_n = (p.N + c.bn - 1) / c.bn;
         plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
-        plan->k_slices = (int)((p.K + c.bk - 1) / c.bk);
-        plan->dp_tiles = plan->tiles;
-        plan->ctas = std::min<int64_t>(plan->tiles, sm_count);
+        tf32_tc_schedule(p, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace);
         return SBGEMM_OK;
     }
 

@@ -15,6 +15,12 @@
 //    column pieces (tcgen05.ld 32x32b.x32), forms alpha*acc (+ C_old) and
 //    stores with masks on ragged M / N, then releases the accumulator, so the
 //    next tile's MMAs overlap this tile's stores.
+// With a workspace the last waves are split along K across the grid (the
+// stream-K work list shared with the FFMA kernel): a head item's accumulator
+// goes to the workspace instead of C, and the epilogue warps seed the TMEM
+// accumulator of a tail item with its predecessor's partial sums (tcgen05.st)
+// before the MMAs continue with accumulation on, so the fp32 accumulation
+// sequence is the data-parallel one.
 // Every mbarrier wait is bounded; a role that gives up records a status code
 // and leaves its loop, the producer then waits (bounded) for the copies it
 // issued, the MMA issuer for its MMAs, and the allocating warp frees TMEM
@@ -29,6 +35,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 namespace sbg {
 namespace {
@@ -42,6 +49,8 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kAccCols = BN;            // fp32 accumulator: one column per n
 constexpr uint32_t kTmemCols = 2 * kAccCols; // double-buffered accumulator
 constexpr int kEpiWarps = 4;
+constexpr int kBM128 = BM;                               // rows of a partial slot
+constexpr int64_t kSlotFloat4 = (int64_t)BM * BN / 4;    // one partial tile, in float4
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 
 __device__ unsigned int g_wait_status = 0;
@@ -56,6 +65,9 @@ struct Params {
     int accumulate;
     int a_bcast, b_bcast;
     int c_vec4;
+    int64_t dp_tiles, sk_units;   // work list (see schedule.cuh)
+    float4* ws_partial;           // [grid][8 chunks][8 quads][128 rows] partial sums
+    unsigned int* ws_flag;        // [grid] partial-ready flags, zeroed before launch
 };
 
 struct Smem {
@@ -66,6 +78,9 @@ struct Smem {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t mma_done;
+    uint64_t seeded[2];       // the epilogue warps wrote a tail's partial into TMEM buffer b
+    uint64_t stored;          // every epilogue thread wrote its head partial
+    Schedule sched;
     uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -94,11 +109,13 @@ __device__ __forceinline__ void producer(Smem& sh, const CUtensorMap* ta, const 
     uint32_t stage = 0, phase = 0;
     uint64_t issued = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < p.tiles_total && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(p, t);
+    const int64_t n_items = sh.sched.n_items;
+    for (int64_t w = 0; w < n_items && ok; ++w) {
+        const Item itm = sh.sched.item(w, p.nk);
+        const TileCoord tc = tile_coord(p, itm.tile);
         const int ba = p.a_bcast ? 0 : (int)tc.b;
         const int bb = p.b_bcast ? 0 : (int)tc.b;
-        for (int kt = 0; kt < p.nk; ++kt) {
+        for (int kt = itm.kb; kt < itm.ke; ++kt) {
             if (issued >= (uint64_t)kStages && !mbar_wait(&sh.empty[stage], phase ^ 1u)) {
                 record_status(&g_wait_status, kWaitEmpty);
                 ok = false;
@@ -122,18 +139,24 @@ __device__ __forceinline__ void producer(Smem& sh, const CUtensorMap* ta, const 
 
 __device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params& p) {
     uint32_t stage = 0, phase = 0;
-    uint64_t local = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < p.tiles_total && ok; t += gridDim.x, ++local) {
-        const uint32_t buf = (uint32_t)(local & 1);
-        const uint64_t use = local >> 1;
+    const int64_t n_items = sh.sched.n_items;
+    for (int64_t w = 0; w < n_items && ok; ++w) {
+        const Item itm = sh.sched.item(w, p.nk);
+        const uint32_t buf = (uint32_t)(w & 1);
+        const uint64_t use = (uint64_t)w >> 1;
         if (use > 0 && !mbar_wait(&sh.acc_empty[buf], (uint32_t)((use - 1) & 1))) {
             record_status(&g_wait_status, kWaitAccFree);
             break;
         }
+        // A tail continues from the partial sums the epilogue seeded.
+        if (itm.mode == kTail && !mbar_wait(&sh.seeded[buf], 0)) {
+            record_status(&g_wait_status, kWaitPartial);
+            break;
+        }
         tc_fence_after();
         const uint32_t d = tmem + buf * kAccCols;
-        for (int kt = 0; kt < p.nk; ++kt) {
+        for (int kt = itm.kb; kt < itm.ke; ++kt) {
             if (!mbar_wait(&sh.full[stage], phase)) {
                 record_status(&g_wait_status, kWaitFull);
                 ok = false;
@@ -146,7 +169,8 @@ __device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params
             for (int kk = 0; kk < BK / kMmaK; ++kk) {
                 const uint64_t ad = umma_desc_kmajor_sw128(a0 + kk * kMmaK * 4);
                 const uint64_t bd = umma_desc_kmajor_sw128(b0 + kk * kMmaK * 4);
-                mma_tf32(d, ad, bd, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                const bool acc = itm.mode == kTail || kt > itm.kb || kk > 0;
+                mma_tf32(d, ad, bd, kIdesc, acc ? 1u : 0u);
             }
             mma_commit(&sh.empty[stage]);
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -159,51 +183,171 @@ __device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params
     if (!mbar_wait(&sh.mma_done, 0)) record_status(&g_wait_status, kWaitMma);
 }
 
+// Partial sums of one 32-column piece of a row: 8 float4 at a stride of 128
+// rows, so a warp's 16-byte accesses cover 512 contiguous bytes.
+__device__ __forceinline__ float4* partial_piece(float4* slot, int c, int row) {
+    return slot + (c * 8) * kBM128 + row;
+}
+
+// Whether the predecessor CTA has published its head partial (warp-uniform,
+// no waiting).  Every lane then takes its own acquire before reading it.
+__device__ __forceinline__ bool pred_partial_ready(const Params& p, int lane) {
+    const unsigned int* flag = p.ws_flag + (blockIdx.x - 1);
+    int up = 0;
+    if (lane == 0) up = ld_acquire_gpu(flag) != 0u;
+    if (!__shfl_sync(0xffffffffu, up, 0)) return false;
+    (void)ld_acquire_gpu(flag);
+    return true;
+}
+
+// Copies the predecessor's partial sums of this thread's row into TMEM buffer
+// `buf` (four 32-column pieces in flight at a time), then tells the MMA lane.
+__device__ __forceinline__ void seed_load(Smem& sh, uint32_t tmem, const Params& p, int quarter,
+                                          int lane, uint32_t buf) {
+    const float4* src = p.ws_partial + (int64_t)(blockIdx.x - 1) * kSlotFloat4;
+    const int row = quarter * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * kAccCols;
+    constexpr int kBatch = 4;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN / 32; c0 += kBatch) {
+        float v[kBatch][32];
+#pragma unroll
+        for (int c = 0; c < kBatch; ++c) {
+            const float4* q = partial_piece(const_cast<float4*>(src), c0 + c, row);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 x = __ldcg(q + j * kBM128);
+                v[c][4 * j] = x.x; v[c][4 * j + 1] = x.y; v[c][4 * j + 2] = x.z; v[c][4 * j + 3] = x.w;
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < kBatch; ++c) tmem_st32(taddr + (c0 + c) * 32, v[c]);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.seeded[buf]);
+}
+
+// Waits (bounded) for the predecessor's partial, then seeds.  False on timeout.
+__device__ __forceinline__ bool seed_tail(Smem& sh, uint32_t tmem, const Params& p, int quarter,
+                                          int lane, uint32_t buf) {
+    int up = 1;
+    if (lane == 0) up = wait_flag(p.ws_flag + (blockIdx.x - 1)) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, up, 0)) return false;
+    (void)ld_acquire_gpu(p.ws_flag + (blockIdx.x - 1));
+    seed_load(sh, tmem, p, quarter, lane, buf);
+    return true;
+}
+
 __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const Params& p, int warp,
                                          int lane) {
     const int quarter = warp & 3;               // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
-    uint64_t local = 0;
-    for (int64_t t = blockIdx.x; t < p.tiles_total; t += gridDim.x, ++local) {
-        const uint32_t buf = (uint32_t)(local & 1);
-        if (!mbar_wait(&sh.acc_full[buf], (uint32_t)((local >> 1) & 1))) {
+    const int64_t n_items = sh.sched.n_items;
+    if (n_items > 0 && sh.sched.item(0, p.nk).mode == kTail &&
+        !seed_tail(sh, tmem, p, quarter, lane, 0)) {
+        record_status(&g_wait_status, kWaitPartial);
+        return;
+    }
+    for (int64_t w = 0; w < n_items; ++w) {
+        const Item itm = sh.sched.item(w, p.nk);
+        const uint32_t buf = (uint32_t)(w & 1);
+        // Seed the next item if it is a tail (its buffer was freed by item w-1),
+        // so its MMAs can start while this item drains.  After a head, the
+        // seeding waits until the head's own partial is published: a CTA
+        // that waited on its predecessor first would chain every CTA's head
+        // behind the one before it.
+        const bool next_tail = w + 1 < n_items && sh.sched.item(w + 1, p.nk).mode == kTail;
+        const uint32_t acc_parity = (uint32_t)((w >> 1) & 1);
+        bool next_seeded = false;
+        if (next_tail && itm.mode != kHead) {
+            if (!seed_tail(sh, tmem, p, quarter, lane, buf ^ 1u)) {
+                record_status(&g_wait_status, kWaitPartial);
+                return;
+            }
+            next_seeded = true;
+        } else if (next_tail) {
+            // Seed early if the predecessor's partial is already out, else
+            // after this head is published (whichever comes first).
+            const uint64_t t0 = global_timer_ns();
+            while (true) {
+                int done = mbar_try_wait(&sh.acc_full[buf], acc_parity) ? 1 : 0;
+                if (__shfl_sync(0xffffffffu, done, 0)) break;
+                if (pred_partial_ready(p, lane)) {
+                    seed_load(sh, tmem, p, quarter, lane, buf ^ 1u);
+                    next_seeded = true;
+                    break;
+                }
+                if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                    record_status(&g_wait_status, kWaitMma);
+                    return;
+                }
+            }
+        }
+        if (!mbar_wait(&sh.acc_full[buf], acc_parity)) {
             record_status(&g_wait_status, kWaitMma);
             return;
         }
         tc_fence_after();
-        const TileCoord tc = tile_coord(p, t);
-        const int64_t m = tc.m0 + row;
-        const bool row_ok = m < p.M;
-        float* crow = p.C + tc.b * p.bsC + (row_ok ? m : 0) * p.rsC;
         const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * kAccCols;
+        if (itm.mode == kHead) {
+            // Partial sums to the workspace, then the successor's flag once every
+            // epilogue thread's stores are visible device-wide.
+            float4* dst = p.ws_partial + (int64_t)blockIdx.x * kSlotFloat4;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            __syncwarp();
-            tmem_ld32(taddr + c * 32, v);      // whole warp, converged, every row
-            const int64_t n0 = tc.n0 + c * 32;
-            if (!row_ok || n0 >= p.N) {
-                // nothing of this piece is in C
-            } else if (p.c_vec4 && n0 + 32 <= p.N) {
-                float4* cp = reinterpret_cast<float4*>(crow + n0);
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                __syncwarp();
+                tmem_ld32(taddr + c * 32, v);
+                float4* q = partial_piece(dst, c, row);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (p.accumulate) o = cp[q];
-                    float4 r;
-                    r.x = p.accumulate ? fmaf(p.alpha, v[4 * q + 0], o.x) : p.alpha * v[4 * q + 0];
-                    r.y = p.accumulate ? fmaf(p.alpha, v[4 * q + 1], o.y) : p.alpha * v[4 * q + 1];
-                    r.z = p.accumulate ? fmaf(p.alpha, v[4 * q + 2], o.z) : p.alpha * v[4 * q + 2];
-                    r.w = p.accumulate ? fmaf(p.alpha, v[4 * q + 3], o.w) : p.alpha * v[4 * q + 3];
-                    cp[q] = r;
+                for (int j = 0; j < 8; ++j)
+                    __stcg(q + j * kBM128, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            }
+            __threadfence();
+            mbar_arrive(&sh.stored);
+            if (warp == 2 && lane == 0) {
+                if (!mbar_wait(&sh.stored, 0)) {
+                    record_status(&g_wait_status, kWaitPartial);
+                    return;
                 }
-            } else {
+                st_release_gpu(p.ws_flag + blockIdx.x, 1u);
+            }
+        } else {
+            const TileCoord tc = tile_coord(p, itm.tile);
+            const int64_t m = tc.m0 + row;
+            const bool row_ok = m < p.M;
+            float* crow = p.C + tc.b * p.bsC + (row_ok ? m : 0) * p.rsC;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                __syncwarp();
+                tmem_ld32(taddr + c * 32, v);      // whole warp, converged, every row
+                const int64_t n0 = tc.n0 + c * 32;
+                if (!row_ok || n0 >= p.N) {
+                    // nothing of this piece is in C
+                } else if (p.c_vec4 && n0 + 32 <= p.N) {
+                    float4* cp = reinterpret_cast<float4*>(crow + n0);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int64_t n = n0 + e;
-                    if (n < p.N) {
-                        float* cptr = crow + n * p.csC;
-                        *cptr = p.accumulate ? fmaf(p.alpha, v[e], *cptr) : p.alpha * v[e];
+                    for (int q = 0; q < 8; ++q) {
+                        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (p.accumulate) o = cp[q];
+                        float4 r;
+                        r.x = p.accumulate ? fmaf(p.alpha, v[4 * q + 0], o.x) : p.alpha * v[4 * q + 0];
+                        r.y = p.accumulate ? fmaf(p.alpha, v[4 * q + 1], o.y) : p.alpha * v[4 * q + 1];
+                        r.z = p.accumulate ? fmaf(p.alpha, v[4 * q + 2], o.z) : p.alpha * v[4 * q + 2];
+                        r.w = p.accumulate ? fmaf(p.alpha, v[4 * q + 3], o.w) : p.alpha * v[4 * q + 3];
+                        cp[q] = r;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int64_t n = n0 + e;
+                        if (n < p.N) {
+                            float* cptr = crow + n * p.csC;
+                            *cptr = p.accumulate ? fmaf(p.alpha, v[e], *cptr) : p.alpha * v[e];
+                        }
                     }
                 }
             }
@@ -211,6 +355,10 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const Params& 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_empty[buf]);
+        if (next_tail && !next_seeded && !seed_tail(sh, tmem, p, quarter, lane, buf ^ 1u)) {
+            record_status(&g_wait_status, kWaitPartial);
+            return;
+        }
     }
 }
 
@@ -231,6 +379,10 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             mbar_init(&sh.acc_empty[b], kEpiWarps);
         }
         mbar_init(&sh.mma_done, 1);
+        mbar_init(&sh.seeded[0], kEpiWarps);
+        mbar_init(&sh.seeded[1], kEpiWarps);
+        mbar_init(&sh.stored, kEpiWarps * 32);
+        sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
         fence_mbar_init();
         prefetch_tensormap(&ta);
         prefetch_tensormap(&tb);
@@ -304,9 +456,56 @@ cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cu
     p.b_bcast = b_bc;
     p.c_vec4 = pr.csC == 1 && (reinterpret_cast<uintptr_t>(pr.C) % 16 == 0) &&
                (pr.M == 1 || pr.rsC % 4 == 0) && (pr.batch == 1 || pr.bsC % 4 == 0);
-    const int64_t grid = plan.tiles < (int64_t)sm_count ? plan.tiles : (int64_t)sm_count;
+    const int64_t grid = plan.ctas;
+    p.dp_tiles = plan.stream_k ? plan.dp_tiles : plan.tiles;
+    p.sk_units = plan.stream_k ? (plan.tiles - plan.dp_tiles) * p.nk : 0;
+    p.ws_partial = nullptr;
+    p.ws_flag = nullptr;
+    if (plan.stream_k) {
+        p.ws_partial = static_cast<float4*>(plan.workspace);
+        p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<char*>(plan.workspace) +
+                                                    (size_t)grid * kSlotFloat4 * sizeof(float4));
+        cudaError_t e = cudaMemsetAsync(p.ws_flag, 0, (size_t)grid * sizeof(unsigned int), stream);
+        if (e != cudaSuccess) return e;
+        // CTAs wait on one another's partial sums: make them co-resident.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel, ta, tb, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     tf32_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(ta, tb, p);
     return cudaGetLastError();
+}
+
+// Same rule as the FFMA path (stream_k_dp_tiles), with the tensor cores' own
+// exchange cost.
+void tf32_tc_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_bytes, const void* ws) {
+    const int64_t nk = (pr.K + BK - 1) / BK;
+    const int64_t G = sm_count;
+    plan.k_slices = (int)nk;
+    plan.stream_k = false;
+    plan.dp_tiles = plan.tiles;
+    plan.ctas = plan.tiles < G ? plan.tiles : G;
+    const size_t need = (size_t)G * (size_t)kSlotFloat4 * sizeof(float4) + (size_t)G * sizeof(unsigned int);
+    if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 256) != 0) return;
+    // Tensor-core slices are short (about 0.4 us for 128 x 256 x 32), so the
+    // 15-20 us of exchange and reset cost counts as about 48 slices: only
+    // long-K problems gain.
+    const int64_t dp = stream_k_dp_tiles(plan.tiles, nk, G, 48);
+    if (dp < 0) return;
+    plan.stream_k = true;
+    plan.dp_tiles = dp;
+    plan.ctas = G;
+    plan.workspace = const_cast<void*>(ws);
 }
 
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream) {

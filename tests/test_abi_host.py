@@ -198,3 +198,24 @@ def test_stream_k_planning():
                        rowmajor(BASE + (2 << 32), 4096, 4096, 1), 4096, 4096, 64, 1,
                        workspace=ws, workspace_bytes=big)
     assert not shortk["stream_k"]
+
+
+def test_tf32_stream_k_planning():
+    """The tensor-core path splits its last waves by the same rule, charged
+    with its own exchange cost: long K splits, K = 1024 stays data-parallel.
+    Its tiles are 128 x 256 with 32-wide K slices."""
+    ws = BASE + (8 << 32)
+    big = 1 << 30
+    M, N = 2048, 5120
+    for K, split in ((4096, True), (1024, False)):
+        A = rowmajor(BASE, M, K, 1)
+        B = (BASE + (1 << 32), 1, K, 0)                 # column-major: K-major
+        C = rowmajor(BASE + (2 << 32), M, N, 1)
+        p0 = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32)
+        assert p0["path"] == sg.PATH_TMA_TF32 and not p0["stream_k"]
+        assert (p0["tile_m"], p0["tile_n"], p0["tile_k"]) == (128, 256, 32)
+        p1 = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32, workspace=ws, workspace_bytes=big)
+        assert p1["path"] == sg.PATH_TMA_TF32 and p1["stream_k"] == split
+        assert p1["tiles"] == 320 and p1["k_slices"] == K // 32
+        if split:
+            assert p1["ctas"] == 152 and p1["dp_tiles"] == 152

@@ -230,6 +230,7 @@ def _run_ws(case, torch, ws, entry_kw=None):
             dC.data_ptr() + 4 * case.C.offset, case.C.rs, case.C.cs, case.C.bs,
             case.M, case.N, case.K, case.batch, case.alpha, case.accumulate,
             torch.cuda.current_stream().cuda_stream)
+    kw.update(entry_kw or {})
     plan = sg.sbgemm_plan(*args[:16], case.accumulate, **kw)
     sg.sbgemm_ex(*args, **kw)
     torch.cuda.synchronize()
@@ -323,6 +324,49 @@ def test_tf32_opt_in_falls_back_to_fp32(torch):
         assert not _supported(c, sg.MATH_TF32, sg.PATH_TMA_TF32)
         got = gu.run_case(c, torch, math=sg.MATH_TF32)
         gu.check_full(c, got)
+
+
+TF32_STREAM_K_SHAPES = [
+    # (name, M, N, K, batch, accumulate); A row-major and B column-major (K-major).
+    # Long K: the tensor cores split tiles only when that outweighs the exchange.
+    ("160_tiles", 2048, 2560, 4096, 1, 0),
+    ("ragged_k", 2560, 2560, 4000, 1, 1),
+    ("batched", 1024, 1024, 4096, 5, 1),
+]
+
+
+@pytest.mark.parametrize("shape", TF32_STREAM_K_SHAPES, ids=[s[0] for s in TF32_STREAM_K_SHAPES])
+def test_tf32_stream_k_bitwise_equals_data_parallel(torch, workspace, shape):
+    """On the tensor cores a split tile's head parks its accumulator in the
+    workspace and the tail loads it back into tensor memory before its first
+    MMA, so the k-ordered accumulation chain is the data-parallel one."""
+    _, M, N, K, batch, acc = shape
+    rng = np.random.default_rng(M * 3 + N + K)
+    case = wl.random_strided(rng, M, N, K, batch, "row16", "col16", values="real",
+                             accumulate=acc, alpha=0.75)
+    kw = dict(math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
+    dp, plan_dp = _run_ws(case, torch, None, kw)
+    sk, plan_sk = _run_ws(case, torch, workspace, kw)
+    assert plan_sk["path"] == sg.PATH_TMA_TF32
+    assert not plan_dp["stream_k"] and plan_sk["stream_k"], (plan_dp, plan_sk)
+    assert np.array_equal(dp, sk)
+    gu.check_points(case, sk, n=4000, tol=gu.TOL_TF32)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
+def test_tf32_stream_k_integer_exact(torch, workspace):
+    """Small integers are exact in TF32, so the split schedule must give the
+    exact product; repeated calls reuse the workspace flags."""
+    rng = np.random.default_rng(5)
+    case = wl.random_strided(rng, 2048, 2560, 4096, 1, "row16", "col16", values="int")
+    kw = dict(math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
+    first, plan = _run_ws(case, torch, workspace, kw)
+    assert plan["stream_k"]
+    for _ in range(2):
+        again, _ = _run_ws(case, torch, workspace, kw)
+        assert np.array_equal(again, first)
+    gu.check_points(case, first, n=4000, exact=True)
 
 
 @pytest.mark.parametrize("name", ["c3", "c3gqa", "c5a", "c5b"])
