@@ -270,3 +270,62 @@ def test_spans_outside_storage_are_refused():
     with pytest.raises(ValueError):
         oracle.product(wl.Operand(a, 0, 3, 1, 0), wl.Operand(a, 0, 3, 1, 0),
                        wl.Operand(a, 0, 3, 1, 0), 3, 3, 3, 1, 1.0, 0)
+
+
+def test_backward_layouts_are_the_linear_layer_gradients():
+    """Pins the backward workloads' layouts (G read transposed through swapped
+    strides for dW; W read as stored for dX) to the definition of a gradient.
+    For L(X, W) = sum(G * (X W^T)) with integer entries, L is linear in W and in
+    X, so dL/dW[i, j] = L(W + E_ij) - L(W) and dL/dX[t, j] = L(X + E_tj) - L(X)
+    exactly in int64, with no product routine involved ("PyTorch demystified
+    3", section "Opt. 3 - Speed up matmul in the backward block through kernel
+    fusion": dA = G B^T, dB = A^T G)."""
+    rng = np.random.default_rng(11)
+    T, d_in, d_out = 7, 5, 6
+    X = rng.integers(-8, 9, size=(T, d_in)).astype(np.int64)
+    W = rng.integers(-8, 9, size=(d_out, d_in)).astype(np.int64)
+    G = rng.integers(-8, 9, size=(T, d_out)).astype(np.int64)
+
+    def loss(X, W):
+        total = 0
+        for t in range(T):
+            for o in range(d_out):
+                y = 0
+                for i in range(d_in):
+                    y += int(X[t, i]) * int(W[o, i])
+                total += int(G[t, o]) * y
+        return total
+
+    base = loss(X, W)
+    want_dW = np.zeros((d_out, d_in), dtype=np.int64)
+    for o in range(d_out):
+        for i in range(d_in):
+            W2 = W.copy(); W2[o, i] += 1
+            want_dW[o, i] = loss(X, W2) - base
+    want_dX = np.zeros((T, d_in), dtype=np.int64)
+    for t in range(T):
+        for i in range(d_in):
+            X2 = X.copy(); X2[t, i] += 1
+            want_dX[t, i] = loss(X2, W) - base
+
+    f32 = lambda a: np.ascontiguousarray(a, dtype=np.float32).reshape(-1)
+    zeros = lambda n: np.zeros(n, dtype=np.float32)
+    # dW = G^T X: A[m][k] = G[k][m] (rsA = 1, csA = d_out), B = X row-major.
+    ref, _ = oracle.product(wl.Operand(f32(G), 0, 1, d_out, 0), wl.Operand(f32(X), 0, d_in, 1, 0),
+                            wl.Operand(zeros(d_out * d_in), 0, d_in, 1, 0),
+                            d_out, d_in, T, 1, 1.0, 0)
+    assert np.array_equal(ref[0], want_dW.astype(np.float64))
+    # dX = G W: A = G row-major, B[k][n] = W[k][n] read as stored.
+    ref, _ = oracle.product(wl.Operand(f32(G), 0, d_out, 1, 0), wl.Operand(f32(W), 0, d_in, 1, 0),
+                            wl.Operand(zeros(T * d_in), 0, d_in, 1, 0),
+                            T, d_in, d_out, 1, 1.0, 0)
+    assert np.array_equal(ref[0], want_dX.astype(np.float64))
+    # The workloads' own dW layout, shrunk: same definition through make().
+    case = wl.make("f1dwa", "int", M=6, N=5, K=7)
+    Gs = case.A.storage.reshape(7, 6).astype(np.int64)    # stored [T, out]
+    Xs = case.B.storage.reshape(7, 5).astype(np.int64)    # stored [T, in]
+    C0 = case.C.storage.reshape(6, 5).astype(np.int64)
+    ref, _ = oracle.case_product(case)
+    want = C0 + np.array([[sum(int(Gs[t, o]) * int(Xs[t, i]) for t in range(7))
+                           for i in range(5)] for o in range(6)])
+    assert np.array_equal(ref[0], want.astype(np.float64))

@@ -21,6 +21,15 @@ and attention shapes of "rvllm CUDA path", section "Matmuls go to cuBLAS"):
   c5c     4096^3, row-major, accumulate
   c5d     4096^3, A and B both read transposed by swapped strides, accumulate
 
+and the backward products of the two projection layers (dX = G W, dW = G^T X for
+Y = X W^T; "PyTorch demystified 3", section "Opt. 3 - Speed up matmul in the
+backward block through kernel fusion"), transposes read through strides:
+
+  f1dxa   dX of c5a's layer: G [8192,2560] . W [2560,960] (W read as stored)
+  f1dwa   dW of c5a's layer: G^T [2560,8192] . X [8192,960], accumulate into dW
+  f1dxb   dX of c5b's layer: G [8192,960] . W [960,2560]
+  f1dwb   dW of c5b's layer: G^T [960,8192] . X [8192,2560], accumulate into dW
+
 Every workload also has an integer pass (values uniform in {-8..8}) in which
 every partial sum is an exact fp32 integer.
 """
@@ -32,7 +41,7 @@ from typing import Dict, Optional, Tuple
 
 import numpy as np
 
-__all__ = ["Operand", "Case", "WORKLOADS", "make", "flops", "gflops_per_s",
+__all__ = ["Operand", "Case", "WORKLOADS", "BACKWARD", "make", "flops", "gflops_per_s",
            "alg_bytes", "SEEDS"]
 
 
@@ -107,10 +116,12 @@ def alg_bytes(case: "Case") -> int:
 # Seeds follow the order of the workload list: c1 = 0 (as the problem states),
 # c2 = 1, c3 = 2, c4 = 3, c5 = 4.
 SEEDS = {"c1": 0, "c2a": 1, "c2b": 1, "c3": 2, "c3gqa": 2, "c4": 3,
-         "c5a": 4, "c5b": 4, "c5c": 4, "c5d": 4}
+         "c5a": 4, "c5b": 4, "c5c": 4, "c5d": 4,
+         "f1dxa": 5, "f1dwa": 5, "f1dxb": 5, "f1dwb": 5}
 # Sub-stream per workload sharing a seed, so c2a and c2b draw different values.
 _STREAM = {"c1": 0, "c2a": 0, "c2b": 1, "c3": 0, "c3gqa": 1, "c4": 0,
-           "c5a": 0, "c5b": 1, "c5c": 2, "c5d": 2}
+           "c5a": 0, "c5b": 1, "c5c": 2, "c5d": 2,
+           "f1dxa": 0, "f1dwa": 1, "f1dxb": 2, "f1dwb": 3}
 
 # Full-size shapes.  Keys that a caller may override to shrink a case for the
 # oracle: batch, M, N, K (and heads/seqs for the attention cases).
@@ -125,8 +136,13 @@ FULL: Dict[str, Dict[str, int]] = {
     "c5b": dict(batch=1, M=8192, N=960, K=2560),
     "c5c": dict(batch=1, M=4096, N=4096, K=4096),
     "c5d": dict(batch=1, M=4096, N=4096, K=4096),
+    "f1dxa": dict(batch=1, M=8192, N=960, K=2560),
+    "f1dwa": dict(batch=1, M=2560, N=960, K=8192),
+    "f1dxb": dict(batch=1, M=8192, N=2560, K=960),
+    "f1dwb": dict(batch=1, M=960, N=2560, K=8192),
 }
 WORKLOADS = tuple(FULL)
+BACKWARD = ("f1dxa", "f1dwa", "f1dxb", "f1dwb")
 
 
 def _rng(name: str, values: str) -> np.random.Generator:
@@ -264,6 +280,28 @@ def make(name: str, values: str = "real", **shape) -> Case:
         return Case(name, A, B, Operand(_flat(c0), 0, N, 1, M * N),
                     M, N, K, batch, 1.0, 1, values, note)
 
+    if name in ("f1dxa", "f1dxb"):
+        # dX [T, in] = G [T, out] . W [out, in]: M = T, K = out, N = in.
+        g = draw("n", (M, K), 1.0)
+        w = draw("n", (K, N), 0.02)
+        return Case(name, Operand(_flat(g), 0, K, 1, M * K),
+                    Operand(_flat(w), 0, N, 1, K * N),
+                    Operand(empty_c(), 0, N, 1, M * N),
+                    M, N, K, batch, 1.0, 0, values,
+                    "input gradient, W [out,in] read as stored (N-major)")
+
+    if name in ("f1dwa", "f1dwb"):
+        # dW [out, in] += G^T . X: M = out, K = T, N = in.  G is stored [T, out]
+        # and read transposed: A[m][k] = G[k][m], rsA = 1, csA = out.
+        g = draw("n", (K, M), 1.0)
+        x = draw("n", (K, N), 1.0)
+        c0 = draw("n", (M, N), 0.01)
+        return Case(name, Operand(_flat(g), 0, 1, M, M * K),
+                    Operand(_flat(x), 0, N, 1, K * N),
+                    Operand(_flat(c0), 0, N, 1, M * N),
+                    M, N, K, batch, 1.0, 1, values,
+                    "weight gradient, G read transposed by swapped strides, accumulate")
+
     raise AssertionError(name)
 
 
@@ -281,6 +319,10 @@ def small_shape(name: str) -> Dict[str, int]:
         "c5b": dict(batch=1, M=300, N=960, K=2560),
         "c5c": dict(batch=1, M=260, N=1028, K=1024),
         "c5d": dict(batch=1, M=260, N=1028, K=1024),
+        "f1dxa": dict(batch=1, M=300, N=960, K=2560),
+        "f1dwa": dict(batch=1, M=260, N=300, K=2052),
+        "f1dxb": dict(batch=1, M=300, N=1028, K=960),
+        "f1dwb": dict(batch=1, M=300, N=260, K=2052),
     }[name]
 
 
