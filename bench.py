@@ -44,10 +44,13 @@ TF32_OVER_BF16_NOMINAL = 1.1 / 2.25  # dense nominal tf32 / bf16 tensor rates
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "sm_max_mhz": 2070.0}
 
-SWEEPS = {"c5": ["c5a", "c5b", "c5c", "c5d"], "c3all": ["c3", "c3gqa"]}
+SWEEPS = {"c5": ["c5a", "c5b", "c5c", "c5d"], "c3all": ["c3", "c3gqa"],
+          "f1": list(wl.BACKWARD)}
 DESCR = {
     "c5": "large projection sweep: 8192x960->2560 (W^T), 8192x2560->960 (W^T), "
           "4096^3 row-major +C, 4096^3 A^T B^T +C",
+    "f1": "backward products of the two projection layers: dX = G W (8192x960x2560, "
+          "8192x2560x960), dW += G^T X (2560x960x8192, 960x2560x8192)",
 }
 
 
@@ -189,8 +192,9 @@ def case_args(case, dA, dB, dC):
 
 
 def kernel_source_digest(path_name):
-    files = {"gather_ffma": ["ffma_gather.cu"], "tma_ffma": ["ffma_tma.cu"],
-             "tma_tf32": ["tf32_tc.cu"]}.get(path_name, [])
+    files = {"gather_ffma": ["ffma_gather.cu"],
+             "tma_ffma": ["ffma_tma.cu", "schedule.cuh", "ptx.cuh"],
+             "tma_tf32": ["tf32_tc.cu", "schedule.cuh", "ptx.cuh"]}.get(path_name, [])
     h = hashlib.sha256()
     for f in files:
         p = os.path.join(ROOT, "strided_gemm_gb300", "csrc", f)
@@ -456,6 +460,51 @@ def run_ours(args, world, rank, local, dist):
                                                f"ratio {TF32_OVER_BF16_NOMINAL:.3f}",
                                 "traffic": profiled_traffic("tma_tf32", n)}
 
+    # Backward products of the same layers (dX = G W, dW += G^T X), each with
+    # the step's workspace and without it: the long-K weight gradients have
+    # fewer tiles than SMs and are split into independent K pieces.
+    backward = None
+    if not args.no_backward and args.workload == "c5" and math == sg.MATH_FP32:
+        backward = {"per_product": {}}
+        reps = max(3, min(args.steps, 10))
+        for n in wl.BACKWARD:
+            c = wl.make(n, "real")
+            bufs = tuple(torch.from_numpy(x).to(dev) for x in (c.A.storage, c.B.storage, c.C.storage))
+            a = case_args(c, *bufs)
+            row = {}
+            for label, kw in (("workspace", ws_kw), ("no_workspace", {})):
+                if label == "workspace" and not kw:
+                    continue
+                pl = sg.sbgemm_plan(*a[:16], c.accumulate, **kw)
+                for _ in range(3):
+                    sg.sbgemm_ex(*a, s_handle, **kw)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(reps):
+                    sg.sbgemm_ex(*a, s_handle, **kw)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / reps
+                row[label] = {"ms": round(ms, 4), "gflops": round(c.flops / ms / 1e6, 1),
+                              "path": pl["path_name"],
+                              "stream_k": {0: "none", 1: "chained", 2: "pieces"}[pl["stream_k"]],
+                              "ctas": pl["ctas"]}
+            backward["per_product"][n] = row
+            del bufs
+        key = "workspace" if ws_kw else "no_workspace"
+        tot_ms = sum(r[key]["ms"] for r in backward["per_product"].values())
+        tot_fl = sum(2 * wl.FULL[n]["batch"] * wl.FULL[n]["M"] * wl.FULL[n]["N"] * wl.FULL[n]["K"]
+                     for n in wl.BACKWARD)
+        backward["gflops"] = round(tot_fl / tot_ms / 1e6, 1)
+        slow = max(backward["per_product"], key=lambda n: backward["per_product"][n][key]["ms"])
+        ach = backward["per_product"][slow][key]["gflops"] / 1e3
+        fp32_peak = sms * FP32_FLOP_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
+        backward["roofline"] = {"bound": "alu", "kernel": f"tma_ffma ({slow})",
+                                "achieved": round(ach, 2), "peak": round(fp32_peak, 2),
+                                "unit": "TFLOP/s", "frac": round(ach / fp32_peak, 4),
+                                "traffic": profiled_traffic("tma_ffma", slow)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -488,6 +537,7 @@ def run_ours(args, world, rank, local, dist):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "tf32": tf32,
+        "backward": backward,
         "gpu_launches": len(calls) * args.steps,
         "clocks": clocks,
         "per_product": {n: {k: v for k, v in d.items() if k != "total_ms"} for n, d in per.items()},
@@ -545,6 +595,8 @@ def main(argv=None):
                     help="force one kernel path for the timed products")
     ap.add_argument("--no-tf32", action="store_true",
                     help="skip the opt-in tensor-core measurement")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward-product measurement")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
     world, rank, local = dist_env()

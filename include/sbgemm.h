@@ -109,6 +109,34 @@ enum {
     SBGEMM_LAYOUT_GENERAL = 2    /* no unit stride */
 };
 
+/* How the planner may split a tile's K range across CTAs when a workspace is
+ * given; sbgemm_options.k_split.  The split follows the work-list scheme of
+ * persistent CTAs, and its partial sums are added in a fixed order, so every
+ * choice is deterministic from run to run (the pages' "Chapter 09 CUDA
+ * backend", section "Reductions", for device sums; "GPU Implementation",
+ * section "Making the embedding gradient repeatable", for gradients). */
+enum {
+    SBGEMM_KSPLIT_ANY = 0,    /* default: chained stream-K over the last waves,
+                                 or, with fewer tiles than SMs and long K
+                                 (e.g. the weight gradient Gt*X), independent K
+                                 pieces summed in a fixed order; the latter
+                                 rounds differently from the unsplit product */
+    SBGEMM_KSPLIT_EXACT = 1,  /* only splits whose result is bit-identical to
+                                 the unsplit schedule (chained stream-K) */
+    SBGEMM_KSPLIT_NONE = 2    /* never split K */
+};
+
+/* sbgemm_plan_info.stream_k. */
+enum {
+    SBGEMM_STREAM_K_NONE = 0,     /* every tile computed whole by one CTA */
+    SBGEMM_STREAM_K_CHAINED = 1,  /* last waves split; a tail continues its
+                                     head's k-ordered accumulation, so results
+                                     do not change */
+    SBGEMM_STREAM_K_PIECES = 2    /* all tiles split into independent K pieces
+                                     over the SMs, the tail adding the earlier
+                                     pieces' partial sums latest first */
+};
+
 typedef struct {
     int math;          /* SBGEMM_MATH_* */
     int force_path;    /* SBGEMM_PATH_AUTO or a specific path */
@@ -119,7 +147,8 @@ typedef struct {
                           library writes it on `stream` during the call; calls
                           that may run concurrently need separate workspaces. */
     size_t workspace_bytes;
-    int reserved[2];   /* must be zero */
+    int k_split;       /* SBGEMM_KSPLIT_*; 0 = any */
+    int reserved[1];   /* must be zero */
 } sbgemm_options;
 
 typedef struct {
@@ -131,9 +160,8 @@ typedef struct {
     int ctas_per_sm;          /* resident CTAs per SM the plan assumes */
     int64_t ctas;             /* CTAs launched (0 when path == NONE) */
     int64_t tiles;            /* output tiles over all batch entries */
-    int stream_k;             /* 1: the last waves are split along K (needs a
-                                 workspace); each split tile continues one
-                                 k-ordered FMA chain, so results do not change */
+    int stream_k;             /* SBGEMM_STREAM_K_*: how tiles are split along K
+                                 (needs a workspace) */
     int k_slices;             /* K slices (tile_k deep) per tile */
     int64_t dp_tiles;         /* tiles computed whole, data-parallel */
     int reserved[4];

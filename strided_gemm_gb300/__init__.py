@@ -50,6 +50,8 @@ EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_workspace_byte
                     "sbgemm_noalloc", "sbgemm_selftest", "sbgemm_device_status",
                     "sbgemm_status_string", "sbgemm_version")
 SELFTEST_MBARRIER, SELFTEST_FLAG = 1, 2
+KSPLIT_ANY, KSPLIT_EXACT, KSPLIT_NONE = 0, 1, 2
+STREAM_K_NONE, STREAM_K_CHAINED, STREAM_K_PIECES = 0, 1, 2
 
 
 class SbgemmError(RuntimeError):
@@ -61,7 +63,7 @@ class SbgemmError(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("math", ctypes.c_int), ("force_path", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("reserved", ctypes.c_int * 2)]
+                ("k_split", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
 
 
 class _PlanInfo(ctypes.Structure):
@@ -119,12 +121,13 @@ def load(path: str = LIB_PATH):
         return lib
 
 
-def _opts(math: int, force_path: int, workspace=0, workspace_bytes=0):
+def _opts(math: int, force_path: int, workspace=0, workspace_bytes=0, k_split=KSPLIT_ANY):
     o = _Options()
     o.math = int(math)
     o.force_path = int(force_path)
     o.workspace = int(workspace) or None
     o.workspace_bytes = int(workspace_bytes)
+    o.k_split = int(k_split)
     return o
 
 
@@ -168,8 +171,8 @@ def sbgemm_noalloc(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
 def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
               M, N, K, batch, alpha, accumulate, stream=0,
               math: int = MATH_FP32, force_path: int = PATH_AUTO,
-              workspace: int = 0, workspace_bytes: int = 0) -> None:
-    o = _opts(math, force_path, workspace, workspace_bytes)
+              workspace: int = 0, workspace_bytes: int = 0, k_split: int = KSPLIT_ANY) -> None:
+    o = _opts(math, force_path, workspace, workspace_bytes, k_split)
     st = load().sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                           M, N, K, batch, float(alpha), int(bool(accumulate)),
                           stream or None, ctypes.byref(o))
@@ -180,9 +183,9 @@ def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
 def sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                 M, N, K, batch, accumulate=0, math: int = MATH_FP32,
                 force_path: int = PATH_AUTO, workspace: int = 0,
-                workspace_bytes: int = 0) -> dict:
+                workspace_bytes: int = 0, k_split: int = KSPLIT_ANY) -> dict:
     """Validate and plan without launching; returns the plan as a dict."""
-    o = _opts(math, force_path, workspace, workspace_bytes)
+    o = _opts(math, force_path, workspace, workspace_bytes, k_split)
     info = _PlanInfo()
     st = load().sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                             M, N, K, batch, int(bool(accumulate)), ctypes.byref(o),
@@ -219,7 +222,7 @@ def _as3(t, name):
 
 def matmul(A, B, C, alpha: float = 1.0, accumulate: bool = False,
            math: int = MATH_FP32, force_path: int = PATH_AUTO, stream=None,
-           workspace=None):
+           workspace=None, k_split: int = KSPLIT_ANY):
     """C <- alpha*A@B (+C) on torch CUDA float32 tensors viewed as [batch, M, K],
     [batch, K, N] and [batch, M, N] (2-D means batch 1).  Strides are taken from
     the tensors, so transposed or expanded views need no copy.  Returns C."""
@@ -245,5 +248,23 @@ def matmul(A, B, C, alpha: float = 1.0, accumulate: bool = False,
     sbgemm_ex(A3.data_ptr(), A3.stride(1), A3.stride(2), bsA,
               B3.data_ptr(), B3.stride(1), B3.stride(2), bsB,
               C3.data_ptr(), C3.stride(1), C3.stride(2), C3.stride(0),
-              M, N, K, batch, alpha, accumulate, stream, math, force_path, ws, ws_bytes)
+              M, N, K, batch, alpha, accumulate, stream, math, force_path, ws, ws_bytes, k_split)
     return C
+
+
+def linear_backward(G, X, W, dX, dW, accumulate_dW: bool = False, stream=None,
+                    workspace=None, k_split: int = KSPLIT_ANY):
+    """Gradients of the linear layer Y = X W^T (X [T, in], W [out, in], upstream
+    gradient G = dL/dY [T, out]), as two strided products that read the
+    transposes through swapped strides, with no copy (the pages' "PyTorch
+    demystified 3", section "Opt. 3 - Speed up matmul in the backward block
+    through kernel fusion"):
+        dX = G W        [T, in]   (B = W read row-major, N-major)
+        dW = G^T X      [out, in] (A = G read with swapped strides; K = T)
+    dW accumulates into the existing gradient when accumulate_dW is set.  With
+    a workspace the long-K dW product may be split into independent K pieces
+    (deterministic; k_split = KSPLIT_EXACT keeps the unsplit rounding)."""
+    matmul(G, W, dX, stream=stream, workspace=workspace, k_split=k_split)
+    matmul(G.t(), X, dW, accumulate=accumulate_dW, stream=stream, workspace=workspace,
+           k_split=k_split)
+    return dX, dW

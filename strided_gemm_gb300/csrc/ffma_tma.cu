@@ -69,6 +69,7 @@ struct Params {
     // the grid (stream-K) when sk_units > 0.
     int64_t dp_tiles;
     int64_t sk_units;       // (tiles_total - dp_tiles) * nk
+    int indep;              // split tiles as independent pieces (schedule.cuh)
     float2* ws_partial;     // [grid][kThreads * 64] partial accumulators
     unsigned int* ws_flag;  // [grid] partial-ready flags, zeroed before launch
 };
@@ -346,7 +347,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     }
     for (int64_t w = 0; w < n_items; ++w) {
         float2 acc[64];
-        if (sc.item(w, p.nk).mode == kTail) {
+        if (sc.item(w, p.nk).mode == kTail && !p.indep) {
             // Continue the predecessor's FMA chains from its partial sums.
             const float2* src = p.ws_partial + (int64_t)(blockIdx.x - 1) * (kThreads * 64);
             if (issuer) {
@@ -486,6 +487,35 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             continue;
         }
 
+        if (itm.mode == kTail && p.indep) {
+            // Add the earlier pieces of this tile, latest CTA first, once all
+            // of them are published.
+            const int64_t first = unit_owner((itm.tile - p.dp_tiles) * p.nk, p.sk_units, gridDim.x);
+            if (issuer) {
+                for (int64_t c = first; c < (int64_t)blockIdx.x; ++c)
+                    if (!wait_flag(p.ws_flag + c)) {
+                        record_status(&g_wait_status, kWaitPartial);
+                        drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
+                        return;
+                    }
+                mbar_arrive(&sh.ready);
+            }
+            if (!mbar_wait(&sh.ready, 0)) {
+                record_status(&g_wait_status, kWaitPartial);
+                return;
+            }
+#pragma unroll 1
+            for (int64_t c = (int64_t)blockIdx.x - 1; c >= first; --c) {
+                const float2* src = p.ws_partial + c * (kThreads * 64);
+#pragma unroll
+                for (int q = 0; q < 64; ++q) {
+                    const float2 v = __ldcg(src + q * kThreads + threadIdx.x);
+                    acc[q].x += v.x;
+                    acc[q].y += v.y;
+                }
+            }
+        }
+
         // Epilogue straight from registers.
         const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
         float* Cb = p.C + tc.b * p.bsC;
@@ -595,6 +625,7 @@ cudaError_t launch_impl(const Problem& pr, const Plan& plan, int sm_count, cudaS
     const int64_t grid = plan.ctas;
     p.dp_tiles = plan.stream_k ? plan.dp_tiles : plan.tiles;
     p.sk_units = plan.stream_k ? (plan.tiles - plan.dp_tiles) * p.nk : 0;
+    p.indep = plan.stream_k && plan.split_indep ? 1 : 0;
     p.ws_partial = nullptr;
     p.ws_flag = nullptr;
     if (plan.stream_k) {
@@ -672,7 +703,7 @@ size_t tma_ffma_workspace_bytes(int sm_count) {
 // is split at most once), and a tile has enough slices to amortise the
 // exchange of its partial sums.
 void tma_ffma_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_bytes,
-                       const void* ws) {
+                       const void* ws, int k_split) {
     const TmaFfmaConfig c = kConfigs[plan.variant];
     const int64_t nk = (pr.K + c.bk - 1) / c.bk;
     const int64_t G = sm_count;
@@ -682,12 +713,24 @@ void tma_ffma_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_by
     plan.ctas = plan.tiles < G ? plan.tiles : G;
     if (!ws || ws_bytes < tma_ffma_workspace_bytes(sm_count)) return;
     if ((reinterpret_cast<uintptr_t>(ws) % 256) != 0) return;
+    if (k_split == SBGEMM_KSPLIT_NONE) return;
     // About 20 us of exchange and reset cost: some 4 slices of a 256 x 128 tile.
     const int64_t dp = stream_k_dp_tiles(plan.tiles, nk, G, 4);
-    if (dp < 0) return;
+    if (dp >= 0) {
+        plan.stream_k = true;
+        plan.dp_tiles = dp;
+        plan.ctas = G;
+        plan.workspace = const_cast<void*>(ws);
+        return;
+    }
+    if (k_split != SBGEMM_KSPLIT_ANY) return;
+    // Fewer tiles than SMs: independent K pieces of at least 8 slices.
+    const int64_t g = split_k_ctas(plan.tiles, nk, G, 8, 4);
+    if (g < 0) return;
     plan.stream_k = true;
-    plan.dp_tiles = dp;
-    plan.ctas = G;
+    plan.split_indep = true;
+    plan.dp_tiles = 0;
+    plan.ctas = g;
     plan.workspace = const_cast<void*>(ws);
 }
 

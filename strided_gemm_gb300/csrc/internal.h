@@ -46,7 +46,8 @@ struct Plan {
     int64_t tiles = 0;              // tiles_m * tiles_n * batch
     int64_t ctas = 0;
     int k_slices = 0;               // K slices per tile
-    bool stream_k = false;          // last waves split along K (needs workspace)
+    bool stream_k = false;          // tiles split along K (needs workspace)
+    bool split_indep = false;       // ... as independent pieces (fewer tiles than SMs)
     int64_t dp_tiles = 0;           // tiles computed whole
     void* workspace = nullptr;      // caller's scratch when stream_k
 };
@@ -68,7 +69,9 @@ int tma_ffma_pick_variant(const Problem& p, int sm_count);
 // Bytes of workspace the stream-K schedule needs on a device with sm_count SMs.
 size_t tma_ffma_workspace_bytes(int sm_count);
 // Fills plan.ctas / stream_k / dp_tiles / k_slices for the chosen variant.
-void tma_ffma_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws);
+// k_split: SBGEMM_KSPLIT_* policy of the caller's options.
+void tma_ffma_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
+                       int k_split);
 cudaError_t launch_tma_ffma(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
 
 // Reads and clears the status words of the kernels that use bounded waits.
@@ -79,7 +82,8 @@ unsigned int read_and_clear_wait_status_tma_ffma(cudaStream_t stream);
 TmaFfmaConfig tf32_tc_config();
 cudaError_t launch_tf32_tc(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
 // Fills plan.ctas / stream_k / dp_tiles / k_slices for the TF32 kernel.
-void tf32_tc_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws);
+void tf32_tc_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
+                      int k_split);
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream);
 
 // ---- failure-detection self-test (selftest.cu) ----------------------------------

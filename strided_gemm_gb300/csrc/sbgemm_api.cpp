@@ -126,6 +126,7 @@ int check_options(const sbgemm_options* opt, sbgemm_options* out) {
     if (opt) o = *opt;
     if (o.math != SBGEMM_MATH_FP32 && o.math != SBGEMM_MATH_TF32) return SBGEMM_ERR_INVALID_VALUE;
     if (o.force_path < SBGEMM_PATH_AUTO || o.force_path > SBGEMM_PATH_TMA_TF32) return SBGEMM_ERR_INVALID_VALUE;
+    if (o.k_split < SBGEMM_KSPLIT_ANY || o.k_split > SBGEMM_KSPLIT_NONE) return SBGEMM_ERR_INVALID_VALUE;
     for (int r : o.reserved) if (r != 0) return SBGEMM_ERR_INVALID_VALUE;
     if (o.workspace && (reinterpret_cast<uintptr_t>(o.workspace) % 256) != 0)
         return SBGEMM_ERR_INVALID_VALUE;
@@ -225,7 +226,8 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
         plan->tiles_m = (p.M + c.bm - 1) / c.bm;
         plan->tiles_n = (p.N + c.bn - 1) / c.bn;
         plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
-        tf32_tc_schedule(p, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace);
+        tf32_tc_schedule(p, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace,
+                         o.k_split);
         return SBGEMM_OK;
     }
 
@@ -240,7 +242,8 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
         plan->tiles_m = (p.M + c.bm - 1) / c.bm;
         plan->tiles_n = (p.N + c.bn - 1) / c.bn;
         plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
-        tma_ffma_schedule(p, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace);
+        tma_ffma_schedule(p, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace,
+                          o.k_split);
         return SBGEMM_OK;
     }
 
@@ -290,7 +293,8 @@ void fill_info(const Plan& plan, sbgemm_plan_info* info) {
     info->ctas_per_sm = plan.ctas_per_sm;
     info->ctas = plan.ctas;
     info->tiles = plan.tiles;
-    info->stream_k = plan.stream_k;
+    info->stream_k = plan.stream_k ? (plan.split_indep ? SBGEMM_STREAM_K_PIECES : SBGEMM_STREAM_K_CHAINED)
+                                   : SBGEMM_STREAM_K_NONE;
     info->k_slices = plan.k_slices;
     info->dp_tiles = plan.dp_tiles;
 }

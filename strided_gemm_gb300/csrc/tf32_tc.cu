@@ -488,7 +488,8 @@ cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cu
 
 // Same rule as the FFMA path (stream_k_dp_tiles), with the tensor cores' own
 // exchange cost.
-void tf32_tc_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_bytes, const void* ws) {
+void tf32_tc_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
+                      int k_split) {
     const int64_t nk = (pr.K + BK - 1) / BK;
     const int64_t G = sm_count;
     plan.k_slices = (int)nk;
@@ -497,6 +498,7 @@ void tf32_tc_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_byt
     plan.ctas = plan.tiles < G ? plan.tiles : G;
     const size_t need = (size_t)G * (size_t)kSlotFloat4 * sizeof(float4) + (size_t)G * sizeof(unsigned int);
     if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 256) != 0) return;
+    if (k_split == SBGEMM_KSPLIT_NONE) return;
     // Tensor-core slices are short (about 0.4 us for 128 x 256 x 32), so the
     // 15-20 us of exchange and reset cost counts as about 48 slices: only
     // long-K problems gain.

@@ -219,3 +219,40 @@ def test_tf32_stream_k_planning():
         assert p1["tiles"] == 320 and p1["k_slices"] == K // 32
         if split:
             assert p1["ctas"] == 152 and p1["dp_tiles"] == 152
+
+
+def test_split_k_pieces_planning():
+    """Fewer tiles than SMs and long K (the weight gradient G^T X of a
+    projection layer): with a workspace the tiles' K slices are spread as
+    independent pieces over all SMs; k_split = EXACT or NONE keeps whole tiles,
+    and NONE also turns off the chained stream-K of many-tile problems."""
+    ws = BASE + (8 << 32)
+    big = 1 << 30
+    M, N, K = 2560, 960, 8192
+    A = (BASE, 1, M, 0)                                  # G^T: G stored [K, M]
+    B = rowmajor(BASE + (1 << 32), K, N, 1)
+    C = rowmajor(BASE + (2 << 32), M, N, 1)
+    p0 = call_plan(A, B, C, M, N, K, 1, 1)
+    assert p0["path"] == sg.PATH_TMA_FFMA and p0["stream_k"] == sg.STREAM_K_NONE
+    assert p0["tiles"] == 80 and p0["ctas"] == 80
+    p1 = call_plan(A, B, C, M, N, K, 1, 1, workspace=ws, workspace_bytes=big)
+    assert p1["stream_k"] == sg.STREAM_K_PIECES
+    assert p1["ctas"] == 152 and p1["dp_tiles"] == 0 and p1["k_slices"] == K // 32
+    for policy in (sg.KSPLIT_EXACT, sg.KSPLIT_NONE):
+        p = call_plan(A, B, C, M, N, K, 1, 1, workspace=ws, workspace_bytes=big, k_split=policy)
+        assert p["stream_k"] == sg.STREAM_K_NONE and p["ctas"] == 80
+    # Many tiles: chained stream-K under ANY and EXACT, none under NONE.
+    Mb = Nb = Kb = 4096
+    A2, B2, C2 = (rowmajor(BASE, Mb, Kb, 1), rowmajor(BASE + (1 << 32), Kb, Nb, 1),
+                  rowmajor(BASE + (2 << 32), Mb, Nb, 1))
+    for policy, want in ((sg.KSPLIT_ANY, sg.STREAM_K_CHAINED), (sg.KSPLIT_EXACT, sg.STREAM_K_CHAINED),
+                         (sg.KSPLIT_NONE, sg.STREAM_K_NONE)):
+        p = call_plan(A2, B2, C2, Mb, Nb, Kb, 1, workspace=ws, workspace_bytes=big, k_split=policy)
+        assert p["stream_k"] == want, (policy, p)
+    # Short K does not split, and an unknown policy is refused.
+    short = call_plan((BASE, 1, M, 0), rowmajor(BASE + (1 << 32), 256, N, 1), C, M, N, 256, 1,
+                      workspace=ws, workspace_bytes=big)
+    assert short["stream_k"] == sg.STREAM_K_NONE
+    with pytest.raises(sg.SbgemmError) as e:
+        call_plan(A, B, C, M, N, K, 1, workspace=ws, workspace_bytes=big, k_split=3)
+    assert e.value.status == sg.SBGEMM_ERR_INVALID_VALUE

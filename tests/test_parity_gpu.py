@@ -267,6 +267,90 @@ def test_stream_k_repeated_calls_reuse_workspace(torch, workspace):
     gu.check_full(case, first, exact=True)
 
 
+# ---- independent K pieces (fewer tiles than SMs, long K) --------------------------
+
+SPLIT_SHAPES = [
+    # (name, M, N, K, batch, a_layout, b_layout, accumulate); 38..151 TMA tiles
+    ("weight_grad_like", 2560, 960, 8192, 1, "col16", "row16", 1),   # 80 tiles, 2-3 pieces each
+    ("ragged", 2000, 1000, 3000, 1, "row16", "col16", 0),            # ragged M, N and K
+    ("batched", 512, 512, 2048, 12, "col16", "row16", 1),
+    ("many_pieces", 1536, 1024, 4096, 1, "row16", "row16", 0),       # 48 tiles, ~4 pieces each
+]
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=[s[0] for s in SPLIT_SHAPES])
+def test_split_k_pieces_parity_and_determinism(torch, workspace, shape):
+    """Every piece starts from zero and the tail adds the earlier pieces in a
+    fixed order: within the FFMA bound of the oracle, identical on every run,
+    and k_split = EXACT restores the unsplit result bit for bit."""
+    _, M, N, K, batch, la, lb, acc = shape
+    rng = np.random.default_rng(M * 7 + N + K + batch)
+    case = wl.random_strided(rng, M, N, K, batch, la, lb, values="real", accumulate=acc,
+                             alpha=0.5)
+    first, plan = _run_ws(case, torch, workspace)
+    assert plan["path"] == sg.PATH_TMA_FFMA and plan["stream_k"] == sg.STREAM_K_PIECES, plan
+    gu.check_points(case, first, n=4000)
+    again, _ = _run_ws(case, torch, workspace)
+    assert np.array_equal(first, again)
+    whole, _ = _run_ws(case, torch, None)
+    exact, plan_x = _run_ws(case, torch, workspace, dict(k_split=sg.KSPLIT_EXACT))
+    assert plan_x["stream_k"] == sg.STREAM_K_NONE
+    assert np.array_equal(exact, whole)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
+def test_split_k_pieces_integer_exact(torch, workspace):
+    """Integer inputs: every partial sum is exact, so the split result is the
+    exact product whatever the order of the pieces."""
+    rng = np.random.default_rng(17)
+    case = wl.random_strided(rng, 1536, 1024, 4096, 1, "col16", "row16", values="int",
+                             accumulate=1)
+    got, plan = _run_ws(case, torch, workspace)
+    assert plan["stream_k"] == sg.STREAM_K_PIECES
+    gu.check_points(case, got, n=6000, exact=True)
+
+
+@pytest.mark.parametrize("name", wl.BACKWARD)
+def test_backward_products_full_size_with_workspace(torch, workspace, name):
+    """The backward products at full size through the schedule a caller with a
+    workspace gets (chained stream-K for dX, independent pieces for dW)."""
+    for values in ("real", "int"):
+        case = wl.make(name, values)
+        got, plan = _run_ws(case, torch, workspace)
+        assert plan["path"] == sg.PATH_TMA_FFMA
+        want_mode = sg.STREAM_K_PIECES if name.startswith("f1dw") else sg.STREAM_K_CHAINED
+        assert plan["stream_k"] == want_mode, plan
+        if values == "int":
+            gu.check_points(case, got, n=3000, exact=True)
+        else:
+            gu.check_points(case, got, n=3000)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
+def test_linear_backward_helper(torch, workspace):
+    """sg.linear_backward on torch tensors: dX = G W and dW += G^T X against
+    float64 torch on the CPU."""
+    gen = torch.Generator().manual_seed(5)
+    T, d_in, d_out = 2048, 384, 640
+    X = torch.randn(T, d_in, generator=gen)
+    W = torch.randn(d_out, d_in, generator=gen) * 0.02
+    G = torch.randn(T, d_out, generator=gen)
+    dW0 = torch.randn(d_out, d_in, generator=gen) * 0.01
+    dX = torch.empty(T, d_in, device="cuda")
+    dW = dW0.clone().cuda()
+    sg.linear_backward(G.cuda(), X.cuda(), W.cuda(), dX, dW, accumulate_dW=True,
+                       workspace=workspace)
+    torch.cuda.synchronize()
+    want_dX = G.double() @ W.double()
+    want_dW = dW0.double() + G.double().t() @ X.double()
+    bound_dX = G.double().abs() @ W.double().abs()
+    bound_dW = dW0.double().abs() + G.double().abs().t() @ X.double().abs()
+    assert bool(((dX.cpu().double() - want_dX).abs() <= gu.TOL_FFMA * bound_dX).all())
+    assert bool(((dW.cpu().double() - want_dW).abs() <= gu.TOL_FFMA * bound_dW).all())
+
+
 # ---- TF32 tensor-core path (opt-in) -------------------------------------------
 
 TF32_WORKLOADS = ["c2a", "c2b", "c3", "c3gqa", "c5a", "c5b"]   # both operands K-major
