@@ -55,6 +55,11 @@ def _bind(path: str):
         _fp, _i64, _i64, _i64, _fp, _i64, _i64, _i64, _fp, _i64, _i64, _i64,
         _i64, _i64, _i64, _i64, ctypes.c_float, ctypes.c_int,
         _fp, _i64, _fp, _fp]
+    lib.sbgemm_ref_activation.restype = ctypes.c_int
+    lib.sbgemm_ref_activation.argtypes = [ctypes.c_int, _fp, _fp, _i64]
+    lib.sbgemm_ref_epilogue_points.restype = ctypes.c_int
+    lib.sbgemm_ref_epilogue_points.argtypes = [_fp, _i64, _i64, _i64, ctypes.c_int,
+                                               _fp, _i64, _fp, _fp, _fp]
     return lib
 
 
@@ -147,3 +152,52 @@ def case_product(case, **kw):
 def case_points(case, idx, **kw):
     return product_points(case.A, case.B, case.C, case.M, case.N, case.K,
                           case.batch, case.alpha, case.accumulate, idx, **kw)
+
+
+# ---- fused epilogue: out = act(alpha*A*B (+C0) + D) ------------------------------
+# Activation codes of sbgemm_ref.c: 0 none, 1 relu, 2 sigmoid, 3 silu,
+# 4 gelu_tanh, 5 gelu_erf.
+ACTIVATIONS = {"none": 0, "relu": 1, "sigmoid": 2, "silu": 3, "gelu_tanh": 4, "gelu_erf": 5}
+
+
+def activation(act, z, lib=None):
+    """act(z) in fp64, elementwise (sbgemm_ref_activation)."""
+    lib = lib or load()
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    out = np.empty_like(z)
+    if lib.sbgemm_ref_activation(int(act), z.ctypes.data, out.ctypes.data, z.size) != 0:
+        raise ValueError(f"oracle: unknown activation {act}")
+    return out
+
+
+def fused_product(A, B, C, M, N, K, batch, alpha, accumulate, D, act, lib=None, **kw):
+    """Full fused product.  D (an operand, or None) is added to the product and
+    act applied: returns (out, z, bound) with z the pre-activation value and
+    bound its error scale |alpha|sum|a||b| + |C0| + |D|."""
+    z, bound = product(A, B, C, M, N, K, batch, alpha, accumulate, lib=lib, **kw)
+    if D is not None:
+        if not _span_ok(D, batch, M, N):
+            raise ValueError("oracle: D strides reach outside its storage")
+        b, m, n = np.meshgrid(np.arange(batch), np.arange(M), np.arange(N), indexing="ij")
+        d = D.storage[D.offset + b * D.bs + m * D.rs + n * D.cs].astype(np.float64)
+        z = z + d
+        bound = bound + np.abs(d)
+    return activation(act, z, lib=lib), z, bound
+
+
+def fused_points(A, B, C, M, N, K, batch, alpha, accumulate, D, act, idx, lib=None):
+    """The fused product at selected outputs (idx [P, 3] of (b, m, n))."""
+    lib = lib or load()
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 3)
+    z, bound = product_points(A, B, C, M, N, K, batch, alpha, accumulate, idx, lib=lib)
+    out = np.empty_like(z)
+    if D is not None and not _span_ok(D, batch, M, N):
+        raise ValueError("oracle: D strides reach outside its storage")
+    rc = lib.sbgemm_ref_epilogue_points(_ptr(D) if D is not None else None,
+                                        D.rs if D is not None else 0, D.cs if D is not None else 0,
+                                        D.bs if D is not None else 0, int(act),
+                                        idx.ctypes.data, idx.shape[0], z.ctypes.data,
+                                        bound.ctypes.data, out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle: unknown activation {act}")
+    return out, z, bound

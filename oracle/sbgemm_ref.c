@@ -163,3 +163,66 @@ int sbgemm_ref_points(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     }
     return 0;
 }
+
+/*
+ * Fused epilogue (test infrastructure, as above).
+ *
+ * The fusion a linear layer asks for ("PyTorch demystified 3", section
+ * "Summary": add the bias term in the matmul kernel instead of a second pass)
+ * extended by an activation, in the usual epilogue order:
+ *     z   = alpha * s + (accumulate ? C0 : 0) + D[b,m,n]
+ *     out = act(z)
+ * D is an addend laid out like any operand (its own row, column and batch
+ * strides; zero strides broadcast, so a per-column bias has rs = 0, cs = 1).
+ * The activations are the mathematical functions the pages name: ReLU and the
+ * two GELUs of "Chapter 09 CUDA backend" (section "Elementwise": Relu,
+ * GeluTanh, GeluExact), the sigmoid of "PyTorch demystified 3" and the SiLU of
+ * "rvllm CUDA path" (silu(gate)), each evaluated in fp64 with the C library:
+ *     0 none       z
+ *     1 relu       max(z, 0)
+ *     2 sigmoid    1 / (1 + e^-z)
+ *     3 silu       z * sigmoid(z)
+ *     4 gelu_tanh  z/2 * (1 + tanh(sqrt(2/pi) * (z + 0.044715 z^3)))
+ *     5 gelu_erf   z/2 * (1 + erf(z / sqrt(2)))
+ * Returns -1 for an unknown activation.
+ */
+static int oracle_act(int act, double z, double* out) {
+    switch (act) {
+        case 0: *out = z; return 0;
+        case 1: *out = z > 0.0 ? z : 0.0; return 0;
+        case 2: *out = 1.0 / (1.0 + exp(-z)); return 0;
+        case 3: *out = z / (1.0 + exp(-z)); return 0;
+        case 4: {
+            const double c = sqrt(2.0 / acos(-1.0));   /* sqrt(2 / pi) */
+            *out = 0.5 * z * (1.0 + tanh(c * (z + 0.044715 * z * z * z)));
+            return 0;
+        }
+        case 5: *out = 0.5 * z * (1.0 + erf(z / sqrt(2.0))); return 0;
+        default: return -1;
+    }
+}
+
+/* out[i] = act(z[i]) for n values. */
+int sbgemm_ref_activation(int act, const double* z, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i)
+        if (oracle_act(act, z[i], &out[i]) != 0) return -1;
+    return 0;
+}
+
+/* Adds D to product results and applies the activation, at the outputs
+ * listed in idx (n_points triples (b, m, n)); z and bound are updated in
+ * place (z += D, bound += |D|) and out receives act(z).  D may be NULL. */
+int sbgemm_ref_epilogue_points(const float* D, int64_t rsD, int64_t csD, int64_t bsD,
+                               int act, const int64_t* idx, int64_t n_points,
+                               double* z, double* bound, double* out) {
+    for (int64_t p = 0; p < n_points; ++p) {
+        const int64_t b = idx[3 * p], m = idx[3 * p + 1], n = idx[3 * p + 2];
+        if (D) {
+            const double d = (double)D[b * bsD + m * rsD + n * csD];
+            z[p] += d;
+            if (bound) bound[p] += fabs(d);
+        }
+        if (oracle_act(act, z[p], &out[p]) != 0) return -1;
+    }
+    return 0;
+}

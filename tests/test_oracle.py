@@ -329,3 +329,87 @@ def test_backward_layouts_are_the_linear_layer_gradients():
     want = C0 + np.array([[sum(int(Gs[t, o]) * int(Xs[t, i]) for t in range(7))
                            for i in range(5)] for o in range(6)])
     assert np.array_equal(ref[0], want.astype(np.float64))
+
+
+# ---- fused epilogue: activations and the added operand D ----------------------
+
+def run_activation_pins(lib=None):
+    """Pins of the oracle's activations against facts independent of its
+    formulas; returns the number of failed checks (0 for a correct oracle).
+    Also used on mutated builds."""
+    A = oracle.ACTIVATIONS
+    act = lambda name, z: oracle.activation(A[name], np.asarray(z, dtype=np.float64), lib=lib)
+    z = np.linspace(-9.0, 9.0, 3601)
+    ln3 = np.log(3.0)
+    checks = []
+    # none and relu: exact identities.
+    checks.append(np.array_equal(act("none", z), z))
+    r = act("relu", z)
+    checks.append(np.array_equal(r - act("relu", -z), z) and np.array_equal(r + act("relu", -z), np.abs(z)))
+    # sigmoid: symmetric about 1/2, and 1/(1 + 1/3) at ln 3.
+    s = act("sigmoid", z)
+    checks.append(np.abs(s + act("sigmoid", -z) - 1.0).max() < 1e-15)
+    checks.append(abs(act("sigmoid", [ln3])[0] - 0.75) < 1e-15 and act("sigmoid", [0.0])[0] == 0.5)
+    # silu: odd part z/2, and (3/4) ln 3 at ln 3.
+    checks.append(np.abs(act("silu", z) - act("silu", -z) - z).max() < 1e-13)
+    checks.append(abs(act("silu", [ln3])[0] - 0.75 * ln3) < 1e-15)
+    # gelu_erf: z * Phi(z), the standard normal CDF of scipy; Phi(1) = 0.841344746068543.
+    from scipy.stats import norm
+    ge = act("gelu_erf", z)
+    checks.append(np.abs(ge - z * norm.cdf(z)).max() < 1e-14)
+    checks.append(abs(act("gelu_erf", [1.0])[0] - 0.841344746068543) < 1e-15)
+    checks.append(np.abs(ge - act("gelu_erf", -z) - z).max() < 1e-13)
+    # gelu_tanh: odd part z/2; the tanh approximation of z * Phi(z) deviates from
+    # it by 4.73e-4 at most (a wrong coefficient moves that by 2x or more).
+    gt = act("gelu_tanh", z)
+    checks.append(np.abs(gt - act("gelu_tanh", -z) - z).max() < 1e-13)
+    zz = np.linspace(-8.0, 8.0, 160001)
+    dev = np.abs(act("gelu_tanh", zz) - zz * norm.cdf(zz)).max()
+    checks.append(4.6e-4 < dev < 4.8e-4)
+    return sum(1 for c in checks if not c)
+
+
+def test_activation_pins():
+    assert run_activation_pins() == 0
+
+
+def test_unknown_activation_is_refused():
+    with pytest.raises(ValueError):
+        oracle.activation(6, np.zeros(3))
+
+
+def run_epilogue_pins(lib=None):
+    """Integer A, B, C0 and D: z is exact and so is relu(z); the sampled-points
+    variant (D added in C) reproduces the full fused product (D added here with
+    numpy) for every activation; D broadcast over rows (a bias per column) and
+    over batches.  Returns the number of failed checks."""
+    rng = np.random.default_rng(23)
+    bad = 0
+    for acc, d_rs, d_bs in ((0, 0, 0), (1, 0, 1), (1, 1, 0)):
+        M, N, K, batch = 19, 21, 33, 3
+        case = wl.random_strided(rng, M, N, K, batch, "row", "col", values="int",
+                                 accumulate=acc, alpha=0.5)
+        dst = rng.integers(-8, 9, size=batch * M * N).astype(np.float32)
+        D = wl.Operand(dst, 0, d_rs * N, 1, d_bs * M * N)
+        out, z, bound = oracle.fused_product(case.A, case.B, case.C, M, N, K, batch,
+                                             case.alpha, acc, D, oracle.ACTIVATIONS["relu"],
+                                             lib=lib)
+        eref, ebound = _int_expected(case)
+        d = D.view(batch, M, N).astype(np.float64)
+        bad += not (np.array_equal(z, eref + d) and np.array_equal(bound, ebound + np.abs(d)))
+        bad += not np.array_equal(out, np.where(z > 0, z, 0.0))
+        idx = np.stack([rng.integers(0, batch, 200), rng.integers(0, M, 200),
+                        rng.integers(0, N, 200)], axis=1)
+        sel = (idx[:, 0], idx[:, 1], idx[:, 2])
+        for code in oracle.ACTIVATIONS.values():
+            fo, fz, fb = oracle.fused_points(case.A, case.B, case.C, M, N, K, batch, case.alpha,
+                                             acc, D, code, idx, lib=lib)
+            full, fullz, fullb = oracle.fused_product(case.A, case.B, case.C, M, N, K, batch,
+                                                      case.alpha, acc, D, code, lib=lib)
+            bad += not (np.array_equal(fo, full[sel]) and np.array_equal(fz, fullz[sel]) and
+                        np.array_equal(fb, fullb[sel]))
+    return bad
+
+
+def test_fused_epilogue_pins():
+    assert run_epilogue_pins() == 0

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests.test_oracle import run_int_pins
+from tests.test_oracle import run_activation_pins, run_epilogue_pins, run_int_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "sbgemm_ref.c")
 
@@ -47,4 +47,33 @@ def test_unmutated_copy_passes(tmp_path):
     shutil.copy(SRC, tmp_path / "same.c")
     so = str(tmp_path / "libsame.so")
     oracle.build(force=True, src=str(tmp_path / "same.c"), out=so)
-    assert run_int_pins(lib=oracle.load(so)) == 0
+    lib = oracle.load(so)
+    assert run_int_pins(lib=lib) == 0
+    assert run_activation_pins(lib=lib) == 0 and run_epilogue_pins(lib=lib) == 0
+
+
+# Slips in the fused epilogue's activations and added operand.
+EPILOGUE_MUTATIONS = [
+    ("relu_leaky", "case 1: *out = z > 0.0 ? z : 0.0;", "case 1: *out = z > 0.0 ? z : 0.01 * z;"),
+    ("sigmoid_sign", "case 2: *out = 1.0 / (1.0 + exp(-z));", "case 2: *out = 1.0 / (1.0 + exp(z));"),
+    ("silu_without_z", "case 3: *out = z / (1.0 + exp(-z));", "case 3: *out = 1.0 / (1.0 + exp(-z));"),
+    ("gelu_tanh_coefficient", "(z + 0.044715 * z", "(z + 0.04715 * z"),
+    ("gelu_tanh_square_not_cube", "z * z * z", "z * z"),
+    ("gelu_erf_without_sqrt2", "erf(z / sqrt(2.0))", "erf(z)"),
+    ("gelu_erf_without_half", "case 5: *out = 0.5 * z *", "case 5: *out = z *"),
+    ("addend_rows_cols_swapped", "D[b * bsD + m * rsD + n * csD]", "D[b * bsD + m * csD + n * rsD]"),
+    ("addend_bound_without_abs", "if (bound) bound[p] += fabs(d);", "if (bound) bound[p] += d;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", EPILOGUE_MUTATIONS, ids=[m[0] for m in EPILOGUE_MUTATIONS])
+def test_planted_epilogue_mistake_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = tmp_path / "mut.c"
+    mutated.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmut.so")
+    oracle.build(force=True, src=str(mutated), out=so)
+    lib = oracle.load(so)
+    assert run_activation_pins(lib=lib) + run_epilogue_pins(lib=lib) > 0, \
+        f"planted mistake {name} went unnoticed"
