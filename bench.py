@@ -505,6 +505,38 @@ def run_ours(args, world, rank, local, dist):
                                 "unit": "TFLOP/s", "frac": round(ach / fp32_peak, 4),
                                 "traffic": profiled_traffic("tma_ffma", slow)}
 
+    # Fused epilogue on the feed-forward projection (c5a): y = act(x W^T + b)
+    # in one launch, against the plain product, on both arithmetic paths.
+    epilogue = None
+    if not args.no_epilogue and args.workload == "c5" and math == sg.MATH_FP32:
+        i5 = names.index("c5a")
+        c = cases[i5]
+        bias = torch.randn(c.N, generator=torch.Generator().manual_seed(6)).to(dev)
+        reps = max(3, min(args.steps, 10))
+        epilogue = {"product": "c5a", "bias": "per output column", "per_variant": {}}
+        for mname, m in (("fp32", sg.MATH_FP32), ("tf32", sg.MATH_TF32)):
+            variants = {"plain": lambda m=m: sg.sbgemm_ex(*calls[i5], s_handle, math=m, **ws_kw)}
+            for act in ("relu", "gelu_erf"):
+                variants["bias+" + act] = (lambda m=m, a=act: sg.sbgemm_fused(
+                    *calls[i5], bias.data_ptr(), 0, 1, 0, sg.ACTIVATIONS[a], s_handle, m, **ws_kw))
+            for k, f in variants.items():
+                for _ in range(3):
+                    f()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(reps):
+                    f()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / reps
+                epilogue["per_variant"][f"{mname} {k}"] = {
+                    "ms": round(ms, 4), "gflops": round(c.flops / ms / 1e6, 1)}
+            base = epilogue["per_variant"][f"{mname} plain"]["ms"]
+            for k in ("bias+relu", "bias+gelu_erf"):
+                v = epilogue["per_variant"][f"{mname} {k}"]
+                v["overhead_vs_plain"] = round(v["ms"] / base - 1.0, 4)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -538,6 +570,7 @@ def run_ours(args, world, rank, local, dist):
         "e2e": e2e,
         "tf32": tf32,
         "backward": backward,
+        "epilogue": epilogue,
         "gpu_launches": len(calls) * args.steps,
         "clocks": clocks,
         "per_product": {n: {k: v for k, v in d.items() if k != "total_ms"} for n, d in per.items()},
@@ -597,6 +630,8 @@ def main(argv=None):
                     help="skip the opt-in tensor-core measurement")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward-product measurement")
+    ap.add_argument("--no-epilogue", action="store_true",
+                    help="skip the fused-epilogue measurement")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
     world, rank, local = dist_env()

@@ -167,6 +167,36 @@ typedef struct {
     int reserved[4];
 } sbgemm_plan_info;
 
+/* Activation of the fused epilogue; sbgemm_epilogue.activation.  The pages
+ * name ReLU, GeluTanh and GeluExact ("Chapter 09 CUDA backend", section
+ * "Elementwise"), the sigmoid ("PyTorch demystified 3") and SiLU ("rvllm
+ * CUDA path", the FFN's silu(gate)). */
+enum {
+    SBGEMM_ACT_NONE = 0,
+    SBGEMM_ACT_RELU = 1,       /* max(z, 0) */
+    SBGEMM_ACT_SIGMOID = 2,    /* 1 / (1 + e^-z) */
+    SBGEMM_ACT_SILU = 3,       /* z / (1 + e^-z) */
+    SBGEMM_ACT_GELU_TANH = 4,  /* z/2 (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))) */
+    SBGEMM_ACT_GELU_ERF = 5    /* z/2 (1 + erf(z / sqrt(2))) */
+};
+
+/* Fused epilogue of sbgemm_fused:
+ *     C[b,m,n] <- act(alpha * (A*B)[b,m,n] + (accumulate ? C_old[b,m,n] : 0) + D[b,m,n])
+ * with D[b,m,n] = D[b*bsD + m*rsD + n*csD] (strides in fp32 elements; zero
+ * strides broadcast, so a bias per output column is rsD = 0, csD = 1, bsD = 0,
+ * and a bias per batch entry and column is bsD = N).  The fusion of
+ * "PyTorch demystified 3", section "Summary": the feed-forward layer's bias is
+ * added inside the matmul kernel, saving a pass over C and a launch.
+ * Rounding: alpha*acc (+ C_old) as sbgemm forms it, one fp32 add of D, then
+ * the activation in fp32 through the CUDA math library. */
+typedef struct {
+    const float* D;            /* NULL = no addend; device memory, 4-byte aligned,
+                                  its span must not meet C's */
+    int64_t rsD, csD, bsD;
+    int activation;            /* SBGEMM_ACT_* */
+    int reserved[3];           /* must be zero */
+} sbgemm_epilogue;
+
 /* Strict fp32 product on the CUDA cores; the planner picks the kernel.
  * Arguments as described above; stream is a cudaStream_t (NULL = default). */
 SBGEMM_API int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
@@ -185,6 +215,21 @@ SBGEMM_API int sbgemm_ex(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
               int64_t M, int64_t N, int64_t K, int64_t batch,
               float alpha, int accumulate, void* stream,
               const sbgemm_options* opt);
+
+/* As sbgemm_ex, with a fused epilogue (NULL = none: same as sbgemm_ex).  All
+ * paths and schedules apply it once per output, after the last K slice.  With
+ * an epilogue, K == 0 with accumulate writes act(C_old + D) instead of
+ * leaving C unchanged.  Errors as sbgemm_ex, plus SBGEMM_ERR_INVALID_VALUE for
+ * an unknown activation, non-zero reserved fields, a misaligned D or a D span
+ * overflowing int64; SBGEMM_ERR_OUTPUT_OVERLAP when D's span meets C's (or the
+ * workspace); SBGEMM_ERR_NOT_DEVICE_MEMORY when D is not inside one device
+ * allocation. */
+SBGEMM_API int sbgemm_fused(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+                 const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+                 float* C, int64_t rsC, int64_t csC, int64_t bsC,
+                 int64_t M, int64_t N, int64_t K, int64_t batch,
+                 float alpha, int accumulate, const sbgemm_epilogue* epi,
+                 void* stream, const sbgemm_options* opt);
 
 /* Validate and plan without launching or touching device memory: reports the
  * layout classes and the kernel path, tile and CTA count that sbgemm_ex would

@@ -24,7 +24,10 @@ __all__ = [
     "SBGEMM_ERR_DEVICE_TIMEOUT", "SBGEMM_ERR_NOT_DEVICE_MEMORY",
     "MATH_FP32", "MATH_TF32", "PATH_NONE", "PATH_AUTO", "PATH_GATHER_FFMA",
     "PATH_TMA_FFMA", "PATH_TMA_TF32", "LAYOUT_K_MAJOR", "LAYOUT_MN_MAJOR",
-    "LAYOUT_GENERAL", "EXPORTED_SYMBOLS", "LIB_PATH",
+    "LAYOUT_GENERAL", "EXPORTED_SYMBOLS", "LIB_PATH", "sbgemm_fused", "linear_backward",
+    "ACT_NONE", "ACT_RELU", "ACT_SIGMOID", "ACT_SILU", "ACT_GELU_TANH", "ACT_GELU_ERF",
+    "ACTIVATIONS", "KSPLIT_ANY", "KSPLIT_EXACT", "KSPLIT_NONE", "STREAM_K_NONE",
+    "STREAM_K_CHAINED", "STREAM_K_PIECES",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -46,9 +49,12 @@ PATH_NAMES = {PATH_NONE: "none", PATH_GATHER_FFMA: "gather_ffma",
               PATH_TMA_FFMA: "tma_ffma", PATH_TMA_TF32: "tma_tf32"}
 
 # Every function include/sbgemm.h declares.
-EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_plan", "sbgemm_workspace_bytes",
-                    "sbgemm_noalloc", "sbgemm_selftest", "sbgemm_device_status",
-                    "sbgemm_status_string", "sbgemm_version")
+EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_fused", "sbgemm_plan",
+                    "sbgemm_workspace_bytes", "sbgemm_noalloc", "sbgemm_selftest",
+                    "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version")
+ACT_NONE, ACT_RELU, ACT_SIGMOID, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4, 5
+ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "sigmoid": ACT_SIGMOID, "silu": ACT_SILU,
+               "gelu_tanh": ACT_GELU_TANH, "gelu_erf": ACT_GELU_ERF}
 SELFTEST_MBARRIER, SELFTEST_FLAG = 1, 2
 KSPLIT_ANY, KSPLIT_EXACT, KSPLIT_NONE = 0, 1, 2
 STREAM_K_NONE, STREAM_K_CHAINED, STREAM_K_PIECES = 0, 1, 2
@@ -64,6 +70,12 @@ class _Options(ctypes.Structure):
     _fields_ = [("math", ctypes.c_int), ("force_path", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("k_split", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
+
+
+class _Epilogue(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_void_p), ("rsD", ctypes.c_int64), ("csD", ctypes.c_int64),
+                ("bsD", ctypes.c_int64), ("activation", ctypes.c_int),
+                ("reserved", ctypes.c_int * 3)]
 
 
 class _PlanInfo(ctypes.Structure):
@@ -99,6 +111,10 @@ def load(path: str = LIB_PATH):
         lib = ctypes.CDLL(path)
         lib.sbgemm.restype = ctypes.c_int
         lib.sbgemm.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp]
+        lib.sbgemm_fused.restype = ctypes.c_int
+        lib.sbgemm_fused.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int,
+                                             ctypes.POINTER(_Epilogue), _vp,
+                                             ctypes.POINTER(_Options)]
         lib.sbgemm_ex.restype = ctypes.c_int
         lib.sbgemm_ex.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp,
                                           ctypes.POINTER(_Options)]
@@ -180,6 +196,24 @@ def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
         raise SbgemmError(st, "sbgemm_ex")
 
 
+def sbgemm_fused(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                 M, N, K, batch, alpha, accumulate, D=0, rsD=0, csD=0, bsD=0,
+                 activation: int = ACT_NONE, stream=0, math: int = MATH_FP32,
+                 force_path: int = PATH_AUTO, workspace: int = 0, workspace_bytes: int = 0,
+                 k_split: int = KSPLIT_ANY) -> None:
+    """C <- act(alpha*A*B (+C) + D) with D read through (rsD, csD, bsD)."""
+    e = _Epilogue()
+    e.D = int(D) or None
+    e.rsD, e.csD, e.bsD = int(rsD), int(csD), int(bsD)
+    e.activation = int(activation)
+    o = _opts(math, force_path, workspace, workspace_bytes, k_split)
+    st = load().sbgemm_fused(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                             M, N, K, batch, float(alpha), int(bool(accumulate)),
+                             ctypes.byref(e), stream or None, ctypes.byref(o))
+    if st:
+        raise SbgemmError(st, "sbgemm_fused")
+
+
 def sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                 M, N, K, batch, accumulate=0, math: int = MATH_FP32,
                 force_path: int = PATH_AUTO, workspace: int = 0,
@@ -222,10 +256,13 @@ def _as3(t, name):
 
 def matmul(A, B, C, alpha: float = 1.0, accumulate: bool = False,
            math: int = MATH_FP32, force_path: int = PATH_AUTO, stream=None,
-           workspace=None, k_split: int = KSPLIT_ANY):
+           workspace=None, k_split: int = KSPLIT_ANY, bias=None, activation=ACT_NONE):
     """C <- alpha*A@B (+C) on torch CUDA float32 tensors viewed as [batch, M, K],
     [batch, K, N] and [batch, M, N] (2-D means batch 1).  Strides are taken from
-    the tensors, so transposed or expanded views need no copy.  Returns C."""
+    the tensors, so transposed or expanded views need no copy.  With `bias` (a
+    tensor broadcastable to C, e.g. [N] per column) or an `activation` (an
+    ACT_* code or its name) the epilogue is fused: C <- act(alpha*A@B (+C) +
+    bias).  Returns C."""
     import torch
     A3, B3, C3 = _as3(A, "A"), _as3(B, "B"), _as3(C, "C")
     for t, n in ((A3, "A"), (B3, "B"), (C3, "C")):
@@ -245,10 +282,22 @@ def matmul(A, B, C, alpha: float = 1.0, accumulate: bool = False,
     ws, ws_bytes = 0, 0
     if workspace is not None:
         ws, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    sbgemm_ex(A3.data_ptr(), A3.stride(1), A3.stride(2), bsA,
-              B3.data_ptr(), B3.stride(1), B3.stride(2), bsB,
-              C3.data_ptr(), C3.stride(1), C3.stride(2), C3.stride(0),
-              M, N, K, batch, alpha, accumulate, stream, math, force_path, ws, ws_bytes, k_split)
+    args = (A3.data_ptr(), A3.stride(1), A3.stride(2), bsA,
+            B3.data_ptr(), B3.stride(1), B3.stride(2), bsB,
+            C3.data_ptr(), C3.stride(1), C3.stride(2), C3.stride(0),
+            M, N, K, batch, alpha, accumulate)
+    act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+    if bias is None and act == ACT_NONE:
+        sbgemm_ex(*args, stream, math, force_path, ws, ws_bytes, k_split)
+        return C
+    D, rsD, csD, bsD = 0, 0, 0, 0
+    if bias is not None:
+        if bias.dtype != torch.float32 or not bias.is_cuda:
+            raise TypeError("bias must be a float32 CUDA tensor")
+        Dv = bias.expand(C3.shape) if bias.dim() == 3 else bias.expand(C3.shape[1:]).unsqueeze(0)
+        Dv = Dv.expand(C3.shape)
+        D, rsD, csD, bsD = Dv.data_ptr(), Dv.stride(1), Dv.stride(2), Dv.stride(0)
+    sbgemm_fused(*args, D, rsD, csD, bsD, act, stream, math, force_path, ws, ws_bytes, k_split)
     return C
 
 

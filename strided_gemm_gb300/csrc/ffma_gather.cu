@@ -15,6 +15,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace sbg {
@@ -170,6 +171,21 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
                 if (n >= p.N) continue;
                 float* c = Cb + m * p.rsC + n * p.csC;
                 *c = p.accumulate ? fmaf(p.alpha, acc[i][j], *c) : p.alpha * acc[i][j];
+            }
+        }
+        if (p.epi.on) {
+            // Fused addend and activation over the thread's own fresh outputs.
+#pragma unroll 1
+            for (int i = 0; i < TM; ++i) {
+                const int64_t m = m0 + (i / 4) * (BM / TM) * 4 + ty * 4 + (i % 4);
+                if (m >= p.M) continue;
+#pragma unroll 1
+                for (int j = 0; j < TN; ++j) {
+                    const int64_t n = n0 + (j / 4) * (BN / TN) * 4 + tx * 4 + (j % 4);
+                    if (n >= p.N) continue;
+                    float* c = Cb + m * p.rsC + n * p.csC;
+                    *c = finish(p.epi, *c, b, m, n);
+                }
             }
         }
     }

@@ -26,7 +26,8 @@
 // keeps one fused multiply-add chain in increasing k, so results are
 // bit-identical to a scalar fmaf loop, to the gather path and across layouts.
 // The epilogue writes alpha*acc (+ C_old) straight from registers with masks
-// on ragged M / N.  Every wait is bounded: on expiry the thread records a
+// on ragged M / N; a fused addend and activation (epilogue.cuh) follow in a
+// second pass over the thread's own outputs.  Every wait is bounded: on expiry the thread records a
 // status code and returns (the copy issuer first waits, again bounded, for the
 // copies it has in flight).
 #include <cuda.h>
@@ -34,7 +35,9 @@
 
 #include <atomic>
 #include <cstdint>
+#include <type_traits>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "schedule.cuh"
@@ -70,6 +73,9 @@ struct Params {
     int64_t dp_tiles;
     int64_t sk_units;       // (tiles_total - dp_tiles) * nk
     int indep;              // split tiles as independent pieces (schedule.cuh)
+    EpiParams epi;          // fused epilogue (epilogue.cuh); epi.on == 0: none
+    int epi_inline;         // ... a bias per column (or none), no activation or ReLU:
+                            // applied in the register epilogue
     float2* ws_partial;     // [grid][kThreads * 64] partial accumulators
     unsigned int* ws_flag;  // [grid] partial-ready flags, zeroed before launch
 };
@@ -275,6 +281,82 @@ __device__ __forceinline__ uint64_t in_flight(uint64_t issued, uint32_t consumed
     return (uint64_t)(uint32_t)((uint32_t)issued - consumed);
 }
 
+
+// Fused addend and activation over the outputs of one thread's micro-tile,
+// which it has just stored, read back 4 rows x 8 columns at a time through L2
+// (float4 when C is row-major), then D added and the activation applied, one
+// function per instantiation.  An addend constant along M (a bias per column)
+// is loaded once per tile.
+template <int ACT>
+__device__ __forceinline__ void fused_pass(const Params& p, const TileCoord& tc, int wm, int wn,
+                                           int lm, int ln) {
+    constexpr int G = 4;
+    float* Cb = p.C + tc.b * p.bsC;
+    const float* Db = p.epi.D ? p.epi.D + tc.b * p.epi.bsD : nullptr;
+    const bool d_per_col = Db && p.epi.rsD == 0;
+    int64_t ncol[TN];
+    float d_col[TN];
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+        ncol[j] = tc.n0 + col_of(wn, ln, j);
+        d_col[j] = (d_per_col && ncol[j] < p.N) ? __ldg(Db + ncol[j] * p.epi.csD) : 0.0f;
+    }
+    const bool vec = p.c_vec4 && ncol[TN - 1] < p.N;   // both runs of 4 wholly inside C
+    auto load = [&](float (&v)[G][TN], int i0) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            const int64_t m = tc.m0 + row_of(wm, lm, i0 + i);
+            const float* crow = Cb + (m < p.M ? m : 0) * p.rsC;
+            if (vec) {
+#pragma unroll
+                for (int h = 0; h < TN / 4; ++h) {
+                    const float4 c4 = m < p.M ? __ldcg(reinterpret_cast<const float4*>(crow + ncol[4 * h]))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[i][4 * h] = c4.x; v[i][4 * h + 1] = c4.y; v[i][4 * h + 2] = c4.z; v[i][4 * h + 3] = c4.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < TN; ++j)
+                    v[i][j] = (m < p.M && ncol[j] < p.N) ? __ldcg(crow + ncol[j] * p.csC) : 0.0f;
+            }
+        }
+    };
+    auto finish_store = [&](float (&v)[G][TN], int i0) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            const int64_t m = tc.m0 + row_of(wm, lm, i0 + i);
+            if (m >= p.M) continue;
+            float* crow = Cb + m * p.rsC;
+            const float* drow = (Db && !d_per_col) ? Db + m * p.epi.rsD : nullptr;
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                float z = v[i][j];
+                if (d_per_col) {
+                    z += d_col[j];
+                } else if (drow && ncol[j] < p.N) {
+                    z += __ldg(drow + ncol[j] * p.epi.csD);
+                }
+                v[i][j] = act_fn<ACT>(z);
+            }
+            if (vec) {
+#pragma unroll
+                for (int h = 0; h < TN / 4; ++h)
+                    *reinterpret_cast<float4*>(crow + ncol[4 * h]) =
+                        make_float4(v[i][4 * h], v[i][4 * h + 1], v[i][4 * h + 2], v[i][4 * h + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < TN; ++j)
+                    if (ncol[j] < p.N) crow[ncol[j] * p.csC] = v[i][j];
+            }
+        }
+    };
+#pragma unroll 1
+    for (int i0 = 0; i0 < TM; i0 += G) {
+        float v[G][TN];
+        load(v, i0);
+        finish_store(v, i0);
+    }
+}
 
 template <int BM, int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -516,54 +598,104 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
             }
         }
 
-        // Epilogue straight from registers.
+        // Epilogue straight from registers.  A fused bias per column, with
+        // ReLU or no activation, is applied here too (a few instructions per
+        // output, in a copy of the epilogue of its own, so the plain one stays
+        // as it is); any other fused epilogue runs as a second pass below.
         const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
         float* Cb = p.C + tc.b * p.bsC;
-#pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const int64_t m = tc.m0 + row_of(wm, lm, i);
-            if (m >= p.M) continue;
-            float* crow = Cb + m * p.rsC;
-            if (p.c_vec4) {
-#pragma unroll
-                for (int h = 0; h < TN / 4; ++h) {
-                    const int64_t n = tc.n0 + col_of(wn, ln, 4 * h);
-                    if (n + 3 < p.N) {
-                        float4* cp = reinterpret_cast<float4*>(crow + n);
-                        float4 v;
-                        if (p.accumulate) {
-                            const float4 o = *cp;
-                            v.x = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 0), o.x);
-                            v.y = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 1), o.y);
-                            v.z = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 2), o.z);
-                            v.w = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 3), o.w);
-                        } else {
-                            v.x = p.alpha * acc_at<PI>(acc, i, 4 * h + 0);
-                            v.y = p.alpha * acc_at<PI>(acc, i, 4 * h + 1);
-                            v.z = p.alpha * acc_at<PI>(acc, i, 4 * h + 2);
-                            v.w = p.alpha * acc_at<PI>(acc, i, 4 * h + 3);
-                        }
-                        *cp = v;
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (n + e < p.N) {
-                                float* c = crow + (n + e);
-                                *c = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + e), *c)
-                                                  : p.alpha * acc_at<PI>(acc, i, 4 * h + e);
-                            }
-                        }
-                    }
-                }
-            } else {
+        auto store_acc = [&](auto fused) {
+            constexpr bool F = decltype(fused)::value;
+            float bias[TN];
+            bool relu = false;
+            if constexpr (F) {
 #pragma unroll
                 for (int j = 0; j < TN; ++j) {
                     const int64_t n = tc.n0 + col_of(wn, ln, j);
-                    if (n >= p.N) continue;
-                    float* c = crow + n * p.csC;
-                    *c = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, j), *c)
-                                      : p.alpha * acc_at<PI>(acc, i, j);
+                    bias[j] = (p.epi.D && n < p.N) ? __ldg(p.epi.D + tc.b * p.epi.bsD + n * p.epi.csD)
+                                                   : 0.0f;
                 }
+                relu = p.epi.act == kActRelu;
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const int64_t m = tc.m0 + row_of(wm, lm, i);
+                if (m >= p.M) continue;
+                float* crow = Cb + m * p.rsC;
+                if (p.c_vec4) {
+#pragma unroll
+                    for (int h = 0; h < TN / 4; ++h) {
+                        const int64_t n = tc.n0 + col_of(wn, ln, 4 * h);
+                        if (n + 3 < p.N) {
+                            float4* cp = reinterpret_cast<float4*>(crow + n);
+                            float4 v;
+                            if (p.accumulate) {
+                                const float4 o = *cp;
+                                v.x = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 0), o.x);
+                                v.y = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 1), o.y);
+                                v.z = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 2), o.z);
+                                v.w = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 3), o.w);
+                            } else {
+                                v.x = p.alpha * acc_at<PI>(acc, i, 4 * h + 0);
+                                v.y = p.alpha * acc_at<PI>(acc, i, 4 * h + 1);
+                                v.z = p.alpha * acc_at<PI>(acc, i, 4 * h + 2);
+                                v.w = p.alpha * acc_at<PI>(acc, i, 4 * h + 3);
+                            }
+                            if constexpr (F) {
+                                v.x += bias[4 * h + 0]; v.y += bias[4 * h + 1];
+                                v.z += bias[4 * h + 2]; v.w += bias[4 * h + 3];
+                                if (relu) {
+                                    v.x = fmaxf(v.x, 0.0f); v.y = fmaxf(v.y, 0.0f);
+                                    v.z = fmaxf(v.z, 0.0f); v.w = fmaxf(v.w, 0.0f);
+                                }
+                            }
+                            *cp = v;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (n + e < p.N) {
+                                    float* c = crow + (n + e);
+                                    float r = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + e), *c)
+                                                           : p.alpha * acc_at<PI>(acc, i, 4 * h + e);
+                                    if constexpr (F) {
+                                        r += bias[4 * h + e];
+                                        if (relu) r = fmaxf(r, 0.0f);
+                                    }
+                                    *c = r;
+                                }
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) {
+                        const int64_t n = tc.n0 + col_of(wn, ln, j);
+                        if (n >= p.N) continue;
+                        float* c = crow + n * p.csC;
+                        float r = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, j), *c)
+                                               : p.alpha * acc_at<PI>(acc, i, j);
+                        if constexpr (F) {
+                            r += bias[j];
+                            if (relu) r = fmaxf(r, 0.0f);
+                        }
+                        *c = r;
+                    }
+                }
+            }
+        };
+        if (p.epi_inline) store_acc(std::true_type{});
+        else store_acc(std::false_type{});
+        if (p.epi.on && !p.epi_inline) {
+            // Fused addend and activation: every thread revisits the outputs it
+            // has just stored (still in L2), so the register epilogue above
+            // stays the plain product's.
+            switch (p.epi.act) {
+                case kActRelu: fused_pass<kActRelu>(p, tc, wm, wn, lm, ln); break;
+                case kActSigmoid: fused_pass<kActSigmoid>(p, tc, wm, wn, lm, ln); break;
+                case kActSilu: fused_pass<kActSilu>(p, tc, wm, wn, lm, ln); break;
+                case kActGeluTanh: fused_pass<kActGeluTanh>(p, tc, wm, wn, lm, ln); break;
+                case kActGeluErf: fused_pass<kActGeluErf>(p, tc, wm, wn, lm, ln); break;
+                default: fused_pass<kActNone>(p, tc, wm, wn, lm, ln); break;
             }
         }
     }
@@ -626,6 +758,9 @@ cudaError_t launch_impl(const Problem& pr, const Plan& plan, int sm_count, cudaS
     p.dp_tiles = plan.stream_k ? plan.dp_tiles : plan.tiles;
     p.sk_units = plan.stream_k ? (plan.tiles - plan.dp_tiles) * p.nk : 0;
     p.indep = plan.stream_k && plan.split_indep ? 1 : 0;
+    p.epi = pr.epi;
+    p.epi_inline = pr.epi.on && (pr.epi.D == nullptr || pr.epi.rsD == 0) &&
+                   (pr.epi.act == kActNone || pr.epi.act == kActRelu) ? 1 : 0;
     p.ws_partial = nullptr;
     p.ws_flag = nullptr;
     if (plan.stream_k) {

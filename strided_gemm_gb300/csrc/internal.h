@@ -11,6 +11,16 @@
 namespace sbg {
 
 // One call of the product, strides in fp32 elements (see include/sbgemm.h).
+// Fused epilogue of sbgemm_fused: out = act(alpha*acc (+ C_old) + D), with D
+// read through its own strides (epilogue.cuh applies it on the device).
+struct EpiParams {
+    const float* D;          // nullptr: no addend
+    int64_t rsD, csD, bsD;
+    int act;                 // SBGEMM_ACT_*
+    int on;                  // D != nullptr || act != SBGEMM_ACT_NONE
+    int d_vec4;              // D has unit stride along N and 16-byte aligned rows
+};
+
 struct Problem {
     const float* A; int64_t rsA, csA, bsA;
     const float* B; int64_t rsB, csB, bsB;
@@ -18,6 +28,7 @@ struct Problem {
     int64_t M, N, K, batch;
     float alpha;
     int accumulate;
+    EpiParams epi;           // all zero: the plain product
 };
 
 // Per-device properties, read once per device and immutable afterwards.

@@ -176,7 +176,8 @@ bool span_in_allocation(const void* base, const Span& s) {
 
 int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empty, Plan* plan) {
     *plan = Plan{};
-    if (empty || (p.K == 0 && p.accumulate)) {
+    // K == 0 with accumulation leaves C as it is, unless an epilogue applies.
+    if (empty || (p.K == 0 && p.accumulate && !p.epi.on)) {
         plan->path = SBGEMM_PATH_NONE;
         return SBGEMM_OK;
     }
@@ -274,6 +275,7 @@ Problem make_problem(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     p.M = M; p.N = N; p.K = K; p.batch = batch;
     p.alpha = alpha;
     p.accumulate = accumulate ? 1 : 0;
+    p.epi = EpiParams{nullptr, 0, 0, 0, SBGEMM_ACT_NONE, 0, 0};
     return p;
 }
 
@@ -308,6 +310,70 @@ int planning_sm_count() {
     }
     cudaGetLastError();
     return 152;
+}
+
+// Validates, plans and launches one product (with its fused epilogue, if
+// any) on `stream`.
+int run(Problem& p, const sbgemm_options& o, void* stream) {
+    Span sa{}, sb{}, sc{};
+    bool empty = false;
+    int st = validate(p, &sa, &sb, &sc, &empty);
+    if (st) return st;
+    if (empty || (p.K == 0 && p.accumulate && !p.epi.on)) return SBGEMM_OK;
+    Span sd{};
+    if (p.epi.D) {
+        // The addend is read while C is written: it must be device memory
+        // outside C's span.
+        if (!aligned(p.epi.D, 4)) return SBGEMM_ERR_INVALID_VALUE;
+        if (!operand_span(p.batch, p.M, p.N, p.epi.bsD, p.epi.rsD, p.epi.csD, &sd))
+            return SBGEMM_ERR_INVALID_VALUE;
+        const __int128 dlo = (__int128)reinterpret_cast<uintptr_t>(p.epi.D) + (__int128)sd.lo * 4;
+        const __int128 dhi = (__int128)reinterpret_cast<uintptr_t>(p.epi.D) + (__int128)sd.hi * 4 + 4;
+        const __int128 clo = (__int128)reinterpret_cast<uintptr_t>(p.C) + (__int128)sc.lo * 4;
+        const __int128 chi = (__int128)reinterpret_cast<uintptr_t>(p.C) + (__int128)sc.hi * 4 + 4;
+        if (dlo < chi && clo < dhi) return SBGEMM_ERR_OUTPUT_OVERLAP;
+    }
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
+    const DeviceProps* props = device_props(dev);
+    if (!props) return SBGEMM_ERR_CUDA;
+
+    if (!span_in_allocation(p.C, sc)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    if (p.K > 0 && (!span_in_allocation(p.A, sa) || !span_in_allocation(p.B, sb)))
+        return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    if (p.epi.D && !span_in_allocation(p.epi.D, sd)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+
+    Plan plan;
+    st = make_plan(p, o, props->sm_count, false, &plan);
+    if (st) return st;
+
+    if (plan.stream_k) {
+        // The workspace is written by the kernel: it must be device memory and
+        // must not meet any operand.
+        const Span sw{0, (int64_t)(o.workspace_bytes / 4) - 1};
+        if (!span_in_allocation(o.workspace, sw)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+        auto meets = [&](const void* base, const Span& sp) {
+            const __int128 lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)sp.lo * 4;
+            const __int128 hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)sp.hi * 4 + 4;
+            const __int128 wlo = (__int128)reinterpret_cast<uintptr_t>(o.workspace);
+            const __int128 whi = wlo + (__int128)o.workspace_bytes;
+            return lo < whi && wlo < hi;
+        };
+        if (meets(p.C, sc) || meets(p.A, sa) || meets(p.B, sb) || (p.epi.D && meets(p.epi.D, sd)))
+            return SBGEMM_ERR_OUTPUT_OVERLAP;
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaSuccess;
+    switch (plan.path) {
+        case SBGEMM_PATH_GATHER_FFMA: err = launch_gather_ffma(p, plan, s); break;
+        case SBGEMM_PATH_TMA_FFMA: err = launch_tma_ffma(p, plan, props->sm_count, s); break;
+        case SBGEMM_PATH_TMA_TF32: err = launch_tf32_tc(p, plan, props->sm_count, s); break;
+        default: return SBGEMM_ERR_UNSUPPORTED;
+    }
+    if (err != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
+    return SBGEMM_OK;
 }
 
 }  // namespace
@@ -367,50 +433,31 @@ int sbgemm_ex(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     if (st) return st;
     Problem p = make_problem(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                              M, N, K, batch, alpha, accumulate);
-    Span sa{}, sb{}, sc{};
-    bool empty = false;
-    st = validate(p, &sa, &sb, &sc, &empty);
+    return run(p, o, stream);
+}
+
+int sbgemm_fused(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
+                 const float* B, int64_t rsB, int64_t csB, int64_t bsB,
+                 float* C, int64_t rsC, int64_t csC, int64_t bsC,
+                 int64_t M, int64_t N, int64_t K, int64_t batch,
+                 float alpha, int accumulate, const sbgemm_epilogue* epi,
+                 void* stream, const sbgemm_options* opt) {
+    sbgemm_options o;
+    int st = check_options(opt, &o);
     if (st) return st;
-    if (empty || (p.K == 0 && p.accumulate)) return SBGEMM_OK;
-
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
-    const DeviceProps* props = device_props(dev);
-    if (!props) return SBGEMM_ERR_CUDA;
-
-    if (!span_in_allocation(p.C, sc)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
-    if (p.K > 0 && (!span_in_allocation(p.A, sa) || !span_in_allocation(p.B, sb)))
-        return SBGEMM_ERR_NOT_DEVICE_MEMORY;
-
-    Plan plan;
-    st = make_plan(p, o, props->sm_count, false, &plan);
-    if (st) return st;
-
-    if (plan.stream_k) {
-        // The workspace is written by the kernel: it must be device memory and
-        // must not meet any operand.
-        const Span sw{0, (int64_t)(o.workspace_bytes / 4) - 1};
-        if (!span_in_allocation(o.workspace, sw)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
-        auto meets = [&](const void* base, const Span& sp) {
-            const __int128 lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)sp.lo * 4;
-            const __int128 hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)sp.hi * 4 + 4;
-            const __int128 wlo = (__int128)reinterpret_cast<uintptr_t>(o.workspace);
-            const __int128 whi = wlo + (__int128)o.workspace_bytes;
-            return lo < whi && wlo < hi;
-        };
-        if (meets(p.C, sc) || meets(p.A, sa) || meets(p.B, sb)) return SBGEMM_ERR_OUTPUT_OVERLAP;
+    Problem p = make_problem(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                             M, N, K, batch, alpha, accumulate);
+    if (epi) {
+        if (epi->activation < SBGEMM_ACT_NONE || epi->activation > SBGEMM_ACT_GELU_ERF)
+            return SBGEMM_ERR_INVALID_VALUE;
+        for (int r : epi->reserved) if (r != 0) return SBGEMM_ERR_INVALID_VALUE;
+        const bool d_vec4 = epi->D && (epi->csD == 1 || N == 1) && aligned(epi->D, 16) &&
+                            epi->rsD % 4 == 0 && epi->bsD % 4 == 0;
+        p.epi = EpiParams{epi->D, epi->rsD, epi->csD, epi->bsD, epi->activation,
+                          (epi->D != nullptr || epi->activation != SBGEMM_ACT_NONE) ? 1 : 0,
+                          d_vec4 ? 1 : 0};
     }
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t err = cudaSuccess;
-    switch (plan.path) {
-        case SBGEMM_PATH_GATHER_FFMA: err = launch_gather_ffma(p, plan, s); break;
-        case SBGEMM_PATH_TMA_FFMA: err = launch_tma_ffma(p, plan, props->sm_count, s); break;
-        case SBGEMM_PATH_TMA_TF32: err = launch_tf32_tc(p, plan, props->sm_count, s); break;
-        default: return SBGEMM_ERR_UNSUPPORTED;
-    }
-    if (err != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
-    return SBGEMM_OK;
+    return run(p, o, stream);
 }
 
 int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,

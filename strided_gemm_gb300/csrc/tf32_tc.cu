@@ -12,9 +12,10 @@
 //    the stage when its MMAs are done, and marks the accumulator full after the
 //    tile's last slice.
 //  * warps 2..5: epilogue.  Each warp reads its 32 TMEM lanes (rows) in 32-
-//    column pieces (tcgen05.ld 32x32b.x32), forms alpha*acc (+ C_old) and
-//    stores with masks on ragged M / N, then releases the accumulator, so the
-//    next tile's MMAs overlap this tile's stores.
+//    column pieces (tcgen05.ld 32x32b.x32), stages each piece in shared
+//    memory, and writes alpha*acc (+ C_old), with the fused addend and
+//    activation if any, in 128-byte rows with masks on ragged M / N; then it
+//    releases the accumulator, so the next tile's MMAs overlap these stores.
 // With a workspace the last waves are split along K across the grid (the
 // stream-K work list shared with the FFMA kernel): a head item's accumulator
 // goes to the workspace instead of C, and the epilogue warps seed the TMEM
@@ -32,7 +33,9 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstring>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "schedule.cuh"
@@ -64,8 +67,9 @@ struct Params {
     float alpha;
     int accumulate;
     int a_bcast, b_bcast;
-    int c_vec4;
+    int c_tma;                    // C goes out through its tensor map (unit stride along N)
     int64_t dp_tiles, sk_units;   // work list (see schedule.cuh)
+    EpiParams epi;                // fused epilogue (epilogue.cuh); epi.on == 0: none
     float4* ws_partial;           // [grid][8 chunks][8 quads][128 rows] partial sums
     unsigned int* ws_flag;        // [grid] partial-ready flags, zeroed before launch
 };
@@ -73,6 +77,9 @@ struct Params {
 struct Smem {
     float a[kStages][BM * BK];
     float b[kStages][BN * BK];
+    // Per epilogue warp: one 32 x 32 piece of C in the 128-byte swizzled layout
+    // of its tensor map (16-byte chunk q of row r at chunk q ^ (r & 7)).
+    alignas(1024) float stage[kEpiWarps][32 * 32];
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t acc_full[2];
@@ -80,10 +87,12 @@ struct Smem {
     uint64_t mma_done;
     uint64_t seeded[2];       // the epilogue warps wrote a tail's partial into TMEM buffer b
     uint64_t stored;          // every epilogue thread wrote its head partial
+    uint64_t c_old[kEpiWarps];   // a warp's C_old piece landed in its staging tile
     Schedule sched;
     uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // Instruction descriptor, kind::tf32: D fp32, A and B tf32, both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.
@@ -240,10 +249,93 @@ __device__ __forceinline__ bool seed_tail(Smem& sh, uint32_t tmem, const Params&
     return true;
 }
 
-__device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const Params& p, int warp,
-                                         int lane) {
+// Writes one finished tile's rows [quarter*32, +32) through the C tensor map:
+// per 32-column piece the warp forms alpha*acc (+ C_old, itself brought in by
+// a TMA load), adds the fused addend and applies ACT, writes the piece into
+// its staging tile and lane 0 issues one bulk tensor store (the parts outside
+// C are not written).  Returns false if a C_old load did not land in time.
+template <int ACT>
+__device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap, const Params& p,
+                                               const TileCoord& tc, uint32_t taddr, int quarter,
+                                               int lane, int ew, uint32_t& c_loads) {
+    float* st = sh.stage[ew];
+    const int64_t m_base = tc.m0 + quarter * 32;
+    const int64_t m = m_base + lane;
+    const float* drow = (p.epi.D && m < p.M) ? p.epi.D + tc.b * p.epi.bsD + m * p.epi.rsD : nullptr;
+    const bool rows_in = m_base < p.M;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        const int64_t n0 = tc.n0 + c * 32;
+        const bool piece_in = rows_in && n0 < p.N;
+        // The staging tile is free once the previous piece's store has read it.
+        if (lane == 0) {
+            bulk_wait_read_all();
+            if (piece_in && p.accumulate) {
+                mbar_arrive_expect_tx(&sh.c_old[ew], 32 * 32 * 4);
+                tma_load_3d(st, cmap, &sh.c_old[ew], (int)n0, (int)m_base, (int)tc.b);
+            }
+        }
+        __syncwarp();
+        float v[32];
+        tmem_ld32(taddr + c * 32, v);      // whole warp, converged: row m, columns n0..n0+31
+        if (!piece_in) continue;
+        if (p.accumulate) {
+            if (!mbar_wait(&sh.c_old[ew], c_loads & 1u)) return false;
+            ++c_loads;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 o = *reinterpret_cast<const float4*>(st + lane * 32 + ((q ^ (lane & 7)) << 2));
+                v[4 * q + 0] = fmaf(p.alpha, v[4 * q + 0], o.x);
+                v[4 * q + 1] = fmaf(p.alpha, v[4 * q + 1], o.y);
+                v[4 * q + 2] = fmaf(p.alpha, v[4 * q + 2], o.z);
+                v[4 * q + 3] = fmaf(p.alpha, v[4 * q + 3], o.w);
+            }
+            __syncwarp();                  // every lane has read its C_old row
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = p.alpha * v[e];
+        }
+        if (drow) {
+            if (p.epi.d_vec4 && n0 + 32 <= p.N) {
+                const float4* d4 = reinterpret_cast<const float4*>(drow + n0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 d = __ldg(d4 + q);
+                    v[4 * q + 0] += d.x;
+                    v[4 * q + 1] += d.y;
+                    v[4 * q + 2] += d.z;
+                    v[4 * q + 3] += d.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (n0 + e < p.N) v[e] += __ldg(drow + (n0 + e) * p.epi.csD);
+            }
+        }
+        if constexpr (ACT != kActNone) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = act_fn<ACT>(v[e]);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(st + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(cmap, st, (int)n0, (int)m_base, (int)tc.b);
+            bulk_commit();
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensorMap* cmap,
+                                         const Params& p, int warp, int lane) {
     const int quarter = warp & 3;               // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
+    const int ew = warp - 2;                    // epilogue warp index: staging tile, C_old barrier
+    uint32_t c_loads = 0;                       // C_old pieces this warp has loaded
     const int64_t n_items = sh.sched.n_items;
     if (n_items > 0 && sh.sched.item(0, p.nk).mode == kTail &&
         !seed_tail(sh, tmem, p, quarter, lane, 0)) {
@@ -314,7 +406,24 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const Params& 
                 }
                 st_release_gpu(p.ws_flag + blockIdx.x, 1u);
             }
+        } else if (p.c_tma) {
+            const TileCoord tc = tile_coord(p, itm.tile);
+            bool ok;
+            switch (p.epi.act) {
+                case kActRelu: ok = store_tile_tma<kActRelu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
+                case kActSigmoid: ok = store_tile_tma<kActSigmoid>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
+                case kActSilu: ok = store_tile_tma<kActSilu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
+                case kActGeluTanh: ok = store_tile_tma<kActGeluTanh>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
+                case kActGeluErf: ok = store_tile_tma<kActGeluErf>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
+                default: ok = store_tile_tma<kActNone>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
+            }
+            if (!ok) {
+                record_status(&g_wait_status, kWaitFull);
+                return;
+            }
         } else {
+            // Any other C: a lane per row, the columns in turn (128-byte rows
+            // when C is column-major).
             const TileCoord tc = tile_coord(p, itm.tile);
             const int64_t m = tc.m0 + row;
             const bool row_ok = m < p.M;
@@ -325,29 +434,15 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const Params& 
                 __syncwarp();
                 tmem_ld32(taddr + c * 32, v);      // whole warp, converged, every row
                 const int64_t n0 = tc.n0 + c * 32;
-                if (!row_ok || n0 >= p.N) {
-                    // nothing of this piece is in C
-                } else if (p.c_vec4 && n0 + 32 <= p.N) {
-                    float4* cp = reinterpret_cast<float4*>(crow + n0);
+                if (!row_ok || n0 >= p.N) continue;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (p.accumulate) o = cp[q];
-                        float4 r;
-                        r.x = p.accumulate ? fmaf(p.alpha, v[4 * q + 0], o.x) : p.alpha * v[4 * q + 0];
-                        r.y = p.accumulate ? fmaf(p.alpha, v[4 * q + 1], o.y) : p.alpha * v[4 * q + 1];
-                        r.z = p.accumulate ? fmaf(p.alpha, v[4 * q + 2], o.z) : p.alpha * v[4 * q + 2];
-                        r.w = p.accumulate ? fmaf(p.alpha, v[4 * q + 3], o.w) : p.alpha * v[4 * q + 3];
-                        cp[q] = r;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int64_t n = n0 + e;
-                        if (n < p.N) {
-                            float* cptr = crow + n * p.csC;
-                            *cptr = p.accumulate ? fmaf(p.alpha, v[e], *cptr) : p.alpha * v[e];
-                        }
+                for (int e = 0; e < 32; ++e) {
+                    const int64_t n = n0 + e;
+                    if (n < p.N) {
+                        float* cptr = crow + n * p.csC;
+                        float r = p.accumulate ? fmaf(p.alpha, v[e], *cptr) : p.alpha * v[e];
+                        if (p.epi.on) r = finish(p.epi, r, tc.b, m, n);
+                        *cptr = r;
                     }
                 }
             }
@@ -364,7 +459,7 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const Params& 
 
 __global__ void __launch_bounds__(kThreads, 1)
 tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-               const Params p) {
+               const __grid_constant__ CUtensorMap tcm, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& sh = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
@@ -382,10 +477,12 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         mbar_init(&sh.seeded[0], kEpiWarps);
         mbar_init(&sh.seeded[1], kEpiWarps);
         mbar_init(&sh.stored, kEpiWarps * 32);
+        for (int w = 0; w < kEpiWarps; ++w) mbar_init(&sh.c_old[w], 1);
         sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
         fence_mbar_init();
         prefetch_tensormap(&ta);
         prefetch_tensormap(&tb);
+        if (p.c_tma) prefetch_tensormap(&tcm);
     }
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, kTmemCols);
@@ -401,7 +498,9 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     } else if (warp == 1) {
         if (lane == 0) mma_issuer(sh, tmem, p);
     } else {
-        epilogue(sh, tmem, p, warp, lane);
+        epilogue(sh, tmem, &tcm, p, warp, lane);
+        // Shared memory must outlive the bulk stores that read it.
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -421,6 +520,27 @@ bool make_kmajor_map(CUtensorMap* map, const float* base, int64_t K, int64_t row
     const uint64_t strides[2] = {(uint64_t)so_b, (uint64_t)sb_b};
     const uint32_t box[3] = {(uint32_t)BK, (uint32_t)box_rows, 1};
     return encode_tmap_f32_3d(map, base, dims, strides, box, true);
+}
+
+// C's tensor map for the epilogue's bulk stores and C_old loads: unit stride
+// along N, a 16-byte aligned base, positive 16-byte multiple strides laid out
+// without overlap (row stride >= N, batch stride >= one matrix), extents that
+// fit 32-bit coordinates; a 32 x 32 box, 128-byte swizzle.  False: C is
+// written by the threads directly.
+bool make_c_map(CUtensorMap* map, const Problem& pr) {
+    if (pr.csC != 1 && pr.N > 1) return false;
+    if (reinterpret_cast<uintptr_t>(pr.C) % 16 != 0) return false;
+    const int64_t lim = (int64_t)1 << 31;
+    if (pr.N >= lim || pr.M >= lim || pr.batch >= lim) return false;
+    auto ok_stride = [](int64_t st) { return st > 0 && (st * 4) % 16 == 0 && st * 4 < ((int64_t)1 << 40); };
+    const int64_t row_b = pr.M > 1 ? pr.rsC * 4 : ((pr.N * 4 + 15) / 16) * 16;
+    if (pr.M > 1 && (!ok_stride(pr.rsC) || pr.rsC < pr.N)) return false;
+    const bool batched = pr.batch > 1;
+    if (batched && (!ok_stride(pr.bsC) || pr.bsC * 4 < row_b * pr.M)) return false;
+    const uint64_t dims[3] = {(uint64_t)pr.N, (uint64_t)pr.M, (uint64_t)pr.batch};
+    const uint64_t strides[2] = {(uint64_t)row_b, batched ? (uint64_t)pr.bsC * 4 : (uint64_t)row_b * pr.M};
+    const uint32_t box[3] = {32, 32, 1};
+    return encode_tmap_f32_3d(map, pr.C, dims, strides, box, true);
 }
 
 }  // namespace
@@ -454,11 +574,13 @@ cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cu
     p.accumulate = pr.accumulate;
     p.a_bcast = a_bc;
     p.b_bcast = b_bc;
-    p.c_vec4 = pr.csC == 1 && (reinterpret_cast<uintptr_t>(pr.C) % 16 == 0) &&
-               (pr.M == 1 || pr.rsC % 4 == 0) && (pr.batch == 1 || pr.bsC % 4 == 0);
+    CUtensorMap tcm;
+    std::memset(&tcm, 0, sizeof(tcm));
+    p.c_tma = make_c_map(&tcm, pr) ? 1 : 0;
     const int64_t grid = plan.ctas;
     p.dp_tiles = plan.stream_k ? plan.dp_tiles : plan.tiles;
     p.sk_units = plan.stream_k ? (plan.tiles - plan.dp_tiles) * p.nk : 0;
+    p.epi = pr.epi;
     p.ws_partial = nullptr;
     p.ws_flag = nullptr;
     if (plan.stream_k) {
@@ -478,11 +600,11 @@ cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cu
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel, ta, tb, p);
+        e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel, ta, tb, tcm, p);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    tf32_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(ta, tb, p);
+    tf32_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(ta, tb, tcm, p);
     return cudaGetLastError();
 }
 
