@@ -192,9 +192,10 @@ def case_args(case, dA, dB, dC):
 
 
 def kernel_source_digest(path_name):
-    files = {"gather_ffma": ["ffma_gather.cu"],
-             "tma_ffma": ["ffma_tma.cu", "schedule.cuh", "ptx.cuh"],
-             "tma_tf32": ["tf32_tc.cu", "schedule.cuh", "ptx.cuh"]}.get(path_name, [])
+    common = ["internal.h", "epilogue.cuh"]
+    files = {"gather_ffma": ["ffma_gather.cu"] + common,
+             "tma_ffma": ["ffma_tma.cu", "schedule.cuh", "ptx.cuh"] + common,
+             "tma_tf32": ["tf32_tc.cu", "schedule.cuh", "ptx.cuh"] + common}.get(path_name, [])
     h = hashlib.sha256()
     for f in files:
         p = os.path.join(ROOT, "strided_gemm_gb300", "csrc", f)

@@ -77,9 +77,10 @@ struct Params {
 struct Smem {
     float a[kStages][BM * BK];
     float b[kStages][BN * BK];
-    // Per epilogue warp: one 32 x 32 piece of C in the 128-byte swizzled layout
-    // of its tensor map (16-byte chunk q of row r at chunk q ^ (r & 7)).
-    alignas(1024) float stage[kEpiWarps][32 * 32];
+    // Per epilogue warp: two 32 x 32 pieces of C (alternating by store) in the
+    // 128-byte swizzled layout of its tensor map (16-byte chunk q of row r at
+    // chunk q ^ (r & 7)).
+    alignas(1024) float stage[kEpiWarps][2][32 * 32];
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t acc_full[2];
@@ -257,8 +258,8 @@ __device__ __forceinline__ bool seed_tail(Smem& sh, uint32_t tmem, const Params&
 template <int ACT>
 __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap, const Params& p,
                                                const TileCoord& tc, uint32_t taddr, int quarter,
-                                               int lane, int ew, uint32_t& c_loads) {
-    float* st = sh.stage[ew];
+                                               int lane, int ew, uint32_t& c_loads,
+                                               uint32_t& stores) {
     const int64_t m_base = tc.m0 + quarter * 32;
     const int64_t m = m_base + lane;
     const float* drow = (p.epi.D && m < p.M) ? p.epi.D + tc.b * p.epi.bsD + m * p.epi.rsD : nullptr;
@@ -267,15 +268,22 @@ __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap
     for (int c = 0; c < BN / 32; ++c) {
         const int64_t n0 = tc.n0 + c * 32;
         const bool piece_in = rows_in && n0 < p.N;
-        // The staging tile is free once the previous piece's store has read it.
-        if (lane == 0) {
-            bulk_wait_read_all();
-            if (piece_in && p.accumulate) {
-                mbar_arrive_expect_tx(&sh.c_old[ew], 32 * 32 * 4);
-                tma_load_3d(st, cmap, &sh.c_old[ew], (int)n0, (int)m_base, (int)tc.b);
+        // Stores alternate between the warp's two staging tiles; a tile is free
+        // once the store before the most recent one has read it.  With
+        // accumulation C_old must land there first; without, the tile is waited
+        // for only just before it is written, so that the TMEM load and the
+        // arithmetic overlap the earlier stores.
+        float* st = sh.stage[ew][stores & 1u];
+        if (p.accumulate) {
+            if (lane == 0) {
+                bulk_wait_read_all_but_one();
+                if (piece_in) {
+                    mbar_arrive_expect_tx(&sh.c_old[ew], 32 * 32 * 4);
+                    tma_load_3d(st, cmap, &sh.c_old[ew], (int)n0, (int)m_base, (int)tc.b);
+                }
             }
+            __syncwarp();
         }
-        __syncwarp();
         float v[32];
         tmem_ld32(taddr + c * 32, v);      // whole warp, converged: row m, columns n0..n0+31
         if (!piece_in) continue;
@@ -316,6 +324,10 @@ __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = act_fn<ACT>(v[e]);
         }
+        if (!p.accumulate) {
+            if (lane == 0) bulk_wait_read_all_but_one();
+            __syncwarp();
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             *reinterpret_cast<float4*>(st + lane * 32 + ((q ^ (lane & 7)) << 2)) =
@@ -326,6 +338,7 @@ __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap
             tma_store_3d(cmap, st, (int)n0, (int)m_base, (int)tc.b);
             bulk_commit();
         }
+        ++stores;
     }
     return true;
 }
@@ -336,6 +349,7 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
     const int row = quarter * 32 + lane;
     const int ew = warp - 2;                    // epilogue warp index: staging tile, C_old barrier
     uint32_t c_loads = 0;                       // C_old pieces this warp has loaded
+    uint32_t stores = 0;                        // bulk stores this warp has issued
     const int64_t n_items = sh.sched.n_items;
     if (n_items > 0 && sh.sched.item(0, p.nk).mode == kTail &&
         !seed_tail(sh, tmem, p, quarter, lane, 0)) {
@@ -410,12 +424,12 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
             const TileCoord tc = tile_coord(p, itm.tile);
             bool ok;
             switch (p.epi.act) {
-                case kActRelu: ok = store_tile_tma<kActRelu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
-                case kActSigmoid: ok = store_tile_tma<kActSigmoid>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
-                case kActSilu: ok = store_tile_tma<kActSilu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
-                case kActGeluTanh: ok = store_tile_tma<kActGeluTanh>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
-                case kActGeluErf: ok = store_tile_tma<kActGeluErf>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
-                default: ok = store_tile_tma<kActNone>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads); break;
+                case kActRelu: ok = store_tile_tma<kActRelu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
+                case kActSigmoid: ok = store_tile_tma<kActSigmoid>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
+                case kActSilu: ok = store_tile_tma<kActSilu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
+                case kActGeluTanh: ok = store_tile_tma<kActGeluTanh>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
+                case kActGeluErf: ok = store_tile_tma<kActGeluErf>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
+                default: ok = store_tile_tma<kActNone>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
             }
             if (!ok) {
                 record_status(&g_wait_status, kWaitFull);
