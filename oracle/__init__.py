@@ -201,3 +201,40 @@ def fused_points(A, B, C, M, N, K, batch, alpha, accumulate, D, act, idx, lib=No
     if rc != 0:
         raise ValueError(f"oracle: unknown activation {act}")
     return out, z, bound
+
+
+# ---- fused attention: O = softmax(alpha * Q K^T [causal]) V ----------------------
+
+def attention(Q, K, V, M, N, D, Dv, batch, alpha, causal=False, q_len=0, lib=None):
+    """The attention oracle (sbgemm_ref_attention).  Q, K, V are operands
+    (storage, offset, rs, cs, bs): Q[b,m,d], K[b,n,d], V[b,n,e].  Returns (O,
+    weight, smag): O and weight = sum_n P|V| of shape [batch, M, Dv], and smag
+    [batch, M], the largest |alpha| * sum_d |q k| over the kept keys."""
+    lib = lib or load()
+    if not hasattr(lib, "_attn_bound"):
+        lib.sbgemm_ref_attention.restype = ctypes.c_int
+        lib.sbgemm_ref_attention.argtypes = [
+            _fp, _i64, _i64, _i64, _fp, _i64, _i64, _i64, _fp, _i64, _i64, _i64,
+            _i64, _i64, _i64, _i64, _i64, ctypes.c_float, ctypes.c_int, _i64, _fp, _fp, _fp]
+        lib._attn_bound = True
+    q_len = int(q_len) if q_len else M
+    if causal and not (0 < q_len <= N):
+        raise ValueError("oracle: causal attention needs 0 < q_len <= N")
+    for op, rows, cols, name in ((Q, M, D, "Q"), (K, N, D, "K"), (V, N, Dv, "V")):
+        if not _span_ok(op, batch, rows, cols):
+            raise ValueError(f"oracle: {name} strides reach outside its storage")
+    O = np.zeros((batch, M, Dv), dtype=np.float64)
+    W = np.zeros((batch, M, Dv), dtype=np.float64)
+    S = np.zeros((batch, M), dtype=np.float64)
+    rc = lib.sbgemm_ref_attention(_ptr(Q), Q.rs, Q.cs, Q.bs, _ptr(K), K.rs, K.cs, K.bs,
+                                  _ptr(V), V.rs, V.cs, V.bs, M, N, D, Dv, batch,
+                                  float(alpha), int(bool(causal)), q_len,
+                                  O.ctypes.data, W.ctypes.data, S.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"oracle sbgemm_ref_attention failed with {rc}")
+    return O, W, S
+
+
+def attention_case(case, lib=None):
+    return attention(case.Q, case.K, case.V, case.M, case.N, case.D, case.Dv, case.batch,
+                     case.alpha, case.causal, case.q_len, lib=lib)

@@ -226,3 +226,74 @@ int sbgemm_ref_epilogue_points(const float* D, int64_t rsD, int64_t csD, int64_t
     }
     return 0;
 }
+
+/*
+ * Fused attention (test infrastructure, as above).
+ *
+ * The three steps of "rvllm CUDA path", section "What's basic about it"
+ * (scores, softmax, then probs @ V), here without the scores ever leaving the
+ * computation, for a batch of (sequence, head) problems laid out by strides
+ * like the product's operands:
+ *     s[n]  = alpha * sum_d Q[b,m,d] * K[b,n,d]        (fp64)
+ *     masked keys (causal: n > position(m)) drop out of the softmax,
+ *     position(m) = (m mod q_len) + N - q_len,
+ *     P[n]  = exp(s[n] - max_n s) / sum_n exp(s[n] - max_n s)   (the three
+ *             passes of the page's softmax: max, sum of exponentials, divide)
+ *     O[b,m,e] = sum_n P[n] * V[b,n,e]
+ * and, for the tolerance of a GPU result,
+ *     weight[b,m,e] = sum_n P[n] * |V[b,n,e]|
+ *     smag[b,m]     = max over kept n of |alpha| * sum_d |Q[b,m,d] * K[b,n,d]|.
+ * Stacked grouped-query heads are rows m of one batch entry with q_len the
+ * rows per head ("rvllm CUDA path", section "Matmuls go to cuBLAS").
+ * Returns 0, or -1 on a bad argument.
+ */
+int sbgemm_ref_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
+                         const float* K, int64_t rsK, int64_t csK, int64_t bsK,
+                         const float* V, int64_t rsV, int64_t csV, int64_t bsV,
+                         int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
+                         float alpha, int causal, int64_t q_len,
+                         double* O, double* weight, double* smag) {
+    if (M < 0 || N <= 0 || D < 0 || Dv < 0 || batch < 0) return -1;
+    if (causal && (q_len <= 0 || q_len > N)) return -1;
+    double* s = (double*)malloc((size_t)N * sizeof(double));
+    double* mag = (double*)malloc((size_t)N * sizeof(double));
+    if (!s || !mag) { free(s); free(mag); return -1; }
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t m = 0; m < M; ++m) {
+            const int64_t kept = causal ? (m % q_len) + N - q_len + 1 : N;
+            double mx = -INFINITY, big = 0.0;
+            for (int64_t n = 0; n < kept; ++n) {
+                double acc = 0.0, t = 0.0;
+                for (int64_t d = 0; d < D; ++d) {
+                    const double prod = (double)Q[b * bsQ + m * rsQ + d * csQ] *
+                                        (double)K[b * bsK + n * rsK + d * csK];
+                    acc += prod;
+                    t += fabs(prod);
+                }
+                s[n] = (double)alpha * acc;
+                mag[n] = fabs((double)alpha) * t;
+                if (s[n] > mx) mx = s[n];
+                if (mag[n] > big) big = mag[n];
+            }
+            double l = 0.0;
+            for (int64_t n = 0; n < kept; ++n) {
+                s[n] = exp(s[n] - mx);
+                l += s[n];
+            }
+            for (int64_t e = 0; e < Dv; ++e) {
+                double o = 0.0, w = 0.0;
+                for (int64_t n = 0; n < kept; ++n) {
+                    const double v = (double)V[b * bsV + n * rsV + e * csV];
+                    o += s[n] * v;
+                    w += s[n] * fabs(v);
+                }
+                O[(b * M + m) * Dv + e] = o / l;
+                if (weight) weight[(b * M + m) * Dv + e] = w / l;
+            }
+            if (smag) smag[b * M + m] = big;
+        }
+    }
+    free(s);
+    free(mag);
+    return 0;
+}

@@ -413,3 +413,90 @@ def run_epilogue_pins(lib=None):
 
 def test_fused_epilogue_pins():
     assert run_epilogue_pins() == 0
+
+
+# ---- fused attention ----------------------------------------------------------
+
+def _attn(Qa, Ka, Va, alpha, causal=False, q_len=0, lib=None):
+    """Oracle attention on dense arrays Q [b,M,D], K [b,N,D], V [b,N,Dv]."""
+    b, M, D = Qa.shape
+    N, Dv = Ka.shape[1], Va.shape[2]
+    op = lambda a: wl.Operand(np.ascontiguousarray(a, dtype=np.float32).reshape(-1), 0,
+                              a.shape[2], 1, a.shape[1] * a.shape[2])
+    return oracle.attention(op(Qa), op(Ka), op(Va), M, N, D, Dv, b, alpha, causal, q_len, lib=lib)
+
+
+def run_attention_pins(lib=None):
+    """Pins of the attention oracle against facts that do not restate its
+    formula; returns the number of failed checks (also used on mutated builds)."""
+    rng = np.random.default_rng(31)
+    attn = lambda *a, **k: _attn(*a, lib=lib, **k)
+    bad = 0
+    b, M, N, D = 2, 6, 9, 5
+    K = rng.standard_normal((b, N, D)).astype(np.float32)
+    V = rng.standard_normal((b, N, D)).astype(np.float32)
+    # Zero queries: every score equal, so O is the mean of the kept value rows.
+    O, W, _ = attn(np.zeros((b, M, D), np.float32), K, V, 0.5)
+    bad += not np.allclose(O, np.broadcast_to(V.astype(np.float64).mean(axis=1, keepdims=True), O.shape),
+                           rtol=0, atol=1e-12)
+    O, _, _ = attn(np.zeros((b, M, D), np.float32), K, V, 0.5, causal=True, q_len=M)
+    for m in range(M):
+        kept = m + N - M + 1
+        bad += not np.allclose(O[:, m], V[:, :kept].astype(np.float64).mean(axis=1), rtol=0, atol=1e-12)
+    # Causal, q_len = N: the first query sees the first key only.
+    Q = rng.standard_normal((b, N, D)).astype(np.float32)
+    O, _, _ = attn(Q, K, V, 0.7, causal=True, q_len=N)
+    bad += not np.array_equal(O[:, 0], V[:, 0].astype(np.float64))
+    # One-hot queries and keys: score alpha on the diagonal, 0 elsewhere.
+    Nh, a = 7, 3.0
+    E = np.eye(Nh, dtype=np.float32)[None]
+    Vh = rng.standard_normal((1, Nh, 4)).astype(np.float32).astype(np.float64)
+    O, _, _ = attn(E, E, Vh, a)
+    want = (np.exp(a) * Vh[0] + (Vh[0].sum(axis=0, keepdims=True) - Vh[0])) / (np.exp(a) + Nh - 1)
+    bad += not np.allclose(O[0], want, rtol=0, atol=1e-12)
+    # A per-row shift of every score (an extra dimension: K = 1, Q = c) changes nothing.
+    c = rng.standard_normal((b, M, 1)).astype(np.float32) * 4
+    Qr = rng.standard_normal((b, M, D)).astype(np.float32)
+    O1, _, _ = attn(Qr, K, V, 0.5)
+    O2, _, _ = attn(np.concatenate([Qr, c], 2), np.concatenate([K, np.ones((b, N, 1), np.float32)], 2), V, 0.5)
+    bad += not np.allclose(O1, O2, rtol=0, atol=1e-12)
+    # Keys and values permuted together (no mask): nothing changes.
+    perm = rng.permutation(N)
+    O3, _, _ = attn(Qr, K[:, perm], V[:, perm], 0.5)
+    bad += not np.allclose(O1, O3, rtol=0, atol=1e-12)
+    # Linear in V (integer values, so V1 + V2 is exact in fp32).
+    V1 = rng.integers(-8, 9, size=(b, N, D)).astype(np.float32)
+    V2 = rng.integers(-8, 9, size=(b, N, D)).astype(np.float32)
+    Oa, _, _ = attn(Qr, K, V1, 0.5)
+    Ob, _, _ = attn(Qr, K, V2, 0.5)
+    Oc, _, _ = attn(Qr, K, V1 + V2, 0.5)
+    bad += not np.allclose(Oc, Oa + Ob, rtol=0, atol=1e-12)
+    # The tolerance weight dominates |O| and equals O when V >= 0.
+    O6, W6, S6 = attn(Qr, K, V, 0.5)
+    bad += not bool((W6 + 1e-15 >= np.abs(O6)).all())
+    Op, Wp, _ = attn(Qr, K, np.abs(V), 0.5)
+    bad += not np.allclose(Op, Wp, rtol=1e-14, atol=0)
+    # Two steps through the product oracle and a numpy softmax.
+    S = np.einsum("bmd,bnd->bmn", Qr.astype(np.float64), K.astype(np.float64)) * 0.5
+    P = np.exp(S - S.max(axis=2, keepdims=True))
+    P /= P.sum(axis=2, keepdims=True)
+    bad += not np.allclose(O6, np.einsum("bmn,bne->bme", P, V.astype(np.float64)), rtol=0, atol=1e-12)
+    bad += not np.allclose(S6, (np.abs(Qr).astype(np.float64) @ np.abs(K.astype(np.float64)).transpose(0, 2, 1)).max(axis=2) * 0.5,
+                           rtol=1e-14, atol=0)
+    return bad
+
+
+def test_attention_pins():
+    assert run_attention_pins() == 0
+
+
+def test_attention_strided_layouts_match_dense():
+    """The 'mixed' layout (K read transposed, V and O column-major with a
+    padded pitch, Q batches walked backwards) reads the same logical operands."""
+    rng = np.random.default_rng(5)
+    c = wl.random_attention(rng, 11, 13, 8, 3, "mixed", causal=1, q_len=11)
+    Qd, Kd, Vd = (np.array(op.view(c.batch, r, cc)) for op, r, cc in
+                  ((c.Q, c.M, c.D), (c.K, c.N, c.D), (c.V, c.N, c.Dv)))
+    O, W, S = oracle.attention_case(c)
+    O2, W2, S2 = _attn(Qd, Kd, Vd, c.alpha, True, 11)
+    assert np.array_equal(O, O2) and np.array_equal(W, W2) and np.array_equal(S, S2)

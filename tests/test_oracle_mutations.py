@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests.test_oracle import run_activation_pins, run_epilogue_pins, run_int_pins
+from tests.test_oracle import (run_activation_pins, run_attention_pins, run_epilogue_pins,
+                               run_int_pins)
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "sbgemm_ref.c")
 
@@ -50,6 +51,7 @@ def test_unmutated_copy_passes(tmp_path):
     lib = oracle.load(so)
     assert run_int_pins(lib=lib) == 0
     assert run_activation_pins(lib=lib) == 0 and run_epilogue_pins(lib=lib) == 0
+    assert run_attention_pins(lib=lib) == 0
 
 
 # Slips in the fused epilogue's activations and added operand.
@@ -77,3 +79,28 @@ def test_planted_epilogue_mistake_is_caught(tmp_path, name, old, new):
     lib = oracle.load(so)
     assert run_activation_pins(lib=lib) + run_epilogue_pins(lib=lib) > 0, \
         f"planted mistake {name} went unnoticed"
+
+
+# Slips in the attention oracle.
+ATTENTION_MUTATIONS = [
+    ("causal_off_by_one", "const int64_t kept = causal ? (m % q_len) + N - q_len + 1 : N;",
+     "const int64_t kept = causal ? (m % q_len) + N - q_len : N;"),
+    ("key_index_uses_row", "(double)K[b * bsK + n * rsK + d * csK];", "(double)K[b * bsK + m * rsK + d * csK];"),
+    ("exponent_sign", "s[n] = exp(s[n] - mx);", "s[n] = exp(mx - s[n]);"),
+    ("not_normalised", "O[(b * M + m) * Dv + e] = o / l;", "O[(b * M + m) * Dv + e] = o;"),
+    ("alpha_dropped", "s[n] = (double)alpha * acc;", "s[n] = acc;"),
+    ("weight_without_abs", "w += s[n] * fabs(v);", "w += s[n] * v;"),
+    ("value_index_transposed", "(double)V[b * bsV + n * rsV + e * csV];", "(double)V[b * bsV + e * rsV + n * csV];"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", ATTENTION_MUTATIONS, ids=[m[0] for m in ATTENTION_MUTATIONS])
+def test_planted_attention_mistake_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = tmp_path / "mut.c"
+    mutated.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmut.so")
+    oracle.build(force=True, src=str(mutated), out=so)
+    lib = oracle.load(so)
+    assert run_attention_pins(lib=lib) > 0, f"planted mistake {name} went unnoticed"

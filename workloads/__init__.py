@@ -42,7 +42,7 @@ from typing import Dict, Optional, Tuple
 import numpy as np
 
 __all__ = ["Operand", "Case", "WORKLOADS", "BACKWARD", "make", "flops", "gflops_per_s",
-           "alg_bytes", "SEEDS"]
+           "alg_bytes", "SEEDS", "AttnCase", "ATTENTION", "make_attention", "random_attention"]
 
 
 @dataclasses.dataclass
@@ -392,3 +392,84 @@ def random_strided(rng: np.random.Generator, M: int, N: int, K: int, batch: int,
             C.storage[:] = rng.uniform(-1, 1, size=C.storage.size)
     return Case(f"rand_{a_layout}_{b_layout}_{c_layout}", A, B, C, M, N, K, batch,
                 alpha, accumulate, values)
+
+
+# ---- fused attention ---------------------------------------------------------
+# O = softmax(alpha * Q K^T, causal optional) V for a batch of (sequence, head)
+# problems: the scores of c3 and the probabilities of c4 computed in one pass
+# ("rvllm CUDA path", section "What's basic about it": scores, softmax and
+# probs @ V as three steps with the scores in global memory is the thing a
+# fused kernel avoids).
+
+@dataclasses.dataclass
+class AttnCase:
+    name: str
+    Q: Operand          # [batch, M, D]
+    K: Operand          # [batch, N, D]
+    V: Operand          # [batch, N, Dv]
+    O: Operand          # [batch, M, Dv] (output; storage is its initial content)
+    M: int
+    N: int
+    D: int
+    Dv: int
+    batch: int
+    alpha: float
+    causal: int
+    q_len: int          # rows per head for the causal position (M for one head)
+
+    @property
+    def flops(self) -> int:
+        """2*M*N*D for the scores plus 2*M*N*Dv for probs @ V (the products'
+        convention), counting every key even where the causal mask drops it."""
+        return 2 * self.batch * self.M * self.N * (self.D + self.Dv)
+
+
+ATTENTION = {
+    # name: (batch, M, N, D, causal, q_len); alpha = 1/sqrt(D)
+    "f2": (128, 512, 512, 64, 0, 512),          # the c3 / c4 problems: 8 sequences x 16 heads
+    "f2causal": (128, 512, 512, 64, 1, 512),    # the same, causal
+    "f2gqa": (32, 2048, 512, 64, 1, 512),       # 4 Q heads stacked as rows per KV head, causal
+}
+
+
+def make_attention(name: str, **shape) -> AttnCase:
+    """Head-major Q, K, V [batch, T, D] as in c3; values N(0,1) (seed 6)."""
+    batch, M, N, D, causal, q_len = ATTENTION[name]
+    dims = dict(batch=batch, M=M, N=N, D=D, q_len=q_len)
+    dims.update({k: int(v) for k, v in shape.items()})
+    batch, M, N, D, q_len = dims["batch"], dims["M"], dims["N"], dims["D"], dims["q_len"]
+    rng = np.random.Generator(np.random.PCG64([6, list(ATTENTION).index(name), 0]))
+    q = _normal(rng, 1.0, (batch, M, D))
+    k = _normal(rng, 1.0, (batch, N, D))
+    v = _normal(rng, 1.0, (batch, N, D))
+    return AttnCase(name, Operand(_flat(q), 0, D, 1, M * D), Operand(_flat(k), 0, D, 1, N * D),
+                    Operand(_flat(v), 0, D, 1, N * D),
+                    Operand(np.zeros(batch * M * D, dtype=np.float32), 0, D, 1, M * D),
+                    M, N, D, D, batch, 1.0 / float(np.sqrt(D)), causal, q_len)
+
+
+def random_attention(rng: np.random.Generator, M: int, N: int, D: int, batch: int,
+                     layout: str = "row", causal: int = 0, q_len: int = 0,
+                     alpha: float = 0.125, scale: float = 1.0) -> AttnCase:
+    """A small attention case.  layout "row": every operand [batch, rows, D]
+    row-major; "mixed": K stored [batch, D, N] and read transposed, V
+    column-major with a padded pitch, O column-major, batches of Q walked
+    backwards."""
+    q = (rng.standard_normal(batch * M * D) * scale).astype(np.float32)
+    k = (rng.standard_normal(batch * N * D) * scale).astype(np.float32)
+    q_len = q_len or M
+    if layout == "row":
+        Q = Operand(q, 0, D, 1, M * D)
+        K = Operand(k, 0, D, 1, N * D)
+        V = Operand(rng.standard_normal(batch * N * D).astype(np.float32), 0, D, 1, N * D)
+        O = Operand(np.zeros(batch * M * D, dtype=np.float32), 0, D, 1, M * D)
+    elif layout == "mixed":
+        Q = Operand(q, (batch - 1) * M * D, D, 1, -M * D)
+        K = Operand(k, 0, 1, N, N * D)                  # K[b,n,d] at b*N*D + d*N + n
+        pitch = N + 3
+        V = Operand(rng.standard_normal(batch * D * pitch).astype(np.float32), 0, 1, pitch, D * pitch)
+        O = Operand(np.zeros(batch * M * D, dtype=np.float32), 0, 1, M, M * D)
+    else:
+        raise ValueError(layout)
+    return AttnCase(f"attn_{layout}_{M}x{N}x{D}", Q, K, V, O, M, N, D, D, batch, alpha,
+                    int(bool(causal)), q_len)
