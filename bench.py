@@ -538,6 +538,58 @@ def run_ours(args, world, rank, local, dist):
                 v = epilogue["per_variant"][f"{mname} {k}"]
                 v["overhead_vs_plain"] = round(v["ms"] / base - 1.0, 4)
 
+    # Fused attention (row f2): softmax(alpha Q K^T [causal]) V on the c3/c4
+    # problems, against the same result computed in three steps (S by this
+    # library's product, a library softmax, P V by this library's product).
+    attention = None
+    if not args.no_attention and args.workload == "c5" and math == sg.MATH_FP32:
+        attention = {"per_workload": {}}
+        reps = max(3, min(args.steps, 10))
+        fp32_peak = sms * FP32_FLOP_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        for n in wl.ATTENTION:
+            c = wl.make_attention(n)
+            dQ, dK, dV, dO = (torch.from_numpy(op.storage).to(dev) for op in (c.Q, c.K, c.V, c.O))
+            a = (dQ.data_ptr(), c.Q.rs, c.Q.cs, c.Q.bs, dK.data_ptr(), c.K.rs, c.K.cs, c.K.bs,
+                 dV.data_ptr(), c.V.rs, c.V.cs, c.V.bs, dO.data_ptr(), c.O.rs, c.O.cs, c.O.bs,
+                 c.M, c.N, c.D, c.Dv, c.batch, c.alpha, c.causal, c.q_len)
+            ms = timed(lambda: sg.sbgemm_attention(*a, s_handle))
+            row = {"ms": round(ms, 4), "gflops": round(c.flops / ms / 1e6, 1),
+                   "flops": "2*M*N*(D+Dv) per batch entry, every key counted",
+                   "causal": bool(c.causal)}
+            if not c.causal:
+                S = torch.empty(c.batch, c.M, c.N, device=dev)
+
+                def three_steps():
+                    sg.sbgemm_ex(dQ.data_ptr(), c.Q.rs, c.Q.cs, c.Q.bs, dK.data_ptr(), c.K.cs, c.K.rs,
+                                 c.K.bs, S.data_ptr(), c.N, 1, c.M * c.N, c.M, c.N, c.D, c.batch,
+                                 c.alpha, 0, s_handle, **ws_kw)
+                    P = torch.softmax(S, dim=-1)
+                    sg.sbgemm_ex(P.data_ptr(), c.N, 1, c.M * c.N, dV.data_ptr(), c.V.rs, c.V.cs,
+                                 c.V.bs, dO.data_ptr(), c.O.rs, c.O.cs, c.O.bs, c.M, c.Dv, c.N,
+                                 c.batch, 1.0, 0, s_handle, **ws_kw)
+                ms3 = timed(three_steps)
+                row["three_steps_ms"] = round(ms3, 4)
+                row["speedup_vs_three_steps"] = round(ms3 / ms, 2)
+                del S
+                attention["roofline"] = {"bound": "alu", "kernel": f"attention ({n})",
+                                         "achieved": round(c.flops / ms / 1e9, 2),
+                                         "peak": round(fp32_peak, 2), "unit": "TFLOP/s",
+                                         "frac": round(c.flops / ms / 1e9 / fp32_peak, 4)}
+            attention["per_workload"][n] = row
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -572,6 +624,7 @@ def run_ours(args, world, rank, local, dist):
         "tf32": tf32,
         "backward": backward,
         "epilogue": epilogue,
+        "attention": attention,
         "gpu_launches": len(calls) * args.steps,
         "clocks": clocks,
         "per_product": {n: {k: v for k, v in d.items() if k != "total_ms"} for n, d in per.items()},
@@ -633,6 +686,8 @@ def main(argv=None):
                     help="skip the backward-product measurement")
     ap.add_argument("--no-epilogue", action="store_true",
                     help="skip the fused-epilogue measurement")
+    ap.add_argument("--no-attention", action="store_true",
+                    help="skip the fused-attention measurement")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
     world, rank, local = dist_env()

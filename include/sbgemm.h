@@ -231,6 +231,34 @@ SBGEMM_API int sbgemm_fused(const float* A, int64_t rsA, int64_t csA, int64_t bs
                  float alpha, int accumulate, const sbgemm_epilogue* epi,
                  void* stream, const sbgemm_options* opt);
 
+/* Fused attention over a batch of (sequence, head) problems, every operand
+ * laid out by strides in fp32 elements like the product's:
+ *     O[b,m,e] = sum_n softmax_n(alpha * sum_d Q[b,m,d] K[b,n,d]) V[b,n,e]
+ * with Q[b,m,d] = Q[b*bsQ + m*rsQ + d*csQ], K[b,n,d], V[b,n,e] and O[b,m,e]
+ * alike.  The pages compute attention as three steps (scores, softmax,
+ * probs @ V) with the scores in global memory between them and name a fused
+ * kernel as the fix ("rvllm CUDA path", section "What's basic about it");
+ * here the scores and probabilities stay on chip.  Grouped-query heads are
+ * rows of one batch entry stacked against one K and V ("rvllm CUDA path",
+ * section "Matmuls go to cuBLAS").
+ *   causal: 0, or 1 to mask keys n > position(m) = (m mod q_len) + N - q_len
+ *           (q_len: query rows per head, 0 < q_len <= N; ignored when 0).
+ *   D, Dv:  head dimensions; this build supports D = Dv = 64.
+ * fp32 arithmetic: scores by FFMA, the softmax with exp2 of alpha*log2(e)
+ * scaled scores, P V by FFMA.  Asynchronous on `stream`; allocates nothing.
+ * Errors: SBGEMM_ERR_INVALID_VALUE (negative size, N == 0 with rows to
+ * compute, a bad causal flag or q_len, misaligned pointer, span overflow),
+ * SBGEMM_ERR_NULL_POINTER, SBGEMM_ERR_OUTPUT_OVERLAP (O not injective or
+ * meeting Q, K or V), SBGEMM_ERR_UNSUPPORTED (another head dimension, M over
+ * 65535 x 128 rows), SBGEMM_ERR_NOT_DEVICE_MEMORY, SBGEMM_ERR_CUDA.  M, batch
+ * or Dv zero: nothing to do. */
+SBGEMM_API int sbgemm_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
+                     const float* K, int64_t rsK, int64_t csK, int64_t bsK,
+                     const float* V, int64_t rsV, int64_t csV, int64_t bsV,
+                     float* O, int64_t rsO, int64_t csO, int64_t bsO,
+                     int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
+                     float alpha, int causal, int64_t q_len, void* stream);
+
 /* Validate and plan without launching or touching device memory: reports the
  * layout classes and the kernel path, tile and CTA count that sbgemm_ex would
  * use.  Pointers are only checked for NULL and alignment (no device query). */

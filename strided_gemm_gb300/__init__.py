@@ -25,6 +25,7 @@ __all__ = [
     "MATH_FP32", "MATH_TF32", "PATH_NONE", "PATH_AUTO", "PATH_GATHER_FFMA",
     "PATH_TMA_FFMA", "PATH_TMA_TF32", "LAYOUT_K_MAJOR", "LAYOUT_MN_MAJOR",
     "LAYOUT_GENERAL", "EXPORTED_SYMBOLS", "LIB_PATH", "sbgemm_fused", "linear_backward",
+    "sbgemm_attention", "attention",
     "ACT_NONE", "ACT_RELU", "ACT_SIGMOID", "ACT_SILU", "ACT_GELU_TANH", "ACT_GELU_ERF",
     "ACTIVATIONS", "KSPLIT_ANY", "KSPLIT_EXACT", "KSPLIT_NONE", "STREAM_K_NONE",
     "STREAM_K_CHAINED", "STREAM_K_PIECES",
@@ -49,7 +50,7 @@ PATH_NAMES = {PATH_NONE: "none", PATH_GATHER_FFMA: "gather_ffma",
               PATH_TMA_FFMA: "tma_ffma", PATH_TMA_TF32: "tma_tf32"}
 
 # Every function include/sbgemm.h declares.
-EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_fused", "sbgemm_plan",
+EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_fused", "sbgemm_attention", "sbgemm_plan",
                     "sbgemm_workspace_bytes", "sbgemm_noalloc", "sbgemm_selftest",
                     "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version")
 ACT_NONE, ACT_RELU, ACT_SIGMOID, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4, 5
@@ -115,6 +116,10 @@ def load(path: str = LIB_PATH):
         lib.sbgemm_fused.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int,
                                              ctypes.POINTER(_Epilogue), _vp,
                                              ctypes.POINTER(_Options)]
+        lib.sbgemm_attention.restype = ctypes.c_int
+        op4 = [_vp, _i64, _i64, _i64]
+        lib.sbgemm_attention.argtypes = (op4 * 4 + [_i64] * 5 +
+                                         [ctypes.c_float, ctypes.c_int, _i64, _vp])
         lib.sbgemm_ex.restype = ctypes.c_int
         lib.sbgemm_ex.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp,
                                           ctypes.POINTER(_Options)]
@@ -212,6 +217,44 @@ def sbgemm_fused(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                              ctypes.byref(e), stream or None, ctypes.byref(o))
     if st:
         raise SbgemmError(st, "sbgemm_fused")
+
+
+def sbgemm_attention(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
+                     O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal=0, q_len=0,
+                     stream=0) -> None:
+    """O = softmax(alpha * Q K^T [causal]) V over strided operands."""
+    st = load().sbgemm_attention(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
+                                 O, rsO, csO, bsO, M, N, D, Dv, batch, float(alpha),
+                                 int(causal), int(q_len), stream or None)
+    if st:
+        raise SbgemmError(st, "sbgemm_attention")
+
+
+def attention(Q, K, V, O, alpha=None, causal=False, q_len=0, stream=None):
+    """Torch helper: Q [batch, M, D], K [batch, N, D], V [batch, N, Dv] and O
+    [batch, M, Dv] float32 CUDA tensors with any strides (2-D means batch 1;
+    K and V may have batch 1 to be shared).  alpha defaults to 1/sqrt(D).
+    Returns O."""
+    import torch
+    Q3, K3, V3, O3 = _as3(Q, "Q"), _as3(K, "K"), _as3(V, "V"), _as3(O, "O")
+    for t, n in ((Q3, "Q"), (K3, "K"), (V3, "V"), (O3, "O")):
+        if t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{n} must be a float32 CUDA tensor")
+    batch, M, D = Q3.shape
+    N, Dv = K3.shape[1], V3.shape[2]
+    if K3.shape[2] != D or V3.shape[1] != N or tuple(O3.shape) != (batch, M, Dv):
+        raise ValueError(f"shape mismatch: Q{tuple(Q3.shape)} K{tuple(K3.shape)} "
+                         f"V{tuple(V3.shape)} O{tuple(O3.shape)}")
+    bs = lambda t: t.stride(0) if t.shape[0] == batch else 0
+    if stream is None:
+        stream = torch.cuda.current_stream(O3.device).cuda_stream
+    sbgemm_attention(Q3.data_ptr(), Q3.stride(1), Q3.stride(2), Q3.stride(0),
+                     K3.data_ptr(), K3.stride(1), K3.stride(2), bs(K3),
+                     V3.data_ptr(), V3.stride(1), V3.stride(2), bs(V3),
+                     O3.data_ptr(), O3.stride(1), O3.stride(2), O3.stride(0),
+                     M, N, D, Dv, batch, (1.0 / D ** 0.5) if alpha is None else alpha,
+                     int(bool(causal)), int(q_len) if causal else 0, stream)
+    return O
 
 
 def sbgemm_plan(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,

@@ -63,6 +63,22 @@ struct Plan {
     void* workspace = nullptr;      // caller's scratch when stream_k
 };
 
+// ---- fused attention (attention.cu) -----------------------------------------
+// O[b,m,:] = softmax_n(alpha * Q[b,m,:] . K[b,n,:], causal optional) V[b,n,:]
+struct AttnProblem {
+    const float* Q; int64_t rsQ, csQ, bsQ;
+    const float* K; int64_t rsK, csK, bsK;
+    const float* V; int64_t rsV, csV, bsV;
+    float* O;       int64_t rsO, csO, bsO;
+    int64_t M, N, D, Dv, batch;
+    float alpha;
+    int causal;
+    int64_t q_len;           // rows per head for the causal position
+};
+bool attention_supported(int64_t D, int64_t Dv);
+int64_t attention_max_rows();   // M limit of one launch
+cudaError_t launch_attention(const AttnProblem& a, cudaStream_t stream);
+
 // ---- strided-gather FFMA path (ffma_gather.cu) --------------------------------
 // Tile configurations of the gather kernel.
 struct GatherConfig { int bm, bn, bk, threads, ctas_per_sm; };

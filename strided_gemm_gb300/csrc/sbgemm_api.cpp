@@ -460,6 +460,50 @@ int sbgemm_fused(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     return run(p, o, stream);
 }
 
+int sbgemm_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
+                     const float* K, int64_t rsK, int64_t csK, int64_t bsK,
+                     const float* V, int64_t rsV, int64_t csV, int64_t bsV,
+                     float* O, int64_t rsO, int64_t csO, int64_t bsO,
+                     int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
+                     float alpha, int causal, int64_t q_len, void* stream) {
+    if (M < 0 || N < 0 || D < 0 || Dv < 0 || batch < 0) return SBGEMM_ERR_INVALID_VALUE;
+    if (causal != 0 && causal != 1) return SBGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || batch == 0 || Dv == 0) return SBGEMM_OK;
+    if (N == 0) return SBGEMM_ERR_INVALID_VALUE;          // a softmax over no keys
+    if (causal && (q_len <= 0 || q_len > N)) return SBGEMM_ERR_INVALID_VALUE;
+    if (!attention_supported(D, Dv)) return SBGEMM_ERR_UNSUPPORTED;
+    if (M > attention_max_rows() || batch >= ((int64_t)1 << 31)) return SBGEMM_ERR_UNSUPPORTED;
+    if (!Q || !K || !V || !O) return SBGEMM_ERR_NULL_POINTER;
+    if (!aligned(Q, 4) || !aligned(K, 4) || !aligned(V, 4) || !aligned(O, 4))
+        return SBGEMM_ERR_INVALID_VALUE;
+    Span sq{}, sk{}, sv{}, so{};
+    if (!operand_span(batch, M, D, bsQ, rsQ, csQ, &sq) || !operand_span(batch, N, D, bsK, rsK, csK, &sk) ||
+        !operand_span(batch, N, Dv, bsV, rsV, csV, &sv) || !operand_span(batch, M, Dv, bsO, rsO, csO, &so))
+        return SBGEMM_ERR_INVALID_VALUE;
+    if (!output_injective(batch, M, Dv, bsO, rsO, csO)) return SBGEMM_ERR_OUTPUT_OVERLAP;
+    auto bytes_meet = [](const void* a, const Span& sa, const void* b, const Span& sb) {
+        const __int128 alo = (__int128)reinterpret_cast<uintptr_t>(a) + (__int128)sa.lo * 4;
+        const __int128 ahi = (__int128)reinterpret_cast<uintptr_t>(a) + (__int128)sa.hi * 4 + 4;
+        const __int128 blo = (__int128)reinterpret_cast<uintptr_t>(b) + (__int128)sb.lo * 4;
+        const __int128 bhi = (__int128)reinterpret_cast<uintptr_t>(b) + (__int128)sb.hi * 4 + 4;
+        return alo < bhi && blo < ahi;
+    };
+    if (bytes_meet(O, so, Q, sq) || bytes_meet(O, so, K, sk) || bytes_meet(O, so, V, sv))
+        return SBGEMM_ERR_OUTPUT_OVERLAP;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
+    if (!span_in_allocation(Q, sq) || !span_in_allocation(K, sk) || !span_in_allocation(V, sv) ||
+        !span_in_allocation(O, so))
+        return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    AttnProblem a{Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV, O, rsO, csO, bsO,
+                  M, N, D, Dv, batch, alpha, causal, causal ? q_len : M};
+    if (launch_attention(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SBGEMM_ERR_CUDA;
+    }
+    return SBGEMM_OK;
+}
+
 int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
            const float* B, int64_t rsB, int64_t csB, int64_t bsB,
            float* C, int64_t rsC, int64_t csC, int64_t bsC,
