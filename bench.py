@@ -45,12 +45,14 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
             "sm_max_mhz": 2070.0}
 
 SWEEPS = {"c5": ["c5a", "c5b", "c5c", "c5d"], "c3all": ["c3", "c3gqa"],
-          "f1": list(wl.BACKWARD)}
+          "f1": list(wl.BACKWARD), "f4": ["f4spec", "f4dist"]}
 DESCR = {
     "c5": "large projection sweep: 8192x960->2560 (W^T), 8192x2560->960 (W^T), "
           "4096^3 row-major +C, 4096^3 A^T B^T +C",
     "f1": "backward products of the two projection layers: dX = G W (8192x960x2560, "
           "8192x2560x960), dW += G^T X (2560x960x8192, 960x2560x8192)",
+    "f4": "spectrogram basis product (64 clips, overlapping 512-sample frames every 128, "
+          "x 512x514 windowed DFT basis) and codebook distances (8192 x 4096 x 256)",
 }
 
 
@@ -590,6 +592,32 @@ def run_ours(args, world, rank, local, dist):
                                          "frac": round(c.flops / ms / 1e9 / fp32_peak, 4)}
             attention["per_workload"][n] = row
 
+    # The other products the pages route through the kernel (row f4): the
+    # spectrogram (frames read as overlapping strided rows) and the tokenizer's
+    # codebook distances.
+    spectral = None
+    if not args.no_f4 and args.workload == "c5" and math == sg.MATH_FP32:
+        spectral = {"per_product": {}}
+        reps = max(3, min(args.steps, 10))
+        for n in ("f4spec", "f4dist"):
+            c = wl.make(n, "real")
+            bufs = tuple(torch.from_numpy(x).to(dev) for x in (c.A.storage, c.B.storage, c.C.storage))
+            a = case_args(c, *bufs)
+            pl = sg.sbgemm_plan(*a[:16], c.accumulate, **ws_kw)
+            for _ in range(3):
+                sg.sbgemm_ex(*a, s_handle, **ws_kw)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                sg.sbgemm_ex(*a, s_handle, **ws_kw)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            spectral["per_product"][n] = {"ms": round(ms, 4), "gflops": round(c.flops / ms / 1e6, 1),
+                                          "path": pl["path_name"], "note": c.note}
+            del bufs
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -625,6 +653,7 @@ def run_ours(args, world, rank, local, dist):
         "backward": backward,
         "epilogue": epilogue,
         "attention": attention,
+        "spectrogram_and_distances": spectral,
         "gpu_launches": len(calls) * args.steps,
         "clocks": clocks,
         "per_product": {n: {k: v for k, v in d.items() if k != "total_ms"} for n, d in per.items()},
@@ -688,6 +717,8 @@ def main(argv=None):
                     help="skip the fused-epilogue measurement")
     ap.add_argument("--no-attention", action="store_true",
                     help="skip the fused-attention measurement")
+    ap.add_argument("--no-f4", action="store_true",
+                    help="skip the spectrogram and distance products")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
     world, rank, local = dist_env()

@@ -500,3 +500,33 @@ def test_attention_strided_layouts_match_dense():
     O, W, S = oracle.attention_case(c)
     O2, W2, S2 = _attn(Qd, Kd, Vd, c.alpha, True, 11)
     assert np.array_equal(O, O2) and np.array_equal(W, W2) and np.array_equal(S, S2)
+
+
+def test_spectrogram_workload_is_the_windowed_dft():
+    """f4spec's product, frames read as overlapping strided rows times the
+    basis, equals numpy's real FFT of the Hann-windowed frames (a library
+    routine of its own): real parts in the first 257 columns, imaginary
+    parts in the next 257."""
+    case = wl.make("f4spec", "real", batch=2, M=9)
+    ref, _ = oracle.case_product(case)
+    K, hop = case.K, case.A.rs
+    L = case.A.bs
+    sig = case.A.storage.reshape(case.batch, L).astype(np.float64)
+    w = np.sin(np.pi * np.arange(K) / K) ** 2
+    for b in range(case.batch):
+        frames = np.stack([sig[b, t * hop: t * hop + K] for t in range(case.M)]) * w
+        X = np.fft.rfft(frames, axis=1)
+        got = ref[b]
+        assert np.allclose(got[:, :257], X.real, rtol=0, atol=1e-4 * np.abs(X).max())
+        assert np.allclose(got[:, 257:], X.imag, rtol=0, atol=1e-4 * np.abs(X).max())
+
+
+def test_distance_workload_is_the_squared_distance():
+    """f4dist's product (-2 X C^T onto |x|^2 + |c|^2) equals the brute-force
+    squared Euclidean distance of every embedding to every codebook entry."""
+    case = wl.make("f4dist", "int", M=23, N=17, K=31)
+    ref, _ = oracle.case_product(case)
+    X = case.A.storage.reshape(23, 31).astype(np.int64)
+    Cb = case.B.storage.reshape(17, 31).astype(np.int64)
+    want = ((X[:, None, :] - Cb[None, :, :]) ** 2).sum(axis=2)
+    assert np.array_equal(ref[0], want.astype(np.float64))

@@ -42,12 +42,21 @@ def _supported(case, math, path):
         return False
 
 
+# Workloads a tensor map cannot describe: the spectrogram's frames are
+# overlapping rows of the signal (row stride 128 < 512 samples per frame) and
+# its basis pitch (514 floats) is not a multiple of 16 bytes.
+NOT_TMA = {"f4spec"}
+
+
 @pytest.mark.parametrize("name", wl.WORKLOADS)
 @pytest.mark.parametrize("values", ["real", "int"])
 @pytest.mark.parametrize("path", FFMA_PATHS)
 def test_workloads_small(torch, name, values, path):
     case = wl.make(name, values, **wl.small_shape(name))
-    assert _supported(case, sg.MATH_FP32, path), "every workload is TMA-eligible"
+    if name in NOT_TMA and path == sg.PATH_TMA_FFMA:
+        assert not _supported(case, sg.MATH_FP32, path)
+        pytest.skip("not TMA-eligible by construction")
+    assert _supported(case, sg.MATH_FP32, path), "every other workload is TMA-eligible"
     got = gu.run_case(case, torch, force_path=path)
     gu.check_full(case, got, exact=(values == "int"))
 

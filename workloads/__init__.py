@@ -30,6 +30,16 @@ backward block through kernel fusion"), transposes read through strides:
   f1dxb   dX of c5b's layer: G [8192,960] . W [960,2560]
   f1dwb   dW of c5b's layer: G^T [960,8192] . X [8192,2560], accumulate into dW
 
+and two more products the StaleyNET page routes through the kernel ("GPU
+Implementation", section "The matrix product": the spectrogram and the
+tokenizer's distances), in the plain reading given there no formula:
+
+  f4spec  power-spectrum basis product of 64 clips of 16384 samples: frames of
+          512 samples every 128 (overlapping rows of the signal, rsA = 128, no
+          framing copy) times the windowed DFT basis [w cos | -w sin] (512 x 514)
+  f4dist  squared distances of 8192 embeddings (256-d) to a 4096-entry codebook:
+          -2 X C^T accumulated onto |x|^2 + |c|^2
+
 Every workload also has an integer pass (values uniform in {-8..8}) in which
 every partial sum is an exact fp32 integer.
 """
@@ -117,11 +127,11 @@ def alg_bytes(case: "Case") -> int:
 # c2 = 1, c3 = 2, c4 = 3, c5 = 4.
 SEEDS = {"c1": 0, "c2a": 1, "c2b": 1, "c3": 2, "c3gqa": 2, "c4": 3,
          "c5a": 4, "c5b": 4, "c5c": 4, "c5d": 4,
-         "f1dxa": 5, "f1dwa": 5, "f1dxb": 5, "f1dwb": 5}
+         "f1dxa": 5, "f1dwa": 5, "f1dxb": 5, "f1dwb": 5, "f4spec": 7, "f4dist": 7}
 # Sub-stream per workload sharing a seed, so c2a and c2b draw different values.
 _STREAM = {"c1": 0, "c2a": 0, "c2b": 1, "c3": 0, "c3gqa": 1, "c4": 0,
            "c5a": 0, "c5b": 1, "c5c": 2, "c5d": 2,
-           "f1dxa": 0, "f1dwa": 1, "f1dxb": 2, "f1dwb": 3}
+           "f1dxa": 0, "f1dwa": 1, "f1dxb": 2, "f1dwb": 3, "f4spec": 0, "f4dist": 1}
 
 # Full-size shapes.  Keys that a caller may override to shrink a case for the
 # oracle: batch, M, N, K (and heads/seqs for the attention cases).
@@ -140,6 +150,9 @@ FULL: Dict[str, Dict[str, int]] = {
     "f1dwa": dict(batch=1, M=2560, N=960, K=8192),
     "f1dxb": dict(batch=1, M=8192, N=2560, K=960),
     "f1dwb": dict(batch=1, M=960, N=2560, K=8192),
+    # frames (16384 - 512) / 128 + 1 = 125 per clip; 257 bins x (cos, sin)
+    "f4spec": dict(batch=64, M=125, N=514, K=512),
+    "f4dist": dict(batch=1, M=8192, N=4096, K=256),
 }
 WORKLOADS = tuple(FULL)
 BACKWARD = ("f1dxa", "f1dwa", "f1dxb", "f1dwb")
@@ -302,7 +315,45 @@ def make(name: str, values: str = "real", **shape) -> Case:
                     M, N, K, batch, 1.0, 1, values,
                     "weight gradient, G read transposed by swapped strides, accumulate")
 
+    if name == "f4spec":
+        # Signal of each clip: (M - 1) * hop + K samples; frame t = samples
+        # [t*hop, t*hop + K): A[b, t, k] = signal[b*L + t*hop + k].
+        hop = 128
+        L = (M - 1) * hop + K
+        sig = draw("n", (batch, L), 1.0)
+        # The integer pass keeps the layout with an integer basis.
+        basis = _ints(rng, (K, N)) if is_int else spectrogram_basis(K, N // 2)
+        return Case(name, Operand(_flat(sig), 0, hop, 1, L),
+                    Operand(_flat(basis), 0, N, 1, 0),
+                    Operand(empty_c(), 0, N, 1, M * N),
+                    M, N, K, batch, 1.0, 0, values,
+                    "overlapping frames read by strides times a windowed DFT basis")
+
+    if name == "f4dist":
+        x = draw("n", (M, K), 1.0)
+        c = draw("n", (N, K), 1.0)
+        # C0 = |x_m|^2 + |c_n|^2, computed in float64 and rounded once.
+        x64, c64 = x.astype(np.float64), c.astype(np.float64)
+        c0 = ((x64 * x64).sum(1)[:, None] + (c64 * c64).sum(1)[None, :]).astype(np.float32)
+        return Case(name, Operand(_flat(x), 0, K, 1, M * K),
+                    Operand(_flat(c), 0, 1, K, N * K),
+                    Operand(_flat(c0), 0, N, 1, M * N),
+                    M, N, K, batch, -2.0, 1, values,
+                    "squared distances: -2 X C^T accumulated onto |x|^2 + |c|^2")
+
     raise AssertionError(name)
+
+
+def spectrogram_basis(K: int, F: int) -> np.ndarray:
+    """[K, 2F] basis of the windowed DFT: column f is w[k] cos(2 pi f k / K),
+    column F + f is -w[k] sin(2 pi f k / K), with the periodic Hann window
+    w[k] = sin^2(pi k / K).  Frames times this basis give the real and
+    imaginary parts of the first F bins of the windowed frames' DFT."""
+    k = np.arange(K, dtype=np.float64)[:, None]
+    f = np.arange(F, dtype=np.float64)[None, :]
+    w = np.sin(np.pi * k / K) ** 2
+    ang = 2.0 * np.pi * f * k / K
+    return np.concatenate([w * np.cos(ang), -w * np.sin(ang)], axis=1).astype(np.float32)
 
 
 def small_shape(name: str) -> Dict[str, int]:
@@ -323,6 +374,8 @@ def small_shape(name: str) -> Dict[str, int]:
         "f1dwa": dict(batch=1, M=260, N=300, K=2052),
         "f1dxb": dict(batch=1, M=300, N=1028, K=960),
         "f1dwb": dict(batch=1, M=300, N=260, K=2052),
+        "f4spec": dict(batch=3, M=41, N=514, K=512),
+        "f4dist": dict(batch=1, M=300, N=260, K=256),
     }[name]
 
 
