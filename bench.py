@@ -592,6 +592,55 @@ def run_ours(args, world, rank, local, dist):
                                          "frac": round(c.flops / ms / 1e9 / fp32_peak, 4)}
             attention["per_workload"][n] = row
 
+    # Every other config of the workload list, each against its own roofline,
+    # min(peak compute, algorithmic bytes x HBM bandwidth): median of 21 timed
+    # launches after 5 warm-ups, and for the latency-bound c1 / c2 the mean of
+    # 1000 back-to-back launches as well.
+    configs = None
+    if not args.no_configs and args.workload == "c5" and math == sg.MATH_FP32:
+        configs = {}
+        hbm = float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+        fp32_peak = sms * FP32_FLOP_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
+        tf32_peak = float(peaks.get("bf16_tflops", FALLBACK["bf16_tflops"])) * TF32_OVER_BF16_NOMINAL
+        for n in ("c1", "c2a", "c2b", "c3", "c3gqa", "c4"):
+            c = wl.make(n, "real")
+            bufs = tuple(torch.from_numpy(x).to(dev) for x in (c.A.storage, c.B.storage, c.C.storage))
+            a = case_args(c, *bufs)
+            row = {"gflop": round(c.flops / 1e9, 4), "alg_mb": round(wl.alg_bytes(c) / 1e6, 2)}
+            for mname, m in (("fp32", sg.MATH_FP32), ("tf32", sg.MATH_TF32)):
+                pl = sg.sbgemm_plan(*a[:16], c.accumulate, math=m, **ws_kw)
+                if m == sg.MATH_TF32 and pl["path_name"] != "tma_tf32":
+                    continue
+                for _ in range(5):
+                    sg.sbgemm_ex(*a, s_handle, math=m, **ws_kw)
+                times = []
+                for _ in range(21):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    sg.sbgemm_ex(*a, s_handle, math=m, **ws_kw)
+                    e1.record(stream)
+                    e1.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                ms = statistics.median(times)
+                peak = fp32_peak if m == sg.MATH_FP32 else tf32_peak
+                roof_c = min(peak, c.flops / wl.alg_bytes(c) * hbm / 1e3)   # TFLOP/s
+                ent = {"ms_median": round(ms, 4), "gflops": round(c.flops / ms / 1e6, 1),
+                       "path": pl["path_name"],
+                       "roof_tflops": round(roof_c, 2),
+                       "bound": "compute" if roof_c == peak else "hbm",
+                       "frac_of_roof": round(c.flops / ms / 1e9 / roof_c, 4)}
+                if n in ("c1", "c2a", "c2b"):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(1000):
+                        sg.sbgemm_ex(*a, s_handle, math=m, **ws_kw)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    ent["us_back_to_back"] = round(e0.elapsed_time(e1), 2)   # 1000 launches -> us each
+                row[mname] = ent
+            configs[n] = row
+            del bufs
+
     # The other products the pages route through the kernel (row f4): the
     # spectrogram (frames read as overlapping strided rows) and the tokenizer's
     # codebook distances.
@@ -654,6 +703,7 @@ def run_ours(args, world, rank, local, dist):
         "epilogue": epilogue,
         "attention": attention,
         "spectrogram_and_distances": spectral,
+        "configs": configs,
         "gpu_launches": len(calls) * args.steps,
         "clocks": clocks,
         "per_product": {n: {k: v for k, v in d.items() if k != "total_ms"} for n, d in per.items()},
@@ -719,6 +769,8 @@ def main(argv=None):
                     help="skip the fused-attention measurement")
     ap.add_argument("--no-f4", action="store_true",
                     help="skip the spectrogram and distance products")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config measurements of c1-c4")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
     world, rank, local = dist_env()

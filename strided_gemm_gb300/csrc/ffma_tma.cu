@@ -813,15 +813,26 @@ TmaFfmaConfig tma_ffma_config(int variant) { return kConfigs[variant]; }
 // Picks the tile shape that wastes the least work, counting both the ragged
 // edge of the last tiles and the idle SMs of the last wave.
 int tma_ffma_pick_variant(const Problem& p, int sm_count) {
+    // K-major operands are transposed in shared memory slice by slice, which
+    // costs in proportion to the tile's rows of that operand: on equal wave
+    // cost, prefer the shape whose transposed side is the shorter one.
+    const bool a_k = p.K == 1 || p.csA == 1;
+    const bool b_k = p.K == 1 || p.rsB == 1;
     int best = 0;
     double best_cost = 0.0;
+    int best_rows = 0;
     for (int v = 0; v < tma_ffma_config_count(); ++v) {
         const TmaFfmaConfig c = kConfigs[v];
         const int64_t tm = (p.M + c.bm - 1) / c.bm, tn = (p.N + c.bn - 1) / c.bn;
         const int64_t tiles = tm * tn * p.batch;
         const int64_t waves = (tiles + sm_count - 1) / sm_count;
         const double cost = (double)waves * c.bm * c.bn;   // time ~ waves x tile work
-        if (v == 0 || cost < best_cost) { best = v; best_cost = cost; }
+        const int rows = (a_k ? c.bm : 0) + (b_k ? c.bn : 0);
+        if (v == 0 || cost < best_cost || (cost == best_cost && rows < best_rows)) {
+            best = v;
+            best_cost = cost;
+            best_rows = rows;
+        }
     }
     return best;
 }
