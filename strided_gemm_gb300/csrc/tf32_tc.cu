@@ -16,12 +16,14 @@
 //    memory, and writes alpha*acc (+ C_old), with the fused addend and
 //    activation if any, in 128-byte rows with masks on ragged M / N; then it
 //    releases the accumulator, so the next tile's MMAs overlap these stores.
-// With a workspace the last waves are split along K across the grid (the
-// stream-K work list shared with the FFMA kernel): a head item's accumulator
-// goes to the workspace instead of C, and the epilogue warps seed the TMEM
-// accumulator of a tail item with its predecessor's partial sums (tcgen05.st)
-// before the MMAs continue with accumulation on, so the fp32 accumulation
-// sequence is the data-parallel one.
+// With a workspace, tiles are split along K across the grid as independent
+// pieces (the work list of schedule.cuh shared with the FFMA kernel): the last
+// waves when there are at least as many tiles as SMs, all tiles otherwise.
+// Every piece accumulates from zero, so no MMA ever waits for another CTA; a
+// head or middle piece leaves its accumulator in the workspace, and the tail
+// piece's epilogue adds the earlier pieces' partial sums, latest CTA first,
+// after loading its own.  Results are deterministic but rounded differently
+// from the unsplit tile.
 // Every mbarrier wait is bounded; a role that gives up records a status code
 // and leaves its loop, the producer then waits (bounded) for the copies it
 // issued, the MMA issuer for its MMAs, and the allocating warp frees TMEM
@@ -86,7 +88,6 @@ struct Smem {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t mma_done;
-    uint64_t seeded[2];       // the epilogue warps wrote a tail's partial into TMEM buffer b
     uint64_t stored;          // every epilogue thread wrote its head partial
     uint64_t c_old[kEpiWarps];   // a warp's C_old piece landed in its staging tile
     Schedule sched;
@@ -159,11 +160,6 @@ __device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params
             record_status(&g_wait_status, kWaitAccFree);
             break;
         }
-        // A tail continues from the partial sums the epilogue seeded.
-        if (itm.mode == kTail && !mbar_wait(&sh.seeded[buf], 0)) {
-            record_status(&g_wait_status, kWaitPartial);
-            break;
-        }
         tc_fence_after();
         const uint32_t d = tmem + buf * kAccCols;
         for (int kt = itm.kb; kt < itm.ke; ++kt) {
@@ -179,7 +175,7 @@ __device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params
             for (int kk = 0; kk < BK / kMmaK; ++kk) {
                 const uint64_t ad = umma_desc_kmajor_sw128(a0 + kk * kMmaK * 4);
                 const uint64_t bd = umma_desc_kmajor_sw128(b0 + kk * kMmaK * 4);
-                const bool acc = itm.mode == kTail || kt > itm.kb || kk > 0;
+                const bool acc = kt > itm.kb || kk > 0;
                 mma_tf32(d, ad, bd, kIdesc, acc ? 1u : 0u);
             }
             mma_commit(&sh.empty[stage]);
@@ -199,55 +195,41 @@ __device__ __forceinline__ float4* partial_piece(float4* slot, int c, int row) {
     return slot + (c * 8) * kBM128 + row;
 }
 
-// Whether the predecessor CTA has published its head partial (warp-uniform,
-// no waiting).  Every lane then takes its own acquire before reading it.
-__device__ __forceinline__ bool pred_partial_ready(const Params& p, int lane) {
-    const unsigned int* flag = p.ws_flag + (blockIdx.x - 1);
-    int up = 0;
-    if (lane == 0) up = ld_acquire_gpu(flag) != 0u;
-    if (!__shfl_sync(0xffffffffu, up, 0)) return false;
-    (void)ld_acquire_gpu(flag);
-    return true;
-}
-
-// Copies the predecessor's partial sums of this thread's row into TMEM buffer
-// `buf` (four 32-column pieces in flight at a time), then tells the MMA lane.
-__device__ __forceinline__ void seed_load(Smem& sh, uint32_t tmem, const Params& p, int quarter,
-                                          int lane, uint32_t buf) {
-    const float4* src = p.ws_partial + (int64_t)(blockIdx.x - 1) * kSlotFloat4;
-    const int row = quarter * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * kAccCols;
-    constexpr int kBatch = 4;
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN / 32; c0 += kBatch) {
-        float v[kBatch][32];
-#pragma unroll
-        for (int c = 0; c < kBatch; ++c) {
-            const float4* q = partial_piece(const_cast<float4*>(src), c0 + c, row);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 x = __ldcg(q + j * kBM128);
-                v[c][4 * j] = x.x; v[c][4 * j + 1] = x.y; v[c][4 * j + 2] = x.z; v[c][4 * j + 3] = x.w;
-            }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < kBatch; ++c) tmem_st32(taddr + (c0 + c) * 32, v[c]);
+// Waits (bounded) until CTAs first..blockIdx.x-1 have published their pieces
+// of this tile; one lane spins, then every lane takes its own acquire.  False
+// on timeout.
+__device__ __forceinline__ bool wait_pieces(const Params& p, int64_t first, int lane) {
+    for (int64_t c = first; c < (int64_t)blockIdx.x; ++c) {
+        int up = 1;
+        if (lane == 0) up = wait_flag(p.ws_flag + c) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, up, 0)) return false;
+        (void)ld_acquire_gpu(p.ws_flag + c);
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.seeded[buf]);
+    return true;
 }
 
-// Waits (bounded) for the predecessor's partial, then seeds.  False on timeout.
-__device__ __forceinline__ bool seed_tail(Smem& sh, uint32_t tmem, const Params& p, int quarter,
-                                          int lane, uint32_t buf) {
-    int up = 1;
-    if (lane == 0) up = wait_flag(p.ws_flag + (blockIdx.x - 1)) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, up, 0)) return false;
-    (void)ld_acquire_gpu(p.ws_flag + (blockIdx.x - 1));
-    seed_load(sh, tmem, p, quarter, lane, buf);
-    return true;
+// One 32-column chunk of this thread's row of a piece's partial sums.
+__device__ __forceinline__ void load_piece_chunk(float (&x)[32], const Params& p, int64_t cta, int chunk,
+                                                 int row) {
+    const float4* q = partial_piece(p.ws_partial + cta * kSlotFloat4, chunk, row);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float4 t = __ldcg(q + j * kBM128);
+        x[4 * j] = t.x; x[4 * j + 1] = t.y; x[4 * j + 2] = t.z; x[4 * j + 3] = t.w;
+    }
+}
+
+// Adds the partial sums of pieces from CTAs `from` down to `first` of one
+// 32-column chunk of this thread's row (latest CTA first: a fixed order).
+__device__ __forceinline__ void add_pieces(float (&v)[32], const Params& p, int64_t first, int64_t from,
+                                           int chunk, int row) {
+#pragma unroll 1
+    for (int64_t c = from; c >= first; --c) {
+        float x[32];
+        load_piece_chunk(x, p, c, chunk, row);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += x[e];
+    }
 }
 
 // Writes one finished tile's rows [quarter*32, +32) through the C tensor map:
@@ -259,11 +241,12 @@ template <int ACT>
 __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap, const Params& p,
                                                const TileCoord& tc, uint32_t taddr, int quarter,
                                                int lane, int ew, uint32_t& c_loads,
-                                               uint32_t& stores) {
+                                               uint32_t& stores, int64_t first_piece) {
     const int64_t m_base = tc.m0 + quarter * 32;
     const int64_t m = m_base + lane;
     const float* drow = (p.epi.D && m < p.M) ? p.epi.D + tc.b * p.epi.bsD + m * p.epi.rsD : nullptr;
     const bool rows_in = m_base < p.M;
+    const int row = quarter * 32 + lane;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
         const int64_t n0 = tc.n0 + c * 32;
@@ -287,6 +270,8 @@ __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap
         float v[32];
         tmem_ld32(taddr + c * 32, v);      // whole warp, converged: row m, columns n0..n0+31
         if (!piece_in) continue;
+        // A tail adds the earlier pieces' partial sums before alpha.
+        if (first_piece >= 0) add_pieces(v, p, first_piece, (int64_t)blockIdx.x - 1, c, row);
         if (p.accumulate) {
             if (!mbar_wait(&sh.c_old[ew], c_loads & 1u)) return false;
             ++c_loads;
@@ -351,44 +336,19 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
     uint32_t c_loads = 0;                       // C_old pieces this warp has loaded
     uint32_t stores = 0;                        // bulk stores this warp has issued
     const int64_t n_items = sh.sched.n_items;
-    if (n_items > 0 && sh.sched.item(0, p.nk).mode == kTail &&
-        !seed_tail(sh, tmem, p, quarter, lane, 0)) {
-        record_status(&g_wait_status, kWaitPartial);
-        return;
-    }
     for (int64_t w = 0; w < n_items; ++w) {
         const Item itm = sh.sched.item(w, p.nk);
         const uint32_t buf = (uint32_t)(w & 1);
-        // Seed the next item if it is a tail (its buffer was freed by item w-1),
-        // so its MMAs can start while this item drains.  After a head, the
-        // seeding waits until the head's own partial is published: a CTA
-        // that waited on its predecessor first would chain every CTA's head
-        // behind the one before it.
-        const bool next_tail = w + 1 < n_items && sh.sched.item(w + 1, p.nk).mode == kTail;
         const uint32_t acc_parity = (uint32_t)((w >> 1) & 1);
-        bool next_seeded = false;
-        if (next_tail && itm.mode != kHead) {
-            if (!seed_tail(sh, tmem, p, quarter, lane, buf ^ 1u)) {
+        // A tail finishes its tile: the earlier pieces (CTAs first..this-1)
+        // were computed at the same time and published as heads, normally
+        // long before this point.
+        int64_t first_piece = -1;
+        if (itm.mode == kTail) {
+            first_piece = unit_owner((itm.tile - p.dp_tiles) * p.nk, p.sk_units, gridDim.x);
+            if (!wait_pieces(p, first_piece, lane)) {
                 record_status(&g_wait_status, kWaitPartial);
                 return;
-            }
-            next_seeded = true;
-        } else if (next_tail) {
-            // Seed early if the predecessor's partial is already out, else
-            // after this head is published (whichever comes first).
-            const uint64_t t0 = global_timer_ns();
-            while (true) {
-                int done = mbar_try_wait(&sh.acc_full[buf], acc_parity) ? 1 : 0;
-                if (__shfl_sync(0xffffffffu, done, 0)) break;
-                if (pred_partial_ready(p, lane)) {
-                    seed_load(sh, tmem, p, quarter, lane, buf ^ 1u);
-                    next_seeded = true;
-                    break;
-                }
-                if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-                    record_status(&g_wait_status, kWaitMma);
-                    return;
-                }
             }
         }
         if (!mbar_wait(&sh.acc_full[buf], acc_parity)) {
@@ -424,12 +384,12 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
             const TileCoord tc = tile_coord(p, itm.tile);
             bool ok;
             switch (p.epi.act) {
-                case kActRelu: ok = store_tile_tma<kActRelu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
-                case kActSigmoid: ok = store_tile_tma<kActSigmoid>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
-                case kActSilu: ok = store_tile_tma<kActSilu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
-                case kActGeluTanh: ok = store_tile_tma<kActGeluTanh>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
-                case kActGeluErf: ok = store_tile_tma<kActGeluErf>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
-                default: ok = store_tile_tma<kActNone>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores); break;
+                case kActRelu: ok = store_tile_tma<kActRelu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActSigmoid: ok = store_tile_tma<kActSigmoid>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActSilu: ok = store_tile_tma<kActSilu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActGeluTanh: ok = store_tile_tma<kActGeluTanh>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActGeluErf: ok = store_tile_tma<kActGeluErf>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                default: ok = store_tile_tma<kActNone>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
             }
             if (!ok) {
                 record_status(&g_wait_status, kWaitFull);
@@ -449,6 +409,7 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
                 tmem_ld32(taddr + c * 32, v);      // whole warp, converged, every row
                 const int64_t n0 = tc.n0 + c * 32;
                 if (!row_ok || n0 >= p.N) continue;
+                if (first_piece >= 0) add_pieces(v, p, first_piece, (int64_t)blockIdx.x - 1, c, row);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int64_t n = n0 + e;
@@ -464,10 +425,6 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_empty[buf]);
-        if (next_tail && !next_seeded && !seed_tail(sh, tmem, p, quarter, lane, buf ^ 1u)) {
-            record_status(&g_wait_status, kWaitPartial);
-            return;
-        }
     }
 }
 
@@ -488,8 +445,6 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             mbar_init(&sh.acc_empty[b], kEpiWarps);
         }
         mbar_init(&sh.mma_done, 1);
-        mbar_init(&sh.seeded[0], kEpiWarps);
-        mbar_init(&sh.seeded[1], kEpiWarps);
         mbar_init(&sh.stored, kEpiWarps * 32);
         for (int w = 0; w < kEpiWarps; ++w) mbar_init(&sh.c_old[w], 1);
         sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
@@ -622,27 +577,38 @@ cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cu
     return cudaGetLastError();
 }
 
-// Same rule as the FFMA path (stream_k_dp_tiles), with the tensor cores' own
-// exchange cost.
+// The FFMA path's rules (stream_k_dp_tiles, split_k_ctas), with independent
+// pieces in both cases.  The exchange is off the MMA path (a piece's partial
+// sums are written while the next item's MMAs run; only the tail's epilogue
+// reads them), but the split still costs about 15 us against the slice model,
+// whose data-parallel estimate ignores that a thin last wave runs faster than
+// a full one: charged as 48 slices of 128 x 256 x 32 (0.37 us each), which
+// reproduces every measured decision (long K or few tiles split; c5a, c5b and
+// K <= 2048 stay data-parallel).  The result is not the unsplit rounding, so
+// k_split = EXACT never splits.
 void tf32_tc_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
                       int k_split) {
     const int64_t nk = (pr.K + BK - 1) / BK;
     const int64_t G = sm_count;
     plan.k_slices = (int)nk;
     plan.stream_k = false;
+    plan.split_indep = false;
     plan.dp_tiles = plan.tiles;
     plan.ctas = plan.tiles < G ? plan.tiles : G;
     const size_t need = (size_t)G * (size_t)kSlotFloat4 * sizeof(float4) + (size_t)G * sizeof(unsigned int);
     if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 256) != 0) return;
-    if (k_split == SBGEMM_KSPLIT_NONE) return;
-    // Tensor-core slices are short (about 0.4 us for 128 x 256 x 32), so the
-    // 15-20 us of exchange and reset cost counts as about 48 slices: only
-    // long-K problems gain.
-    const int64_t dp = stream_k_dp_tiles(plan.tiles, nk, G, 48);
-    if (dp < 0) return;
+    if (k_split != SBGEMM_KSPLIT_ANY) return;
+    int64_t dp = stream_k_dp_tiles(plan.tiles, nk, G, 48);
+    int64_t ctas = G;
+    if (dp < 0) {
+        ctas = split_k_ctas(plan.tiles, nk, G, 8, 48);
+        if (ctas < 0) return;
+        dp = 0;
+    }
     plan.stream_k = true;
+    plan.split_indep = true;
     plan.dp_tiles = dp;
-    plan.ctas = G;
+    plan.ctas = ctas;
     plan.workspace = const_cast<void*>(ws);
 }
 

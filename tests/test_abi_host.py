@@ -201,9 +201,10 @@ def test_stream_k_planning():
 
 
 def test_tf32_stream_k_planning():
-    """The tensor-core path splits its last waves by the same rule, charged
-    with its own exchange cost: long K splits, K = 1024 stays data-parallel.
-    Its tiles are 128 x 256 with 32-wide K slices."""
+    """The tensor-core path splits with independent pieces: the last waves of
+    a many-tile long-K problem, or all tiles of a few-tile long-K one; short K
+    stays data-parallel and k_split = EXACT never splits it.  Its tiles are
+    128 x 256 with 32-wide K slices."""
     ws = BASE + (8 << 32)
     big = 1 << 30
     M, N = 2048, 5120
@@ -212,13 +213,25 @@ def test_tf32_stream_k_planning():
         B = (BASE + (1 << 32), 1, K, 0)                 # column-major: K-major
         C = rowmajor(BASE + (2 << 32), M, N, 1)
         p0 = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32)
-        assert p0["path"] == sg.PATH_TMA_TF32 and not p0["stream_k"]
+        assert p0["path"] == sg.PATH_TMA_TF32 and p0["stream_k"] == sg.STREAM_K_NONE
         assert (p0["tile_m"], p0["tile_n"], p0["tile_k"]) == (128, 256, 32)
         p1 = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32, workspace=ws, workspace_bytes=big)
-        assert p1["path"] == sg.PATH_TMA_TF32 and p1["stream_k"] == split
         assert p1["tiles"] == 320 and p1["k_slices"] == K // 32
         if split:
+            assert p1["stream_k"] == sg.STREAM_K_PIECES
             assert p1["ctas"] == 152 and p1["dp_tiles"] == 152
+        else:
+            assert p1["stream_k"] == sg.STREAM_K_NONE
+        px = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32, workspace=ws, workspace_bytes=big,
+                       k_split=sg.KSPLIT_EXACT)
+        assert px["stream_k"] == sg.STREAM_K_NONE
+    # 32 tiles of 1024 x 1024 with K = 8192: every tile split into pieces.
+    M = N = 1024
+    K = 8192
+    p = call_plan(rowmajor(BASE, M, K, 1), (BASE + (1 << 32), 1, K, 0),
+                  rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1, math=sg.MATH_TF32,
+                  workspace=ws, workspace_bytes=big)
+    assert p["stream_k"] == sg.STREAM_K_PIECES and p["dp_tiles"] == 0 and p["ctas"] == 152
 
 
 def test_split_k_pieces_planning():

@@ -420,30 +420,33 @@ def test_tf32_opt_in_falls_back_to_fp32(torch):
 
 
 TF32_STREAM_K_SHAPES = [
-    # (name, M, N, K, batch, accumulate); A row-major and B column-major (K-major).
-    # Long K: the tensor cores split tiles only when that outweighs the exchange.
-    ("160_tiles", 2048, 2560, 4096, 1, 0),
+    # (name, M, N, K, batch, accumulate); A row-major and B column-major (K-major)
+    ("160_tiles_long_k", 2048, 2560, 4096, 1, 0),
     ("ragged_k", 2560, 2560, 4000, 1, 1),
     ("batched", 1024, 1024, 4096, 5, 1),
+    ("320_tiles", 2048, 5120, 4096, 1, 0),
+    ("few_tiles_pieces", 1024, 1024, 8192, 1, 1),      # 32 tiles: several pieces per tile
 ]
 
 
 @pytest.mark.parametrize("shape", TF32_STREAM_K_SHAPES, ids=[s[0] for s in TF32_STREAM_K_SHAPES])
-def test_tf32_stream_k_bitwise_equals_data_parallel(torch, workspace, shape):
-    """On the tensor cores a split tile's head parks its accumulator in the
-    workspace and the tail loads it back into tensor memory before its first
-    MMA, so the k-ordered accumulation chain is the data-parallel one."""
+def test_tf32_split_pieces_parity_and_determinism(torch, workspace, shape):
+    """On the tensor cores a split tile's pieces accumulate independently and
+    the tail adds the earlier ones in a fixed order: within the TF32 bound,
+    identical from run to run; k_split = EXACT keeps the unsplit result."""
     _, M, N, K, batch, acc = shape
     rng = np.random.default_rng(M * 3 + N + K)
     case = wl.random_strided(rng, M, N, K, batch, "row16", "col16", values="real",
                              accumulate=acc, alpha=0.75)
     kw = dict(math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
-    dp, plan_dp = _run_ws(case, torch, None, kw)
-    sk, plan_sk = _run_ws(case, torch, workspace, kw)
-    assert plan_sk["path"] == sg.PATH_TMA_TF32
-    assert not plan_dp["stream_k"] and plan_sk["stream_k"], (plan_dp, plan_sk)
-    assert np.array_equal(dp, sk)
-    gu.check_points(case, sk, n=4000, tol=gu.TOL_TF32)
+    first, plan = _run_ws(case, torch, workspace, kw)
+    assert plan["path"] == sg.PATH_TMA_TF32 and plan["stream_k"] == sg.STREAM_K_PIECES, plan
+    gu.check_points(case, first, n=4000, tol=gu.TOL_TF32)
+    again, _ = _run_ws(case, torch, workspace, kw)
+    assert np.array_equal(first, again)
+    whole, _ = _run_ws(case, torch, None, kw)
+    exact, plan_x = _run_ws(case, torch, workspace, dict(kw, k_split=sg.KSPLIT_EXACT))
+    assert plan_x["stream_k"] == sg.STREAM_K_NONE and np.array_equal(exact, whole)
     st, where = sg.sbgemm_device_status()
     assert st == sg.SBGEMM_OK, where
 
