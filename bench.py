@@ -197,7 +197,8 @@ def kernel_source_digest(path_name):
     common = ["internal.h", "epilogue.cuh"]
     files = {"gather_ffma": ["ffma_gather.cu"] + common,
              "tma_ffma": ["ffma_tma.cu", "schedule.cuh", "ptx.cuh"] + common,
-             "tma_tf32": ["tf32_tc.cu", "schedule.cuh", "ptx.cuh"] + common}.get(path_name, [])
+             "tma_tf32": ["tf32_tc.cu", "schedule.cuh", "ptx.cuh"] + common,
+             "attention": ["attention.cu", "internal.h"]}.get(path_name, [])
     h = hashlib.sha256()
     for f in files:
         p = os.path.join(ROOT, "strided_gemm_gb300", "csrc", f)
@@ -589,7 +590,8 @@ def run_ours(args, world, rank, local, dist):
                 attention["roofline"] = {"bound": "alu", "kernel": f"attention ({n})",
                                          "achieved": round(c.flops / ms / 1e9, 2),
                                          "peak": round(fp32_peak, 2), "unit": "TFLOP/s",
-                                         "frac": round(c.flops / ms / 1e9 / fp32_peak, 4)}
+                                         "frac": round(c.flops / ms / 1e9 / fp32_peak, 4),
+                                         "traffic": profiled_traffic("attention", n)}
             attention["per_workload"][n] = row
 
     # Every other config of the workload list, each against its own roofline,
