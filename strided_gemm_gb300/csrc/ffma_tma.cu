@@ -133,12 +133,12 @@ struct Cfg {
 };
 
 // Transposes one K-major operand slice ([R rows][32 k], 128-byte swizzle) into
-// [32 k][R].  Two task shapes, measured per operand:
-//  - rows (A, 256 rows): task = one row's 16-byte chunk of 4 k values; a warp
+// [32 k][R].  Two task shapes, chosen by slice height (transpose_slice):
+//  - rows (256 rows): task = one row's 16-byte chunk of 4 k values; a warp
 //    takes 32 consecutive rows of one chunk, so its 16-byte loads hit 8
 //    distinct swizzled chunks per quarter-warp and its 4-byte stores 32
 //    consecutive columns: no bank conflicts, more instructions;
-//  - quads (B, 128 rows): task = a 4-row x 4-k block, four 16-byte loads and
+//  - quads (128 rows): task = a 4-row x 4-k block, four 16-byte loads and
 //    four 16-byte stores: fewer instructions, some load conflicts.
 template <int R>
 __device__ __forceinline__ void transpose_rows(const float* raw, float* dst) {
@@ -175,6 +175,13 @@ __device__ __forceinline__ void transpose_quads(const float* raw, float* dst) {
         *reinterpret_cast<float4*>(d + 2 * R) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
         *reinterpret_cast<float4*>(d + 3 * R) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
     }
+}
+
+// The task shape by slice height: row tasks for 256 rows, quads for 128.
+template <int R>
+__device__ __forceinline__ void transpose_slice(const float* raw, float* dst) {
+    if constexpr (R >= 256) transpose_rows<R>(raw, dst);
+    else transpose_quads<R>(raw, dst);
 }
 
 struct TileCoord { int64_t b, m0, n0; };
@@ -418,8 +425,8 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 if (issuer) drain<S>(sh.full, 0, is.issued);
                 return;
             }
-            if constexpr (TA) transpose_rows<BM>(sh.a[0], sh.at);
-            if constexpr (TB) transpose_quads<BN>(sh.b[0], sh.bt);
+            if constexpr (TA) transpose_slice<BM>(sh.a[0], sh.at);
+            if constexpr (TB) transpose_slice<BN>(sh.b[0], sh.bt);
             if constexpr (RAW_EARLY) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.empty[0]);
@@ -538,8 +545,8 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                         if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, nx), is.issued);
                         return;
                     }
-                    if constexpr (TA) transpose_rows<BM>(sh.a[stage], sh.at + nb * (BK * BM));
-                    if constexpr (TB) transpose_quads<BN>(sh.b[stage], sh.bt + nb * (BK * BN));
+                    if constexpr (TA) transpose_slice<BM>(sh.a[stage], sh.at + nb * (BK * BM));
+                    if constexpr (TB) transpose_slice<BN>(sh.b[stage], sh.bt + nb * (BK * BN));
                     if constexpr (RAW_EARLY) {
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sh.empty[stage]);
