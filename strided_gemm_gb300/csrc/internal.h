@@ -59,6 +59,8 @@ struct Plan {
     int k_slices = 0;               // K slices per tile
     bool stream_k = false;          // tiles split along K (needs workspace)
     bool split_indep = false;       // ... as independent pieces (fewer tiles than SMs)
+    bool transposed = false;        // computed as C^T = B^T A^T (tiles, schedule and
+                                    // launch are those of the transposed problem)
     int64_t dp_tiles = 0;           // tiles computed whole
     void* workspace = nullptr;      // caller's scratch when stream_k
 };
@@ -75,6 +77,10 @@ struct AttnProblem {
     int causal;
     int64_t q_len;           // rows per head for the causal position
 };
+// C^T = B^T A^T as a problem of its own: A' = B^T, B' = A^T, C' = C^T, M' = N,
+// N' = M (the fused addend transposed alike).
+Problem transposed_problem(const Problem& p);
+
 bool attention_supported(int64_t D, int64_t Dv);
 int64_t attention_max_rows();   // M limit of one launch
 cudaError_t launch_attention(const AttnProblem& a, cudaStream_t stream);

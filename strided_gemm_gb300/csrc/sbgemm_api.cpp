@@ -197,9 +197,10 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
     }
 
     const bool tma_ok = p.K > 0 && plan->a_tma && plan->b_tma;
-    // The tensor-core path reads both operands K-major (unit stride along K).
-    const bool tf32_ok = tma_ok && plan->a_layout == SBGEMM_LAYOUT_K_MAJOR &&
-                         plan->b_layout == SBGEMM_LAYOUT_K_MAJOR;
+    // The tensor-core path reads its operands K-major (unit stride along K);
+    // one MN-major operand is transposed in shared memory on the way.
+    const bool tf32_ok = tma_ok && (plan->a_layout == SBGEMM_LAYOUT_K_MAJOR ||
+                                    plan->b_layout == SBGEMM_LAYOUT_K_MAJOR);
     int path = o.force_path;
     if (path == SBGEMM_PATH_TMA_TF32 && !tf32_ok) return SBGEMM_ERR_UNSUPPORTED;
     if (path == SBGEMM_PATH_TMA_FFMA && !tma_ok) return SBGEMM_ERR_UNSUPPORTED;
@@ -219,15 +220,24 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
     plan->path = path;
 
     if (path == SBGEMM_PATH_TMA_TF32) {
+        // A K-major A with an N-major B is computed as C^T = B^T A^T: the
+        // MN-major operand to transpose in shared memory is then the 128-row
+        // one (B^T as A') instead of the 256-row one, at the price of the
+        // per-row epilogue stores (C^T has its unit stride along M').  Not
+        // worth it when N is below one tile row of the transposed problem.
+        const bool swap = plan->a_layout == SBGEMM_LAYOUT_K_MAJOR &&
+                          plan->b_layout != SBGEMM_LAYOUT_K_MAJOR && p.N >= 128;
+        const Problem q = swap ? transposed_problem(p) : p;
         const TmaFfmaConfig c = tf32_tc_config();
-        plan->tile_m = c.bm;
-        plan->tile_n = c.bn;
+        plan->transposed = swap;
+        plan->tile_m = swap ? c.bn : c.bm;   // reported in C's own orientation
+        plan->tile_n = swap ? c.bm : c.bn;
         plan->tile_k = c.bk;
         plan->ctas_per_sm = 1;
-        plan->tiles_m = (p.M + c.bm - 1) / c.bm;
-        plan->tiles_n = (p.N + c.bn - 1) / c.bn;
-        plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
-        tf32_tc_schedule(p, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace,
+        plan->tiles_m = (q.M + c.bm - 1) / c.bm;
+        plan->tiles_n = (q.N + c.bn - 1) / c.bn;
+        plan->tiles = plan->tiles_m * plan->tiles_n * q.batch;
+        tf32_tc_schedule(q, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace,
                          o.k_split);
         return SBGEMM_OK;
     }
@@ -278,6 +288,23 @@ Problem make_problem(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     p.epi = EpiParams{nullptr, 0, 0, 0, SBGEMM_ACT_NONE, 0, 0};
     return p;
 }
+
+}  // namespace
+
+Problem transposed_problem(const Problem& p) {
+    Problem q = p;
+    q.A = p.B; q.rsA = p.csB; q.csA = p.rsB; q.bsA = p.bsB;
+    q.B = p.A; q.rsB = p.csA; q.csB = p.rsA; q.bsB = p.bsA;
+    q.rsC = p.csC; q.csC = p.rsC;
+    q.M = p.N; q.N = p.M;
+    q.epi.rsD = p.epi.csD; q.epi.csD = p.epi.rsD;
+    q.epi.d_vec4 = q.epi.D && (q.epi.csD == 1 || q.N == 1) &&
+                   (reinterpret_cast<uintptr_t>(q.epi.D) % 16 == 0) && q.epi.rsD % 4 == 0 &&
+                   q.epi.bsD % 4 == 0;
+    return q;
+}
+
+namespace {
 
 void fill_info(const Plan& plan, sbgemm_plan_info* info) {
     std::memset(info, 0, sizeof(*info));
@@ -369,7 +396,9 @@ int run(Problem& p, const sbgemm_options& o, void* stream) {
     switch (plan.path) {
         case SBGEMM_PATH_GATHER_FFMA: err = launch_gather_ffma(p, plan, s); break;
         case SBGEMM_PATH_TMA_FFMA: err = launch_tma_ffma(p, plan, props->sm_count, s); break;
-        case SBGEMM_PATH_TMA_TF32: err = launch_tf32_tc(p, plan, props->sm_count, s); break;
+        case SBGEMM_PATH_TMA_TF32:
+            err = launch_tf32_tc(plan.transposed ? transposed_problem(p) : p, plan, props->sm_count, s);
+            break;
         default: return SBGEMM_ERR_UNSUPPORTED;
     }
     if (err != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }

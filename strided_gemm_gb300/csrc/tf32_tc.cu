@@ -1,6 +1,8 @@
 // TF32 tensor-core path (opt-in through sbgemm_options.math): tcgen05.mma
-// kind::tf32 with fp32 accumulators in tensor memory, for operands whose unit
-// stride runs along K (A row-major, B = a row-major matrix read transposed).
+// kind::tf32 with fp32 accumulators in tensor memory.  The MMAs read both
+// operands K-major (unit stride along K); one operand whose unit stride runs
+// along M or N is transposed in shared memory on the way by four transposer
+// warps (raw 32 x 32 boxes -> the K-major swizzled layout).
 //
 // Persistent, warp-specialised CTAs, one per SM, 192 threads:
 //  * warp 0, one lane: TMA producer.  Walks the CTA's tiles and their 32-deep
@@ -47,16 +49,60 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 32;   // CTA tile; UMMA 128 x 256 x 8
 constexpr int kMmaK = 8;                     // tf32 elements per MMA
-constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 4;         // 16 KB
 constexpr int kBBytes = BN * BK * 4;         // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kAccCols = BN;            // fp32 accumulator: one column per n
 constexpr uint32_t kTmemCols = 2 * kAccCols; // double-buffered accumulator
 constexpr int kEpiWarps = 4;
+constexpr int kTransWarps = 4;               // transposers of an MN-major operand
 constexpr int kBM128 = BM;                               // rows of a partial slot
 constexpr int64_t kSlotFloat4 = (int64_t)BM * BN / 4;    // one partial tile, in float4
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kBox = 32 * 32;                // floats in one 32 x 32 raw box of an MN-major operand
+
+// Shared-memory plan by operand orientation.  MN: 0 both operands K-major;
+// 1 A MN-major (unit stride along M); 2 B MN-major (along N).  An MN-major
+// slice lands as raw 32 x 32 boxes (rows along K, 128-byte swizzle) in a ring
+// of its own, and the transposer warps rewrite it into the K-major swizzled
+// layout the MMAs read.
+template <int MN>
+struct TCfg {
+    static constexpr bool kTA = MN == 1, kTB = MN == 2;
+    static constexpr int kWarps = 2 + kEpiWarps + (MN ? kTransWarps : 0);
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kStages = MN ? 3 : 4;          // K-major stages (MMA operands)
+    static constexpr int kRawRows = kTA ? BM : (kTB ? BN : 0);
+    static constexpr int kRawStages = kTA ? 3 : (kTB ? 2 : 0);
+    static constexpr int kStageBufs = kTB ? 1 : 2;       // epilogue staging tiles per warp
+    // Bytes the K-major operand copies bring into a stage.
+    static constexpr uint32_t kKBytes = (kTA ? 0 : kABytes) + (kTB ? 0 : kBBytes);
+    static constexpr uint32_t kRawBytes = kRawRows * BK * 4;
+    static constexpr int kRawSlots = kRawStages > 0 ? kRawStages : 1;
+    static constexpr int kRawFloats = kRawRows > 0 ? kRawRows * BK : 4;
+    struct Smem {
+        float a[kStages][BM * BK];
+        float b[kStages][BN * BK];
+        // Per epilogue warp: pieces of C (alternating by store when there are
+        // two) in the 128-byte swizzled layout of its tensor map (16-byte chunk
+        // q of row r at chunk q ^ (r & 7)).
+        alignas(1024) float stage[kEpiWarps][kStageBufs][32 * 32];
+        alignas(1024) float raw[kRawSlots][kRawFloats];
+        uint64_t full[kStages];
+        uint64_t empty[kStages];
+        uint64_t tdone[kStages];      // the transposers wrote stage s's MN-major operand
+        uint64_t rfull[kRawSlots];
+        uint64_t rempty[kRawSlots];
+        uint64_t acc_full[2];
+        uint64_t acc_empty[2];
+        uint64_t mma_done;
+        uint64_t stored;          // every epilogue thread wrote its head partial
+        uint64_t c_old[kEpiWarps];   // a warp's C_old piece landed in its staging tile
+        Schedule sched;
+        uint32_t tmem_base;
+    };
+    static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(kRawBytes % 4096 == 0, "raw slices are whole 32 x 32 boxes");
+};
 
 __device__ unsigned int g_wait_status = 0;
 
@@ -76,25 +122,6 @@ struct Params {
     unsigned int* ws_flag;        // [grid] partial-ready flags, zeroed before launch
 };
 
-struct Smem {
-    float a[kStages][BM * BK];
-    float b[kStages][BN * BK];
-    // Per epilogue warp: two 32 x 32 pieces of C (alternating by store) in the
-    // 128-byte swizzled layout of its tensor map (16-byte chunk q of row r at
-    // chunk q ^ (r & 7)).
-    alignas(1024) float stage[kEpiWarps][2][32 * 32];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
-    uint64_t mma_done;
-    uint64_t stored;          // every epilogue thread wrote its head partial
-    uint64_t c_old[kEpiWarps];   // a warp's C_old piece landed in its staging tile
-    Schedule sched;
-    uint32_t tmem_base;
-};
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // Instruction descriptor, kind::tf32: D fp32, A and B tf32, both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.
@@ -115,10 +142,12 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t) {
     return {b, (first_m + w % gm) * BM, (w / gm) * BN};
 }
 
-__device__ __forceinline__ void producer(Smem& sh, const CUtensorMap* ta, const CUtensorMap* tb,
-                                         const Params& p) {
-    uint32_t stage = 0, phase = 0;
-    uint64_t issued = 0;
+template <int MN>
+__device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUtensorMap* ta,
+                                         const CUtensorMap* tb, const Params& p) {
+    using C = TCfg<MN>;
+    constexpr int S = C::kStages, R = C::kRawSlots;
+    uint64_t i = 0;   // slices issued
     bool ok = true;
     const int64_t n_items = sh.sched.n_items;
     for (int64_t w = 0; w < n_items && ok; ++w) {
@@ -126,30 +155,122 @@ __device__ __forceinline__ void producer(Smem& sh, const CUtensorMap* ta, const 
         const TileCoord tc = tile_coord(p, itm.tile);
         const int ba = p.a_bcast ? 0 : (int)tc.b;
         const int bb = p.b_bcast ? 0 : (int)tc.b;
-        for (int kt = itm.kb; kt < itm.ke; ++kt) {
-            if (issued >= (uint64_t)kStages && !mbar_wait(&sh.empty[stage], phase ^ 1u)) {
+        for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
+            if constexpr (MN != 0) {
+                // The MN-major operand: 32 x 32 boxes along M (A) or N (B), rows
+                // along K, into the raw ring.
+                const int r = (int)(i % R);
+                if (i >= (uint64_t)R && !mbar_wait(&sh.rempty[r], (uint32_t)(((i / R) - 1) & 1))) {
+                    record_status(&g_wait_status, kWaitEmpty);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sh.rfull[r], C::kRawBytes);
+                const CUtensorMap* tm = C::kTA ? ta : tb;
+                const int x0 = C::kTA ? (int)tc.m0 : (int)tc.n0;
+                const int bz = C::kTA ? ba : bb;
+#pragma unroll 1
+                for (int j = 0; j < C::kRawRows / 32; ++j)
+                    tma_load_3d(sh.raw[r] + j * kBox, tm, &sh.rfull[r], x0 + 32 * j, kt * BK, bz);
+            }
+            const int st = (int)(i % S);
+            if (i >= (uint64_t)S && !mbar_wait(&sh.empty[st], (uint32_t)(((i / S) - 1) & 1))) {
                 record_status(&g_wait_status, kWaitEmpty);
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(&sh.full[stage], kStageBytes);
-            tma_load_3d(sh.a[stage], ta, &sh.full[stage], kt * BK, (int)tc.m0, ba);
-            tma_load_3d(sh.b[stage], tb, &sh.full[stage], kt * BK, (int)tc.n0, bb);
-            ++issued;
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            mbar_arrive_expect_tx(&sh.full[st], C::kKBytes);
+            if constexpr (!C::kTA) tma_load_3d(sh.a[st], ta, &sh.full[st], kt * BK, (int)tc.m0, ba);
+            if constexpr (!C::kTB) tma_load_3d(sh.b[st], tb, &sh.full[st], kt * BK, (int)tc.n0, bb);
         }
     }
-    // Wait for the copies still landing (the last kStages issued).
-    const uint64_t first = issued > (uint64_t)kStages ? issued - kStages : 0;
-    for (uint64_t q = first; q < issued; ++q)
-        if (!mbar_wait(&sh.full[q % kStages], (uint32_t)((q / kStages) & 1))) {
+    // Wait for the copies still landing.
+    for (uint64_t q = i > (uint64_t)S ? i - S : 0; q < i; ++q)
+        if (!mbar_wait(&sh.full[q % S], (uint32_t)((q / S) & 1))) {
             record_status(&g_wait_status, kWaitDrain);
             return;
         }
+    if constexpr (MN != 0) {
+        for (uint64_t q = i > (uint64_t)R ? i - R : 0; q < i; ++q)
+            if (!mbar_wait(&sh.rfull[q % R], (uint32_t)((q / R) & 1))) {
+                record_status(&g_wait_status, kWaitDrain);
+                return;
+            }
+    }
 }
 
-__device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params& p) {
-    uint32_t stage = 0, phase = 0;
+// Rewrites the raw boxes of one MN-major slice (rows along K, 128-byte
+// swizzle) into the K-major swizzled layout of the MMA operand (row m = 32 k
+// values, 16-byte chunk c at chunk c ^ (m & 7)), in 4 x 4 quads: four 16-byte
+// loads of 4 rows of K, four 16-byte stores of 4 rows of M.  The quads of a
+// quarter-warp span 2 groups of 4 rows and 4 groups of 4 k, so the stores hit
+// 8 distinct chunks (no bank conflict) and the loads two ways at most.
+template <int ROWS>
+__device__ __forceinline__ void transpose_mn_slice(const float* raw, float* dst, int t) {
+    constexpr int kQuads = (ROWS / 4) * (BK / 4);
+#pragma unroll 1
+    for (int q = t; q < kQuads; q += kTransWarps * 32) {
+        const int kq = (q & 3) | (((q >> 5) & 1) << 2);         // 4-k group, 0..7
+        const int mq = ((q >> 6) << 3) | ((q >> 2) & 7);         // 4-row group
+        const float* box = raw + (mq >> 3) * kBox;
+        const int mc = mq & 7;                                    // chunk of the box row
+        float4 v[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int k = 4 * kq + r;
+            v[r] = *reinterpret_cast<const float4*>(box + k * 32 + ((mc ^ (k & 7)) << 2));
+        }
+        const int m = 4 * mq;
+        *reinterpret_cast<float4*>(dst + (m + 0) * 32 + ((kq ^ ((m + 0) & 7)) << 2)) =
+            make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
+        *reinterpret_cast<float4*>(dst + (m + 1) * 32 + ((kq ^ ((m + 1) & 7)) << 2)) =
+            make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
+        *reinterpret_cast<float4*>(dst + (m + 2) * 32 + ((kq ^ ((m + 2) & 7)) << 2)) =
+            make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
+        *reinterpret_cast<float4*>(dst + (m + 3) * 32 + ((kq ^ ((m + 3) & 7)) << 2)) =
+            make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+    }
+}
+
+// Transposer warps: per slice, wait for the raw boxes and for the stage's
+// previous MMAs, rewrite the MN-major operand, order the writes before the
+// tensor cores' reads (async proxy), then signal the MMA lane and free the
+// raw slot.
+template <int MN>
+__device__ __forceinline__ void transposer(typename TCfg<MN>::Smem& sh, const Params& p, int t,
+                                           int lane) {
+    using C = TCfg<MN>;
+    constexpr int S = C::kStages, R = C::kRawSlots;
+    uint64_t i = 0;
+    const int64_t n_items = sh.sched.n_items;
+    for (int64_t w = 0; w < n_items; ++w) {
+        const Item itm = sh.sched.item(w, p.nk);
+        for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
+            const int r = (int)(i % R), st = (int)(i % S);
+            if (!mbar_wait(&sh.rfull[r], (uint32_t)((i / R) & 1))) {
+                record_status(&g_wait_status, kWaitFull);
+                return;
+            }
+            if (i >= (uint64_t)S && !mbar_wait(&sh.empty[st], (uint32_t)(((i / S) - 1) & 1))) {
+                record_status(&g_wait_status, kWaitEmpty);
+                return;
+            }
+            transpose_mn_slice<C::kRawRows>(sh.raw[r], C::kTA ? sh.a[st] : sh.b[st], t);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sh.tdone[st]);
+                mbar_arrive(&sh.rempty[r]);
+            }
+        }
+    }
+}
+
+template <int MN>
+__device__ __forceinline__ void mma_issuer(typename TCfg<MN>::Smem& sh, uint32_t tmem, const Params& p) {
+    using C = TCfg<MN>;
+    constexpr int S = C::kStages;
+    uint64_t i = 0;
     bool ok = true;
     const int64_t n_items = sh.sched.n_items;
     for (int64_t w = 0; w < n_items && ok; ++w) {
@@ -162,15 +283,17 @@ __device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params
         }
         tc_fence_after();
         const uint32_t d = tmem + buf * kAccCols;
-        for (int kt = itm.kb; kt < itm.ke; ++kt) {
-            if (!mbar_wait(&sh.full[stage], phase)) {
+        for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
+            const int st = (int)(i % S);
+            const uint32_t ph = (uint32_t)((i / S) & 1);
+            if (!mbar_wait(&sh.full[st], ph) || (MN != 0 && !mbar_wait(&sh.tdone[st], ph))) {
                 record_status(&g_wait_status, kWaitFull);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sh.a[stage]);
-            const uint32_t b0 = smem_u32(sh.b[stage]);
+            const uint32_t a0 = smem_u32(sh.a[st]);
+            const uint32_t b0 = smem_u32(sh.b[st]);
 #pragma unroll
             for (int kk = 0; kk < BK / kMmaK; ++kk) {
                 const uint64_t ad = umma_desc_kmajor_sw128(a0 + kk * kMmaK * 4);
@@ -178,8 +301,7 @@ __device__ __forceinline__ void mma_issuer(Smem& sh, uint32_t tmem, const Params
                 const bool acc = kt > itm.kb || kk > 0;
                 mma_tf32(d, ad, bd, kIdesc, acc ? 1u : 0u);
             }
-            mma_commit(&sh.empty[stage]);
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            mma_commit(&sh.empty[st]);
         }
         if (!ok) break;
         mma_commit(&sh.acc_full[buf]);
@@ -237,8 +359,8 @@ __device__ __forceinline__ void add_pieces(float (&v)[32], const Params& p, int6
 // a TMA load), adds the fused addend and applies ACT, writes the piece into
 // its staging tile and lane 0 issues one bulk tensor store (the parts outside
 // C are not written).  Returns false if a C_old load did not land in time.
-template <int ACT>
-__device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap, const Params& p,
+template <int ACT, typename SmemT, int NBUF>
+__device__ __forceinline__ bool store_tile_tma(SmemT& sh, const CUtensorMap* cmap, const Params& p,
                                                const TileCoord& tc, uint32_t taddr, int quarter,
                                                int lane, int ew, uint32_t& c_loads,
                                                uint32_t& stores, int64_t first_piece) {
@@ -256,10 +378,10 @@ __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap
         // accumulation C_old must land there first; without, the tile is waited
         // for only just before it is written, so that the TMEM load and the
         // arithmetic overlap the earlier stores.
-        float* st = sh.stage[ew][stores & 1u];
+        float* st = sh.stage[ew][NBUF == 2 ? (stores & 1u) : 0u];
         if (p.accumulate) {
             if (lane == 0) {
-                bulk_wait_read_all_but_one();
+                if (NBUF == 2) bulk_wait_read_all_but_one(); else bulk_wait_read_all();
                 if (piece_in) {
                     mbar_arrive_expect_tx(&sh.c_old[ew], 32 * 32 * 4);
                     tma_load_3d(st, cmap, &sh.c_old[ew], (int)n0, (int)m_base, (int)tc.b);
@@ -310,7 +432,9 @@ __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap
             for (int e = 0; e < 32; ++e) v[e] = act_fn<ACT>(v[e]);
         }
         if (!p.accumulate) {
-            if (lane == 0) bulk_wait_read_all_but_one();
+            if (lane == 0) {
+                if (NBUF == 2) bulk_wait_read_all_but_one(); else bulk_wait_read_all();
+            }
             __syncwarp();
         }
 #pragma unroll
@@ -328,8 +452,12 @@ __device__ __forceinline__ bool store_tile_tma(Smem& sh, const CUtensorMap* cmap
     return true;
 }
 
-__device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensorMap* cmap,
-                                         const Params& p, int warp, int lane) {
+template <int MN>
+__device__ __forceinline__ void epilogue(typename TCfg<MN>::Smem& sh, uint32_t tmem,
+                                         const CUtensorMap* cmap, const Params& p, int warp,
+                                         int lane) {
+    using SmemT = typename TCfg<MN>::Smem;
+    constexpr int NB = TCfg<MN>::kStageBufs;
     const int quarter = warp & 3;               // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
     const int ew = warp - 2;                    // epilogue warp index: staging tile, C_old barrier
@@ -384,12 +512,12 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
             const TileCoord tc = tile_coord(p, itm.tile);
             bool ok;
             switch (p.epi.act) {
-                case kActRelu: ok = store_tile_tma<kActRelu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                case kActSigmoid: ok = store_tile_tma<kActSigmoid>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                case kActSilu: ok = store_tile_tma<kActSilu>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                case kActGeluTanh: ok = store_tile_tma<kActGeluTanh>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                case kActGeluErf: ok = store_tile_tma<kActGeluErf>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                default: ok = store_tile_tma<kActNone>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActRelu: ok = store_tile_tma<kActRelu, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActSigmoid: ok = store_tile_tma<kActSigmoid, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActSilu: ok = store_tile_tma<kActSilu, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActGeluTanh: ok = store_tile_tma<kActGeluTanh, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                case kActGeluErf: ok = store_tile_tma<kActGeluErf, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
+                default: ok = store_tile_tma<kActNone, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
             }
             if (!ok) {
                 record_status(&g_wait_status, kWaitFull);
@@ -410,14 +538,26 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
                 const int64_t n0 = tc.n0 + c * 32;
                 if (!row_ok || n0 >= p.N) continue;
                 if (first_piece >= 0) add_pieces(v, p, first_piece, (int64_t)blockIdx.x - 1, c, row);
+                // C_old of the whole piece is loaded before any store, so the 32
+                // loads are in flight together (the compiler cannot move a load
+                // of C above a store to C).
+                if (p.accumulate) {
+                    float o[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = n0 + e < p.N ? crow[(n0 + e) * p.csC] : 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = fmaf(p.alpha, v[e], o[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = p.alpha * v[e];
+                }
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int64_t n = n0 + e;
                     if (n < p.N) {
-                        float* cptr = crow + n * p.csC;
-                        float r = p.accumulate ? fmaf(p.alpha, v[e], *cptr) : p.alpha * v[e];
+                        float r = v[e];
                         if (p.epi.on) r = finish(p.epi, r, tc.b, m, n);
-                        *cptr = r;
+                        crow[n * p.csC] = r;
                     }
                 }
             }
@@ -428,9 +568,13 @@ __device__ __forceinline__ void epilogue(Smem& sh, uint32_t tmem, const CUtensor
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MN>
+__global__ void __launch_bounds__(TCfg<MN>::kThreads, 1)
 tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                const __grid_constant__ CUtensorMap tcm, const Params p) {
+    using C = TCfg<MN>;
+    using Smem = typename C::Smem;
+    constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     Smem& sh = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
@@ -439,6 +583,11 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], 1);
+            mbar_init(&sh.tdone[s], kTransWarps);
+        }
+        for (int r = 0; r < C::kRawSlots; ++r) {
+            mbar_init(&sh.rfull[r], 1);
+            mbar_init(&sh.rempty[r], kTransWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sh.acc_full[b], 1);
@@ -463,13 +612,15 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     const uint32_t tmem = sh.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) producer(sh, &ta, &tb, p);
+        if (lane == 0) producer<MN>(sh, &ta, &tb, p);
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer(sh, tmem, p);
-    } else {
-        epilogue(sh, tmem, &tcm, p, warp, lane);
+        if (lane == 0) mma_issuer<MN>(sh, tmem, p);
+    } else if (warp < 2 + kEpiWarps) {
+        epilogue<MN>(sh, tmem, &tcm, p, warp, lane);
         // Shared memory must outlive the bulk stores that read it.
         if (lane == 0) bulk_wait_all();
+    } else if constexpr (MN != 0) {
+        transposer<MN>(sh, p, threadIdx.x - (2 + kEpiWarps) * 32, lane);
     }
 
     tc_fence_before();
@@ -478,6 +629,20 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// An MN-major operand (unit stride along M or N): dims (M or N, K, batch), a
+// 32 x 32 box (32 values along the unit stride, 32 rows along K), 128-byte
+// swizzle.
+bool make_mn_map(CUtensorMap* map, const float* base, int64_t inner, int64_t K, int64_t sk,
+                 int64_t sb, int64_t batch, bool broadcast) {
+    const int64_t nb = broadcast ? 1 : batch;
+    const int64_t sk_b = K > 1 ? sk * 4 : ((inner * 4 + 15) / 16) * 16;
+    const int64_t sb_b = nb > 1 ? sb * 4 : sk_b * (K > 1 ? K : 1);
+    const uint64_t dims[3] = {(uint64_t)inner, (uint64_t)K, (uint64_t)nb};
+    const uint64_t strides[2] = {(uint64_t)sk_b, (uint64_t)sb_b};
+    const uint32_t box[3] = {32, 32, 1};
+    return encode_tmap_f32_3d(map, base, dims, strides, box, true);
 }
 
 bool make_kmajor_map(CUtensorMap* map, const float* base, int64_t K, int64_t rows, int64_t so,
@@ -514,26 +679,32 @@ bool make_c_map(CUtensorMap* map, const Problem& pr) {
 
 }  // namespace
 
-TmaFfmaConfig tf32_tc_config() { return {BM, BN, BK, kStages, kThreads}; }
+TmaFfmaConfig tf32_tc_config() { return {BM, BN, BK, TCfg<0>::kStages, TCfg<0>::kThreads}; }
 
-cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cudaStream_t stream) {
+namespace {
+
+template <int MN>
+cudaError_t launch_mn(const Problem& pr, const Plan& plan, cudaStream_t stream) {
+    using C = TCfg<MN>;
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(tf32_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(tf32_tc_kernel<MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
     }
     CUtensorMap ta, tb;
     const bool a_bc = pr.batch == 1 || pr.bsA == 0;
     const bool b_bc = pr.batch == 1 || pr.bsB == 0;
-    if (!make_kmajor_map(&ta, pr.A, pr.K, pr.M, pr.rsA, pr.bsA, pr.batch, a_bc, BM))
-        return cudaErrorInvalidValue;
-    if (!make_kmajor_map(&tb, pr.B, pr.K, pr.N, pr.csB, pr.bsB, pr.batch, b_bc, BN))
-        return cudaErrorInvalidValue;
+    // A[m][k] = A + m*rsA + k*csA; B[k][n] = B + k*rsB + n*csB.
+    const bool ok_a = C::kTA ? make_mn_map(&ta, pr.A, pr.M, pr.K, pr.csA, pr.bsA, pr.batch, a_bc)
+                             : make_kmajor_map(&ta, pr.A, pr.K, pr.M, pr.rsA, pr.bsA, pr.batch, a_bc, BM);
+    const bool ok_b = C::kTB ? make_mn_map(&tb, pr.B, pr.N, pr.K, pr.rsB, pr.bsB, pr.batch, b_bc)
+                             : make_kmajor_map(&tb, pr.B, pr.K, pr.N, pr.csB, pr.bsB, pr.batch, b_bc, BN);
+    if (!ok_a || !ok_b) return cudaErrorInvalidValue;
     Params p;
     p.C = pr.C; p.rsC = pr.rsC; p.csC = pr.csC; p.bsC = pr.bsC;
     p.M = pr.M; p.N = pr.N; p.K = pr.K;
@@ -561,20 +732,34 @@ cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cu
         // CTAs wait on one another's partial sums: make them co-resident.
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.blockDim = dim3(C::kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeCooperative;
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel, ta, tb, tcm, p);
+        e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel<MN>, ta, tb, tcm, p);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    tf32_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(ta, tb, tcm, p);
+    tf32_tc_kernel<MN><<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(ta, tb, tcm, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cudaStream_t stream) {
+    (void)sm_count;
+    // Orientation of the problem as launched (the plan's layouts describe C's
+    // own orientation, which differs when the plan computes C^T).
+    const bool a_mn = !(pr.K == 1 || pr.csA == 1);
+    const bool b_mn = !(pr.K == 1 || pr.rsB == 1);
+    if (a_mn && b_mn) return cudaErrorInvalidValue;   // the planner never sends this here
+    if (a_mn) return launch_mn<1>(pr, plan, stream);
+    if (b_mn) return launch_mn<2>(pr, plan, stream);
+    return launch_mn<0>(pr, plan, stream);
 }
 
 // The FFMA path's rules (stream_k_dp_tiles, split_k_ctas), with independent

@@ -269,3 +269,18 @@ def test_split_k_pieces_planning():
     with pytest.raises(sg.SbgemmError) as e:
         call_plan(A, B, C, M, N, K, 1, workspace=ws, workspace_bytes=big, k_split=3)
     assert e.value.status == sg.SBGEMM_ERR_INVALID_VALUE
+
+
+def test_tf32_takes_one_mn_major_operand():
+    """TF32 reads operands K-major; one MN-major operand (A M-major or B
+    N-major) is transposed in shared memory, both MN-major fall back."""
+    M, N, K = 1024, 768, 512
+    A_k, A_m = rowmajor(BASE, M, K, 1), (BASE, 1, M, 0)
+    B_k, B_n = (BASE + (1 << 32), 1, K, 0), rowmajor(BASE + (1 << 32), K, N, 1)
+    C = rowmajor(BASE + (2 << 32), M, N, 1)
+    for A, B, tf32 in ((A_k, B_k, True), (A_m, B_k, True), (A_k, B_n, True), (A_m, B_n, False)):
+        p = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32)
+        assert (p["path"] == sg.PATH_TMA_TF32) == tf32, (A, B, p)
+    with pytest.raises(sg.SbgemmError) as e:
+        call_plan(A_m, B_n, C, M, N, K, 1, math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
+    assert e.value.status == sg.SBGEMM_ERR_UNSUPPORTED

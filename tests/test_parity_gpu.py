@@ -362,7 +362,10 @@ def test_linear_backward_helper(torch, workspace):
 
 # ---- TF32 tensor-core path (opt-in) -------------------------------------------
 
-TF32_WORKLOADS = ["c2a", "c2b", "c3", "c3gqa", "c5a", "c5b"]   # both operands K-major
+# Both operands K-major, or one MN-major (transposed in shared memory): c4's V
+# and c5c's B are N-major, c5d's A is M-major.
+TF32_WORKLOADS = ["c2a", "c2b", "c3", "c3gqa", "c4", "c5a", "c5b", "c5c", "c5d",
+                  "f1dxa", "f1dxb", "f4dist"]
 
 
 @pytest.mark.parametrize("name", TF32_WORKLOADS)
@@ -378,7 +381,8 @@ TF32_SHAPES = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (130, 70, 257), (257, 129, 
                (128, 32, 256), (300, 1000, 520)]
 
 
-TF32_LAYOUTS = [("row16", "col16")]   # A row-major, B column-major: both K-major
+# (A, B): both K-major; A M-major with B K-major; A K-major with B N-major.
+TF32_LAYOUTS = [("row16", "col16"), ("col16", "col16"), ("row16", "row16")]
 
 
 @pytest.mark.parametrize("mkn", TF32_SHAPES, ids=[f"{m}x{k}x{n}" for m, k, n in TF32_SHAPES])
@@ -402,9 +406,10 @@ def test_tf32_awkward_shapes(torch, mkn, layouts):
 
 def test_tf32_opt_in_falls_back_to_fp32(torch):
     """math=TF32 without a forced path serves operands the tensor-core path
-    does not take (MN-major tiles; strides TMA cannot fetch) with strict fp32."""
-    case = wl.make("c4", "real", **wl.small_shape("c4"))          # V is N-major
+    does not take (both operands MN-major; strides TMA cannot fetch) with
+    strict fp32."""
     rng = np.random.default_rng(21)
+    case = wl.random_strided(rng, 300, 260, 200, 2, "col16", "row16", values="real")   # both MN-major
     general = wl.random_strided(rng, 70, 90, 50, 2, "gap", "neg_row", values="real",
                                 accumulate=1, alpha=0.5)
     for c, want_path in ((case, (sg.PATH_TMA_FFMA, sg.PATH_GATHER_FFMA)),
@@ -465,9 +470,10 @@ def test_tf32_stream_k_integer_exact(torch, workspace):
     gu.check_points(case, first, n=4000, exact=True)
 
 
-@pytest.mark.parametrize("name", ["c3", "c3gqa", "c5a", "c5b"])
+@pytest.mark.parametrize("name", ["c3", "c3gqa", "c4", "c5a", "c5b", "c5c", "c5d"])
 def test_tf32_full_size_sampled(torch, name):
     case = wl.make(name, "real")
+    assert _supported(case, sg.MATH_TF32, sg.PATH_TMA_TF32)
     got = gu.run_case(case, torch, math=sg.MATH_TF32)
     gu.check_points(case, got, tol=gu.TOL_TF32)
     case_i = wl.make(name, "int")
