@@ -115,7 +115,7 @@ struct Params {
     float alpha;
     int accumulate;
     int a_bcast, b_bcast;
-    int c_tma;                    // C goes out through its tensor map (unit stride along N)
+    int c_tma;                    // C goes out through its tensor map: 1 unit stride along N, 2 along M
     int64_t dp_tiles, sk_units;   // work list (see schedule.cuh)
     EpiParams epi;                // fused epilogue (epilogue.cuh); epi.on == 0: none
     float4* ws_partial;           // [grid][8 chunks][8 quads][128 rows] partial sums
@@ -358,8 +358,12 @@ __device__ __forceinline__ void add_pieces(float (&v)[32], const Params& p, int6
 // per 32-column piece the warp forms alpha*acc (+ C_old, itself brought in by
 // a TMA load), adds the fused addend and applies ACT, writes the piece into
 // its staging tile and lane 0 issues one bulk tensor store (the parts outside
-// C are not written).  Returns false if a C_old load did not land in time.
-template <int ACT, typename SmemT, int NBUF>
+// C are not written).  A row-major C (COLC false) stages a 128-byte row of C
+// per lane, written as float4s; a column-major C stages one 128-byte column
+// of the piece per n, each lane (one m) writing its element of every column,
+// which the 128-byte swizzle keeps free of bank conflicts.  Returns false if
+// a C_old load did not land in time.
+template <int ACT, bool COLC, typename SmemT, int NBUF>
 __device__ __forceinline__ bool store_tile_tma(SmemT& sh, const CUtensorMap* cmap, const Params& p,
                                                const TileCoord& tc, uint32_t taddr, int quarter,
                                                int lane, int ew, uint32_t& c_loads,
@@ -384,7 +388,8 @@ __device__ __forceinline__ bool store_tile_tma(SmemT& sh, const CUtensorMap* cma
                 if (NBUF == 2) bulk_wait_read_all_but_one(); else bulk_wait_read_all();
                 if (piece_in) {
                     mbar_arrive_expect_tx(&sh.c_old[ew], 32 * 32 * 4);
-                    tma_load_3d(st, cmap, &sh.c_old[ew], (int)n0, (int)m_base, (int)tc.b);
+                    if (COLC) tma_load_3d(st, cmap, &sh.c_old[ew], (int)m_base, (int)n0, (int)tc.b);
+                    else tma_load_3d(st, cmap, &sh.c_old[ew], (int)n0, (int)m_base, (int)tc.b);
                 }
             }
             __syncwarp();
@@ -397,13 +402,19 @@ __device__ __forceinline__ bool store_tile_tma(SmemT& sh, const CUtensorMap* cma
         if (p.accumulate) {
             if (!mbar_wait(&sh.c_old[ew], c_loads & 1u)) return false;
             ++c_loads;
+if constexpr (COLC) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 o = *reinterpret_cast<const float4*>(st + lane * 32 + ((q ^ (lane & 7)) << 2));
-                v[4 * q + 0] = fmaf(p.alpha, v[4 * q + 0], o.x);
-                v[4 * q + 1] = fmaf(p.alpha, v[4 * q + 1], o.y);
-                v[4 * q + 2] = fmaf(p.alpha, v[4 * q + 2], o.z);
-                v[4 * q + 3] = fmaf(p.alpha, v[4 * q + 3], o.w);
+                for (int e = 0; e < 32; ++e)
+                    v[e] = fmaf(p.alpha, v[e], st[e * 32 + (((lane >> 2) ^ (e & 7)) << 2) + (lane & 3)]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 o = *reinterpret_cast<const float4*>(st + lane * 32 + ((q ^ (lane & 7)) << 2));
+                    v[4 * q + 0] = fmaf(p.alpha, v[4 * q + 0], o.x);
+                    v[4 * q + 1] = fmaf(p.alpha, v[4 * q + 1], o.y);
+                    v[4 * q + 2] = fmaf(p.alpha, v[4 * q + 2], o.z);
+                    v[4 * q + 3] = fmaf(p.alpha, v[4 * q + 3], o.w);
+                }
             }
             __syncwarp();                  // every lane has read its C_old row
         } else {
@@ -437,19 +448,41 @@ __device__ __forceinline__ bool store_tile_tma(SmemT& sh, const CUtensorMap* cma
             }
             __syncwarp();
         }
+if constexpr (COLC) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(st + lane * 32 + ((q ^ (lane & 7)) << 2)) =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int e = 0; e < 32; ++e) st[e * 32 + (((lane >> 2) ^ (e & 7)) << 2) + (lane & 3)] = v[e];
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(st + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_3d(cmap, st, (int)n0, (int)m_base, (int)tc.b);
+            if (COLC) tma_store_3d(cmap, st, (int)m_base, (int)n0, (int)tc.b);
+            else tma_store_3d(cmap, st, (int)n0, (int)m_base, (int)tc.b);
             bulk_commit();
         }
         ++stores;
     }
     return true;
+}
+
+// store_tile_tma for the run-time activation.
+template <bool COLC, typename SmemT, int NB>
+__device__ __forceinline__ bool store_tile_act(SmemT& sh, const CUtensorMap* cmap, const Params& p,
+                                               const TileCoord& tc, uint32_t taddr, int quarter,
+                                               int lane, int ew, uint32_t& c_loads,
+                                               uint32_t& stores, int64_t first_piece) {
+    switch (p.epi.act) {
+        case kActRelu: return store_tile_tma<kActRelu, COLC, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece);
+        case kActSigmoid: return store_tile_tma<kActSigmoid, COLC, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece);
+        case kActSilu: return store_tile_tma<kActSilu, COLC, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece);
+        case kActGeluTanh: return store_tile_tma<kActGeluTanh, COLC, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece);
+        case kActGeluErf: return store_tile_tma<kActGeluErf, COLC, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece);
+        default: return store_tile_tma<kActNone, COLC, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece);
+    }
 }
 
 template <int MN>
@@ -510,15 +543,9 @@ __device__ __forceinline__ void epilogue(typename TCfg<MN>::Smem& sh, uint32_t t
             }
         } else if (p.c_tma) {
             const TileCoord tc = tile_coord(p, itm.tile);
-            bool ok;
-            switch (p.epi.act) {
-                case kActRelu: ok = store_tile_tma<kActRelu, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                case kActSigmoid: ok = store_tile_tma<kActSigmoid, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                case kActSilu: ok = store_tile_tma<kActSilu, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                case kActGeluTanh: ok = store_tile_tma<kActGeluTanh, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                case kActGeluErf: ok = store_tile_tma<kActGeluErf, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-                default: ok = store_tile_tma<kActNone, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece); break;
-            }
+            const bool ok = p.c_tma == 2
+                ? store_tile_act<true, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece)
+                : store_tile_act<false, SmemT, NB>(sh, cmap, p, tc, taddr, quarter, lane, ew, c_loads, stores, first_piece);
             if (!ok) {
                 record_status(&g_wait_status, kWaitFull);
                 return;
@@ -661,20 +688,30 @@ bool make_kmajor_map(CUtensorMap* map, const float* base, int64_t K, int64_t row
 // without overlap (row stride >= N, batch stride >= one matrix), extents that
 // fit 32-bit coordinates; a 32 x 32 box, 128-byte swizzle.  False: C is
 // written by the threads directly.
-bool make_c_map(CUtensorMap* map, const Problem& pr) {
-    if (pr.csC != 1 && pr.N > 1) return false;
-    if (reinterpret_cast<uintptr_t>(pr.C) % 16 != 0) return false;
+// The C tensor map, 32x32 boxes: 1 when C has unit stride along N (inner
+// dimension N), 2 when it has unit stride along M (inner dimension M), 0 when
+// neither (or an extent, stride or alignment TMA cannot take).
+int make_c_map(CUtensorMap* map, const Problem& pr) {
+    const bool row_major = pr.csC == 1 || pr.N == 1;
+    const bool col_major = !row_major && (pr.rsC == 1 || pr.M == 1);
+    if (!row_major && !col_major) return 0;
+    if (reinterpret_cast<uintptr_t>(pr.C) % 16 != 0) return 0;
     const int64_t lim = (int64_t)1 << 31;
-    if (pr.N >= lim || pr.M >= lim || pr.batch >= lim) return false;
+    if (pr.N >= lim || pr.M >= lim || pr.batch >= lim) return 0;
+    // inner: the unit-stride extent; outer: the other one and its stride.
+    const int64_t inner = row_major ? pr.N : pr.M;
+    const int64_t outer = row_major ? pr.M : pr.N;
+    const int64_t so = row_major ? pr.rsC : pr.csC;
     auto ok_stride = [](int64_t st) { return st > 0 && (st * 4) % 16 == 0 && st * 4 < ((int64_t)1 << 40); };
-    const int64_t row_b = pr.M > 1 ? pr.rsC * 4 : ((pr.N * 4 + 15) / 16) * 16;
-    if (pr.M > 1 && (!ok_stride(pr.rsC) || pr.rsC < pr.N)) return false;
+    const int64_t outer_b = outer > 1 ? so * 4 : ((inner * 4 + 15) / 16) * 16;
+    if (outer > 1 && (!ok_stride(so) || so < inner)) return 0;
     const bool batched = pr.batch > 1;
-    if (batched && (!ok_stride(pr.bsC) || pr.bsC * 4 < row_b * pr.M)) return false;
-    const uint64_t dims[3] = {(uint64_t)pr.N, (uint64_t)pr.M, (uint64_t)pr.batch};
-    const uint64_t strides[2] = {(uint64_t)row_b, batched ? (uint64_t)pr.bsC * 4 : (uint64_t)row_b * pr.M};
+    if (batched && (!ok_stride(pr.bsC) || pr.bsC * 4 < outer_b * outer)) return 0;
+    const uint64_t dims[3] = {(uint64_t)inner, (uint64_t)outer, (uint64_t)pr.batch};
+    const uint64_t strides[2] = {(uint64_t)outer_b, batched ? (uint64_t)pr.bsC * 4 : (uint64_t)outer_b * outer};
     const uint32_t box[3] = {32, 32, 1};
-    return encode_tmap_f32_3d(map, pr.C, dims, strides, box, true);
+    if (!encode_tmap_f32_3d(map, pr.C, dims, strides, box, true)) return 0;
+    return row_major ? 1 : 2;
 }
 
 }  // namespace
@@ -716,7 +753,7 @@ cudaError_t launch_mn(const Problem& pr, const Plan& plan, cudaStream_t stream) 
     p.b_bcast = b_bc;
     CUtensorMap tcm;
     std::memset(&tcm, 0, sizeof(tcm));
-    p.c_tma = make_c_map(&tcm, pr) ? 1 : 0;
+    p.c_tma = make_c_map(&tcm, pr);
     const int64_t grid = plan.ctas;
     p.dp_tiles = plan.stream_k ? plan.dp_tiles : plan.tiles;
     p.sk_units = plan.stream_k ? (plan.tiles - plan.dp_tiles) * p.nk : 0;
