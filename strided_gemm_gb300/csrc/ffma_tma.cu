@@ -139,7 +139,8 @@ struct Cfg {
 //    distinct swizzled chunks per quarter-warp and its 4-byte stores 32
 //    consecutive columns: no bank conflicts, more instructions;
 //  - quads (128 rows): task = a 4-row x 4-k block, four 16-byte loads and
-//    four 16-byte stores: fewer instructions, some load conflicts.
+//    four 16-byte stores: fewer instructions, lanes placed so that neither
+//    the loads nor the stores conflict.
 template <int R>
 __device__ __forceinline__ void transpose_rows(const float* raw, float* dst) {
     static_assert(R % 32 == 0, "a warp covers 32 rows of one chunk");
@@ -156,12 +157,19 @@ __device__ __forceinline__ void transpose_rows(const float* raw, float* dst) {
     }
 }
 
+// Quads: a quarter-warp's 8 lanes (task bits 0..2 = x, y, z) take row quads
+// nq = (x, y, z, ..) and k chunks c = (y ^ t3, z ^ t4, t5) (t = task bits): the
+// loads read chunk c ^ (row & 7), bits (y, z, x) up to a constant, and the
+// stores write chunk nq & 7 of rows R floats apart: 8 distinct chunks each.
 template <int R>
 __device__ __forceinline__ void transpose_quads(const float* raw, float* dst) {
     constexpr int kQuads = R / 4;
+    static_assert(BK / 4 == 8 && kQuads % 8 == 0 && R % 32 == 0, "8 chunks; whole quarter-warps");
 #pragma unroll
     for (int task = threadIdx.x; task < kQuads * (BK / 4); task += kThreads) {
-        const int nq = task % kQuads, c = task / kQuads;
+        const int nq = (task & 7) | ((task >> 6) << 3);
+        const int c = (((task >> 1) ^ (task >> 3)) & 1) | ((((task >> 2) ^ (task >> 4)) & 1) << 1) |
+                      (((task >> 5) & 1) << 2);
         float4 v[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -459,9 +467,12 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
         }
 
         int kt_end;
+        bool busy;          // this warp's 64 x 64 block holds outputs of the tile
         {
             const Item itm = sc.item(w, p.nk);
             kt_end = itm.ke - itm.kb;
+            const TileCoord t0 = tile_coord<BM, BN>(p, itm.tile);
+            busy = t0.m0 + wm < p.M && t0.n0 + wn < p.N;
         }
         for (int kt = 0; kt < kt_end; ++kt, ++it) {
             if (issuer && (int64_t)is.issued < is.total) {
@@ -490,7 +501,10 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                     return;
                 }
             }
-            {
+            // A warp whose block lies wholly past a ragged edge (N = 64 in a
+            // 128-wide tile, say) skips the FMAs; it still takes its part in
+            // the transposes and the stage barriers.
+            if (busy) {
                 // One k ahead: the next k's fragments (24 registers, 16-byte
                 // loads of 4 adjacent rows of A and columns of B) load while
                 // this k's 64 packed FMAs run.  Deeper unrolling spills.

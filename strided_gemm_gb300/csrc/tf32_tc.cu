@@ -124,9 +124,23 @@ struct Params {
 
 
 // Instruction descriptor, kind::tf32: D fp32, A and B tf32, both K-major,
-// N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) |
-                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// N >> 3 at bit 17, M >> 4 at bit 24.  N is set per tile (idesc_for).
+constexpr uint32_t kIdescNoN = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BM >> 4) << 24);
+
+// The MMA width for a tile whose first column is n0: BN, or at a ragged N
+// edge the valid columns rounded up to the 16 an M = 128 MMA takes.  The
+// accumulator columns past it keep stale values that no store reads.
+__device__ __forceinline__ uint32_t idesc_for(int64_t N, int64_t n0) {
+    const int64_t nv = N - n0;
+    const uint32_t nn = nv >= BN ? (uint32_t)BN : (uint32_t)((nv + 15) & ~(int64_t)15);
+    return kIdescNoN | ((nn >> 3) << 17);
+}
+
+// Raw 32-row boxes of an MN-major tile that hold valid rows (ext of them).
+template <int ROWS>
+__device__ __forceinline__ int valid_boxes(int64_t ext) {
+    return ext >= ROWS ? ROWS / 32 : (int)((ext + 31) / 32);
+}
 
 struct TileCoord { int64_t b, m0, n0; };
 
@@ -165,12 +179,14 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&sh.rfull[r], C::kRawBytes);
+                // Boxes wholly past a ragged edge are not fetched.
+                const int boxes = valid_boxes<C::kRawRows>(C::kTA ? p.M - tc.m0 : p.N - tc.n0);
+                mbar_arrive_expect_tx(&sh.rfull[r], (uint32_t)boxes * kBox * 4);
                 const CUtensorMap* tm = C::kTA ? ta : tb;
                 const int x0 = C::kTA ? (int)tc.m0 : (int)tc.n0;
                 const int bz = C::kTA ? ba : bb;
 #pragma unroll 1
-                for (int j = 0; j < C::kRawRows / 32; ++j)
+                for (int j = 0; j < boxes; ++j)
                     tma_load_3d(sh.raw[r] + j * kBox, tm, &sh.rfull[r], x0 + 32 * j, kt * BK, bz);
             }
             const int st = (int)(i % S);
@@ -202,16 +218,23 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
 // Rewrites the raw boxes of one MN-major slice (rows along K, 128-byte
 // swizzle) into the K-major swizzled layout of the MMA operand (row m = 32 k
 // values, 16-byte chunk c at chunk c ^ (m & 7)), in 4 x 4 quads: four 16-byte
-// loads of 4 rows of K, four 16-byte stores of 4 rows of M.  The quads of a
-// quarter-warp span 2 groups of 4 rows and 4 groups of 4 k, so the stores hit
-// 8 distinct chunks (no bank conflict) and the loads two ways at most.
+// loads of 4 rows of K, four 16-byte stores of 4 rows of M.  A 16-byte access
+// is served a quarter-warp at a time, and the 8 lanes of a quarter take quads
+// (mq, kq) with q bits 0..2 = (a, b, c) as mq = (a, b, ..), kq = (c, a^b^d, ..)
+// (d = q bit 3): a load reads chunk (mq & 7) ^ (k & 7), whose bits are (a, b,
+// mq2 ^ c) up to a constant, and a store writes chunk kq ^ (m & 7), bits (c,
+// a^b^d, kq2 ^ a): 8 distinct chunks either way, so neither conflicts.
+// Only the first `boxes` boxes are rewritten (the rows past a ragged edge
+// are never multiplied into a stored output).
 template <int ROWS>
-__device__ __forceinline__ void transpose_mn_slice(const float* raw, float* dst, int t) {
-    constexpr int kQuads = (ROWS / 4) * (BK / 4);
+__device__ __forceinline__ void transpose_mn_slice(const float* raw, float* dst, int t, int boxes) {
+    static_assert(BK / 4 == 8 && ROWS % 32 == 0, "8 k groups; whole 32-row boxes");
+    const int quads = boxes * 64;     // 32 rows x 32 k per box, in 4 x 4 quads
 #pragma unroll 1
-    for (int q = t; q < kQuads; q += kTransWarps * 32) {
-        const int kq = (q & 3) | (((q >> 5) & 1) << 2);         // 4-k group, 0..7
-        const int mq = ((q >> 6) << 3) | ((q >> 2) & 7);         // 4-row group
+    for (int q = t; q < quads; q += kTransWarps * 32) {
+        const int kq = ((q >> 2) & 1) | (((q ^ (q >> 1) ^ (q >> 3)) & 1) << 1) |
+                       (((q >> 4) & 1) << 2);                    // 4-k group, 0..7
+        const int mq = (q & 3) | ((q >> 5) << 2);                // 4-row group
         const float* box = raw + (mq >> 3) * kBox;
         const int mc = mq & 7;                                    // chunk of the box row
         float4 v[4];
@@ -245,6 +268,8 @@ __device__ __forceinline__ void transposer(typename TCfg<MN>::Smem& sh, const Pa
     const int64_t n_items = sh.sched.n_items;
     for (int64_t w = 0; w < n_items; ++w) {
         const Item itm = sh.sched.item(w, p.nk);
+        const TileCoord tc = tile_coord(p, itm.tile);
+        const int boxes = valid_boxes<C::kRawRows>(C::kTA ? p.M - tc.m0 : p.N - tc.n0);
         for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
             const int r = (int)(i % R), st = (int)(i % S);
             if (!mbar_wait(&sh.rfull[r], (uint32_t)((i / R) & 1))) {
@@ -255,7 +280,7 @@ __device__ __forceinline__ void transposer(typename TCfg<MN>::Smem& sh, const Pa
                 record_status(&g_wait_status, kWaitEmpty);
                 return;
             }
-            transpose_mn_slice<C::kRawRows>(sh.raw[r], C::kTA ? sh.a[st] : sh.b[st], t);
+            transpose_mn_slice<C::kRawRows>(sh.raw[r], C::kTA ? sh.a[st] : sh.b[st], t, boxes);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -283,6 +308,7 @@ __device__ __forceinline__ void mma_issuer(typename TCfg<MN>::Smem& sh, uint32_t
         }
         tc_fence_after();
         const uint32_t d = tmem + buf * kAccCols;
+        const uint32_t idesc = idesc_for(p.N, tile_coord(p, itm.tile).n0);
         for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
             const int st = (int)(i % S);
             const uint32_t ph = (uint32_t)((i / S) & 1);
@@ -299,7 +325,7 @@ __device__ __forceinline__ void mma_issuer(typename TCfg<MN>::Smem& sh, uint32_t
                 const uint64_t ad = umma_desc_kmajor_sw128(a0 + kk * kMmaK * 4);
                 const uint64_t bd = umma_desc_kmajor_sw128(b0 + kk * kMmaK * 4);
                 const bool acc = kt > itm.kb || kk > 0;
-                mma_tf32(d, ad, bd, kIdesc, acc ? 1u : 0u);
+                mma_tf32(d, ad, bd, idesc, acc ? 1u : 0u);
             }
             mma_commit(&sh.empty[st]);
         }
