@@ -42,6 +42,10 @@
 #include "ptx.cuh"
 #include "schedule.cuh"
 
+#ifndef SBGEMM_EPI_GROUP
+#define SBGEMM_EPI_GROUP 4
+#endif
+
 #ifndef SBGEMM_FFMA2
 #define SBGEMM_FFMA2 1
 #endif
@@ -638,69 +642,74 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 }
                 relu = p.epi.act == kActRelu;
             }
-#pragma unroll
-            for (int i = 0; i < TM; ++i) {
+            const int64_t n0c = tc.n0 + wn;
+            auto ncol = [&](int j) { return n0c + col_of(0, ln, j); };
+            // Both runs of 4 wholly inside a row-major, 16-byte aligned C: float4.
+            const bool vec = p.c_vec4 && ncol(TN - 1) < p.N;
+            auto put = [&](int i, float (&r)[TN]) {
                 const int64_t m = tc.m0 + row_of(wm, lm, i);
-                if (m >= p.M) continue;
                 float* crow = Cb + m * p.rsC;
-                if (p.c_vec4) {
-#pragma unroll
-                    for (int h = 0; h < TN / 4; ++h) {
-                        const int64_t n = tc.n0 + col_of(wn, ln, 4 * h);
-                        if (n + 3 < p.N) {
-                            float4* cp = reinterpret_cast<float4*>(crow + n);
-                            float4 v;
-                            if (p.accumulate) {
-                                const float4 o = *cp;
-                                v.x = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 0), o.x);
-                                v.y = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 1), o.y);
-                                v.z = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 2), o.z);
-                                v.w = fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + 3), o.w);
-                            } else {
-                                v.x = p.alpha * acc_at<PI>(acc, i, 4 * h + 0);
-                                v.y = p.alpha * acc_at<PI>(acc, i, 4 * h + 1);
-                                v.z = p.alpha * acc_at<PI>(acc, i, 4 * h + 2);
-                                v.w = p.alpha * acc_at<PI>(acc, i, 4 * h + 3);
-                            }
-                            if constexpr (F) {
-                                v.x += bias[4 * h + 0]; v.y += bias[4 * h + 1];
-                                v.z += bias[4 * h + 2]; v.w += bias[4 * h + 3];
-                                if (relu) {
-                                    v.x = fmaxf(v.x, 0.0f); v.y = fmaxf(v.y, 0.0f);
-                                    v.z = fmaxf(v.z, 0.0f); v.w = fmaxf(v.w, 0.0f);
-                                }
-                            }
-                            *cp = v;
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                if (n + e < p.N) {
-                                    float* c = crow + (n + e);
-                                    float r = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, 4 * h + e), *c)
-                                                           : p.alpha * acc_at<PI>(acc, i, 4 * h + e);
-                                    if constexpr (F) {
-                                        r += bias[4 * h + e];
-                                        if (relu) r = fmaxf(r, 0.0f);
-                                    }
-                                    *c = r;
-                                }
-                            }
-                        }
-                    }
-                } else {
+                if constexpr (F) {
 #pragma unroll
                     for (int j = 0; j < TN; ++j) {
-                        const int64_t n = tc.n0 + col_of(wn, ln, j);
-                        if (n >= p.N) continue;
-                        float* c = crow + n * p.csC;
-                        float r = p.accumulate ? fmaf(p.alpha, acc_at<PI>(acc, i, j), *c)
-                                               : p.alpha * acc_at<PI>(acc, i, j);
-                        if constexpr (F) {
-                            r += bias[j];
-                            if (relu) r = fmaxf(r, 0.0f);
-                        }
-                        *c = r;
+                        r[j] += bias[j];
+                        if (relu) r[j] = fmaxf(r[j], 0.0f);
                     }
+                }
+                if (vec) {
+#pragma unroll
+                    for (int h = 0; h < TN / 4; ++h)
+                        *reinterpret_cast<float4*>(crow + ncol(4 * h)) =
+                            make_float4(r[4 * h], r[4 * h + 1], r[4 * h + 2], r[4 * h + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < TN; ++j)
+                        if (ncol(j) < p.N) crow[ncol(j) * p.csC] = r[j];
+                }
+            };
+            if (p.accumulate) {
+                // C_old of G rows is loaded before any of them is stored, so the
+                // loads are in flight together (the compiler cannot move a load
+                // of C above a store to C).
+                constexpr int G = SBGEMM_EPI_GROUP;
+#pragma unroll
+                for (int i0 = 0; i0 < TM; i0 += G) {
+                    float old[G][TN];
+#pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        const int64_t m = tc.m0 + row_of(wm, lm, i0 + i);
+                        const float* crow = Cb + (m < p.M ? m : 0) * p.rsC;
+                        if (vec) {
+#pragma unroll
+                            for (int h = 0; h < TN / 4; ++h) {
+                                const float4 o = m < p.M ? *reinterpret_cast<const float4*>(crow + ncol(4 * h))
+                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                                old[i][4 * h] = o.x; old[i][4 * h + 1] = o.y;
+                                old[i][4 * h + 2] = o.z; old[i][4 * h + 3] = o.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < TN; ++j)
+                                old[i][j] = (m < p.M && ncol(j) < p.N) ? crow[ncol(j) * p.csC] : 0.0f;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        if (tc.m0 + row_of(wm, lm, i0 + i) >= p.M) continue;
+                        float r[TN];
+#pragma unroll
+                        for (int j = 0; j < TN; ++j) r[j] = fmaf(p.alpha, acc_at<PI>(acc, i0 + i, j), old[i][j]);
+                        put(i0 + i, r);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    if (tc.m0 + row_of(wm, lm, i) >= p.M) continue;
+                    float r[TN];
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) r[j] = p.alpha * acc_at<PI>(acc, i, j);
+                    put(i, r);
                 }
             }
         };
