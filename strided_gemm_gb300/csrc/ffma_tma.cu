@@ -137,36 +137,17 @@ struct Cfg {
 };
 
 // Transposes one K-major operand slice ([R rows][32 k], 128-byte swizzle) into
-// [32 k][R].  Two task shapes, chosen by slice height (transpose_slice):
-//  - rows (256 rows): task = one row's 16-byte chunk of 4 k values; a warp
-//    takes 32 consecutive rows of one chunk, so its 16-byte loads hit 8
-//    distinct swizzled chunks per quarter-warp and its 4-byte stores 32
-//    consecutive columns: no bank conflicts, more instructions;
-//  - quads (128 rows): task = a 4-row x 4-k block, four 16-byte loads and
-//    four 16-byte stores: fewer instructions, lanes placed so that neither
-//    the loads nor the stores conflict.
+// [32 k][R] in 4-row x 4-k quads: four 16-byte loads and four 16-byte stores
+// per task.  A 16-byte access is served a quarter-warp at a time; its 8 lanes
+// (task bits 0..2 = x, y, z) take row quads nq = (x, y, z, ..) and k chunks
+// c = (y ^ t3, z ^ t4, t5) (t = task bits), so the loads read chunk
+// c ^ (row & 7), bits (y, z, x) up to a constant, and the stores write chunk
+// nq & 7 of rows R floats apart: 8 distinct chunks either way, no bank
+// conflict.  (A row-per-lane form with 4-byte stores, once used for 256-row
+// slices, issued 2.5x the instructions and ran 2-4% slower on products with
+// both operands K-major.)
 template <int R>
-__device__ __forceinline__ void transpose_rows(const float* raw, float* dst) {
-    static_assert(R % 32 == 0, "a warp covers 32 rows of one chunk");
-#pragma unroll 2
-    for (int task = threadIdx.x; task < R * (BK / 4); task += kThreads) {
-        const int row = task % R, c = task / R;
-        const float4 v = *reinterpret_cast<const float4*>(
-            reinterpret_cast<const char*>(raw) + row * 128 + (((c ^ (row & 7)) & 7) << 4));
-        float* d = dst + (4 * c) * R + row;
-        d[0] = v.x;
-        d[R] = v.y;
-        d[2 * R] = v.z;
-        d[3 * R] = v.w;
-    }
-}
-
-// Quads: a quarter-warp's 8 lanes (task bits 0..2 = x, y, z) take row quads
-// nq = (x, y, z, ..) and k chunks c = (y ^ t3, z ^ t4, t5) (t = task bits): the
-// loads read chunk c ^ (row & 7), bits (y, z, x) up to a constant, and the
-// stores write chunk nq & 7 of rows R floats apart: 8 distinct chunks each.
-template <int R>
-__device__ __forceinline__ void transpose_quads(const float* raw, float* dst) {
+__device__ __forceinline__ void transpose_slice(const float* raw, float* dst) {
     constexpr int kQuads = R / 4;
     static_assert(BK / 4 == 8 && kQuads % 8 == 0 && R % 32 == 0, "8 chunks; whole quarter-warps");
 #pragma unroll
@@ -187,13 +168,6 @@ __device__ __forceinline__ void transpose_quads(const float* raw, float* dst) {
         *reinterpret_cast<float4*>(d + 2 * R) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
         *reinterpret_cast<float4*>(d + 3 * R) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
     }
-}
-
-// The task shape by slice height: row tasks for 256 rows, quads for 128.
-template <int R>
-__device__ __forceinline__ void transpose_slice(const float* raw, float* dst) {
-    if constexpr (R >= 256) transpose_rows<R>(raw, dst);
-    else transpose_quads<R>(raw, dst);
 }
 
 struct TileCoord { int64_t b, m0, n0; };
