@@ -63,32 +63,41 @@ constexpr int kBox = 32 * 32;                // floats in one 32 x 32 raw box of
 // 1 A MN-major (unit stride along M); 2 B MN-major (along N).  An MN-major
 // slice lands as raw 32 x 32 boxes (rows along K, 128-byte swizzle) in a ring
 // of its own, and the transposer warps rewrite it into the K-major swizzled
-// layout the MMAs read.
+// layout the MMAs read, in a ring of kTStages stages; the operand TMA brings
+// in K-major has a ring of kStages stages.  The load latency is what the
+// stages cover (each waits out about 1.1-1.3 us of it), so the TMA-fed rings
+// get the depth and the transposed ring, filled from shared memory, two
+// stages (3 transposed stages with 2 raw ones measured 11% slower).
 template <int MN>
 struct TCfg {
     static constexpr bool kTA = MN == 1, kTB = MN == 2;
-    static constexpr int kWarps = 2 + kEpiWarps + (MN ? kTransWarps : 0);
+    static constexpr bool kTrans = kTA || kTB;
+    static constexpr int kWarps = 2 + kEpiWarps + (kTrans ? kTransWarps : 0);
     static constexpr int kThreads = kWarps * 32;
-    static constexpr int kStages = MN ? 3 : 4;          // K-major stages (MMA operands)
+    static constexpr int kStages = 4;                      // TMA-fed K-major ring
+    static constexpr int kTStages = kTrans ? 2 : 1;        // transposed ring
+    static constexpr int kStagesA = kTA ? kTStages : kStages;
+    static constexpr int kStagesB = kTB ? kTStages : kStages;
     static constexpr int kRawRows = kTA ? BM : (kTB ? BN : 0);
     static constexpr int kRawStages = kTA ? 3 : (kTB ? 2 : 0);
-    static constexpr int kStageBufs = kTB ? 1 : 2;       // epilogue staging tiles per warp
+    static constexpr int kStageBufs = kTrans ? 1 : 2;     // epilogue staging tiles per warp
     // Bytes the K-major operand copies bring into a stage.
     static constexpr uint32_t kKBytes = (kTA ? 0 : kABytes) + (kTB ? 0 : kBBytes);
     static constexpr uint32_t kRawBytes = kRawRows * BK * 4;
     static constexpr int kRawSlots = kRawStages > 0 ? kRawStages : 1;
     static constexpr int kRawFloats = kRawRows > 0 ? kRawRows * BK : 4;
     struct Smem {
-        float a[kStages][BM * BK];
-        float b[kStages][BN * BK];
+        float a[kStagesA][BM * BK];
+        float b[kStagesB][BN * BK];
         // Per epilogue warp: pieces of C (alternating by store when there are
         // two) in the 128-byte swizzled layout of its tensor map (16-byte chunk
         // q of row r at chunk q ^ (r & 7)).
         alignas(1024) float stage[kEpiWarps][kStageBufs][32 * 32];
         alignas(1024) float raw[kRawSlots][kRawFloats];
-        uint64_t full[kStages];
-        uint64_t empty[kStages];
-        uint64_t tdone[kStages];      // the transposers wrote stage s's MN-major operand
+        uint64_t full[kStages];       // the K-major operand of stage s landed
+        uint64_t empty[kStages];      // the MMAs that read it are done
+        uint64_t tdone[kTStages];     // the transposers wrote transposed stage t
+        uint64_t tempty[kTStages];    // the MMAs that read it are done
         uint64_t rfull[kRawSlots];
         uint64_t rempty[kRawSlots];
         uint64_t acc_full[2];
@@ -170,7 +179,7 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
         const int ba = p.a_bcast ? 0 : (int)tc.b;
         const int bb = p.b_bcast ? 0 : (int)tc.b;
         for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
-            if constexpr (MN != 0) {
+            if constexpr (C::kTrans) {
                 // The MN-major operand: 32 x 32 boxes along M (A) or N (B), rows
                 // along K, into the raw ring.
                 const int r = (int)(i % R);
@@ -206,7 +215,7 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
             record_status(&g_wait_status, kWaitDrain);
             return;
         }
-    if constexpr (MN != 0) {
+    if constexpr (C::kTrans) {
         for (uint64_t q = i > (uint64_t)R ? i - R : 0; q < i; ++q)
             if (!mbar_wait(&sh.rfull[q % R], (uint32_t)((q / R) & 1))) {
                 record_status(&g_wait_status, kWaitDrain);
@@ -226,32 +235,43 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
 // a^b^d, kq2 ^ a): 8 distinct chunks either way, so neither conflicts.
 // Only the first `boxes` boxes are rewritten (the rows past a ragged edge
 // are never multiplied into a stored output).
+// One 4 x 4 quad q of transpose_mn_slice.
+__device__ __forceinline__ void transpose_quad(const float* raw, float* dst, int q) {
+    const int kq = ((q >> 2) & 1) | (((q ^ (q >> 1) ^ (q >> 3)) & 1) << 1) |
+                   (((q >> 4) & 1) << 2);                    // 4-k group, 0..7
+    const int mq = (q & 3) | ((q >> 5) << 2);                // 4-row group
+    const float* box = raw + (mq >> 3) * kBox;
+    const int mc = mq & 7;                                    // chunk of the box row
+    float4 v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int k = 4 * kq + r;
+        v[r] = *reinterpret_cast<const float4*>(box + k * 32 + ((mc ^ (k & 7)) << 2));
+    }
+    const int m = 4 * mq;
+    *reinterpret_cast<float4*>(dst + (m + 0) * 32 + ((kq ^ ((m + 0) & 7)) << 2)) =
+        make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
+    *reinterpret_cast<float4*>(dst + (m + 1) * 32 + ((kq ^ ((m + 1) & 7)) << 2)) =
+        make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
+    *reinterpret_cast<float4*>(dst + (m + 2) * 32 + ((kq ^ ((m + 2) & 7)) << 2)) =
+        make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
+    *reinterpret_cast<float4*>(dst + (m + 3) * 32 + ((kq ^ ((m + 3) & 7)) << 2)) =
+        make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+}
+
 template <int ROWS>
 __device__ __forceinline__ void transpose_mn_slice(const float* raw, float* dst, int t, int boxes) {
     static_assert(BK / 4 == 8 && ROWS % 32 == 0, "8 k groups; whole 32-row boxes");
-    const int quads = boxes * 64;     // 32 rows x 32 k per box, in 4 x 4 quads
-#pragma unroll 1
-    for (int q = t; q < quads; q += kTransWarps * 32) {
-        const int kq = ((q >> 2) & 1) | (((q ^ (q >> 1) ^ (q >> 3)) & 1) << 1) |
-                       (((q >> 4) & 1) << 2);                    // 4-k group, 0..7
-        const int mq = (q & 3) | ((q >> 5) << 2);                // 4-row group
-        const float* box = raw + (mq >> 3) * kBox;
-        const int mc = mq & 7;                                    // chunk of the box row
-        float4 v[4];
+    constexpr int kStep = kTransWarps * 32;
+    if (boxes == ROWS / 32) {
+        // Every box: a fixed trip count, unrolled so that all of a thread's
+        // loads are in flight together.
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int k = 4 * kq + r;
-            v[r] = *reinterpret_cast<const float4*>(box + k * 32 + ((mc ^ (k & 7)) << 2));
-        }
-        const int m = 4 * mq;
-        *reinterpret_cast<float4*>(dst + (m + 0) * 32 + ((kq ^ ((m + 0) & 7)) << 2)) =
-            make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
-        *reinterpret_cast<float4*>(dst + (m + 1) * 32 + ((kq ^ ((m + 1) & 7)) << 2)) =
-            make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
-        *reinterpret_cast<float4*>(dst + (m + 2) * 32 + ((kq ^ ((m + 2) & 7)) << 2)) =
-            make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
-        *reinterpret_cast<float4*>(dst + (m + 3) * 32 + ((kq ^ ((m + 3) & 7)) << 2)) =
-            make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+        for (int q = t; q < ROWS * 2; q += kStep) transpose_quad(raw, dst, q);
+    } else {
+        const int quads = boxes * 64;     // 32 rows x 32 k per box, in 4 x 4 quads
+#pragma unroll 1
+        for (int q = t; q < quads; q += kStep) transpose_quad(raw, dst, q);
     }
 }
 
@@ -263,7 +283,7 @@ template <int MN>
 __device__ __forceinline__ void transposer(typename TCfg<MN>::Smem& sh, const Params& p, int t,
                                            int lane) {
     using C = TCfg<MN>;
-    constexpr int S = C::kStages, R = C::kRawSlots;
+    constexpr int T = C::kTStages, R = C::kRawSlots;
     uint64_t i = 0;
     const int64_t n_items = sh.sched.n_items;
     for (int64_t w = 0; w < n_items; ++w) {
@@ -271,20 +291,20 @@ __device__ __forceinline__ void transposer(typename TCfg<MN>::Smem& sh, const Pa
         const TileCoord tc = tile_coord(p, itm.tile);
         const int boxes = valid_boxes<C::kRawRows>(C::kTA ? p.M - tc.m0 : p.N - tc.n0);
         for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
-            const int r = (int)(i % R), st = (int)(i % S);
+            const int r = (int)(i % R), ts = (int)(i % T);
             if (!mbar_wait(&sh.rfull[r], (uint32_t)((i / R) & 1))) {
                 record_status(&g_wait_status, kWaitFull);
                 return;
             }
-            if (i >= (uint64_t)S && !mbar_wait(&sh.empty[st], (uint32_t)(((i / S) - 1) & 1))) {
+            if (i >= (uint64_t)T && !mbar_wait(&sh.tempty[ts], (uint32_t)(((i / T) - 1) & 1))) {
                 record_status(&g_wait_status, kWaitEmpty);
                 return;
             }
-            transpose_mn_slice<C::kRawRows>(sh.raw[r], C::kTA ? sh.a[st] : sh.b[st], t, boxes);
+            transpose_mn_slice<C::kRawRows>(sh.raw[r], C::kTA ? sh.a[ts] : sh.b[ts], t, boxes);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&sh.tdone[st]);
+                mbar_arrive(&sh.tdone[ts]);
                 mbar_arrive(&sh.rempty[r]);
             }
         }
@@ -310,16 +330,16 @@ __device__ __forceinline__ void mma_issuer(typename TCfg<MN>::Smem& sh, uint32_t
         const uint32_t d = tmem + buf * kAccCols;
         const uint32_t idesc = idesc_for(p.N, tile_coord(p, itm.tile).n0);
         for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
-            const int st = (int)(i % S);
-            const uint32_t ph = (uint32_t)((i / S) & 1);
-            if (!mbar_wait(&sh.full[st], ph) || (MN != 0 && !mbar_wait(&sh.tdone[st], ph))) {
+            const int st = (int)(i % S), ts = (int)(i % C::kTStages);
+            if (!mbar_wait(&sh.full[st], (uint32_t)((i / S) & 1)) ||
+                (C::kTrans && !mbar_wait(&sh.tdone[ts], (uint32_t)((i / C::kTStages) & 1)))) {
                 record_status(&g_wait_status, kWaitFull);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sh.a[st]);
-            const uint32_t b0 = smem_u32(sh.b[st]);
+            const uint32_t a0 = smem_u32(sh.a[C::kTA ? ts : st]);
+            const uint32_t b0 = smem_u32(sh.b[C::kTB ? ts : st]);
 #pragma unroll
             for (int kk = 0; kk < BK / kMmaK; ++kk) {
                 const uint64_t ad = umma_desc_kmajor_sw128(a0 + kk * kMmaK * 4);
@@ -328,6 +348,7 @@ __device__ __forceinline__ void mma_issuer(typename TCfg<MN>::Smem& sh, uint32_t
                 mma_tf32(d, ad, bd, idesc, acc ? 1u : 0u);
             }
             mma_commit(&sh.empty[st]);
+            if constexpr (C::kTrans) mma_commit(&sh.tempty[ts]);
         }
         if (!ok) break;
         mma_commit(&sh.acc_full[buf]);
@@ -636,7 +657,10 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], 1);
+        }
+        for (int s = 0; s < C::kTStages; ++s) {
             mbar_init(&sh.tdone[s], kTransWarps);
+            mbar_init(&sh.tempty[s], 1);
         }
         for (int r = 0; r < C::kRawSlots; ++r) {
             mbar_init(&sh.rfull[r], 1);
@@ -672,7 +696,7 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         epilogue<MN>(sh, tmem, &tcm, p, warp, lane);
         // Shared memory must outlive the bulk stores that read it.
         if (lane == 0) bulk_wait_all();
-    } else if constexpr (MN != 0) {
+    } else if constexpr (C::kTrans) {
         transposer<MN>(sh, p, threadIdx.x - (2 + kEpiWarps) * 32, lane);
     }
 
