@@ -146,28 +146,55 @@ struct Cfg {
 // conflict.  (A row-per-lane form with 4-byte stores, once used for 256-row
 // slices, issued 2.5x the instructions and ran 2-4% slower on products with
 // both operands K-major.)
+// Quad task -> (row quad nq, k chunk c), see above.
+__device__ __forceinline__ int quad_row(int task) { return (task & 7) | ((task >> 6) << 3); }
+__device__ __forceinline__ int quad_chunk(int task) {
+    return (((task >> 1) ^ (task >> 3)) & 1) | ((((task >> 2) ^ (task >> 4)) & 1) << 1) |
+           (((task >> 5) & 1) << 2);
+}
+
 template <int R>
-__device__ __forceinline__ void transpose_slice(const float* raw, float* dst) {
-    constexpr int kQuads = R / 4;
-    static_assert(BK / 4 == 8 && kQuads % 8 == 0 && R % 32 == 0, "8 chunks; whole quarter-warps");
+__device__ __forceinline__ void quad_load(const float* raw, int task, float4 (&v)[4]) {
+    const int nq = quad_row(task), c = quad_chunk(task);
 #pragma unroll
-    for (int task = threadIdx.x; task < kQuads * (BK / 4); task += kThreads) {
-        const int nq = (task & 7) | ((task >> 6) << 3);
-        const int c = (((task >> 1) ^ (task >> 3)) & 1) | ((((task >> 2) ^ (task >> 4)) & 1) << 1) |
-                      (((task >> 5) & 1) << 2);
-        float4 v[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int row = 4 * nq + r;
-            v[r] = *reinterpret_cast<const float4*>(reinterpret_cast<const char*>(raw) + row * 128 +
-                                                    (((c ^ (row & 7)) & 7) << 4));
-        }
-        float* d = dst + (4 * c) * R + 4 * nq;
-        *reinterpret_cast<float4*>(d) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
-        *reinterpret_cast<float4*>(d + R) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
-        *reinterpret_cast<float4*>(d + 2 * R) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
-        *reinterpret_cast<float4*>(d + 3 * R) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+    for (int r = 0; r < 4; ++r) {
+        const int row = 4 * nq + r;
+        v[r] = *reinterpret_cast<const float4*>(reinterpret_cast<const char*>(raw) + row * 128 +
+                                                (((c ^ (row & 7)) & 7) << 4));
     }
+}
+
+template <int R>
+__device__ __forceinline__ void quad_store(float* dst, int task, const float4 (&v)[4]) {
+    const int nq = quad_row(task), c = quad_chunk(task);
+    float* d = dst + (4 * c) * R + 4 * nq;
+    *reinterpret_cast<float4*>(d) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
+    *reinterpret_cast<float4*>(d + R) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
+    *reinterpret_cast<float4*>(d + 2 * R) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
+    *reinterpret_cast<float4*>(d + 3 * R) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+}
+
+// Transposes the K-major slices of A (RA rows) and B (RB rows; 0 = not
+// transposed).  Every load of the thread's tasks is issued before any store:
+// the compiler cannot move a load of one buffer above a store to another, and
+// the transposes sit on every warp's path between two slices.
+template <int RA, int RB>
+__device__ __forceinline__ void transpose_slices(const float* rawA, float* dstA, const float* rawB,
+                                                 float* dstB) {
+    static_assert(BK / 4 == 8 && RA % 32 == 0 && RB % 32 == 0, "8 chunks; whole quarter-warps");
+    constexpr int TA_ = RA / 4 * (BK / 4) / kThreads;     // tasks per thread
+    constexpr int TB_ = RB / 4 * (BK / 4) / kThreads;
+    static_assert(TA_ * kThreads == RA / 4 * (BK / 4) && TB_ * kThreads == RB / 4 * (BK / 4),
+                  "whole tasks per thread");
+    float4 va[TA_ > 0 ? TA_ : 1][4], vb[TB_ > 0 ? TB_ : 1][4];
+#pragma unroll
+    for (int j = 0; j < TA_; ++j) quad_load<RA>(rawA, threadIdx.x + j * kThreads, va[j]);
+#pragma unroll
+    for (int j = 0; j < TB_; ++j) quad_load<RB>(rawB, threadIdx.x + j * kThreads, vb[j]);
+#pragma unroll
+    for (int j = 0; j < TA_; ++j) quad_store<RA>(dstA, threadIdx.x + j * kThreads, va[j]);
+#pragma unroll
+    for (int j = 0; j < TB_; ++j) quad_store<RB>(dstB, threadIdx.x + j * kThreads, vb[j]);
 }
 
 struct TileCoord { int64_t b, m0, n0; };
@@ -411,8 +438,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 if (issuer) drain<S>(sh.full, 0, is.issued);
                 return;
             }
-            if constexpr (TA) transpose_slice<BM>(sh.a[0], sh.at);
-            if constexpr (TB) transpose_slice<BN>(sh.b[0], sh.bt);
+            transpose_slices<TA ? BM : 0, TB ? BN : 0>(sh.a[0], sh.at, sh.b[0], sh.bt);
             if constexpr (RAW_EARLY) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.empty[0]);
@@ -537,8 +563,8 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                         if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, nx), is.issued);
                         return;
                     }
-                    if constexpr (TA) transpose_slice<BM>(sh.a[stage], sh.at + nb * (BK * BM));
-                    if constexpr (TB) transpose_slice<BN>(sh.b[stage], sh.bt + nb * (BK * BN));
+                    transpose_slices<TA ? BM : 0, TB ? BN : 0>(sh.a[stage], sh.at + nb * (BK * BM),
+                                                               sh.b[stage], sh.bt + nb * (BK * BN));
                     if constexpr (RAW_EARLY) {
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sh.empty[stage]);
