@@ -222,11 +222,12 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
     if (path == SBGEMM_PATH_TMA_TF32) {
         // A K-major A with an N-major B is computed as C^T = B^T A^T: the
         // MN-major operand to transpose in shared memory is then the 128-row
-        // one (B^T as A') instead of the 256-row one, at the price of the
-        // per-row epilogue stores (C^T has its unit stride along M').  Not
-        // worth it when N is below one tile row of the transposed problem.
+        // one (B^T as A') instead of the 256-row one, and C^T goes out
+        // through a tensor map with M' inner.  Below N = 128 the transposed
+        // problem fills only part of the 128-row MMA, which such a narrow,
+        // HBM-bound product can afford (c4, N = 64: 51 -> 45 us).
         const bool swap = plan->a_layout == SBGEMM_LAYOUT_K_MAJOR &&
-                          plan->b_layout != SBGEMM_LAYOUT_K_MAJOR && p.N >= 128;
+                          plan->b_layout != SBGEMM_LAYOUT_K_MAJOR;
         const Problem q = swap ? transposed_problem(p) : p;
         const TmaFfmaConfig c = tf32_tc_config();
         plan->transposed = swap;

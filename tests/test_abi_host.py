@@ -284,3 +284,18 @@ def test_tf32_takes_one_mn_major_operand():
     with pytest.raises(sg.SbgemmError) as e:
         call_plan(A_m, B_n, C, M, N, K, 1, math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
     assert e.value.status == sg.SBGEMM_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("N", [64, 768])
+def test_tf32_k_major_a_with_n_major_b_runs_transposed(N):
+    """K-major A with N-major B is planned as C^T = B^T A^T, whatever N: the
+    tile is reported in C's orientation, 256 rows by 128 columns, against
+    128 x 256 for the untransposed plan of A M-major with B K-major."""
+    M, K = 1024, 512
+    A_k, A_m = rowmajor(BASE, M, K, 1), (BASE, 1, M, 0)
+    B_k, B_n = (BASE + (1 << 32), 1, K, 0), rowmajor(BASE + (1 << 32), K, N, 1)
+    C = rowmajor(BASE + (2 << 32), M, N, 1)
+    p = call_plan(A_k, B_n, C, M, N, K, 1, math=sg.MATH_TF32)
+    assert p["path"] == sg.PATH_TMA_TF32 and (p["tile_m"], p["tile_n"]) == (256, 128), p
+    q = call_plan(A_m, B_k, C, M, N, K, 1, math=sg.MATH_TF32)
+    assert q["path"] == sg.PATH_TMA_TF32 and (q["tile_m"], q["tile_n"]) == (128, 256), q
