@@ -42,14 +42,6 @@
 #include "ptx.cuh"
 #include "schedule.cuh"
 
-#ifndef SBGEMM_EPI_GROUP
-#define SBGEMM_EPI_GROUP 4
-#endif
-
-#ifndef SBGEMM_FFMA2
-#define SBGEMM_FFMA2 1
-#endif
-
 namespace sbg {
 namespace {
 
@@ -235,7 +227,6 @@ __device__ __forceinline__ float& acc_at(float2 (&acc)[64], int i, int j) {
 // acc(i, j) += a[i] * b[j] for one k.
 template <bool PAIR_I>
 __device__ __forceinline__ void fma_step(float2 (&acc)[64], const float (&a)[TM], const float (&b)[TN]) {
-#if SBGEMM_FFMA2
     if (PAIR_I) {
 #pragma unroll
         for (int ip = 0; ip < TM / 2; ++ip) {
@@ -254,12 +245,6 @@ __device__ __forceinline__ void fma_step(float2 (&acc)[64], const float (&a)[TM]
                     __ffma2_rn(av, make_float2(b[2 * jp], b[2 * jp + 1]), acc[i * (TN / 2) + jp]);
         }
     }
-#else
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc_at<PAIR_I>(acc, i, j) = fmaf(a[i], b[j], acc_at<PAIR_I>(acc, i, j));
-#endif
 }
 
 template <int BM, int BN, bool A_K, bool B_K>
@@ -671,7 +656,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 // C_old of G rows is loaded before any of them is stored, so the
                 // loads are in flight together (the compiler cannot move a load
                 // of C above a store to C).
-                constexpr int G = SBGEMM_EPI_GROUP;
+                constexpr int G = 4;   // 2 ran slower, 8 spilled
 #pragma unroll
                 for (int i0 = 0; i0 < TM; i0 += G) {
                     float old[G][TN];
