@@ -102,19 +102,27 @@ struct Cfg {
     static constexpr int kABytes = BM * BK * 4, kBBytes = BN * BK * 4;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr bool kRawEarly = TA && TB;
-    static constexpr int kAtFloats = TA ? 2 * BK * BM : 4;
-    static constexpr int kBtFloats = TB ? 2 * BK * BN : 4;
+    // Transposed buffers: two (a slice is transposed while the previous one is
+    // computed) unless that leaves fewer than two raw stages, as with 512-row
+    // tiles; with one, the transpose waits for every warp to finish the slice.
+    static constexpr size_t kT1Bytes = (size_t)((TA ? BK * BM : 0) + (TB ? BK * BN : 0)) * 4;
+    static constexpr int kTBufs = (kSmemBudget - 2 * kT1Bytes) / kStageBytes >= 2 ? 2 : 1;
+    static constexpr int kAtFloats = TA ? kTBufs * BK * BM : 4;
+    static constexpr int kBtFloats = TB ? kTBufs * BK * BN : 4;
     static constexpr size_t kTBytes = (size_t)(kAtFloats + kBtFloats) * 4;
     static constexpr int kFit = (int)((kSmemBudget - kTBytes) / kStageBytes);
     static constexpr int kStages = kFit > 4 ? 4 : kFit;
     static_assert(kStages >= 2, "at least two raw stages");
+    // TMA boxes span at most 256 rows: a 512-row K-major A comes in two.
+    static constexpr int kABoxes = BM > 256 ? BM / 256 : 1;
+    static_assert(BM <= 256 || TA, "an MN-major A box spans at most 256 rows");
     // Slices issued ahead of the one being computed.
     static constexpr int kLookahead = kRawEarly ? kStages : kStages - 1;
     struct Smem {
         float a[kStages][BM * BK];
         float b[kStages][BN * BK];
-        float at[kAtFloats];          // TA: [2][BK][BM]
-        float bt[kBtFloats];          // TB: [2][BK][BN]
+        float at[kAtFloats];          // TA: [kTBufs][BK][BM]
+        float bt[kBtFloats];          // TB: [kTBufs][BK][BN]
         uint64_t full[kStages];
         uint64_t empty[kStages];
         uint64_t t_done[2];           // every thread wrote its part of buffer b
@@ -174,19 +182,26 @@ template <int RA, int RB>
 __device__ __forceinline__ void transpose_slices(const float* rawA, float* dstA, const float* rawB,
                                                  float* dstB) {
     static_assert(BK / 4 == 8 && RA % 32 == 0 && RB % 32 == 0, "8 chunks; whole quarter-warps");
-    constexpr int TA_ = RA / 4 * (BK / 4) / kThreads;     // tasks per thread
-    constexpr int TB_ = RB / 4 * (BK / 4) / kThreads;
-    static_assert(TA_ * kThreads == RA / 4 * (BK / 4) && TB_ * kThreads == RB / 4 * (BK / 4),
-                  "whole tasks per thread");
+    constexpr int NA = RA / 4 * (BK / 4), NB = RB / 4 * (BK / 4);   // tasks
+    constexpr int TA_ = (NA + kThreads - 1) / kThreads;             // tasks per thread
+    constexpr int TB_ = (NB + kThreads - 1) / kThreads;
+    static_assert(NA % 32 == 0 && NB % 32 == 0, "whole warps of tasks");
     float4 va[TA_ > 0 ? TA_ : 1][4], vb[TB_ > 0 ? TB_ : 1][4];
+    // Only a part of the last round has a task when the count is not a
+    // multiple of the block (64-row slices).
+    auto has = [](int n, int j) { return n % kThreads == 0 || (int)threadIdx.x + j * kThreads < n; };
 #pragma unroll
-    for (int j = 0; j < TA_; ++j) quad_load<RA>(rawA, threadIdx.x + j * kThreads, va[j]);
+    for (int j = 0; j < TA_; ++j)
+        if (has(NA, j)) quad_load<RA>(rawA, threadIdx.x + j * kThreads, va[j]);
 #pragma unroll
-    for (int j = 0; j < TB_; ++j) quad_load<RB>(rawB, threadIdx.x + j * kThreads, vb[j]);
+    for (int j = 0; j < TB_; ++j)
+        if (has(NB, j)) quad_load<RB>(rawB, threadIdx.x + j * kThreads, vb[j]);
 #pragma unroll
-    for (int j = 0; j < TA_; ++j) quad_store<RA>(dstA, threadIdx.x + j * kThreads, va[j]);
+    for (int j = 0; j < TA_; ++j)
+        if (has(NA, j)) quad_store<RA>(dstA, threadIdx.x + j * kThreads, va[j]);
 #pragma unroll
-    for (int j = 0; j < TB_; ++j) quad_store<RB>(dstB, threadIdx.x + j * kThreads, vb[j]);
+    for (int j = 0; j < TB_; ++j)
+        if (has(NB, j)) quad_store<RB>(dstB, threadIdx.x + j * kThreads, vb[j]);
 }
 
 struct TileCoord { int64_t b, m0, n0; };
@@ -260,8 +275,13 @@ __device__ __forceinline__ void issue_next(typename Cfg<BM, BN, A_K, B_K>::Smem&
     const int bb = p.b_bcast ? 0 : (int)tc.b;
     const int k0 = is.kt * BK;
     mbar_arrive_expect_tx(&sh.full[s], C::kStageBytes);
-    if (A_K) tma_load_3d(sh.a[s], ta, &sh.full[s], k0, (int)tc.m0, ba);
-    else     tma_load_3d(sh.a[s], ta, &sh.full[s], (int)tc.m0, k0, ba);
+    if (A_K) {
+#pragma unroll
+        for (int j = 0; j < C::kABoxes; ++j)
+            tma_load_3d(sh.a[s] + j * 256 * BK, ta, &sh.full[s], k0, (int)tc.m0 + 256 * j, ba);
+    } else {
+        tma_load_3d(sh.a[s], ta, &sh.full[s], (int)tc.m0, k0, ba);
+    }
     if (B_K) tma_load_3d(sh.b[s], tb, &sh.full[s], k0, (int)tc.n0, bb);
     else     tma_load_3d(sh.b[s], tb, &sh.full[s], (int)tc.n0, k0, bb);
     ++is.issued;
@@ -372,6 +392,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     using C = Cfg<BM, BN, TA, TB>;
     constexpr int S = C::kStages;
     constexpr bool RAW_EARLY = C::kRawEarly;
+    constexpr uint32_t NT = C::kTBufs;
     extern __shared__ uint8_t smem_raw[];
     auto& sh = *reinterpret_cast<typename C::Smem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -481,10 +502,10 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 return;
             }
             if (++stage == S) { stage = 0; phase ^= 1u; }
-            const float* As = TA ? sh.at + (it & 1) * (BK * BM) : sh.a[s];
-            const float* Bs = TB ? sh.bt + (it & 1) * (BK * BN) : sh.b[s];
+            const float* As = TA ? sh.at + (it % NT) * (BK * BM) : sh.a[s];
+            const float* Bs = TB ? sh.bt + (it % NT) * (BK * BN) : sh.b[s];
             if constexpr (TT) {
-                if (!mbar_wait(&sh.t_done[it & 1], (it >> 1) & 1)) {
+                if (!mbar_wait(&sh.t_done[it % NT], (it / NT) & 1)) {
                     record_status(&g_wait_status, kWaitFull);
                     if (issuer) drain<S>(sh.full, is.issued - in_flight(is.issued, it), is.issued);
                     return;
@@ -535,13 +556,13 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 if (lane == 0) mbar_arrive(&sh.empty[s]);
             }
             if constexpr (TT) {
-                mbar_arrive(&sh.t_used[it & 1]);
+                mbar_arrive(&sh.t_used[it % NT]);
                 const uint32_t nx = it + 1;
                 if ((int64_t)nx < is.total) {
-                    const int nb = (int)(nx & 1);
-                    // Buffer nb last held slice nx-2: every thread must be done with it,
+                    const int nb = (int)(nx % NT);
+                    // Buffer nb last held slice nx-NT: every thread must be done with it,
                     // and slice nx's raw tiles (stage `stage`, phase `phase`) must have landed.
-                    const bool ok = (nx < 2 || mbar_wait(&sh.t_used[nb], ((nx >> 1) - 1) & 1)) &&
+                    const bool ok = (nx < NT || mbar_wait(&sh.t_used[nb], ((nx / NT) - 1) & 1)) &&
                                     mbar_wait(&sh.full[stage], phase);
                     if (!ok) {
                         record_status(&g_wait_status, kWaitFull);
@@ -752,7 +773,7 @@ cudaError_t launch_impl(const Problem& pr, const Plan& plan, int sm_count, cudaS
     const bool b_bc = pr.batch == 1 || pr.bsB == 0;
     // A: K-major -> inner K, outer M (stride rsA); MN-major -> inner M, outer K (csA).
     if (!make_map(&ta, pr.A, A_K ? pr.K : pr.M, A_K ? pr.M : pr.K, A_K ? pr.rsA : pr.csA,
-                  pr.bsA, pr.batch, a_bc, A_K, BM))
+                  pr.bsA, pr.batch, a_bc, A_K, BM / C::kABoxes))
         return cudaErrorInvalidValue;
     // B: K-major -> inner K, outer N (csB); MN-major -> inner N, outer K (rsB).
     if (!make_map(&tb, pr.B, B_K ? pr.K : pr.N, B_K ? pr.N : pr.K, B_K ? pr.csB : pr.rsB,
@@ -817,7 +838,9 @@ cudaError_t launch_tile(const Problem& p, const Plan& plan, int sm_count, cudaSt
 constexpr TmaFfmaConfig kConfigs[] = {
     {256, 128, BK, Cfg<256, 128>::kStages, kThreads},
     {128, 256, BK, Cfg<128, 256>::kStages, kThreads},
+    {512, 64, BK, Cfg<512, 64, true, false>::kStages, kThreads},   // N <= 64, K-major A only
 };
+constexpr int kNarrowVariant = 2;
 
 }  // namespace
 
@@ -837,6 +860,9 @@ int tma_ffma_pick_variant(const Problem& p, int sm_count) {
     double best_cost = 0.0;
     int best_rows = 0;
     for (int v = 0; v < tma_ffma_config_count(); ++v) {
+        // 512 x 64 tiles, for N <= 64 with a K-major A: all 8 warps busy where a
+        // 128-wide tile leaves half of them idle.
+        if (v == kNarrowVariant && !(a_k && p.N <= 64)) continue;
         const TmaFfmaConfig c = kConfigs[v];
         const int64_t tm = (p.M + c.bm - 1) / c.bm, tn = (p.N + c.bn - 1) / c.bn;
         const int64_t tiles = tm * tn * p.batch;
@@ -899,6 +925,13 @@ cudaError_t launch_tma_ffma(const Problem& p, const Plan& plan, int sm_count, cu
     switch (plan.variant) {
         case 0: return launch_tile<256, 128>(p, plan, sm_count, stream);
         case 1: return launch_tile<128, 256>(p, plan, sm_count, stream);
+        case kNarrowVariant: {
+            // Only planned for a K-major A (tma_ffma_pick_variant).
+            if (plan.a_layout != SBGEMM_LAYOUT_K_MAJOR) return cudaErrorInvalidValue;
+            if (plan.b_layout == SBGEMM_LAYOUT_K_MAJOR)
+                return launch_impl<512, 64, true, true>(p, plan, sm_count, stream);
+            return launch_impl<512, 64, true, false>(p, plan, sm_count, stream);
+        }
         default: return cudaErrorInvalidValue;
     }
 }

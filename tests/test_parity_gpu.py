@@ -61,8 +61,11 @@ def test_workloads_small(torch, name, values, path):
     gu.check_full(case, got, exact=(values == "int"))
 
 
+# (M, K, N).  N <= 64 with a K-major A takes the 512 x 64 tiles on the TMA
+# path; 1100 x 300 x 50 spans three of them with a ragged last one.
 AWKWARD = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (4, 4, 4), (5, 9, 3), (8, 7, 16),
-           (33, 65, 20), (64, 64, 1), (1, 1, 64), (130, 70, 257), (257, 129, 131)]
+           (33, 65, 20), (64, 64, 1), (1, 1, 64), (130, 70, 257), (257, 129, 131),
+           (1100, 300, 50)]
 LAYOUT_PAIRS = [("row", "row"), ("row", "col"), ("col", "row"), ("col", "col"),
                 ("neg_row", "gap"), ("gap", "bcast_row"), ("bcast_row", "neg_row"),
                 ("row16", "row16"), ("row16", "col16"), ("col16", "row16"), ("col16", "col16")]
