@@ -196,7 +196,8 @@ def case_args(case, dA, dB, dC):
 def kernel_source_digest(path_name):
     common = ["internal.h", "epilogue.cuh"]
     files = {"gather_ffma": ["ffma_gather.cu"] + common,
-             "tma_ffma": ["ffma_tma.cu", "schedule.cuh", "ptx.cuh"] + common,
+             "tma_ffma": ["ffma_tma.cu", "ffma_tma_kernel.cuh", "ffma_tma_256x128.cu", "ffma_tma_128x256.cu",
+                          "ffma_tma_512x64.cu", "schedule.cuh", "ptx.cuh"] + common,
              "tma_tf32": ["tf32_tc.cu", "schedule.cuh", "ptx.cuh"] + common,
              "attention": ["attention.cu", "internal.h"]}.get(path_name, [])
     h = hashlib.sha256()

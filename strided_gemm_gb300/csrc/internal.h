@@ -94,7 +94,7 @@ GatherConfig gather_config(int variant);
 int gather_pick_variant(const Problem& p, int sm_count);
 cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t stream);
 
-// ---- TMA-fed FFMA path (ffma_tma.cu) -----------------------------------------
+// ---- TMA-fed FFMA path (ffma_tma.cu; kernels in ffma_tma_<shape>.cu) ---------
 struct TmaFfmaConfig { int bm, bn, bk, stages, threads; };
 int tma_ffma_config_count();
 TmaFfmaConfig tma_ffma_config(int variant);
@@ -106,6 +106,13 @@ size_t tma_ffma_workspace_bytes(int sm_count);
 void tma_ffma_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
                        int k_split);
 cudaError_t launch_tma_ffma(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
+// One per tile shape (ffma_tma_<shape>.cu), each with its own status word.
+cudaError_t launch_tma_ffma_256x128(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
+cudaError_t launch_tma_ffma_128x256(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
+cudaError_t launch_tma_ffma_512x64(const Problem& p, const Plan& plan, int sm_count, cudaStream_t stream);
+unsigned int read_and_clear_wait_status_tma_ffma_256x128(cudaStream_t stream);
+unsigned int read_and_clear_wait_status_tma_ffma_128x256(cudaStream_t stream);
+unsigned int read_and_clear_wait_status_tma_ffma_512x64(cudaStream_t stream);
 
 // Reads and clears the status words of the kernels that use bounded waits.
 // Returns the first non-zero code found (0 if none).
