@@ -114,6 +114,22 @@ def test_fused_every_path_activation_and_addend(torch, path, act):
         check_fused(case, D, act, got, tol=tol)
 
 
+@pytest.mark.parametrize("act", ACTS)
+def test_fused_tf32_column_major_c_through_tma(torch, act):
+    """TF32 with a column-major C whose pitch (256 rows) suits a tensor map.
+    Both operands K-major: the epilogue stages each 32 x 32 piece column by
+    column and writes it with a TMA store through an M-inner map (C_old comes
+    in the same way).  A K-major with B N-major: the plan is the transposed
+    product, whose C^T is row-major."""
+    rng = np.random.default_rng(40 + len(act))
+    for la, lb, kind in (("row16", "col16", "col_bias"), ("row16", "row16", "matrix_colmajor")):
+        case = wl.random_strided(rng, 256, 200, 96, 2, la, lb, c_layout="col", values="real",
+                                 accumulate=1, alpha=0.75)
+        D = make_D(rng, case, kind, "real")
+        got = run_fused(case, D, act, torch, sg.MATH_TF32, sg.PATH_TMA_TF32)
+        check_fused(case, D, act, got, tol=gu.TOL_TF32)
+
+
 @pytest.mark.parametrize("act", ["none", "relu"])
 @pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
 def test_fused_integer_inputs_exact(torch, path, act):
