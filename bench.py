@@ -229,6 +229,28 @@ def profiled_traffic(path_name, case_name):
 
 # ---------------------------------------------------------------- CPU oracle
 
+def host_cpu():
+    """The host CPU as /proc/cpuinfo names it (model name, or on Arm the
+    implementer and part codes), plus the machine type."""
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    import platform
+    if "model name" in fields:
+        name = fields["model name"]
+    elif "CPU implementer" in fields:
+        name = f"implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    else:
+        name = "unknown"
+    return f"{name} ({platform.machine()})"
+
+
 def oracle_sample(cases, seconds_target, threads, rows_override=None):
     """Times the oracle on the first rows of each product.  Returns
     (gflop_per_s, seconds, flops, rows)."""
@@ -683,7 +705,8 @@ def run_ours(args, world, rank, local, dist):
         g, dt, fl, rows = oracle_sample(cases, args.cpu_seconds, threads)
         cpu = {"value": round(g, 3), "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"first {rows} rows of each product of the step "
-                         f"({fl / 1e9:.2f} GFLOP, {dt:.1f} s), fp64 accumulation"}
+                         f"({fl / 1e9:.2f} GFLOP, {dt:.1f} s), fp64 accumulation",
+               "cpu": host_cpu()}
 
     if rank != 0:
         return None
@@ -744,7 +767,7 @@ def run_reference(args, world, rank):
         "config": {"workload": DESCR.get(args.workload, args.workload), "math": "fp64 oracle"},
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "kind": "oracle",
-                         "cores": threads, "sample": sample},
+                         "cores": threads, "sample": sample, "cpu": host_cpu()},
         "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
