@@ -11,8 +11,16 @@
 // product", with the 4 x 4 block grown to 8 x 8).  The epilogue forms
 // fmaf(alpha, acc, C_old) (or alpha*acc) and stores with masks on ragged M / N;
 // ragged K is covered by zero-filled loads.
+//
+// Small products (a few dozen tiles, as a 256 x 512 layer) would leave most
+// SMs idle, so with a caller workspace their K range is cut into pieces, one
+// CTA per (tile, piece): each piece parks its partial sums, and the CTA that
+// finishes a tile last (an atomic count per tile) adds the pieces in piece
+// order and runs the epilogue.  Deterministic, but rounded differently from
+// one chain, so only under k_split = ANY.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "epilogue.cuh"
@@ -22,6 +30,14 @@ namespace sbg {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMinPieceSlices = 4;   // K slices (of 16) per piece at least
+constexpr int kMaxPieces = 16;
+
+struct Split {
+    int pieces;                 // K pieces per tile (grid z); 1 = whole tiles
+    float* part;                // [tile][piece][BM * BN] partial sums
+    unsigned int* count;        // [tile] pieces finished, zeroed before launch
+};
 
 // Loads one operand's R x BK slice (R = rows of the tile: BM for A, BN for B).
 // `rs` steps along R, `ks` along K.  RFAST: consecutive threads take
@@ -75,13 +91,14 @@ struct SliceLoader {
 
 template <int BM, int BN, int BK, int TM, int TN, bool A_MFAST, bool B_NFAST>
 __global__ void __launch_bounds__(kThreads, 2)
-gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n) {
+gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n, const Split sp) {
     static_assert((BM / TM) * (BN / TN) == kThreads, "thread grid must cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "micro-tile is built from float4 rows");
     constexpr int LDA = BM + 4;   // +4 floats keeps float4 alignment of each k-row
     constexpr int LDB = BN + 4;
     __shared__ __align__(16) float As[2][BK][LDA];
     __shared__ __align__(16) float Bs[2][BK][LDB];
+    __shared__ unsigned int last_piece;
 
     const int tid = threadIdx.x;
     const int tx = tid % (BN / TN);
@@ -101,6 +118,9 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
     const int64_t m0 = tm * BM, n0 = tn * BN;
     const int64_t rows_a = p.M - m0, rows_b = p.N - n0;
     const int64_t nk = (p.K + BK - 1) / BK;
+    // This CTA's K slices [kb, ke): all of them, or its piece's share.
+    const int piece = (int)blockIdx.z;
+    const int64_t kb = nk * piece / sp.pieces, ke = nk * (piece + 1) / sp.pieces;
 
     for (int64_t b = blockIdx.y; b < p.batch; b += gridDim.y) {
         const float* __restrict__ Ab = p.A + b * p.bsA;
@@ -117,17 +137,17 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
 #pragma unroll
             for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
-        if (nk > 0) {
-            la.load(Ab, 0, rows_a, p.K);
-            lb.load(Bb, 0, rows_b, p.K);
+        if (ke > kb) {
+            la.load(Ab, kb, rows_a, p.K - kb * BK);
+            lb.load(Bb, kb, rows_b, p.K - kb * BK);
             la.template store<LDA>(As[0]);
             lb.template store<LDB>(Bs[0]);
         }
         __syncthreads();
 
-        for (int64_t kt = 0; kt < nk; ++kt) {
-            const int buf = (int)(kt & 1);
-            const bool more = kt + 1 < nk;
+        for (int64_t kt = kb; kt < ke; ++kt) {
+            const int buf = (int)((kt - kb) & 1);
+            const bool more = kt + 1 < ke;
             if (more) {
                 la.load(Ab, kt + 1, rows_a, p.K - (kt + 1) * BK);
                 lb.load(Bb, kt + 1, rows_b, p.K - (kt + 1) * BK);
@@ -157,6 +177,37 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
                 lb.template store<LDB>(Bs[buf ^ 1]);
             }
             __syncthreads();
+        }
+
+        if (sp.pieces > 1) {
+            // Park this piece; the last piece of the tile to finish sums them
+            // all in piece order (a warp's stores and loads are contiguous).
+            const int64_t tile_id = b * (tiles_m * tiles_n) + t;
+            float* slot = sp.part + (tile_id * sp.pieces + piece) * (int64_t)(BM * BN);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) __stcg(slot + (i * TN + j) * kThreads + tid, acc[i][j]);
+            __threadfence();
+            __syncthreads();
+            if (tid == 0)
+                last_piece = atomicAdd(sp.count + tile_id, 1u) == (unsigned int)(sp.pieces - 1);
+            __syncthreads();
+            if (!last_piece) continue;
+            __threadfence();
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+            const float* first = sp.part + tile_id * sp.pieces * (int64_t)(BM * BN);
+#pragma unroll 1
+            for (int q = 0; q < sp.pieces; ++q) {
+                const float* src = first + q * (int64_t)(BM * BN);
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] += __ldcg(src + (i * TN + j) * kThreads + tid);
+            }
         }
 
         // Epilogue: alpha * acc (+ C_old), masked on ragged M / N.
@@ -191,6 +242,13 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
     }
 }
 
+// Bytes of the partial sums of `tiles` tiles cut into `pieces`, rounded up to
+// 256 so that the counters after them stay aligned.
+size_t split_part_bytes(int64_t tiles, int pieces, int tile_elems) {
+    const size_t b = (size_t)tiles * (size_t)pieces * (size_t)tile_elems * sizeof(float);
+    return (b + 255) / 256 * 256;
+}
+
 template <int BM, int BN, int BK, int TM, int TN>
 cudaError_t launch_variant(const Problem& p, const Plan& plan, cudaStream_t stream) {
     // A: tile rows are M (stride rsA), k stride csA; B: tile rows are N (stride
@@ -199,17 +257,26 @@ cudaError_t launch_variant(const Problem& p, const Plan& plan, cudaStream_t stre
     auto mag = [](int64_t x) { return x < 0 ? -x : x; };
     const bool a_fast = mag(p.rsA) < mag(p.csA);
     const bool b_fast = mag(p.csB) < mag(p.rsB);
+    Split sp{1, nullptr, nullptr};
+    if (plan.k_pieces > 1) {
+        sp.pieces = plan.k_pieces;
+        sp.part = static_cast<float*>(plan.workspace);
+        sp.count = reinterpret_cast<unsigned int*>(static_cast<char*>(plan.workspace) +
+                                                   split_part_bytes(plan.tiles, plan.k_pieces, BM * BN));
+        cudaError_t e = cudaMemsetAsync(sp.count, 0, (size_t)plan.tiles * sizeof(unsigned int), stream);
+        if (e != cudaSuccess) return e;
+    }
     dim3 grid((unsigned)(plan.tiles_m * plan.tiles_n),
-              (unsigned)(p.batch < 65535 ? p.batch : 65535));
+              (unsigned)(p.batch < 65535 ? p.batch : 65535), (unsigned)sp.pieces);
     dim3 block(kThreads);
     if (a_fast && b_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, true, true><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, true, true><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
     else if (a_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, true, false><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, true, false><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
     else if (b_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, false, true><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, false, true><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
     else
-        gather_ffma_kernel<BM, BN, BK, TM, TN, false, false><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, false, false><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
     return cudaGetLastError();
 }
 
@@ -228,6 +295,33 @@ int gather_pick_variant(const Problem& p, int sm_count) {
     // Prefer the large tile when it still gives every SM at least one CTA.
     const int64_t big = ((p.M + 127) / 128) * ((p.N + 127) / 128) * p.batch;
     return big >= sm_count ? 0 : 1;
+}
+
+void gather_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
+                     int k_split) {
+    const GatherConfig g = kConfigs[plan.variant];
+    const int64_t nk = (p.K + g.bk - 1) / g.bk;
+    plan.k_slices = (int)nk;
+    plan.k_pieces = 1;
+    if (!ws || k_split != SBGEMM_KSPLIT_ANY || p.batch > 65535) return;
+    if ((reinterpret_cast<uintptr_t>(ws) % 256) != 0) return;
+    // Only when the tiles would fill less than half of the CTA slots; then
+    // enough pieces to fill them about once, each at least 4 slices.
+    const int64_t slots = (int64_t)sm_count * g.ctas_per_sm;
+    if (plan.tiles * 2 > slots) return;
+    int64_t pieces = (slots + plan.tiles - 1) / plan.tiles;
+    pieces = std::min<int64_t>(pieces, nk / kMinPieceSlices);
+    pieces = std::min<int64_t>(pieces, kMaxPieces);
+    if (pieces < 2) return;
+    const size_t need = split_part_bytes(plan.tiles, (int)pieces, g.bm * g.bn) +
+                        (size_t)plan.tiles * sizeof(unsigned int);
+    if (need > ws_bytes) return;
+    plan.k_pieces = (int)pieces;
+    plan.stream_k = true;
+    plan.split_indep = true;
+    plan.dp_tiles = 0;
+    plan.ctas = plan.tiles * pieces;
+    plan.workspace = const_cast<void*>(ws);
 }
 
 cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t stream) {

@@ -62,6 +62,7 @@ struct Plan {
     bool transposed = false;        // computed as C^T = B^T A^T (tiles, schedule and
                                     // launch are those of the transposed problem)
     int64_t dp_tiles = 0;           // tiles computed whole
+    int k_pieces = 1;               // gather path: K pieces per tile (independent)
     void* workspace = nullptr;      // caller's scratch when stream_k
 };
 
@@ -92,6 +93,10 @@ int gather_config_count();
 GatherConfig gather_config(int variant);
 // Picks a variant for the problem size on a device with `sm_count` SMs.
 int gather_pick_variant(const Problem& p, int sm_count);
+// With a workspace and k_split = ANY, cuts the K range of products with few
+// tiles into pieces (plan.k_pieces, summed in a fixed order).
+void gather_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
+                     int k_split);
 cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t stream);
 
 // ---- TMA-fed FFMA path (ffma_tma.cu; kernels in ffma_tma_<shape>.cu) ---------

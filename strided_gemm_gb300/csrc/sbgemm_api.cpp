@@ -271,6 +271,7 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
     if (plan->tiles_m * plan->tiles_n >= ((int64_t)1 << 31)) return SBGEMM_ERR_UNSUPPORTED;
     plan->tiles = plan->tiles_m * plan->tiles_n * p.batch;
     plan->ctas = plan->tiles_m * plan->tiles_n * std::min<int64_t>(p.batch, 65535);
+    gather_schedule(p, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace, o.k_split);
     return SBGEMM_OK;
 }
 

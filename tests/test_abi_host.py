@@ -189,11 +189,13 @@ def test_stream_k_planning():
     with pytest.raises(sg.SbgemmError) as e:
         call_plan(A, B, C, M, N, K, 1, workspace=ws + 16, workspace_bytes=big)
     assert e.value.status == sg.SBGEMM_ERR_INVALID_VALUE
-    # Fewer tiles than SMs, or few K slices: nothing to gain.
+    # Fewer tiles than a quarter of the SMs: the gather path, whose 64 tiles
+    # are cut into K pieces (test_gather_k_pieces_planning); few K slices:
+    # nothing to gain.
     small = call_plan(rowmajor(BASE, 512, 512, 1), rowmajor(BASE + (1 << 32), 512, 512, 1),
                       rowmajor(BASE + (2 << 32), 512, 512, 1), 512, 512, 512, 1,
                       workspace=ws, workspace_bytes=big)
-    assert not small["stream_k"]
+    assert small["path"] == sg.PATH_GATHER_FFMA and small["stream_k"] == sg.STREAM_K_PIECES
     shortk = call_plan(rowmajor(BASE, 4096, 64, 1), (BASE + (1 << 32), 1, 64, 0),
                        rowmajor(BASE + (2 << 32), 4096, 4096, 1), 4096, 4096, 64, 1,
                        workspace=ws, workspace_bytes=big)
@@ -299,3 +301,28 @@ def test_tf32_k_major_a_with_n_major_b_runs_transposed(N):
     assert p["path"] == sg.PATH_TMA_TF32 and (p["tile_m"], p["tile_n"]) == (256, 128), p
     q = call_plan(A_m, B_k, C, M, N, K, 1, math=sg.MATH_TF32)
     assert q["path"] == sg.PATH_TMA_TF32 and (q["tile_m"], q["tile_n"]) == (128, 256), q
+
+
+def test_gather_k_pieces_planning():
+    """The gather path cuts K into pieces only for products whose tiles fill
+    less than half of the CTA slots, with a workspace and k_split = ANY; each
+    piece keeps at least 4 slices of 16."""
+    ws, big = BASE + (8 << 32), 64 << 20
+    M, N, K = 256, 512, 784
+    A = (BASE, 786, 1, 0)                    # gapped rows: no tensor map, gather path
+    B = (BASE + (1 << 32), 1, K + 3, 0)
+    C = rowmajor(BASE + (2 << 32), M, N, 1)
+    p = call_plan(A, B, C, M, N, K, 1, workspace=ws, workspace_bytes=big)
+    assert p["path"] == sg.PATH_GATHER_FFMA and p["stream_k"] == sg.STREAM_K_PIECES, p
+    pieces = p["ctas"] // p["tiles"]
+    assert p["ctas"] == p["tiles"] * pieces and 2 <= pieces <= 16
+    assert pieces * 4 <= -(-K // 16)
+    for kw in ({}, dict(workspace=ws, workspace_bytes=big, k_split=sg.KSPLIT_EXACT),
+               dict(workspace=ws, workspace_bytes=1024)):
+        q = call_plan(A, B, C, M, N, K, 1, **kw)
+        assert q["path"] == sg.PATH_GATHER_FFMA and q["stream_k"] == sg.STREAM_K_NONE, (kw, q)
+    # Short K (2 slices) or enough tiles to fill the GPU: whole tiles.
+    q = call_plan(A, B, C, M, N, 32, 1, workspace=ws, workspace_bytes=big)
+    assert q["stream_k"] == sg.STREAM_K_NONE
+    q = call_plan(A, B, C, M, N, K, 40, workspace=ws, workspace_bytes=big)
+    assert q["stream_k"] == sg.STREAM_K_NONE

@@ -312,6 +312,33 @@ def test_split_k_pieces_parity_and_determinism(torch, workspace, shape):
     assert st == sg.SBGEMM_OK, where
 
 
+@pytest.mark.parametrize("name", ["c2a", "c2b", "strided"])
+def test_gather_k_pieces_parity_and_determinism(torch, workspace, name):
+    """Small products on the gather path cut K into pieces (one CTA per tile
+    and piece, summed in piece order by the tile's last CTA): within the
+    oracle's bound, exact on integers, identical on every run; k_split = EXACT
+    keeps one chain per output, bit for bit the result without a workspace."""
+    rng = np.random.default_rng(23 + len(name))
+    for values in ("real", "int"):
+        if name == "strided":
+            # Gapped and negative strides (no tensor map), ragged, batched, +C.
+            case = wl.random_strided(rng, 100, 70, 900, 3, "gap", "neg_row", values=values,
+                                     accumulate=1, alpha=-0.5)
+        else:
+            case = wl.make(name, values)
+        first, plan = _run_ws(case, torch, workspace)
+        assert plan["path"] == sg.PATH_GATHER_FFMA and plan["stream_k"] == sg.STREAM_K_PIECES, plan
+        gu.check_full(case, first, exact=(values == "int"))
+        again, _ = _run_ws(case, torch, workspace)
+        assert np.array_equal(first, again)
+    whole, _ = _run_ws(case, torch, None)
+    exact, plan_x = _run_ws(case, torch, workspace, dict(k_split=sg.KSPLIT_EXACT))
+    assert plan_x["stream_k"] == sg.STREAM_K_NONE
+    assert np.array_equal(exact, whole)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
 def test_split_k_pieces_integer_exact(torch, workspace):
     """Integer inputs: every partial sum is exact, so the split result is the
     exact product whatever the order of the pieces."""
