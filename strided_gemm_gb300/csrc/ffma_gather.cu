@@ -89,7 +89,9 @@ struct SliceLoader {
     }
 };
 
-template <int BM, int BN, int BK, int TM, int TN, bool A_MFAST, bool B_NFAST>
+// SPLIT: the instantiation for K pieces (64 x 64 tiles only), so that the
+// others keep their registers.
+template <int BM, int BN, int BK, int TM, int TN, bool A_MFAST, bool B_NFAST, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
 gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n, const Split sp) {
     static_assert((BM / TM) * (BN / TN) == kThreads, "thread grid must cover the tile");
@@ -119,8 +121,9 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
     const int64_t rows_a = p.M - m0, rows_b = p.N - n0;
     const int64_t nk = (p.K + BK - 1) / BK;
     // This CTA's K slices [kb, ke): all of them, or its piece's share.
-    const int piece = (int)blockIdx.z;
-    const int64_t kb = nk * piece / sp.pieces, ke = nk * (piece + 1) / sp.pieces;
+    const int piece = SPLIT ? (int)blockIdx.z : 0;
+    const int64_t kb = SPLIT ? nk * piece / sp.pieces : 0;
+    const int64_t ke = SPLIT ? nk * (piece + 1) / sp.pieces : nk;
 
     for (int64_t b = blockIdx.y; b < p.batch; b += gridDim.y) {
         const float* __restrict__ Ab = p.A + b * p.bsA;
@@ -179,7 +182,7 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
             __syncthreads();
         }
 
-        if (sp.pieces > 1) {
+        if constexpr (SPLIT) {
             // Park this piece; the last piece of the tile to finish sums them
             // all in piece order (a warp's stores and loads are contiguous).
             const int64_t tile_id = b * (tiles_m * tiles_n) + t;
@@ -249,7 +252,7 @@ size_t split_part_bytes(int64_t tiles, int pieces, int tile_elems) {
     return (b + 255) / 256 * 256;
 }
 
-template <int BM, int BN, int BK, int TM, int TN>
+template <int BM, int BN, int BK, int TM, int TN, bool SPLIT>
 cudaError_t launch_variant(const Problem& p, const Plan& plan, cudaStream_t stream) {
     // A: tile rows are M (stride rsA), k stride csA; B: tile rows are N (stride
     // csB), k stride rsB.  Consecutive threads walk whichever index has the
@@ -258,7 +261,7 @@ cudaError_t launch_variant(const Problem& p, const Plan& plan, cudaStream_t stre
     const bool a_fast = mag(p.rsA) < mag(p.csA);
     const bool b_fast = mag(p.csB) < mag(p.rsB);
     Split sp{1, nullptr, nullptr};
-    if (plan.k_pieces > 1) {
+    if (SPLIT) {
         sp.pieces = plan.k_pieces;
         sp.part = static_cast<float*>(plan.workspace);
         sp.count = reinterpret_cast<unsigned int*>(static_cast<char*>(plan.workspace) +
@@ -270,13 +273,13 @@ cudaError_t launch_variant(const Problem& p, const Plan& plan, cudaStream_t stre
               (unsigned)(p.batch < 65535 ? p.batch : 65535), (unsigned)sp.pieces);
     dim3 block(kThreads);
     if (a_fast && b_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, true, true><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, true, true, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
     else if (a_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, true, false><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, true, false, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
     else if (b_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, false, true><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, false, true, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
     else
-        gather_ffma_kernel<BM, BN, BK, TM, TN, false, false><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, false, false, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
     return cudaGetLastError();
 }
 
@@ -303,7 +306,8 @@ void gather_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes
     const int64_t nk = (p.K + g.bk - 1) / g.bk;
     plan.k_slices = (int)nk;
     plan.k_pieces = 1;
-    if (!ws || k_split != SBGEMM_KSPLIT_ANY || p.batch > 65535) return;
+    // Only the 64 x 64 tiles of small products are cut.
+    if (plan.variant != 1 || !ws || k_split != SBGEMM_KSPLIT_ANY || p.batch > 65535) return;
     if ((reinterpret_cast<uintptr_t>(ws) % 256) != 0) return;
     // Only when the tiles would fill less than half of the CTA slots; then
     // enough pieces to fill them about once, each at least 4 slices.
@@ -326,8 +330,10 @@ void gather_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes
 
 cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t stream) {
     switch (plan.variant) {
-        case 0: return launch_variant<128, 128, 16, 8, 8>(p, plan, stream);
-        case 1: return launch_variant<64, 64, 16, 4, 4>(p, plan, stream);
+        case 0: return launch_variant<128, 128, 16, 8, 8, false>(p, plan, stream);
+        case 1:
+            if (plan.k_pieces > 1) return launch_variant<64, 64, 16, 4, 4, true>(p, plan, stream);
+            return launch_variant<64, 64, 16, 4, 4, false>(p, plan, stream);
         default: return cudaErrorInvalidValue;
     }
 }
