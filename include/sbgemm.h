@@ -122,7 +122,9 @@ enum {
                                  or, with fewer tiles than SMs and long K
                                  (e.g. the weight gradient Gt*X), independent K
                                  pieces summed in a fixed order; the latter
-                                 rounds differently from the unsplit product */
+                                 rounds differently from the unsplit product.
+                                 Small products on the gather path are cut
+                                 into K pieces the same way. */
     SBGEMM_KSPLIT_EXACT = 1,  /* only splits whose result is bit-identical to
                                  the unsplit schedule (chained stream-K) */
     SBGEMM_KSPLIT_NONE = 2    /* never split K */
@@ -136,7 +138,9 @@ enum {
                                      do not change */
     SBGEMM_STREAM_K_PIECES = 2    /* all tiles split into independent K pieces
                                      over the SMs, the tail adding the earlier
-                                     pieces' partial sums latest first */
+                                     pieces' partial sums latest first (on the
+                                     gather path the tile's last CTA adds all
+                                     pieces in piece order) */
 };
 
 typedef struct {
@@ -273,7 +277,8 @@ SBGEMM_API int sbgemm_plan(const float* A, int64_t rsA, int64_t csA, int64_t bsA
                 sbgemm_plan_info* info);
 
 /* Workspace size that lets sbgemm_ex use the stream-K schedule on `device`
- * (one fp32 tile of partial sums per SM plus one flag word per SM).  Returns
+ * (one fp32 tile of partial sums per SM plus one flag word per SM); the
+ * gather path's K pieces of small products fit in it too.  Returns
  * SBGEMM_OK and writes *bytes, or SBGEMM_ERR_CUDA if the device cannot be
  * queried. */
 SBGEMM_API int sbgemm_workspace_bytes(int device, size_t* bytes);
