@@ -199,7 +199,8 @@ def kernel_source_digest(path_name):
              "tma_ffma": ["ffma_tma.cu", "ffma_tma_kernel.cuh", "ffma_tma_256x128.cu", "ffma_tma_128x256.cu",
                           "ffma_tma_512x64.cu", "schedule.cuh", "ptx.cuh"] + common,
              "tma_tf32": ["tf32_tc.cu", "schedule.cuh", "ptx.cuh"] + common,
-             "attention": ["attention.cu", "internal.h"]}.get(path_name, [])
+             "attention": ["attention.cu", "internal.h"],
+             "attention_tc": ["attention_tc.cu", "attention_tc.h", "ptx.cuh", "internal.h"]}.get(path_name, [])
     h = hashlib.sha256()
     for f in files:
         p = os.path.join(ROOT, "strided_gemm_gb300", "csrc", f)
@@ -595,6 +596,11 @@ def run_ours(args, world, rank, local, dist):
             row = {"ms": round(ms, 4), "gflops": round(c.flops / ms / 1e6, 1),
                    "flops": "2*M*N*(D+Dv) per batch entry, every key counted",
                    "causal": bool(c.causal)}
+            # The opt-in TF32 kernel (both products on the tensor cores).
+            ms_tc = timed(lambda: sg.sbgemm_attention(*a, s_handle, math=sg.MATH_TF32,
+                                                      force_path=sg.PATH_TMA_TF32))
+            row["tf32"] = {"ms": round(ms_tc, 4), "gflops": round(c.flops / ms_tc / 1e6, 1),
+                           "speedup_vs_fp32": round(ms / ms_tc, 2)}
             if not c.causal:
                 S = torch.empty(c.batch, c.M, c.N, device=dev)
 

@@ -266,6 +266,24 @@ SBGEMM_API int sbgemm_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_
                      int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
                      float alpha, int causal, int64_t q_len, void* stream);
 
+/* sbgemm_attention with options.  opt->math = SBGEMM_MATH_TF32 opts in to the
+ * tensor-core kernel: S = Q K^T and P V by tcgen05 MMAs (tf32 inputs, fp32
+ * accumulation), the softmax in fp32 as above.  It takes Q, K and V with unit
+ * stride along the head dimension (csQ = csK = csV = 1), 16-byte aligned bases
+ * and row / batch strides (a zero batch stride broadcasts); other layouts run
+ * the fp32 kernel, unless opt->force_path = SBGEMM_PATH_TMA_TF32, which then
+ * returns SBGEMM_ERR_UNSUPPORTED.  opt->workspace and k_split are ignored;
+ * force_path must be AUTO or TMA_TF32 (TMA_TF32 with math = TF32).  NULL opt
+ * is sbgemm_attention.  Errors as sbgemm_attention, plus those of the
+ * options. */
+SBGEMM_API int sbgemm_attention_ex(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
+                        const float* K, int64_t rsK, int64_t csK, int64_t bsK,
+                        const float* V, int64_t rsV, int64_t csV, int64_t bsV,
+                        float* O, int64_t rsO, int64_t csO, int64_t bsO,
+                        int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
+                        float alpha, int causal, int64_t q_len, void* stream,
+                        const sbgemm_options* opt);
+
 /* Validate and plan without launching or touching device memory: reports the
  * layout classes and the kernel path, tile and CTA count that sbgemm_ex would
  * use.  Pointers are only checked for NULL and alignment (no device query). */

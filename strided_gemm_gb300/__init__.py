@@ -25,7 +25,7 @@ __all__ = [
     "MATH_FP32", "MATH_TF32", "PATH_NONE", "PATH_AUTO", "PATH_GATHER_FFMA",
     "PATH_TMA_FFMA", "PATH_TMA_TF32", "LAYOUT_K_MAJOR", "LAYOUT_MN_MAJOR",
     "LAYOUT_GENERAL", "EXPORTED_SYMBOLS", "LIB_PATH", "sbgemm_fused", "linear_backward",
-    "sbgemm_attention", "attention",
+    "sbgemm_attention", "sbgemm_attention_ex", "attention",
     "ACT_NONE", "ACT_RELU", "ACT_SIGMOID", "ACT_SILU", "ACT_GELU_TANH", "ACT_GELU_ERF",
     "ACTIVATIONS", "KSPLIT_ANY", "KSPLIT_EXACT", "KSPLIT_NONE", "STREAM_K_NONE",
     "STREAM_K_CHAINED", "STREAM_K_PIECES",
@@ -50,7 +50,8 @@ PATH_NAMES = {PATH_NONE: "none", PATH_GATHER_FFMA: "gather_ffma",
               PATH_TMA_FFMA: "tma_ffma", PATH_TMA_TF32: "tma_tf32"}
 
 # Every function include/sbgemm.h declares.
-EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_fused", "sbgemm_attention", "sbgemm_plan",
+EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_fused", "sbgemm_attention",
+                    "sbgemm_attention_ex", "sbgemm_plan",
                     "sbgemm_workspace_bytes", "sbgemm_noalloc", "sbgemm_selftest",
                     "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version")
 ACT_NONE, ACT_RELU, ACT_SIGMOID, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4, 5
@@ -120,6 +121,10 @@ def load(path: str = LIB_PATH):
         op4 = [_vp, _i64, _i64, _i64]
         lib.sbgemm_attention.argtypes = (op4 * 4 + [_i64] * 5 +
                                          [ctypes.c_float, ctypes.c_int, _i64, _vp])
+        lib.sbgemm_attention_ex.restype = ctypes.c_int
+        lib.sbgemm_attention_ex.argtypes = (op4 * 4 + [_i64] * 5 +
+                                            [ctypes.c_float, ctypes.c_int, _i64, _vp,
+                                             ctypes.POINTER(_Options)])
         lib.sbgemm_ex.restype = ctypes.c_int
         lib.sbgemm_ex.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp,
                                           ctypes.POINTER(_Options)]
@@ -221,8 +226,14 @@ def sbgemm_fused(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
 
 def sbgemm_attention(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
                      O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal=0, q_len=0,
-                     stream=0) -> None:
-    """O = softmax(alpha * Q K^T [causal]) V over strided operands."""
+                     stream=0, math: int = MATH_FP32, force_path: int = PATH_AUTO) -> None:
+    """O = softmax(alpha * Q K^T [causal]) V over strided operands; math =
+    MATH_TF32 opts in to the tensor-core kernel (sbgemm_attention_ex)."""
+    if math != MATH_FP32 or force_path != PATH_AUTO:
+        sbgemm_attention_ex(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
+                            O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal, q_len,
+                            stream, math=math, force_path=force_path)
+        return
     st = load().sbgemm_attention(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
                                  O, rsO, csO, bsO, M, N, D, Dv, batch, float(alpha),
                                  int(causal), int(q_len), stream or None)
@@ -230,11 +241,25 @@ def sbgemm_attention(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
         raise SbgemmError(st, "sbgemm_attention")
 
 
-def attention(Q, K, V, O, alpha=None, causal=False, q_len=0, stream=None):
+def sbgemm_attention_ex(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
+                        O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal=0, q_len=0,
+                        stream=0, math: int = MATH_FP32, force_path: int = PATH_AUTO) -> None:
+    """sbgemm_attention with options: math = MATH_TF32 runs the tensor-core
+    kernel when Q, K and V suit tensor maps (force_path = PATH_TMA_TF32 makes
+    that a requirement)."""
+    o = _opts(math, force_path)
+    st = load().sbgemm_attention_ex(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
+                                    O, rsO, csO, bsO, M, N, D, Dv, batch, float(alpha),
+                                    int(causal), int(q_len), stream or None, ctypes.byref(o))
+    if st:
+        raise SbgemmError(st, "sbgemm_attention_ex")
+
+
+def attention(Q, K, V, O, alpha=None, causal=False, q_len=0, stream=None, math=MATH_FP32):
     """Torch helper: Q [batch, M, D], K [batch, N, D], V [batch, N, Dv] and O
     [batch, M, Dv] float32 CUDA tensors with any strides (2-D means batch 1;
-    K and V may have batch 1 to be shared).  alpha defaults to 1/sqrt(D).
-    Returns O."""
+    K and V may have batch 1 to be shared).  alpha defaults to 1/sqrt(D);
+    math = MATH_TF32 opts in to the tensor cores.  Returns O."""
     import torch
     Q3, K3, V3, O3 = _as3(Q, "Q"), _as3(K, "K"), _as3(V, "V"), _as3(O, "O")
     for t, n in ((Q3, "Q"), (K3, "K"), (V3, "V"), (O3, "O")):
@@ -253,7 +278,7 @@ def attention(Q, K, V, O, alpha=None, causal=False, q_len=0, stream=None):
                      V3.data_ptr(), V3.stride(1), V3.stride(2), bs(V3),
                      O3.data_ptr(), O3.stride(1), O3.stride(2), O3.stride(0),
                      M, N, D, Dv, batch, (1.0 / D ** 0.5) if alpha is None else alpha,
-                     int(bool(causal)), int(q_len) if causal else 0, stream)
+                     int(bool(causal)), int(q_len) if causal else 0, stream, math=math)
     return O
 
 

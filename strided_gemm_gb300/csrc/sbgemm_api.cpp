@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "attention_tc.h"
 #include "internal.h"
 #include "sbgemm.h"
 
@@ -491,12 +492,19 @@ int sbgemm_fused(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     return run(p, o, stream);
 }
 
-int sbgemm_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
-                     const float* K, int64_t rsK, int64_t csK, int64_t bsK,
-                     const float* V, int64_t rsV, int64_t csV, int64_t bsV,
-                     float* O, int64_t rsO, int64_t csO, int64_t bsO,
-                     int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
-                     float alpha, int causal, int64_t q_len, void* stream) {
+int sbgemm_attention_ex(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
+                        const float* K, int64_t rsK, int64_t csK, int64_t bsK,
+                        const float* V, int64_t rsV, int64_t csV, int64_t bsV,
+                        float* O, int64_t rsO, int64_t csO, int64_t bsO,
+                        int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
+                        float alpha, int causal, int64_t q_len, void* stream,
+                        const sbgemm_options* opt) {
+    sbgemm_options o;
+    const int ost = check_options(opt, &o);
+    if (ost) return ost;
+    if (o.force_path != SBGEMM_PATH_AUTO && o.force_path != SBGEMM_PATH_TMA_TF32)
+        return SBGEMM_ERR_UNSUPPORTED;
+    if (o.force_path == SBGEMM_PATH_TMA_TF32 && o.math != SBGEMM_MATH_TF32) return SBGEMM_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || D < 0 || Dv < 0 || batch < 0) return SBGEMM_ERR_INVALID_VALUE;
     if (causal != 0 && causal != 1) return SBGEMM_ERR_INVALID_VALUE;
     if (M == 0 || batch == 0 || Dv == 0) return SBGEMM_OK;
@@ -528,11 +536,28 @@ int sbgemm_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
         return SBGEMM_ERR_NOT_DEVICE_MEMORY;
     AttnProblem a{Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV, O, rsO, csO, bsO,
                   M, N, D, Dv, batch, alpha, causal, causal ? q_len : M};
-    if (launch_attention(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    // TF32 on the tensor cores when asked for and the operands suit tensor
+    // maps; otherwise the fp32 kernel (or, when forced, unsupported).
+    const bool tc = o.math == SBGEMM_MATH_TF32 && attention_tc_supported(a);
+    if (o.force_path == SBGEMM_PATH_TMA_TF32 && !tc) return SBGEMM_ERR_UNSUPPORTED;
+    const cudaError_t e = tc ? launch_attention_tc(a, static_cast<cudaStream_t>(stream))
+                             : launch_attention(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return SBGEMM_ERR_CUDA;
     }
     return SBGEMM_OK;
+}
+
+int sbgemm_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
+                     const float* K, int64_t rsK, int64_t csK, int64_t bsK,
+                     const float* V, int64_t rsV, int64_t csV, int64_t bsV,
+                     float* O, int64_t rsO, int64_t csO, int64_t bsO,
+                     int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
+                     float alpha, int causal, int64_t q_len, void* stream) {
+    return sbgemm_attention_ex(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
+                               O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal, q_len,
+                               stream, nullptr);
 }
 
 int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
@@ -562,8 +587,10 @@ int sbgemm_device_status(void* stream, int* where_out) {
     unsigned int code = read_and_clear_wait_status_tma_ffma(s);
     const unsigned int code_tc = read_and_clear_wait_status_tf32(s);
     const unsigned int code_st = read_and_clear_wait_status_selftest(s);
+    const unsigned int code_at = read_and_clear_wait_status_attention_tc(s);
     if (code == 0) code = code_tc;
     if (code == 0) code = code_st;
+    if (code == 0) code = code_at;
     if (code != 0) {
         if (where_out) *where_out = (int)code;
         return SBGEMM_ERR_DEVICE_TIMEOUT;

@@ -5,7 +5,9 @@ Tolerance, from the products' convention: the scores carry 1e-5 of their
 magnitude (smag, the largest |alpha| sum_d |q k| of the row) plus a few
 units of 2^-24 for the scale and exp2, which perturbs each probability by
 at most delta = 1e-5 * smag + 8u relative; P V carries 1e-5 of sum_n P |V|
-(the oracle's weight W).  So |O - O_ref| <= (1e-5 + 2 delta) W + 4u |O_ref|."""
+(the oracle's weight W).  So |O - O_ref| <= (1e-5 + 2 delta) W + 4u |O_ref|.
+The TF32 tensor-core kernel rounds Q, K, P and V to tf32: the same bound with
+2e-3 in place of 1e-5 (the products' TF32 reading)."""
 
 import numpy as np
 import pytest
@@ -29,7 +31,7 @@ def torch():
     return t
 
 
-def run_attention(case, torch, O_init=None):
+def run_attention(case, torch, O_init=None, math=sg.MATH_FP32, force=sg.PATH_AUTO):
     dQ, dK, dV = (gu.to_device(op, torch) for op in (case.Q, case.K, case.V))
     dO = torch.from_numpy(case.O.storage.copy() if O_init is None else O_init.copy()).to("cuda")
     sg.sbgemm_attention(dQ.data_ptr() + 4 * case.Q.offset, case.Q.rs, case.Q.cs, case.Q.bs,
@@ -37,7 +39,8 @@ def run_attention(case, torch, O_init=None):
                         dV.data_ptr() + 4 * case.V.offset, case.V.rs, case.V.cs, case.V.bs,
                         dO.data_ptr() + 4 * case.O.offset, case.O.rs, case.O.cs, case.O.bs,
                         case.M, case.N, case.D, case.Dv, case.batch, case.alpha, case.causal,
-                        case.q_len, torch.cuda.current_stream().cuda_stream)
+                        case.q_len, torch.cuda.current_stream().cuda_stream, math=math,
+                        force_path=force)
     torch.cuda.synchronize()
     return dO.cpu().numpy()
 
@@ -47,7 +50,7 @@ def _sub(op, b):
     return wl.Operand(op.storage, op.offset + b * op.bs, op.rs, op.cs, 0)
 
 
-def check_attention(case, got_storage, batches=None):
+def check_attention(case, got_storage, batches=None, tol=1e-5):
     batches = range(case.batch) if batches is None else batches
     for b in batches:
         O, W, S = oracle.attention(_sub(case.Q, b), _sub(case.K, b), _sub(case.V, b), case.M, case.N,
@@ -55,8 +58,8 @@ def check_attention(case, got_storage, batches=None):
         o = case.O
         got = np.array(wl.Operand(got_storage, o.offset + b * o.bs, o.rs, o.cs, 0).view(1, case.M, case.Dv),
                        dtype=np.float64)
-        delta = 1e-5 * S[..., None] + 8 * U
-        lim = (1e-5 + 2 * delta) * W + 4 * U * np.abs(O)
+        delta = tol * S[..., None] + 8 * U
+        lim = (tol + 2 * delta) * W + 4 * U * np.abs(O)
         err = np.abs(got - O)
         bad = np.argwhere(~(err <= lim))
         assert bad.size == 0, (f"{case.name} batch {b}: {len(bad)} outputs outside the bound; first "
@@ -155,3 +158,79 @@ def test_attention_torch_helper_shared_kv(torch):
     want = p @ v.double()
     w = p @ v.double().abs()
     assert bool(((o.cpu().double() - want).abs() <= 2e-4 * w + 1e-6).all())
+
+
+# ---- TF32 tensor-core kernel (opt-in) -------------------------------------------
+
+TOL_TF32 = 2e-3
+# (M, N, batch, causal, q_len); row-major operands, which suit its tensor maps.
+TF32_SMALL = [
+    (100, 130, 3, 0, 0),          # ragged rows and keys
+    (192, 300, 2, 1, 192),        # causal, end-aligned
+    (384, 96, 2, 1, 96),          # 4 heads stacked as rows against one K (grouped query)
+    (1, 777, 3, 1, 1),            # one decode row against a long context
+    (70, 5, 2, 0, 0),             # fewer keys than one block
+    (256, 512, 2, 0, 0),          # whole blocks: 2 row blocks, 8 key blocks
+]
+
+
+@pytest.mark.parametrize("shape", TF32_SMALL, ids=[f"{s[0]}x{s[1]}x{s[2]}-c{s[3]}" for s in TF32_SMALL])
+def test_attention_tf32_small_against_oracle(torch, shape):
+    M, N, batch, causal, q_len = shape
+    rng = np.random.default_rng(M * 11 + N)
+    case = wl.random_attention(rng, M, N, 64, batch, "row", causal=causal, q_len=q_len)
+    got = run_attention(case, torch, math=sg.MATH_TF32, force=sg.PATH_TMA_TF32)
+    check_attention(case, got, tol=TOL_TF32)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
+@pytest.mark.parametrize("name", list(wl.ATTENTION))
+def test_attention_tf32_full_size_sampled_batches(torch, name):
+    case = wl.make_attention(name)
+    got = run_attention(case, torch, math=sg.MATH_TF32, force=sg.PATH_TMA_TF32)
+    check_attention(case, got, batches=[0, case.batch // 2, case.batch - 1], tol=TOL_TF32)
+
+
+def test_attention_tf32_saturated_scores_and_stale_output(torch):
+    """Scores of several hundred, and O's previous content (NaN) never read."""
+    rng = np.random.default_rng(12)
+    case = wl.random_attention(rng, 200, 333, 64, 2, "row", alpha=1.0, scale=3.0)
+    got = run_attention(case, torch, O_init=np.full(case.O.storage.shape, np.nan, np.float32),
+                        math=sg.MATH_TF32, force=sg.PATH_TMA_TF32)
+    assert np.isfinite(got).all()
+    check_attention(case, got, tol=TOL_TF32)
+
+
+def test_attention_tf32_other_layouts_fall_back_or_refuse(torch):
+    """K read transposed (no unit stride along the head dimension): with
+    math = TF32 the fp32 kernel runs (fp32 bound); forcing the tensor-core
+    kernel is refused."""
+    rng = np.random.default_rng(13)
+    case = wl.random_attention(rng, 128, 128, 64, 2, "mixed", causal=1, q_len=128)
+    got = run_attention(case, torch, math=sg.MATH_TF32)
+    check_attention(case, got)
+    with pytest.raises(sg.SbgemmError) as e:
+        run_attention(case, torch, math=sg.MATH_TF32, force=sg.PATH_TMA_TF32)
+    assert e.value.status == sg.SBGEMM_ERR_UNSUPPORTED
+    with pytest.raises(sg.SbgemmError) as e:
+        run_attention(case, torch, math=sg.MATH_FP32, force=sg.PATH_TMA_TF32)
+    assert e.value.status == sg.SBGEMM_ERR_INVALID_VALUE
+    with pytest.raises(sg.SbgemmError) as e:
+        run_attention(case, torch, math=sg.MATH_TF32, force=sg.PATH_GATHER_FFMA)
+    assert e.value.status == sg.SBGEMM_ERR_UNSUPPORTED
+
+
+def test_attention_tf32_torch_helper(torch):
+    """sg.attention(math=TF32) on tensors against float64 torch on the CPU."""
+    gen = torch.Generator().manual_seed(9)
+    q = torch.randn(4, 300, 64, generator=gen)
+    k = torch.randn(4, 260, 64, generator=gen)
+    v = torch.randn(4, 260, 64, generator=gen)
+    o = torch.empty(4, 300, 64, device="cuda")
+    sg.attention(q.cuda(), k.cuda(), v.cuda(), o, math=sg.MATH_TF32)
+    torch.cuda.synchronize()
+    p = torch.softmax((q.double() @ k.double().transpose(1, 2)) / 8.0, dim=-1)
+    want = p @ v.double()
+    w = p @ v.double().abs()
+    assert bool(((o.cpu().double() - want).abs() <= 2e-2 * w + 1e-6).all())
