@@ -304,23 +304,33 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             // Mask (keys past N, or past the row's causal position), scale to
             // the exp2 domain, and the running maximum.
             const int64_t n0 = (int64_t)j * BN;
-            float mx = -INFINITY;
+            // Keys c <= lim of the block are kept.  Eight partial maxima and
+            // sums, so that no chain runs through all 64 keys.
+            const int64_t last = (pos < p.N - 1 ? pos : p.N - 1) - n0;
+            const int lim = last < 0 ? -1 : (last >= BN ? BN - 1 : (int)last);
+            float part[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part[i] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < BN; ++c) {
-                const int64_t n = n0 + c;
-                s[c] = (n < p.N && n <= pos) ? s[c] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[c]);
+                s[c] = c <= lim ? s[c] * p.scale_log2 : -INFINITY;
+                part[c & 7] = fmaxf(part[c & 7], s[c]);
             }
+            const float mx = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                                   fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
             const float m_new = fmaxf(m_run, mx);
             // A row with no kept key so far keeps m = -inf; its terms stay 0.
             const float base = m_new == -INFINITY ? 0.0f : m_new;
             const float corr = exp2f(m_run - base);
-            float sum = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part[i] = 0.0f;
 #pragma unroll
             for (int c = 0; c < BN; ++c) {
                 s[c] = exp2f(s[c] - base);
-                sum += s[c];
+                part[c & 7] += s[c];
             }
+            const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
+                              ((part[4] + part[5]) + (part[6] + part[7]));
             l_run = l_run * corr + sum;
             m_run = m_new;
             // P_j to shared memory once P V_{j-1} has read P_{j-1}.
