@@ -234,3 +234,21 @@ def test_attention_tf32_torch_helper(torch):
     want = p @ v.double()
     w = p @ v.double().abs()
     assert bool(((o.cpu().double() - want).abs() <= 2e-2 * w + 1e-6).all())
+
+
+def test_attention_tf32_shared_kv_and_column_major_o(torch):
+    """TF32 kernel with K and V shared by every batch entry (zero batch
+    stride, grouped-query heads stacked as rows, causal per head) and O
+    written column-major (strided stores)."""
+    rng = np.random.default_rng(21)
+    T, H, batch = 160, 3, 2
+    M, N, D = H * T, T, 64
+    q = rng.standard_normal(batch * M * D).astype(np.float32)
+    k = rng.standard_normal(N * D).astype(np.float32)
+    v = rng.standard_normal(N * D).astype(np.float32)
+    case = wl.AttnCase("tf32_shared", wl.Operand(q, 0, D, 1, M * D), wl.Operand(k, 0, D, 1, 0),
+                       wl.Operand(v, 0, D, 1, 0),
+                       wl.Operand(np.zeros(batch * M * D, np.float32), 0, 1, M, M * D),
+                       M, N, D, D, batch, 0.125, 1, T)
+    got = run_attention(case, torch, math=sg.MATH_TF32, force=sg.PATH_TMA_TF32)
+    check_attention(case, got, tol=TOL_TF32)
