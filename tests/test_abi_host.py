@@ -326,3 +326,19 @@ def test_gather_k_pieces_planning():
     assert q["stream_k"] == sg.STREAM_K_NONE
     q = call_plan(A, B, C, M, N, K, 40, workspace=ws, workspace_bytes=big)
     assert q["stream_k"] == sg.STREAM_K_NONE
+
+
+def test_attention_ex_option_checks():
+    """sbgemm_attention_ex refuses options it cannot honour before touching the
+    device: a forced path other than the tensor-core one, the tensor-core path
+    without math = TF32, and non-zero reserved fields."""
+    q, k, v, o = BASE, BASE + (1 << 32), BASE + (2 << 32), BASE + (3 << 32)
+    args = (q, 64, 1, 128 * 64, k, 64, 1, 128 * 64, v, 64, 1, 128 * 64, o, 64, 1, 128 * 64,
+            128, 128, 64, 64, 2, 0.125, 0, 0, 0)
+    for math, force, want in ((sg.MATH_TF32, sg.PATH_GATHER_FFMA, sg.SBGEMM_ERR_UNSUPPORTED),
+                              (sg.MATH_FP32, sg.PATH_TMA_FFMA, sg.SBGEMM_ERR_UNSUPPORTED),
+                              (sg.MATH_FP32, sg.PATH_TMA_TF32, sg.SBGEMM_ERR_INVALID_VALUE),
+                              (7, sg.PATH_AUTO, sg.SBGEMM_ERR_INVALID_VALUE)):
+        with pytest.raises(sg.SbgemmError) as e:
+            sg.sbgemm_attention_ex(*args, math=math, force_path=force)
+        assert e.value.status == want, (math, force, e.value.status)
