@@ -500,7 +500,10 @@ def run_ours(args, world, rank, local, dist):
             bufs = tuple(torch.from_numpy(x).to(dev) for x in (c.A.storage, c.B.storage, c.C.storage))
             a = case_args(c, *bufs)
             row = {}
-            for label, kw in (("workspace", ws_kw), ("no_workspace", {})):
+            # "tf32": the opt-in tensor-core path, with the workspace when
+            # there is one (the weight gradients have both operands MN-major).
+            for label, kw in (("workspace", ws_kw), ("no_workspace", {}),
+                              ("tf32", dict(ws_kw, math=sg.MATH_TF32))):
                 if label == "workspace" and not kw:
                     continue
                 pl = sg.sbgemm_plan(*a[:16], c.accumulate, **kw)

@@ -96,10 +96,10 @@ enum {
                                      shared memory, FFMA register micro-tiles */
     SBGEMM_PATH_TMA_FFMA = 2,     /* unit-stride operands: TMA + mbarrier ring,
                                      FFMA register micro-tiles */
-    SBGEMM_PATH_TMA_TF32 = 3      /* unit-stride operands, at least one K-major
-                                     (an MN-major one is transposed in shared
-                                     memory): TMA + tcgen05.mma kind::tf32
-                                     with the accumulator in TMEM */
+    SBGEMM_PATH_TMA_TF32 = 3      /* unit-stride operands (an MN-major one is
+                                     transposed in shared memory): TMA +
+                                     tcgen05.mma kind::tf32 with the
+                                     accumulator in TMEM */
 };
 
 /* Operand layout classes reported by sbgemm_plan. */
@@ -213,9 +213,9 @@ SBGEMM_API int sbgemm(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
 
 /* As sbgemm, with the arithmetic and the kernel path chosen by `opt` (NULL =
  * defaults).  math = SBGEMM_MATH_TF32 opts in to the tensor cores; when the
- * operands cannot be fetched by TMA, or neither has its unit stride along K,
- * the planner falls back to strict fp32 unless the TF32 path was forced (then
- * SBGEMM_ERR_UNSUPPORTED). */
+ * operands cannot be fetched by TMA (each needs a unit stride along K or
+ * along its M / N index), the planner falls back to strict fp32 unless the
+ * TF32 path was forced (then SBGEMM_ERR_UNSUPPORTED). */
 SBGEMM_API int sbgemm_ex(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
               const float* B, int64_t rsB, int64_t csB, int64_t bsB,
               float* C, int64_t rsC, int64_t csC, int64_t bsC,

@@ -199,9 +199,8 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
 
     const bool tma_ok = p.K > 0 && plan->a_tma && plan->b_tma;
     // The tensor-core path reads its operands K-major (unit stride along K);
-    // one MN-major operand is transposed in shared memory on the way.
-    const bool tf32_ok = tma_ok && (plan->a_layout == SBGEMM_LAYOUT_K_MAJOR ||
-                                    plan->b_layout == SBGEMM_LAYOUT_K_MAJOR);
+    // an MN-major operand is transposed in shared memory on the way.
+    const bool tf32_ok = tma_ok;
     int path = o.force_path;
     if (path == SBGEMM_PATH_TMA_TF32 && !tf32_ok) return SBGEMM_ERR_UNSUPPORTED;
     if (path == SBGEMM_PATH_TMA_FFMA && !tma_ok) return SBGEMM_ERR_UNSUPPORTED;

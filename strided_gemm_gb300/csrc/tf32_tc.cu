@@ -54,32 +54,38 @@ constexpr int kBBytes = BN * BK * 4;         // 32 KB
 constexpr uint32_t kAccCols = BN;            // fp32 accumulator: one column per n
 constexpr uint32_t kTmemCols = 2 * kAccCols; // double-buffered accumulator
 constexpr int kEpiWarps = 4;
-constexpr int kTransWarps = 4;               // transposers of an MN-major operand
+constexpr int kTransWarps = 4;               // transposers of the MN-major operands
 constexpr int kBM128 = BM;                               // rows of a partial slot
 constexpr int64_t kSlotFloat4 = (int64_t)BM * BN / 4;    // one partial tile, in float4
 constexpr int kBox = 32 * 32;                // floats in one 32 x 32 raw box of an MN-major operand
 
 // Shared-memory plan by operand orientation.  MN: 0 both operands K-major;
-// 1 A MN-major (unit stride along M); 2 B MN-major (along N).  An MN-major
-// slice lands as raw 32 x 32 boxes (rows along K, 128-byte swizzle) in a ring
-// of its own, and the transposer warps rewrite it into the K-major swizzled
-// layout the MMAs read, in a ring of kTStages stages; the operand TMA brings
+// 1 A MN-major (unit stride along M); 2 B MN-major (along N); 3 both.  An
+// MN-major slice lands as raw 32 x 32 boxes (rows along K, 128-byte swizzle)
+// in a ring of its own (with both MN-major, A's boxes and then B's share one
+// raw stage), and the transposer warps rewrite it into the K-major swizzled
+// layout the MMAs read, in a ring of kTStages stages; an operand TMA brings
 // in K-major has a ring of kStages stages.  The load latency is what the
 // stages cover (each waits out about 1.1-1.3 us of it), so the TMA-fed rings
 // get the depth and the transposed ring, filled from shared memory, two
-// stages (3 transposed stages with 2 raw ones measured 11% slower).
+// stages (3 transposed stages with 2 raw ones measured 11% slower).  With
+// both operands MN-major a raw stage holds 48 KB and the shared memory has
+// room for four such stages: 2 raw and 2 transposed measured 8% faster than
+// 3 raw and 1 transposed (which makes the transposers wait on the MMAs).
 template <int MN>
 struct TCfg {
-    static constexpr bool kTA = MN == 1, kTB = MN == 2;
+    static constexpr bool kTA = MN == 1 || MN == 3, kTB = MN == 2 || MN == 3;
     static constexpr bool kTrans = kTA || kTB;
+    static constexpr bool kKRing = !(kTA && kTB);          // an operand comes in K-major
     static constexpr int kWarps = 2 + kEpiWarps + (kTrans ? kTransWarps : 0);
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kStages = 4;                      // TMA-fed K-major ring
     static constexpr int kTStages = kTrans ? 2 : 1;        // transposed ring
     static constexpr int kStagesA = kTA ? kTStages : kStages;
     static constexpr int kStagesB = kTB ? kTStages : kStages;
-    static constexpr int kRawRows = kTA ? BM : (kTB ? BN : 0);
-    static constexpr int kRawStages = kTA ? 3 : (kTB ? 2 : 0);
+    static constexpr int kRawRowsA = kTA ? BM : 0;         // A's rows lead a raw stage
+    static constexpr int kRawRows = kRawRowsA + (kTB ? BN : 0);
+    static constexpr int kRawStages = (kTA && kTB) ? 2 : (kTA ? 3 : (kTB ? 2 : 0));
     static constexpr int kStageBufs = kTrans ? 1 : 2;     // epilogue staging tiles per warp
     // Bytes the K-major operand copies bring into a stage.
     static constexpr uint32_t kKBytes = (kTA ? 0 : kABytes) + (kTB ? 0 : kBBytes);
@@ -110,6 +116,7 @@ struct TCfg {
     };
     static constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(kKRing == (kKBytes > 0), "the K-major ring carries an operand");
     static_assert(kRawBytes % 4096 == 0, "raw slices are whole 32 x 32 boxes");
 };
 
@@ -180,8 +187,8 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
         const int bb = p.b_bcast ? 0 : (int)tc.b;
         for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
             if constexpr (C::kTrans) {
-                // The MN-major operand: 32 x 32 boxes along M (A) or N (B), rows
-                // along K, into the raw ring.
+                // An MN-major operand: 32 x 32 boxes along M (A) or N (B), rows
+                // along K, into the raw ring (A's boxes first when both are).
                 const int r = (int)(i % R);
                 if (i >= (uint64_t)R && !mbar_wait(&sh.rempty[r], (uint32_t)(((i / R) - 1) & 1))) {
                     record_status(&g_wait_status, kWaitEmpty);
@@ -189,32 +196,38 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
                     break;
                 }
                 // Boxes wholly past a ragged edge are not fetched.
-                const int boxes = valid_boxes<C::kRawRows>(C::kTA ? p.M - tc.m0 : p.N - tc.n0);
-                mbar_arrive_expect_tx(&sh.rfull[r], (uint32_t)boxes * kBox * 4);
-                const CUtensorMap* tm = C::kTA ? ta : tb;
-                const int x0 = C::kTA ? (int)tc.m0 : (int)tc.n0;
-                const int bz = C::kTA ? ba : bb;
+                const int boxes_a = C::kTA ? valid_boxes<BM>(p.M - tc.m0) : 0;
+                const int boxes_b = C::kTB ? valid_boxes<BN>(p.N - tc.n0) : 0;
+                mbar_arrive_expect_tx(&sh.rfull[r], (uint32_t)(boxes_a + boxes_b) * kBox * 4);
 #pragma unroll 1
-                for (int j = 0; j < boxes; ++j)
-                    tma_load_3d(sh.raw[r] + j * kBox, tm, &sh.rfull[r], x0 + 32 * j, kt * BK, bz);
+                for (int j = 0; j < boxes_a; ++j)
+                    tma_load_3d(sh.raw[r] + j * kBox, ta, &sh.rfull[r], (int)tc.m0 + 32 * j, kt * BK, ba);
+                float* raw_b = sh.raw[r] + (C::kRawRowsA / 32) * kBox;
+#pragma unroll 1
+                for (int j = 0; j < boxes_b; ++j)
+                    tma_load_3d(raw_b + j * kBox, tb, &sh.rfull[r], (int)tc.n0 + 32 * j, kt * BK, bb);
             }
-            const int st = (int)(i % S);
-            if (i >= (uint64_t)S && !mbar_wait(&sh.empty[st], (uint32_t)(((i / S) - 1) & 1))) {
-                record_status(&g_wait_status, kWaitEmpty);
-                ok = false;
-                break;
+            if constexpr (C::kKRing) {
+                const int st = (int)(i % S);
+                if (i >= (uint64_t)S && !mbar_wait(&sh.empty[st], (uint32_t)(((i / S) - 1) & 1))) {
+                    record_status(&g_wait_status, kWaitEmpty);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sh.full[st], C::kKBytes);
+                if constexpr (!C::kTA) tma_load_3d(sh.a[st], ta, &sh.full[st], kt * BK, (int)tc.m0, ba);
+                if constexpr (!C::kTB) tma_load_3d(sh.b[st], tb, &sh.full[st], kt * BK, (int)tc.n0, bb);
             }
-            mbar_arrive_expect_tx(&sh.full[st], C::kKBytes);
-            if constexpr (!C::kTA) tma_load_3d(sh.a[st], ta, &sh.full[st], kt * BK, (int)tc.m0, ba);
-            if constexpr (!C::kTB) tma_load_3d(sh.b[st], tb, &sh.full[st], kt * BK, (int)tc.n0, bb);
         }
     }
     // Wait for the copies still landing.
-    for (uint64_t q = i > (uint64_t)S ? i - S : 0; q < i; ++q)
-        if (!mbar_wait(&sh.full[q % S], (uint32_t)((q / S) & 1))) {
-            record_status(&g_wait_status, kWaitDrain);
-            return;
-        }
+    if constexpr (C::kKRing) {
+        for (uint64_t q = i > (uint64_t)S ? i - S : 0; q < i; ++q)
+            if (!mbar_wait(&sh.full[q % S], (uint32_t)((q / S) & 1))) {
+                record_status(&g_wait_status, kWaitDrain);
+                return;
+            }
+    }
     if constexpr (C::kTrans) {
         for (uint64_t q = i > (uint64_t)R ? i - R : 0; q < i; ++q)
             if (!mbar_wait(&sh.rfull[q % R], (uint32_t)((q / R) & 1))) {
@@ -276,9 +289,9 @@ __device__ __forceinline__ void transpose_mn_slice(const float* raw, float* dst,
 }
 
 // Transposer warps: per slice, wait for the raw boxes and for the stage's
-// previous MMAs, rewrite the MN-major operand, order the writes before the
-// tensor cores' reads (async proxy), then signal the MMA lane and free the
-// raw slot.
+// previous MMAs, rewrite the MN-major operand (A's boxes, then B's, when both
+// are), order the writes before the tensor cores' reads (async proxy), then
+// signal the MMA lane and free the raw slot.
 template <int MN>
 __device__ __forceinline__ void transposer(typename TCfg<MN>::Smem& sh, const Params& p, int t,
                                            int lane) {
@@ -289,7 +302,8 @@ __device__ __forceinline__ void transposer(typename TCfg<MN>::Smem& sh, const Pa
     for (int64_t w = 0; w < n_items; ++w) {
         const Item itm = sh.sched.item(w, p.nk);
         const TileCoord tc = tile_coord(p, itm.tile);
-        const int boxes = valid_boxes<C::kRawRows>(C::kTA ? p.M - tc.m0 : p.N - tc.n0);
+        const int boxes_a = C::kTA ? valid_boxes<BM>(p.M - tc.m0) : 0;
+        const int boxes_b = C::kTB ? valid_boxes<BN>(p.N - tc.n0) : 0;
         for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
             const int r = (int)(i % R), ts = (int)(i % T);
             if (!mbar_wait(&sh.rfull[r], (uint32_t)((i / R) & 1))) {
@@ -300,7 +314,9 @@ __device__ __forceinline__ void transposer(typename TCfg<MN>::Smem& sh, const Pa
                 record_status(&g_wait_status, kWaitEmpty);
                 return;
             }
-            transpose_mn_slice<C::kRawRows>(sh.raw[r], C::kTA ? sh.a[ts] : sh.b[ts], t, boxes);
+            if constexpr (C::kTA) transpose_mn_slice<BM>(sh.raw[r], sh.a[ts], t, boxes_a);
+            if constexpr (C::kTB)
+                transpose_mn_slice<BN>(sh.raw[r] + (C::kRawRowsA / 32) * kBox, sh.b[ts], t, boxes_b);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -331,7 +347,7 @@ __device__ __forceinline__ void mma_issuer(typename TCfg<MN>::Smem& sh, uint32_t
         const uint32_t idesc = idesc_for(p.N, tile_coord(p, itm.tile).n0);
         for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
             const int st = (int)(i % S), ts = (int)(i % C::kTStages);
-            if (!mbar_wait(&sh.full[st], (uint32_t)((i / S) & 1)) ||
+            if ((C::kKRing && !mbar_wait(&sh.full[st], (uint32_t)((i / S) & 1))) ||
                 (C::kTrans && !mbar_wait(&sh.tdone[ts], (uint32_t)((i / C::kTStages) & 1)))) {
                 record_status(&g_wait_status, kWaitFull);
                 ok = false;
@@ -347,7 +363,7 @@ __device__ __forceinline__ void mma_issuer(typename TCfg<MN>::Smem& sh, uint32_t
                 const bool acc = kt > itm.kb || kk > 0;
                 mma_tf32(d, ad, bd, idesc, acc ? 1u : 0u);
             }
-            mma_commit(&sh.empty[st]);
+            if constexpr (C::kKRing) mma_commit(&sh.empty[st]);
             if constexpr (C::kTrans) mma_commit(&sh.tempty[ts]);
         }
         if (!ok) break;
@@ -843,7 +859,7 @@ cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cu
     // own orientation, which differs when the plan computes C^T).
     const bool a_mn = !(pr.K == 1 || pr.csA == 1);
     const bool b_mn = !(pr.K == 1 || pr.rsB == 1);
-    if (a_mn && b_mn) return cudaErrorInvalidValue;   // the planner never sends this here
+    if (a_mn && b_mn) return launch_mn<3>(pr, plan, stream);
     if (a_mn) return launch_mn<1>(pr, plan, stream);
     if (b_mn) return launch_mn<2>(pr, plan, stream);
     return launch_mn<0>(pr, plan, stream);

@@ -273,18 +273,26 @@ def test_split_k_pieces_planning():
     assert e.value.status == sg.SBGEMM_ERR_INVALID_VALUE
 
 
-def test_tf32_takes_one_mn_major_operand():
-    """TF32 reads operands K-major; one MN-major operand (A M-major or B
-    N-major) is transposed in shared memory, both MN-major fall back."""
+def test_tf32_takes_mn_major_operands():
+    """TF32 reads operands K-major; an MN-major operand (A M-major or B
+    N-major, or both) is transposed in shared memory.  Both MN-major is the
+    weight gradient G^T X and is planned as it stands (its transpose is
+    both MN-major as well)."""
     M, N, K = 1024, 768, 512
     A_k, A_m = rowmajor(BASE, M, K, 1), (BASE, 1, M, 0)
     B_k, B_n = (BASE + (1 << 32), 1, K, 0), rowmajor(BASE + (1 << 32), K, N, 1)
     C = rowmajor(BASE + (2 << 32), M, N, 1)
-    for A, B, tf32 in ((A_k, B_k, True), (A_m, B_k, True), (A_k, B_n, True), (A_m, B_n, False)):
+    for A, B in ((A_k, B_k), (A_m, B_k), (A_k, B_n), (A_m, B_n)):
         p = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32)
-        assert (p["path"] == sg.PATH_TMA_TF32) == tf32, (A, B, p)
+        assert p["path"] == sg.PATH_TMA_TF32, (A, B, p)
+    p = call_plan(A_m, B_n, C, M, N, K, 1, math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
+    assert p["a_layout"] == sg.LAYOUT_MN_MAJOR and p["b_layout"] == sg.LAYOUT_MN_MAJOR
+    assert (p["tile_m"], p["tile_n"]) == (128, 256), p   # not transposed
+    # A gathered A (no unit stride) still falls back, and refuses a forced TF32.
+    A_g = (BASE, 2, 2 * M, 0)
+    assert call_plan(A_g, B_n, C, M, N, K, 1, math=sg.MATH_TF32)["path"] != sg.PATH_TMA_TF32
     with pytest.raises(sg.SbgemmError) as e:
-        call_plan(A_m, B_n, C, M, N, K, 1, math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
+        call_plan(A_g, B_n, C, M, N, K, 1, math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
     assert e.value.status == sg.SBGEMM_ERR_UNSUPPORTED
 
 

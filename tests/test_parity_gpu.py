@@ -392,10 +392,11 @@ def test_linear_backward_helper(torch, workspace):
 
 # ---- TF32 tensor-core path (opt-in) -------------------------------------------
 
-# Both operands K-major, or one MN-major (transposed in shared memory): c4's V
-# and c5c's B are N-major, c5d's A is M-major.
+# Both operands K-major, one MN-major or both (transposed in shared memory):
+# c4's V and c5c's B are N-major, c5d's A is M-major, and the weight
+# gradients' G^T and X are M-major and N-major.
 TF32_WORKLOADS = ["c2a", "c2b", "c3", "c3gqa", "c4", "c5a", "c5b", "c5c", "c5d",
-                  "f1dxa", "f1dxb", "f4dist"]
+                  "f1dxa", "f1dwa", "f1dxb", "f1dwb", "f4dist"]
 
 
 @pytest.mark.parametrize("name", TF32_WORKLOADS)
@@ -411,14 +412,16 @@ TF32_SHAPES = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (130, 70, 257), (257, 129, 
                (128, 32, 256), (300, 1000, 520)]
 
 
-# (A, B): both K-major; A M-major with B K-major; A K-major with B N-major.
-TF32_LAYOUTS = [("row16", "col16"), ("col16", "col16"), ("row16", "row16")]
+# (A, B): both K-major; A M-major with B K-major; A K-major with B N-major;
+# both MN-major.
+TF32_LAYOUTS = [("row16", "col16"), ("col16", "col16"), ("row16", "row16"), ("col16", "row16")]
 
 
 @pytest.mark.parametrize("mkn", TF32_SHAPES, ids=[f"{m}x{k}x{n}" for m, k, n in TF32_SHAPES])
 @pytest.mark.parametrize("layouts", TF32_LAYOUTS, ids=["-".join(l) for l in TF32_LAYOUTS])
 def test_tf32_awkward_shapes(torch, mkn, layouts):
-    """Both operands K-major; zero batch strides, column-major C, ragged edges."""
+    """Every unit-stride orientation of A and B; zero batch strides,
+    column-major C, ragged edges."""
     M, K, N = mkn
     rng = np.random.default_rng(M * 31 + K * 7 + N)
     for i, (bsm, c_layout, acc, alpha) in enumerate([
@@ -436,14 +439,11 @@ def test_tf32_awkward_shapes(torch, mkn, layouts):
 
 def test_tf32_opt_in_falls_back_to_fp32(torch):
     """math=TF32 without a forced path serves operands the tensor-core path
-    does not take (both operands MN-major; strides TMA cannot fetch) with
-    strict fp32."""
+    does not take (strides TMA cannot fetch) with strict fp32."""
     rng = np.random.default_rng(21)
-    case = wl.random_strided(rng, 300, 260, 200, 2, "col16", "row16", values="real")   # both MN-major
     general = wl.random_strided(rng, 70, 90, 50, 2, "gap", "neg_row", values="real",
                                 accumulate=1, alpha=0.5)
-    for c, want_path in ((case, (sg.PATH_TMA_FFMA, sg.PATH_GATHER_FFMA)),
-                         (general, (sg.PATH_GATHER_FFMA,))):
+    for c, want_path in ((general, (sg.PATH_GATHER_FFMA,)),):
         plan = sg.sbgemm_plan(0x10000000 + 4 * c.A.offset, c.A.rs, c.A.cs, c.A.bs,
                               0x20000000 + 4 * c.B.offset, c.B.rs, c.B.cs, c.B.bs,
                               0x1000000000, c.C.rs, c.C.cs, c.C.bs,
@@ -455,12 +455,14 @@ def test_tf32_opt_in_falls_back_to_fp32(torch):
 
 
 TF32_STREAM_K_SHAPES = [
-    # (name, M, N, K, batch, accumulate); A row-major and B column-major (K-major)
+    # (name, M, N, K, batch, accumulate[, A layout, B layout]); by default A
+    # row-major and B column-major (both K-major)
     ("160_tiles_long_k", 2048, 2560, 4096, 1, 0),
     ("ragged_k", 2560, 2560, 4000, 1, 1),
     ("batched", 1024, 1024, 4096, 5, 1),
     ("320_tiles", 2048, 5120, 4096, 1, 0),
     ("few_tiles_pieces", 1024, 1024, 8192, 1, 1),      # 32 tiles: several pieces per tile
+    ("weight_grad_both_mn", 2560, 960, 8192, 1, 1, "col16", "row16"),   # dW = G^T X
 ]
 
 
@@ -469,9 +471,10 @@ def test_tf32_split_pieces_parity_and_determinism(torch, workspace, shape):
     """On the tensor cores a split tile's pieces accumulate independently and
     the tail adds the earlier ones in a fixed order: within the TF32 bound,
     identical from run to run; k_split = EXACT keeps the unsplit result."""
-    _, M, N, K, batch, acc = shape
+    _, M, N, K, batch, acc = shape[:6]
+    la, lb = shape[6:] if len(shape) > 6 else ("row16", "col16")
     rng = np.random.default_rng(M * 3 + N + K)
-    case = wl.random_strided(rng, M, N, K, batch, "row16", "col16", values="real",
+    case = wl.random_strided(rng, M, N, K, batch, la, lb, values="real",
                              accumulate=acc, alpha=0.75)
     kw = dict(math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
     first, plan = _run_ws(case, torch, workspace, kw)
@@ -500,7 +503,7 @@ def test_tf32_stream_k_integer_exact(torch, workspace):
     gu.check_points(case, first, n=4000, exact=True)
 
 
-@pytest.mark.parametrize("name", ["c3", "c3gqa", "c4", "c5a", "c5b", "c5c", "c5d"])
+@pytest.mark.parametrize("name", ["c3", "c3gqa", "c4", "c5a", "c5b", "c5c", "c5d", "f1dwa", "f1dwb"])
 def test_tf32_full_size_sampled(torch, name):
     case = wl.make(name, "real")
     assert _supported(case, sg.MATH_TF32, sg.PATH_TMA_TF32)
