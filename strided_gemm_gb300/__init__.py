@@ -370,7 +370,7 @@ def matmul(A, B, C, alpha: float = 1.0, accumulate: bool = False,
 
 
 def linear_backward(G, X, W, dX, dW, accumulate_dW: bool = False, stream=None,
-                    workspace=None, k_split: int = KSPLIT_ANY):
+                    workspace=None, k_split: int = KSPLIT_ANY, math: int = MATH_FP32):
     """Gradients of the linear layer Y = X W^T (X [T, in], W [out, in], upstream
     gradient G = dL/dY [T, out]), as two strided products that read the
     transposes through swapped strides, with no copy (the pages' "PyTorch
@@ -380,8 +380,10 @@ def linear_backward(G, X, W, dX, dW, accumulate_dW: bool = False, stream=None,
         dW = G^T X      [out, in] (A = G read with swapped strides; K = T)
     dW accumulates into the existing gradient when accumulate_dW is set.  With
     a workspace the long-K dW product may be split into independent K pieces
-    (deterministic; k_split = KSPLIT_EXACT keeps the unsplit rounding)."""
-    matmul(G, W, dX, stream=stream, workspace=workspace, k_split=k_split)
-    matmul(G.t(), X, dW, accumulate=accumulate_dW, stream=stream, workspace=workspace,
+    (deterministic; k_split = KSPLIT_EXACT keeps the unsplit rounding).
+    math = MATH_TF32 runs both on the tensor cores (dW's operands are both
+    MN-major and are transposed in shared memory)."""
+    matmul(G, W, dX, math=math, stream=stream, workspace=workspace, k_split=k_split)
+    matmul(G.t(), X, dW, accumulate=accumulate_dW, math=math, stream=stream, workspace=workspace,
            k_split=k_split)
     return dX, dW

@@ -368,9 +368,12 @@ def test_backward_products_full_size_with_workspace(torch, workspace, name):
     assert st == sg.SBGEMM_OK, where
 
 
-def test_linear_backward_helper(torch, workspace):
+@pytest.mark.parametrize("math", ["fp32", "tf32"])
+def test_linear_backward_helper(torch, workspace, math):
     """sg.linear_backward on torch tensors: dX = G W and dW += G^T X against
-    float64 torch on the CPU."""
+    float64 torch on the CPU, on either arithmetic path."""
+    m = sg.MATH_TF32 if math == "tf32" else sg.MATH_FP32
+    tol = gu.TOL_TF32 if math == "tf32" else gu.TOL_FFMA
     gen = torch.Generator().manual_seed(5)
     T, d_in, d_out = 2048, 384, 640
     X = torch.randn(T, d_in, generator=gen)
@@ -380,14 +383,14 @@ def test_linear_backward_helper(torch, workspace):
     dX = torch.empty(T, d_in, device="cuda")
     dW = dW0.clone().cuda()
     sg.linear_backward(G.cuda(), X.cuda(), W.cuda(), dX, dW, accumulate_dW=True,
-                       workspace=workspace)
+                       workspace=workspace, math=m)
     torch.cuda.synchronize()
     want_dX = G.double() @ W.double()
     want_dW = dW0.double() + G.double().t() @ X.double()
     bound_dX = G.double().abs() @ W.double().abs()
     bound_dW = dW0.double().abs() + G.double().abs().t() @ X.double().abs()
-    assert bool(((dX.cpu().double() - want_dX).abs() <= gu.TOL_FFMA * bound_dX).all())
-    assert bool(((dW.cpu().double() - want_dW).abs() <= gu.TOL_FFMA * bound_dW).all())
+    assert bool(((dX.cpu().double() - want_dX).abs() <= tol * bound_dX).all())
+    assert bool(((dW.cpu().double() - want_dW).abs() <= tol * bound_dW).all())
 
 
 # ---- TF32 tensor-core path (opt-in) -------------------------------------------
