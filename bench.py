@@ -454,8 +454,8 @@ def run_ours(args, world, rank, local, dist):
                "steps": n_e2e, "ms_per_step": round(e_ms / n_e2e, 3),
                "copies": "pinned host buffers, two copy streams overlapping the products"}
 
-    # The opt-in tensor-core path on the same products (operands that are not
-    # K-major fall back to strict fp32 and are reported as such).
+    # The opt-in tensor-core path on the same products (operands TMA cannot
+    # fetch fall back to strict fp32 and are reported as such).
     tf32 = None
     if not args.no_tf32 and math == sg.MATH_FP32:
         tf32 = {"per_product": {}}
