@@ -301,23 +301,39 @@ SBGEMM_API int sbgemm_plan(const float* A, int64_t rsA, int64_t csA, int64_t bsA
  * queried. */
 SBGEMM_API int sbgemm_workspace_bytes(int device, size_t* bytes);
 
-/* The strict fp32 product for callers that cannot allocate device memory.
- * The paper has no counterpart: it exists because the stream-K schedule needs
- * scratch that sbgemm_ex takes from its caller, and some callers cannot make
- * any (code running under CUDA graph capture, plugins given only their input
- * and output buffers, loops that must not pay cudaMalloc's synchronisation,
- * runtimes whose allocator owns all device memory).
+/* Size in bytes of sbgemm_noalloc's scratch array (20 MiB + 4 KiB). */
+#define SBGEMM_NOALLOC_SCRATCH_BYTES ((size_t)20 * 1024 * 1024 + 4096)
+
+/* The fp32 product for callers that cannot allocate device memory.
+ * The paper has no counterpart: it exists because the stream-K schedule (and
+ * the K pieces of small products) needs scratch that sbgemm_ex takes from its
+ * caller, and some callers cannot make any (code running under CUDA graph
+ * capture, plugins given only their input and output buffers, loops that
+ * must not pay cudaMalloc's synchronisation, runtimes whose allocator owns
+ * all device memory).
  *
- * Arguments, layout and errors are those of sbgemm.  The scratch is a
- * file-scope device array of 20 MiB + 4 KiB inside the library (room for the
- * schedule on devices of up to 160 SMs), created when the library's module is
- * loaded and held on every GPU that loads the library until the process
- * exits.  Nothing is allocated per call: no cudaMalloc, cudaFree or
- * allocating library routine runs.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call shares the one
- * array and the schedule clears its flags on `stream` before each launch, so
- * calls that overlap on the GPU (different streams, or different host
+ * Arguments, layout and errors are those of sbgemm.  The call is sbgemm_ex
+ * with math = FP32, the automatic path, k_split = SBGEMM_KSPLIT_ANY and the
+ * library's scratch as the workspace, so its results are bit-identical to
+ * sbgemm_ex given those options and a workspace of
+ * SBGEMM_NOALLOC_SCRATCH_BYTES.  Against sbgemm (no workspace) they can
+ * differ in rounding, within the fp32 bound, for the products the planner
+ * cuts into independent K pieces (few output tiles with a long K, or small
+ * products on the gather path): those pieces are summed in a fixed order
+ * rather than in one k-ordered chain.
+ *
+ * The scratch is a file-scope device array of SBGEMM_NOALLOC_SCRATCH_BYTES
+ * inside the library (room for the schedule on devices of up to 160 SMs),
+ * created when the library's module is loaded and held on every GPU that
+ * loads the library until the process exits.  Nothing is allocated per call:
+ * no cudaMalloc, cudaFree or allocating library routine runs.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture
+ * (a first call on a capturing stream returns SBGEMM_ERR_CUDA without
+ * touching the stream, and a failed lookup is retried by the next call).
+ * Every call shares the one array, which keeps the last call's contents; the
+ * schedule clears its flags and counters on `stream` before each launch.
+ * Calls that overlap on the GPU (different streams, or different host
  * threads) race on the scratch and must be serialised by the caller.
  * Returns SBGEMM_ERR_UNSUPPORTED if the current device would need more
  * scratch than the array holds (more than 160 SMs). */

@@ -23,6 +23,13 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "sbgemm_ref.c")
 _LIB_PATH = os.path.join(_HERE, "libsbgemm_ref.so")
+# A build with AddressSanitizer and UndefinedBehaviorSanitizer, loaded instead
+# of the plain one when SBGEMM_ORACLE_SANITIZE=1 (the process must then start
+# with the sanitizer runtimes preloaded, as tests/test_oracle_sanitized.py
+# arranges).
+_SAN_LIB_PATH = os.path.join(_HERE, "libsbgemm_ref_san.so")
+SANITIZE_FLAGS = ["-fsanitize=address,undefined", "-fno-sanitize-recover=all",
+                  "-fno-omit-frame-pointer", "-g"]
 _lock = threading.Lock()
 _lib = None
 
@@ -30,14 +37,19 @@ _i64 = ctypes.c_int64
 _fp = ctypes.c_void_p
 
 
-def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+def build(force: bool = False, src: str = _SRC, out: str | None = None,
+          sanitize: bool = False) -> str:
     """Compile the oracle with gcc.  Contraction of a*b+c into fused
     multiply-adds is switched off so the fp64 arithmetic is the same on every
-    host architecture."""
+    host architecture.  ``sanitize`` adds AddressSanitizer and
+    UndefinedBehaviorSanitizer (any report aborts the process)."""
+    if out is None:
+        out = _SAN_LIB_PATH if sanitize else _LIB_PATH
     if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
         tmp = out + f".tmp{os.getpid()}"
         subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                        "-ffp-contract=off", "-fno-fast-math", "-o", tmp, src, "-lm"],
+                        "-ffp-contract=off", "-fno-fast-math"] +
+                       (SANITIZE_FLAGS if sanitize else []) + ["-o", tmp, src, "-lm"],
                        check=True)
         os.replace(tmp, out)
     return out
@@ -71,7 +83,8 @@ def load(path: str | None = None):
         return _bind(path)
     with _lock:
         if _lib is None:
-            _lib = _bind(build())
+            san = os.environ.get("SBGEMM_ORACLE_SANITIZE") == "1"
+            _lib = _bind(build(sanitize=san))
         return _lib
 
 

@@ -28,7 +28,7 @@ __all__ = [
     "sbgemm_attention", "sbgemm_attention_ex", "attention",
     "ACT_NONE", "ACT_RELU", "ACT_SIGMOID", "ACT_SILU", "ACT_GELU_TANH", "ACT_GELU_ERF",
     "ACTIVATIONS", "KSPLIT_ANY", "KSPLIT_EXACT", "KSPLIT_NONE", "STREAM_K_NONE",
-    "STREAM_K_CHAINED", "STREAM_K_PIECES",
+    "STREAM_K_CHAINED", "STREAM_K_PIECES", "NOALLOC_SCRATCH_BYTES",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -59,6 +59,8 @@ ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "sigmoid": ACT_SIGMOID, "silu
                "gelu_tanh": ACT_GELU_TANH, "gelu_erf": ACT_GELU_ERF}
 SELFTEST_MBARRIER, SELFTEST_FLAG = 1, 2
 KSPLIT_ANY, KSPLIT_EXACT, KSPLIT_NONE = 0, 1, 2
+# Bytes of sbgemm_noalloc's static scratch (SBGEMM_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024 + 4096
 STREAM_K_NONE, STREAM_K_CHAINED, STREAM_K_PIECES = 0, 1, 2
 
 
@@ -184,9 +186,11 @@ def sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
 
 def sbgemm_noalloc(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                    M, N, K, batch, alpha, accumulate, stream=0) -> None:
-    """As sbgemm, for callers that cannot allocate device memory: the scratch
-    of the stream-K schedule is the library's own static device array (shared
-    by all calls, so calls that overlap on the GPU must be serialised)."""
+    """As sbgemm_ex with k_split = KSPLIT_ANY, for callers that cannot
+    allocate device memory: the scratch of the stream-K schedule and of the K
+    pieces is the library's own static device array of NOALLOC_SCRATCH_BYTES
+    (shared by all calls, so calls that overlap on the GPU must be
+    serialised).  Make the first call on a device outside stream capture."""
     st = load().sbgemm_noalloc(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
                                M, N, K, batch, float(alpha), int(bool(accumulate)),
                                stream or None)

@@ -54,7 +54,9 @@ int tma_ffma_pick_variant(const Problem& p, int sm_count) {
 size_t tma_ffma_workspace_bytes(int sm_count) {
     // One partial tile per CTA (every thread's 64 accumulator pairs) and one
     // flag word per CTA; the same for every tile shape (256 threads x 128).
-    return (size_t)sm_count * kThreads * 64 * sizeof(float2) + (size_t)sm_count * sizeof(unsigned int);
+    static_assert(kWorkspaceBytesPerSm == (size_t)kThreads * 64 * sizeof(float2) + sizeof(unsigned int),
+                  "one partial tile of this kernel's accumulators and one flag per CTA");
+    return (size_t)sm_count * kWorkspaceBytesPerSm;
 }
 
 // Data-parallel for all but the last one or two waves, whose K slices are

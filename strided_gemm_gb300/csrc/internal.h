@@ -104,6 +104,10 @@ struct TmaFfmaConfig { int bm, bn, bk, stages, threads; };
 int tma_ffma_config_count();
 TmaFfmaConfig tma_ffma_config(int variant);
 int tma_ffma_pick_variant(const Problem& p, int sm_count);
+// Stream-K scratch per SM (one CTA each): one tile of partial sums, kept as
+// the 64 accumulator pairs of each of the 256 threads of a TMA FFMA CTA (the
+// TF32 kernel's 128 x 256 fp32 tile is the same size), plus one flag word.
+constexpr size_t kWorkspaceBytesPerSm = (size_t)256 * 64 * 2 * sizeof(float) + sizeof(unsigned int);
 // Bytes of workspace the stream-K schedule needs on a device with sm_count SMs.
 size_t tma_ffma_workspace_bytes(int sm_count);
 // Fills plan.ctas / stream_k / dp_tiles / k_slices for the chosen variant.

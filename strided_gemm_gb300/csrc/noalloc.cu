@@ -1,8 +1,9 @@
 // sbgemm_noalloc: the product for callers that cannot allocate device memory.
 //
 // The stream-K schedule of the TMA FFMA kernel needs scratch (partial sums
-// of split tiles and their ready flags).  sbgemm_ex takes that scratch from
-// the caller.  Some callers have no way to provide it:
+// of split tiles and their ready flags), and so do the gather kernel's K
+// pieces of small products.  sbgemm_ex takes that scratch from the caller.
+// Some callers have no way to provide it:
 //  - code that runs while a CUDA graph is being captured, where cudaMalloc
 //    is not allowed;
 //  - a plugin that the host application hands only its input and output
@@ -10,10 +11,10 @@
 //  - a latency-critical loop that must not pay cudaMalloc's implicit
 //    synchronisation;
 //  - a runtime whose allocator owns all device memory.
-// This entry point gives them the same kernel with scratch that belongs to the
-// library: a file-scope array in device memory, created once when the module
-// is loaded and held by every GPU that loads the library until the process
-// exits.
+// This entry point gives them the same kernels with scratch that belongs to
+// the library: a file-scope array in device memory, created once when the
+// module is loaded and held by every GPU that loads the library until the
+// process exits.
 #include <cuda_runtime.h>
 
 #include <array>
@@ -28,29 +29,44 @@ namespace {
 // Capacity: the stream-K scratch of a device with up to 160 SMs (one fp32
 // partial tile per SM plus one flag word per SM); 20 MiB + 4 KiB.
 constexpr int kNoAllocMaxSms = 160;
-constexpr size_t kNoAllocScratchBytes = (size_t)20 * 1024 * 1024 + 4096;
+constexpr size_t kNoAllocScratchBytes = SBGEMM_NOALLOC_SCRATCH_BYTES;
 
-static_assert(kNoAllocScratchBytes >= (size_t)kNoAllocMaxSms * (256 * 64 * 8 + 4),
-              "one partial tile (256 threads x 64 float pairs) and one flag per SM");
+static_assert(kNoAllocScratchBytes >= (size_t)kNoAllocMaxSms * kWorkspaceBytesPerSm,
+              "the schedule's scratch for a device of kNoAllocMaxSms SMs");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::array<std::once_flag, kMaxDevices> g_once;
-std::array<void*, kMaxDevices> g_scratch{};
-std::array<cudaError_t, kMaxDevices> g_scratch_err{};
+std::mutex g_lookup_mutex;
+std::array<void*, kMaxDevices> g_scratch{};   // written under the mutex, once non-null never again
 
-// Device address of the scratch array on the current device.  In host code
-// the array's name is only a host-side handle, so the address is looked up
-// once per device, with that device current.
-void* scratch_address(int dev) {
-    std::call_once(g_once[dev], [dev] {
-        void* p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        g_scratch[dev] = p;
-        if (g_scratch_err[dev] != cudaSuccess) cudaGetLastError();
-    });
-    return g_scratch_err[dev] == cudaSuccess ? g_scratch[dev] : nullptr;
+// Device address of the scratch array on the current device, or nullptr if
+// it could not be looked up.  In host code the array's name is only a
+// host-side handle, so the address is looked up with the device current.
+// Only a successful lookup is kept: a failed one (say, a transient error) is
+// retried by the next call.  A lookup may load the library's module on the
+// device, which a stream being captured must not see, so the first call on a
+// device is refused while `stream` is capturing.
+int scratch_address(int dev, cudaStream_t stream, void** out) {
+    std::lock_guard<std::mutex> lock(g_lookup_mutex);
+    if (g_scratch[dev]) {
+        *out = g_scratch[dev];
+        return SBGEMM_OK;
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return SBGEMM_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return SBGEMM_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return SBGEMM_ERR_CUDA;
+    }
+    g_scratch[dev] = p;
+    *out = p;
+    return SBGEMM_OK;
 }
 
 }  // namespace
@@ -73,11 +89,13 @@ extern "C" int sbgemm_noalloc(const float* A, int64_t rsA, int64_t csA, int64_t 
     // A device with more SMs than the array was sized for would need more
     // scratch than it holds.
     if (need > sbg::kNoAllocScratchBytes) return SBGEMM_ERR_UNSUPPORTED;
-    void* scratch = sbg::scratch_address(dev);
-    if (!scratch) return SBGEMM_ERR_CUDA;
+    void* scratch = nullptr;
+    st = sbg::scratch_address(dev, static_cast<cudaStream_t>(stream), &scratch);
+    if (st != SBGEMM_OK) return st;
     sbgemm_options o{};
     o.math = SBGEMM_MATH_FP32;
     o.force_path = SBGEMM_PATH_AUTO;
+    o.k_split = SBGEMM_KSPLIT_ANY;
     o.workspace = scratch;
     o.workspace_bytes = sbg::kNoAllocScratchBytes;
     return sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,

@@ -58,6 +58,8 @@ constexpr int kTransWarps = 4;               // transposers of the MN-major oper
 constexpr int kBM128 = BM;                               // rows of a partial slot
 constexpr int64_t kSlotFloat4 = (int64_t)BM * BN / 4;    // one partial tile, in float4
 constexpr int kBox = 32 * 32;                // floats in one 32 x 32 raw box of an MN-major operand
+static_assert((size_t)kSlotFloat4 * sizeof(float4) + sizeof(unsigned int) == kWorkspaceBytesPerSm,
+              "a partial tile and a flag per CTA fit the workspace sbgemm_workspace_bytes reports");
 
 // Shared-memory plan by operand orientation.  MN: 0 both operands K-major;
 // 1 A MN-major (unit stride along M); 2 B MN-major (along N); 3 both.  An

@@ -43,6 +43,18 @@ def test_library_exports_every_declared_symbol():
     assert exported == set(header_functions()), exported
 
 
+def test_noalloc_scratch_size_matches_header():
+    # The binding's copy of SBGEMM_NOALLOC_SCRATCH_BYTES (the size the no-alloc
+    # test gives sbgemm_ex's workspace to reproduce sbgemm_noalloc bit for bit).
+    src = open(os.path.join(ROOT, "include", "sbgemm.h")).read()
+    m = re.search(r"#define SBGEMM_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) \* (\d+) \* (\d+) \+ (\d+)\)", src)
+    assert m, "macro not found"
+    a, b, c, d = (int(x) for x in m.groups())
+    assert a * b * c + d == sg.NOALLOC_SCRATCH_BYTES
+    # Room for the stream-K scratch of 160 SMs: 256 threads x 64 float pairs + a flag each.
+    assert sg.NOALLOC_SCRATCH_BYTES >= 160 * (256 * 64 * 8 + 4)
+
+
 def test_status_strings_and_version():
     assert sg.sbgemm_status_string(0) == "SBGEMM_OK"
     assert sg.sbgemm_status_string(3) == "SBGEMM_ERR_OUTPUT_OVERLAP"
