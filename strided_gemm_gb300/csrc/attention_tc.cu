@@ -4,33 +4,51 @@
 // section "What's basic about it": three steps with the scores in global
 // memory, which a fused kernel avoids).
 //
-// One CTA per 128 query rows of one batch entry, head dimension 64, keys in
-// blocks of 64.  Per block j:
-//   S_j  = Q K_j^T   tcgen05.mma kind::tf32, M 128 x N 64 x K 64, into TMEM
-//   P_j  = exp2(alpha log2(e) S_j - m)   one thread per query row, read from
-//          TMEM with tcgen05.ld, the running maximum m and sum l in registers,
-//          written to shared memory as the next MMA's K-major operand
-//   PV_j = P_j V_j   M 128 x N 64 x K 64, into TMEM
-//   O    = O exp2(m_old - m_new) + PV_j   in the row thread's registers
-// and O / l is stored at the end.  Roles, all waits bounded (a timeout records
-// a status code and returns):
-//   warp 0       TMA: Q once; K_j (two 128-byte swizzled boxes of 32 along
-//                the head dimension) and V_j (four raw 32 x 32 boxes) into a
-//                2-stage ring;
-//   warp 1       one lane issues the MMAs: S_0, then S_{j+1} ahead of PV_j, so
-//                the next block's scores are ready when its softmax starts;
-//   warps 2-5    softmax and output, one TMEM lane quarter each;
-//   warps 6-7    rewrite V_j (rows along the keys) into V_j^T with rows along
-//                the values, the K-major layout P V's B operand takes
-//                (4 x 4 quads, conflict-free under the swizzle).
-// S and PV are double-buffered in TMEM (4 x 64 columns).  The adding of PV_j
-// into O waits until P_{j+1} is written, so PV_j overlaps the next softmax.
+// One CTA per 256 query rows of one batch entry: two tiles of 128 rows (the
+// MMA's M) that share every K and V block, head dimension 64, keys in blocks
+// of 128.  Per block j and tile t:
+//   S_tj = Q_t K_j^T   tcgen05.mma kind::tf32, M 128 x N 128 x K 64, into TMEM
+//   P_tj = exp2(alpha log2(e) S_tj - m_t)   one thread per query row: a pass
+//          over the row's 128 scores (tcgen05.ld) for the block maximum, then
+//          the exponentials, written back over S_tj (tcgen05.st); the row sum
+//          l_t in registers
+//   O_t += P_tj V_j   M 128 x N 64 x K 128, A = P_tj from TMEM, accumulated in
+//          TMEM by the MMA
+// and O_t / l_t is stored at the end.  The reference maximum m_t of a row is
+// raised only when a block's maximum exceeds it by more than 8 (a factor of
+// 2^8): then O_t and l_t are scaled by exp2(m_old - m_new), O_t in TMEM by the
+// row's own thread.  Between raises the exponentials stay below 2^8, and O / l
+// is the same function either way.
+//
+// The MMA lane issues, per block: P V_0, then (once P V_0 has read P_0) the
+// scores of tile 0's next block, then the same for tile 1.  So each tile's
+// softmax runs while the tensor cores work on the other tile, and since the
+// next scores of a tile are issued only after its P V, they also tell its
+// softmax that O_t is settled.  Measured on this GPU, a tcgen05.mma issue
+// blocks until the one before it is nearly done, and a branch or wait between
+// two MMAs costs the tensor pipe as much as an N = 64 MMA: hence 128-key
+// blocks (N = 128 score MMAs, half the instructions per key of N = 64, and
+// each lane's waits and commits spread over twice the keys) and straight-line
+// MMA sequences with every operand one add away.
+// Roles (12 warps), all waits bounded (a timeout records a status code and
+// the role leaves its loop):
+//   warp 0       TMA: both Q tiles once; K_j (two 128-byte swizzled boxes of
+//                32 along the head dimension) and V_j (eight raw 32 x 32
+//                boxes) into a 2-stage ring;
+//   warp 1       one lane issues the MMAs;
+//   warps 2-3    rewrite V_j (rows along the keys) into V_j^T with rows along
+//                the values, the K-major layout P V's B operand takes (4 x 4
+//                quads, conflict-free under the swizzle);
+//   warps 4-7    softmax of tile 0, one TMEM lane quarter each;
+//   warps 8-11   softmax of tile 1.
+// TMEM: S / P (2 tiles x 128 columns) and O (2 x 64).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 
 #include "attention_tc.h"
 #include "ptx.cuh"
@@ -39,36 +57,49 @@ namespace sbg {
 namespace {
 
 constexpr int kD = 64;               // head dimension of Q, K and V
-constexpr int BM = 128;              // query rows per CTA (the MMA's M)
-constexpr int BN = 64;               // keys per block
 constexpr int kAtom = 32;            // fp32 values in one 128-byte swizzled row
+constexpr int kDA = kD / kAtom;      // atoms along the head dimension
+constexpr int BM = 128;              // query rows per tile (the MMA's M)
+constexpr int kTiles = 2;            // query tiles per CTA, sharing each K and V block
+constexpr int BN = 128;              // keys per block
+constexpr int kKA = BN / kAtom;      // key atoms per block
 constexpr int kMmaK = 8;             // tf32 elements per MMA
 constexpr int kStages = 2;           // K and raw V blocks in flight
-constexpr int kSoftWarps = 4, kTransWarps = 2;   // 8 warps: up to 255 registers a thread
-constexpr int kWarps = 2 + kSoftWarps + kTransWarps;
+constexpr int kSoftWarps = 4;        // per tile: one TMEM lane quarter each
+constexpr int kTransWarps = 2;
+constexpr int kWarpSoft = 4;         // first softmax warp
+constexpr int kWarps = kWarpSoft + kTiles * kSoftWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr int kBox = 32 * 32;
-constexpr uint32_t kTmemCols = 256;  // S[2], PV[2]
-constexpr uint32_t kColS = 0, kColPV = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;                         // S / P [t] at t * BN
+constexpr uint32_t kColO = kTiles * BN;               // O[t] at kColO + t * kD
+static_assert(kColO + kTiles * kD <= kTmemCols, "TMEM columns");
+static_assert((kWarpSoft % 4) == 0 && kSoftWarps == 4, "each tile's softmax warps cover the four lane quarters");
+static_assert(kTiles == 2, "the softmax warps pick their tile's block count from two");
+static_assert(kD % 32 == 0 && BN == 128, "32-column TMEM transfers; 128-key blocks in two 64-column halves");
+constexpr float kRaise = 8.0f;       // log2 headroom before the reference maximum is raised
 
-// Instruction descriptor, kind::tf32: D fp32, A and B tf32 K-major, N 64
-// (both products), M 128.
-constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptors, kind::tf32: D fp32, A and B tf32 K-major, M 128;
+// N = BN for the scores, kD for P V.
+constexpr uint32_t idesc(int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+constexpr uint32_t kIdescS = idesc(BN), kIdescPV = idesc(kD);
 
 struct Smem {
-    alignas(1024) float q[2][BM * kAtom];           // Q, K-major: head-dim atoms 0-31, 32-63
-    alignas(1024) float k[kStages][2][BN * kAtom];  // K_j, K-major, same atoms
-    alignas(1024) float vraw[kStages][4][kBox];     // V_j: box (key half h, value half g) at 2h + g
-    alignas(1024) float vt[2][2][kD * kAtom];       // V_j^T: rows along the values, key atoms
-    alignas(1024) float p[2][BM * kAtom];           // P_j, K-major: key atoms 0-31, 32-63
+    alignas(1024) float q[kTiles][kDA][BM * kAtom];       // Q tiles, K-major, head-dim atoms
+    alignas(1024) float k[kStages][kDA][BN * kAtom];      // K_j, K-major, same atoms
+    alignas(1024) float vraw[kStages][kKA * kDA][kBox];   // V_j: box (key atom h, value atom g) at h kDA + g
+    alignas(1024) float vt[kKA][kD * kAtom];              // V_j^T: rows along the values, key atoms
     uint64_t q_full;
     uint64_t k_full[kStages], k_empty[kStages];
     uint64_t v_full[kStages], v_empty[kStages];
-    uint64_t vt_full[2], vt_empty[2];
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, p_empty;
-    uint64_t pv_full[2], pv_empty[2];
+    uint64_t vt_full, vt_empty;
+    uint64_t s_full[kTiles];      // a tile's scores of the current block are in TMEM
+    uint64_t p_full[kTiles];      // a tile's P of the current block is in TMEM
+    uint64_t pv_done[kTiles];     // a tile's P V has read P and added into O
+    uint64_t o_done[kTiles];      // a tile's last P V is done
     uint64_t mma_done;
     uint32_t tmem_base;
 };
@@ -86,18 +117,34 @@ struct Params {
     int64_t q_len;
     int bq, bk, bv;                  // batch coordinate follows blockIdx.x (else 0: broadcast)
     int o_vec;                       // O rows unit-stride and 16-byte aligned
+    int o_tma;                       // O goes out through its tensor map
+    int bo;                          // O's batch coordinate follows blockIdx.x
 };
 
-// Rewrites one key atom of V_j: two raw boxes (32 keys x 32 values each, the
-// value halves) into V_j^T rows 0..63 (values) x 32 keys, K-major 128-byte
-// swizzle.  A quarter-warp's quads hit 8 distinct 16-byte chunks on both the
-// loads and the stores.
+// Keys [0, n_end) a tile of rows starting at m0 needs: all of them, or
+// (causal) those up to its rows' last position.  0 when the tile holds no row.
+__device__ __forceinline__ int tile_blocks(const Params& p, int64_t m0) {
+    if (m0 >= p.M) return 0;
+    int64_t n_end = p.N;
+    if (p.causal) {
+        const int64_t m_last = (m0 + BM - 1 < p.M ? m0 + BM - 1 : p.M - 1);
+        const int64_t r0 = m0 % p.q_len;
+        const bool wraps = r0 + (m_last - m0) >= p.q_len;
+        n_end = (wraps ? p.N - 1 : (m_last % p.q_len) + p.N - p.q_len) + 1;
+    }
+    return (int)((n_end + BN - 1) / BN);
+}
+
+// Rewrites one key atom of V_j: kDA raw boxes (32 keys x 32 values each) into
+// V_j^T rows 0..kD-1 (values) x 32 keys, K-major 128-byte swizzle.  A
+// quarter-warp's quads hit 8 distinct 16-byte chunks on both the loads and
+// the stores.
 __device__ __forceinline__ void transpose_atom(const float* raw, float* dst, int t) {
-    constexpr int kQuads = kD / 4 * (kAtom / 4);     // 128: two per transposer thread
+    constexpr int kQuads = kD / 4 * (kAtom / 4);
 #pragma unroll
     for (int q = t; q < kQuads; q += kTransWarps * 32) {
         const int kq = ((q >> 2) & 1) | (((q ^ (q >> 1) ^ (q >> 3)) & 1) << 1) | (((q >> 4) & 1) << 2);
-        const int mq = (q & 3) | ((q >> 5) << 2);    // 4-row group of values, 0..15
+        const int mq = (q & 3) | ((q >> 5) << 2);    // 4-row group of values
         const float* box = raw + (mq >> 3) * kBox;
         const int mc = mq & 7;
         float4 v[4];
@@ -118,38 +165,51 @@ __device__ __forceinline__ void transpose_atom(const float* raw, float* dst, int
     }
 }
 
-// The 8 MMAs (K = 64 in steps of 8) of one 128 x 64 x 64 product whose
-// operands are two 32-wide K atoms each.
-__device__ __forceinline__ void mma_128x64x64(uint32_t d, const float* a0, const float* a1,
-                                              const float* b0, const float* b1) {
+// The scores of one tile: D = Q_t K_j^T, A (Q_t) and B (K_j) in 32-wide
+// K-major swizzled atoms in shared memory (descriptor low words a_lo, b_lo);
+// kD / 8 MMAs in straight-line code.
+__device__ __forceinline__ void mma_scores(uint32_t d, uint32_t a_lo, uint32_t b_lo) {
+    constexpr uint32_t kAAtom = (uint32_t)(BM * kAtom * 4) >> 4;   // next atom, in descriptor units
+    constexpr uint32_t kBAtom = (uint32_t)(BN * kAtom * 4) >> 4;
 #pragma unroll
-    for (int kk = 0; kk < kD / kMmaK; ++kk) {
-        const uint32_t off = (uint32_t)(kk & 3) * kMmaK * 4;
-        const uint64_t ad = umma_desc_kmajor_sw128(smem_u32(kk < 4 ? a0 : a1) + off);
-        const uint64_t bd = umma_desc_kmajor_sw128(smem_u32(kk < 4 ? b0 : b1) + off);
-        mma_tf32(d, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
-    }
+    for (int kk = 0; kk < kD / kMmaK; ++kk)
+        mma_tf32_ss_lo(d, a_lo + (uint32_t)(kk / 4) * kAAtom + (uint32_t)(kk & 3) * 2,
+                       b_lo + (uint32_t)(kk / 4) * kBAtom + (uint32_t)(kk & 3) * 2, kIdescS, kk > 0 ? 1u : 0u);
+}
+
+// P V of one tile: O (+)= P_t V_j, A (P_t) in TMEM from column a, B (V_j^T) in
+// 32-wide K-major swizzled key atoms of kD rows (descriptor low word b_lo);
+// BN / 8 MMAs in straight-line code.  en0: the first adds to O.
+__device__ __forceinline__ void mma_pv(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t en0) {
+    constexpr uint32_t kBAtom = (uint32_t)(kD * kAtom * 4) >> 4;
+    constexpr int kSteps = BN / kMmaK;
+    uint64_t bd[kSteps];
+#pragma unroll
+    for (int kk = 0; kk < kSteps; ++kk)
+        bd[kk] = ((uint64_t)kDescHiSw128 << 32) | (b_lo + (uint32_t)(kk / 4) * kBAtom + (uint32_t)(kk & 3) * 2);
+#pragma unroll
+    for (int kk = 0; kk < kSteps; ++kk)
+        mma_tf32_ts_desc(d, a + (uint32_t)(kk * kMmaK), bd[kk], kIdescPV, kk > 0 ? 1u : en0);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const Params p) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& sh = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t b = blockIdx.x;
     const int64_t mb = p.causal ? (int64_t)gridDim.y - 1 - blockIdx.y : (int64_t)blockIdx.y;
-    const int64_t m0 = mb * BM;
-    // Keys this CTA needs: all, or (causal) up to its rows' last position.
-    int64_t n_end = p.N;
-    if (p.causal) {
-        const int64_t m_last = (m0 + BM - 1 < p.M ? m0 + BM - 1 : p.M - 1);
-        const int64_t r0 = m0 % p.q_len;
-        const bool wraps = r0 + (m_last - m0) >= p.q_len;
-        n_end = (wraps ? p.N - 1 : (m_last % p.q_len) + p.N - p.q_len) + 1;
+    const int64_t m0 = mb * (kTiles * BM);
+    int nb_t[kTiles];
+    int nblk = 0;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        nb_t[t] = tile_blocks(p, m0 + t * BM);
+        nblk = nb_t[t] > nblk ? nb_t[t] : nblk;
     }
-    const int nblk = (int)((n_end + BN - 1) / BN);
 
     if (threadIdx.x == 0) {
         mbar_init(&sh.q_full, 1);
@@ -159,21 +219,20 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             mbar_init(&sh.v_full[s], 1);
             mbar_init(&sh.v_empty[s], kTransWarps);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.vt_full[i], kTransWarps);
-            mbar_init(&sh.vt_empty[i], 1);
-            mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.s_empty[i], kSoftWarps);
-            mbar_init(&sh.pv_full[i], 1);
-            mbar_init(&sh.pv_empty[i], kSoftWarps);
+        mbar_init(&sh.vt_full, kTransWarps);
+        mbar_init(&sh.vt_empty, 1);
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(&sh.s_full[t], 1);
+            mbar_init(&sh.p_full[t], kSoftWarps);
+            mbar_init(&sh.pv_done[t], 1);
+            mbar_init(&sh.o_done[t], 1);
         }
-        mbar_init(&sh.p_full, kSoftWarps);
-        mbar_init(&sh.p_empty, 1);
         mbar_init(&sh.mma_done, 1);
         fence_mbar_init();
         prefetch_tensormap(&tq);
         prefetch_tensormap(&tk);
         prefetch_tensormap(&tv);
+        if (p.o_tma) prefetch_tensormap(&to);
     }
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, kTmemCols);
@@ -188,9 +247,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         // ---- TMA producer -------------------------------------------------
         if (lane == 0) {
             const int zq = p.bq ? (int)b : 0, zk = p.bk ? (int)b : 0, zv = p.bv ? (int)b : 0;
-            mbar_arrive_expect_tx(&sh.q_full, 2 * BM * kAtom * 4);
-            tma_load_3d(sh.q[0], &tq, &sh.q_full, 0, (int)m0, zq);
-            tma_load_3d(sh.q[1], &tq, &sh.q_full, kAtom, (int)m0, zq);
+            int tiles_in = 0;
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t) tiles_in += nb_t[t] > 0 ? 1 : 0;
+            mbar_arrive_expect_tx(&sh.q_full, (uint32_t)tiles_in * kDA * BM * kAtom * 4);
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t) {
+                if (nb_t[t] == 0) continue;
+#pragma unroll
+                for (int a = 0; a < kDA; ++a)
+                    tma_load_3d(sh.q[t][a], &tq, &sh.q_full, kAtom * a, (int)(m0 + t * BM), zq);
+            }
             int j = 0;
             for (; j < nblk; ++j) {
                 const int s = j % kStages;
@@ -200,15 +267,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     break;
                 }
                 const int n0 = j * BN;
-                mbar_arrive_expect_tx(&sh.k_full[s], 2 * BN * kAtom * 4);
-                tma_load_3d(sh.k[s][0], &tk, &sh.k_full[s], 0, n0, zk);
-                tma_load_3d(sh.k[s][1], &tk, &sh.k_full[s], kAtom, n0, zk);
-                mbar_arrive_expect_tx(&sh.v_full[s], 4 * kBox * 4);
+                mbar_arrive_expect_tx(&sh.k_full[s], kDA * BN * kAtom * 4);
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int a = 0; a < kDA; ++a) tma_load_3d(sh.k[s][a], &tk, &sh.k_full[s], kAtom * a, n0, zk);
+                mbar_arrive_expect_tx(&sh.v_full[s], kKA * kDA * kBox * 4);
 #pragma unroll
-                    for (int g = 0; g < 2; ++g)
-                        tma_load_3d(sh.vraw[s][2 * h + g], &tv, &sh.v_full[s], 32 * g, n0 + 32 * h, zv);
+                for (int h = 0; h < kKA; ++h)
+#pragma unroll
+                    for (int g = 0; g < kDA; ++g)
+                        tma_load_3d(sh.vraw[s][h * kDA + g], &tv, &sh.v_full[s], 32 * g, n0 + 32 * h, zv);
             }
             // Wait for the copies still landing before the CTA may exit.
             for (int q = j > kStages ? j - kStages : 0; q < j; ++q) {
@@ -224,167 +291,237 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         // ---- MMA issuer ---------------------------------------------------
         if (lane == 0) {
             bool ok = mbar_wait(&sh.q_full, 0);
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % kStages, buf = j & 1;
-                if (!mbar_wait(&sh.k_full[s], (uint32_t)((j / kStages) & 1))) return false;
-                if (j >= 2 && !mbar_wait(&sh.s_empty[buf], (uint32_t)(((j >> 1) - 1) & 1))) return false;
+            // Descriptor low words of every shared-memory operand: stage
+            // offsets are whole multiples of 16 bytes.
+            const uint32_t k_lo0 = desc_lo_sw128(smem_u32(sh.k[0][0]));
+            constexpr uint32_t kKStage = (uint32_t)sizeof(sh.k[0]) >> 4;
+            const uint32_t vt_lo = desc_lo_sw128(smem_u32(sh.vt[0]));
+            uint32_t q_lo[kTiles];
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t) q_lo[t] = desc_lo_sw128(smem_u32(sh.q[t][0]));
+            // The scores of block j for tile t, once P V_t of block j-1 has
+            // read P_t (the same TMEM columns).  K_j is released after the
+            // last tile's scores.
+            auto scores = [&](int t, int j) -> bool {
+                if (j >= nb_t[t]) return true;
+                if (j > 0 && !mbar_wait(&sh.pv_done[t], (uint32_t)((j - 1) & 1))) return false;
                 tc_fence_after();
-                mma_128x64x64(tmem + kColS + buf * BN, sh.q[0], sh.q[1], sh.k[s][0], sh.k[s][1]);
-                mma_commit(&sh.k_empty[s]);
-                mma_commit(&sh.s_full[buf]);
+                mma_scores(tmem + kColS + (uint32_t)t * BN, q_lo[t], k_lo0 + (uint32_t)(j % kStages) * kKStage);
+                mma_commit(&sh.s_full[t]);
                 return true;
             };
-            if (ok && nblk > 0) ok = issue_s(0);
+            auto release_k = [&](int j) { mma_commit(&sh.k_empty[j % kStages]); };
+            if (ok && nblk > 0) {
+                ok = mbar_wait(&sh.k_full[0], 0) && scores(0, 0) && scores(1, 0);
+                release_k(0);
+            }
             for (int j = 0; j < nblk && ok; ++j) {
-                if (j + 1 < nblk && !issue_s(j + 1)) { ok = false; break; }
-                const int buf = j & 1;
-                if (!mbar_wait(&sh.p_full, (uint32_t)(j & 1)) ||
-                    !mbar_wait(&sh.vt_full[buf], (uint32_t)((j >> 1) & 1)) ||
-                    (j >= 2 && !mbar_wait(&sh.pv_empty[buf], (uint32_t)(((j >> 1) - 1) & 1)))) {
+                if (!mbar_wait(&sh.vt_full, (uint32_t)(j & 1))) { ok = false; break; }
+                const bool next = j + 1 < nblk;
+                if (next && !mbar_wait(&sh.k_full[(j + 1) % kStages], (uint32_t)(((j + 1) / kStages) & 1))) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                mma_128x64x64(tmem + kColPV + buf * kD, sh.p[0], sh.p[1], sh.vt[buf][0], sh.vt[buf][1]);
-                mma_commit(&sh.p_empty);
-                mma_commit(&sh.vt_empty[buf]);
-                mma_commit(&sh.pv_full[buf]);
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t) {
+                    if (j < nb_t[t]) {
+                        if (!mbar_wait(&sh.p_full[t], (uint32_t)(j & 1))) { ok = false; break; }
+                        tc_fence_after();
+                        mma_pv(tmem + kColO + (uint32_t)t * kD, tmem + kColS + (uint32_t)t * BN, vt_lo,
+                               j > 0 ? 1u : 0u);
+                        mma_commit(&sh.pv_done[t]);
+                        if (j == nb_t[t] - 1) mma_commit(&sh.o_done[t]);
+                    }
+                    if (t == kTiles - 1) mma_commit(&sh.vt_empty);   // after every P V of block j
+                    if (next && !scores(t, j + 1)) { ok = false; break; }
+                }
+                if (!ok) break;
+                if (next) release_k(j + 1);
             }
             if (!ok) record_status(&g_wait_status, kWaitFull);
             // Nothing may still be writing TMEM when it is freed.
             mma_commit(&sh.mma_done);
             if (!mbar_wait(&sh.mma_done, 0)) record_status(&g_wait_status, kWaitMma);
         }
-    } else if (warp < 2 + kSoftWarps) {
-        // ---- softmax and output, one query row per thread ------------------
-        const int quarter = warp & 3;                 // TMEM lanes this warp may read
-        const int row = quarter * 32 + lane;
-        const int64_t m = m0 + row;
-        const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-        const int64_t pos = p.causal ? (m % p.q_len) + p.N - p.q_len : p.N - 1;
-        float o[kD];
-#pragma unroll
-        for (int e = 0; e < kD; ++e) o[e] = 0.0f;
-        float m_run = -INFINITY, l_run = 0.0f, corr_prev = 1.0f;
-        bool ok = true;
-        // O = O * corr_prev + PV_{j}, once PV_j has landed.
-        auto add_pv = [&](int j) -> bool {
-            const int buf = j & 1;
-            if (!mbar_wait(&sh.pv_full[buf], (uint32_t)((j >> 1) & 1))) return false;
-            tc_fence_after();
-            float v[32];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                tmem_ld32(tmem + lanes + kColPV + buf * kD + h * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[h * 32 + e] = fmaf(o[h * 32 + e], corr_prev, v[e]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.pv_empty[buf]);
-            return true;
-        };
-        for (int j = 0; j < nblk; ++j) {
-            const int buf = j & 1;
-            if (!mbar_wait(&sh.s_full[buf], (uint32_t)((j >> 1) & 1))) { ok = false; break; }
-            tc_fence_after();
-            float s[BN];
-            {
-                float v[32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tmem_ld32(tmem + lanes + kColS + buf * BN + h * 32, v);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) s[h * 32 + c] = v[c];
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.s_empty[buf]);
-            // Mask (keys past N, or past the row's causal position), scale to
-            // the exp2 domain, and the running maximum.
-            const int64_t n0 = (int64_t)j * BN;
-            // Keys c <= lim of the block are kept.  Eight partial maxima and
-            // sums, so that no chain runs through all 64 keys.
-            const int64_t last = (pos < p.N - 1 ? pos : p.N - 1) - n0;
-            const int lim = last < 0 ? -1 : (last >= BN ? BN - 1 : (int)last);
-            float part[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) part[i] = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                s[c] = c <= lim ? s[c] * p.scale_log2 : -INFINITY;
-                part[c & 7] = fmaxf(part[c & 7], s[c]);
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
-                                   fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
-            const float m_new = fmaxf(m_run, mx);
-            // A row with no kept key so far keeps m = -inf; its terms stay 0.
-            const float base = m_new == -INFINITY ? 0.0f : m_new;
-            const float corr = exp2f(m_run - base);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) part[i] = 0.0f;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                s[c] = exp2f(s[c] - base);
-                part[c & 7] += s[c];
-            }
-            const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
-                              ((part[4] + part[5]) + (part[6] + part[7]));
-            l_run = l_run * corr + sum;
-            m_run = m_new;
-            // P_j to shared memory once P V_{j-1} has read P_{j-1}.
-            if (j > 0 && !mbar_wait(&sh.p_empty, (uint32_t)((j - 1) & 1))) { ok = false; break; }
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4*>(&sh.p[a][row * kAtom + ((q ^ (row & 7)) << 2)]) =
-                        make_float4(s[a * 32 + 4 * q], s[a * 32 + 4 * q + 1], s[a * 32 + 4 * q + 2],
-                                    s[a * 32 + 4 * q + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.p_full);
-            // The previous block's P V joins O while this block's runs.
-            if (j > 0 && !add_pv(j - 1)) { ok = false; break; }
-            corr_prev = corr;
-        }
-        if (ok && nblk > 0) ok = add_pv(nblk - 1);
-        if (!ok) {
-            record_status(&g_wait_status, kWaitMma);
-        } else if (m < p.M) {
-            const float inv = 1.0f / l_run;
-            float* orow = p.O + b * p.bsO + m * p.rsO;
-            if (p.o_vec) {
-#pragma unroll
-                for (int e = 0; e < kD; e += 4)
-                    *reinterpret_cast<float4*>(orow + e) =
-                        make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
-            } else {
-#pragma unroll
-                for (int e = 0; e < kD; ++e) orow[e * p.csO] = o[e] * inv;
-            }
-        }
-    } else {
+    } else if (warp < kWarpSoft) {
         // ---- V_j -> V_j^T -------------------------------------------------
-        const int t = threadIdx.x - (2 + kSoftWarps) * 32;
+        const int t = threadIdx.x - 2 * 32;
         for (int j = 0; j < nblk; ++j) {
-            const int s = j % kStages, buf = j & 1;
+            const int s = j % kStages;
             if (!mbar_wait(&sh.v_full[s], (uint32_t)((j / kStages) & 1))) {
                 record_status(&g_wait_status, kWaitFull);
                 break;
             }
-            if (j >= 2 && !mbar_wait(&sh.vt_empty[buf], (uint32_t)(((j >> 1) - 1) & 1))) {
+            if (j >= 1 && !mbar_wait(&sh.vt_empty, (uint32_t)((j - 1) & 1))) {
                 record_status(&g_wait_status, kWaitEmpty);
                 break;
             }
-            transpose_atom(sh.vraw[s][0], sh.vt[buf][0], t);    // keys 0..31 of the block
-            transpose_atom(sh.vraw[s][2], sh.vt[buf][1], t);    // keys 32..63
+#pragma unroll
+            for (int h = 0; h < kKA; ++h) transpose_atom(sh.vraw[s][h * kDA], sh.vt[h], t);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&sh.vt_full[buf]);
+                mbar_arrive(&sh.vt_full);
                 mbar_arrive(&sh.v_empty[s]);
+            }
+        }
+    } else {
+        // ---- softmax and output, one query row per thread ------------------
+        const int t = (warp - kWarpSoft) / kSoftWarps;   // query tile
+        const int quarter = warp & 3;                    // TMEM lanes this warp may read
+        const int row = quarter * 32 + lane;
+        const int64_t m = m0 + t * BM + row;
+        const int nbt = t == 0 ? nb_t[0] : nb_t[kTiles - 1];
+        const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+        const uint32_t o_addr = tmem + lanes + kColO + (uint32_t)t * kD;
+        const uint32_t s_addr = tmem + lanes + kColS + (uint32_t)t * BN;
+        const int64_t pos = p.causal ? (m % p.q_len) + p.N - p.q_len : p.N - 1;
+        const int64_t last_key = pos < p.N - 1 ? pos : p.N - 1;
+        const float scale = p.scale_log2;
+        float m_ref = -INFINITY, l_run = 0.0f;
+        bool ok = nbt > 0;
+        for (int j = 0; ok && j < nbt; ++j) {
+            // The scores of block j were issued after P V of block j-1, so
+            // their barrier also tells that O is settled.
+            if (!mbar_wait(&sh.s_full[t], (uint32_t)(j & 1))) { ok = false; break; }
+            tc_fence_after();
+            // Keys c <= lim of the block are kept (keys past N, or past the
+            // row's causal position, are not).
+            const int64_t last = last_key - (int64_t)j * BN;
+            const int lim = last < 0 ? -1 : (last >= BN ? BN - 1 : (int)last);
+            const bool whole = __all_sync(0xffffffffu, lim == BN - 1);
+            // Pass 1: the block's largest scaled score.  Scaling is monotonic,
+            // so it is the scaled largest (or, for a negative alpha, smallest)
+            // score.
+            float part[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part[i] = scale >= 0.0f ? -INFINITY : INFINITY;
+#pragma unroll
+            for (int hh = 0; hh < BN / 64; ++hh) {
+                float s[64];
+                tmem_ld64(s_addr + 64 * hh, s);
+                if (scale >= 0.0f) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (whole || 64 * hh + c <= lim) part[c & 7] = fmaxf(part[c & 7], s[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (whole || 64 * hh + c <= lim) part[c & 7] = fminf(part[c & 7], s[c]);
+                }
+            }
+            float ext;
+            if (scale >= 0.0f)
+                ext = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                            fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+            else
+                ext = fminf(fminf(fminf(part[0], part[1]), fminf(part[2], part[3])),
+                            fminf(fminf(part[4], part[5]), fminf(part[6], part[7])));
+            const float m_blk = lim >= 0 ? ext * scale : -INFINITY;
+            // Raise the reference maximum only past the headroom; O and l
+            // follow with the factor exp2(m_old - m_new) (0 from -inf).
+            const bool raise = m_blk > m_ref + kRaise;
+            float corr = 1.0f;
+            if (raise) {
+                corr = ex2_approx(m_ref - m_blk);
+                m_ref = m_blk;
+                l_run *= corr;
+            }
+            // Pass 2: probabilities relative to the reference maximum (a row
+            // with no kept key so far has m_ref = -inf and every term
+            // masked), written over the scores.
+            const float neg = -m_ref;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part[i] = 0.0f;
+#pragma unroll
+            for (int hh = 0; hh < BN / 64; ++hh) {
+                float s[64];
+                tmem_ld64(s_addr + 64 * hh, s);
+                if (whole) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        s[c] = ex2_approx(fmaf(s[c], scale, neg));
+                        part[c & 7] += s[c];
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        s[c] = 64 * hh + c <= lim ? ex2_approx(fmaf(s[c], scale, neg)) : 0.0f;
+                        part[c & 7] += s[c];
+                    }
+                }
+                tmem_st64_nowait(s_addr + 64 * hh, s);
+            }
+            l_run += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+            if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                // O row *= corr (1 for the rows that did not raise).
+#pragma unroll
+                for (int h = 0; h < kD / 32; ++h) {
+                    float o[32];
+                    tmem_ld32(o_addr + 32 * h, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= corr;
+                    tmem_st32_nowait(o_addr + 32 * h, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.p_full[t]);
+        }
+        if (ok && nbt > 0) {
+            if (!mbar_wait(&sh.o_done[t], 0)) ok = false;
+        }
+        if (!ok) {
+            if (nbt > 0) record_status(&g_wait_status, kWaitMma);
+        } else if (p.o_tma) {
+            // O / l through the tile's Q buffer (the score MMAs that read it
+            // are done) in the swizzled layout of the O tensor map; each
+            // warp stores its 32 rows with one bulk tensor copy per head-dim
+            // atom, and the copy leaves out the rows past M.
+            tc_fence_after();
+            const float inv = 1.0f / l_run;
+#pragma unroll
+            for (int a = 0; a < kDA; ++a) {
+                float o[32];
+                tmem_ld32(o_addr + 32 * a, o);
+                float* st = sh.q[t][a];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4*>(st + row * kAtom + ((c ^ (row & 7)) << 2)) =
+                        make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv, o[4 * c + 3] * inv);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && m0 + t * BM + quarter * 32 < p.M) {
+#pragma unroll
+                for (int a = 0; a < kDA; ++a)
+                    tma_store_3d(&to, sh.q[t][a] + quarter * 32 * kAtom, kAtom * a,
+                                 (int)(m0 + t * BM + quarter * 32), p.bo ? (int)b : 0);
+                bulk_commit();
+                // Shared memory must outlive the copies' reads of it; the
+                // writes themselves complete with the grid.
+                bulk_wait_read_all();
+            }
+        } else {
+            tc_fence_after();
+            const float inv = 1.0f / l_run;
+            float* orow = p.O + b * p.bsO + (m < p.M ? m : 0) * p.rsO;
+#pragma unroll
+            for (int h = 0; h < kD / 32; ++h) {
+                float o[32];
+                tmem_ld32(o_addr + 32 * h, o);    // whole warp, converged
+                if (m < p.M) {
+                    if (p.o_vec) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(orow + 32 * h + e) =
+                                make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) orow[(32 * h + e) * p.csO] = o[e] * inv;
+                    }
+                }
             }
         }
     }
@@ -457,8 +594,17 @@ cudaError_t launch_attention_tc(const AttnProblem& a, cudaStream_t stream) {
     p.bv = !(a.batch == 1 || a.bsV == 0);
     p.o_vec = a.csO == 1 && reinterpret_cast<uintptr_t>(a.O) % 16 == 0 && a.rsO % 4 == 0 &&
               (a.batch == 1 || a.bsO % 4 == 0);
-    const dim3 grid((unsigned)a.batch, (unsigned)((a.M + BM - 1) / BM));
-    attention_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    // O through a tensor map when it has the layout of one (unit stride along
+    // the values, 16-byte strides laid out without overlap), else by the row
+    // threads.  A zero batch stride is never an O layout (validated injective).
+    CUtensorMap to;
+    std::memset(&to, 0, sizeof(to));
+    p.o_tma = tma_operand(a.O, a.M, a.rsO, a.csO, a.bsO, a.batch) && (a.batch == 1 || a.bsO != 0) &&
+              make_map(&to, a.O, a.M, a.rsO, a.bsO, a.batch, kD, 32);
+    p.bo = a.batch > 1;
+    const int64_t rows = kTiles * BM;
+    const dim3 grid((unsigned)a.batch, (unsigned)((a.M + rows - 1) / rows));
+    attention_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
