@@ -32,7 +32,9 @@ __all__ = [
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libsbgemm.so")
+# SBGEMM_LIBRARY selects another build of the library, e.g. the debug build
+# (build(debug=True): libsbgemm_debug.so, with device bounds checks).
+LIB_PATH = os.environ.get("SBGEMM_LIBRARY") or os.path.join(HERE, "libsbgemm.so")
 
 SBGEMM_OK = 0
 SBGEMM_ERR_INVALID_VALUE = 1
@@ -110,7 +112,7 @@ def load(path: str = LIB_PATH):
             return _lib
         if not os.path.exists(path):
             raise RuntimeError(
-                f"libsbgemm.so is missing at {path}; build it with "
+                f"the library is missing at {path}; build it with "
                 "`python -m strided_gemm_gb300.build` (nvcc, sm_103a)")
         lib = ctypes.CDLL(path)
         lib.sbgemm.restype = ctypes.c_int

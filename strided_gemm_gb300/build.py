@@ -3,6 +3,11 @@
 Each translation unit is compiled in parallel, then linked into one shared
 library next to this file.  A stamp holding a hash of the sources and flags
 lets an unchanged tree skip the compile.
+
+build(debug=True) makes libsbgemm_debug.so instead: the same sources with
+SBGEMM_DEBUG defined, so that every kernel checks the global addresses it
+loads and stores against the operand spans the host validated (a violation
+is reported by sbgemm_device_status and the access skipped).
 """
 
 from __future__ import annotations
@@ -20,6 +25,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libsbgemm.so")
 STAMP = os.path.join(HERE, ".libsbgemm.stamp")
+DEBUG_LIB_PATH = os.path.join(HERE, "libsbgemm_debug.so")
+DEBUG_STAMP = os.path.join(HERE, ".libsbgemm_debug.stamp")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -48,14 +55,15 @@ def _digest(srcs, deps, extra) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    extra = list(extra_flags or [])
+def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    extra = list(extra_flags or []) + (["-DSBGEMM_DEBUG"] if debug else [])
+    lib_path, stamp = (DEBUG_LIB_PATH, DEBUG_STAMP) if debug else (LIB_PATH, STAMP)
     srcs, deps = _sources()
     digest = _digest(srcs, deps, extra)
-    if not force and os.path.exists(LIB_PATH) and os.path.exists(STAMP):
-        with open(STAMP) as fh:
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp):
+        with open(stamp) as fh:
             if fh.read().strip() == digest:
-                return LIB_PATH
+                return lib_path
     with tempfile.TemporaryDirectory(prefix="sbgemm_build_") as tmp:
         procs = []
         objs = []
@@ -77,14 +85,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         if failed:
             msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
             raise RuntimeError(f"nvcc failed:\n{msg}")
-        tmp_lib = LIB_PATH + f".tmp{os.getpid()}"
+        tmp_lib = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp_lib] + objs + ["-cudart", "static"]
         subprocess.run(cmd, check=True)
-        os.replace(tmp_lib, LIB_PATH)
-    with open(STAMP, "w") as fh:
+        os.replace(tmp_lib, lib_path)
+    with open(stamp, "w") as fh:
         fh.write(digest + "\n")
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -26,6 +26,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "debug_check.cuh"
 #include "internal.h"
 
 namespace sbg {
@@ -49,6 +50,7 @@ struct AttnParams {
     int causal;
     int64_t q_len;
     int v_vec, o_vec;            // unit stride along e and 16-byte aligned rows
+    ElemSpan sq, sk, sv, so;     // debug builds: valid element offsets of the operands
 };
 
 struct Smem {
@@ -62,6 +64,9 @@ struct Smem {
 __device__ __forceinline__ int row_of(int ty, int i) { return (i < 4 ? 0 : 64) + ty * 4 + (i & 3); }
 // Columns (keys of a block, or value dimensions) of column-group tx (0..7).
 __device__ __forceinline__ int col_of(int tx, int j) { return (j < 4 ? 0 : 32) + tx * 4 + (j & 3); }
+
+// Status word of this kernel's debug bounds checks (sbgemm_device_status).
+__device__ unsigned int g_status = 0;
 
 __global__ void __launch_bounds__(kThreads, 2) attention_kernel(const AttnParams p) {
     extern __shared__ float4 smem4[];
@@ -89,7 +94,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_kernel(const AttnParams
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int64_t m = m0 + 4 * m4 + q;
-                x[q] = m < p.M ? Qb[m * p.rsQ + d * p.csQ] : 0.0f;
+                const float* a = Qb + m * p.rsQ + d * p.csQ;
+                x[q] = (m < p.M && dbg_in_span(p.Q, a, p.sq, &g_status)) ? *a : 0.0f;
             }
             *reinterpret_cast<float4*>(&sh.q[d * QP + 4 * m4]) = make_float4(x[0], x[1], x[2], x[3]);
         }
@@ -137,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_kernel(const AttnParams
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int64_t n = n0 + 4 * n4 + q;
-                    x[q] = n < p.N ? Kb[n * p.rsK + d * p.csK] : 0.0f;
+                    const float* a = Kb + n * p.rsK + d * p.csK;
+                    x[q] = (n < p.N && dbg_in_span(p.K, a, p.sk, &g_status)) ? *a : 0.0f;
                 }
                 *reinterpret_cast<float4*>(&sh.k[d * KP + 4 * n4]) = make_float4(x[0], x[1], x[2], x[3]);
             }
@@ -147,8 +154,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_kernel(const AttnParams
             for (int r = t >> 4; r < BN; r += kThreads / 16) {
                 const int64_t n = n0 + r;
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (n < p.N) {
-                    const float* vrow = Vb + n * p.rsV;
+                const float* vrow = Vb + n * p.rsV;
+                if (n < p.N && dbg_in_span(p.V, vrow, p.sv, &g_status) &&
+                    dbg_in_span(p.V, vrow + (4 * e4 + 3) * p.csV, p.sv, &g_status)) {
                     if (p.v_vec) {
                         x = __ldg(reinterpret_cast<const float4*>(vrow) + e4);
                     } else {
@@ -260,6 +268,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_kernel(const AttnParams
         if (m >= p.M) continue;
         const float inv = 1.0f / l;
         float* orow = Ob + m * p.rsO;
+        if (!dbg_in_span(p.O, orow, p.so, &g_status) ||
+            !dbg_in_span(p.O, orow + (kD - 1) * p.csO, p.so, &g_status))
+            continue;
         if (p.o_vec) {
             *reinterpret_cast<float4*>(orow + tx * 4) =
                 make_float4(O_AT(i, 0) * inv, O_AT(i, 1) * inv, O_AT(i, 2) * inv, O_AT(i, 3) * inv);
@@ -303,9 +314,22 @@ cudaError_t launch_attention(const AttnProblem& a, cudaStream_t stream) {
               (a.batch == 1 || a.bsV % 4 == 0);
     p.o_vec = a.csO == 1 && reinterpret_cast<uintptr_t>(a.O) % 16 == 0 && a.rsO % 4 == 0 &&
               (a.batch == 1 || a.bsO % 4 == 0);
+    p.sq = a.sq; p.sk = a.sk; p.sv = a.sv; p.so = a.so;
     const dim3 grid((unsigned)a.batch, (unsigned)((a.M + BM - 1) / BM));
     attention_kernel<<<grid, kThreads, sizeof(Smem), stream>>>(p);
     return cudaGetLastError();
+}
+
+unsigned int read_and_clear_status_attention(cudaStream_t stream) {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return v;
 }
 
 }  // namespace sbg

@@ -51,6 +51,7 @@
 #include <cstring>
 
 #include "attention_tc.h"
+#include "debug_check.cuh"
 #include "ptx.cuh"
 
 namespace sbg {
@@ -119,6 +120,7 @@ struct Params {
     int o_vec;                       // O rows unit-stride and 16-byte aligned
     int o_tma;                       // O goes out through its tensor map
     int bo;                          // O's batch coordinate follows blockIdx.x
+    ElemSpan so;                     // debug builds: O's valid element offsets
 };
 
 // Keys [0, n_end) a tile of rows starting at m0 needs: all of them, or
@@ -511,7 +513,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             for (int h = 0; h < kD / 32; ++h) {
                 float o[32];
                 tmem_ld32(o_addr + 32 * h, o);    // whole warp, converged
-                if (m < p.M) {
+                if (m < p.M && dbg_in_span(p.O, orow + 32 * h * p.csO, p.so, &g_wait_status) &&
+                    dbg_in_span(p.O, orow + (32 * h + 31) * p.csO, p.so, &g_wait_status)) {
                     if (p.o_vec) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
@@ -602,6 +605,7 @@ cudaError_t launch_attention_tc(const AttnProblem& a, cudaStream_t stream) {
     p.o_tma = tma_operand(a.O, a.M, a.rsO, a.csO, a.bsO, a.batch) && (a.batch == 1 || a.bsO != 0) &&
               make_map(&to, a.O, a.M, a.rsO, a.bsO, a.batch, kD, 32);
     p.bo = a.batch > 1;
+    p.so = a.so;
     const int64_t rows = kTiles * BM;
     const dim3 grid((unsigned)a.batch, (unsigned)((a.M + rows - 1) / rows));
     attention_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);

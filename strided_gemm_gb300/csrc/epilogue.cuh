@@ -15,6 +15,7 @@
 
 #include <cstdint>
 
+#include "debug_check.cuh"
 #include "internal.h"
 
 namespace sbg {
@@ -56,9 +57,13 @@ __device__ __forceinline__ float activate(int act, float z) {
 }
 
 // The fused part for output (b, m, n), applied to the product's epilogue value.
+// `status`: the calling kernel's status word (debug bounds checks).
 __device__ __forceinline__ float finish(const EpiParams& e, float v, int64_t b, int64_t m,
-                                        int64_t n) {
-    if (e.D) v += __ldg(e.D + b * e.bsD + m * e.rsD + n * e.csD);
+                                        int64_t n, unsigned int* status) {
+    if (e.D) {
+        const float* d = e.D + b * e.bsD + m * e.rsD + n * e.csD;
+        if (dbg_in_span(e.D, d, e.d_span, status)) v += __ldg(d);
+    }
     return activate(e.act, v);
 }
 

@@ -23,6 +23,7 @@
 #include <algorithm>
 #include <cstdint>
 
+#include "debug_check.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
 
@@ -30,6 +31,9 @@ namespace sbg {
 namespace {
 
 constexpr int kThreads = 256;
+
+// Status word of this kernel's debug bounds checks (sbgemm_device_status).
+__device__ unsigned int g_status = 0;
 constexpr int kMinPieceSlices = 4;   // K slices (of 16) per piece at least
 constexpr int kMaxPieces = 16;
 
@@ -66,15 +70,18 @@ struct SliceLoader {
     }
 
     // Fetch slice kt (k0 = kt*BK).  rows_left = valid rows from r0, k_left = K - k0.
+    // op / span: the operand's base pointer and valid offsets (debug checks).
     __device__ __forceinline__ void load(const float* __restrict__ base, int64_t kt,
-                                         int64_t rows_left, int64_t k_left) {
+                                         int64_t rows_left, int64_t k_left, const float* op,
+                                         const ElemSpan& span) {
         const int64_t off = off0 + kt * step_k;
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
             int r = RFAST ? r_first : r_first + i * (kThreads / BK);
             int k = RFAST ? k_first + i * (kThreads / R) : k_first;
             bool ok = (r < rows_left) && (k < k_left);
-            v[i] = ok ? __ldg(base + off + i * step_i) : 0.0f;
+            const float* a = base + off + i * step_i;
+            v[i] = (ok && dbg_in_span(op, a, span, &g_status)) ? __ldg(a) : 0.0f;
         }
     }
 
@@ -134,15 +141,19 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
         la.init(tid, m0, p.rsA, p.csA);
         lb.init(tid, n0, p.csB, p.rsB);
 
-        float acc[TM][TN];
+        // Accumulators of adjacent row pairs (i, i+1) of one column, for the
+        // packed FMA (fma.rn.f32x2: each lane rounds like fmaf, so every output
+        // keeps one k-ordered FMA chain).
+        float2 acc2[TM][TN / 2];
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+            for (int j = 0; j < TN / 2; ++j) acc2[i][j] = make_float2(0.0f, 0.0f);
+#define ACC(i, j) (((j) & 1) ? acc2[i][(j) >> 1].y : acc2[i][(j) >> 1].x)
 
         if (ke > kb) {
-            la.load(Ab, kb, rows_a, p.K - kb * BK);
-            lb.load(Bb, kb, rows_b, p.K - kb * BK);
+            la.load(Ab, kb, rows_a, p.K - kb * BK, p.A, p.sa);
+            lb.load(Bb, kb, rows_b, p.K - kb * BK, p.B, p.sb);
             la.template store<LDA>(As[0]);
             lb.template store<LDB>(Bs[0]);
         }
@@ -152,8 +163,8 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
             const int buf = (int)((kt - kb) & 1);
             const bool more = kt + 1 < ke;
             if (more) {
-                la.load(Ab, kt + 1, rows_a, p.K - (kt + 1) * BK);
-                lb.load(Bb, kt + 1, rows_b, p.K - (kt + 1) * BK);
+                la.load(Ab, kt + 1, rows_a, p.K - (kt + 1) * BK, p.A, p.sa);
+                lb.load(Bb, kt + 1, rows_b, p.K - (kt + 1) * BK, p.B, p.sb);
             }
 #pragma unroll
             for (int kk = 0; kk < BK; ++kk) {
@@ -171,9 +182,12 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
                     bv[4 * h + 0] = x.x; bv[4 * h + 1] = x.y; bv[4 * h + 2] = x.z; bv[4 * h + 3] = x.w;
                 }
 #pragma unroll
-                for (int i = 0; i < TM; ++i)
+                for (int i = 0; i < TM; ++i) {
+                    const float2 av = make_float2(a[i], a[i]);
 #pragma unroll
-                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
+                    for (int jp = 0; jp < TN / 2; ++jp)
+                        acc2[i][jp] = __ffma2_rn(av, make_float2(bv[2 * jp], bv[2 * jp + 1]), acc2[i][jp]);
+                }
             }
             if (more) {
                 la.template store<LDA>(As[buf ^ 1]);
@@ -190,7 +204,7 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < TN; ++j) __stcg(slot + (i * TN + j) * kThreads + tid, acc[i][j]);
+                for (int j = 0; j < TN; ++j) __stcg(slot + (i * TN + j) * kThreads + tid, ACC(i, j));
             __threadfence();
             __syncthreads();
             if (tid == 0)
@@ -201,7 +215,7 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+                for (int j = 0; j < TN; ++j) ACC(i, j) = 0.0f;
             const float* first = sp.part + tile_id * sp.pieces * (int64_t)(BM * BN);
 #pragma unroll 1
             for (int q = 0; q < sp.pieces; ++q) {
@@ -209,7 +223,7 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
-                    for (int j = 0; j < TN; ++j) acc[i][j] += __ldcg(src + (i * TN + j) * kThreads + tid);
+                    for (int j = 0; j < TN; ++j) ACC(i, j) += __ldcg(src + (i * TN + j) * kThreads + tid);
             }
         }
 
@@ -224,7 +238,8 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
                 const int64_t n = n0 + (j / 4) * (BN / TN) * 4 + tx * 4 + (j % 4);
                 if (n >= p.N) continue;
                 float* c = Cb + m * p.rsC + n * p.csC;
-                *c = p.accumulate ? fmaf(p.alpha, acc[i][j], *c) : p.alpha * acc[i][j];
+                if (!dbg_in_span(p.C, c, p.sc, &g_status)) continue;
+                *c = p.accumulate ? fmaf(p.alpha, ACC(i, j), *c) : p.alpha * ACC(i, j);
             }
         }
         if (p.epi.on) {
@@ -238,11 +253,13 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
                     const int64_t n = n0 + (j / 4) * (BN / TN) * 4 + tx * 4 + (j % 4);
                     if (n >= p.N) continue;
                     float* c = Cb + m * p.rsC + n * p.csC;
-                    *c = finish(p.epi, *c, b, m, n);
+                    if (!dbg_in_span(p.C, c, p.sc, &g_status)) continue;
+                    *c = finish(p.epi, *c, b, m, n, &g_status);
                 }
             }
         }
     }
+#undef ACC
 }
 
 // Bytes of the partial sums of `tiles` tiles cut into `pieces`, rounded up to
@@ -336,6 +353,22 @@ cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t 
             return launch_variant<64, 64, 16, 4, 4, false>(p, plan, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+}  // namespace sbg
+
+namespace sbg {
+
+unsigned int read_and_clear_status_gather(cudaStream_t stream) {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return v;
 }
 
 }  // namespace sbg

@@ -39,6 +39,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "debug_check.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -76,7 +77,13 @@ struct Params {
                             // applied in the register epilogue
     float2* ws_partial;     // [grid][kThreads * 64] partial accumulators
     unsigned int* ws_flag;  // [grid] partial-ready flags, zeroed before launch
+    ElemSpan sc;            // debug builds: C's valid element offsets
 };
+
+// Debug builds: [p, p + n) lies inside C's span (records a violation if not).
+__device__ __forceinline__ bool c_ok(const Params& p, const float* x, int n) {
+    return dbg_in_span(p.C, x, p.sc, &g_wait_status) && dbg_in_span(p.C, x + (n - 1), p.sc, &g_wait_status);
+}
 
 // Copy issuer state (thread 0 only, kept in shared memory so that it costs
 // no registers in the consumers' hot loop): the next (item, slice) to load.
@@ -326,7 +333,9 @@ __device__ __forceinline__ void fused_pass(const Params& p, const TileCoord& tc,
 #pragma unroll
     for (int j = 0; j < TN; ++j) {
         ncol[j] = tc.n0 + col_of(wn, ln, j);
-        d_col[j] = (d_per_col && ncol[j] < p.N) ? __ldg(Db + ncol[j] * p.epi.csD) : 0.0f;
+        const float* d = Db ? Db + ncol[j] * p.epi.csD : nullptr;
+        d_col[j] = (d_per_col && ncol[j] < p.N && dbg_in_span(p.epi.D, d, p.epi.d_span, &g_wait_status))
+                       ? __ldg(d) : 0.0f;
     }
     const bool vec = p.c_vec4 && ncol[TN - 1] < p.N;   // both runs of 4 wholly inside C
     auto load = [&](float (&v)[G][TN], int i0) {
@@ -337,14 +346,16 @@ __device__ __forceinline__ void fused_pass(const Params& p, const TileCoord& tc,
             if (vec) {
 #pragma unroll
                 for (int h = 0; h < TN / 4; ++h) {
-                    const float4 c4 = m < p.M ? __ldcg(reinterpret_cast<const float4*>(crow + ncol[4 * h]))
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 c4 = (m < p.M && c_ok(p, crow + ncol[4 * h], 4))
+                                          ? __ldcg(reinterpret_cast<const float4*>(crow + ncol[4 * h]))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
                     v[i][4 * h] = c4.x; v[i][4 * h + 1] = c4.y; v[i][4 * h + 2] = c4.z; v[i][4 * h + 3] = c4.w;
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < TN; ++j)
-                    v[i][j] = (m < p.M && ncol[j] < p.N) ? __ldcg(crow + ncol[j] * p.csC) : 0.0f;
+                    v[i][j] = (m < p.M && ncol[j] < p.N && c_ok(p, crow + ncol[j] * p.csC, 1))
+                                  ? __ldcg(crow + ncol[j] * p.csC) : 0.0f;
             }
         }
     };
@@ -360,7 +371,8 @@ __device__ __forceinline__ void fused_pass(const Params& p, const TileCoord& tc,
                 float z = v[i][j];
                 if (d_per_col) {
                     z += d_col[j];
-                } else if (drow && ncol[j] < p.N) {
+                } else if (drow && ncol[j] < p.N &&
+                           dbg_in_span(p.epi.D, drow + ncol[j] * p.epi.csD, p.epi.d_span, &g_wait_status)) {
                     z += __ldg(drow + ncol[j] * p.epi.csD);
                 }
                 v[i][j] = act_fn<ACT>(z);
@@ -368,12 +380,13 @@ __device__ __forceinline__ void fused_pass(const Params& p, const TileCoord& tc,
             if (vec) {
 #pragma unroll
                 for (int h = 0; h < TN / 4; ++h)
-                    *reinterpret_cast<float4*>(crow + ncol[4 * h]) =
-                        make_float4(v[i][4 * h], v[i][4 * h + 1], v[i][4 * h + 2], v[i][4 * h + 3]);
+                    if (c_ok(p, crow + ncol[4 * h], 4))
+                        *reinterpret_cast<float4*>(crow + ncol[4 * h]) =
+                            make_float4(v[i][4 * h], v[i][4 * h + 1], v[i][4 * h + 2], v[i][4 * h + 3]);
             } else {
 #pragma unroll
                 for (int j = 0; j < TN; ++j)
-                    if (ncol[j] < p.N) crow[ncol[j] * p.csC] = v[i][j];
+                    if (ncol[j] < p.N && c_ok(p, crow + ncol[j] * p.csC, 1)) crow[ncol[j] * p.csC] = v[i][j];
             }
         }
     };
@@ -645,8 +658,9 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
 #pragma unroll
                 for (int j = 0; j < TN; ++j) {
                     const int64_t n = tc.n0 + col_of(wn, ln, j);
-                    bias[j] = (p.epi.D && n < p.N) ? __ldg(p.epi.D + tc.b * p.epi.bsD + n * p.epi.csD)
-                                                   : 0.0f;
+                    const float* d = p.epi.D ? p.epi.D + tc.b * p.epi.bsD + n * p.epi.csD : nullptr;
+                    bias[j] = (p.epi.D && n < p.N && dbg_in_span(p.epi.D, d, p.epi.d_span, &g_wait_status))
+                                  ? __ldg(d) : 0.0f;
                 }
                 relu = p.epi.act == kActRelu;
             }
@@ -667,12 +681,13 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                 if (vec) {
 #pragma unroll
                     for (int h = 0; h < TN / 4; ++h)
-                        *reinterpret_cast<float4*>(crow + ncol(4 * h)) =
-                            make_float4(r[4 * h], r[4 * h + 1], r[4 * h + 2], r[4 * h + 3]);
+                        if (c_ok(p, crow + ncol(4 * h), 4))
+                            *reinterpret_cast<float4*>(crow + ncol(4 * h)) =
+                                make_float4(r[4 * h], r[4 * h + 1], r[4 * h + 2], r[4 * h + 3]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < TN; ++j)
-                        if (ncol(j) < p.N) crow[ncol(j) * p.csC] = r[j];
+                        if (ncol(j) < p.N && c_ok(p, crow + ncol(j) * p.csC, 1)) crow[ncol(j) * p.csC] = r[j];
                 }
             };
             if (p.accumulate) {
@@ -690,15 +705,17 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
                         if (vec) {
 #pragma unroll
                             for (int h = 0; h < TN / 4; ++h) {
-                                const float4 o = m < p.M ? *reinterpret_cast<const float4*>(crow + ncol(4 * h))
-                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                                const float4 o = (m < p.M && c_ok(p, crow + ncol(4 * h), 4))
+                                                     ? *reinterpret_cast<const float4*>(crow + ncol(4 * h))
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                                 old[i][4 * h] = o.x; old[i][4 * h + 1] = o.y;
                                 old[i][4 * h + 2] = o.z; old[i][4 * h + 3] = o.w;
                             }
                         } else {
 #pragma unroll
                             for (int j = 0; j < TN; ++j)
-                                old[i][j] = (m < p.M && ncol(j) < p.N) ? crow[ncol(j) * p.csC] : 0.0f;
+                                old[i][j] = (m < p.M && ncol(j) < p.N && c_ok(p, crow + ncol(j) * p.csC, 1))
+                                                ? crow[ncol(j) * p.csC] : 0.0f;
                         }
                     }
 #pragma unroll
@@ -801,6 +818,7 @@ cudaError_t launch_impl(const Problem& pr, const Plan& plan, int sm_count, cudaS
                    (pr.epi.act == kActNone || pr.epi.act == kActRelu) ? 1 : 0;
     p.ws_partial = nullptr;
     p.ws_flag = nullptr;
+    p.sc = pr.sc;
     if (plan.stream_k) {
         // Partials first, then one flag word per CTA (see workspace_bytes).
         p.ws_partial = static_cast<float2*>(plan.workspace);

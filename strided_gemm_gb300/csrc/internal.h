@@ -10,6 +10,11 @@
 
 namespace sbg {
 
+// Element offsets [lo, hi] from an operand's base pointer that lie inside the
+// memory the caller described (the host's span check before every launch).
+// Only the bounds checks of a debug build (SBGEMM_DEBUG) read them.
+struct ElemSpan { int64_t lo, hi; };
+
 // One call of the product, strides in fp32 elements (see include/sbgemm.h).
 // Fused epilogue of sbgemm_fused: out = act(alpha*acc (+ C_old) + D), with D
 // read through its own strides (epilogue.cuh applies it on the device).
@@ -19,6 +24,7 @@ struct EpiParams {
     int act;                 // SBGEMM_ACT_*
     int on;                  // D != nullptr || act != SBGEMM_ACT_NONE
     int d_vec4;              // D has unit stride along N and 16-byte aligned rows
+    ElemSpan d_span;         // debug builds: D's valid element offsets
 };
 
 struct Problem {
@@ -29,6 +35,7 @@ struct Problem {
     float alpha;
     int accumulate;
     EpiParams epi;           // all zero: the plain product
+    ElemSpan sa, sb, sc;     // debug builds: valid element offsets of A, B and C
 };
 
 // Per-device properties, read once per device and immutable afterwards.
@@ -77,6 +84,7 @@ struct AttnProblem {
     float alpha;
     int causal;
     int64_t q_len;           // rows per head for the causal position
+    ElemSpan sq, sk, sv, so; // debug builds: valid element offsets of Q, K, V and O
 };
 // C^T = B^T A^T as a problem of its own: A' = B^T, B' = A^T, C' = C^T, M' = N,
 // N' = M (the fused addend transposed alike).
@@ -134,6 +142,10 @@ cudaError_t launch_tf32_tc(const Problem& p, const Plan& plan, int sm_count, cud
 void tf32_tc_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
                       int k_split);
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream);
+
+// ---- status words of the kernels without bounded waits (debug bounds checks) ----
+unsigned int read_and_clear_status_gather(cudaStream_t stream);
+unsigned int read_and_clear_status_attention(cudaStream_t stream);
 
 // ---- failure-detection self-test (selftest.cu) ----------------------------------
 unsigned int read_and_clear_wait_status_selftest(cudaStream_t stream);

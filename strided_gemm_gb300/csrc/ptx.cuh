@@ -21,6 +21,7 @@ enum : unsigned int {
     kWaitPartial = 6,    // stream-K: exchanging partial sums between CTAs
     kWaitSelftestMbar = 7,   // self-test: an mbarrier phase nothing completes
     kWaitSelftestFlag = 8,   // self-test: a global flag nothing sets
+    kBoundsViolation = 9,    // debug build: an access outside its operand's span (skipped)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

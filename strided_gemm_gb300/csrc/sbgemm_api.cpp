@@ -287,7 +287,8 @@ Problem make_problem(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
     p.M = M; p.N = N; p.K = K; p.batch = batch;
     p.alpha = alpha;
     p.accumulate = accumulate ? 1 : 0;
-    p.epi = EpiParams{nullptr, 0, 0, 0, SBGEMM_ACT_NONE, 0, 0};
+    p.epi = EpiParams{nullptr, 0, 0, 0, SBGEMM_ACT_NONE, 0, 0, ElemSpan{0, -1}};
+    p.sa = p.sb = p.sc = ElemSpan{0, -1};
     return p;
 }
 
@@ -299,6 +300,7 @@ Problem transposed_problem(const Problem& p) {
     q.B = p.A; q.rsB = p.csA; q.csB = p.rsA; q.bsB = p.bsA;
     q.rsC = p.csC; q.csC = p.rsC;
     q.M = p.N; q.N = p.M;
+    q.sa = p.sb; q.sb = p.sa;
     q.epi.rsD = p.epi.csD; q.epi.csD = p.epi.rsD;
     q.epi.d_vec4 = q.epi.D && (q.epi.csD == 1 || q.N == 1) &&
                    (reinterpret_cast<uintptr_t>(q.epi.D) % 16 == 0) && q.epi.rsD % 4 == 0 &&
@@ -372,6 +374,12 @@ int run(Problem& p, const sbgemm_options& o, void* stream) {
     if (p.K > 0 && (!span_in_allocation(p.A, sa) || !span_in_allocation(p.B, sb)))
         return SBGEMM_ERR_NOT_DEVICE_MEMORY;
     if (p.epi.D && !span_in_allocation(p.epi.D, sd)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+
+    // The validated spans, for the bounds checks of a debug build.
+    p.sa = ElemSpan{sa.lo, sa.hi};
+    p.sb = ElemSpan{sb.lo, sb.hi};
+    p.sc = ElemSpan{sc.lo, sc.hi};
+    if (p.epi.D) p.epi.d_span = ElemSpan{sd.lo, sd.hi};
 
     Plan plan;
     st = make_plan(p, o, props->sm_count, false, &plan);
@@ -486,7 +494,7 @@ int sbgemm_fused(const float* A, int64_t rsA, int64_t csA, int64_t bsA,
                             epi->rsD % 4 == 0 && epi->bsD % 4 == 0;
         p.epi = EpiParams{epi->D, epi->rsD, epi->csD, epi->bsD, epi->activation,
                           (epi->D != nullptr || epi->activation != SBGEMM_ACT_NONE) ? 1 : 0,
-                          d_vec4 ? 1 : 0};
+                          d_vec4 ? 1 : 0, ElemSpan{0, -1}};
     }
     return run(p, o, stream);
 }
@@ -534,7 +542,9 @@ int sbgemm_attention_ex(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
         !span_in_allocation(O, so))
         return SBGEMM_ERR_NOT_DEVICE_MEMORY;
     AttnProblem a{Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV, O, rsO, csO, bsO,
-                  M, N, D, Dv, batch, alpha, causal, causal ? q_len : M};
+                  M, N, D, Dv, batch, alpha, causal, causal ? q_len : M,
+                  ElemSpan{sq.lo, sq.hi}, ElemSpan{sk.lo, sk.hi}, ElemSpan{sv.lo, sv.hi},
+                  ElemSpan{so.lo, so.hi}};
     // TF32 on the tensor cores when asked for and the operands suit tensor
     // maps; otherwise the fp32 kernel (or, when forced, unsupported).
     const bool tc = o.math == SBGEMM_MATH_TF32 && attention_tc_supported(a);
@@ -587,9 +597,13 @@ int sbgemm_device_status(void* stream, int* where_out) {
     const unsigned int code_tc = read_and_clear_wait_status_tf32(s);
     const unsigned int code_st = read_and_clear_wait_status_selftest(s);
     const unsigned int code_at = read_and_clear_wait_status_attention_tc(s);
+    const unsigned int code_g = read_and_clear_status_gather(s);
+    const unsigned int code_a = read_and_clear_status_attention(s);
     if (code == 0) code = code_tc;
     if (code == 0) code = code_st;
     if (code == 0) code = code_at;
+    if (code == 0) code = code_g;
+    if (code == 0) code = code_a;
     if (code != 0) {
         if (where_out) *where_out = (int)code;
         return SBGEMM_ERR_DEVICE_TIMEOUT;

@@ -39,6 +39,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "debug_check.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -138,6 +139,7 @@ struct Params {
     EpiParams epi;                // fused epilogue (epilogue.cuh); epi.on == 0: none
     float4* ws_partial;           // [grid][8 chunks][8 quads][128 rows] partial sums
     unsigned int* ws_flag;        // [grid] partial-ready flags, zeroed before launch
+    ElemSpan sc;                  // debug builds: C's valid element offsets
 };
 
 
@@ -486,7 +488,9 @@ if constexpr (COLC) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = p.alpha * v[e];
         }
-        if (drow) {
+        if (drow && (!kDebugChecks || (dbg_in_span(p.epi.D, drow + n0 * p.epi.csD, p.epi.d_span, &g_wait_status) &&
+                                        dbg_in_span(p.epi.D, drow + (n0 + 31 < p.N ? n0 + 31 : p.N - 1) * p.epi.csD,
+                                                    p.epi.d_span, &g_wait_status)))) {
             if (p.epi.d_vec4 && n0 + 32 <= p.N) {
                 const float4* d4 = reinterpret_cast<const float4*>(drow + n0);
 #pragma unroll
@@ -636,7 +640,9 @@ __device__ __forceinline__ void epilogue(typename TCfg<MN>::Smem& sh, uint32_t t
                 if (p.accumulate) {
                     float o[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = n0 + e < p.N ? crow[(n0 + e) * p.csC] : 0.0f;
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = (n0 + e < p.N && dbg_in_span(p.C, crow + (n0 + e) * p.csC, p.sc, &g_wait_status))
+                                   ? crow[(n0 + e) * p.csC] : 0.0f;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = fmaf(p.alpha, v[e], o[e]);
                 } else {
@@ -646,9 +652,9 @@ __device__ __forceinline__ void epilogue(typename TCfg<MN>::Smem& sh, uint32_t t
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int64_t n = n0 + e;
-                    if (n < p.N) {
+                    if (n < p.N && dbg_in_span(p.C, crow + n * p.csC, p.sc, &g_wait_status)) {
                         float r = v[e];
-                        if (p.epi.on) r = finish(p.epi, r, tc.b, m, n);
+                        if (p.epi.on) r = finish(p.epi, r, tc.b, m, n, &g_wait_status);
                         crow[n * p.csC] = r;
                     }
                 }
@@ -828,6 +834,7 @@ cudaError_t launch_mn(const Problem& pr, const Plan& plan, cudaStream_t stream) 
     p.epi = pr.epi;
     p.ws_partial = nullptr;
     p.ws_flag = nullptr;
+    p.sc = pr.sc;
     if (plan.stream_k) {
         p.ws_partial = static_cast<float4*>(plan.workspace);
         p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<char*>(plan.workspace) +

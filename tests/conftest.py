@@ -19,6 +19,18 @@ def pytest_collection_modifyitems(config, items):
     pass
 
 
+@pytest.fixture(autouse=True)
+def _device_status_after_each_gpu_test(request):
+    """With SBGEMM_CHECK_STATUS=1 (the debug-build run), every GPU test must
+    leave the device status words clean: no bounded wait ran out and no
+    bounds check of the debug build fired."""
+    yield
+    if os.environ.get("SBGEMM_CHECK_STATUS") == "1" and request.node.get_closest_marker("gpu"):
+        import strided_gemm_gb300 as sg
+        st, where = sg.sbgemm_device_status()
+        assert st == sg.SBGEMM_OK, f"device status {st} (code {where}) after {request.node.nodeid}"
+
+
 @pytest.fixture(scope="session")
 def oracle_lib():
     import oracle

@@ -8,6 +8,7 @@ on the tf32 path; integer-valued inputs must match bit for bit.
 import numpy as np
 import pytest
 
+import oracle
 import strided_gemm_gb300 as sg
 import workloads as wl
 from strided_gemm_gb300 import build as sgbuild
@@ -214,8 +215,14 @@ def test_torch_tensor_helper(torch):
     C = torch.empty(3, 70, 50, device="cuda")
     sg.matmul(A, W.t().unsqueeze(0).expand(3, 90, 50), C)
     torch.cuda.synchronize()
-    want = (A.double() @ W.t().double()).float()
-    assert torch.allclose(C, want, atol=1e-4, rtol=1e-5)
+    # The oracle on the same memory: W [50, 90] read as B[k][n] = W[n][k],
+    # shared by the three batch entries.
+    a = wl.Operand(A.cpu().numpy().ravel(), 0, 90, 1, 70 * 90)
+    w = wl.Operand(W.cpu().numpy().ravel(), 0, 1, 90, 0)
+    c0 = wl.Operand(np.zeros(3 * 70 * 50, np.float32), 0, 50, 1, 70 * 50)
+    ref, bound = oracle.product(a, w, c0, 70, 50, 90, 3, 1.0, 0)
+    got = C.cpu().numpy().astype(np.float64)
+    assert bool((np.abs(got - ref) <= gu.TOL_FFMA * bound).all())
 
 
 STREAM_K_SHAPES = [
@@ -385,12 +392,16 @@ def test_linear_backward_helper(torch, workspace, math):
     sg.linear_backward(G.cuda(), X.cuda(), W.cuda(), dX, dW, accumulate_dW=True,
                        workspace=workspace, math=m)
     torch.cuda.synchronize()
-    want_dX = G.double() @ W.double()
-    want_dW = dW0.double() + G.double().t() @ X.double()
-    bound_dX = G.double().abs() @ W.double().abs()
-    bound_dW = dW0.double().abs() + G.double().abs().t() @ X.double().abs()
-    assert bool(((dX.cpu().double() - want_dX).abs() <= tol * bound_dX).all())
-    assert bool(((dW.cpu().double() - want_dW).abs() <= tol * bound_dW).all())
+    # The oracle on the same memory: dX = G W (G [T, out], W [out, in]) and
+    # dW = dW0 + G^T X (G read with swapped strides, X [T, in]).
+    g = G.numpy().ravel()
+    zero = wl.Operand(np.zeros(T * d_in, np.float32), 0, d_in, 1, 0)
+    want_dX, bound_dX = oracle.product(wl.Operand(g, 0, d_out, 1, 0), wl.Operand(W.numpy().ravel(), 0, d_in, 1, 0),
+                                       zero, T, d_in, d_out, 1, 1.0, 0)
+    want_dW, bound_dW = oracle.product(wl.Operand(g, 0, 1, d_out, 0), wl.Operand(X.numpy().ravel(), 0, d_in, 1, 0),
+                                       wl.Operand(dW0.numpy().ravel(), 0, d_in, 1, 0), d_out, d_in, T, 1, 1.0, 1)
+    assert bool((np.abs(dX.cpu().double().numpy() - want_dX[0]) <= tol * bound_dX[0]).all())
+    assert bool((np.abs(dW.cpu().double().numpy() - want_dW[0]) <= tol * bound_dW[0]).all())
 
 
 # ---- TF32 tensor-core path (opt-in) -------------------------------------------
