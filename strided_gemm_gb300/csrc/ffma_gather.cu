@@ -44,29 +44,69 @@ struct Split {
 };
 
 // Loads one operand's R x BK slice (R = rows of the tile: BM for A, BN for B).
-// `rs` steps along R, `ks` along K.  RFAST: consecutive threads take
-// consecutive R indices (unit stride along R); otherwise consecutive K.
+// `rs` steps along R, `ks` along K.  RFAST: the thread-to-element map runs
+// along R first (the operand's smaller stride is along R); otherwise along K.
+// With a unit stride along that fast index and alignment to match (checked
+// on the host), each thread fetches `vec` = 2 or 4 consecutive elements with
+// one 8- or 16-byte load; a vector that crosses a ragged edge of the tile or
+// of K falls back to guarded scalar loads of its elements.
 template <int R, int BK, bool RFAST>
 struct SliceLoader {
     static constexpr int kPer = R * BK / kThreads;   // elements per thread
+    static_assert(kPer % 4 == 0, "whole vectors of 4");
     float v[kPer];
+    int vec;           // elements per load: 1, 2 or 4 (vector i holds v[i * vec ..])
     int64_t off0;      // element offset of this thread's first element at k0 = 0
-    int64_t step_i;    // offset between this thread's consecutive elements
+    int64_t step_i;    // offset between this thread's consecutive vectors
     int64_t step_k;    // offset step of one BK slice
     int r_first, k_first;
+    int line_step;     // slow-index step between consecutive vectors
 
-    __device__ __forceinline__ void init(int tid, int64_t r0, int64_t rs, int64_t ks) {
+    __device__ __forceinline__ void init(int tid, int64_t r0, int64_t rs, int64_t ks, int vec_) {
+        vec = vec_;
+        const int per_line = (RFAST ? R : BK) / vec;    // threads along the fast index
+        const int fast = (tid % per_line) * vec, slow = tid / per_line;
+        line_step = kThreads / per_line;
         if (RFAST) {
-            r_first = tid % R;
-            k_first = tid / R;
-            step_i = (int64_t)(kThreads / R) * ks;
+            r_first = fast;
+            k_first = slow;
+            step_i = (int64_t)line_step * ks;
         } else {
-            k_first = tid % BK;
-            r_first = tid / BK;
-            step_i = (int64_t)(kThreads / BK) * rs;
+            k_first = fast;
+            r_first = slow;
+            step_i = (int64_t)line_step * rs;
         }
         off0 = (r0 + r_first) * rs + (int64_t)k_first * ks;
         step_k = (int64_t)BK * ks;
+    }
+
+    template <int V>
+    __device__ __forceinline__ void load_v(const float* __restrict__ base, int64_t off, int64_t rows_left,
+                                           int64_t k_left, const float* op, const ElemSpan& span) {
+#pragma unroll
+        for (int i = 0; i < kPer / V; ++i) {
+            const int r = RFAST ? r_first : r_first + i * line_step;
+            const int k = RFAST ? k_first + i * line_step : k_first;
+            const float* a = base + off + i * step_i;
+            // The vector's elements run along the fast index, whose stride is
+            // 1 when V > 1.
+            const bool whole = RFAST ? (r + V - 1 < rows_left && k < k_left)
+                                     : (r < rows_left && k + V - 1 < k_left);
+            if (V == 4 && whole && dbg_in_span(op, a, span, &g_status) && dbg_in_span(op, a + 3, span, &g_status)) {
+                const float4 x = __ldg(reinterpret_cast<const float4*>(a));
+                v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+            } else if (V == 2 && whole && dbg_in_span(op, a, span, &g_status) &&
+                       dbg_in_span(op, a + 1, span, &g_status)) {
+                const float2 x = __ldg(reinterpret_cast<const float2*>(a));
+                v[2 * i] = x.x; v[2 * i + 1] = x.y;
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const bool ok = RFAST ? (r + e < rows_left && k < k_left) : (r < rows_left && k + e < k_left);
+                    v[V * i + e] = (ok && dbg_in_span(op, a + e, span, &g_status)) ? __ldg(a + e) : 0.0f;
+                }
+            }
+        }
     }
 
     // Fetch slice kt (k0 = kt*BK).  rows_left = valid rows from r0, k_left = K - k0.
@@ -75,24 +115,36 @@ struct SliceLoader {
                                          int64_t rows_left, int64_t k_left, const float* op,
                                          const ElemSpan& span) {
         const int64_t off = off0 + kt * step_k;
+        if (vec == 4) load_v<4>(base, off, rows_left, k_left, op, span);
+        else if (vec == 2) load_v<2>(base, off, rows_left, k_left, op, span);
+        else load_v<1>(base, off, rows_left, k_left, op, span);
+    }
+
+    template <int V, int LD>
+    __device__ __forceinline__ void store_v(float (*S)[LD]) const {
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            int r = RFAST ? r_first : r_first + i * (kThreads / BK);
-            int k = RFAST ? k_first + i * (kThreads / R) : k_first;
-            bool ok = (r < rows_left) && (k < k_left);
-            const float* a = base + off + i * step_i;
-            v[i] = (ok && dbg_in_span(op, a, span, &g_status)) ? __ldg(a) : 0.0f;
+        for (int i = 0; i < kPer / V; ++i) {
+            const int r = RFAST ? r_first : r_first + i * line_step;
+            const int k = RFAST ? k_first + i * line_step : k_first;
+            if (RFAST && V == 4) {
+                *reinterpret_cast<float4*>(&S[k][r]) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            } else if (RFAST && V == 2) {
+                *reinterpret_cast<float2*>(&S[k][r]) = make_float2(v[2 * i], v[2 * i + 1]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    if (RFAST) S[k][r + e] = v[V * i + e];
+                    else S[k + e][r] = v[V * i + e];
+                }
+            }
         }
     }
 
     template <int LD>
     __device__ __forceinline__ void store(float (*S)[LD]) const {
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            int r = RFAST ? r_first : r_first + i * (kThreads / BK);
-            int k = RFAST ? k_first + i * (kThreads / R) : k_first;
-            S[k][r] = v[i];
-        }
+        if (vec == 4) store_v<4>(S);
+        else if (vec == 2) store_v<2>(S);
+        else store_v<1>(S);
     }
 };
 
@@ -100,7 +152,8 @@ struct SliceLoader {
 // others keep their registers.
 template <int BM, int BN, int BK, int TM, int TN, bool A_MFAST, bool B_NFAST, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
-gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n, const Split sp) {
+gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n, const Split sp,
+                   const int va, const int vb) {
     static_assert((BM / TM) * (BN / TN) == kThreads, "thread grid must cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "micro-tile is built from float4 rows");
     constexpr int LDA = BM + 4;   // +4 floats keeps float4 alignment of each k-row
@@ -138,8 +191,8 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
 
         SliceLoader<BM, BK, A_MFAST> la;
         SliceLoader<BN, BK, B_NFAST> lb;
-        la.init(tid, m0, p.rsA, p.csA);
-        lb.init(tid, n0, p.csB, p.rsB);
+        la.init(tid, m0, p.rsA, p.csA, va);
+        lb.init(tid, n0, p.csB, p.rsB, vb);
 
         // Accumulators of adjacent row pairs (i, i+1) of one column, for the
         // packed FMA (fma.rn.f32x2: each lane rounds like fmaf, so every output
@@ -277,6 +330,20 @@ cudaError_t launch_variant(const Problem& p, const Plan& plan, cudaStream_t stre
     auto mag = [](int64_t x) { return x < 0 ? -x : x; };
     const bool a_fast = mag(p.rsA) < mag(p.csA);
     const bool b_fast = mag(p.csB) < mag(p.rsB);
+    // Vector width of each operand's loads: the fast index has stride +1 and
+    // the base and the other strides keep every vector of `v` elements
+    // aligned to 4 v bytes (tile origins and thread offsets along the fast
+    // index are multiples of 4).
+    auto width = [&](const float* base, int64_t fast, int64_t other, int64_t bs) {
+        if (fast != 1) return 1;
+        for (int v : {4, 2})
+            if (reinterpret_cast<uintptr_t>(base) % (4u * v) == 0 && other % v == 0 &&
+                (p.batch == 1 || bs % v == 0))
+                return v;
+        return 1;
+    };
+    const int va = width(p.A, a_fast ? p.rsA : p.csA, a_fast ? p.csA : p.rsA, p.bsA);
+    const int vb = width(p.B, b_fast ? p.csB : p.rsB, b_fast ? p.rsB : p.csB, p.bsB);
     Split sp{1, nullptr, nullptr};
     if (SPLIT) {
         sp.pieces = plan.k_pieces;
@@ -290,19 +357,20 @@ cudaError_t launch_variant(const Problem& p, const Plan& plan, cudaStream_t stre
               (unsigned)(p.batch < 65535 ? p.batch : 65535), (unsigned)sp.pieces);
     dim3 block(kThreads);
     if (a_fast && b_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, true, true, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, true, true, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp, va, vb);
     else if (a_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, true, false, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, true, false, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp, va, vb);
     else if (b_fast)
-        gather_ffma_kernel<BM, BN, BK, TM, TN, false, true, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, false, true, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp, va, vb);
     else
-        gather_ffma_kernel<BM, BN, BK, TM, TN, false, false, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp);
+        gather_ffma_kernel<BM, BN, BK, TM, TN, false, false, SPLIT><<<grid, block, 0, stream>>>(p, plan.tiles_m, plan.tiles_n, sp, va, vb);
     return cudaGetLastError();
 }
 
 constexpr GatherConfig kConfigs[] = {
     {128, 128, 16, kThreads, 2},   // 8 x 8 micro-tiles
     {64, 64, 16, kThreads, 2},     // 4 x 4 micro-tiles, for small problems
+    {128, 64, 16, kThreads, 2},    // 8 x 4 micro-tiles, for narrow or ragged N
 };
 
 }  // namespace
@@ -312,9 +380,20 @@ int gather_config_count() { return (int)(sizeof(kConfigs) / sizeof(kConfigs[0]))
 GatherConfig gather_config(int variant) { return kConfigs[variant]; }
 
 int gather_pick_variant(const Problem& p, int sm_count) {
-    // Prefer the large tile when it still gives every SM at least one CTA.
-    const int64_t big = ((p.M + 127) / 128) * ((p.N + 127) / 128) * p.batch;
-    return big >= sm_count ? 0 : 1;
+    // The tile shape with the smallest estimated time: waves of CTAs (two
+    // per SM) times the tile's work, the smaller tiles charged 4/3 (64 x 64)
+    // and 7/6 (128 x 64) for their lower arithmetic per load.  Large tiles
+    // win on big products; smaller ones when the large tiles would leave a
+    // nearly empty last wave (a 64-clip spectrogram of 125 frames x 514
+    // bins: 320 tiles of 128 x 128 on 304 slots, 576 of 128 x 64).
+    auto cost = [&](int v, double charge) {
+        const GatherConfig g = kConfigs[v];
+        const int64_t tiles = ((p.M + g.bm - 1) / g.bm) * ((p.N + g.bn - 1) / g.bn) * p.batch;
+        const int64_t slots = (int64_t)sm_count * g.ctas_per_sm;
+        return (double)((tiles + slots - 1) / slots) * g.bm * g.bn * charge;
+    };
+    const double c0 = cost(0, 1.0), c1 = cost(1, 4.0 / 3.0), c2 = cost(2, 7.0 / 6.0);
+    return c0 <= c1 && c0 <= c2 ? 0 : (c2 <= c1 ? 2 : 1);
 }
 
 void gather_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
@@ -351,6 +430,7 @@ cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t 
         case 1:
             if (plan.k_pieces > 1) return launch_variant<64, 64, 16, 4, 4, true>(p, plan, stream);
             return launch_variant<64, 64, 16, 4, 4, false>(p, plan, stream);
+        case 2: return launch_variant<128, 64, 16, 8, 4, false>(p, plan, stream);
         default: return cudaErrorInvalidValue;
     }
 }

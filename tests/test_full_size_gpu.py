@@ -7,7 +7,8 @@ schedule, through the call a caller with a workspace makes:
 - TMA-fed FFMA, independent K pieces of a few-tile long-K product (f1dwa);
 - TMA-fed FFMA, data-parallel over a batch of 128 (c3) and the 512 x 64
   tiles of a narrow accumulating product (c4);
-- strided gather, K pieces of a small product (c2a);
+- strided gather, K pieces of a small product (c2a), and the 128 x 64 tiles
+  of the spectrogram's overlapping frames (f4spec);
 - TF32 tensor cores, the transposed plan with split K (c5c, real and
   integer) and both operands MN-major with split K (f1dwb).
 
@@ -47,6 +48,7 @@ CASES = [
     ("c3", "real", sg.MATH_FP32, "tma_ffma", sg.STREAM_K_NONE),
     ("c4", "real", sg.MATH_FP32, "tma_ffma", sg.STREAM_K_NONE),
     ("c2a", "real", sg.MATH_FP32, "gather_ffma", sg.STREAM_K_PIECES),
+    ("f4spec", "real", sg.MATH_FP32, "gather_ffma", sg.STREAM_K_NONE),
     ("c5c", "real", sg.MATH_TF32, "tma_tf32", sg.STREAM_K_PIECES),
     ("c5c", "int", sg.MATH_TF32, "tma_tf32", sg.STREAM_K_PIECES),
     ("f1dwb", "real", sg.MATH_TF32, "tma_tf32", sg.STREAM_K_PIECES),
@@ -67,6 +69,8 @@ def test_full_size_every_element(torch, workspace, name, values, math, path, sch
     kw = dict(math=math, workspace=workspace.data_ptr(), workspace_bytes=workspace.numel())
     plan = sg.sbgemm_plan(*args[:16], case.accumulate, **kw)
     assert plan["path_name"] == path and plan["stream_k"] == schedule, plan
+    if name == "f4spec":
+        assert (plan["tile_m"], plan["tile_n"]) == (128, 64), plan
     sg.sbgemm_ex(*args, **kw)
     torch.cuda.synchronize()
     got = dC.cpu().numpy()
