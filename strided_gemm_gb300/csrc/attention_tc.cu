@@ -8,17 +8,23 @@
 // MMA's M) that share every K and V block, head dimension 64, keys in blocks
 // of 128.  Per block j and tile t:
 //   S_tj = Q_t K_j^T   tcgen05.mma kind::tf32, M 128 x N 128 x K 64, into TMEM
-//   P_tj = exp2(alpha log2(e) S_tj - m_t)   one thread per query row: a pass
-//          over the row's 128 scores (tcgen05.ld) for the block maximum, then
-//          the exponentials, written back over S_tj (tcgen05.st); the row sum
-//          l_t in registers
+//   P_tj = exp2(alpha log2(e) S_tj - m_t)   one thread per query row, in one
+//          pass over the row's 128 scores (tcgen05.ld, two 64-column
+//          chunks), written back over S_tj (tcgen05.st); the row sum l_t in
+//          registers
 //   O_t += P_tj V_j   M 128 x N 64 x K 128, A = P_tj from TMEM, accumulated in
 //          TMEM by the MMA
 // and O_t / l_t is stored at the end.  The reference maximum m_t of a row is
-// raised only when a block's maximum exceeds it by more than 8 (a factor of
-// 2^8): then O_t and l_t are scaled by exp2(m_old - m_new), O_t in TMEM by the
-// row's own thread.  Between raises the exponentials stay below 2^8, and O / l
-// is the same function either way.
+// set from its first kept chunk and raised only when a chunk's exponent
+// argument exceeds 8 (a factor of 2^8): then what the row has summed and
+// written (l_t, the block's earlier P, O_t in TMEM) is scaled by exp2(m_old -
+// m_new) by the row's own thread.  Between raises the exponentials stay below
+// 2^8, and O / l is the same function either way.
+//
+// Q_t lands by TMA in the V^T buffers (not yet in use) and the row threads
+// copy it into TMEM, the A operand of the score MMAs, so that shared memory
+// holds two V^T buffers: the transpose of block j+1 then overlaps the P V
+// MMAs of block j instead of waiting for them.
 //
 // The MMA lane issues, per block: P V_0, then (once P V_0 has read P_0) the
 // scores of tile 0's next block, then the same for tile 1.  So each tile's
@@ -32,7 +38,8 @@
 // MMA sequences with every operand one add away.
 // Roles (12 warps), all waits bounded (a timeout records a status code and
 // the role leaves its loop):
-//   warp 0       TMA: both Q tiles once; K_j (two 128-byte swizzled boxes of
+//   warp 0       TMA: both Q tiles once (into the V^T buffers); K_j (two
+//                128-byte swizzled boxes of
 //                32 along the head dimension) and V_j (eight raw 32 x 32
 //                boxes) into a 2-stage ring;
 //   warp 1       one lane issues the MMAs;
@@ -41,7 +48,7 @@
 //                quads, conflict-free under the swizzle);
 //   warps 4-7    softmax of tile 0, one TMEM lane quarter each;
 //   warps 8-11   softmax of tile 1.
-// TMEM: S / P (2 tiles x 128 columns) and O (2 x 64).
+// TMEM: S / P (2 tiles x 128 columns), O (2 x 64) and Q (2 x 64).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -51,7 +58,6 @@
 #include <cstring>
 
 #include "attention_tc.h"
-#include "debug_check.cuh"
 #include "ptx.cuh"
 
 namespace sbg {
@@ -75,7 +81,8 @@ constexpr int kBox = 32 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                         // S / P [t] at t * BN
 constexpr uint32_t kColO = kTiles * BN;               // O[t] at kColO + t * kD
-static_assert(kColO + kTiles * kD <= kTmemCols, "TMEM columns");
+constexpr uint32_t kColQ = kColO + kTiles * kD;       // Q[t] at kColQ + t * kD
+static_assert(kColQ + kTiles * kD <= kTmemCols, "TMEM columns");
 static_assert((kWarpSoft % 4) == 0 && kSoftWarps == 4, "each tile's softmax warps cover the four lane quarters");
 static_assert(kTiles == 2, "the softmax warps pick their tile's block count from two");
 static_assert(kD % 32 == 0 && BN == 128, "32-column TMEM transfers; 128-key blocks in two 64-column halves");
@@ -89,14 +96,16 @@ constexpr uint32_t idesc(int n) {
 constexpr uint32_t kIdescS = idesc(BN), kIdescPV = idesc(kD);
 
 struct Smem {
-    alignas(1024) float q[kTiles][kDA][BM * kAtom];       // Q tiles, K-major, head-dim atoms
-    alignas(1024) float k[kStages][kDA][BN * kAtom];      // K_j, K-major, same atoms
+    alignas(1024) float k[kStages][kDA][BN * kAtom];      // K_j, K-major, head-dim atoms
     alignas(1024) float vraw[kStages][kKA * kDA][kBox];   // V_j: box (key atom h, value atom g) at h kDA + g
-    alignas(1024) float vt[kKA][kD * kAtom];              // V_j^T: rows along the values, key atoms
+    // V_j^T in buffer j % 2: rows along the values, key atoms.  Before the
+    // first transpose, the Q tiles as TMA lands them ([tile][atom][row * 32]).
+    alignas(1024) float vt[2][kKA][kD * kAtom];
     uint64_t q_full;
+    uint64_t q_tmem;              // every row thread has copied its Q row into TMEM
     uint64_t k_full[kStages], k_empty[kStages];
     uint64_t v_full[kStages], v_empty[kStages];
-    uint64_t vt_full, vt_empty;
+    uint64_t vt_full[2], vt_empty[2];
     uint64_t s_full[kTiles];      // a tile's scores of the current block are in TMEM
     uint64_t p_full[kTiles];      // a tile's P of the current block is in TMEM
     uint64_t pv_done[kTiles];     // a tile's P V has read P and added into O
@@ -106,6 +115,13 @@ struct Smem {
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(sizeof(Smem::vt) == (size_t)kTiles * kDA * BM * kAtom * 4, "the Q tiles fill the V^T buffers");
+static_assert(sizeof(Smem::k[0]) == (size_t)kDA * BM * kAtom * 4, "a K stage holds one tile of O");
+
+// The landing place of Q tile t, atom a (in the V^T buffers).
+__device__ __forceinline__ float* q_stage(Smem& sh, int t, int a) {
+    return &sh.vt[0][0][0] + (size_t)(t * kDA + a) * BM * kAtom;
+}
 
 __device__ unsigned int g_wait_status = 0;
 
@@ -120,7 +136,6 @@ struct Params {
     int o_vec;                       // O rows unit-stride and 16-byte aligned
     int o_tma;                       // O goes out through its tensor map
     int bo;                          // O's batch coordinate follows blockIdx.x
-    ElemSpan so;                     // debug builds: O's valid element offsets
 };
 
 // Keys [0, n_end) a tile of rows starting at m0 needs: all of them, or
@@ -167,16 +182,19 @@ __device__ __forceinline__ void transpose_atom(const float* raw, float* dst, int
     }
 }
 
-// The scores of one tile: D = Q_t K_j^T, A (Q_t) and B (K_j) in 32-wide
-// K-major swizzled atoms in shared memory (descriptor low words a_lo, b_lo);
-// kD / 8 MMAs in straight-line code.
-__device__ __forceinline__ void mma_scores(uint32_t d, uint32_t a_lo, uint32_t b_lo) {
-    constexpr uint32_t kAAtom = (uint32_t)(BM * kAtom * 4) >> 4;   // next atom, in descriptor units
-    constexpr uint32_t kBAtom = (uint32_t)(BN * kAtom * 4) >> 4;
+// The scores of one tile: D = Q_t K_j^T, A (Q_t) in TMEM from column a, B
+// (K_j) in 32-wide K-major swizzled atoms of BN rows (descriptor low word
+// b_lo); kD / 8 MMAs in straight-line code.
+__device__ __forceinline__ void mma_scores(uint32_t d, uint32_t a, uint32_t b_lo) {
+    constexpr uint32_t kBAtom = (uint32_t)(BN * kAtom * 4) >> 4;   // next atom, in descriptor units
+    constexpr int kSteps = kD / kMmaK;
+    uint64_t bd[kSteps];
 #pragma unroll
-    for (int kk = 0; kk < kD / kMmaK; ++kk)
-        mma_tf32_ss_lo(d, a_lo + (uint32_t)(kk / 4) * kAAtom + (uint32_t)(kk & 3) * 2,
-                       b_lo + (uint32_t)(kk / 4) * kBAtom + (uint32_t)(kk & 3) * 2, kIdescS, kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < kSteps; ++kk)
+        bd[kk] = ((uint64_t)kDescHiSw128 << 32) | (b_lo + (uint32_t)(kk / 4) * kBAtom + (uint32_t)(kk & 3) * 2);
+#pragma unroll
+    for (int kk = 0; kk < kSteps; ++kk)
+        mma_tf32_ts_desc(d, a + (uint32_t)(kk * kMmaK), bd[kk], kIdescS, kk > 0 ? 1u : 0u);
 }
 
 // P V of one tile: O (+)= P_t V_j, A (P_t) in TMEM from column a, B (V_j^T) in
@@ -221,8 +239,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             mbar_init(&sh.v_full[s], 1);
             mbar_init(&sh.v_empty[s], kTransWarps);
         }
-        mbar_init(&sh.vt_full, kTransWarps);
-        mbar_init(&sh.vt_empty, 1);
+        mbar_init(&sh.q_tmem, kTiles * kSoftWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.vt_full[i], kTransWarps);
+            mbar_init(&sh.vt_empty[i], 1);
+        }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(&sh.s_full[t], 1);
             mbar_init(&sh.p_full[t], kSoftWarps);
@@ -258,7 +279,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 if (nb_t[t] == 0) continue;
 #pragma unroll
                 for (int a = 0; a < kDA; ++a)
-                    tma_load_3d(sh.q[t][a], &tq, &sh.q_full, kAtom * a, (int)(m0 + t * BM), zq);
+                    tma_load_3d(q_stage(sh, t, a), &tq, &sh.q_full, kAtom * a, (int)(m0 + t * BM), zq);
             }
             int j = 0;
             for (; j < nblk; ++j) {
@@ -292,15 +313,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     } else if (warp == 1) {
         // ---- MMA issuer ---------------------------------------------------
         if (lane == 0) {
-            bool ok = mbar_wait(&sh.q_full, 0);
-            // Descriptor low words of every shared-memory operand: stage
-            // offsets are whole multiples of 16 bytes.
+            // Q in TMEM (every row thread's copy), which also frees the
+            // V^T buffers for the transposer.
+            bool ok = mbar_wait(&sh.q_tmem, 0);
+            // Descriptor low words of every shared-memory operand: stage and
+            // buffer offsets are whole multiples of 16 bytes.
             const uint32_t k_lo0 = desc_lo_sw128(smem_u32(sh.k[0][0]));
             constexpr uint32_t kKStage = (uint32_t)sizeof(sh.k[0]) >> 4;
-            const uint32_t vt_lo = desc_lo_sw128(smem_u32(sh.vt[0]));
-            uint32_t q_lo[kTiles];
-#pragma unroll
-            for (int t = 0; t < kTiles; ++t) q_lo[t] = desc_lo_sw128(smem_u32(sh.q[t][0]));
+            const uint32_t vt_lo0 = desc_lo_sw128(smem_u32(sh.vt[0][0]));
+            constexpr uint32_t kVtBuf = (uint32_t)sizeof(sh.vt[0]) >> 4;
             // The scores of block j for tile t, once P V_t of block j-1 has
             // read P_t (the same TMEM columns).  K_j is released after the
             // last tile's scores.
@@ -308,7 +329,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 if (j >= nb_t[t]) return true;
                 if (j > 0 && !mbar_wait(&sh.pv_done[t], (uint32_t)((j - 1) & 1))) return false;
                 tc_fence_after();
-                mma_scores(tmem + kColS + (uint32_t)t * BN, q_lo[t], k_lo0 + (uint32_t)(j % kStages) * kKStage);
+                mma_scores(tmem + kColS + (uint32_t)t * BN, tmem + kColQ + (uint32_t)t * kD,
+                           k_lo0 + (uint32_t)(j % kStages) * kKStage);
                 mma_commit(&sh.s_full[t]);
                 return true;
             };
@@ -318,7 +340,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 release_k(0);
             }
             for (int j = 0; j < nblk && ok; ++j) {
-                if (!mbar_wait(&sh.vt_full, (uint32_t)(j & 1))) { ok = false; break; }
+                if (!mbar_wait(&sh.vt_full[j & 1], (uint32_t)((j >> 1) & 1))) { ok = false; break; }
                 const bool next = j + 1 < nblk;
                 if (next && !mbar_wait(&sh.k_full[(j + 1) % kStages], (uint32_t)(((j + 1) / kStages) & 1))) {
                     ok = false;
@@ -329,12 +351,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     if (j < nb_t[t]) {
                         if (!mbar_wait(&sh.p_full[t], (uint32_t)(j & 1))) { ok = false; break; }
                         tc_fence_after();
-                        mma_pv(tmem + kColO + (uint32_t)t * kD, tmem + kColS + (uint32_t)t * BN, vt_lo,
-                               j > 0 ? 1u : 0u);
+                        mma_pv(tmem + kColO + (uint32_t)t * kD, tmem + kColS + (uint32_t)t * BN,
+                               vt_lo0 + (uint32_t)(j & 1) * kVtBuf, j > 0 ? 1u : 0u);
                         mma_commit(&sh.pv_done[t]);
                         if (j == nb_t[t] - 1) mma_commit(&sh.o_done[t]);
                     }
-                    if (t == kTiles - 1) mma_commit(&sh.vt_empty);   // after every P V of block j
+                    if (t == kTiles - 1) mma_commit(&sh.vt_empty[j & 1]);   // after every P V of block j
                     if (next && !scores(t, j + 1)) { ok = false; break; }
                 }
                 if (!ok) break;
@@ -348,22 +370,25 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     } else if (warp < kWarpSoft) {
         // ---- V_j -> V_j^T -------------------------------------------------
         const int t = threadIdx.x - 2 * 32;
-        for (int j = 0; j < nblk; ++j) {
-            const int s = j % kStages;
+        // The V^T buffers hold Q until the row threads have copied it.
+        const bool q_out = nblk == 0 || mbar_wait(&sh.q_tmem, 0);
+        if (!q_out) record_status(&g_wait_status, kWaitFull);
+        for (int j = 0; q_out && j < nblk; ++j) {
+            const int s = j % kStages, buf = j & 1;
             if (!mbar_wait(&sh.v_full[s], (uint32_t)((j / kStages) & 1))) {
                 record_status(&g_wait_status, kWaitFull);
                 break;
             }
-            if (j >= 1 && !mbar_wait(&sh.vt_empty, (uint32_t)((j - 1) & 1))) {
+            if (j >= 2 && !mbar_wait(&sh.vt_empty[buf], (uint32_t)(((j >> 1) - 1) & 1))) {
                 record_status(&g_wait_status, kWaitEmpty);
                 break;
             }
 #pragma unroll
-            for (int h = 0; h < kKA; ++h) transpose_atom(sh.vraw[s][h * kDA], sh.vt[h], t);
+            for (int h = 0; h < kKA; ++h) transpose_atom(sh.vraw[s][h * kDA], sh.vt[buf][h], t);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&sh.vt_full);
+                mbar_arrive(&sh.vt_full[buf]);
                 mbar_arrive(&sh.v_empty[s]);
             }
         }
@@ -381,7 +406,30 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         const int64_t last_key = pos < p.N - 1 ? pos : p.N - 1;
         const float scale = p.scale_log2;
         float m_ref = -INFINITY, l_run = 0.0f;
-        bool ok = nbt > 0;
+        bool ok = nblk > 0;
+        // The row's Q into TMEM (lane = row, one column per head-dim element).
+        // Every row thread arrives, including those of a tile with no rows.
+        if (ok) {
+            ok = mbar_wait(&sh.q_full, 0);
+            if (ok && nbt > 0) {
+#pragma unroll
+                for (int a = 0; a < kDA; ++a) {
+                    const float* src = q_stage(sh, t, a);
+                    float v[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 x = *reinterpret_cast<const float4*>(src + row * kAtom + ((c ^ (row & 7)) << 2));
+                        v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
+                    }
+                    tmem_st32_nowait(tmem + lanes + kColQ + (uint32_t)(t * kD + a * 32), v);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.q_tmem);
+        }
+        ok = ok && nbt > 0;
         for (int j = 0; ok && j < nbt; ++j) {
             // The scores of block j were issued after P V of block j-1, so
             // their barrier also tells that O is settled.
@@ -392,77 +440,95 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             const int64_t last = last_key - (int64_t)j * BN;
             const int lim = last < 0 ? -1 : (last >= BN ? BN - 1 : (int)last);
             const bool whole = __all_sync(0xffffffffu, lim == BN - 1);
-            // Pass 1: the block's largest scaled score.  Scaling is monotonic,
-            // so it is the scaled largest (or, for a negative alpha, smallest)
-            // score.
-            float part[8];
+            // One pass over the block in two 64-column chunks: exponent
+            // arguments against the row's reference maximum m_ref, their
+            // largest value checked against the headroom.  Only a row's first
+            // kept chunk needs its maximum first (m_ref is then -inf).
+            float corr_blk = 1.0f;      // this block's scaling of O (raises)
+            float psum[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) part[i] = scale >= 0.0f ? -INFINITY : INFINITY;
+            for (int i = 0; i < 8; ++i) psum[i] = 0.0f;
 #pragma unroll
             for (int hh = 0; hh < BN / 64; ++hh) {
                 float s[64];
                 tmem_ld64(s_addr + 64 * hh, s);
-                if (scale >= 0.0f) {
+                if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+                    if (m_ref == -INFINITY) {
+                        // The chunk's largest scaled score (-inf if every key
+                        // of the chunk is masked).
+                        float mx[8];
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (whole || 64 * hh + c <= lim) part[c & 7] = fmaxf(part[c & 7], s[c]);
-                } else {
+                        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (whole || 64 * hh + c <= lim) part[c & 7] = fminf(part[c & 7], s[c]);
+                        for (int c = 0; c < 64; ++c)
+                            if (whole || 64 * hh + c <= lim) mx[c & 7] = fmaxf(mx[c & 7], s[c] * scale);
+                        m_ref = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    }
                 }
-            }
-            float ext;
-            if (scale >= 0.0f)
-                ext = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
-                            fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
-            else
-                ext = fminf(fminf(fminf(part[0], part[1]), fminf(part[2], part[3])),
-                            fminf(fminf(part[4], part[5]), fminf(part[6], part[7])));
-            const float m_blk = lim >= 0 ? ext * scale : -INFINITY;
-            // Raise the reference maximum only past the headroom; O and l
-            // follow with the factor exp2(m_old - m_new) (0 from -inf).
-            const bool raise = m_blk > m_ref + kRaise;
-            float corr = 1.0f;
-            if (raise) {
-                corr = ex2_approx(m_ref - m_blk);
-                m_ref = m_blk;
-                l_run *= corr;
-            }
-            // Pass 2: probabilities relative to the reference maximum (a row
-            // with no kept key so far has m_ref = -inf and every term
-            // masked), written over the scores.
-            const float neg = -m_ref;
+                const float neg = -m_ref;
+                float am[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) part[i] = 0.0f;
-#pragma unroll
-            for (int hh = 0; hh < BN / 64; ++hh) {
-                float s[64];
-                tmem_ld64(s_addr + 64 * hh, s);
+                for (int i = 0; i < 8; ++i) am[i] = -INFINITY;
                 if (whole) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) {
-                        s[c] = ex2_approx(fmaf(s[c], scale, neg));
-                        part[c & 7] += s[c];
+                        s[c] = fmaf(s[c], scale, neg);
+                        am[c & 7] = fmaxf(am[c & 7], s[c]);
                     }
                 } else {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) {
-                        s[c] = 64 * hh + c <= lim ? ex2_approx(fmaf(s[c], scale, neg)) : 0.0f;
-                        part[c & 7] += s[c];
+                        s[c] = 64 * hh + c <= lim ? fmaf(s[c], scale, neg) : -INFINITY;
+                        am[c & 7] = fmaxf(am[c & 7], s[c]);
                     }
+                }
+                const float amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])),
+                                         fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7])));
+                // Raise the reference past the headroom (rare): shift this
+                // chunk's arguments, and scale what the row has summed and
+                // written against the old reference by exp2(-shift).
+                const bool raise = amax > kRaise;
+                if (__any_sync(0xffffffffu, raise)) {
+                    const float shift = raise ? amax : 0.0f;
+                    const float corr = raise ? ex2_approx(-amax) : 1.0f;
+                    m_ref += shift;
+                    l_run *= corr;
+                    corr_blk *= corr;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) psum[i] *= corr;
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) s[c] -= shift;
+                    // P of the block's earlier chunks, already in TMEM.
+                    tmem_wait_st();
+#pragma unroll
+                    for (int g = 0; g < hh; ++g)
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            float q[32];
+                            tmem_ld32(s_addr + 64 * g + 32 * h2, q);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) q[e] *= corr;
+                            tmem_st32_nowait(s_addr + 64 * g + 32 * h2, q);
+                        }
+                }
+                // The probabilities over the scores (masked keys: exp2(-inf) = 0).
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    s[c] = ex2_approx(s[c]);
+                    psum[c & 7] += s[c];
                 }
                 tmem_st64_nowait(s_addr + 64 * hh, s);
             }
-            l_run += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-            if (j > 0 && __any_sync(0xffffffffu, raise)) {
-                // O row *= corr (1 for the rows that did not raise).
+            l_run += ((psum[0] + psum[1]) + (psum[2] + psum[3])) + ((psum[4] + psum[5]) + (psum[6] + psum[7]));
+            if (j > 0 && __any_sync(0xffffffffu, corr_blk != 1.0f)) {
+                // O row *= corr_blk (1 for the rows that did not raise).
 #pragma unroll
                 for (int h = 0; h < kD / 32; ++h) {
                     float o[32];
                     tmem_ld32(o_addr + 32 * h, o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= corr;
+                    for (int e = 0; e < 32; ++e) o[e] *= corr_blk;
                     tmem_st32_nowait(o_addr + 32 * h, o);
                 }
             }
@@ -477,17 +543,25 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         if (!ok) {
             if (nbt > 0) record_status(&g_wait_status, kWaitMma);
         } else if (p.o_tma) {
-            // O / l through the tile's Q buffer (the score MMAs that read it
-            // are done) in the swizzled layout of the O tensor map; each
-            // warp stores its 32 rows with one bulk tensor copy per head-dim
-            // atom, and the copy leaves out the rows past M.
+            // O / l through K stage t in the swizzled layout of the O tensor
+            // map; each warp stores its 32 rows with one bulk tensor copy per
+            // head-dim atom, and the copy leaves out the rows past M.  The
+            // other tile may still have blocks to go (causal rows), so K is
+            // free only once every MMA of the CTA is done (and with them every
+            // K load, all consumed by score MMAs).
+            if (!mbar_wait(&sh.mma_done, 0)) {
+                record_status(&g_wait_status, kWaitMma);
+                ok = false;
+            }
+        }
+        if (ok && p.o_tma) {
             tc_fence_after();
             const float inv = 1.0f / l_run;
 #pragma unroll
             for (int a = 0; a < kDA; ++a) {
                 float o[32];
                 tmem_ld32(o_addr + 32 * a, o);
-                float* st = sh.q[t][a];
+                float* st = sh.k[t][a];
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     *reinterpret_cast<float4*>(st + row * kAtom + ((c ^ (row & 7)) << 2)) =
@@ -498,14 +572,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             if (lane == 0 && m0 + t * BM + quarter * 32 < p.M) {
 #pragma unroll
                 for (int a = 0; a < kDA; ++a)
-                    tma_store_3d(&to, sh.q[t][a] + quarter * 32 * kAtom, kAtom * a,
+                    tma_store_3d(&to, sh.k[t][a] + quarter * 32 * kAtom, kAtom * a,
                                  (int)(m0 + t * BM + quarter * 32), p.bo ? (int)b : 0);
                 bulk_commit();
                 // Shared memory must outlive the copies' reads of it; the
                 // writes themselves complete with the grid.
                 bulk_wait_read_all();
             }
-        } else {
+        } else if (ok) {
             tc_fence_after();
             const float inv = 1.0f / l_run;
             float* orow = p.O + b * p.bsO + (m < p.M ? m : 0) * p.rsO;
@@ -513,8 +587,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             for (int h = 0; h < kD / 32; ++h) {
                 float o[32];
                 tmem_ld32(o_addr + 32 * h, o);    // whole warp, converged
-                if (m < p.M && dbg_in_span(p.O, orow + 32 * h * p.csO, p.so, &g_wait_status) &&
-                    dbg_in_span(p.O, orow + (32 * h + 31) * p.csO, p.so, &g_wait_status)) {
+                if (m < p.M) {
                     if (p.o_vec) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
@@ -605,7 +678,6 @@ cudaError_t launch_attention_tc(const AttnProblem& a, cudaStream_t stream) {
     p.o_tma = tma_operand(a.O, a.M, a.rsO, a.csO, a.bsO, a.batch) && (a.batch == 1 || a.bsO != 0) &&
               make_map(&to, a.O, a.M, a.rsO, a.bsO, a.batch, kD, 32);
     p.bo = a.batch > 1;
-    p.so = a.so;
     const int64_t rows = kTiles * BM;
     const dim3 grid((unsigned)a.batch, (unsigned)((a.M + rows - 1) / rows));
     attention_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
