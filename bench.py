@@ -200,7 +200,8 @@ def kernel_source_digest(path_name):
                           "ffma_tma_512x64.cu", "schedule.cuh", "ptx.cuh"] + common,
              "tma_tf32": ["tf32_tc.cu", "schedule.cuh", "ptx.cuh"] + common,
              "attention": ["attention.cu", "internal.h"],
-             "attention_tc": ["attention_tc.cu", "attention_tc.h", "ptx.cuh", "internal.h"]}.get(path_name, [])
+             "attention_tc": ["attention_tc.cu", "attention_tc.h", "ptx.cuh", "internal.h"],
+             "attention_decode": ["attention_decode.cu", "internal.h"]}.get(path_name, [])
     h = hashlib.sha256()
     for f in files:
         p = os.path.join(ROOT, "strided_gemm_gb300", "csrc", f)
@@ -625,6 +626,50 @@ def run_ours(args, world, rank, local, dist):
                                          "frac": round(c.flops / ms / 1e9 / fp32_peak, 4),
                                          "traffic": profiled_traffic("attention", n)}
             attention["per_workload"][n] = row
+
+        # A decode step over a paged K / V cache (row f2's paged read): four
+        # query heads per KV head against each sequence's whole context, K and
+        # V rows read through the block table.  The stream of K and V rows is
+        # the work, so the roofline is the measured copy bandwidth.  Beside
+        # it, the same step over the same context stored contiguously.
+        hbm_peak = float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+        for n in wl.PAGED:
+            c = wl.make_paged(n)
+            dQ = torch.from_numpy(c.Q.storage).to(dev)
+            dKc = torch.from_numpy(c.K_cache.reshape(-1)).to(dev)
+            dVc = torch.from_numpy(c.V_cache.reshape(-1)).to(dev)
+            dT = torch.from_numpy(c.block_table).to(dev)
+            dL = torch.from_numpy(c.seq_lens).to(dev)
+            dO = torch.from_numpy(c.O.storage).to(dev)
+            a = (dQ.data_ptr(), c.Q.rs, c.Q.cs, c.Q.bs, dKc.data_ptr(), dVc.data_ptr(),
+                 c.K_cache.shape[0], c.block_size, c.n_kv_heads, dT.data_ptr(),
+                 c.block_table.shape[1], dL.data_ptr(), dO.data_ptr(), c.O.rs, c.O.cs, c.O.bs,
+                 c.M, c.N, c.D, c.D, c.n_seqs, c.alpha, c.causal, c.q_len)
+            ms = timed(lambda: sg.sbgemm_attention_paged(*a, s_handle, **ws_kw))
+            gbs = c.alg_bytes / ms / 1e6
+            row = {"ms": round(ms, 4), "gb_s": round(gbs, 1), "alg_mb": round(c.alg_bytes / 1e6, 2),
+                   "keys": c.keys, "gflops": round(c.flops / ms / 1e6, 1),
+                   "shape": {"n_seqs": c.n_seqs, "n_kv_heads": c.n_kv_heads, "rows_per_entry": c.M,
+                             "head_dim": c.D, "block_size": c.block_size,
+                             "context": [int(c.seq_lens.min()), int(c.seq_lens.max())]},
+                   "roofline": {"bound": "hbm", "kernel": "attention_decode (paged)",
+                                "achieved": round(gbs, 1), "peak": round(hbm_peak, 1),
+                                "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                                "traffic": profiled_traffic("attention_decode", n)}}
+            del dKc, dVc
+            # The same keys stored contiguously, [entry][N][D] padded to N.
+            dK = torch.from_numpy(c.K_ctx.reshape(-1)).to(dev)
+            dV = torch.from_numpy(c.V_ctx.reshape(-1)).to(dev)
+            b = (dQ.data_ptr(), c.Q.rs, c.Q.cs, c.Q.bs, dK.data_ptr(), c.D, 1, c.N * c.D,
+                 dV.data_ptr(), c.D, 1, c.N * c.D, dO.data_ptr(), c.O.rs, c.O.cs, c.O.bs,
+                 c.M, c.N, c.D, c.D, c.batch, c.alpha, c.causal, c.q_len)
+            ms_c = timed(lambda: sg.sbgemm_attention(*b, s_handle, **ws_kw))
+            row["contiguous_padded_ms"] = round(ms_c, 4)
+            row["contiguous_note"] = ("every entry padded to the longest context (keys past it are "
+                                      "masked but still read), the layout a gather into one buffer "
+                                      "gives")
+            attention["per_workload"][n] = row
+            del dK, dV
 
     # Every other config of the workload list, each against its own roofline,
     # min(peak compute, algorithmic bytes x HBM bandwidth): median of 21 timed

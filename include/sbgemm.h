@@ -77,8 +77,13 @@ typedef enum {
                                        tensor-map encoding, no device) */
     SBGEMM_ERR_DEVICE_TIMEOUT = 6,  /* a bounded in-kernel wait expired; see
                                        sbgemm_device_status */
-    SBGEMM_ERR_NOT_DEVICE_MEMORY = 7 /* an operand is not device-accessible memory,
+    SBGEMM_ERR_NOT_DEVICE_MEMORY = 7, /* an operand is not device-accessible memory,
                                        or its span leaves its allocation */
+    SBGEMM_ERR_DEVICE_CHECK = 8     /* a kernel's own check found an input it
+                                       could not use (a paged block id or
+                                       sequence length out of range; a debug
+                                       build's out-of-span address) and skipped
+                                       it; see sbgemm_device_status */
 } sbgemm_status;
 
 /* Arithmetic of sbgemm_options.math. */
@@ -250,9 +255,12 @@ SBGEMM_API int sbgemm_fused(const float* A, int64_t rsA, int64_t csA, int64_t bs
  * section "Matmuls go to cuBLAS").
  *   causal: 0, or 1 to mask keys n > position(m) = (m mod q_len) + N - q_len
  *           (q_len: query rows per head, 0 < q_len <= N; ignored when 0).
- *   D, Dv:  head dimensions; this build supports D = Dv = 64.
+ *   D, Dv:  head dimensions; this build supports D = Dv = 32, 64, 96 or 128.
  * fp32 arithmetic: scores by FFMA, the softmax with exp2 of alpha*log2(e)
- * scaled scores, P V by FFMA.  Asynchronous on `stream`; allocates nothing.
+ * scaled scores, P V by FFMA.  Up to 8 query rows per batch entry (4 when D
+ * is 96 or 128), a decode step, run a kernel that splits each entry's keys
+ * across CTAs when sbgemm_attention_ex gives it a workspace (one CTA per
+ * entry without one).  Asynchronous on `stream`; allocates nothing.
  * Errors: SBGEMM_ERR_INVALID_VALUE (negative size, N == 0 with rows to
  * compute, a bad causal flag or q_len, misaligned pointer, span overflow),
  * SBGEMM_ERR_NULL_POINTER, SBGEMM_ERR_OUTPUT_OVERLAP (O not injective or
@@ -272,10 +280,16 @@ SBGEMM_API int sbgemm_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_
  * stride along the head dimension (csQ = csK = csV = 1), 16-byte aligned bases
  * and row / batch strides (a zero batch stride broadcasts); other layouts run
  * the fp32 kernel, unless opt->force_path = SBGEMM_PATH_TMA_TF32, which then
- * returns SBGEMM_ERR_UNSUPPORTED.  opt->workspace and k_split are ignored;
- * force_path must be AUTO or TMA_TF32 (TMA_TF32 with math = TF32).  NULL opt
- * is sbgemm_attention.  Errors as sbgemm_attention, plus those of the
- * options. */
+ * returns SBGEMM_ERR_UNSUPPORTED.  Problems of a few rows per entry (see
+ * sbgemm_attention) run the fp32 decode kernel in either math unless the
+ * tensor-core kernel is forced.  opt->workspace (caller-owned device memory
+ * of opt->workspace_bytes, meeting no operand) lets the decode kernel split
+ * the keys of an entry into chunks, each writing (2 + Dv) floats per row,
+ * that a second launch merges in chunk order; sbgemm_workspace_bytes is
+ * plenty.  k_split is ignored; force_path must be AUTO or TMA_TF32 (TMA_TF32
+ * with math = TF32).  NULL opt is sbgemm_attention.  Errors as
+ * sbgemm_attention, plus those of the options and of the workspace
+ * (SBGEMM_ERR_NOT_DEVICE_MEMORY, SBGEMM_ERR_OUTPUT_OVERLAP). */
 SBGEMM_API int sbgemm_attention_ex(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
                         const float* K, int64_t rsK, int64_t csK, int64_t bsK,
                         const float* V, int64_t rsV, int64_t csV, int64_t bsV,
@@ -283,6 +297,46 @@ SBGEMM_API int sbgemm_attention_ex(const float* Q, int64_t rsQ, int64_t csQ, int
                         int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t batch,
                         float alpha, int causal, int64_t q_len, void* stream,
                         const sbgemm_options* opt);
+
+/* Fused attention reading K and V straight out of a paged cache through a
+ * block table ("rvllm CUDA path", section "The kernels": the cache is one
+ * buffer [num_blocks][block_size][n_kv_heads][head_dim], and context position
+ * pos of a sequence lives in block block_table[seq * max_blocks + pos /
+ * block_size] at offset pos % block_size; section "What's basic about it":
+ * reading the blocks directly instead of gathering the whole context into a
+ * contiguous buffer every decode step).
+ *   K_cache, V_cache: [num_blocks][block_size][n_kv_heads][D] and [..][Dv]
+ *           fp32, contiguous, 16-byte aligned.
+ *   block_table: int32 [n_seqs][max_blocks] on the device; entries past a
+ *           sequence's last block are never read.
+ *   seq_lens: int32 [n_seqs] on the device, each sequence's context length
+ *           (1..N, and >= q_len when causal), or NULL for N everywhere.
+ *   N:      the longest context, at most max_blocks * block_size.
+ *   Q, O:   strided like sbgemm_attention's, batch entry b = seq * n_kv_heads
+ *           + head, M rows each (grouped-query heads stacked as rows);
+ *           causal positions use the entry's own length:
+ *           position(m) = (m mod q_len) + len - q_len.
+ * O[b] is sbgemm_attention of Q[b] against the keys and values of positions
+ * 0..len-1 of (seq, head).  D = Dv = 32, 64, 96 or 128; fp32 arithmetic as
+ * sbgemm_attention (opt->math is not read); few-row problems use the decode
+ * kernel and opt->workspace as sbgemm_attention_ex, others the row-block
+ * kernel.  The host checks sizes, spans and overlaps as sbgemm_attention
+ * (the caches, the table and seq_lens as operands O must not meet); the
+ * table's and seq_lens' contents are device data and are checked by the
+ * kernels: a block id outside [0, num_blocks) reads as a zero key and value,
+ * a length out of range is clamped, and either makes the next
+ * sbgemm_device_status return SBGEMM_ERR_DEVICE_CHECK (code 10); no access
+ * leaves the caches.  opt->force_path must be AUTO.  Asynchronous on
+ * `stream`; allocates nothing. */
+SBGEMM_API int sbgemm_attention_paged(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
+                                      const float* K_cache, const float* V_cache,
+                                      int64_t num_blocks, int64_t block_size, int64_t n_kv_heads,
+                                      const int32_t* block_table, int64_t max_blocks,
+                                      const int32_t* seq_lens,
+                                      float* O, int64_t rsO, int64_t csO, int64_t bsO,
+                                      int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t n_seqs,
+                                      float alpha, int causal, int64_t q_len, void* stream,
+                                      const sbgemm_options* opt);
 
 /* Validate and plan without launching or touching device memory: reports the
  * layout classes and the kernel path, tile and CTA count that sbgemm_ex would
@@ -343,12 +397,16 @@ SBGEMM_API int sbgemm_noalloc(const float* A, int64_t rsA, int64_t csA, int64_t 
                               int64_t M, int64_t N, int64_t K, int64_t batch,
                               float alpha, int accumulate, void* stream);
 
-/* Reads and clears the device-side status words that bounded in-kernel waits
- * set when they give up (after synchronising `stream`).  Returns SBGEMM_OK or
- * SBGEMM_ERR_DEVICE_TIMEOUT; *where_out (may be NULL) receives a code naming
- * the wait that expired (0 if none): 1 a loaded stage, 2 a released stage, 3
- * copies in flight at exit, 4 the MMAs of a tile, 5 a free accumulator, 6 a
- * stream-K partial sum, 7 / 8 the self-test's mbarrier / flag. */
+/* Reads and clears the device-side status words that kernels set when a
+ * bounded in-kernel wait gives up or a device-side check skips an input
+ * (after synchronising `stream`; the first code recorded is kept).  Returns
+ * SBGEMM_OK, SBGEMM_ERR_DEVICE_TIMEOUT (codes 1-8) or SBGEMM_ERR_DEVICE_CHECK
+ * (codes 9-10); *where_out (may be NULL) receives the code (0 if none): 1 a
+ * loaded stage, 2 a released stage, 3 copies in flight at exit, 4 the MMAs of
+ * a tile, 5 a free accumulator, 6 a stream-K partial sum, 7 / 8 the
+ * self-test's mbarrier / flag, 9 an address outside its operand's span (debug
+ * builds only; the access was skipped), 10 a paged-attention block id or
+ * sequence length out of range. */
 SBGEMM_API int sbgemm_device_status(void* stream, int* where_out);
 
 /* Failure-detection self-test (a diagnostic of the library, not part of the

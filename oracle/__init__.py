@@ -17,6 +17,7 @@ import ctypes
 import os
 import subprocess
 import threading
+import types
 
 import numpy as np
 
@@ -251,3 +252,60 @@ def attention(Q, K, V, M, N, D, Dv, batch, alpha, causal=False, q_len=0, lib=Non
 def attention_case(case, lib=None):
     return attention(case.Q, case.K, case.V, case.M, case.N, case.D, case.Dv, case.batch,
                      case.alpha, case.causal, case.q_len, lib=lib)
+
+
+def kv_gather(cache, block_table, seq, head, length, lib=None):
+    """Rows 0..length-1 of one (sequence, head) of a paged cache, gathered into
+    a contiguous [length, head_dim] float32 array (sbgemm_ref_kv_gather).
+    ``cache`` is float32 [num_blocks, block_size, n_kv_heads, head_dim] and
+    ``block_table`` int32 [n_seqs, max_blocks]."""
+    lib = lib or load()
+    if not hasattr(lib, "_kvg_bound"):
+        lib.sbgemm_ref_kv_gather.restype = ctypes.c_int
+        lib.sbgemm_ref_kv_gather.argtypes = [_fp, _i64, _i64, _i64, _i64, _fp, _i64,
+                                             _i64, _i64, _i64, _fp]
+        lib._kvg_bound = True
+    cache = np.ascontiguousarray(cache, dtype=np.float32)
+    table = np.ascontiguousarray(block_table, dtype=np.int32)
+    if cache.ndim != 4 or table.ndim != 2 or not 0 <= seq < table.shape[0]:
+        raise ValueError("oracle: kv_gather needs a 4-d cache and a 2-d block table")
+    nb, bsz, heads, hd = cache.shape
+    out = np.empty((int(length), hd), dtype=np.float32)
+    rc = lib.sbgemm_ref_kv_gather(cache.ctypes.data, nb, bsz, heads, hd, table.ctypes.data,
+                                  table.shape[1], int(seq), int(head), int(length),
+                                  out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle: a position maps outside the block table or the cache")
+    return out
+
+
+def attention_paged(Q, K_cache, V_cache, block_table, seq_lens, M, alpha, causal=False,
+                    q_len=0, lib=None):
+    """Attention of every (sequence, kv head) over its keys in a paged cache:
+    the page's gather of the context into contiguous K and V, then the
+    attention oracle with N = that sequence's length.  Q is an operand of
+    batch n_seqs * n_kv_heads (entry b = seq * n_kv_heads + head, M rows of
+    D); the caches are [num_blocks, block_size, n_kv_heads, D or Dv].
+    Returns (O, weight, smag) as ``attention``, over the whole batch."""
+    lib = lib or load()
+    n_seqs = int(np.asarray(block_table).shape[0])
+    heads, D, Dv = K_cache.shape[2], K_cache.shape[3], V_cache.shape[3]
+    batch = n_seqs * heads
+    if not _span_ok(Q, batch, M, D):
+        raise ValueError("oracle: Q strides reach outside its storage")
+    O = np.zeros((batch, M, Dv), dtype=np.float64)
+    W = np.zeros((batch, M, Dv), dtype=np.float64)
+    S = np.zeros((batch, M), dtype=np.float64)
+    for s in range(n_seqs):
+        n = int(seq_lens[s])
+        for h in range(heads):
+            b = s * heads + h
+            Kc = kv_gather(K_cache, block_table, s, h, n, lib=lib).reshape(-1)
+            Vc = kv_gather(V_cache, block_table, s, h, n, lib=lib).reshape(-1)
+            Qb = types.SimpleNamespace(storage=Q.storage, offset=Q.offset + b * Q.bs,
+                                       rs=Q.rs, cs=Q.cs, bs=0)
+            Kb = types.SimpleNamespace(storage=Kc, offset=0, rs=D, cs=1, bs=0)
+            Vb = types.SimpleNamespace(storage=Vc, offset=0, rs=Dv, cs=1, bs=0)
+            O[b:b + 1], W[b:b + 1], S[b:b + 1] = attention(Qb, Kb, Vb, M, n, D, Dv, 1, alpha,
+                                                           causal, q_len, lib=lib)
+    return O, W, S

@@ -297,3 +297,36 @@ int sbgemm_ref_attention(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
     free(mag);
     return 0;
 }
+
+/*
+ * Paged key / value cache read (test infrastructure, as above).
+ *
+ * "rvllm CUDA path", section "The kernels": the cache is one buffer shaped
+ * [num_blocks][block_size][n_kv_heads][head_dim]; a sequence's context
+ * position pos lives in the block that the sequence's row of the block table
+ * names for pos / block_size, at offset pos % block_size inside it.  This
+ * copies the rows of positions 0..len-1 of one (sequence, head) into a
+ * contiguous [len][head_dim] buffer, the gather step the page describes, so
+ * that attention over paged keys is this gather followed by
+ * sbgemm_ref_attention.  Returns 0, or -1 if a position needs a table entry
+ * past max_blocks or a block id outside [0, num_blocks) (nothing is read
+ * from the cache then).
+ */
+int sbgemm_ref_kv_gather(const float* cache, int64_t num_blocks, int64_t block_size,
+                         int64_t n_kv_heads, int64_t head_dim,
+                         const int32_t* block_table, int64_t max_blocks,
+                         int64_t seq, int64_t head, int64_t len, float* out) {
+    if (num_blocks <= 0 || block_size <= 0 || n_kv_heads <= 0 || head_dim < 0 ||
+        max_blocks <= 0 || seq < 0 || head < 0 || head >= n_kv_heads || len < 0)
+        return -1;
+    for (int64_t pos = 0; pos < len; ++pos) {
+        const int64_t block_pos = pos / block_size;
+        const int64_t offset = pos % block_size;
+        if (block_pos >= max_blocks) return -1;
+        const int64_t block = block_table[seq * max_blocks + block_pos];
+        if (block < 0 || block >= num_blocks) return -1;
+        const float* row = cache + ((block * block_size + offset) * n_kv_heads + head) * head_dim;
+        for (int64_t d = 0; d < head_dim; ++d) out[pos * head_dim + d] = row[d];
+    }
+    return 0;
+}

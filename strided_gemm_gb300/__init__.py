@@ -21,11 +21,11 @@ __all__ = [
     "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version", "matmul",
     "SBGEMM_OK", "SBGEMM_ERR_INVALID_VALUE", "SBGEMM_ERR_NULL_POINTER",
     "SBGEMM_ERR_OUTPUT_OVERLAP", "SBGEMM_ERR_UNSUPPORTED", "SBGEMM_ERR_CUDA",
-    "SBGEMM_ERR_DEVICE_TIMEOUT", "SBGEMM_ERR_NOT_DEVICE_MEMORY",
+    "SBGEMM_ERR_DEVICE_TIMEOUT", "SBGEMM_ERR_NOT_DEVICE_MEMORY", "SBGEMM_ERR_DEVICE_CHECK",
     "MATH_FP32", "MATH_TF32", "PATH_NONE", "PATH_AUTO", "PATH_GATHER_FFMA",
     "PATH_TMA_FFMA", "PATH_TMA_TF32", "LAYOUT_K_MAJOR", "LAYOUT_MN_MAJOR",
     "LAYOUT_GENERAL", "EXPORTED_SYMBOLS", "LIB_PATH", "sbgemm_fused", "linear_backward",
-    "sbgemm_attention", "sbgemm_attention_ex", "attention",
+    "sbgemm_attention", "sbgemm_attention_ex", "sbgemm_attention_paged", "attention",
     "ACT_NONE", "ACT_RELU", "ACT_SIGMOID", "ACT_SILU", "ACT_GELU_TANH", "ACT_GELU_ERF",
     "ACTIVATIONS", "KSPLIT_ANY", "KSPLIT_EXACT", "KSPLIT_NONE", "STREAM_K_NONE",
     "STREAM_K_CHAINED", "STREAM_K_PIECES", "NOALLOC_SCRATCH_BYTES",
@@ -44,6 +44,7 @@ SBGEMM_ERR_UNSUPPORTED = 4
 SBGEMM_ERR_CUDA = 5
 SBGEMM_ERR_DEVICE_TIMEOUT = 6
 SBGEMM_ERR_NOT_DEVICE_MEMORY = 7
+SBGEMM_ERR_DEVICE_CHECK = 8
 
 MATH_FP32, MATH_TF32 = 0, 1
 PATH_NONE, PATH_AUTO, PATH_GATHER_FFMA, PATH_TMA_FFMA, PATH_TMA_TF32 = -1, 0, 1, 2, 3
@@ -53,7 +54,7 @@ PATH_NAMES = {PATH_NONE: "none", PATH_GATHER_FFMA: "gather_ffma",
 
 # Every function include/sbgemm.h declares.
 EXPORTED_SYMBOLS = ("sbgemm", "sbgemm_ex", "sbgemm_fused", "sbgemm_attention",
-                    "sbgemm_attention_ex", "sbgemm_plan",
+                    "sbgemm_attention_ex", "sbgemm_attention_paged", "sbgemm_plan",
                     "sbgemm_workspace_bytes", "sbgemm_noalloc", "sbgemm_selftest",
                     "sbgemm_device_status", "sbgemm_status_string", "sbgemm_version")
 ACT_NONE, ACT_RELU, ACT_SIGMOID, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4, 5
@@ -129,6 +130,11 @@ def load(path: str = LIB_PATH):
         lib.sbgemm_attention_ex.argtypes = (op4 * 4 + [_i64] * 5 +
                                             [ctypes.c_float, ctypes.c_int, _i64, _vp,
                                              ctypes.POINTER(_Options)])
+        lib.sbgemm_attention_paged.restype = ctypes.c_int
+        lib.sbgemm_attention_paged.argtypes = (op4 + [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp] +
+                                               op4 + [_i64] * 5 +
+                                               [ctypes.c_float, ctypes.c_int, _i64, _vp,
+                                                ctypes.POINTER(_Options)])
         lib.sbgemm_ex.restype = ctypes.c_int
         lib.sbgemm_ex.argtypes = _ARGS + [ctypes.c_float, ctypes.c_int, _vp,
                                           ctypes.POINTER(_Options)]
@@ -232,13 +238,16 @@ def sbgemm_fused(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
 
 def sbgemm_attention(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
                      O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal=0, q_len=0,
-                     stream=0, math: int = MATH_FP32, force_path: int = PATH_AUTO) -> None:
+                     stream=0, math: int = MATH_FP32, force_path: int = PATH_AUTO,
+                     workspace: int = 0, workspace_bytes: int = 0) -> None:
     """O = softmax(alpha * Q K^T [causal]) V over strided operands; math =
-    MATH_TF32 opts in to the tensor-core kernel (sbgemm_attention_ex)."""
-    if math != MATH_FP32 or force_path != PATH_AUTO:
+    MATH_TF32 opts in to the tensor-core kernel, and a workspace lets the
+    decode kernel split keys (sbgemm_attention_ex)."""
+    if math != MATH_FP32 or force_path != PATH_AUTO or workspace:
         sbgemm_attention_ex(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
                             O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal, q_len,
-                            stream, math=math, force_path=force_path)
+                            stream, math=math, force_path=force_path, workspace=workspace,
+                            workspace_bytes=workspace_bytes)
         return
     st = load().sbgemm_attention(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
                                  O, rsO, csO, bsO, M, N, D, Dv, batch, float(alpha),
@@ -249,16 +258,36 @@ def sbgemm_attention(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
 
 def sbgemm_attention_ex(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
                         O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal=0, q_len=0,
-                        stream=0, math: int = MATH_FP32, force_path: int = PATH_AUTO) -> None:
+                        stream=0, math: int = MATH_FP32, force_path: int = PATH_AUTO,
+                        workspace: int = 0, workspace_bytes: int = 0) -> None:
     """sbgemm_attention with options: math = MATH_TF32 runs the tensor-core
     kernel when Q, K and V suit tensor maps (force_path = PATH_TMA_TF32 makes
-    that a requirement)."""
-    o = _opts(math, force_path)
+    that a requirement); a workspace lets the decode kernel split each entry's
+    keys across CTAs."""
+    o = _opts(math, force_path, workspace, workspace_bytes)
     st = load().sbgemm_attention_ex(Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV,
                                     O, rsO, csO, bsO, M, N, D, Dv, batch, float(alpha),
                                     int(causal), int(q_len), stream or None, ctypes.byref(o))
     if st:
         raise SbgemmError(st, "sbgemm_attention_ex")
+
+
+def sbgemm_attention_paged(Q, rsQ, csQ, bsQ, K_cache, V_cache, num_blocks, block_size,
+                           n_kv_heads, block_table, max_blocks, seq_lens, O, rsO, csO, bsO,
+                           M, N, D, Dv, n_seqs, alpha, causal=0, q_len=0, stream=0,
+                           workspace: int = 0, workspace_bytes: int = 0) -> None:
+    """Attention with K and V read from a paged cache [num_blocks, block_size,
+    n_kv_heads, D] through an int32 block table [n_seqs, max_blocks] and
+    optional int32 sequence lengths (device pointers; 0 for seq_lens means N
+    keys everywhere).  Batch entry b of Q and O is (sequence b // n_kv_heads,
+    head b % n_kv_heads)."""
+    o = _opts(MATH_FP32, PATH_AUTO, workspace, workspace_bytes)
+    st = load().sbgemm_attention_paged(Q, rsQ, csQ, bsQ, K_cache, V_cache, num_blocks, block_size,
+                                       n_kv_heads, block_table, max_blocks, seq_lens or None,
+                                       O, rsO, csO, bsO, M, N, D, Dv, n_seqs, float(alpha),
+                                       int(causal), int(q_len), stream or None, ctypes.byref(o))
+    if st:
+        raise SbgemmError(st, "sbgemm_attention_paged")
 
 
 def attention(Q, K, V, O, alpha=None, causal=False, q_len=0, stream=None, math=MATH_FP32):

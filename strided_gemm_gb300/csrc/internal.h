@@ -10,6 +10,20 @@
 
 namespace sbg {
 
+// Codes written to a path's device status word (first writer wins).
+enum : unsigned int {
+    kWaitFull = 1,       // consumer waiting for a loaded stage
+    kWaitEmpty = 2,      // producer waiting for a released stage
+    kWaitDrain = 3,      // producer draining its last copies on the way out
+    kWaitMma = 4,        // epilogue waiting for the accumulator
+    kWaitAccFree = 5,    // MMA issuer waiting for the epilogue to free TMEM
+    kWaitPartial = 6,    // stream-K: exchanging partial sums between CTAs
+    kWaitSelftestMbar = 7,   // self-test: an mbarrier phase nothing completes
+    kWaitSelftestFlag = 8,   // self-test: a global flag nothing sets
+    kBoundsViolation = 9,    // debug build: an access outside its operand's span (skipped)
+    kPagedInput = 10,        // paged attention: a block id or sequence length out of range (skipped)
+};
+
 // Element offsets [lo, hi] from an operand's base pointer that lie inside the
 // memory the caller described (the host's span check before every launch).
 // Only the bounds checks of a debug build (SBGEMM_DEBUG) read them.
@@ -85,6 +99,17 @@ struct AttnProblem {
     int causal;
     int64_t q_len;           // rows per head for the causal position
     ElemSpan sq, sk, sv, so; // debug builds: valid element offsets of Q, K, V and O
+    // Paged K and V: K and V are then caches [num_blocks][block_size][n_kv_heads]
+    // [D or Dv]; batch entry b is (sequence b / n_kv_heads, head b % n_kv_heads)
+    // and key n of a sequence lives in block table[seq][n / block_size] at
+    // offset n % block_size.  seq_lens (or N for all) gives each sequence's keys.
+    int paged = 0;
+    const int32_t* table = nullptr;
+    const int32_t* seq_lens = nullptr;
+    int64_t max_blocks = 0, block_size = 0, n_kv_heads = 0, num_blocks = 0;
+    // Scratch of the split-key decode kernel (caller's workspace; may be null).
+    void* workspace = nullptr;
+    size_t workspace_bytes = 0;
 };
 // C^T = B^T A^T as a problem of its own: A' = B^T, B' = A^T, C' = C^T, M' = N,
 // N' = M (the fused addend transposed alike).
@@ -93,6 +118,10 @@ Problem transposed_problem(const Problem& p);
 bool attention_supported(int64_t D, int64_t Dv);
 int64_t attention_max_rows();   // M limit of one launch
 cudaError_t launch_attention(const AttnProblem& a, cudaStream_t stream);
+// Few query rows per batch entry (decode): keys split across CTAs.
+bool attention_decode_supported(const AttnProblem& a);
+cudaError_t launch_attention_decode(const AttnProblem& a, cudaStream_t stream);
+unsigned int read_and_clear_status_attention_decode(cudaStream_t stream);
 
 // ---- strided-gather FFMA path (ffma_gather.cu) --------------------------------
 // Tile configurations of the gather kernel.

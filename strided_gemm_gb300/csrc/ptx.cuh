@@ -5,24 +5,16 @@
 #include <cuda.h>
 #include <cstdint>
 
+#include "internal.h"
+
 namespace sbg {
 
 // A wait that has not completed after this long is treated as a hang: the
 // kernel records where it gave up and returns instead of spinning forever.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s
 
-// Codes written to a path's device status word (first writer wins).
-enum : unsigned int {
-    kWaitFull = 1,       // consumer waiting for a loaded stage
-    kWaitEmpty = 2,      // producer waiting for a released stage
-    kWaitDrain = 3,      // producer draining its last copies on the way out
-    kWaitMma = 4,        // epilogue waiting for the accumulator
-    kWaitAccFree = 5,    // MMA issuer waiting for the epilogue to free TMEM
-    kWaitPartial = 6,    // stream-K: exchanging partial sums between CTAs
-    kWaitSelftestMbar = 7,   // self-test: an mbarrier phase nothing completes
-    kWaitSelftestFlag = 8,   // self-test: a global flag nothing sets
-    kBoundsViolation = 9,    // debug build: an access outside its operand's span (skipped)
-};
+// The status codes (kWaitFull ...) are declared in internal.h.
+
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

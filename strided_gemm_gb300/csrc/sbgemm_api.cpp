@@ -10,7 +10,9 @@
 #include <array>
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
+#include <utility>
 
 #include "attention_tc.h"
 #include "internal.h"
@@ -173,6 +175,27 @@ bool span_in_allocation(const void* base, const Span& s) {
     const __int128 lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.lo * 4;
     const __int128 hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.hi * 4 + 4;
     return lo >= (__int128)abase && hi <= (__int128)abase + (__int128)asize;
+}
+
+bool bytes_meet(const void* a, const Span& sa, const void* b, const Span& sb) {
+    const __int128 alo = (__int128)reinterpret_cast<uintptr_t>(a) + (__int128)sa.lo * 4;
+    const __int128 ahi = (__int128)reinterpret_cast<uintptr_t>(a) + (__int128)sa.hi * 4 + 4;
+    const __int128 blo = (__int128)reinterpret_cast<uintptr_t>(b) + (__int128)sb.lo * 4;
+    const __int128 bhi = (__int128)reinterpret_cast<uintptr_t>(b) + (__int128)sb.hi * 4 + 4;
+    return alo < bhi && blo < ahi;
+}
+
+// An attention workspace, when given, is device memory that meets no operand
+// (the decode kernel writes its per-chunk partial results there).
+int check_attention_workspace(const sbgemm_options& o,
+                              std::initializer_list<std::pair<const void*, Span>> operands) {
+    if (!o.workspace) return SBGEMM_OK;
+    if (o.workspace_bytes < 4) return SBGEMM_ERR_INVALID_VALUE;
+    const Span sw{0, (int64_t)(o.workspace_bytes / 4) - 1};
+    if (!span_in_allocation(o.workspace, sw)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    for (const auto& op : operands)
+        if (bytes_meet(op.first, op.second, o.workspace, sw)) return SBGEMM_ERR_OUTPUT_OVERLAP;
+    return SBGEMM_OK;
 }
 
 int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empty, Plan* plan) {
@@ -434,6 +457,7 @@ const char* sbgemm_status_string(int status) {
         case SBGEMM_ERR_CUDA: return "SBGEMM_ERR_CUDA";
         case SBGEMM_ERR_DEVICE_TIMEOUT: return "SBGEMM_ERR_DEVICE_TIMEOUT";
         case SBGEMM_ERR_NOT_DEVICE_MEMORY: return "SBGEMM_ERR_NOT_DEVICE_MEMORY";
+        case SBGEMM_ERR_DEVICE_CHECK: return "SBGEMM_ERR_DEVICE_CHECK";
         default: return "SBGEMM_ERR_UNKNOWN";
     }
 }
@@ -527,13 +551,6 @@ int sbgemm_attention_ex(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
         !operand_span(batch, N, Dv, bsV, rsV, csV, &sv) || !operand_span(batch, M, Dv, bsO, rsO, csO, &so))
         return SBGEMM_ERR_INVALID_VALUE;
     if (!output_injective(batch, M, Dv, bsO, rsO, csO)) return SBGEMM_ERR_OUTPUT_OVERLAP;
-    auto bytes_meet = [](const void* a, const Span& sa, const void* b, const Span& sb) {
-        const __int128 alo = (__int128)reinterpret_cast<uintptr_t>(a) + (__int128)sa.lo * 4;
-        const __int128 ahi = (__int128)reinterpret_cast<uintptr_t>(a) + (__int128)sa.hi * 4 + 4;
-        const __int128 blo = (__int128)reinterpret_cast<uintptr_t>(b) + (__int128)sb.lo * 4;
-        const __int128 bhi = (__int128)reinterpret_cast<uintptr_t>(b) + (__int128)sb.hi * 4 + 4;
-        return alo < bhi && blo < ahi;
-    };
     if (bytes_meet(O, so, Q, sq) || bytes_meet(O, so, K, sk) || bytes_meet(O, so, V, sv))
         return SBGEMM_ERR_OUTPUT_OVERLAP;
     int dev = 0;
@@ -541,16 +558,106 @@ int sbgemm_attention_ex(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
     if (!span_in_allocation(Q, sq) || !span_in_allocation(K, sk) || !span_in_allocation(V, sv) ||
         !span_in_allocation(O, so))
         return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    const int wst = check_attention_workspace(o, {{Q, sq}, {K, sk}, {V, sv}, {O, so}});
+    if (wst) return wst;
     AttnProblem a{Q, rsQ, csQ, bsQ, K, rsK, csK, bsK, V, rsV, csV, bsV, O, rsO, csO, bsO,
                   M, N, D, Dv, batch, alpha, causal, causal ? q_len : M,
                   ElemSpan{sq.lo, sq.hi}, ElemSpan{sk.lo, sk.hi}, ElemSpan{sv.lo, sv.hi},
                   ElemSpan{so.lo, so.hi}};
-    // TF32 on the tensor cores when asked for and the operands suit tensor
-    // maps; otherwise the fp32 kernel (or, when forced, unsupported).
-    const bool tc = o.math == SBGEMM_MATH_TF32 && attention_tc_supported(a);
-    if (o.force_path == SBGEMM_PATH_TMA_TF32 && !tc) return SBGEMM_ERR_UNSUPPORTED;
-    const cudaError_t e = tc ? launch_attention_tc(a, static_cast<cudaStream_t>(stream))
-                             : launch_attention(a, static_cast<cudaStream_t>(stream));
+    a.workspace = o.workspace;
+    a.workspace_bytes = o.workspace ? o.workspace_bytes : 0;
+    // Forced: the tensor-core kernel.  Otherwise a few rows per entry go to the
+    // split-key decode kernel (fp32, in either math), and the rest to the
+    // tensor-core kernel when TF32 is asked for and the operands suit tensor
+    // maps, else to the fp32 kernel.
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (o.force_path == SBGEMM_PATH_TMA_TF32) {
+        if (!attention_tc_supported(a)) return SBGEMM_ERR_UNSUPPORTED;
+        e = launch_attention_tc(a, s);
+    } else if (attention_decode_supported(a)) {
+        e = launch_attention_decode(a, s);
+    } else if (o.math == SBGEMM_MATH_TF32 && attention_tc_supported(a)) {
+        e = launch_attention_tc(a, s);
+    } else {
+        e = launch_attention(a, s);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SBGEMM_ERR_CUDA;
+    }
+    return SBGEMM_OK;
+}
+
+int sbgemm_attention_paged(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
+                           const float* K_cache, const float* V_cache,
+                           int64_t num_blocks, int64_t block_size, int64_t n_kv_heads,
+                           const int32_t* block_table, int64_t max_blocks, const int32_t* seq_lens,
+                           float* O, int64_t rsO, int64_t csO, int64_t bsO,
+                           int64_t M, int64_t N, int64_t D, int64_t Dv, int64_t n_seqs,
+                           float alpha, int causal, int64_t q_len, void* stream,
+                           const sbgemm_options* opt) {
+    sbgemm_options o;
+    const int ost = check_options(opt, &o);
+    if (ost) return ost;
+    if (o.force_path != SBGEMM_PATH_AUTO) return SBGEMM_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || D < 0 || Dv < 0 || n_seqs < 0) return SBGEMM_ERR_INVALID_VALUE;
+    if (causal != 0 && causal != 1) return SBGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || n_seqs == 0 || Dv == 0) return SBGEMM_OK;
+    if (N == 0) return SBGEMM_ERR_INVALID_VALUE;
+    if (causal && (q_len <= 0 || q_len > N)) return SBGEMM_ERR_INVALID_VALUE;
+    if (num_blocks <= 0 || block_size <= 0 || n_kv_heads <= 0 || max_blocks <= 0)
+        return SBGEMM_ERR_INVALID_VALUE;
+    if ((__int128)max_blocks * block_size < (__int128)N) return SBGEMM_ERR_INVALID_VALUE;
+    if (!attention_supported(D, Dv)) return SBGEMM_ERR_UNSUPPORTED;
+    const __int128 batch128 = (__int128)n_seqs * n_kv_heads;
+    if (M > attention_max_rows() || batch128 >= ((__int128)1 << 31)) return SBGEMM_ERR_UNSUPPORTED;
+    const int64_t batch = (int64_t)batch128;
+    if (!Q || !K_cache || !V_cache || !block_table || !O) return SBGEMM_ERR_NULL_POINTER;
+    if (!aligned(Q, 4) || !aligned(O, 4) || !aligned(block_table, 4) || (seq_lens && !aligned(seq_lens, 4)))
+        return SBGEMM_ERR_INVALID_VALUE;
+    if (!aligned(K_cache, 16) || !aligned(V_cache, 16)) return SBGEMM_ERR_INVALID_VALUE;
+    // Element counts of the caches and the int32 tables (4 bytes each, so the
+    // float spans' byte arithmetic holds for them too).
+    const __int128 rows = (__int128)num_blocks * block_size * n_kv_heads;
+    const __int128 k_elems = rows * D, v_elems = rows * Dv, t_elems = (__int128)n_seqs * max_blocks;
+    const __int128 lim = (__int128)1 << 60;
+    if (k_elems >= lim || v_elems >= lim || t_elems >= lim) return SBGEMM_ERR_INVALID_VALUE;
+    Span sq{}, so{};
+    if (!operand_span(batch, M, D, bsQ, rsQ, csQ, &sq) || !operand_span(batch, M, Dv, bsO, rsO, csO, &so))
+        return SBGEMM_ERR_INVALID_VALUE;
+    const Span sk{0, (int64_t)k_elems - 1}, sv{0, (int64_t)v_elems - 1};
+    const Span st{0, (int64_t)t_elems - 1}, sl{0, n_seqs - 1};
+    if (!output_injective(batch, M, Dv, bsO, rsO, csO)) return SBGEMM_ERR_OUTPUT_OVERLAP;
+    if (bytes_meet(O, so, Q, sq) || bytes_meet(O, so, K_cache, sk) || bytes_meet(O, so, V_cache, sv) ||
+        bytes_meet(O, so, block_table, st) || (seq_lens && bytes_meet(O, so, seq_lens, sl)))
+        return SBGEMM_ERR_OUTPUT_OVERLAP;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
+    if (!span_in_allocation(Q, sq) || !span_in_allocation(K_cache, sk) || !span_in_allocation(V_cache, sv) ||
+        !span_in_allocation(block_table, st) || (seq_lens && !span_in_allocation(seq_lens, sl)) ||
+        !span_in_allocation(O, so))
+        return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    const int wst = check_attention_workspace(
+        o, {{Q, sq}, {K_cache, sk}, {V_cache, sv}, {block_table, st}, {O, so},
+            {seq_lens ? static_cast<const void*>(seq_lens) : static_cast<const void*>(O), seq_lens ? sl : so}});
+    if (wst) return wst;
+    AttnProblem a{Q, rsQ, csQ, bsQ, K_cache, n_kv_heads * D, 1, 0, V_cache, n_kv_heads * Dv, 1, 0,
+                  O, rsO, csO, bsO, M, N, D, Dv, batch, alpha, causal, causal ? q_len : M,
+                  ElemSpan{sq.lo, sq.hi}, ElemSpan{sk.lo, sk.hi}, ElemSpan{sv.lo, sv.hi},
+                  ElemSpan{so.lo, so.hi}};
+    a.paged = 1;
+    a.table = block_table;
+    a.seq_lens = seq_lens;
+    a.max_blocks = max_blocks;
+    a.block_size = block_size;
+    a.n_kv_heads = n_kv_heads;
+    a.num_blocks = num_blocks;
+    a.workspace = o.workspace;
+    a.workspace_bytes = o.workspace ? o.workspace_bytes : 0;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = attention_decode_supported(a) ? launch_attention_decode(a, s)
+                                                         : launch_attention(a, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SBGEMM_ERR_CUDA;
@@ -599,14 +706,17 @@ int sbgemm_device_status(void* stream, int* where_out) {
     const unsigned int code_at = read_and_clear_wait_status_attention_tc(s);
     const unsigned int code_g = read_and_clear_status_gather(s);
     const unsigned int code_a = read_and_clear_status_attention(s);
+    const unsigned int code_d = read_and_clear_status_attention_decode(s);
     if (code == 0) code = code_tc;
     if (code == 0) code = code_st;
     if (code == 0) code = code_at;
     if (code == 0) code = code_g;
     if (code == 0) code = code_a;
+    if (code == 0) code = code_d;
     if (code != 0) {
         if (where_out) *where_out = (int)code;
-        return SBGEMM_ERR_DEVICE_TIMEOUT;
+        return (code == kBoundsViolation || code == kPagedInput) ? SBGEMM_ERR_DEVICE_CHECK
+                                                                  : SBGEMM_ERR_DEVICE_TIMEOUT;
     }
     return SBGEMM_OK;
 }

@@ -128,7 +128,8 @@ def test_attention_errors(torch):
             return e.status
 
     assert status() == sg.SBGEMM_OK
-    assert status(D=32, Dv=32) == sg.SBGEMM_ERR_UNSUPPORTED
+    assert status(D=48, Dv=48) == sg.SBGEMM_ERR_UNSUPPORTED
+    assert status(D=64, Dv=32) == sg.SBGEMM_ERR_UNSUPPORTED
     assert status(N=0) == sg.SBGEMM_ERR_INVALID_VALUE
     assert status(M=0, N=0) == sg.SBGEMM_OK
     assert status(causal=1, q_len=0) == sg.SBGEMM_ERR_INVALID_VALUE

@@ -27,6 +27,9 @@ CASES = [
     "tests/test_fused_gpu.py::test_fused_every_path_activation_and_addend",
     "tests/test_attention_gpu.py::test_attention_small_against_oracle",
     "tests/test_attention_gpu.py::test_attention_tf32_small_against_oracle",
+    "tests/test_attention_paged_gpu.py::test_head_dims_against_oracle",
+    "tests/test_attention_paged_gpu.py::test_decode_against_oracle",
+    "tests/test_attention_paged_gpu.py::test_paged_against_oracle",
 ]
 
 

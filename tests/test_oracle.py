@@ -483,6 +483,21 @@ def run_attention_pins(lib=None):
     bad += not np.allclose(O6, np.einsum("bmn,bne->bme", P, V.astype(np.float64)), rtol=0, atol=1e-12)
     bad += not np.allclose(S6, (np.abs(Qr).astype(np.float64) @ np.abs(K.astype(np.float64)).transpose(0, 2, 1)).max(axis=2) * 0.5,
                            rtol=1e-14, atol=0)
+    # The head dimensions the kernels take (32, 64, 96, 128): zero queries give
+    # the mean of the value rows; one-hot queries against one-hot keys give the
+    # closed form above, with the remaining dimensions zero.
+    for Dh in (32, 64, 96, 128):
+        Kd = rng.standard_normal((1, 11, Dh)).astype(np.float32)
+        Vd = rng.standard_normal((1, 11, Dh)).astype(np.float32)
+        O, _, _ = attn(np.zeros((1, 3, Dh), np.float32), Kd, Vd, 1.0 / np.sqrt(Dh))
+        bad += not np.allclose(O[0], np.broadcast_to(Vd[0].astype(np.float64).mean(axis=0), O[0].shape),
+                               rtol=0, atol=1e-12)
+        Eh = np.zeros((1, Nh, Dh), np.float32)
+        Eh[0, np.arange(Nh), np.arange(Nh) * (Dh // Nh)] = 1.0
+        Vh = rng.standard_normal((1, Nh, Dh)).astype(np.float32).astype(np.float64)
+        O, _, _ = attn(Eh, Eh, Vh, a)
+        want = (np.exp(a) * Vh[0] + (Vh[0].sum(axis=0, keepdims=True) - Vh[0])) / (np.exp(a) + Nh - 1)
+        bad += not np.allclose(O[0], want, rtol=0, atol=1e-12)
     return bad
 
 
@@ -500,6 +515,67 @@ def test_attention_strided_layouts_match_dense():
     O, W, S = oracle.attention_case(c)
     O2, W2, S2 = _attn(Qd, Kd, Vd, c.alpha, True, 11)
     assert np.array_equal(O, O2) and np.array_equal(W, W2) and np.array_equal(S, S2)
+
+
+# ---- paged key / value reads ----------------------------------------------------
+
+def run_paged_pins(lib=None):
+    """Pins of the paged-cache reader and of paged attention.  The caches come
+    from the workload generator, which writes each token at the offset it
+    counts up inside the block it takes from a shuffled free list (the
+    scheduler's side of the page's layout); the oracle divides positions back
+    into (block, offset) through the table.  Returns the number of failures."""
+    rng = np.random.default_rng(41)
+    bad = 0
+
+    def gather(cache, table, s, h, n):
+        try:
+            return oracle.kv_gather(cache, table, s, h, n, lib=lib)
+        except ValueError:            # a refusal where the pages' layout has the row
+            return np.full((n, cache.shape[3]), np.nan, np.float32)
+
+    for bsz, lens, heads, Dh in ((4, [1, 5, 16, 17, 40], 3, 8), (1, [3, 9], 2, 4),
+                                 (64, [64, 2, 65], 2, 4), (5, [23, 24, 25], 4, 3)):
+        Kc, Vc, table, seq_lens, K_ctx, V_ctx = wl.paged_cache(rng, lens, heads, Dh, bsz)
+        for s, n in enumerate(lens):
+            for h in range(heads):
+                bad += not np.array_equal(gather(Kc, table, s, h, n), K_ctx[s, h, :n])
+                bad += not np.array_equal(gather(Vc, table, s, h, n), V_ctx[s, h, :n])
+        # No slot outside a sequence's tokens is ever read (they hold NaN).
+        bad += not all(np.isfinite(gather(Kc, table, s, h, n)).all()
+                       for s, n in enumerate(lens) for h in range(heads))
+    # A block id outside the cache, or a position past the table, is refused.
+    Kc, Vc, table, seq_lens, K_ctx, V_ctx = wl.paged_cache(rng, [9, 4], 1, 2, 4)
+    t2 = table.copy()
+    t2[0, 1] = Kc.shape[0]
+    for tab, n in ((t2, 9), (table, 4 * table.shape[1] + 1)):
+        try:
+            oracle.kv_gather(Kc, tab, 0, 0, n, lib=lib)
+            bad += 1
+        except ValueError:
+            pass
+    # Paged attention equals the attention oracle on the contiguous context
+    # of each (sequence, head), with causal positions taken from that
+    # sequence's own length.
+    case = wl.random_paged_attention(rng, [3, 30, 19], 2, 3, 2, 8, 4, causal=1)
+    try:
+        O, W, S = oracle.attention_paged(case.Q, case.K_cache, case.V_cache, case.block_table,
+                                         case.seq_lens, case.M, case.alpha, True, case.q_len, lib=lib)
+    except ValueError:
+        return bad + 1
+    Qd = np.array(case.Q.view(case.batch, case.M, case.D))
+    for s, n in enumerate(case.seq_lens):
+        for h in range(case.n_kv_heads):
+            b = s * case.n_kv_heads + h
+            O2, W2, S2 = _attn(Qd[b:b + 1], case.K_ctx[s:s + 1, h, :n], case.V_ctx[s:s + 1, h, :n],
+                               case.alpha, True, case.q_len, lib=lib)
+            bad += not (np.array_equal(O[b:b + 1], O2) and np.array_equal(W[b:b + 1], W2) and
+                        np.array_equal(S[b:b + 1], S2))
+    return bad
+
+
+def test_paged_pins():
+    assert run_paged_pins() == 0
 
 
 def test_spectrogram_workload_is_the_windowed_dft():

@@ -11,7 +11,7 @@ import pytest
 import oracle
 import workloads as wl
 from tests.test_oracle import (run_activation_pins, run_attention_pins, run_epilogue_pins,
-                               run_int_pins)
+                               run_int_pins, run_paged_pins)
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "sbgemm_ref.c")
 
@@ -52,6 +52,7 @@ def test_unmutated_copy_passes(tmp_path):
     assert run_int_pins(lib=lib) == 0
     assert run_activation_pins(lib=lib) == 0 and run_epilogue_pins(lib=lib) == 0
     assert run_attention_pins(lib=lib) == 0
+    assert run_paged_pins(lib=lib) == 0
 
 
 # Slips in the fused epilogue's activations and added operand.
@@ -104,3 +105,28 @@ def test_planted_attention_mistake_is_caught(tmp_path, name, old, new):
     oracle.build(force=True, src=str(mutated), out=so)
     lib = oracle.load(so)
     assert run_attention_pins(lib=lib) > 0, f"planted mistake {name} went unnoticed"
+
+
+# Slips in the paged-cache reader.
+PAGED_MUTATIONS = [
+    ("block_index_modulo", "const int64_t block_pos = pos / block_size;",
+     "const int64_t block_pos = pos % block_size;"),
+    ("offset_divides", "const int64_t offset = pos % block_size;", "const int64_t offset = pos / block_size;"),
+    ("head_stride_dropped", "* n_kv_heads + head) * head_dim", "+ head) * head_dim"),
+    ("table_row_ignored", "block_table[seq * max_blocks + block_pos]", "block_table[block_pos]"),
+    ("block_stride_dropped", "((block * block_size + offset)", "((block + offset)"),
+    ("last_position_dropped", "for (int64_t pos = 0; pos < len; ++pos) {",
+     "for (int64_t pos = 0; pos + 1 < len; ++pos) {"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", PAGED_MUTATIONS, ids=[m[0] for m in PAGED_MUTATIONS])
+def test_planted_paged_mistake_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = tmp_path / "mut.c"
+    mutated.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmut.so")
+    oracle.build(force=True, src=str(mutated), out=so)
+    lib = oracle.load(so)
+    assert run_paged_pins(lib=lib) > 0, f"planted mistake {name} went unnoticed"

@@ -52,7 +52,8 @@ from typing import Dict, Optional, Tuple
 import numpy as np
 
 __all__ = ["Operand", "Case", "WORKLOADS", "BACKWARD", "make", "flops", "gflops_per_s",
-           "alg_bytes", "SEEDS", "AttnCase", "ATTENTION", "make_attention", "random_attention"]
+           "alg_bytes", "SEEDS", "AttnCase", "ATTENTION", "make_attention", "random_attention",
+           "PagedCase", "PAGED", "paged_cache", "random_paged_attention", "make_paged"]
 
 
 @dataclasses.dataclass
@@ -526,3 +527,135 @@ def random_attention(rng: np.random.Generator, M: int, N: int, D: int, batch: in
         raise ValueError(layout)
     return AttnCase(f"attn_{layout}_{M}x{N}x{D}", Q, K, V, O, M, N, D, D, batch, alpha,
                     int(bool(causal)), q_len)
+
+
+# ---- paged key / value cache ---------------------------------------------------
+# "rvllm CUDA path", section "The kernels": the cache is one buffer
+# [num_blocks, block_size, n_kv_heads, head_dim]; each new token's K and V go
+# to a block id and an offset handed out by the cache scheduler, and a
+# sequence's block table lists its blocks in order.  The generator below plays
+# the scheduler: sequences append one token per step (a batched decode loop),
+# each takes the next block of a shuffled free list when its current block is
+# full, and the token is written at (current block, next free offset).  It
+# counts offsets up instead of dividing positions, so it is an independent
+# statement of the layout the readers (oracle and kernels) divide back out.
+
+@dataclasses.dataclass
+class PagedCase:
+    name: str
+    Q: Operand                 # [n_seqs * n_kv_heads, M, D]; entry b = seq * n_kv_heads + head
+    O: Operand                 # [n_seqs * n_kv_heads, M, D] (output)
+    K_cache: np.ndarray        # float32 [num_blocks, block_size, n_kv_heads, D]; unused slots NaN
+    V_cache: np.ndarray
+    block_table: np.ndarray    # int32 [n_seqs, max_blocks]; entries past a sequence's blocks -1
+    seq_lens: np.ndarray       # int32 [n_seqs]
+    K_ctx: np.ndarray          # float32 [n_seqs, n_kv_heads, N, D]: the keys appended, in order
+    V_ctx: np.ndarray          #   (positions past a sequence's length are zero)
+    M: int
+    N: int                     # longest context
+    D: int
+    n_kv_heads: int
+    block_size: int
+    alpha: float
+    causal: int
+    q_len: int
+
+    @property
+    def n_seqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def batch(self) -> int:
+        return self.n_seqs * self.n_kv_heads
+
+    @property
+    def keys(self) -> int:
+        """Keys read over the batch: every head of every context position."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.n_kv_heads
+
+    @property
+    def flops(self) -> int:
+        """2*M*len*(D + Dv) per entry, every key counted."""
+        return 2 * self.M * self.keys * 2 * self.D
+
+    @property
+    def alg_bytes(self) -> int:
+        """K and V rows of every context position read once, Q read and O
+        written once, the table and lengths read once."""
+        return (self.keys * 2 * self.D * 4 + 2 * self.batch * self.M * self.D * 4 +
+                self.block_table.size * 4 + self.seq_lens.size * 4)
+
+
+def paged_cache(rng: np.random.Generator, lens, n_kv_heads: int, D: int, block_size: int,
+                spare_blocks: int = 3, scale: float = 1.0):
+    """A paged cache holding, for each sequence s, lens[s] tokens of random K
+    and V.  Returns (K_cache, V_cache, block_table, seq_lens, K_ctx, V_ctx)."""
+    lens = np.asarray(lens, dtype=np.int64)
+    n_seqs, N = len(lens), int(lens.max())
+    need = np.zeros(n_seqs, dtype=np.int64)
+    for s in range(n_seqs):          # blocks each sequence will fill, by counting
+        c = 0
+        while c * block_size < lens[s]:
+            c += 1
+        need[s] = c
+    num_blocks = int(need.sum()) + spare_blocks
+    max_blocks = int(need.max()) + 1
+    K_ctx = np.zeros((n_seqs, n_kv_heads, N, D), dtype=np.float32)
+    V_ctx = np.zeros((n_seqs, n_kv_heads, N, D), dtype=np.float32)
+    for s in range(n_seqs):
+        K_ctx[s, :, :lens[s]] = _normal(rng, scale, (n_kv_heads, int(lens[s]), D))
+        V_ctx[s, :, :lens[s]] = _normal(rng, 1.0, (n_kv_heads, int(lens[s]), D))
+    K_cache = np.full((num_blocks, block_size, n_kv_heads, D), np.nan, dtype=np.float32)
+    V_cache = np.full((num_blocks, block_size, n_kv_heads, D), np.nan, dtype=np.float32)
+    table = np.full((n_seqs, max_blocks), -1, dtype=np.int32)
+    free = list(rng.permutation(num_blocks))
+    cur_block = np.full(n_seqs, -1, dtype=np.int64)
+    cur_off = np.full(n_seqs, block_size, dtype=np.int64)   # "full": take a block first
+    n_blocks = np.zeros(n_seqs, dtype=np.int64)
+    for t in range(N):
+        active = np.nonzero(lens > t)[0]
+        for s in active[cur_off[active] == block_size]:
+            cur_block[s] = free.pop(0)
+            cur_off[s] = 0
+            table[s, n_blocks[s]] = cur_block[s]
+            n_blocks[s] += 1
+        K_cache[cur_block[active], cur_off[active]] = K_ctx[active, :, t]
+        V_cache[cur_block[active], cur_off[active]] = V_ctx[active, :, t]
+        cur_off[active] += 1
+    return K_cache, V_cache, table, lens.astype(np.int32), K_ctx, V_ctx
+
+
+def random_paged_attention(rng: np.random.Generator, lens, n_kv_heads: int, group: int,
+                           q_len: int, D: int, block_size: int, causal: int = 1,
+                           alpha: Optional[float] = None, scale: float = 1.0,
+                           name: str = "paged") -> PagedCase:
+    """Attention of M = group * q_len query rows per (sequence, kv head)
+    (grouped-query heads stacked as rows) over a paged cache of the given
+    context lengths."""
+    Kc, Vc, table, seq_lens, K_ctx, V_ctx = paged_cache(rng, lens, n_kv_heads, D, block_size,
+                                                        scale=scale)
+    n_seqs = len(seq_lens)
+    M = group * q_len
+    batch = n_seqs * n_kv_heads
+    q = _normal(rng, 1.0, (batch, M, D))
+    return PagedCase(name, Operand(_flat(q), 0, D, 1, M * D),
+                     Operand(np.zeros(batch * M * D, dtype=np.float32), 0, D, 1, M * D),
+                     Kc, Vc, table, seq_lens, K_ctx, V_ctx, M, int(seq_lens.max()), D, n_kv_heads,
+                     block_size, 1.0 / float(np.sqrt(D)) if alpha is None else alpha,
+                     int(bool(causal)), q_len)
+
+
+PAGED = {
+    # name: (n_seqs, n_kv_heads, group, q_len, D, block_size, context lengths)
+    # A batched decode step: 32 sequences (the pages' largest batch), 8 KV heads
+    # with 4 query heads each, head dimension 64, 16-token blocks, contexts
+    # drawn uniformly from 1024..4096 tokens.
+    "f2paged": (32, 8, 4, 1, 64, 16, (1024, 4096)),
+}
+
+
+def make_paged(name: str) -> PagedCase:
+    n_seqs, heads, group, q_len, D, bsz, (lo, hi) = PAGED[name]
+    rng = np.random.Generator(np.random.PCG64([7, list(PAGED).index(name), 0]))
+    lens = rng.integers(lo, hi + 1, size=n_seqs)
+    return random_paged_attention(rng, lens, heads, group, q_len, D, bsz, causal=1, name=name)
