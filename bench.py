@@ -488,6 +488,33 @@ def run_ours(args, world, rank, local, dist):
                                 "peak_source": f"{peaks_src} bf16 dense burst x nominal tf32/bf16 "
                                                f"ratio {TF32_OVER_BF16_NOMINAL:.3f}",
                                 "traffic": profiled_traffic("tma_tf32", n)}
+            # The rate the hardware demonstrably reaches in tf32, measured
+            # here: the vendor library's tf32 GEMM on an 8192^3 row-major
+            # product (a comparison denominator only; nothing on the
+            # library's path calls it).
+            prev = torch.backends.cuda.matmul.allow_tf32
+            torch.backends.cuda.matmul.allow_tf32 = True
+            try:
+                ga = torch.randn(8192, 8192, device=dev)
+                gb = torch.randn(8192, 8192, device=dev)
+                gc = torch.empty(8192, 8192, device=dev)
+                for _ in range(3):
+                    torch.matmul(ga, gb, out=gc)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(10):
+                    torch.matmul(ga, gb, out=gc)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                lib_tf = 2 * 8192 ** 3 / (e0.elapsed_time(e1) / 10 * 1e-3) / 1e12
+                tf32["roofline"]["peak_library_measured"] = round(lib_tf, 1)
+                tf32["roofline"]["frac_of_library_measured"] = round(ach / lib_tf, 4)
+                tf32["roofline"]["library_measured_source"] = (
+                    "torch.matmul tf32 (cuBLAS), 8192^3 fp32, mean of 10 after 3 warm-ups, this run")
+                del ga, gb, gc
+            finally:
+                torch.backends.cuda.matmul.allow_tf32 = prev
 
     # Backward products of the same layers (dX = G W, dW += G^T X), each with
     # the step's workspace and without it: the long-K weight gradients have
@@ -682,6 +709,18 @@ def run_ours(args, world, rank, local, dist):
         hbm = float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]))
         fp32_peak = sms * FP32_FLOP_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
         tf32_peak = float(peaks.get("bf16_tflops", FALLBACK["bf16_tflops"])) * TF32_OVER_BF16_NOMINAL
+        # The floor of the single-launch figure: two events recorded back to
+        # back with nothing between them (the host's event-record calls and
+        # the GPU's timestamp latency, which every single-launch median
+        # below includes on top of the call and the kernel).
+        floor = []
+        for _ in range(41):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            e1.record(stream)
+            e1.synchronize()
+            floor.append(e0.elapsed_time(e1) * 1e3)
+        configs["single_launch_event_floor_us"] = round(statistics.median(floor), 2)
         for n in ("c1", "c2a", "c2b", "c3", "c3gqa", "c4"):
             c = wl.make(n, "real")
             bufs = tuple(torch.from_numpy(x).to(dev) for x in (c.A.storage, c.B.storage, c.C.storage))

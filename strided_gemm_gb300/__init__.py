@@ -108,6 +108,8 @@ def load(path: str = LIB_PATH):
     """Load libsbgemm.so.  Raises if the library has not been built: there is
     no fallback implementation."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -167,6 +169,22 @@ def _opts(math: int, force_path: int, workspace=0, workspace_bytes=0, k_split=KS
     return o
 
 
+# Option structs by value, reused across calls (the library reads them only
+# during the call): a call with options it has seen before builds nothing.
+_opts_cache: dict = {}
+
+
+def _opts_ref(math, force_path, workspace, workspace_bytes, k_split):
+    key = (math, force_path, workspace, workspace_bytes, k_split)
+    r = _opts_cache.get(key)
+    if r is None:
+        o = _opts(math, force_path, workspace, workspace_bytes, k_split)
+        if len(_opts_cache) >= 256:
+            _opts_cache.clear()
+        r = _opts_cache[key] = (o, ctypes.byref(o))
+    return r[1]
+
+
 def sbgemm_workspace_bytes(device: int = 0) -> int:
     """Bytes of caller-owned workspace that enable the stream-K schedule."""
     n = ctypes.c_size_t(0)
@@ -186,8 +204,9 @@ def sbgemm_version() -> int:
 
 def sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
            M, N, K, batch, alpha, accumulate, stream=0) -> None:
-    st = load().sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
-                       M, N, K, batch, float(alpha), int(bool(accumulate)), stream or None)
+    lib = _lib if _lib is not None else load()
+    st = lib.sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                    M, N, K, batch, alpha, 1 if accumulate else 0, stream or None)
     if st:
         raise SbgemmError(st, "sbgemm")
 
@@ -210,10 +229,10 @@ def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
               M, N, K, batch, alpha, accumulate, stream=0,
               math: int = MATH_FP32, force_path: int = PATH_AUTO,
               workspace: int = 0, workspace_bytes: int = 0, k_split: int = KSPLIT_ANY) -> None:
-    o = _opts(math, force_path, workspace, workspace_bytes, k_split)
-    st = load().sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
-                          M, N, K, batch, float(alpha), int(bool(accumulate)),
-                          stream or None, ctypes.byref(o))
+    lib = _lib if _lib is not None else load()
+    st = lib.sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                       M, N, K, batch, alpha, 1 if accumulate else 0, stream or None,
+                       _opts_ref(math, force_path, workspace, workspace_bytes, k_split))
     if st:
         raise SbgemmError(st, "sbgemm_ex")
 

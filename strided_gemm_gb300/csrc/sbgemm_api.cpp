@@ -167,13 +167,32 @@ int validate(const Problem& p, Span* sa, Span* sb, Span* sc, bool* empty) {
     return SBGEMM_OK;
 }
 
+// Allocation ranges already looked up during one call: an operand whose span
+// lies inside one of them needs no driver query (operands in one pool
+// segment, or views of one buffer, share a lookup).  Lives for one call only,
+// so it never outlasts an allocation.
+struct Ranges {
+    int n = 0;
+    uintptr_t base[8];
+    size_t size[8];
+};
+
 // The operand's whole span lies inside one device-accessible allocation.
-bool span_in_allocation(const void* base, const Span& s) {
+bool span_in_allocation(const void* base, const Span& s, Ranges* seen = nullptr) {
+    const __int128 lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.lo * 4;
+    const __int128 hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.hi * 4 + 4;
+    if (seen)
+        for (int i = 0; i < seen->n; ++i)
+            if (lo >= (__int128)seen->base[i] && hi <= (__int128)seen->base[i] + (__int128)seen->size[i])
+                return true;
     uintptr_t abase = 0;
     size_t asize = 0;
     if (!device_allocation_range(base, &abase, &asize)) return false;
-    const __int128 lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.lo * 4;
-    const __int128 hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)s.hi * 4 + 4;
+    if (seen && seen->n < 8) {
+        seen->base[seen->n] = abase;
+        seen->size[seen->n] = asize;
+        ++seen->n;
+    }
     return lo >= (__int128)abase && hi <= (__int128)abase + (__int128)asize;
 }
 
@@ -393,10 +412,11 @@ int run(Problem& p, const sbgemm_options& o, void* stream) {
     const DeviceProps* props = device_props(dev);
     if (!props) return SBGEMM_ERR_CUDA;
 
-    if (!span_in_allocation(p.C, sc)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
-    if (p.K > 0 && (!span_in_allocation(p.A, sa) || !span_in_allocation(p.B, sb)))
+    Ranges seen;
+    if (!span_in_allocation(p.C, sc, &seen)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    if (p.K > 0 && (!span_in_allocation(p.A, sa, &seen) || !span_in_allocation(p.B, sb, &seen)))
         return SBGEMM_ERR_NOT_DEVICE_MEMORY;
-    if (p.epi.D && !span_in_allocation(p.epi.D, sd)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+    if (p.epi.D && !span_in_allocation(p.epi.D, sd, &seen)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
 
     // The validated spans, for the bounds checks of a debug build.
     p.sa = ElemSpan{sa.lo, sa.hi};
@@ -412,7 +432,7 @@ int run(Problem& p, const sbgemm_options& o, void* stream) {
         // The workspace is written by the kernel: it must be device memory and
         // must not meet any operand.
         const Span sw{0, (int64_t)(o.workspace_bytes / 4) - 1};
-        if (!span_in_allocation(o.workspace, sw)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
+        if (!span_in_allocation(o.workspace, sw, &seen)) return SBGEMM_ERR_NOT_DEVICE_MEMORY;
         auto meets = [&](const void* base, const Span& sp) {
             const __int128 lo = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)sp.lo * 4;
             const __int128 hi = (__int128)reinterpret_cast<uintptr_t>(base) + (__int128)sp.hi * 4 + 4;
@@ -555,8 +575,9 @@ int sbgemm_attention_ex(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ,
         return SBGEMM_ERR_OUTPUT_OVERLAP;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
-    if (!span_in_allocation(Q, sq) || !span_in_allocation(K, sk) || !span_in_allocation(V, sv) ||
-        !span_in_allocation(O, so))
+    Ranges seen;
+    if (!span_in_allocation(Q, sq, &seen) || !span_in_allocation(K, sk, &seen) ||
+        !span_in_allocation(V, sv, &seen) || !span_in_allocation(O, so, &seen))
         return SBGEMM_ERR_NOT_DEVICE_MEMORY;
     const int wst = check_attention_workspace(o, {{Q, sq}, {K, sk}, {V, sv}, {O, so}});
     if (wst) return wst;
@@ -634,9 +655,10 @@ int sbgemm_attention_paged(const float* Q, int64_t rsQ, int64_t csQ, int64_t bsQ
         return SBGEMM_ERR_OUTPUT_OVERLAP;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SBGEMM_ERR_CUDA; }
-    if (!span_in_allocation(Q, sq) || !span_in_allocation(K_cache, sk) || !span_in_allocation(V_cache, sv) ||
-        !span_in_allocation(block_table, st) || (seq_lens && !span_in_allocation(seq_lens, sl)) ||
-        !span_in_allocation(O, so))
+    Ranges seen;
+    if (!span_in_allocation(Q, sq, &seen) || !span_in_allocation(K_cache, sk, &seen) ||
+        !span_in_allocation(V_cache, sv, &seen) || !span_in_allocation(block_table, st, &seen) ||
+        (seq_lens && !span_in_allocation(seq_lens, sl, &seen)) || !span_in_allocation(O, so, &seen))
         return SBGEMM_ERR_NOT_DEVICE_MEMORY;
     const int wst = check_attention_workspace(
         o, {{Q, sq}, {K_cache, sk}, {V_cache, sv}, {block_table, st}, {O, so},
