@@ -188,5 +188,8 @@ bool device_allocation_range(const void* ptr, uintptr_t* base, size_t* size);
 // and 2, box extents, optional 128-byte swizzle.  Zero fill out of bounds.
 bool encode_tmap_f32_3d(CUtensorMap* map, const void* base, const uint64_t dims[3],
                         const uint64_t strides_bytes[2], const uint32_t box[3], bool swizzle128);
+// The same with rank 4 (byte strides of dims 1, 2 and 3).
+bool encode_tmap_f32_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                        const uint64_t strides_bytes[3], const uint32_t box[4], bool swizzle128);
 
 }  // namespace sbg

@@ -135,6 +135,7 @@ struct Params {
     int accumulate;
     int a_bcast, b_bcast;
     int c_tma;                    // C goes out through its tensor map: 1 unit stride along N, 2 along M
+    int a_blk4, b_blk4;           // the MN-major operand's map is rank 4: a slice's boxes in one copy
     int64_t dp_tiles, sk_units;   // work list (see schedule.cuh)
     EpiParams epi;                // fused epilogue (epilogue.cuh); epi.on == 0: none
     float4* ws_partial;           // [grid][8 chunks][8 quads][128 rows] partial sums
@@ -199,17 +200,32 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
                     ok = false;
                     break;
                 }
-                // Boxes wholly past a ragged edge are not fetched.
-                const int boxes_a = C::kTA ? valid_boxes<BM>(p.M - tc.m0) : 0;
-                const int boxes_b = C::kTB ? valid_boxes<BN>(p.N - tc.n0) : 0;
+                // With a rank-4 map (the extent a multiple of 32) one copy
+                // brings all of a slice's boxes, those past a ragged edge
+                // zero-filled; otherwise boxes wholly past the edge are not
+                // fetched.
+                const int boxes_a = C::kTA ? (p.a_blk4 ? BM / 32 : valid_boxes<BM>(p.M - tc.m0)) : 0;
+                const int boxes_b = C::kTB ? (p.b_blk4 ? BN / 32 : valid_boxes<BN>(p.N - tc.n0)) : 0;
                 mbar_arrive_expect_tx(&sh.rfull[r], (uint32_t)(boxes_a + boxes_b) * kBox * 4);
-#pragma unroll 1
-                for (int j = 0; j < boxes_a; ++j)
-                    tma_load_3d(sh.raw[r] + j * kBox, ta, &sh.rfull[r], (int)tc.m0 + 32 * j, kt * BK, ba);
                 float* raw_b = sh.raw[r] + (C::kRawRowsA / 32) * kBox;
+                if constexpr (C::kTA) {
+                    if (p.a_blk4) {
+                        tma_load_4d(sh.raw[r], ta, &sh.rfull[r], 0, kt * BK, (int)(tc.m0 / 32), ba);
+                    } else {
 #pragma unroll 1
-                for (int j = 0; j < boxes_b; ++j)
-                    tma_load_3d(raw_b + j * kBox, tb, &sh.rfull[r], (int)tc.n0 + 32 * j, kt * BK, bb);
+                        for (int j = 0; j < boxes_a; ++j)
+                            tma_load_3d(sh.raw[r] + j * kBox, ta, &sh.rfull[r], (int)tc.m0 + 32 * j, kt * BK, ba);
+                    }
+                }
+                if constexpr (C::kTB) {
+                    if (p.b_blk4) {
+                        tma_load_4d(raw_b, tb, &sh.rfull[r], 0, kt * BK, (int)(tc.n0 / 32), bb);
+                    } else {
+#pragma unroll 1
+                        for (int j = 0; j < boxes_b; ++j)
+                            tma_load_3d(raw_b + j * kBox, tb, &sh.rfull[r], (int)tc.n0 + 32 * j, kt * BK, bb);
+                    }
+                }
             }
             if constexpr (C::kKRing) {
                 const int st = (int)(i % S);
@@ -746,6 +762,22 @@ bool make_mn_map(CUtensorMap* map, const float* base, int64_t inner, int64_t K, 
     return encode_tmap_f32_3d(map, base, dims, strides, box, true);
 }
 
+// The same operand as a rank-4 map for an extent that is a multiple of 32:
+// dims (32 along M or N, K, blocks of 32, batch), so that one box of
+// (32, 32, rows / 32) lands as the rows / 32 boxes of make_mn_map one after
+// another.  False if the extent does not divide or the driver refuses it.
+bool make_mn_map4(CUtensorMap* map, const float* base, int64_t inner, int64_t K, int64_t sk,
+                  int64_t sb, int64_t batch, bool broadcast, int rows) {
+    if (inner % 32 != 0 || inner / 32 >= ((int64_t)1 << 31)) return false;
+    const int64_t nb = broadcast ? 1 : batch;
+    const int64_t sk_b = K > 1 ? sk * 4 : ((inner * 4 + 15) / 16) * 16;
+    const int64_t sb_b = nb > 1 ? sb * 4 : sk_b * (K > 1 ? K : 1);
+    const uint64_t dims[4] = {32, (uint64_t)K, (uint64_t)(inner / 32), (uint64_t)nb};
+    const uint64_t strides[3] = {(uint64_t)sk_b, 128, (uint64_t)sb_b};
+    const uint32_t box[4] = {32, 32, (uint32_t)(rows / 32), 1};
+    return encode_tmap_f32_4d(map, base, dims, strides, box, true);
+}
+
 bool make_kmajor_map(CUtensorMap* map, const float* base, int64_t K, int64_t rows, int64_t so,
                      int64_t sb, int64_t batch, bool broadcast, int box_rows) {
     const int64_t nb = broadcast ? 1 : batch;
@@ -811,12 +843,16 @@ cudaError_t launch_mn(const Problem& pr, const Plan& plan, cudaStream_t stream) 
     const bool a_bc = pr.batch == 1 || pr.bsA == 0;
     const bool b_bc = pr.batch == 1 || pr.bsB == 0;
     // A[m][k] = A + m*rsA + k*csA; B[k][n] = B + k*rsB + n*csB.
-    const bool ok_a = C::kTA ? make_mn_map(&ta, pr.A, pr.M, pr.K, pr.csA, pr.bsA, pr.batch, a_bc)
-                             : make_kmajor_map(&ta, pr.A, pr.K, pr.M, pr.rsA, pr.bsA, pr.batch, a_bc, BM);
-    const bool ok_b = C::kTB ? make_mn_map(&tb, pr.B, pr.N, pr.K, pr.rsB, pr.bsB, pr.batch, b_bc)
-                             : make_kmajor_map(&tb, pr.B, pr.K, pr.N, pr.csB, pr.bsB, pr.batch, b_bc, BN);
+    const int a4 = C::kTA && make_mn_map4(&ta, pr.A, pr.M, pr.K, pr.csA, pr.bsA, pr.batch, a_bc, BM) ? 1 : 0;
+    const int b4 = C::kTB && make_mn_map4(&tb, pr.B, pr.N, pr.K, pr.rsB, pr.bsB, pr.batch, b_bc, BN) ? 1 : 0;
+    const bool ok_a = a4 || (C::kTA ? make_mn_map(&ta, pr.A, pr.M, pr.K, pr.csA, pr.bsA, pr.batch, a_bc)
+                                    : make_kmajor_map(&ta, pr.A, pr.K, pr.M, pr.rsA, pr.bsA, pr.batch, a_bc, BM));
+    const bool ok_b = b4 || (C::kTB ? make_mn_map(&tb, pr.B, pr.N, pr.K, pr.rsB, pr.bsB, pr.batch, b_bc)
+                                    : make_kmajor_map(&tb, pr.B, pr.K, pr.N, pr.csB, pr.bsB, pr.batch, b_bc, BN));
     if (!ok_a || !ok_b) return cudaErrorInvalidValue;
     Params p;
+    p.a_blk4 = a4;
+    p.b_blk4 = b4;
     p.C = pr.C; p.rsC = pr.rsC; p.csC = pr.csC; p.bsC = pr.bsC;
     p.M = pr.M; p.N = pr.N; p.K = pr.K;
     p.tiles_m = plan.tiles_m; p.tiles_n = plan.tiles_n; p.tiles_total = plan.tiles;
