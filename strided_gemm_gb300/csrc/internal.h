@@ -170,6 +170,8 @@ cudaError_t launch_tf32_tc(const Problem& p, const Plan& plan, int sm_count, cud
 // Fills plan.ctas / stream_k / dp_tiles / k_slices for the TF32 kernel.
 void tf32_tc_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
                       int k_split);
+// Switches a data-parallel plan of two K-major operands to CTA-pair tiles.
+void tf32_tc_pair(const Problem& pr, Plan& plan, int sm_count);
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream);
 
 // ---- status words of the kernels without bounded waits (debug bounds checks) ----

@@ -39,9 +39,15 @@ struct Schedule {
     int head_begin, head_end;     // head: slices [head_begin, head_end)
     int tail_begin;               // tail: slices [tail_begin, nk)
     int has_head, has_tail;
+    int64_t cta, nctas;           // this worker and the number of workers (CTAs, or CTA pairs)
 
     __device__ __forceinline__ void init(int64_t dp_tiles, int64_t sk_units, int nk) {
-        const int64_t c = blockIdx.x, G = gridDim.x;
+        init(dp_tiles, sk_units, nk, blockIdx.x, gridDim.x);
+    }
+
+    __device__ __forceinline__ void init(int64_t dp_tiles, int64_t sk_units, int nk, int64_t c, int64_t G) {
+        cta = c;
+        nctas = G;
         n_dp = dp_tiles > c ? (dp_tiles - 1 - c) / G + 1 : 0;
         has_head = has_tail = 0;
         n_full = 0;
@@ -70,7 +76,7 @@ struct Schedule {
     }
 
     __device__ __forceinline__ Item item(int64_t w, int nk) const {
-        if (w < n_dp) return {blockIdx.x + w * (int64_t)gridDim.x, 0, nk, kFull};
+        if (w < n_dp) return {cta + w * nctas, 0, nk, kFull};
         w -= n_dp;
         if (has_head) {
             if (w == 0) return {head_tile, head_begin, head_end, kHead};

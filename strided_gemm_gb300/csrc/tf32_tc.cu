@@ -59,6 +59,7 @@ constexpr int kTransWarps = 4;               // transposers of the MN-major oper
 constexpr int kBM128 = BM;                               // rows of a partial slot
 constexpr int64_t kSlotFloat4 = (int64_t)BM * BN / 4;    // one partial tile, in float4
 constexpr int kBox = 32 * 32;                // floats in one 32 x 32 raw box of an MN-major operand
+constexpr int kPairVariant = 1;              // Plan::variant of the CTA-pair kernel
 static_assert((size_t)kSlotFloat4 * sizeof(float4) + sizeof(unsigned int) == kWorkspaceBytesPerSm,
               "a partial tile and a flag per CTA fit the workspace sbgemm_workspace_bytes reports");
 
@@ -75,14 +76,19 @@ static_assert((size_t)kSlotFloat4 * sizeof(float4) + sizeof(unsigned int) == kWo
 // both operands MN-major a raw stage holds 48 KB and the shared memory has
 // room for four such stages: 2 raw and 2 transposed measured 8% faster than
 // 3 raw and 1 transposed (which makes the transposers wait on the MMAs).
+// MN 4: both operands K-major on a CTA pair (cta_group::2): a 256 x 256 tile
+// of which each CTA loads 128 rows of A and 128 of B's 256 columns and holds
+// 128 rows of the accumulator; a stage is then 32 KB, so six fit.
 template <int MN>
 struct TCfg {
+    static constexpr bool kPair = MN == 4;
     static constexpr bool kTA = MN == 1 || MN == 3, kTB = MN == 2 || MN == 3;
     static constexpr bool kTrans = kTA || kTB;
     static constexpr bool kKRing = !(kTA && kTB);          // an operand comes in K-major
     static constexpr int kWarps = 2 + kEpiWarps + (kTrans ? kTransWarps : 0);
     static constexpr int kThreads = kWarps * 32;
-    static constexpr int kStages = 4;                      // TMA-fed K-major ring
+    static constexpr int kStages = kPair ? 6 : 4;          // TMA-fed K-major ring
+    static constexpr int kBRows = kPair ? BN / 2 : BN;     // rows of B (columns of C) a CTA loads
     static constexpr int kTStages = kTrans ? 2 : 1;        // transposed ring
     static constexpr int kStagesA = kTA ? kTStages : kStages;
     static constexpr int kStagesB = kTB ? kTStages : kStages;
@@ -91,13 +97,13 @@ struct TCfg {
     static constexpr int kRawStages = (kTA && kTB) ? 2 : (kTA ? 3 : (kTB ? 2 : 0));
     static constexpr int kStageBufs = kTrans ? 1 : 2;     // epilogue staging tiles per warp
     // Bytes the K-major operand copies bring into a stage.
-    static constexpr uint32_t kKBytes = (kTA ? 0 : kABytes) + (kTB ? 0 : kBBytes);
+    static constexpr uint32_t kKBytes = (kTA ? 0 : kABytes) + (kTB ? 0 : (uint32_t)kBRows * BK * 4);
     static constexpr uint32_t kRawBytes = kRawRows * BK * 4;
     static constexpr int kRawSlots = kRawStages > 0 ? kRawStages : 1;
     static constexpr int kRawFloats = kRawRows > 0 ? kRawRows * BK : 4;
     struct Smem {
         float a[kStagesA][BM * BK];
-        float b[kStagesB][BN * BK];
+        float b[kStagesB][kBRows * BK];
         // Per epilogue warp: pieces of C (alternating by store when there are
         // two) in the 128-byte swizzled layout of its tensor map (16-byte chunk
         // q of row r at chunk q ^ (r & 7)).
@@ -136,6 +142,7 @@ struct Params {
     int a_bcast, b_bcast;
     int c_tma;                    // C goes out through its tensor map: 1 unit stride along N, 2 along M
     int a_blk4, b_blk4;           // the MN-major operand's map is rank 4: a slice's boxes in one copy
+    int pair;                     // CTA-pair kernel: tiles of 2 BM rows, this CTA's half by its rank
     int64_t dp_tiles, sk_units;   // work list (see schedule.cuh)
     EpiParams epi;                // fused epilogue (epilogue.cuh); epi.on == 0: none
     float4* ws_partial;           // [grid][8 chunks][8 quads][128 rows] partial sums
@@ -174,7 +181,9 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t) {
     const int64_t first_m = group * G;
     const int64_t gm = (p.tiles_m - first_m < G) ? (p.tiles_m - first_m) : G;
     const int64_t w = r - group * G * p.tiles_n;
-    return {b, (first_m + w % gm) * BM, (w / gm) * BN};
+    const int64_t tm = p.pair ? 2 * BM : BM;
+    const int64_t sub = p.pair ? (int64_t)BM * (cluster_rank() & 1) : 0;
+    return {b, (first_m + w % gm) * tm + sub, (w / gm) * BN};
 }
 
 template <int MN>
@@ -229,18 +238,31 @@ __device__ __forceinline__ void producer(typename TCfg<MN>::Smem& sh, const CUte
             }
             if constexpr (C::kKRing) {
                 const int st = (int)(i % S);
+                // (On a pair the leader's commits free this CTA's stages.)
                 if (i >= (uint64_t)S && !mbar_wait(&sh.empty[st], (uint32_t)(((i / S) - 1) & 1))) {
                     record_status(&g_wait_status, kWaitEmpty);
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&sh.full[st], C::kKBytes);
-                if constexpr (!C::kTA) tma_load_3d(sh.a[st], ta, &sh.full[st], kt * BK, (int)tc.m0, ba);
-                if constexpr (!C::kTB) tma_load_3d(sh.b[st], tb, &sh.full[st], kt * BK, (int)tc.n0, bb);
+                if constexpr (C::kPair) {
+                    // Both CTAs' copies of a stage complete on the leader's
+                    // barrier, which expects the bytes of both.
+                    const uint32_t rank = cluster_rank() & 1;
+                    if (rank == 0) mbar_arrive_expect_tx(&sh.full[st], 2 * C::kKBytes);
+                    const uint32_t bar = cluster_addr(&sh.full[st], 0);
+                    tma_load_3d_pair(sh.a[st], ta, bar, kt * BK, (int)tc.m0, ba);
+                    tma_load_3d_pair(sh.b[st], tb, bar, kt * BK, (int)tc.n0 + C::kBRows * (int)rank, bb);
+                } else {
+                    mbar_arrive_expect_tx(&sh.full[st], C::kKBytes);
+                    if constexpr (!C::kTA) tma_load_3d(sh.a[st], ta, &sh.full[st], kt * BK, (int)tc.m0, ba);
+                    if constexpr (!C::kTB) tma_load_3d(sh.b[st], tb, &sh.full[st], kt * BK, (int)tc.n0, bb);
+                }
             }
         }
     }
-    // Wait for the copies still landing.
+    // Wait for the copies still landing (on a pair, the leader's barrier
+    // counts both CTAs' copies; the peer's own barrier is unused).
+    if (C::kPair && (cluster_rank() & 1) != 0) return;
     if constexpr (C::kKRing) {
         for (uint64_t q = i > (uint64_t)S ? i - S : 0; q < i; ++q)
             if (!mbar_wait(&sh.full[q % S], (uint32_t)((q / S) & 1))) {
@@ -391,6 +413,57 @@ __device__ __forceinline__ void mma_issuer(typename TCfg<MN>::Smem& sh, uint32_t
     }
     // Nothing may still be writing TMEM when it is freed.
     mma_commit(&sh.mma_done);
+    if (!mbar_wait(&sh.mma_done, 0)) record_status(&g_wait_status, kWaitMma);
+}
+
+// CTA pair, leader (rank 0): per slice, wait for the stage of both CTAs (one
+// barrier counts both CTAs' copies), then four 256 x 256 x 8 MMAs over both CTAs' shared
+// memory into both CTAs' TMEM; the commits free the stage and fill the
+// accumulator in both CTAs.  The accumulator is free again once the epilogue
+// warps of both CTAs have drained it.
+template <int MN>
+__device__ __forceinline__ void mma_issuer_pair(typename TCfg<MN>::Smem& sh, uint32_t tmem, const Params& p) {
+    using C = TCfg<MN>;
+    constexpr int S = C::kStages;
+    constexpr uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                               ((uint32_t)((2 * BM) >> 4) << 24);
+    uint64_t i = 0;
+    bool ok = true;
+    const int64_t n_items = sh.sched.n_items;
+    for (int64_t w = 0; w < n_items && ok; ++w) {
+        const Item itm = sh.sched.item(w, p.nk);
+        const uint32_t buf = (uint32_t)(w & 1);
+        const uint64_t use = (uint64_t)w >> 1;
+        if (use > 0 && !mbar_wait_cluster(&sh.acc_empty[buf], (uint32_t)((use - 1) & 1))) {
+            record_status(&g_wait_status, kWaitAccFree);
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kAccCols;
+        for (int kt = itm.kb; kt < itm.ke; ++kt, ++i) {
+            const int st = (int)(i % S);
+            const uint32_t par = (uint32_t)((i / S) & 1);
+            if (!mbar_wait(&sh.full[st], par)) {
+                record_status(&g_wait_status, kWaitFull);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sh.a[st]);
+            const uint32_t b0 = smem_u32(sh.b[st]);
+#pragma unroll
+            for (int kk = 0; kk < BK / kMmaK; ++kk) {
+                const uint64_t ad = umma_desc_kmajor_sw128(a0 + kk * kMmaK * 4);
+                const uint64_t bd = umma_desc_kmajor_sw128(b0 + kk * kMmaK * 4);
+                mma_tf32_pair(d, ad, bd, idesc, (kt > itm.kb || kk > 0) ? 1u : 0u);
+            }
+            mma_commit_pair_both(&sh.empty[st]);
+        }
+        if (!ok) break;
+        mma_commit_pair_both(&sh.acc_full[buf]);
+    }
+    // Nothing may still be writing either CTA's TMEM when it is freed.
+    mma_commit_pair_local(&sh.mma_done);
     if (!mbar_wait(&sh.mma_done, 0)) record_status(&g_wait_status, kWaitMma);
 }
 
@@ -678,7 +751,14 @@ __device__ __forceinline__ void epilogue(typename TCfg<MN>::Smem& sh, uint32_t t
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.acc_empty[buf]);
+        if (lane == 0) {
+            // On a pair the leader's MMAs write both CTAs' accumulators: the
+            // peer's epilogue warps free theirs on the leader's barrier.
+            if (TCfg<MN>::kPair && (cluster_rank() & 1) != 0)
+                mbar_arrive_remote(&sh.acc_empty[buf], 0);
+            else
+                mbar_arrive(&sh.acc_empty[buf]);
+        }
     }
 }
 
@@ -708,30 +788,49 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sh.acc_full[b], 1);
-            mbar_init(&sh.acc_empty[b], kEpiWarps);
+            mbar_init(&sh.acc_empty[b], kEpiWarps * (C::kPair ? 2 : 1));
         }
         mbar_init(&sh.mma_done, 1);
         mbar_init(&sh.stored, kEpiWarps * 32);
         for (int w = 0; w < kEpiWarps; ++w) mbar_init(&sh.c_old[w], 1);
-        sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
-        fence_mbar_init();
+        if constexpr (C::kPair) {
+            sh.sched.init(p.dp_tiles, p.sk_units, p.nk, blockIdx.x >> 1, gridDim.x >> 1);
+            fence_mbar_init_cluster();
+        } else {
+            sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
+            fence_mbar_init();
+        }
         prefetch_tensormap(&ta);
         prefetch_tensormap(&tb);
         if (p.c_tma) prefetch_tensormap(&tcm);
     }
     if (warp == 1) {
-        tmem_alloc(&sh.tmem_base, kTmemCols);
-        tmem_relinquish();
+        if constexpr (C::kPair) {
+            // One warp of each CTA of the pair: the same columns in both.
+            tmem_alloc_pair(&sh.tmem_base, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&sh.tmem_base, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    // A pair's barriers and TMEM are set up in both CTAs before either uses
+    // the other's.
+    if constexpr (C::kPair) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
     if (warp == 0) {
         if (lane == 0) producer<MN>(sh, &ta, &tb, p);
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer<MN>(sh, tmem, p);
+        if constexpr (C::kPair) {
+            // The leader issues the pair's MMAs; the peer's MMA lane has no work.
+            if (lane == 0 && (cluster_rank() & 1) == 0) mma_issuer_pair<MN>(sh, tmem, p);
+        } else {
+            if (lane == 0) mma_issuer<MN>(sh, tmem, p);
+        }
     } else if (warp < 2 + kEpiWarps) {
         epilogue<MN>(sh, tmem, &tcm, p, warp, lane);
         // Shared memory must outlive the bulk stores that read it.
@@ -742,9 +841,13 @@ tf32_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
 
     tc_fence_before();
     __syncthreads();
+    // Neither CTA of a pair leaves (or frees TMEM) while the other may still
+    // use its shared memory, barriers or TMEM.
+    if constexpr (C::kPair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if constexpr (C::kPair) tmem_dealloc_pair(tmem, kTmemCols);
+        else tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -848,11 +951,13 @@ cudaError_t launch_mn(const Problem& pr, const Plan& plan, cudaStream_t stream) 
     const bool ok_a = a4 || (C::kTA ? make_mn_map(&ta, pr.A, pr.M, pr.K, pr.csA, pr.bsA, pr.batch, a_bc)
                                     : make_kmajor_map(&ta, pr.A, pr.K, pr.M, pr.rsA, pr.bsA, pr.batch, a_bc, BM));
     const bool ok_b = b4 || (C::kTB ? make_mn_map(&tb, pr.B, pr.N, pr.K, pr.rsB, pr.bsB, pr.batch, b_bc)
-                                    : make_kmajor_map(&tb, pr.B, pr.K, pr.N, pr.csB, pr.bsB, pr.batch, b_bc, BN));
+                                    : make_kmajor_map(&tb, pr.B, pr.K, pr.N, pr.csB, pr.bsB, pr.batch, b_bc,
+                                                      C::kBRows));
     if (!ok_a || !ok_b) return cudaErrorInvalidValue;
     Params p;
     p.a_blk4 = a4;
     p.b_blk4 = b4;
+    p.pair = C::kPair ? 1 : 0;
     p.C = pr.C; p.rsC = pr.rsC; p.csC = pr.csC; p.bsC = pr.bsC;
     p.M = pr.M; p.N = pr.N; p.K = pr.K;
     p.tiles_m = plan.tiles_m; p.tiles_n = plan.tiles_n; p.tiles_total = plan.tiles;
@@ -892,6 +997,24 @@ cudaError_t launch_mn(const Problem& pr, const Plan& plan, cudaStream_t stream) 
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
+    if constexpr (C::kPair) {
+        // Clusters of two CTAs, each pair one worker of the tile list.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(C::kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel<MN>, ta, tb, tcm, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     tf32_tc_kernel<MN><<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(ta, tb, tcm, p);
     return cudaGetLastError();
 }
@@ -907,6 +1030,7 @@ cudaError_t launch_tf32_tc(const Problem& pr, const Plan& plan, int sm_count, cu
     if (a_mn && b_mn) return launch_mn<3>(pr, plan, stream);
     if (a_mn) return launch_mn<1>(pr, plan, stream);
     if (b_mn) return launch_mn<2>(pr, plan, stream);
+    if (plan.variant == kPairVariant) return launch_mn<4>(pr, plan, stream);
     return launch_mn<0>(pr, plan, stream);
 }
 
@@ -943,6 +1067,29 @@ void tf32_tc_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_byt
     plan.dp_tiles = dp;
     plan.ctas = ctas;
     plan.workspace = const_cast<void*>(ws);
+}
+
+// Both operands K-major and no split: 256 x 256 tiles on CTA pairs when there
+// are enough of them for a wave of pairs.  Each CTA then reads half of B per
+// slice: a 32 KB stage instead of 48, six stages instead of four, and a
+// third less shared-memory traffic per MMA, which is what holds the one-CTA
+// tile near 0.7 of the tensor rate.
+void tf32_tc_pair(const Problem& pr, Plan& plan, int sm_count) {
+    const bool a_k = pr.K == 1 || pr.csA == 1;
+    const bool b_k = pr.K == 1 || pr.rsB == 1;
+    if (!a_k || !b_k || plan.stream_k) return;
+    const int64_t tm = (pr.M + 2 * BM - 1) / (2 * BM), tn = (pr.N + BN - 1) / BN;
+    const int64_t tiles = tm * tn * pr.batch;
+    const int64_t pairs = sm_count / 2;
+    if (pairs < 1 || tiles < pairs) return;
+    plan.variant = kPairVariant;
+    plan.tiles_m = tm;
+    plan.tiles_n = tn;
+    plan.tiles = tiles;
+    plan.dp_tiles = tiles;
+    plan.ctas = 2 * (tiles < pairs ? tiles : pairs);
+    plan.tile_m = plan.transposed ? BN : 2 * BM;   // reported in C's own orientation
+    plan.tile_n = plan.transposed ? 2 * BM : BN;
 }
 
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream) {

@@ -216,9 +216,10 @@ def test_stream_k_planning():
 
 def test_tf32_stream_k_planning():
     """The tensor-core path splits with independent pieces: the last waves of
-    a many-tile long-K problem, or all tiles of a few-tile long-K one; short K
-    stays data-parallel and k_split = EXACT never splits it.  Its tiles are
-    128 x 256 with 32-wide K slices."""
+    a many-tile long-K problem, or all tiles of a few-tile long-K one.  A
+    split plan keeps one CTA's 128 x 256 tiles with 32-wide K slices; a
+    product of two K-major operands that stays data-parallel (no workspace,
+    short K, k_split = EXACT) runs 256 x 256 tiles on CTA pairs instead."""
     ws = BASE + (8 << 32)
     big = 1 << 30
     M, N = 2048, 5120
@@ -228,17 +229,19 @@ def test_tf32_stream_k_planning():
         C = rowmajor(BASE + (2 << 32), M, N, 1)
         p0 = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32)
         assert p0["path"] == sg.PATH_TMA_TF32 and p0["stream_k"] == sg.STREAM_K_NONE
-        assert (p0["tile_m"], p0["tile_n"], p0["tile_k"]) == (128, 256, 32)
+        assert (p0["tile_m"], p0["tile_n"], p0["tile_k"]) == (256, 256, 32)   # CTA pairs
+        assert p0["tiles"] == 160 and p0["ctas"] == 152
         p1 = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32, workspace=ws, workspace_bytes=big)
-        assert p1["tiles"] == 320 and p1["k_slices"] == K // 32
+        assert p1["k_slices"] == K // 32
         if split:
-            assert p1["stream_k"] == sg.STREAM_K_PIECES
+            assert p1["stream_k"] == sg.STREAM_K_PIECES and p1["tiles"] == 320
+            assert (p1["tile_m"], p1["tile_n"]) == (128, 256)
             assert p1["ctas"] == 152 and p1["dp_tiles"] == 152
         else:
-            assert p1["stream_k"] == sg.STREAM_K_NONE
+            assert p1["stream_k"] == sg.STREAM_K_NONE and p1["tiles"] == 160
         px = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32, workspace=ws, workspace_bytes=big,
                        k_split=sg.KSPLIT_EXACT)
-        assert px["stream_k"] == sg.STREAM_K_NONE
+        assert px["stream_k"] == sg.STREAM_K_NONE and (px["tile_m"], px["tile_n"]) == (256, 256)
     # 32 tiles of 1024 x 1024 with K = 8192: every tile split into pieces.
     M = N = 1024
     K = 8192
@@ -362,3 +365,21 @@ def test_attention_ex_option_checks():
         with pytest.raises(sg.SbgemmError) as e:
             sg.sbgemm_attention_ex(*args, math=math, force_path=force)
         assert e.value.status == want, (math, force, e.value.status)
+
+
+def test_tf32_pair_tiles_need_a_wave_of_pairs():
+    """Two K-major operands run on CTA pairs only when the 256 x 256 tiles fill
+    at least one wave of pairs (76 on 152 SMs); fewer stay on one CTA's
+    128 x 256 tiles, and an MN-major operand never takes pairs."""
+    K = 1024
+    for M, N, pair in ((2048, 2304, False), (2560, 2048, True)):   # 72 and 80 pair tiles
+        A = rowmajor(BASE, M, K, 1)
+        B = (BASE + (1 << 32), 1, K, 0)
+        C = rowmajor(BASE + (2 << 32), M, N, 1)
+        p = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32)
+        assert (p["tile_m"], p["tile_n"]) == ((256, 256) if pair else (128, 256)), p
+    M, N = 4096, 4096
+    A_m = (BASE, 1, M, 0)
+    B = (BASE + (1 << 32), 1, K, 0)
+    p = call_plan(A_m, B, rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1, math=sg.MATH_TF32)
+    assert (p["tile_m"], p["tile_n"]) == (128, 256), p
