@@ -1069,8 +1069,8 @@ void tf32_tc_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_byt
     plan.workspace = const_cast<void*>(ws);
 }
 
-// Both operands K-major and no split: 256 x 256 tiles on CTA pairs when there
-// are enough of them for a wave of pairs.  Each CTA then reads half of B per
+// Both operands K-major, no split and at least 8 K slices: 256 x 256 tiles on
+// CTA pairs when there are enough of them for a wave of pairs.  Each CTA then reads half of B per
 // slice: a 32 KB stage instead of 48, six stages instead of four, and a
 // third less shared-memory traffic per MMA, which is what holds the one-CTA
 // tile near 0.7 of the tensor rate.
@@ -1078,6 +1078,10 @@ void tf32_tc_pair(const Problem& pr, Plan& plan, int sm_count) {
     const bool a_k = pr.K == 1 || pr.csA == 1;
     const bool b_k = pr.K == 1 || pr.rsB == 1;
     if (!a_k || !b_k || plan.stream_k) return;
+    // Short K (c3's 64: two slices) is bound by the C stores, and a pair's two
+    // epilogues, which both must drain an accumulator before either is
+    // reused, measured slower there (41 against 35 us back to back).
+    if ((pr.K + BK - 1) / BK < 8) return;
     const int64_t tm = (pr.M + 2 * BM - 1) / (2 * BM), tn = (pr.N + BN - 1) / BN;
     const int64_t tiles = tm * tn * pr.batch;
     const int64_t pairs = sm_count / 2;

@@ -369,8 +369,9 @@ def test_attention_ex_option_checks():
 
 def test_tf32_pair_tiles_need_a_wave_of_pairs():
     """Two K-major operands run on CTA pairs only when the 256 x 256 tiles fill
-    at least one wave of pairs (76 on 152 SMs); fewer stay on one CTA's
-    128 x 256 tiles, and an MN-major operand never takes pairs."""
+    at least one wave of pairs (76 on 152 SMs) and K has at least 8 slices;
+    otherwise they stay on one CTA's 128 x 256 tiles, and an MN-major operand
+    never takes pairs."""
     K = 1024
     for M, N, pair in ((2048, 2304, False), (2560, 2048, True)):   # 72 and 80 pair tiles
         A = rowmajor(BASE, M, K, 1)
@@ -382,4 +383,9 @@ def test_tf32_pair_tiles_need_a_wave_of_pairs():
     A_m = (BASE, 1, M, 0)
     B = (BASE + (1 << 32), 1, K, 0)
     p = call_plan(A_m, B, rowmajor(BASE + (2 << 32), M, N, 1), M, N, K, 1, math=sg.MATH_TF32)
+    assert (p["tile_m"], p["tile_n"]) == (128, 256), p
+    # Short K (under 8 slices of 32) stays on one CTA: the C stores set the pace.
+    Ks = 128
+    p = call_plan(rowmajor(BASE, M, Ks, 1), (BASE + (1 << 32), 1, Ks, 0), rowmajor(BASE + (2 << 32), M, N, 1),
+                  M, N, Ks, 1, math=sg.MATH_TF32)
     assert (p["tile_m"], p["tile_n"]) == (128, 256), p
