@@ -170,8 +170,10 @@ cudaError_t launch_tf32_tc(const Problem& p, const Plan& plan, int sm_count, cud
 // Fills plan.ctas / stream_k / dp_tiles / k_slices for the TF32 kernel.
 void tf32_tc_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
                       int k_split);
-// Switches a data-parallel plan of two K-major operands to CTA-pair tiles.
-void tf32_tc_pair(const Problem& pr, Plan& plan, int sm_count);
+// Switches a plan of two K-major operands to CTA-pair tiles where they apply
+// (with their own split over the workspace); false leaves the plan as it was.
+bool tf32_tc_pair(const Problem& pr, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
+                  int k_split);
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream);
 
 // ---- status words of the kernels without bounded waits (debug bounds checks) ----

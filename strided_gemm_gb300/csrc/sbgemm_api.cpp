@@ -282,7 +282,7 @@ int make_plan(const Problem& p, const sbgemm_options& o, int sm_count, bool empt
         plan->tiles = plan->tiles_m * plan->tiles_n * q.batch;
         tf32_tc_schedule(q, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace,
                          o.k_split);
-        tf32_tc_pair(q, *plan, sm_count);
+        tf32_tc_pair(q, *plan, sm_count, o.workspace ? o.workspace_bytes : 0, o.workspace, o.k_split);
         return SBGEMM_OK;
     }
 

@@ -473,11 +473,25 @@ __device__ __forceinline__ float4* partial_piece(float4* slot, int c, int row) {
     return slot + (c * 8) * kBM128 + row;
 }
 
-// Waits (bounded) until CTAs first..blockIdx.x-1 have published their pieces
+// The split schedule's workers: CTAs, or on a pair clusters of two CTAs, each
+// CTA of which parks and collects its own 128 rows of a tile's partial sums.
+__device__ __forceinline__ int64_t worker(const Params& p) {
+    return p.pair ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+}
+__device__ __forceinline__ int64_t n_workers(const Params& p) {
+    return p.pair ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+}
+// The CTA of worker w that holds the same rows as this CTA.
+__device__ __forceinline__ int64_t worker_cta(const Params& p, int64_t w) {
+    return p.pair ? 2 * w + (int64_t)(blockIdx.x & 1) : w;
+}
+
+// Waits (bounded) until workers first..worker-1 have published their pieces
 // of this tile; one lane spins, then every lane takes its own acquire.  False
 // on timeout.
 __device__ __forceinline__ bool wait_pieces(const Params& p, int64_t first, int lane) {
-    for (int64_t c = first; c < (int64_t)blockIdx.x; ++c) {
+    for (int64_t w = first; w < worker(p); ++w) {
+        const int64_t c = worker_cta(p, w);
         int up = 1;
         if (lane == 0) up = wait_flag(p.ws_flag + c) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, up, 0)) return false;
@@ -497,14 +511,14 @@ __device__ __forceinline__ void load_piece_chunk(float (&x)[32], const Params& p
     }
 }
 
-// Adds the partial sums of pieces from CTAs `from` down to `first` of one
-// 32-column chunk of this thread's row (latest CTA first: a fixed order).
+// Adds the partial sums of pieces from workers `from` down to `first` of one
+// 32-column chunk of this thread's row (latest first: a fixed order).
 __device__ __forceinline__ void add_pieces(float (&v)[32], const Params& p, int64_t first, int64_t from,
                                            int chunk, int row) {
 #pragma unroll 1
-    for (int64_t c = from; c >= first; --c) {
+    for (int64_t w = from; w >= first; --w) {
         float x[32];
-        load_piece_chunk(x, p, c, chunk, row);
+        load_piece_chunk(x, p, worker_cta(p, w), chunk, row);
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] += x[e];
     }
@@ -554,7 +568,7 @@ __device__ __forceinline__ bool store_tile_tma(SmemT& sh, const CUtensorMap* cma
         tmem_ld32(taddr + c * 32, v);      // whole warp, converged: row m, columns n0..n0+31
         if (!piece_in) continue;
         // A tail adds the earlier pieces' partial sums before alpha.
-        if (first_piece >= 0) add_pieces(v, p, first_piece, (int64_t)blockIdx.x - 1, c, row);
+        if (first_piece >= 0) add_pieces(v, p, first_piece, worker(p) - 1, c, row);
         if (p.accumulate) {
             if (!mbar_wait(&sh.c_old[ew], c_loads & 1u)) return false;
             ++c_loads;
@@ -664,7 +678,7 @@ __device__ __forceinline__ void epilogue(typename TCfg<MN>::Smem& sh, uint32_t t
         // long before this point.
         int64_t first_piece = -1;
         if (itm.mode == kTail) {
-            first_piece = unit_owner((itm.tile - p.dp_tiles) * p.nk, p.sk_units, gridDim.x);
+            first_piece = unit_owner((itm.tile - p.dp_tiles) * p.nk, p.sk_units, n_workers(p));
             if (!wait_pieces(p, first_piece, lane)) {
                 record_status(&g_wait_status, kWaitPartial);
                 return;
@@ -722,7 +736,7 @@ __device__ __forceinline__ void epilogue(typename TCfg<MN>::Smem& sh, uint32_t t
                 tmem_ld32(taddr + c * 32, v);      // whole warp, converged, every row
                 const int64_t n0 = tc.n0 + c * 32;
                 if (!row_ok || n0 >= p.N) continue;
-                if (first_piece >= 0) add_pieces(v, p, first_piece, (int64_t)blockIdx.x - 1, c, row);
+                if (first_piece >= 0) add_pieces(v, p, first_piece, worker(p) - 1, c, row);
                 // C_old of the whole piece is loaded before any store, so the 32
                 // loads are in flight together (the compiler cannot move a load
                 // of C above a store to C).
@@ -980,30 +994,75 @@ cudaError_t launch_mn(const Problem& pr, const Plan& plan, cudaStream_t stream) 
         p.ws_partial = static_cast<float4*>(plan.workspace);
         p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<char*>(plan.workspace) +
                                                     (size_t)grid * kSlotFloat4 * sizeof(float4));
-        cudaError_t e = cudaMemsetAsync(p.ws_flag, 0, (size_t)grid * sizeof(unsigned int), stream);
+        const cudaError_t e = cudaMemsetAsync(p.ws_flag, 0, (size_t)grid * sizeof(unsigned int), stream);
         if (e != cudaSuccess) return e;
-        // CTAs wait on one another's partial sums: make them co-resident.
+    }
+    if (plan.stream_k || C::kPair) {
+        // A split's CTAs wait on one another's partial sums: a cooperative
+        // launch makes them co-resident.  A pair kernel runs in clusters of
+        // two CTAs, each pair one worker; where the driver takes no
+        // cooperative launch of clusters, the planner's bound on the pairs
+        // (the clusters that fit the device at once) stands in for it.
+        static std::atomic<int> coop_clusters{1};
+        const bool coop = plan.stream_k && (!C::kPair || coop_clusters.load() != 0);
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3(C::kThreads);
         cfg.dynamicSmemBytes = C::kSmemBytes;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
+        cudaLaunchAttribute attr[2];
+        int na = 0;
+        if (coop) {
+            attr[na].id = cudaLaunchAttributeCooperative;
+            attr[na].val.cooperative = 1;
+            ++na;
+        }
+        if (C::kPair) {
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = 2;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = 1;
+            ++na;
+        }
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel<MN>, ta, tb, tcm, p);
+        cfg.numAttrs = na;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel<MN>, ta, tb, tcm, p);
+        if (e != cudaSuccess && coop && C::kPair) {
+            (void)cudaGetLastError();
+            coop_clusters.store(0);
+            cfg.attrs = attr + 1;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel<MN>, ta, tb, tcm, p);
+        }
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    if constexpr (C::kPair) {
-        // Clusters of two CTAs, each pair one worker of the tile list.
+    tf32_tc_kernel<MN><<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(ta, tb, tcm, p);
+    return cudaGetLastError();
+}
+
+// Clusters of two CTAs of the pair kernel the device holds at once (one CTA
+// per SM), asked of the driver once per device; 0 if it does not say.
+template <int MN>
+int pair_clusters_fit(int sm_count) {
+    using C = TCfg<MN>;
+    static std::atomic<int> fit[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    std::atomic<int>& slot = fit[dev & 63];
+    const int known = slot.load();
+    if (known != 0) return known > 0 ? known : 0;
+    int n = 0;
+    cudaError_t e = cudaFuncSetAttribute(tf32_tc_kernel<MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmemBytes);
+    if (e == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
+        cfg.gridDim = dim3((unsigned)(sm_count / 2 * 2));
         cfg.blockDim = dim3(C::kThreads);
         cfg.dynamicSmemBytes = C::kSmemBytes;
-        cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -1011,12 +1070,14 @@ cudaError_t launch_mn(const Problem& pr, const Plan& plan, cudaStream_t stream) 
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, tf32_tc_kernel<MN>, ta, tb, tcm, p);
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
+        e = cudaOccupancyMaxActiveClusters(&n, tf32_tc_kernel<MN>, &cfg);
     }
-    tf32_tc_kernel<MN><<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(ta, tb, tcm, p);
-    return cudaGetLastError();
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    slot.store(n > 0 ? n : -1);
+    return n > 0 ? n : 0;
 }
 
 }  // namespace
@@ -1069,31 +1130,54 @@ void tf32_tc_schedule(const Problem& pr, Plan& plan, int sm_count, size_t ws_byt
     plan.workspace = const_cast<void*>(ws);
 }
 
-// Both operands K-major, no split and at least 8 K slices: 256 x 256 tiles on
-// CTA pairs when there are enough of them for a wave of pairs.  Each CTA then reads half of B per
-// slice: a 32 KB stage instead of 48, six stages instead of four, and a
-// third less shared-memory traffic per MMA, which is what holds the one-CTA
-// tile near 0.7 of the tensor rate.
-void tf32_tc_pair(const Problem& pr, Plan& plan, int sm_count) {
+// Both operands K-major, at least 8 K slices, and 256 x 256 tiles enough
+// for a wave of pairs: the tiles go to CTA pairs.  Each CTA then reads
+// half of B per slice: a 32 KB stage instead of 48, six stages instead of
+// four, and a third less shared-memory traffic per MMA, which is what holds
+// the one-CTA tile near 0.7 of the tensor rate.  With a workspace the last
+// waves are split into independent K pieces as on one CTA, each pair one
+// worker.  Returns false (nothing changed) when pairs do not apply.
+bool tf32_tc_pair(const Problem& pr, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
+                  int k_split) {
+    // An MN-major A on pairs (each CTA transposing its 128 rows, the peer's
+    // transposers signalling the leader by 16-byte bulk copies) measured 3-7%
+    // slower than one CTA's tiles, split or not (c5c 235 against 227 us).
     const bool a_k = pr.K == 1 || pr.csA == 1;
     const bool b_k = pr.K == 1 || pr.rsB == 1;
-    if (!a_k || !b_k || plan.stream_k) return;
+    if (!a_k || !b_k) return false;
+    const int64_t nk = (pr.K + BK - 1) / BK;
     // Short K (c3's 64: two slices) is bound by the C stores, and a pair's two
     // epilogues, which both must drain an accumulator before either is
     // reused, measured slower there (41 against 35 us back to back).
-    if ((pr.K + BK - 1) / BK < 8) return;
+    if (nk < 8) return false;
     const int64_t tm = (pr.M + 2 * BM - 1) / (2 * BM), tn = (pr.N + BN - 1) / BN;
     const int64_t tiles = tm * tn * pr.batch;
-    const int64_t pairs = sm_count / 2;
-    if (pairs < 1 || tiles < pairs) return;
+    int64_t pairs = sm_count / 2;
+    const int fit = pair_clusters_fit<4>(sm_count);
+    if (fit > 0 && fit < pairs) pairs = fit;
+    if (pairs < 1 || tiles < pairs) return false;
     plan.variant = kPairVariant;
     plan.tiles_m = tm;
     plan.tiles_n = tn;
     plan.tiles = tiles;
-    plan.dp_tiles = tiles;
-    plan.ctas = 2 * (tiles < pairs ? tiles : pairs);
+    plan.k_slices = (int)nk;
     plan.tile_m = plan.transposed ? BN : 2 * BM;   // reported in C's own orientation
     plan.tile_n = plan.transposed ? 2 * BM : BN;
+    plan.stream_k = false;
+    plan.split_indep = false;
+    plan.dp_tiles = tiles;
+    plan.ctas = 2 * pairs;
+    const size_t need = (size_t)(2 * pairs) * (size_t)kSlotFloat4 * sizeof(float4) +
+                        (size_t)(2 * pairs) * sizeof(unsigned int);
+    if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 256) != 0) return true;
+    if (k_split != SBGEMM_KSPLIT_ANY) return true;
+    const int64_t dp = stream_k_dp_tiles(tiles, nk, pairs, 48);
+    if (dp < 0) return true;
+    plan.stream_k = true;
+    plan.split_indep = true;
+    plan.dp_tiles = dp;
+    plan.workspace = const_cast<void*>(ws);
+    return true;
 }
 
 unsigned int read_and_clear_wait_status_tf32(cudaStream_t stream) {

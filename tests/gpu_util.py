@@ -80,8 +80,10 @@ def sample_points(case, n=1500, seed=0):
     return np.concatenate([np.array(pts, dtype=np.int64), r.astype(np.int64)])
 
 
-def check_points(case, got_storage, tol=TOL_FFMA, exact=False, n=1500):
-    idx = sample_points(case, n)
+def check_points(case, got_storage, tol=TOL_FFMA, exact=False, n=1500, points=None):
+    """Compares sampled elements (or the given (b, m, n) points) with the
+    oracle, one by one."""
+    idx = sample_points(case, n) if points is None else np.asarray(points, dtype=np.int64)
     ref, bound = oracle.case_points(case, idx)
     c = case.C
     got = c_storage_at(case, got_storage, idx)

@@ -216,10 +216,10 @@ def test_stream_k_planning():
 
 def test_tf32_stream_k_planning():
     """The tensor-core path splits with independent pieces: the last waves of
-    a many-tile long-K problem, or all tiles of a few-tile long-K one.  A
-    split plan keeps one CTA's 128 x 256 tiles with 32-wide K slices; a
-    product of two K-major operands that stays data-parallel (no workspace,
-    short K, k_split = EXACT) runs 256 x 256 tiles on CTA pairs instead."""
+    a many-tile long-K problem, or all tiles of a few-tile long-K one.  Two
+    K-major operands with a wave of 256 x 256 tiles run on CTA pairs, split or
+    not (each pair one worker of the split); fewer tiles keep one CTA's
+    128 x 256 tiles with 32-wide K slices."""
     ws = BASE + (8 << 32)
     big = 1 << 30
     M, N = 2048, 5120
@@ -233,10 +233,11 @@ def test_tf32_stream_k_planning():
         assert p0["tiles"] == 160 and p0["ctas"] == 152
         p1 = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32, workspace=ws, workspace_bytes=big)
         assert p1["k_slices"] == K // 32
+        assert (p1["tile_m"], p1["tile_n"]) == (256, 256) and p1["ctas"] == 152
         if split:
-            assert p1["stream_k"] == sg.STREAM_K_PIECES and p1["tiles"] == 320
-            assert (p1["tile_m"], p1["tile_n"]) == (128, 256)
-            assert p1["ctas"] == 152 and p1["dp_tiles"] == 152
+            # 160 pair tiles on 76 pairs: one data-parallel wave, the rest split.
+            assert p1["stream_k"] == sg.STREAM_K_PIECES and p1["tiles"] == 160
+            assert p1["dp_tiles"] == 76
         else:
             assert p1["stream_k"] == sg.STREAM_K_NONE and p1["tiles"] == 160
         px = call_plan(A, B, C, M, N, K, 1, math=sg.MATH_TF32, workspace=ws, workspace_bytes=big,

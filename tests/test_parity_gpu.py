@@ -503,6 +503,38 @@ def test_tf32_split_pieces_parity_and_determinism(torch, workspace, shape):
     assert st == sg.SBGEMM_OK, where
 
 
+TF32_PAIR_SPLIT_SHAPES = [
+    # (name, M, N, K, A layout, tile): B column-major (K-major), ragged M, N
+    # and K edges, every tile split into K pieces: two K-major operands on
+    # 100 tiles of 256 x 256 (CTA pairs), an M-major A on one CTA's tiles
+    ("k_major_pairs", 2500, 2470, 4100, "row16", (256, 256)),
+    ("a_m_major", 2500, 2470, 4100, "col16", (128, 256)),
+]
+
+
+@pytest.mark.parametrize("shape", TF32_PAIR_SPLIT_SHAPES, ids=[s[0] for s in TF32_PAIR_SPLIT_SHAPES])
+def test_tf32_pair_split_parity(torch, workspace, shape):
+    """Tiles whose K slices are split into pieces (on CTA pairs each pair is
+    one worker, and each CTA of a pair parks and collects its own rows):
+    within the TF32 bound at sampled points and along the ragged last rows
+    and columns, identical from run to run; integers exact."""
+    _, M, N, K, la, tile = shape
+    rng = np.random.default_rng(M + 7 * N + K)
+    kw = dict(math=sg.MATH_TF32, force_path=sg.PATH_TMA_TF32)
+    for values in ("real", "int"):
+        case = wl.random_strided(rng, M, N, K, 1, la, "col16", values=values, accumulate=1, alpha=0.75)
+        first, plan = _run_ws(case, torch, workspace, kw)
+        assert plan["stream_k"] == sg.STREAM_K_PIECES and (plan["tile_m"], plan["tile_n"]) == tile, plan
+        gu.check_points(case, first, n=4000, tol=gu.TOL_TF32, exact=(values == "int"))
+        edge = [(0, m, n) for m in range(M - 200, M) for n in range(N - 3, N)] + \
+               [(0, m, n) for m in range(0, M, 97) for n in range(N - 200, N, 7)]
+        gu.check_points(case, first, points=edge, tol=gu.TOL_TF32, exact=(values == "int"))
+        again, _ = _run_ws(case, torch, workspace, kw)
+        assert np.array_equal(first, again)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
 def test_tf32_stream_k_integer_exact(torch, workspace):
     """Small integers are exact in TF32, so the split schedule must give the
     exact product; repeated calls reuse the workspace flags."""
