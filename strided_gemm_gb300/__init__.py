@@ -99,6 +99,10 @@ class _PlanInfo(ctypes.Structure):
 
 _lock = threading.Lock()
 _lib = None
+# The fast-call module (csrc/fastcall.c), bound to the loaded library's
+# sbgemm_ex and sbgemm: the same calls with cheaper argument conversion.
+# None where it was not built; the ctypes calls below then serve.
+_fast = None
 _i64, _vp = ctypes.c_int64, ctypes.c_void_p
 _ARGS = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _i64,
          _i64, _i64, _i64, _i64]
@@ -155,6 +159,14 @@ def load(path: str = LIB_PATH):
         lib.sbgemm_status_string.argtypes = [ctypes.c_int]
         lib.sbgemm_version.restype = ctypes.c_int
         lib.sbgemm_version.argtypes = []
+        global _fast
+        try:
+            from . import _fastcall
+            _fastcall.bind(ctypes.cast(lib.sbgemm_ex, ctypes.c_void_p).value,
+                           ctypes.cast(lib.sbgemm, ctypes.c_void_p).value)
+            _fast = _fastcall
+        except ImportError:
+            _fast = None
         _lib = lib
         return lib
 
@@ -181,8 +193,8 @@ def _opts_ref(math, force_path, workspace, workspace_bytes, k_split):
         o = _opts(math, force_path, workspace, workspace_bytes, k_split)
         if len(_opts_cache) >= 256:
             _opts_cache.clear()
-        r = _opts_cache[key] = (o, ctypes.byref(o))
-    return r[1]
+        r = _opts_cache[key] = (o, ctypes.byref(o), ctypes.addressof(o))
+    return r
 
 
 def sbgemm_workspace_bytes(device: int = 0) -> int:
@@ -205,8 +217,12 @@ def sbgemm_version() -> int:
 def sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
            M, N, K, batch, alpha, accumulate, stream=0) -> None:
     lib = _lib if _lib is not None else load()
-    st = lib.sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
-                    M, N, K, batch, alpha, 1 if accumulate else 0, stream or None)
+    if _fast is not None:
+        st = _fast.sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                          M, N, K, batch, alpha, 1 if accumulate else 0, stream or 0)
+    else:
+        st = lib.sbgemm(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                        M, N, K, batch, alpha, 1 if accumulate else 0, stream or None)
     if st:
         raise SbgemmError(st, "sbgemm")
 
@@ -230,9 +246,13 @@ def sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
               math: int = MATH_FP32, force_path: int = PATH_AUTO,
               workspace: int = 0, workspace_bytes: int = 0, k_split: int = KSPLIT_ANY) -> None:
     lib = _lib if _lib is not None else load()
-    st = lib.sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
-                       M, N, K, batch, alpha, 1 if accumulate else 0, stream or None,
-                       _opts_ref(math, force_path, workspace, workspace_bytes, k_split))
+    o = _opts_ref(math, force_path, workspace, workspace_bytes, k_split)
+    if _fast is not None:
+        st = _fast.sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                             M, N, K, batch, alpha, 1 if accumulate else 0, stream or 0, o[2])
+    else:
+        st = lib.sbgemm_ex(A, rsA, csA, bsA, B, rsB, csB, bsB, C, rsC, csC, bsC,
+                           M, N, K, batch, alpha, 1 if accumulate else 0, stream or None, o[1])
     if st:
         raise SbgemmError(st, "sbgemm_ex")
 

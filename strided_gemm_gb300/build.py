@@ -8,6 +8,10 @@ build(debug=True) makes libsbgemm_debug.so instead: the same sources with
 SBGEMM_DEBUG defined, so that every kernel checks the global addresses it
 loads and stores against the operand spans the host validated (a violation
 is reported by sbgemm_device_status and the access skipped).
+
+build() also compiles the binding's fast-call module (csrc/fastcall.c, with
+the host C compiler against Python's headers) when those headers are
+present; without it the binding calls the library through ctypes alone.
 """
 
 from __future__ import annotations
@@ -15,8 +19,10 @@ from __future__ import annotations
 import glob
 import hashlib
 import os
+import shutil
 import subprocess
 import sys
+import sysconfig
 import tempfile
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +37,11 @@ DEBUG_STAMP = os.path.join(HERE, ".libsbgemm_debug.stamp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
           "-I", INCLUDE, "-I", CSRC]
+
+
+FASTCALL_SRC = os.path.join(CSRC, "fastcall.c")
+FASTCALL_PATH = os.path.join(HERE, "_fastcall" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+FASTCALL_STAMP = os.path.join(HERE, ".fastcall.stamp")
 
 
 def nvcc() -> str:
@@ -55,7 +66,37 @@ def _digest(srcs, deps, extra) -> str:
     return h.hexdigest()
 
 
+def build_fastcall(force: bool = False) -> str | None:
+    """Compiles the fast-call module next to the library; None when Python's
+    headers or a C compiler are missing (the binding then uses ctypes)."""
+    inc = sysconfig.get_paths().get("include") or ""
+    cc = os.environ.get("CC") or shutil.which("gcc") or shutil.which("cc")
+    if not cc or not os.path.exists(os.path.join(inc, "Python.h")):
+        return None
+    h = hashlib.sha256()
+    for f in (FASTCALL_SRC, os.path.join(INCLUDE, "sbgemm.h")):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update((cc + inc + FASTCALL_PATH).encode())
+    digest = h.hexdigest()
+    if not force and os.path.exists(FASTCALL_PATH) and os.path.exists(FASTCALL_STAMP):
+        with open(FASTCALL_STAMP) as fh:
+            if fh.read().strip() == digest:
+                return FASTCALL_PATH
+    tmp = FASTCALL_PATH + f".tmp{os.getpid()}"
+    cmd = [cc, "-O2", "-shared", "-fPIC", "-fvisibility=hidden", "-I", inc, "-I", INCLUDE,
+           FASTCALL_SRC, "-o", tmp]
+    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"the fast-call module failed to compile:\n{r.stdout}")
+    os.replace(tmp, FASTCALL_PATH)
+    with open(FASTCALL_STAMP, "w") as fh:
+        fh.write(digest + "\n")
+    return FASTCALL_PATH
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    build_fastcall(force)
     extra = list(extra_flags or []) + (["-DSBGEMM_DEBUG"] if debug else [])
     lib_path, stamp = (DEBUG_LIB_PATH, DEBUG_STAMP) if debug else (LIB_PATH, STAMP)
     srcs, deps = _sources()

@@ -315,6 +315,50 @@ gather_ffma_kernel(const Problem p, const int64_t tiles_m, const int64_t tiles_n
 #undef ACC
 }
 
+// Products of a few thousand outputs with short K (a 64 x 48 x 32 layer):
+// one 64 x 64 tile leaves each of its 256 threads 16 outputs' chains, run by
+// 2 warps per scheduler with nothing to hide their latencies (about 10k
+// cycles for such a product).  Here each thread computes one output straight
+// from global memory (the L1 serves the reuse), so the work spreads over
+// many SMs and each thread's chain is one dot product.  A warp covers 32
+// consecutive columns of a row, a CTA 8 rows.  The loads of 32 k steps go
+// out together before their FMAs; k runs in increasing order in one fmaf
+// chain from +0, as in the tiled kernel, so the two agree to the bit.
+constexpr int kDirectRows = kThreads / 32, kDirectCols = 32, kDirectChunk = 32;
+
+__global__ void __launch_bounds__(kThreads)
+gather_direct_kernel(const Problem p, const int64_t tiles_n) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t tile = blockIdx.x;
+    const uint32_t tm = tile / (uint32_t)tiles_n, tn = tile - tm * (uint32_t)tiles_n;
+    const int64_t m = (int64_t)tm * kDirectRows + w, n = (int64_t)tn * kDirectCols + lane;
+    if (m >= p.M || n >= p.N) return;   // no barrier below
+    for (int64_t b = blockIdx.y; b < p.batch; b += gridDim.y) {
+        const float* __restrict__ arow = p.A + b * p.bsA + m * p.rsA;
+        const float* __restrict__ bcol = p.B + b * p.bsB + n * p.csB;
+        float acc = 0.0f;
+        for (int64_t k0 = 0; k0 < p.K; k0 += kDirectChunk) {
+            float av[kDirectChunk], bv[kDirectChunk];
+#pragma unroll
+            for (int k = 0; k < kDirectChunk; ++k) {
+                const bool in = k0 + k < p.K;
+                const float* pa = arow + (k0 + k) * p.csA;
+                const float* pb = bcol + (k0 + k) * p.rsB;
+                av[k] = (in && dbg_in_span(p.A, pa, p.sa, &g_status)) ? __ldg(pa) : 0.0f;
+                bv[k] = (in && dbg_in_span(p.B, pb, p.sb, &g_status)) ? __ldg(pb) : 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < kDirectChunk; ++k)
+                if (k0 + k < p.K) acc = fmaf(av[k], bv[k], acc);
+        }
+        float* c = p.C + b * p.bsC + m * p.rsC + n * p.csC;
+        if (!dbg_in_span(p.C, c, p.sc, &g_status)) continue;
+        float v = p.accumulate ? fmaf(p.alpha, acc, *c) : p.alpha * acc;
+        if (p.epi.on) v = finish(p.epi, v, b, m, n, &g_status);
+        *c = v;
+    }
+}
+
 // Bytes of the partial sums of `tiles` tiles cut into `pieces`, rounded up to
 // 256 so that the counters after them stay aligned.
 size_t split_part_bytes(int64_t tiles, int pieces, int tile_elems) {
@@ -371,7 +415,12 @@ constexpr GatherConfig kConfigs[] = {
     {128, 128, 16, kThreads, 2},   // 8 x 8 micro-tiles
     {64, 64, 16, kThreads, 2},     // 4 x 4 micro-tiles, for small problems
     {128, 64, 16, kThreads, 2},    // 8 x 4 micro-tiles, for narrow or ragged N
+    {kDirectRows, kDirectCols, kDirectChunk, kThreads, 8},   // one output per thread
 };
+constexpr int kDirectVariant = 3;
+// The direct kernel serves products of at most this many outputs (over the
+// batch) and this K.
+constexpr int64_t kDirectMaxOutputs = 16384, kDirectMaxK = 128;
 
 }  // namespace
 
@@ -380,6 +429,10 @@ int gather_config_count() { return (int)(sizeof(kConfigs) / sizeof(kConfigs[0]))
 GatherConfig gather_config(int variant) { return kConfigs[variant]; }
 
 int gather_pick_variant(const Problem& p, int sm_count) {
+    // Tiny products: one output per thread (gather_direct_kernel).
+    if (p.K <= kDirectMaxK && p.M <= kDirectMaxOutputs && p.N <= kDirectMaxOutputs &&
+        p.batch <= kDirectMaxOutputs && p.M * p.N * p.batch <= kDirectMaxOutputs)
+        return kDirectVariant;
     // The tile shape with the smallest estimated time: waves of CTAs (two
     // per SM) times the tile's work, the smaller tiles charged 4/3 (64 x 64)
     // and 7/6 (128 x 64) for their lower arithmetic per load.  Large tiles
@@ -431,6 +484,11 @@ cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t 
             if (plan.k_pieces > 1) return launch_variant<64, 64, 16, 4, 4, true>(p, plan, stream);
             return launch_variant<64, 64, 16, 4, 4, false>(p, plan, stream);
         case 2: return launch_variant<128, 64, 16, 8, 4, false>(p, plan, stream);
+        case kDirectVariant: {
+            dim3 grid((unsigned)(plan.tiles_m * plan.tiles_n), (unsigned)(p.batch < 65535 ? p.batch : 65535));
+            gather_direct_kernel<<<grid, kThreads, 0, stream>>>(p, plan.tiles_n);
+            return cudaGetLastError();
+        }
         default: return cudaErrorInvalidValue;
     }
 }

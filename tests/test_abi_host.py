@@ -144,6 +144,43 @@ def test_validation_errors():
     assert code(A, B, C, 8, 8, 8, 1, force_path=9) == sg.SBGEMM_ERR_INVALID_VALUE
 
 
+def test_fastcall_statuses_match_ctypes():
+    """The fast-call module converts the arguments itself and calls the same
+    sbgemm_ex / sbgemm: on calls the host checks settle (no device is
+    touched) it returns the same status as the ctypes call, takes objects
+    with __index__ for sizes, and refuses a wrong argument count."""
+    if sg._fast is None:
+        pytest.skip("the fast-call module is not built (no Python headers)")
+    import numpy as np
+    lib = sg.load()
+    A = rowmajor(BASE, 8, 8, 1)
+    B = rowmajor(BASE + (1 << 32), 8, 8, 1)
+    C = rowmajor(BASE + (2 << 32), 8, 8, 1)
+    cases = [(A, B, C, -1, 8, 8, 1), (A, B, C, 8, 8, 8, -2), (A, B, (0, 8, 1, 64), 8, 8, 8, 1),
+             ((BASE + 2, 8, 1, 64), B, C, 8, 8, 8, 1), (A, B, (C[0], 8, 1, 0), 8, 8, 8, 2),
+             (A, B, (BASE + 4 * 32, 8, 1, 64), 8, 8, 8, 1), ((BASE, 1 << 62, 1, 0), B, C, 8, 8, 8, 1),
+             (A, B, C, 0, 8, 8, 1), (A, B, C, 8, 8, 8, 0)]
+    bad_opts = sg._opts_ref(7, sg.PATH_AUTO, 0, 0, sg.KSPLIT_ANY)
+    ok_opts = sg._opts_ref(sg.MATH_FP32, sg.PATH_AUTO, 0, 0, sg.KSPLIT_ANY)
+    for a, b, c, M, N, K, batch in cases:
+        args = (*a, *b, *c, M, N, K, batch, 0.5, 1)
+        for o in (ok_opts, bad_opts):
+            want = lib.sbgemm_ex(*args, None, o[1])
+            assert sg._fast.sbgemm_ex(*args, 0, o[2]) == want, (args, want)
+        want = lib.sbgemm(*args, None)
+        assert sg._fast.sbgemm(*args, None) == want
+        if want:
+            with pytest.raises(sg.SbgemmError) as e:
+                sg.sbgemm_ex(*args)
+            assert e.value.status == want
+    sizes = tuple(np.int64(v) for v in (8, 8, 8, 1))
+    assert sg._fast.sbgemm_ex(*A, *B, *C, -1, *sizes[1:], 1.0, 0, 0, 0) == sg.SBGEMM_ERR_INVALID_VALUE
+    with pytest.raises(TypeError):
+        sg._fast.sbgemm_ex(*A, *B, *C, 8, 8, 8, 1, 1.0, 0, 0)
+    with pytest.raises(TypeError):
+        sg._fast.sbgemm(*A, *B, *C, "8", 8, 8, 1, 1.0, 0, 0)
+
+
 def test_injective_layouts_accepted():
     A = rowmajor(BASE, 8, 8, 1)
     B = rowmajor(BASE + (1 << 32), 8, 8, 1)

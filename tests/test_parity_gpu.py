@@ -5,6 +5,8 @@ Tolerances follow the strided-batched problem statement: every element within
 on the tf32 path; integer-valued inputs must match bit for bit.
 """
 
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -91,6 +93,45 @@ def test_awkward_shapes_all_layouts(torch, mkn, layouts):
                     continue
                 got = gu.run_case(case, torch, force_path=path)
                 gu.check_full(case, got, exact=(values == "int"))
+
+
+TINY = [(17, 9, 33), (5, 31, 129), (1, 1, 1), (4, 4, 4), (5, 9, 3), (8, 7, 16), (64, 64, 1),
+        (1, 1, 64), (64, 32, 48)]
+TINY_LAYOUTS = [("row", "row"), ("col", "col"), ("neg_row", "gap"), ("bcast_row", "neg_row"),
+                ("col16", "row16")]
+
+
+@pytest.mark.parametrize("mkn", TINY, ids=[f"{m}x{k}x{n}" for m, k, n in TINY])
+@pytest.mark.parametrize("layouts", TINY_LAYOUTS, ids=["-".join(l) for l in TINY_LAYOUTS])
+def test_tiny_products_direct_and_tiled_agree(torch, mkn, layouts):
+    """A product of at most 16384 outputs with K <= 128 runs one output per
+    thread (8 x 32 blocks); the same shapes over a batch large enough to pass
+    that bound take the tiled kernel.  Both match the oracle on every
+    element, and batch entry 0 of the tiled run equals the one-entry direct
+    run to the bit (one k-ordered fmaf chain per output in both)."""
+    M, K, N = mkn
+    rng = np.random.default_rng(M * 7 + K * 3 + N)
+    batch = 16384 // (M * N) + 1
+    for acc, alpha in ((0, 1.0), (1, -0.75)):
+        big = wl.random_strided(rng, M, N, K, batch, layouts[0], layouts[1], c_layout="row",
+                                values="real", accumulate=acc, alpha=alpha)
+        one = dataclasses.replace(big, batch=1)
+        kw = dict(force_path=sg.PATH_GATHER_FFMA)
+        p_big = sg.sbgemm_plan(0x10000000 + 4 * big.A.offset, big.A.rs, big.A.cs, big.A.bs,
+                               0x20000000 + 4 * big.B.offset, big.B.rs, big.B.cs, big.B.bs,
+                               0x1000000000, big.C.rs, big.C.cs, big.C.bs, M, N, K, batch, acc, **kw)
+        p_one = sg.sbgemm_plan(0x10000000 + 4 * big.A.offset, big.A.rs, big.A.cs, big.A.bs,
+                               0x20000000 + 4 * big.B.offset, big.B.rs, big.B.cs, big.B.bs,
+                               0x1000000000, big.C.rs, big.C.cs, big.C.bs, M, N, K, 1, acc, **kw)
+        assert (p_one["tile_m"], p_one["tile_n"]) == (8, 32), p_one
+        assert (p_big["tile_m"], p_big["tile_n"]) != (8, 32), p_big
+        got_big = gu.run_case(big, torch, **kw)
+        gu.check_full(big, got_big)
+        got_one = gu.run_case(one, torch, **kw)
+        gu.check_full(one, got_one)
+        c0_big = gu.logical_c(big, got_big)[0]
+        c0_one = gu.logical_c(one, got_one)[0]
+        assert np.array_equal(c0_big.view(np.uint32), c0_one.view(np.uint32))
 
 
 @pytest.mark.parametrize("name", wl.WORKLOADS)
