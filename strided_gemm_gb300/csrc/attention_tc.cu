@@ -88,6 +88,13 @@ static_assert(kTiles == 2, "the softmax warps pick their tile's block count from
 static_assert(kD % 32 == 0 && BN == 128, "32-column TMEM transfers; 128-key blocks in two 64-column halves");
 constexpr float kRaise = 8.0f;       // log2 headroom before the reference maximum is raised
 
+// max(a, b, c) in one instruction (the three-input form of max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Instruction descriptors, kind::tf32: D fp32, A and B tf32 K-major, M 128;
 // N = BN for the scores, kD for P V.
 constexpr uint32_t idesc(int n) {
@@ -471,10 +478,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
 #pragma unroll
                 for (int i = 0; i < 8; ++i) am[i] = -INFINITY;
                 if (whole) {
+                    // In pairs on the FMA pipe (each lane rounds as fmaf), the
+                    // running maxima three operands at a time: the softmax is
+                    // bound by instruction issue (moving a share of its exp2
+                    // to the FMA pipe made it slower), not by the MUFU.
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        s[c] = fmaf(s[c], scale, neg);
-                        am[c & 7] = fmaxf(am[c & 7], s[c]);
+                    for (int c = 0; c < 64; c += 2) {
+                        const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), make_float2(scale, scale),
+                                                    make_float2(neg, neg));
+                        s[c] = x.x;
+                        s[c + 1] = x.y;
+                        am[(c / 2) & 7] = fmax3(am[(c / 2) & 7], x.x, x.y);
                     }
                 } else {
 #pragma unroll
@@ -514,9 +528,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 }
                 // The probabilities over the scores (masked keys: exp2(-inf) = 0).
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 64; c += 2) {
                     s[c] = ex2_approx(s[c]);
-                    psum[c & 7] += s[c];
+                    s[c + 1] = ex2_approx(s[c + 1]);
+                    const float2 ps = __fadd2_rn(make_float2(psum[c & 7], psum[(c + 1) & 7]),
+                                                 make_float2(s[c], s[c + 1]));
+                    psum[c & 7] = ps.x;
+                    psum[(c + 1) & 7] = ps.y;
                 }
                 tmem_st64_nowait(s_addr + 64 * hh, s);
             }
