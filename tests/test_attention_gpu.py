@@ -203,6 +203,29 @@ def test_attention_tf32_saturated_scores_and_stale_output(torch):
     check_attention(case, got, tol=TOL_TF32)
 
 
+@pytest.mark.parametrize("ramp", ["every_chunk", "second_chunk"])
+def test_attention_tf32_reference_raises_inside_blocks(torch, ramp):
+    """Scores that climb along the keys, so that a row's reference maximum
+    moves by more than 2^8 inside later blocks: in every 64-key chunk, or only
+    in the second chunk of each 128-key block (then the block's first half of
+    P and O are rescaled after that half's exponentials were written, before
+    P V reads it)."""
+    rng = np.random.default_rng(31 if ramp == "every_chunk" else 32)
+    M, N, D, batch = 256, 512, 64, 2
+    case = wl.random_attention(rng, M, N, D, batch, "row", alpha=1.0, scale=0.1)
+    q = case.Q.storage.reshape(batch, M, D)
+    k = case.K.storage.reshape(batch, N, D)
+    q[:, :, 0] += 1.0
+    n = np.arange(N, dtype=np.float32)
+    climb = 0.15 * n if ramp == "every_chunk" else np.where(n % 128 >= 64, 0.15 * n, 0.0)
+    k[:, :, 0] += climb.astype(np.float32)
+    got = run_attention(case, torch, math=sg.MATH_TF32, force=sg.PATH_TMA_TF32)
+    assert np.isfinite(got).all()
+    check_attention(case, got, tol=TOL_TF32)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
 def test_attention_tf32_other_layouts_fall_back_or_refuse(torch):
     """K read transposed (no unit stride along the head dimension): with
     math = TF32 the fp32 kernel runs (fp32 bound); forcing the tensor-core
