@@ -359,6 +359,51 @@ gather_direct_kernel(const Problem p, const int64_t tiles_n) {
     }
 }
 
+// Tiny products with long K (a 256 x 10 x 512 classifier layer), under
+// k_split = ANY with a workspace: one warp per output, its lanes taking k =
+// lane, lane + 32, ... in one fmaf chain each, then a butterfly of shuffles
+// adds the 32 partial sums (a + b = b + a exactly, so every lane ends with
+// the same sum, the same on every run).  The K split rounds differently from
+// one chain, like the K pieces; consecutive lanes read consecutive k, so an
+// operand with unit stride along K is read in whole lines.  A CTA holds 8
+// outputs, consecutive in (batch, row, column) order.
+constexpr int kDotWarps = kThreads / 32, kDotUnroll = 8;
+
+__global__ void __launch_bounds__(kThreads)
+gather_warpdot_kernel(const Problem p) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t o = blockIdx.x * (uint32_t)kDotWarps + (uint32_t)w;
+    const uint32_t mn = (uint32_t)(p.M * p.N);
+    if ((int64_t)o >= p.M * p.N * p.batch) return;   // whole warps; no barrier below
+    const int64_t b = o / mn, r = o - (uint32_t)b * mn;
+    const int64_t m = r / p.N, n = r - m * p.N;
+    const float* __restrict__ arow = p.A + b * p.bsA + m * p.rsA;
+    const float* __restrict__ bcol = p.B + b * p.bsB + n * p.csB;
+    float acc = 0.0f;
+    for (int64_t k0 = 0; k0 < p.K; k0 += 32 * kDotUnroll) {
+        float av[kDotUnroll], bv[kDotUnroll];
+#pragma unroll
+        for (int i = 0; i < kDotUnroll; ++i) {
+            const int64_t k = k0 + 32 * i + lane;
+            const float* pa = arow + k * p.csA;
+            const float* pb = bcol + k * p.rsB;
+            av[i] = (k < p.K && dbg_in_span(p.A, pa, p.sa, &g_status)) ? __ldg(pa) : 0.0f;
+            bv[i] = (k < p.K && dbg_in_span(p.B, pb, p.sb, &g_status)) ? __ldg(pb) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < kDotUnroll; ++i)
+            if (k0 + 32 * i + lane < p.K) acc = fmaf(av[i], bv[i], acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane != 0) return;
+    float* c = p.C + b * p.bsC + m * p.rsC + n * p.csC;
+    if (!dbg_in_span(p.C, c, p.sc, &g_status)) return;
+    float v = p.accumulate ? fmaf(p.alpha, acc, *c) : p.alpha * acc;
+    if (p.epi.on) v = finish(p.epi, v, b, m, n, &g_status);
+    *c = v;
+}
+
 // Bytes of the partial sums of `tiles` tiles cut into `pieces`, rounded up to
 // 256 so that the counters after them stay aligned.
 size_t split_part_bytes(int64_t tiles, int pieces, int tile_elems) {
@@ -416,8 +461,10 @@ constexpr GatherConfig kConfigs[] = {
     {64, 64, 16, kThreads, 2},     // 4 x 4 micro-tiles, for small problems
     {128, 64, 16, kThreads, 2},    // 8 x 4 micro-tiles, for narrow or ragged N
     {kDirectRows, kDirectCols, kDirectChunk, kThreads, 8},   // one output per thread
+    {1, kDotWarps, 32, kThreads, 8},                          // one output per warp, K over lanes
 };
 constexpr int kDirectVariant = 3;
+constexpr int kWarpDotVariant = 4;
 // The direct kernel serves products of at most this many outputs (over the
 // batch) and this K.
 constexpr int64_t kDirectMaxOutputs = 16384, kDirectMaxK = 128;
@@ -451,6 +498,30 @@ int gather_pick_variant(const Problem& p, int sm_count) {
 
 void gather_schedule(const Problem& p, Plan& plan, int sm_count, size_t ws_bytes, const void* ws,
                      int k_split) {
+    // Tiny products whose K is too long for one thread's chain: with the
+    // caller's consent to split K, one warp per output.
+    if (ws && k_split == SBGEMM_KSPLIT_ANY && p.K > kDirectMaxK && p.M <= kDirectMaxOutputs &&
+        p.N <= kDirectMaxOutputs && p.batch <= kDirectMaxOutputs &&
+        p.M * p.N * p.batch <= kDirectMaxOutputs) {
+        const GatherConfig d = kConfigs[kWarpDotVariant];
+        const int64_t outputs = p.M * p.N * p.batch;
+        plan.variant = kWarpDotVariant;
+        plan.tile_m = d.bm;
+        plan.tile_n = d.bn;
+        plan.tile_k = d.bk;
+        plan.ctas_per_sm = d.ctas_per_sm;
+        plan.tiles = (outputs + kDotWarps - 1) / kDotWarps;
+        plan.tiles_m = plan.tiles;
+        plan.tiles_n = 1;
+        plan.ctas = plan.tiles;
+        plan.k_slices = (int)((p.K + 31) / 32);
+        plan.k_pieces = 32;
+        plan.stream_k = true;      // reported as K pieces; no workspace is used
+        plan.split_indep = true;
+        plan.dp_tiles = 0;
+        plan.workspace = nullptr;
+        return;
+    }
     const GatherConfig g = kConfigs[plan.variant];
     const int64_t nk = (p.K + g.bk - 1) / g.bk;
     plan.k_slices = (int)nk;
@@ -484,6 +555,9 @@ cudaError_t launch_gather_ffma(const Problem& p, const Plan& plan, cudaStream_t 
             if (plan.k_pieces > 1) return launch_variant<64, 64, 16, 4, 4, true>(p, plan, stream);
             return launch_variant<64, 64, 16, 4, 4, false>(p, plan, stream);
         case 2: return launch_variant<128, 64, 16, 8, 4, false>(p, plan, stream);
+        case kWarpDotVariant:
+            gather_warpdot_kernel<<<(unsigned)plan.ctas, kThreads, 0, stream>>>(p);
+            return cudaGetLastError();
         case kDirectVariant: {
             dim3 grid((unsigned)(plan.tiles_m * plan.tiles_n), (unsigned)(p.batch < 65535 ? p.batch : 65535));
             gather_direct_kernel<<<grid, kThreads, 0, stream>>>(p, plan.tiles_n);

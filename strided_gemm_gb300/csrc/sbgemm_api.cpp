@@ -429,7 +429,7 @@ int run(Problem& p, const sbgemm_options& o, void* stream) {
     st = make_plan(p, o, props->sm_count, false, &plan);
     if (st) return st;
 
-    if (plan.stream_k) {
+    if (plan.stream_k && plan.workspace) {
         // The workspace is written by the kernel: it must be device memory and
         // must not meet any operand.
         const Span sw{0, (int64_t)(o.workspace_bytes / 4) - 1};

@@ -154,7 +154,8 @@ def workspace(torch):
     ("chained", 2048, 2560, 1024, "row16", "col16", sg.STREAM_K_CHAINED),
     ("pieces", 2560, 960, 8192, "col16", "row16", sg.STREAM_K_PIECES),
     ("gather_pieces", 256, 512, 784, "gap", "neg_row", sg.STREAM_K_PIECES),
-], ids=["chained", "pieces", "gather_pieces"])
+    ("warp_per_output", 40, 30, 700, "gap", "neg_row", sg.STREAM_K_PIECES),
+], ids=["chained", "pieces", "gather_pieces", "warp_per_output"])
 def test_fused_after_split_k(torch, workspace, shape):
     """Split tiles apply the epilogue once, after the last piece."""
     _, M, N, K, la, lb, mode = shape

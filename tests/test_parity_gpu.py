@@ -363,9 +363,10 @@ def test_split_k_pieces_parity_and_determinism(torch, workspace, shape):
 @pytest.mark.parametrize("name", ["c2a", "c2b", "strided"])
 def test_gather_k_pieces_parity_and_determinism(torch, workspace, name):
     """Small products on the gather path cut K into pieces (one CTA per tile
-    and piece, summed in piece order by the tile's last CTA): within the
-    oracle's bound, exact on integers, identical on every run; k_split = EXACT
-    keeps one chain per output, bit for bit the result without a workspace."""
+    and piece, summed in piece order by the tile's last CTA; c2b, 2560
+    outputs, splits K across a warp's lanes instead): within the oracle's
+    bound, exact on integers, identical on every run; k_split = EXACT keeps
+    one chain per output, bit for bit the result without a workspace."""
     rng = np.random.default_rng(23 + len(name))
     for values in ("real", "int"):
         if name == "strided":
@@ -383,6 +384,37 @@ def test_gather_k_pieces_parity_and_determinism(torch, workspace, name):
     exact, plan_x = _run_ws(case, torch, workspace, dict(k_split=sg.KSPLIT_EXACT))
     assert plan_x["stream_k"] == sg.STREAM_K_NONE
     assert np.array_equal(exact, whole)
+    st, where = sg.sbgemm_device_status()
+    assert st == sg.SBGEMM_OK, where
+
+
+WARPDOT = [(5, 300, 7, 3), (1, 1000, 1, 1), (17, 129, 33, 2), (64, 512, 10, 4), (3, 4097, 5, 1)]
+WARPDOT_LAYOUTS = [("row", "col"), ("col", "row"), ("gap", "neg_row"), ("bcast_row", "gap")]
+
+
+@pytest.mark.parametrize("mknb", WARPDOT, ids=[f"{m}x{k}x{n}x{b}" for m, k, n, b in WARPDOT])
+@pytest.mark.parametrize("layouts", WARPDOT_LAYOUTS, ids=["-".join(l) for l in WARPDOT_LAYOUTS])
+def test_tiny_long_k_one_warp_per_output(torch, workspace, mknb, layouts):
+    """At most 16384 outputs with K > 128, a workspace and k_split = ANY: one
+    warp per output, its lanes splitting K and a shuffle butterfly adding
+    them (reported as K pieces, 1 x 8 outputs per CTA).  Within the oracle's
+    bound, exact on integers, identical from run to run; k_split = EXACT keeps
+    one chain per output, bit for bit the result without a workspace."""
+    M, K, N, batch = mknb
+    rng = np.random.default_rng(M * 13 + K + N * 7 + batch)
+    for values, acc, alpha in (("real", 0, 1.0), ("int", 1, -0.5)):
+        case = wl.random_strided(rng, M, N, K, batch, layouts[0], layouts[1], values=values,
+                                 accumulate=acc, alpha=alpha)
+        first, plan = _run_ws(case, torch, workspace)
+        assert plan["path"] == sg.PATH_GATHER_FFMA and plan["stream_k"] == sg.STREAM_K_PIECES, plan
+        assert (plan["tile_m"], plan["tile_n"]) == (1, 8), plan
+        gu.check_full(case, first, exact=(values == "int"))
+        again, _ = _run_ws(case, torch, workspace)
+        assert np.array_equal(first, again)
+        whole, plan_w = _run_ws(case, torch, None)
+        exact, plan_x = _run_ws(case, torch, workspace, dict(k_split=sg.KSPLIT_EXACT))
+        assert plan_x["stream_k"] == sg.STREAM_K_NONE and (plan_x["tile_m"], plan_x["tile_n"]) != (1, 8)
+        assert np.array_equal(exact, whole)
     st, where = sg.sbgemm_device_status()
     assert st == sg.SBGEMM_OK, where
 
