@@ -5,10 +5,11 @@
  * bind(), so the library instance is the one the binding loaded.
  *
  * Why: a ctypes call converts each of the twenty arguments through its
- * argtypes, about 2.5 us per call on the Grace host against 2 us for the
- * library's whole host side (checks, plan, launch); a latency-bound product
- * such as a 64 x 48 x 32 one pays that on every launch.  Here the conversion
- * is one PyLong_AsLongLong / PyFloat_AsDouble per argument.
+ * argtypes, which measured about 2.5 us per call on an Arm server core,
+ * more than the library's whole host side (checks, plan, launch: 2 us); a
+ * latency-bound product such as a 64 x 48 x 32 one pays that on every
+ * launch.  Here the conversion is one PyLong_AsLongLong / PyFloat_AsDouble
+ * per argument.
  *
  * Pointers are Python ints (0 or None for NULL), strides and sizes ints (or
  * objects with __index__), alpha a float.  Each call returns the library's
