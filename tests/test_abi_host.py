@@ -181,6 +181,25 @@ def test_fastcall_statuses_match_ctypes():
         sg._fast.sbgemm(*A, *B, *C, "8", 8, 8, 1, 1.0, 0, 0)
 
 
+def test_ctypes_path_without_the_fast_call_module(monkeypatch, tmp_path):
+    """Without Python's headers the build skips the fast-call module, and the
+    binding's ctypes calls give the same statuses."""
+    import sysconfig
+    real = sysconfig.get_paths
+    monkeypatch.setattr(sysconfig, "get_paths", lambda *a, **k: dict(real(*a, **k), include=str(tmp_path)))
+    assert sgbuild.build_fastcall(force=True) is None
+    monkeypatch.setattr(sg, "_fast", None)
+    A = rowmajor(BASE, 8, 8, 1)
+    B = rowmajor(BASE + (1 << 32), 8, 8, 1)
+    C = rowmajor(BASE + (2 << 32), 8, 8, 1)
+    for M, batch, want in ((-1, 1, sg.SBGEMM_ERR_INVALID_VALUE), (8, -2, sg.SBGEMM_ERR_INVALID_VALUE)):
+        for call in (sg.sbgemm, sg.sbgemm_ex):
+            with pytest.raises(sg.SbgemmError) as e:
+                call(*A, *B, *C, M, 8, 8, batch, 1.0, 0)
+            assert e.value.status == want
+    sg.sbgemm_ex(*A, *B, *C, 0, 8, 8, 1, 1.0, 0)   # empty: nothing to do
+
+
 def test_injective_layouts_accepted():
     A = rowmajor(BASE, 8, 8, 1)
     B = rowmajor(BASE + (1 << 32), 8, 8, 1)
