@@ -93,6 +93,12 @@ struct Issuer {
     int pad;
     uint64_t issued;    // slices issued so far (global iteration count)
     int64_t total;      // slices this CTA loads in all
+    // Item w's slice range and copy coordinates, worked out once per item
+    // (the tile's coordinates take 64-bit divisions, which thread 0 would
+    // otherwise pay on every slice while its warp is part of the mainloop).
+    int64_t cw;         // the item they belong to (-1: none yet)
+    int kb, ke;
+    int m0, n0, ba, bb;
 };
 
 // Shared-memory plan of one tile shape.  TA / TB: the A / B operand is
@@ -276,25 +282,33 @@ __device__ __forceinline__ void issue_next(typename Cfg<BM, BN, A_K, B_K>::Smem&
                                            const CUtensorMap* tb, const Params& p,
                                            const Schedule& sc, Issuer& is) {
     using C = Cfg<BM, BN, A_K, B_K>;
-    Item itm = sc.item(is.w, p.nk);
-    if (is.kt < itm.kb) is.kt = itm.kb;
-    const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
+    if (is.cw != is.w) {
+        const Item itm = sc.item(is.w, p.nk);
+        const TileCoord tc = tile_coord<BM, BN>(p, itm.tile);
+        is.cw = is.w;
+        is.kb = itm.kb;
+        is.ke = itm.ke;
+        is.m0 = (int)tc.m0;
+        is.n0 = (int)tc.n0;
+        is.ba = p.a_bcast ? 0 : (int)tc.b;
+        is.bb = p.b_bcast ? 0 : (int)tc.b;
+        if (is.kt < is.kb) is.kt = is.kb;
+    }
     const int s = (int)(is.issued % C::kStages);
-    const int ba = p.a_bcast ? 0 : (int)tc.b;
-    const int bb = p.b_bcast ? 0 : (int)tc.b;
+    const int ba = is.ba, bb = is.bb;
     const int k0 = is.kt * BK;
     mbar_arrive_expect_tx(&sh.full[s], C::kStageBytes);
     if (A_K) {
 #pragma unroll
         for (int j = 0; j < C::kABoxes; ++j)
-            tma_load_3d(sh.a[s] + j * 256 * BK, ta, &sh.full[s], k0, (int)tc.m0 + 256 * j, ba);
+            tma_load_3d(sh.a[s] + j * 256 * BK, ta, &sh.full[s], k0, is.m0 + 256 * j, ba);
     } else {
-        tma_load_3d(sh.a[s], ta, &sh.full[s], (int)tc.m0, k0, ba);
+        tma_load_3d(sh.a[s], ta, &sh.full[s], is.m0, k0, ba);
     }
-    if (B_K) tma_load_3d(sh.b[s], tb, &sh.full[s], k0, (int)tc.n0, bb);
-    else     tma_load_3d(sh.b[s], tb, &sh.full[s], (int)tc.n0, k0, bb);
+    if (B_K) tma_load_3d(sh.b[s], tb, &sh.full[s], k0, is.n0, bb);
+    else     tma_load_3d(sh.b[s], tb, &sh.full[s], is.n0, k0, bb);
     ++is.issued;
-    if (++is.kt == itm.ke) { is.kt = 0; ++is.w; }
+    if (++is.kt == is.ke) { is.kt = 0; ++is.w; }
 }
 
 // On a failed wait the issuer may still have copies landing in shared memory;
@@ -418,6 +432,7 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
         sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
         is.w = 0;
         is.kt = 0;
+        is.cw = -1;
         is.issued = 0;
         is.total = sh.sched.slices(p.nk);
         for (int s = 0; s < S; ++s) {
