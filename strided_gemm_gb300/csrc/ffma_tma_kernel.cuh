@@ -72,6 +72,14 @@ struct Params {
     int64_t dp_tiles;
     int64_t sk_units;       // (tiles_total - dp_tiles) * nk
     int indep;              // split tiles as independent pieces (schedule.cuh)
+    // Chained split of a product whose last tile column is at most half
+    // full: those tiles run in about 2/3 of a full tile's time (their idle
+    // warps are one per scheduler), so they are ordered after every full tile
+    // (tile_coord) and the split counts their units at w_rag against w_full
+    // (Schedule::init_weighted).  w_full == 0: plain order and split.
+    int64_t full_tiles;     // tiles outside the last column
+    int64_t sk_full_units;  // split units of full tiles: (full_tiles - dp_tiles) * nk
+    int w_full, w_rag;
     EpiParams epi;          // fused epilogue (epilogue.cuh); epi.on == 0: none
     int epi_inline;         // ... a bias per column (or none), no activation or ReLU:
                             // applied in the register epilogue
@@ -224,16 +232,26 @@ struct TileCoord { int64_t b, m0, n0; };
 // Tile t -> (batch entry, first row, first column); grouped raster of 8
 // tile-rows within a batch entry so concurrently resident CTAs share slices.
 template <int BM, int BN>
-__device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t) {
-    const int64_t per_batch = p.tiles_m * p.tiles_n;
+__device__ __forceinline__ TileCoord raster_coord(int64_t t, int64_t tiles_m, int64_t tiles_n) {
+    const int64_t per_batch = tiles_m * tiles_n;
     const int64_t b = t / per_batch;
     const int64_t r = t - b * per_batch;
     constexpr int64_t G = 8;
-    const int64_t group = r / (G * p.tiles_n);
+    const int64_t group = r / (G * tiles_n);
     const int64_t first_m = group * G;
-    const int64_t gm = (p.tiles_m - first_m < G) ? (p.tiles_m - first_m) : G;
-    const int64_t w = r - group * G * p.tiles_n;
+    const int64_t gm = (tiles_m - first_m < G) ? (tiles_m - first_m) : G;
+    const int64_t w = r - group * G * tiles_n;
     return {b, (first_m + w % gm) * BM, (w / gm) * BN};
+}
+
+// With a weighted split the tiles of the last column come after all others.
+template <int BM, int BN>
+__device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t) {
+    if (p.w_full == 0) return raster_coord<BM, BN>(t, p.tiles_m, p.tiles_n);
+    if (t < p.full_tiles) return raster_coord<BM, BN>(t, p.tiles_m, p.tiles_n - 1);
+    const int64_t r = t - p.full_tiles;
+    const int64_t b = r / p.tiles_m;
+    return {b, (r - b * p.tiles_m) * BM, (p.tiles_n - 1) * BN};
 }
 
 // Thread -> tile row of its i-th A row (16) / tile column of its j-th B column
@@ -429,7 +447,10 @@ tma_ffma_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
     const Schedule& sc = sh.sched;
     Issuer& is = sh.iss;
     if (issuer) {
-        sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
+        if (p.w_full)
+            sh.sched.init_weighted(p.dp_tiles, p.sk_units, p.nk, p.sk_full_units, p.w_full, p.w_rag);
+        else
+            sh.sched.init(p.dp_tiles, p.sk_units, p.nk);
         is.w = 0;
         is.kt = 0;
         is.cw = -1;
@@ -828,6 +849,26 @@ cudaError_t launch_impl(const Problem& pr, const Plan& plan, int sm_count, cudaS
     p.dp_tiles = plan.stream_k ? plan.dp_tiles : plan.tiles;
     p.sk_units = plan.stream_k ? (plan.tiles - plan.dp_tiles) * p.nk : 0;
     p.indep = plan.stream_k && plan.split_indep ? 1 : 0;
+    p.full_tiles = p.sk_full_units = 0;
+    p.w_full = p.w_rag = 0;
+    const int64_t rag = pr.N % BN;
+    if (plan.stream_k && !plan.split_indep && rag != 0 && 2 * rag <= BN && p.tiles_n > 1) {
+        // The tiles of the last column hold at most BN / 2 columns: the warps
+        // past it skip their FMAs, one per scheduler, and such a tile measured
+        // 0.67 of a full one's time (N = 960 in 128-wide tiles).
+        constexpr int kWf = 3, kWr = 2;
+        const int64_t full = p.tiles_m * (p.tiles_n - 1) * pr.batch;
+        if (p.dp_tiles <= full) {
+            const int64_t skf = (full - p.dp_tiles) * p.nk;
+            const int64_t total = skf * kWf + (p.sk_units - skf) * kWr;
+            if (total >= grid * (int64_t)p.nk * kWf) {   // every range still spans a whole tile
+                p.full_tiles = full;
+                p.sk_full_units = skf;
+                p.w_full = kWf;
+                p.w_rag = kWr;
+            }
+        }
+    }
     p.epi = pr.epi;
     p.epi_inline = pr.epi.on && (pr.epi.D == nullptr || pr.epi.rsD == 0) &&
                    (pr.epi.act == kActNone || pr.epi.act == kActRelu) ? 1 : 0;

@@ -46,6 +46,33 @@ struct Schedule {
     }
 
     __device__ __forceinline__ void init(int64_t dp_tiles, int64_t sk_units, int nk, int64_t c, int64_t G) {
+        set(dp_tiles, sk_units, nk, c, G, c * sk_units / G, (c + 1) * sk_units / G);
+    }
+
+    // The split by cost instead of by unit: the first sk_full units cost wf
+    // each and the rest wr (tiles whose later units are cheaper, ordered
+    // last), so every CTA gets the same cost.  Each range must still span at
+    // least one tile's units (the caller checks total cost >= G nk wf).
+    __device__ __forceinline__ void init_weighted(int64_t dp_tiles, int64_t sk_units, int nk, int64_t sk_full,
+                                                  int wf, int wr) {
+        const int64_t c = blockIdx.x, G = gridDim.x;
+        const int64_t total = unit_cost(sk_units, sk_full, wf, wr);
+        set(dp_tiles, sk_units, nk, c, G, unit_at_cost(c * total / G, sk_full, wf, wr),
+            unit_at_cost((c + 1) * total / G, sk_full, wf, wr));
+    }
+
+    // Cost of the units before unit x, and the first unit whose cost starts at
+    // or after `cost`.
+    __device__ __forceinline__ static int64_t unit_cost(int64_t x, int64_t sk_full, int wf, int wr) {
+        return x <= sk_full ? x * wf : sk_full * wf + (x - sk_full) * wr;
+    }
+    __device__ __forceinline__ static int64_t unit_at_cost(int64_t cost, int64_t sk_full, int wf, int wr) {
+        const int64_t cf = sk_full * wf;
+        return cost <= cf ? (cost + wf - 1) / wf : sk_full + (cost - cf + wr - 1) / wr;
+    }
+
+    __device__ __forceinline__ void set(int64_t dp_tiles, int64_t sk_units, int nk, int64_t c, int64_t G,
+                                        int64_t u0, int64_t u1) {
         cta = c;
         nctas = G;
         n_dp = dp_tiles > c ? (dp_tiles - 1 - c) / G + 1 : 0;
@@ -54,7 +81,6 @@ struct Schedule {
         full_first = head_tile = tail_tile = 0;
         head_begin = head_end = tail_begin = 0;
         if (sk_units > 0) {
-            const int64_t u0 = c * sk_units / G, u1 = (c + 1) * sk_units / G;
             const int64_t t0 = u0 / nk, t1 = (u1 - 1) / nk;
             const int s0 = (int)(u0 % nk), e1 = (int)((u1 - 1) % nk);
             has_tail = s0 > 0;

@@ -3,7 +3,8 @@
 a plain CPU implementation of the same formula).  One case per kernel and
 schedule, through the call a caller with a workspace makes:
 
-- TMA-fed FFMA, chained stream-K over the last waves (c5a, real and integer);
+- TMA-fed FFMA, chained stream-K over the last waves (c5a, real and integer;
+  c5b, whose half-full last tile column is split by weighted cost);
 - TMA-fed FFMA, independent K pieces of a few-tile long-K product (f1dwa);
 - TMA-fed FFMA, data-parallel over a batch of 128 (c3) and the 512 x 64
   tiles of a narrow accumulating product (c4);
@@ -44,6 +45,7 @@ CASES = [
     # (workload, values, math, path, stream_k schedule)
     ("c5a", "real", sg.MATH_FP32, "tma_ffma", sg.STREAM_K_CHAINED),
     ("c5a", "int", sg.MATH_FP32, "tma_ffma", sg.STREAM_K_CHAINED),
+    ("c5b", "real", sg.MATH_FP32, "tma_ffma", sg.STREAM_K_CHAINED),
     ("f1dwa", "real", sg.MATH_FP32, "tma_ffma", sg.STREAM_K_PIECES),
     ("c3", "real", sg.MATH_FP32, "tma_ffma", sg.STREAM_K_NONE),
     ("c4", "real", sg.MATH_FP32, "tma_ffma", sg.STREAM_K_NONE),

@@ -272,6 +272,10 @@ STREAM_K_SHAPES = [
     ("ragged_k", 2048, 2600, 1000, 1, "row16", "row16", 1),
     ("batched", 1024, 1024, 768, 5, "col16", "row16", 1),
     ("mn_major_both", 4100, 1200, 640, 1, "col16", "row16", 0),
+    # the last 128-wide tile column half full: its units weighted lighter, its
+    # tiles ordered last
+    ("ragged_last_column", 8192, 960, 2560, 1, "row16", "col16", 0),
+    ("ragged_last_column_batched", 2048, 936, 1536, 3, "row16", "col16", 1),
 ]
 
 
