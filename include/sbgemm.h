@@ -129,7 +129,10 @@ enum {
                                  pieces summed in a fixed order; the latter
                                  rounds differently from the unsplit product.
                                  Small products on the gather path are cut
-                                 into K pieces the same way. */
+                                 into K pieces the same way, and products of
+                                 at most 16384 outputs with K > 128 split K
+                                 across the 32 lanes of a warp (one output per
+                                 warp, a fixed shuffle tree). */
     SBGEMM_KSPLIT_EXACT = 1,  /* only splits whose result is bit-identical to
                                  the unsplit schedule (chained stream-K) */
     SBGEMM_KSPLIT_NONE = 2    /* never split K */
